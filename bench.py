@@ -1,0 +1,358 @@
+"""Benchmark of the PIC link step on GB300.
+
+One step = the whole link hot path for one request batch: row selection, splice,
+RoPE tables, re-rotation of cached K, fresh K/V, link attention (+ LSE merge).
+Default workload: 100 chunks x 1000 tokens linked in a random order + a 256-token
+query, k = 8, Hq = 32, Hkv = 8, d = 128, bf16, 16-token pages (100,256 tokens).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0).  value = context tokens (T + q, summed over requests
+and ranks) per second of device time, the pool and inputs resident in HBM; L2 is
+flushed (512 MB memset, untimed) before every timed step.  e2e = the same metric
+through the Python binding with per-step host->device copies of the step's inputs
+from pinned memory and a device->host copy of the attention output.
+`--impl reference` times the float64 CPU oracle on a bounded sample of the same
+workload on the host cores.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "PIC link: context tokens/s per layer; % of HBM / bf16 tensor-core roofline"
+UNIT = "tokens/s"
+
+# ncu DRAM bytes (read + write) per launch of the attention call and of the
+# re-rotation kernel, with the kernel source they were taken from; reported as
+# roofline traffic only while the source is unchanged.
+NCU_TRAFFIC = {}
+
+
+def _src_hash(name):
+    p = os.path.join(ROOT, "position_independent_kv_pic_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), float(j.get("bf16_tflops_sustained", 0)), "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def _workload(name):
+    from position_independent_kv_pic_gb300 import inputs
+    if name not in inputs.PRESETS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(inputs.PRESETS)}")
+    return inputs.PRESETS[name]()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args, rank, world):
+    import torch
+    import torch.distributed as dist
+
+    import position_independent_kv_pic_gb300 as pic
+    from position_independent_kv_pic_gb300 import build as pic_build
+    from position_independent_kv_pic_gb300.link import LinkBatch
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if rank == 0 or world == 1:
+        pic_build.build()
+    if world > 1:
+        dist.barrier()
+    pic.load()
+
+    wl = _workload(args.workload)
+    batch = LinkBatch(wl)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+
+    for _ in range(args.warmup):
+        batch.run()
+    torch.cuda.synchronize()
+    if batch.error() != 0:
+        raise SystemExit(f"device error: {pic.pic_strerror(batch.error())}")
+
+    # algorithmic work, from the step's own outputs
+    rows = batch.rows.cpu().numpy().astype(np.int64)
+    rot = batch.rot.cpu().numpy()
+    lohi = rot[:, 3].view(np.int16).reshape(-1, 2) if len(rot) else np.zeros((0, 2), np.int16)
+    rot_tokens = int((lohi[:, 1].astype(np.int64) - lohi[:, 0]).sum())
+    el = 2 if wl.dtype == "bf16" else 4
+    rot_bytes = 2 * rot_tokens * wl.Hkv * wl.d * el
+    attn_flops = 4.0 * wl.d * wl.Hq * float((rows + 1).sum())
+
+    K = args.steps
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    step_ev = [(ev(), ev()) for _ in range(K)]
+    rot_ev = [(ev(), ev()) for _ in range(K)]
+    att_ev = [(ev(), ev()) for _ in range(K)]
+
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            step_ev[i][0].record(stream)
+            batch.run(marks={"rerotate": rot_ev[i], "attention": att_ev[i]})
+            step_ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    if world > 1:
+        dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    rot_ms = [a.elapsed_time(b) for a, b in rot_ev]
+    att_ms = [a.elapsed_time(b) for a, b in att_ev]
+    if batch.error() != 0:
+        raise SystemExit(f"device error: {pic.pic_strerror(batch.error())}")
+
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    tokens = batch.tokens
+    value = world * K * tokens / (total_ms / 1e3)
+
+    # end to end through the binding: H2D inputs, step, D2H output
+    batch.pin_host_inputs()
+    Ke = max(3, min(K, 50))
+    for _ in range(2):
+        batch.upload()
+        batch.run()
+        batch.download()
+    torch.cuda.synchronize()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(Ke):
+        batch.upload()
+        batch.run()
+        batch.download()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+
+    hbm, tf_burst, tf_sus, peak_kind = _peaks()
+    att_avg = statistics.mean(att_ms)
+    rot_avg = statistics.mean(rot_ms)
+    att_tflops = attn_flops / (att_avg / 1e3) / 1e12
+    rot_gbs = rot_bytes / (rot_avg / 1e3) / 1e9
+    traffic = NCU_TRAFFIC.get(("attention", _src_hash("attention.cu")))
+    rtraffic = NCU_TRAFFIC.get(("rerotate", _src_hash("rotate.cu")))
+
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.dtype,
+        "data": "synthetic: seeded N(0,1) K/V/Q, cached K drawn as stored (position-encoded) keys",
+        "config": {"workload": wl.name, "requests": batch.n_req, "chunks": batch.n_chunks,
+                   "tokens": tokens, "rows": batch.n_rows, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
+                   "page": 16, "pages": batch.n_pages, "rot_pages": batch.n_rot,
+                   "l2": "flushed (512 MB memset, untimed) before every timed step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": tf_burst, "unit": "TFLOP/s",
+                     "frac": att_tflops / tf_burst, "traffic": traffic,
+                     "kernel": "pic_link_attention (unit plan + tcgen05 attention + LSE merge)",
+                     "algorithmic": f"4*d*Hq*sum(p_r+1) = {attn_flops:.4e} flop per launch",
+                     "peak_source": f"{peak_kind} bf16 dense burst"},
+        "rooflines": {
+            "attention": {"bound": "tensor", "achieved": att_tflops, "peak": tf_burst, "unit": "TFLOP/s",
+                          "frac": att_tflops / tf_burst, "ms": att_avg, "traffic": traffic,
+                          "frac_of_sustained": att_tflops / tf_sus if tf_sus else None},
+            "rerotate": {"bound": "hbm", "achieved": rot_gbs, "peak": hbm, "unit": "GB/s", "frac": rot_gbs / hbm,
+                         "ms": rot_avg, "traffic": rtraffic, "algorithmic_bytes": rot_bytes,
+                         "frac_of_8tbs": rot_gbs / 8000.0},
+        },
+        "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": batch.h2d_bytes(), "d2h_bytes_per_step": batch.d2h_bytes()},
+        "clocks": clocks.summary(),
+        "gpu_launches": K * batch.LAUNCHES_PER_STEP,
+        "wall_s_timed_region": t_wall,
+    }
+    return result, batch
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample_time(wl, batch_rows=None, n_chunks=8, n_rows=4, seed=0):
+    """Time the float64 oracle on a bounded sample of one step of ``wl`` and extrapolate
+    to the whole step.  Returns (seconds for a full step, description, threads)."""
+    import oracle.pic_oracle as O
+    from position_independent_kv_pic_gb300 import inputs
+
+    rng = np.random.default_rng(seed)
+    kst, vst, off = inputs.chunk_store(wl)
+    total_rot_tokens, total_pp1, t_rot, t_att = 0, 0, 0.0, 0.0
+    s_rot_tokens, s_pp1 = 0, 0
+    for req in wl.requests[:1] if len(wl.requests) == 1 else wl.requests[:2]:
+        lens = wl.chunk_lens[req.chunk_ids]
+        rows, starts, T = O.select_rows(lens, req.q, req.k)
+        ck = [kst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
+        cv = [vst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
+        n = len(rows)
+        qr, kn, vn = (t.double().numpy() for t in inputs.row_inputs(wl, n))
+        # context built once, untimed; the timed sample re-runs pieces of it
+        K_ctx, V_ctx, rows, starts, T = O.splice_context(ck, cv, req.q, req.k, kn, vn, wl.theta, wl.dtype)
+        q_rot = O.round_to(O.rope(qr, rows, wl.theta), wl.dtype)
+        cs = rng.choice(np.arange(1, len(ck)), size=min(n_chunks, len(ck) - 1), replace=False) if len(ck) > 1 else []
+        t0 = time.perf_counter()
+        for c in cs:
+            O.rerotate_k(ck[c], int(starts[c]), wl.theta, wl.dtype)
+        t_rot += time.perf_counter() - t0
+        s_rot_tokens += sum(len(ck[c]) for c in cs)
+        total_rot_tokens += sum(len(c) for c in ck[1:])
+        which = sorted(rng.choice(n, size=min(n_rows, n), replace=False).tolist()) if n else []
+        t0 = time.perf_counter()
+        O.attention_rows(q_rot, rows, K_ctx, V_ctx, 1.0 / np.sqrt(wl.d), which=which)
+        t_att += time.perf_counter() - t0
+        s_pp1 += int((rows[which] + 1).sum())
+        total_pp1 += int((rows + 1).sum())
+    scale_reqs = len(wl.requests) / min(len(wl.requests), 2)
+    full = scale_reqs * (t_rot * total_rot_tokens / max(s_rot_tokens, 1) + t_att * total_pp1 / max(s_pp1, 1))
+    desc = (f"oracle as it stands on {n_chunks} of the re-rotated chunks and {n_rows} of the recomputed rows "
+            f"per request (first {min(len(wl.requests), 2)} request(s)); time extrapolated by re-rotated tokens "
+            f"and by sum(p+1) over rows to the full step")
+    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return full, desc, threads
+
+
+def run_reference(args):
+    wl = _workload(args.workload)
+    tokens = wl.total_tokens()
+    for _ in range(args.warmup):
+        oracle_sample_time(wl, n_chunks=2, n_rows=1)
+    times = []
+    for i in range(args.steps):
+        full, desc, threads = oracle_sample_time(wl, seed=i)
+        times.append(full)
+    step_s = statistics.mean(times)
+    value = tokens / step_s
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
+        "config": {"workload": wl.name, "tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="long_context_100x1000")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    result, batch = run_gpu(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            full, desc, threads = oracle_sample_time(batch.wl)
+            result["cpu_baseline"] = {"value": batch.tokens / full, "unit": UNIT, "cores": threads,
+                                      "kind": "oracle", "sample": desc}
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,285 @@
+/*
+ * pic.h -- C ABI of the position-independent-caching (PIC) "link" step for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The link step takes KV caches that were computed per chunk at local positions
+ * 0..L_c-1 and
+ *   1. selects the rows to recompute: the first min(k, L_c) tokens of every chunk
+ *      except the first, plus every query token (EPIC's LegoLink-k);
+ *   2. splices the chunks into one context at global positions (a page list);
+ *   3. re-rotates every cached K of chunk c by its offset Delta_c = s_c, one
+ *      rotation R(theta * Delta_c) ("rotary correction");
+ *   4. writes the recomputed rows' fresh K (RoPE at the global position) and V;
+ *   5. runs causal attention (key_pos <= query_pos, scale 1/sqrt(d)) for the
+ *      recomputed rows only, against the whole spliced K/V, Q roped at global
+ *      positions.
+ *
+ * Sources: blog review "EPIC: Efficient Position-Independent Caching for Serving
+ * Large Language Models" (compile/link walk-through; link_legolink Steps 1-3);
+ * article on RoPE and prefix caching, sections 2.2 (RoPE) and 3.3 (rotary
+ * correction); HYPIC article, section 2.2 (seam window = recomputed chunk heads);
+ * blog "KV cache from scratch", mask section (offset causal mask).
+ *
+ * Conventions shared by every entry point
+ *   - Pointers are DEVICE pointers unless their name ends in _host.  The caller
+ *     owns all memory and streams; the library allocates nothing and keeps no
+ *     state between calls.
+ *   - Every device entry point is asynchronous on `stream`.  Its return value
+ *     reports only what the host can check synchronously: PIC_ERR_INVALID for a
+ *     bad argument, PIC_ERR_UNSUPPORTED for a valid but unimplemented shape,
+ *     PIC_ERR_WORKSPACE for a short workspace, PIC_ERR_CUDA when a launch fails.
+ *   - Problems only the device can see (an out-of-range block id, metadata that
+ *     disagrees with the host-computed sizes, a bounded wait that ran out) are
+ *     written to *err_flag (int32, device), first error wins.  The caller zeroes
+ *     it before the calls and reads it after synchronising.  Kernels never trap.
+ *   - KV pools: K and V each [num_blocks][Hkv][PIC_PAGE][d] in the pool dtype
+ *     (bf16 or fp32), row-major, 16-byte aligned.  A block is one 16-token page
+ *     of one layer for all KV heads.
+ *   - Request metadata is CSR: request r links chunks chunk_off[r] ..
+ *     chunk_off[r+1]-1 (indices into the flat chunk arrays), in link order.
+ *   - GQA: query head h reads KV head h / (Hq / Hkv).
+ *   - Positions are int32 (sequence length < 2^31).
+ *   - RoPE pairs dimension i with i + d/2, angle p * theta^(-2i/d).
+ */
+#ifndef PIC_H_
+#define PIC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (binary compatible); NULL means the legacy default stream. */
+typedef struct CUstream_st* pic_stream_t;
+
+typedef enum {
+  PIC_OK = 0,
+  PIC_ERR_INVALID = 1,     /* bad argument (host check) or bad metadata (device flag) */
+  PIC_ERR_CUDA = 2,        /* a CUDA runtime / driver call failed */
+  PIC_ERR_UNSUPPORTED = 3, /* dtype / head-dim / GQA-group combination not implemented */
+  PIC_ERR_TIMEOUT = 4,     /* device: a bounded pipeline wait ran out (err_flag only) */
+  PIC_ERR_RANGE = 5,       /* device: block id, slot or count outside its buffer (err_flag only) */
+  PIC_ERR_WORKSPACE = 6    /* workspace smaller than pic_link_attention_workspace() */
+} pic_status;
+
+typedef enum { PIC_BF16 = 0, PIC_FP32 = 1 } pic_dtype;
+
+#define PIC_PAGE 16 /* tokens per KV page (block) */
+
+/* One entry of a request's spliced context: 16 key slots at global positions
+ * gpos0 .. gpos0+15, of which slots [lo, hi) are valid.  K comes from block
+ * k_block of the K pool and V from block v_block of the V pool (they differ
+ * when K was rotated out of place while V stays shared).  A request's entries
+ * are sorted by gpos0 + lo (strictly increasing).  16 bytes. */
+typedef struct {
+  int32_t k_block;
+  int32_t v_block;
+  int32_t gpos0;
+  int16_t lo, hi;
+} pic_link_page;
+
+/* One unit of re-rotation work: rotate slots [lo, hi) of every KV head of K
+ * block src_block by the offset in row `tab` of the offset table and store
+ * them into dst_block (dst_block == src_block: in place).  16 bytes. */
+typedef struct {
+  int32_t src_block;
+  int32_t dst_block;
+  int32_t tab;
+  int16_t lo, hi;
+} pic_rot_page;
+
+/* Sizes of one request, all closed-form in the chunk lengths, q and k. */
+typedef struct {
+  int64_t tokens;      /* T + q: spliced context length                         */
+  int64_t rows;        /* n_sel = sum_{c>=1} min(k, L_c) + q: recomputed rows   */
+  int64_t link_pages;  /* entries of the request's pic_link_page list           */
+  int64_t rot_pages;   /* entries of the request's pic_rot_page list            */
+  int64_t fresh_pages; /* fresh blocks the recomputed rows are written into     */
+  int64_t chunk_pages; /* pages of the request's cached chunks: sum ceil(L_c/16) */
+} pic_request_sizes;
+
+/* ------------------------------------------------------------------------
+ * Host helpers (no device work).
+ * ------------------------------------------------------------------------ */
+
+/* Number of recomputed rows of one request: sum over chunks c >= 1 of
+ * min(k, L_c), plus q (EPIC link_legolink Step 1; the worked example gives 7 of
+ * 17 for lengths {4,5,5}, q = 3, k = 2).  chunk_lens_host: n_chunks lengths in
+ * link order, each >= 1.  Returns -1 on invalid input (n_chunks < 0, q < 0,
+ * k < 0, a length < 1, or a NULL pointer with n_chunks > 0). */
+int64_t pic_count_rows(const int32_t* chunk_lens_host, int32_t n_chunks, int32_t q, int32_t k);
+
+/* All sizes of one request (see pic_request_sizes).  The layout they describe:
+ *   link pages, in order, for each chunk c: ceil(m_c/16) fresh pages holding the
+ *   recomputed head rows (m_c = min(k, L_c) for c >= 1, 0 for c = 0), then the
+ *   chunk's cached pages j that keep at least one slot (valid slots
+ *   [max(0, m_c - 16j), min(16, L_c - 16j))); finally ceil(q/16) fresh query pages.
+ *   rot pages: the kept cached pages of chunks c >= 1 (chunk 0 has Delta = 0).
+ *   fresh pages: the fresh link pages above, in the same order.
+ * Returns PIC_ERR_INVALID on the same conditions as pic_count_rows. */
+pic_status pic_request_sizes_of(const int32_t* chunk_lens_host, int32_t n_chunks, int32_t q,
+                                int32_t k, pic_request_sizes* out);
+
+/* Exclusive prefix offsets over n_req requests, from host copies of the
+ * metadata: row_off, page_off, rot_off, fresh_off and chunk_page_off receive
+ * n_req+1 (chunk_page_off: n_chunks_total+1) entries; any output may be NULL.
+ * chunk_page_off[c] is the first page of chunk c in a per-chunk page table that
+ * gives every chunk ceil(L_c/16) pages.  Returns PIC_ERR_INVALID on bad input. */
+pic_status pic_plan_offsets(const int32_t* chunk_lens_host, const int32_t* chunk_off_host,
+                            const int32_t* q_len_host, const int32_t* k_host, int32_t n_req,
+                            int32_t* row_off_host, int32_t* page_off_host,
+                            int32_t* rot_off_host, int32_t* fresh_off_host,
+                            int32_t* chunk_page_off_host);
+
+/* Message for a status code (static string, never NULL). */
+const char* pic_strerror(pic_status status);
+
+/* ------------------------------------------------------------------------
+ * a1  Row selection (EPIC link_legolink Step 1; worked example).
+ * ------------------------------------------------------------------------
+ * For every request r (one thread block each): walks its chunks in link order,
+ * writes each chunk's start s_c (exclusive prefix sum of the lengths) to
+ * chunk_start[c], and writes the recomputed rows' global positions, ascending,
+ * to rows[row_off[r] ...]: the first min(k[r], L_c) positions of every chunk
+ * c >= 1, then T .. T + q[r] - 1.
+ *   chunk_lens  [n_chunks_total] int32, >= 1       (device)
+ *   chunk_off   [n_req+1] int32 CSR                 (device)
+ *   q_len, k    [n_req] int32, >= 0                 (device)
+ *   row_off     [n_req+1] int32 from pic_plan_offsets (device)
+ *   rows        [row_off[n_req]] int32  out         (device)
+ *   chunk_start [n_chunks_total] int32  out         (device)
+ * Device errors: PIC_ERR_INVALID (length < 1, q or k < 0), PIC_ERR_RANGE (the
+ * request's row count disagrees with row_off). */
+pic_status pic_select_rows(const int32_t* chunk_lens, const int32_t* chunk_off,
+                           const int32_t* q_len, const int32_t* k, const int32_t* row_off,
+                           int32_t n_req, int32_t* rows, int32_t* chunk_start,
+                           int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Splice: build each request's link page list, its re-rotation work list and
+ * the pool slot of every recomputed row (EPIC Step 3: cached K/V are copied to
+ * their global positions and the recomputed rows overwrite theirs; HYPIC 2.2:
+ * seam rows are not taken from the cache).  Layout as in pic_request_sizes_of.
+ *   chunk_lens, chunk_off, q_len, k, n_req: as for pic_select_rows
+ *   chunk_start     [n_chunks_total] from pic_select_rows
+ *   chunk_page_off  [n_chunks_total+1] CSR into the three per-chunk page tables
+ *   k_src_blocks    [chunk_page_off[n]] K-pool block of each chunk page as cached
+ *   k_dst_blocks    same shape: where the rotated K goes; NULL = in place
+ *   v_blocks        same shape: V-pool block of each chunk page (never written)
+ *   fresh_off       [n_req+1] CSR into fresh_blocks
+ *   fresh_blocks    block ids (same id in the K and V pools) for recomputed rows
+ *   page_off, rot_off [n_req+1] from pic_plan_offsets
+ *   pages   out [page_off[n_req]]   link page lists (gpos0 global)
+ *   rot     out [rot_off[n_req]]    re-rotation work (tab = flat chunk index)
+ *   row_block, row_slot out [n_rows]: pool block and slot of each recomputed row
+ *                 (row order as written by pic_select_rows; row_off gives n_rows)
+ *   row_off [n_req+1]
+ * Device errors: PIC_ERR_RANGE when a count disagrees with the offsets. */
+pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
+                            const int32_t* q_len, const int32_t* k, int32_t n_req,
+                            const int32_t* chunk_start, const int32_t* chunk_page_off,
+                            const int32_t* k_src_blocks, const int32_t* k_dst_blocks,
+                            const int32_t* v_blocks, const int32_t* fresh_off,
+                            const int32_t* fresh_blocks, const int32_t* row_off,
+                            const int32_t* page_off, const int32_t* rot_off,
+                            pic_link_page* pages, pic_rot_page* rot, int32_t* row_block,
+                            int32_t* row_slot, int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a2  RoPE tables (RoPE article 2.2 and footnote 3).
+ * ------------------------------------------------------------------------
+ * table[i][j] = { cos_hi, sin_hi, cos_lo, sin_lo } of the angle pos[i] * theta^(-2j/d),
+ * j < d/2: cos and sin are computed in fp64 on the device and stored as two fp32
+ * parts each (hi = fp32(v), lo = fp32(v - hi)), so the rotation kernels can
+ * apply them with ~2^-46 error and store K within one bf16 ulp of the exact
+ * rotation.  Used with pos = chunk_start (offset table for the rotary correction
+ * by Delta_c) and with pos = rows (per-row table for fresh K and for Q).
+ *   pos [n] int32 (device); table out [n][d/2][4] fp32 (device, 16-byte aligned);
+ *   d even, 2..256.
+ * Errors: PIC_ERR_INVALID (n < 0, bad d, theta <= 0). */
+pic_status pic_rope_table(const int32_t* pos, int64_t n, int32_t d, double theta, float* table,
+                          pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a3  Re-rotation of cached K by the chunk offset (rotary correction, RoPE
+ *     article 3.3): K <- R(theta * Delta) K, one rotation, fp32 math, one
+ *     rounding to the pool dtype (bf16 round-to-nearest-even).  V untouched.
+ * ------------------------------------------------------------------------
+ *   k_pool     [num_blocks][Hkv][16][d] (read and written)
+ *   rot        [n_rot] work entries (pic_splice_pages); tab < n_tab
+ *   table      [n_tab][d/2][4] offset table (pic_rope_table over chunk_start)
+ * In place entries read and write the same slots; out-of-place entries must not
+ * overlap another entry's source.  Device errors: PIC_ERR_RANGE (block id outside
+ * [0, num_blocks), tab outside [0, n_tab), lo/hi outside [0, 16]).
+ * Supported: bf16 or fp32 pools, d even, 2 <= d <= 256, d % 16 == 0 for bf16. */
+pic_status pic_rerotate_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int32_t Hkv,
+                          int32_t d, const pic_rot_page* rot, int64_t n_rot, const float* table,
+                          int64_t n_tab, int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a4  Fresh K/V of the recomputed rows (EPIC Step 3: the new K/V replace the
+ *     cached slots / append the query): K <- RoPE(k_raw[i], p_i) rounded to the
+ *     pool dtype, V <- v_raw[i], written to slot row_slot[i] of block
+ *     row_block[i] in both pools.
+ * ------------------------------------------------------------------------
+ *   k_raw, v_raw [n_rows][Hkv][d] pool dtype (un-roped K, V)
+ *   row_table    [n_rows][d/2][4] (pic_rope_table over rows)
+ *   row_block, row_slot [n_rows] (pic_splice_pages)
+ * Device errors: PIC_ERR_RANGE (block or slot out of range). */
+pic_status pic_write_fresh_kv(void* k_pool, void* v_pool, int64_t num_blocks, pic_dtype dtype,
+                              int32_t Hkv, int32_t d, const void* k_raw, const void* v_raw,
+                              const float* row_table, const int32_t* row_block,
+                              const int32_t* row_slot, int64_t n_rows, int32_t* err_flag,
+                              pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a5+a6  Recompute-row link attention (EPIC Step 3; offset causal mask of the
+ *        KV-cache blog).  For every recomputed row i of request r and query
+ *        head h:  out[i][h] = sum_j softmax_j(scale * RoPE(q[i][h], p_i) . K_j) V_j
+ *        over the request's pages, keys at global positions <= p_i, KV head
+ *        h / (Hq/Hkv).  Q is roped on load and rounded to the pool dtype; scores,
+ *        softmax and accumulation are fp32; out is written in the pool dtype.
+ * ------------------------------------------------------------------------
+ *   q           [n_rows][Hq][d] un-roped Q (pool dtype)
+ *   row_table   [n_rows][d/2][4] (pic_rope_table over rows)
+ *   rows        [n_rows] global positions (pic_select_rows); row_off [n_req+1]
+ *   k_pool, v_pool [num_blocks][Hkv][16][d]
+ *   pages       link page lists (pic_splice_pages); page_off [n_req+1]
+ *   out         [n_rows][Hq][d] pool dtype
+ *   ws          workspace of at least pic_link_attention_workspace() bytes,
+ *               256-byte aligned; contents need not be initialised.
+ * bf16 pools with d = 128 and Hq/Hkv in {1, 2, 4, 8, 16} run on the tensor cores
+ * (tcgen05, TMEM accumulators, TMA page loads); fp32 pools and other bf16 shapes
+ * run on the SIMT kernel.  Every bounded wait that runs out sets
+ * PIC_ERR_TIMEOUT in *err_flag and the kernel returns.
+ * Errors: PIC_ERR_INVALID (Hq % Hkv != 0, bad d, n_req < 0, ...),
+ * PIC_ERR_WORKSPACE, PIC_ERR_UNSUPPORTED, PIC_ERR_CUDA. */
+size_t pic_link_attention_workspace(int64_t n_rows, int32_t n_req, int32_t Hq, int32_t Hkv,
+                                    int32_t d, pic_dtype dtype);
+
+pic_status pic_link_attention(const void* q, const float* row_table, const int32_t* rows,
+                              const int32_t* row_off, const void* k_pool, const void* v_pool,
+                              int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                              const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                              int32_t Hkv, int32_t d, float scale, void* out, void* ws,
+                              size_t ws_bytes, int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Diagnostics.
+ * ------------------------------------------------------------------------
+ * One 128 x 128 x 128 bf16 tensor-core product through the same shared-memory
+ * layouts, descriptors and TMEM read-back the attention kernel uses:
+ *   d_kmajor[m][n] = sum_k a[m][k] * b[n][k]    (B K-major, as Q.K^T)
+ *   d_mnmajor[m][n] = sum_k a[m][k] * b[k][n]   (B MN-major, as P.V)
+ * a, b: [128][128] bf16 row-major (device); outputs [128][128] fp32 (device).
+ * One launch of one thread block.  Not part of the link step. */
+pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, float* d_mnmajor,
+                             int32_t* err_flag, pic_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PIC_H_ */

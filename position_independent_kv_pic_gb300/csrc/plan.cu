@@ -1,0 +1,260 @@
+// Link-step metadata on the device: LegoLink row selection, the splice (page
+// lists, re-rotation work, fresh-row slots) and the RoPE cos/sin tables.
+//
+// Row selection follows the EPIC blog review's link_legolink Step 1: chunk 0 is
+// never recomputed, every later chunk recomputes its first min(k, L_c) tokens,
+// and every query token is recomputed.  The splice follows Step 3: cached K/V
+// land at their global positions, the recomputed rows' fresh K/V replace the
+// cached head rows (HYPIC's seam window keeps those rows out of the cache), and
+// the query's K/V are appended.
+#include "pic_internal.cuh"
+
+namespace pic {
+namespace {
+
+constexpr int kPlanThreads = 256;
+
+// Per-chunk quantities of one request, for chunks processed in groups of
+// kPlanThreads.  m = recomputed head rows, np = pages of the chunk,
+// kept = cached pages keeping at least one slot, fp = fresh pages.
+struct ChunkInfo {
+  int L, m, np, kept, fp;
+};
+
+__device__ __forceinline__ ChunkInfo chunk_info(int L, int c_local, int k) {
+  ChunkInfo ci;
+  ci.L = L;
+  ci.m = (c_local == 0) ? 0 : min(k, L);
+  ci.np = ceil_div(L, PIC_PAGE);
+  ci.kept = (ci.m == L) ? 0 : ci.np - ci.m / PIC_PAGE;
+  ci.fp = ceil_div(ci.m, PIC_PAGE);
+  return ci;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+select_rows_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict__ chunk_off,
+                   const int32_t* __restrict__ q_len, const int32_t* __restrict__ kk,
+                   const int32_t* __restrict__ row_off, int32_t* __restrict__ rows,
+                   int32_t* __restrict__ chunk_start, int32_t* err) {
+  __shared__ int scratch[kPlanThreads / 32 + 1];
+  const int r = blockIdx.x;
+  const int c0 = chunk_off[r], c1 = chunk_off[r + 1];
+  const int q = q_len[r], k = kk[r];
+  const int rbeg = row_off[r], rend = row_off[r + 1];
+  if (q < 0 || k < 0 || c1 < c0) {
+    if (threadIdx.x == 0) set_err(err, PIC_ERR_INVALID);
+    return;
+  }
+  int pos_base = 0, row_base = 0;  // running s_c and running row count
+  for (int g = c0; g < c1; g += kPlanThreads) {
+    const int c = g + threadIdx.x;
+    int L = 0, m = 0;
+    if (c < c1) {
+      L = chunk_lens[c];
+      if (L < 1) {
+        set_err(err, PIC_ERR_INVALID);
+        L = 1;
+      }
+      m = (c == c0) ? 0 : min(k, L);
+    }
+    int totL, totM;
+    const int s = pos_base + block_exclusive_scan<kPlanThreads>(L, scratch, &totL);
+    const int mo = row_base + block_exclusive_scan<kPlanThreads>(m, scratch, &totM);
+    if (c < c1) {
+      chunk_start[c] = s;
+      for (int j = 0; j < m; ++j) {
+        const int idx = rbeg + mo + j;
+        if (idx < rend) rows[idx] = s + j;
+      }
+    }
+    pos_base += totL;
+    row_base += totM;
+  }
+  // query rows at T .. T+q-1
+  for (int j = threadIdx.x; j < q; j += kPlanThreads) {
+    const int idx = rbeg + row_base + j;
+    if (idx < rend) rows[idx] = pos_base + j;
+  }
+  if (threadIdx.x == 0 && row_base + q != rend - rbeg) set_err(err, PIC_ERR_RANGE);
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict__ chunk_off,
+              const int32_t* __restrict__ q_len, const int32_t* __restrict__ kk,
+              const int32_t* __restrict__ chunk_start, const int32_t* __restrict__ chunk_page_off,
+              const int32_t* __restrict__ k_src, const int32_t* __restrict__ k_dst,
+              const int32_t* __restrict__ v_blk, const int32_t* __restrict__ fresh_off,
+              const int32_t* __restrict__ fresh_blocks, const int32_t* __restrict__ row_off,
+              const int32_t* __restrict__ page_off, const int32_t* __restrict__ rot_off,
+              pic_link_page* __restrict__ pages, pic_rot_page* __restrict__ rot,
+              int32_t* __restrict__ row_block, int32_t* __restrict__ row_slot, int32_t* err) {
+  __shared__ int scratch[kPlanThreads / 32 + 1];
+  const int r = blockIdx.x;
+  const int c0 = chunk_off[r], c1 = chunk_off[r + 1];
+  const int q = q_len[r], k = kk[r];
+  if (q < 0 || k < 0 || c1 < c0) {
+    if (threadIdx.x == 0) set_err(err, PIC_ERR_INVALID);
+    return;
+  }
+  const int pbeg = page_off[r], pend = page_off[r + 1];
+  const int obeg = rot_off[r], oend = rot_off[r + 1];
+  const int fbeg = fresh_off[r], fend = fresh_off[r + 1];
+  const int rbeg = row_off[r], rend = row_off[r + 1];
+
+  int link_base = 0, rot_base = 0, fresh_base = 0, row_base = 0, T = 0;
+  for (int g = c0; g < c1; g += kPlanThreads) {
+    const int c = g + threadIdx.x;
+    ChunkInfo ci = {0, 0, 0, 0, 0};
+    if (c < c1) {
+      ci = chunk_info(max(chunk_lens[c], 1), c - c0, k);
+      if (chunk_page_off[c + 1] - chunk_page_off[c] != ci.np) set_err(err, PIC_ERR_RANGE);
+    }
+    int t_link, t_rot, t_fresh, t_row, t_len;
+    const int lo_link = link_base + block_exclusive_scan<kPlanThreads>(ci.fp + ci.kept, scratch, &t_link);
+    const int lo_rot = rot_base + block_exclusive_scan<kPlanThreads>((c > c0) ? ci.kept : 0, scratch, &t_rot);
+    const int lo_fresh = fresh_base + block_exclusive_scan<kPlanThreads>(ci.fp, scratch, &t_fresh);
+    const int lo_row = row_base + block_exclusive_scan<kPlanThreads>(ci.m, scratch, &t_row);
+    block_exclusive_scan<kPlanThreads>(ci.L, scratch, &t_len);
+    if (c < c1) {
+      const int s = chunk_start[c];
+      // fresh head pages of this chunk
+      for (int f = 0; f < ci.fp; ++f) {
+        const int fi = fbeg + lo_fresh + f, pi = pbeg + lo_link + f;
+        if (fi >= fend || pi >= pend) { set_err(err, PIC_ERR_RANGE); break; }
+        const int b = fresh_blocks[fi];
+        pic_link_page pg;
+        pg.k_block = b; pg.v_block = b; pg.gpos0 = s + PIC_PAGE * f;
+        pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, ci.m - PIC_PAGE * f);
+        pages[pi] = pg;
+      }
+      for (int j = 0; j < ci.m; ++j) {
+        const int ri = rbeg + lo_row + j, fi = fbeg + lo_fresh + j / PIC_PAGE;
+        if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); break; }
+        row_block[ri] = fresh_blocks[fi];
+        row_slot[ri] = j % PIC_PAGE;
+      }
+      // cached pages that keep at least one slot
+      const int j0 = ci.np - ci.kept;
+      for (int j = j0; j < ci.np; ++j) {
+        const int t = j - j0;
+        const int pi = pbeg + lo_link + ci.fp + t;
+        if (pi >= pend) { set_err(err, PIC_ERR_RANGE); break; }
+        const int cp = chunk_page_off[c] + j;
+        const int src = k_src[cp];
+        const int dst = (k_dst != nullptr) ? k_dst[cp] : src;
+        pic_link_page pg;
+        pg.k_block = (c == c0) ? src : dst;  // chunk 0 keeps Delta = 0
+        pg.v_block = v_blk[cp];
+        pg.gpos0 = s + PIC_PAGE * j;
+        pg.lo = (int16_t)max(0, ci.m - PIC_PAGE * j);
+        pg.hi = (int16_t)min(PIC_PAGE, ci.L - PIC_PAGE * j);
+        pages[pi] = pg;
+        if (c > c0) {
+          const int oi = obeg + lo_rot + t;
+          if (oi >= oend) { set_err(err, PIC_ERR_RANGE); break; }
+          pic_rot_page rp;
+          rp.src_block = src; rp.dst_block = dst; rp.tab = c; rp.lo = pg.lo; rp.hi = pg.hi;
+          rot[oi] = rp;
+        }
+      }
+    }
+    link_base += t_link;
+    rot_base += t_rot;
+    fresh_base += t_fresh;
+    row_base += t_row;
+    T += t_len;
+  }
+  // query pages and rows
+  const int qp = ceil_div(q, PIC_PAGE);
+  for (int f = threadIdx.x; f < qp; f += kPlanThreads) {
+    const int fi = fbeg + fresh_base + f, pi = pbeg + link_base + f;
+    if (fi >= fend || pi >= pend) { set_err(err, PIC_ERR_RANGE); continue; }
+    const int b = fresh_blocks[fi];
+    pic_link_page pg;
+    pg.k_block = b; pg.v_block = b; pg.gpos0 = T + PIC_PAGE * f;
+    pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, q - PIC_PAGE * f);
+    pages[pi] = pg;
+  }
+  for (int j = threadIdx.x; j < q; j += kPlanThreads) {
+    const int ri = rbeg + row_base + j, fi = fbeg + fresh_base + j / PIC_PAGE;
+    if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
+    row_block[ri] = fresh_blocks[fi];
+    row_slot[ri] = j % PIC_PAGE;
+  }
+  if (threadIdx.x == 0) {
+    if (link_base + qp != pend - pbeg || rot_base != oend - obeg ||
+        fresh_base + qp != fend - fbeg || row_base + q != rend - rbeg)
+      set_err(err, PIC_ERR_RANGE);
+  }
+}
+
+// table[i][j] = {cos_hi, sin_hi, cos_lo, sin_lo} of pos[i] * theta^(-2j/d): fp64 math,
+// hi = fp32(v) and lo = fp32(v - hi).
+__global__ void rope_table_kernel(const int32_t* __restrict__ pos, int64_t n, int half, double theta,
+                                  float4* __restrict__ table) {
+  const int64_t total = n * half;
+  for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
+       t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = t / half;
+    const int j = (int)(t - i * half);
+    const double inv_freq = pow(theta, -2.0 * (double)j / (double)(2 * half));
+    const double ang = (double)pos[i] * inv_freq;
+    double s, c;
+    sincos(ang, &s, &c);
+    const float ch = (float)c, sh = (float)s;
+    table[t] = make_float4(ch, sh, (float)(c - (double)ch), (float)(s - (double)sh));
+  }
+}
+
+}  // namespace
+}  // namespace pic
+
+using namespace pic;
+
+extern "C" {
+
+pic_status pic_select_rows(const int32_t* chunk_lens, const int32_t* chunk_off, const int32_t* q_len,
+                           const int32_t* k, const int32_t* row_off, int32_t n_req, int32_t* rows,
+                           int32_t* chunk_start, int32_t* err_flag, pic_stream_t stream) {
+  if (n_req < 0) return PIC_ERR_INVALID;
+  if (n_req == 0) return PIC_OK;
+  if (!chunk_off || !q_len || !k || !row_off || !err_flag) return PIC_ERR_INVALID;
+  select_rows_kernel<<<n_req, kPlanThreads, 0, (cudaStream_t)stream>>>(
+      chunk_lens, chunk_off, q_len, k, row_off, rows, chunk_start, err_flag);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off, const int32_t* q_len,
+                            const int32_t* k, int32_t n_req, const int32_t* chunk_start,
+                            const int32_t* chunk_page_off, const int32_t* k_src_blocks,
+                            const int32_t* k_dst_blocks, const int32_t* v_blocks,
+                            const int32_t* fresh_off, const int32_t* fresh_blocks,
+                            const int32_t* row_off, const int32_t* page_off, const int32_t* rot_off,
+                            pic_link_page* pages, pic_rot_page* rot, int32_t* row_block,
+                            int32_t* row_slot, int32_t* err_flag, pic_stream_t stream) {
+  if (n_req < 0) return PIC_ERR_INVALID;
+  if (n_req == 0) return PIC_OK;
+  if (!chunk_off || !q_len || !k || !chunk_page_off || !fresh_off || !row_off || !page_off ||
+      !rot_off || !err_flag)
+    return PIC_ERR_INVALID;
+  splice_kernel<<<n_req, kPlanThreads, 0, (cudaStream_t)stream>>>(
+      chunk_lens, chunk_off, q_len, k, chunk_start, chunk_page_off, k_src_blocks, k_dst_blocks,
+      v_blocks, fresh_off, fresh_blocks, row_off, page_off, rot_off, pages, rot, row_block, row_slot,
+      err_flag);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+pic_status pic_rope_table(const int32_t* pos, int64_t n, int32_t d, double theta, float* table,
+                          pic_stream_t stream) {
+  if (n < 0 || d < 2 || d > 256 || (d & 1) || !(theta > 0.0)) return PIC_ERR_INVALID;
+  if (n == 0) return PIC_OK;
+  if (!pos || !table) return PIC_ERR_INVALID;
+  const int64_t total = n * (d / 2);
+  const int threads = 256;
+  const int64_t blocks = (total + threads - 1) / threads;
+  rope_table_kernel<<<(unsigned)(blocks < 65535 ? blocks : 65535), threads, 0, (cudaStream_t)stream>>>(
+      pos, n, d / 2, theta, reinterpret_cast<float4*>(table));
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,255 @@
+// Rotary correction of cached K (article on RoPE and prefix caching, section
+// 3.3): a K cached at local position j is moved to global position j + Delta by
+// ONE rotation R(theta * Delta) of every dimension pair (i, i + d/2), with
+// cos/sin taken from a per-offset table.  Also the fresh K/V writer of the
+// recomputed rows (EPIC link_legolink Step 3).
+//
+// Both are HBM-bound streaming passes.  One work item is one 16-byte vector of
+// the low half of a key row plus the matching vector of its high half (the
+// pair partners), so every warp access is a run of full 32-byte sectors; the
+// cos/sin vectors come from a small table that stays in L1/L2.
+#include "pic_internal.cuh"
+
+namespace pic {
+namespace {
+
+constexpr int kRotThreads = 256;
+constexpr int kRotUnroll = 4;  // independent items in flight per thread
+
+template <typename T> struct Vec16;
+template <> struct Vec16<__nv_bfloat16> { static constexpr int N = 8; };
+template <> struct Vec16<float> { static constexpr int N = 4; };
+
+template <typename T>
+__device__ __forceinline__ void unpack(const uint4& v, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 t = __bfloat1622float2(h[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  } else {
+    const float* s = reinterpret_cast<const float*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) f[i] = s[i];
+  }
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 pack(const float* f) {
+  uint4 v;
+  if constexpr (sizeof(T) == 2) {
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+  } else {
+    float* s = reinterpret_cast<float*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] = f[i];
+  }
+  return v;
+}
+
+template <int N>
+__device__ __forceinline__ void rotate(float* lo, float* hi, const float4* cs) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) rope_rotate(lo[i], hi[i], cs[i], lo[i], hi[i]);
+}
+
+template <int N>
+__device__ __forceinline__ void load_cs(const float4* __restrict__ p, float4* cs) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) cs[i] = __ldg(p + i);
+}
+
+// Item index -> (entry e, head h, slot s, vector v); G = vectors per half row.
+template <typename T>
+__global__ void __launch_bounds__(kRotThreads)
+rerotate_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d,
+                const pic_rot_page* __restrict__ rot, int64_t n_rot, const float4* __restrict__ table,
+                int64_t n_tab, int32_t* err) {
+  constexpr int N = Vec16<T>::N;
+  const int half = d / 2;
+  const int G = half / N;
+  const int64_t per_entry = (int64_t)Hkv * PIC_PAGE * G;
+  const int64_t total = n_rot * per_entry;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; base < total;
+       base += stride * kRotUnroll) {
+    uint4 xl[kRotUnroll], xh[kRotUnroll];
+    T* dst[kRotUnroll];
+    const float4* cs_ptr[kRotUnroll];
+    bool act[kRotUnroll];
+#pragma unroll
+    for (int u = 0; u < kRotUnroll; ++u) {
+      const int64_t it = base + u * stride;
+      act[u] = false;
+      if (it < total) {
+        const int64_t e = it / per_entry;
+        const int rem = (int)(it - e * per_entry);
+        const int v = rem % G;
+        const int s = (rem / G) % PIC_PAGE;
+        const int h = rem / (G * PIC_PAGE);
+        const pic_rot_page rp = rot[e];
+        if (s >= rp.lo && s < rp.hi) {
+          if (rp.src_block < 0 || rp.src_block >= num_blocks || rp.dst_block < 0 ||
+              rp.dst_block >= num_blocks || rp.tab < 0 || rp.tab >= n_tab || rp.lo < 0 ||
+              rp.hi > PIC_PAGE) {
+            set_err(err, PIC_ERR_RANGE);
+          } else {
+            const int64_t row = ((int64_t)rp.src_block * Hkv + h) * PIC_PAGE + s;
+            const int64_t drow = ((int64_t)rp.dst_block * Hkv + h) * PIC_PAGE + s;
+            const T* src = pool + row * d + v * N;
+            xl[u] = __ldcs(reinterpret_cast<const uint4*>(src));
+            xh[u] = __ldcs(reinterpret_cast<const uint4*>(src + half));
+            dst[u] = pool + drow * d + v * N;
+            cs_ptr[u] = table + (int64_t)rp.tab * half + v * N;
+            act[u] = true;
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kRotUnroll; ++u) {
+      if (!act[u]) continue;
+      float lo[N], hi[N];
+      float4 cs[N];
+      load_cs<N>(cs_ptr[u], cs);
+      unpack<T>(xl[u], lo);
+      unpack<T>(xh[u], hi);
+      rotate<N>(lo, hi, cs);
+      __stcs(reinterpret_cast<uint4*>(dst[u]), pack<T>(lo));
+      __stcs(reinterpret_cast<uint4*>(dst[u] + half), pack<T>(hi));
+    }
+  }
+}
+
+// Fresh rows: item = (row i, head h, vector v).  K is roped at the row's global
+// position (row table), V is copied.
+template <typename T>
+__global__ void __launch_bounds__(kRotThreads)
+write_fresh_kernel(T* __restrict__ kpool, T* __restrict__ vpool, int64_t num_blocks, int Hkv, int d,
+                   const T* __restrict__ k_raw, const T* __restrict__ v_raw,
+                   const float4* __restrict__ row_table, const int32_t* __restrict__ row_block,
+                   const int32_t* __restrict__ row_slot, int64_t n_rows, int32_t* err) {
+  constexpr int N = Vec16<T>::N;
+  const int half = d / 2;
+  const int G = half / N;
+  const int64_t per_row = (int64_t)Hkv * G;
+  const int64_t total = n_rows * per_row;
+  for (int64_t it = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; it < total;
+       it += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t i = it / per_row;
+    const int rem = (int)(it - i * per_row);
+    const int v = rem % G;
+    const int h = rem / G;
+    const int b = row_block[i], s = row_slot[i];
+    if (b < 0 || b >= num_blocks || s < 0 || s >= PIC_PAGE) {
+      set_err(err, PIC_ERR_RANGE);
+      continue;
+    }
+    const int64_t src = (i * Hkv + h) * (int64_t)d + v * N;
+    const int64_t dst = (((int64_t)b * Hkv + h) * PIC_PAGE + s) * d + v * N;
+    const uint4 kl = *reinterpret_cast<const uint4*>(k_raw + src);
+    const uint4 kh = *reinterpret_cast<const uint4*>(k_raw + src + half);
+    const uint4 vl = *reinterpret_cast<const uint4*>(v_raw + src);
+    const uint4 vh = *reinterpret_cast<const uint4*>(v_raw + src + half);
+    float lo[N], hi[N];
+    float4 cs[N];
+    load_cs<N>(row_table + i * half + v * N, cs);
+    unpack<T>(kl, lo);
+    unpack<T>(kh, hi);
+    rotate<N>(lo, hi, cs);
+    *reinterpret_cast<uint4*>(kpool + dst) = pack<T>(lo);
+    *reinterpret_cast<uint4*>(kpool + dst + half) = pack<T>(hi);
+    *reinterpret_cast<uint4*>(vpool + dst) = vl;
+    *reinterpret_cast<uint4*>(vpool + dst + half) = vh;
+  }
+}
+
+int grid_for(int64_t items) {
+  const int sms = num_sms_of_current_device();
+  const int64_t want = (items + kRotThreads * kRotUnroll - 1) / (kRotThreads * kRotUnroll);
+  const int64_t cap = (int64_t)sms * 8;  // 8 blocks of 256 threads fill an SM
+  return (int)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+bool shape_ok(pic_dtype dt, int Hkv, int d) {
+  if (Hkv < 1 || d < 2 || d > 256 || (d & 1)) return false;
+  const int n = (dt == PIC_BF16) ? 8 : 4;
+  return (d / 2) % n == 0;
+}
+
+}  // namespace
+
+int num_sms_of_current_device() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+  return n > 0 ? n : 1;
+}
+
+}  // namespace pic
+
+using namespace pic;
+
+extern "C" {
+
+pic_status pic_rerotate_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int32_t Hkv, int32_t d,
+                          const pic_rot_page* rot, int64_t n_rot, const float* table, int64_t n_tab,
+                          int32_t* err_flag, pic_stream_t stream) {
+  if (n_rot < 0 || num_blocks < 0 || n_tab < 0) return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (!shape_ok(dtype, Hkv, d)) return (d > 0 && !(d & 1)) ? PIC_ERR_UNSUPPORTED : PIC_ERR_INVALID;
+  if (n_rot == 0) return PIC_OK;
+  if (!k_pool || !rot || !table || !err_flag) return PIC_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(table) & 15))
+    return PIC_ERR_INVALID;
+  const int n = (dtype == PIC_BF16) ? 8 : 4;
+  const int64_t items = n_rot * Hkv * PIC_PAGE * (d / 2 / n);
+  const int grid = grid_for(items);
+  if (dtype == PIC_BF16)
+    rerotate_kernel<__nv_bfloat16><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<__nv_bfloat16*>(k_pool), num_blocks, Hkv, d, rot, n_rot,
+        reinterpret_cast<const float4*>(table), n_tab, err_flag);
+  else
+    rerotate_kernel<float><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<float*>(k_pool), num_blocks, Hkv, d, rot, n_rot,
+        reinterpret_cast<const float4*>(table), n_tab, err_flag);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+pic_status pic_write_fresh_kv(void* k_pool, void* v_pool, int64_t num_blocks, pic_dtype dtype,
+                              int32_t Hkv, int32_t d, const void* k_raw, const void* v_raw,
+                              const float* row_table, const int32_t* row_block,
+                              const int32_t* row_slot, int64_t n_rows, int32_t* err_flag,
+                              pic_stream_t stream) {
+  if (n_rows < 0 || num_blocks < 0) return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (!shape_ok(dtype, Hkv, d)) return (d > 0 && !(d & 1)) ? PIC_ERR_UNSUPPORTED : PIC_ERR_INVALID;
+  if (n_rows == 0) return PIC_OK;
+  if (!k_pool || !v_pool || !k_raw || !v_raw || !row_table || !row_block || !row_slot || !err_flag)
+    return PIC_ERR_INVALID;
+  const uintptr_t mis = reinterpret_cast<uintptr_t>(k_pool) | reinterpret_cast<uintptr_t>(v_pool) |
+                        reinterpret_cast<uintptr_t>(k_raw) | reinterpret_cast<uintptr_t>(v_raw) |
+                        reinterpret_cast<uintptr_t>(row_table);
+  if (mis & 15) return PIC_ERR_INVALID;
+  const int n = (dtype == PIC_BF16) ? 8 : 4;
+  const int64_t items = n_rows * Hkv * (d / 2 / n);
+  const int grid = grid_for(items * kRotUnroll);
+  if (dtype == PIC_BF16)
+    write_fresh_kernel<__nv_bfloat16><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<__nv_bfloat16*>(k_pool), static_cast<__nv_bfloat16*>(v_pool), num_blocks, Hkv, d,
+        static_cast<const __nv_bfloat16*>(k_raw), static_cast<const __nv_bfloat16*>(v_raw),
+        reinterpret_cast<const float4*>(row_table), row_block, row_slot, n_rows, err_flag);
+  else
+    write_fresh_kernel<float><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<float*>(k_pool), static_cast<float*>(v_pool), num_blocks, Hkv, d,
+        static_cast<const float*>(k_raw), static_cast<const float*>(v_raw),
+        reinterpret_cast<const float4*>(row_table), row_block, row_slot, n_rows, err_flag);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+}  // extern "C"

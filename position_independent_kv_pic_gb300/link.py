@@ -1,0 +1,213 @@
+"""One link step over a batch of requests, through the C ABI.
+
+Host side of the step, as a serving engine would drive it:
+  * the paged KV pool (K and V, [num_blocks][Hkv][16][d]) holds every cached chunk as
+    it was compiled, one chunk per run of pages (a block manager's job: this module
+    assigns the physical block ids, scattered by a seeded permutation);
+  * per-request metadata (chunk lengths in link order, q, k, block tables, fresh
+    blocks) and the recomputed rows' un-roped Q, K and V are the step's inputs;
+  * ``run()`` issues the device calls: row selection, splice, RoPE tables,
+    re-rotation of cached K, fresh K/V, link attention.  Every one is a kernel of
+    libpic.so; nothing here computes on the data.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import (PIC_BF16, PIC_FP32, PIC_PAGE, pic_link_attention, pic_link_attention_workspace,
+               pic_plan_offsets, pic_rerotate_k, pic_rope_table, pic_select_rows, pic_splice_pages,
+               pic_write_fresh_kv)
+from .inputs import Workload, block_shuffle, chunk_store, row_inputs
+
+
+def _cdiv(a, b):
+    return (a + b - 1) // b
+
+
+class LinkBatch:
+    """Device state and inputs of one link step for the requests of a workload."""
+
+    def __init__(self, wl: Workload, device="cuda", rows_inputs=None):
+        self.wl = wl
+        self.device = torch.device(device)
+        self.dtype = wl.torch_dtype
+        self.pic_dtype = PIC_BF16 if wl.dtype == "bf16" else PIC_FP32
+        Hkv, d = wl.Hkv, wl.d
+
+        # ---- request metadata (host)
+        flat_ids = np.concatenate([r.chunk_ids for r in wl.requests]).astype(np.int64) \
+            if wl.requests else np.zeros(0, np.int64)
+        self.flat_store_ids = flat_ids
+        self.chunk_lens = wl.chunk_lens[flat_ids].astype(np.int32)
+        self.chunk_off = np.zeros(len(wl.requests) + 1, np.int32)
+        self.chunk_off[1:] = np.cumsum([len(r.chunk_ids) for r in wl.requests])
+        self.q_len = np.array([r.q for r in wl.requests], np.int32)
+        self.k = np.array([r.k for r in wl.requests], np.int32)
+        offs = pic_plan_offsets(self.chunk_lens, self.chunk_off, self.q_len, self.k)
+        self.offs = offs
+        self.n_req = len(wl.requests)
+        self.n_rows = int(offs["row_off"][-1])
+        self.n_pages = int(offs["page_off"][-1])
+        self.n_rot = int(offs["rot_off"][-1])
+        self.n_fresh = int(offs["fresh_off"][-1])
+        self.n_chunks = len(self.chunk_lens)
+        self.tokens = int(self.chunk_lens.sum()) + int(self.q_len.sum())
+
+        # ---- block allocation
+        store_np = np.array([_cdiv(int(L), PIC_PAGE) for L in wl.chunk_lens], np.int64)
+        store_base = np.zeros(len(store_np) + 1, np.int64)
+        store_base[1:] = np.cumsum(store_np)
+        n_store_pages = int(store_base[-1])
+        n_chunk_pages = int(offs["chunk_page_off"][-1])
+        n_dst = n_chunk_pages if wl.out_of_place else 0
+        self.num_blocks = n_store_pages + n_dst + self.n_fresh
+        perm = block_shuffle(wl, self.num_blocks).astype(np.int64)
+        self.store_blocks = [perm[store_base[c]:store_base[c + 1]] for c in range(len(store_np))]
+        k_src = np.concatenate([self.store_blocks[c] for c in flat_ids]) if len(flat_ids) else np.zeros(0, np.int64)
+        self.k_src = k_src.astype(np.int32)
+        self.v_blocks = self.k_src.copy()
+        self.k_dst = perm[n_store_pages:n_store_pages + n_dst].astype(np.int32) if wl.out_of_place else None
+        self.fresh_blocks = perm[n_store_pages + n_dst:].astype(np.int32)
+
+        # ---- pool: the cached chunks as compiled
+        kst, vst, soff = chunk_store(wl)
+        self.store_k, self.store_v, self.store_off = kst, vst, soff
+        shape = (self.num_blocks, Hkv, PIC_PAGE, d)
+        self.k_pool = torch.zeros(shape, dtype=self.dtype, device=self.device)
+        self.v_pool = torch.zeros(shape, dtype=self.dtype, device=self.device)
+        self.reset_pool()
+
+        # ---- recomputed rows' inputs
+        if rows_inputs is None:
+            rows_inputs = row_inputs(wl, self.n_rows)
+        self.q_raw_h, self.k_new_h, self.v_new_h = rows_inputs
+
+        # ---- device buffers
+        dev, i32 = self.device, torch.int32
+        self.host = {
+            "chunk_lens": torch.from_numpy(self.chunk_lens), "chunk_off": torch.from_numpy(self.chunk_off),
+            "q_len": torch.from_numpy(self.q_len), "k": torch.from_numpy(self.k),
+            "row_off": torch.from_numpy(offs["row_off"]), "page_off": torch.from_numpy(offs["page_off"]),
+            "rot_off": torch.from_numpy(offs["rot_off"]), "fresh_off": torch.from_numpy(offs["fresh_off"]),
+            "chunk_page_off": torch.from_numpy(offs["chunk_page_off"]),
+            "k_src": torch.from_numpy(self.k_src), "v_blocks": torch.from_numpy(self.v_blocks),
+            "fresh_blocks": torch.from_numpy(self.fresh_blocks),
+            "q_raw": self.q_raw_h, "k_new": self.k_new_h, "v_new": self.v_new_h,
+        }
+        if self.k_dst is not None:
+            self.host["k_dst"] = torch.from_numpy(self.k_dst)
+        self.dev = {n: t.to(dev) for n, t in self.host.items()}
+        self.rows = torch.empty(self.n_rows, dtype=i32, device=dev)
+        self.chunk_start = torch.empty(self.n_chunks, dtype=i32, device=dev)
+        self.pages = torch.empty((self.n_pages, 4), dtype=i32, device=dev)   # pic_link_page, 16 B
+        self.rot = torch.empty((self.n_rot, 4), dtype=i32, device=dev)       # pic_rot_page, 16 B
+        self.row_block = torch.empty(self.n_rows, dtype=i32, device=dev)
+        self.row_slot = torch.empty(self.n_rows, dtype=i32, device=dev)
+        self.delta_table = torch.empty((self.n_chunks, d // 2, 4), dtype=torch.float32, device=dev)
+        self.row_table = torch.empty((self.n_rows, d // 2, 4), dtype=torch.float32, device=dev)
+        self.out = torch.empty((self.n_rows, wl.Hq, d), dtype=self.dtype, device=dev)
+        ws = pic_link_attention_workspace(self.n_rows, self.n_req, wl.Hq, wl.Hkv, d, self.pic_dtype)
+        self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws > 0 else None
+        self.err = torch.zeros(1, dtype=i32, device=dev)
+        self.scale = 1.0 / math.sqrt(d)
+
+    # ------------------------------------------------------------------ state
+    def reset_pool(self):
+        """Write every cached chunk, as compiled, into its pages (zeroing the rest)."""
+        wl = self.wl
+        self.k_pool.zero_()
+        self.v_pool.zero_()
+        blk, slot, src = [], [], []
+        for c, blocks in enumerate(self.store_blocks):
+            L = int(wl.chunk_lens[c])
+            j = np.arange(L)
+            blk.append(blocks[j // PIC_PAGE])
+            slot.append(j % PIC_PAGE)
+            src.append(self.store_off[c] + j)
+        if blk:
+            b = torch.from_numpy(np.concatenate(blk)).to(self.device)
+            s = torch.from_numpy(np.concatenate(slot)).to(self.device)
+            idx = torch.from_numpy(np.concatenate(src)).to(self.device)
+            self.k_pool[b, :, s, :] = self.store_k.to(self.device)[idx]
+            self.v_pool[b, :, s, :] = self.store_v.to(self.device)[idx]
+
+    def pin_host_inputs(self):
+        """Page-locked copies of the step's per-request inputs (for end-to-end timing)."""
+        self.host_pinned = {n: t.pin_memory() for n, t in self.host.items()}
+        self.out_host = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+
+    def upload(self):
+        """Host -> device copies of the step's inputs (async on the current stream)."""
+        for n, t in self.host_pinned.items():
+            self.dev[n].copy_(t, non_blocking=True)
+
+    def download(self):
+        """Device -> host copy of the step's result (async on the current stream)."""
+        self.out_host.copy_(self.out, non_blocking=True)
+        return self.out_host
+
+    def h2d_bytes(self) -> int:
+        return sum(t.numel() * t.element_size() for t in self.host.values())
+
+    def d2h_bytes(self) -> int:
+        return self.out.numel() * self.out.element_size()
+
+    # ------------------------------------------------------------------ step
+    # kernels one run() launches: select, splice, 2 tables, re-rotate, fresh K/V, and the
+    # attention call (unit planning, attention, LSE merge)
+    LAUNCHES_PER_STEP = 9
+
+    def run(self, stream=None, marks=None):
+        """The link step: a1 select, splice, a2 tables, a3 re-rotate, a4 fresh K/V, a5+a6 attention.
+
+        ``marks`` (optional) maps "rerotate" / "attention" to (start, end) CUDA events that
+        are recorded around those calls on the current stream."""
+        wl, dv = self.wl, self.dev
+        mk = marks or {}
+        pic_select_rows(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], dv["row_off"], self.rows,
+                        self.chunk_start, self.err, stream)
+        pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
+                         dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
+                         dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
+                         self.row_block, self.row_slot, self.err, stream)
+        pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, stream)
+        pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, stream)
+        if "rerotate" in mk:
+            mk["rerotate"][0].record()
+        pic_rerotate_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, self.rot, self.n_rot, self.delta_table,
+                       self.n_chunks, self.err, stream)
+        if "rerotate" in mk:
+            mk["rerotate"][1].record()
+        pic_write_fresh_kv(self.k_pool, self.v_pool, self.pic_dtype, wl.Hkv, wl.d, dv["k_new"], dv["v_new"],
+                           self.row_table, self.row_block, self.row_slot, self.n_rows, self.err, stream)
+        if "attention" in mk:
+            mk["attention"][0].record()
+        pic_link_attention(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
+                           self.pic_dtype, self.pages, dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv,
+                           wl.d, self.scale, self.out, self.ws, self.err, stream)
+        if "attention" in mk:
+            mk["attention"][1].record()
+
+    # ------------------------------------------------------------------ read-back helpers (tests)
+    def error(self) -> int:
+        return int(self.err.item())
+
+    def pages_host(self) -> np.ndarray:
+        return self.pages.cpu().numpy().view(np.uint8).view(
+            np.dtype([("k_block", "<i4"), ("v_block", "<i4"), ("gpos0", "<i4"), ("lo", "<i2"), ("hi", "<i2")]))[:, 0]
+
+    def rotated_chunk_k(self, flat_chunk: int) -> torch.Tensor:
+        """K of one linked chunk as it sits in the pool after the step ([L][Hkv][d], CPU)."""
+        L = int(self.chunk_lens[flat_chunk])
+        cp0 = int(self.offs["chunk_page_off"][flat_chunk])
+        r = int(np.searchsorted(self.chunk_off, flat_chunk, side="right") - 1)
+        first = flat_chunk == int(self.chunk_off[r])
+        table = self.k_src if (self.k_dst is None or first) else self.k_dst
+        j = np.arange(L)
+        b = torch.from_numpy(table[cp0 + j // PIC_PAGE].astype(np.int64)).to(self.device)
+        s = torch.from_numpy(j % PIC_PAGE).to(self.device)
+        return self.k_pool[b, :, s, :].cpu()
