@@ -124,6 +124,24 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+# ----------------------------------------------------------------------------- aggregation
+
+def reduce_max(x: float, device: str) -> float:
+    """Max of a per-rank float over the process group (identity without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(world: int, steps: int, tokens_per_rank_step: int, max_total_ms: float) -> float:
+    """Tokens all ranks processed divided by the slowest rank's timed region."""
+    return world * steps * tokens_per_rank_step / (max_total_ms / 1e3)
+
+
 # ----------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args, rank, world):
@@ -156,7 +174,7 @@ def run_gpu(args, rank, world):
     # algorithmic work, from the step's own outputs
     rows = batch.rows.cpu().numpy().astype(np.int64)
     rot = batch.rot.cpu().numpy()
-    lohi = rot[:, 3].view(np.int16).reshape(-1, 2) if len(rot) else np.zeros((0, 2), np.int16)
+    lohi = np.ascontiguousarray(rot[:, 3]).view(np.int16).reshape(-1, 2) if len(rot) else np.zeros((0, 2), np.int16)
     rot_tokens = int((lohi[:, 1].astype(np.int64) - lohi[:, 0]).sum())
     el = 2 if wl.dtype == "bf16" else 4
     rot_bytes = 2 * rot_tokens * wl.Hkv * wl.d * el
@@ -188,13 +206,9 @@ def run_gpu(args, rank, world):
     if batch.error() != 0:
         raise SystemExit(f"device error: {pic.pic_strerror(batch.error())}")
 
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = reduce_max(sum(step_ms), "cuda")
     tokens = batch.tokens
-    value = world * K * tokens / (total_ms / 1e3)
+    value = whole_job_throughput(world, K, tokens, total_ms)
 
     # end to end through the binding: H2D inputs, step, D2H output
     batch.pin_host_inputs()
@@ -256,57 +270,67 @@ def run_gpu(args, rank, world):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_sample_time(wl, batch_rows=None, n_chunks=8, n_rows=4, seed=0):
-    """Time the float64 oracle on a bounded sample of one step of ``wl`` and extrapolate
-    to the whole step.  Returns (seconds for a full step, description, threads)."""
-    import oracle.pic_oracle as O
-    from position_independent_kv_pic_gb300 import inputs
+class OracleSampler:
+    """The float64 oracle, as it stands, timed on a bounded sample of one step.
 
-    rng = np.random.default_rng(seed)
-    kst, vst, off = inputs.chunk_store(wl)
-    total_rot_tokens, total_pp1, t_rot, t_att = 0, 0, 0.0, 0.0
-    s_rot_tokens, s_pp1 = 0, 0
-    for req in wl.requests[:1] if len(wl.requests) == 1 else wl.requests[:2]:
-        lens = wl.chunk_lens[req.chunk_ids]
-        rows, starts, T = O.select_rows(lens, req.q, req.k)
-        ck = [kst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
-        cv = [vst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
-        n = len(rows)
-        qr, kn, vn = (t.double().numpy() for t in inputs.row_inputs(wl, n))
-        # context built once, untimed; the timed sample re-runs pieces of it
-        K_ctx, V_ctx, rows, starts, T = O.splice_context(ck, cv, req.q, req.k, kn, vn, wl.theta, wl.dtype)
-        q_rot = O.round_to(O.rope(qr, rows, wl.theta), wl.dtype)
-        cs = rng.choice(np.arange(1, len(ck)), size=min(n_chunks, len(ck) - 1), replace=False) if len(ck) > 1 else []
-        t0 = time.perf_counter()
-        for c in cs:
-            O.rerotate_k(ck[c], int(starts[c]), wl.theta, wl.dtype)
-        t_rot += time.perf_counter() - t0
-        s_rot_tokens += sum(len(ck[c]) for c in cs)
-        total_rot_tokens += sum(len(c) for c in ck[1:])
-        which = sorted(rng.choice(n, size=min(n_rows, n), replace=False).tolist()) if n else []
-        t0 = time.perf_counter()
-        O.attention_rows(q_rot, rows, K_ctx, V_ctx, 1.0 / np.sqrt(wl.d), which=which)
-        t_att += time.perf_counter() - t0
-        s_pp1 += int((rows[which] + 1).sum())
-        total_pp1 += int((rows + 1).sum())
-    scale_reqs = len(wl.requests) / min(len(wl.requests), 2)
-    full = scale_reqs * (t_rot * total_rot_tokens / max(s_rot_tokens, 1) + t_att * total_pp1 / max(s_pp1, 1))
-    desc = (f"oracle as it stands on {n_chunks} of the re-rotated chunks and {n_rows} of the recomputed rows "
-            f"per request (first {min(len(wl.requests), 2)} request(s)); time extrapolated by re-rotated tokens "
-            f"and by sum(p+1) over rows to the full step")
-    threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return full, desc, threads
+    Set-up (untimed): draw the workload's inputs and build the spliced context of
+    up to two requests with the oracle.  A sample re-runs the oracle's re-rotation
+    on a few chunks and its attention on a few recomputed rows, and extrapolates to
+    the whole step by re-rotated tokens and by sum(p + 1) over rows."""
+
+    def __init__(self, wl):
+        import oracle.pic_oracle as O
+        from position_independent_kv_pic_gb300 import inputs
+        self.O, self.wl = O, wl
+        kst, vst, off = inputs.chunk_store(wl)
+        self.reqs = []
+        self.n_used = min(len(wl.requests), 2)
+        for req in wl.requests[:self.n_used]:
+            ck = [kst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
+            cv = [vst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
+            n = O.count_rows(wl.chunk_lens[req.chunk_ids], req.q, req.k)
+            qr, kn, vn = (t.double().numpy() for t in inputs.row_inputs(wl, n))
+            K, V, rows, starts, T = O.splice_context(ck, cv, req.q, req.k, kn, vn, wl.theta, wl.dtype)
+            q_rot = O.round_to(O.rope(qr, rows, wl.theta), wl.dtype)
+            self.reqs.append(dict(ck=ck, K=K, V=V, rows=rows, starts=starts, q_rot=q_rot,
+                                  rot_tokens=sum(len(c) for c in ck[1:])))
+        self.threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+    def sample(self, n_chunks, n_rows, seed=0):
+        """Seconds the oracle would need for the whole step, from one bounded sample."""
+        O, wl = self.O, self.wl
+        rng = np.random.default_rng(seed)
+        full = 0.0
+        for r in self.reqs:
+            ck, rows = r["ck"], r["rows"]
+            cs = rng.choice(np.arange(1, len(ck)), size=min(n_chunks, len(ck) - 1), replace=False) \
+                if len(ck) > 1 else []
+            t0 = time.perf_counter()
+            for c in cs:
+                O.rerotate_k(ck[c], int(r["starts"][c]), wl.theta, wl.dtype)
+            t_rot = time.perf_counter() - t0
+            s_tok = sum(len(ck[c]) for c in cs)
+            n = len(rows)
+            which = sorted(rng.choice(n, size=min(n_rows, n), replace=False).tolist()) if n else []
+            t0 = time.perf_counter()
+            O.attention_rows(r["q_rot"], rows, r["K"], r["V"], 1.0 / np.sqrt(wl.d), which=which)
+            t_att = time.perf_counter() - t0
+            full += t_rot * r["rot_tokens"] / max(s_tok, 1) + t_att * n / max(len(which), 1)
+        return full * len(wl.requests) / self.n_used
+
+    def describe(self, n_chunks, n_rows):
+        return (f"float64 oracle as it stands: re-rotation of {n_chunks} random chunks and attention of {n_rows} "
+                f"uniformly drawn recomputed rows per request (first {self.n_used} request(s)), extrapolated to "
+                f"the full step by re-rotated tokens and by row count; spliced context built once, untimed")
 
 
 def run_reference(args):
     wl = _workload(args.workload)
     tokens = wl.total_tokens()
-    for _ in range(args.warmup):
-        oracle_sample_time(wl, n_chunks=2, n_rows=1)
-    times = []
-    for i in range(args.steps):
-        full, desc, threads = oracle_sample_time(wl, seed=i)
-        times.append(full)
+    sampler = OracleSampler(wl)
+    for i in range(args.warmup):
+        sampler.sample(1, 1, seed=1000 + i)
+    times = [sampler.sample(1, 1, seed=i) for i in range(args.steps)]
     step_s = statistics.mean(times)
     value = tokens / step_s
     return {
@@ -314,7 +338,8 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
         "config": {"workload": wl.name, "tokens": tokens},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle", "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": sampler.threads, "kind": "oracle",
+                         "sample": sampler.describe(1, 1) + f"; mean over {args.steps} samples"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -345,9 +370,10 @@ def main():
     result, batch = run_gpu(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
-            full, desc, threads = oracle_sample_time(batch.wl)
-            result["cpu_baseline"] = {"value": batch.tokens / full, "unit": UNIT, "cores": threads,
-                                      "kind": "oracle", "sample": desc}
+            sampler = OracleSampler(batch.wl)
+            full = statistics.mean(sampler.sample(8, 8, seed=i) for i in range(3))
+            result["cpu_baseline"] = {"value": batch.tokens / full, "unit": UNIT, "cores": sampler.threads,
+                                      "kind": "oracle", "sample": sampler.describe(8, 8) + "; mean of 3 samples"}
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist
