@@ -23,7 +23,8 @@
  * Conventions shared by every entry point
  *   - Pointers are DEVICE pointers unless their name ends in _host.  The caller
  *     owns all memory and streams; the library allocates nothing and keeps no
- *     state between calls.
+ *     state between calls (one exception, pic_link_attention_noalloc, is
+ *     described where it is declared).
  *   - Every device entry point is asynchronous on `stream`.  Its return value
  *     reports only what the host can check synchronously: PIC_ERR_INVALID for a
  *     bad argument, PIC_ERR_UNSUPPORTED for a valid but unimplemented shape,
@@ -265,6 +266,44 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
                               const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
                               int32_t Hkv, int32_t d, float scale, void* out, void* ws,
                               size_t ws_bytes, int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * Link attention without a caller workspace.  (No counterpart in the
+ * papers: this is a packaging variant of pic_link_attention.)
+ * ------------------------------------------------------------------------
+ * Some callers cannot allocate device memory at the point where they run the
+ * link step: a serving engine that has already reserved nearly all of HBM for
+ * its KV pool (a cudaMalloc then fails, and it also synchronises the device,
+ * stalling every other stream), or a plugin that is handed device pointers by a
+ * host framework that owns all allocation.  For them this entry point computes
+ * exactly what pic_link_attention computes, same arguments minus ws/ws_bytes,
+ * with its planning and split-KV scratch in one fixed device array of
+ * PIC_NOALLOC_SCRATCH_BYTES inside the library.  It calls no cudaMalloc,
+ * cudaFree or allocating routine.
+ *   - The array exists on every GPU that loads the library and stays allocated
+ *     until the process exits.
+ *   - The first call on a device looks up the array's device address (with that
+ *     device current) and keeps it; make that first call before any stream
+ *     capture.
+ *   - Every call on a device uses the same array, which keeps the previous
+ *     call's contents (nothing in it needs to start at zero).  Calls whose work
+ *     overlaps on the GPU (different streams, or host threads without ordering)
+ *     race on the array: order them.
+ *   - The tensor-core path (bf16, d = 128) splits long key ranges into at most
+ *     128 extra work units; a call whose scratch would exceed the array (about
+ *     1,400 recomputed rows of one request at Hkv = 8, fewer with more requests)
+ *     is refused with PIC_ERR_WORKSPACE before any other check or launch.  The
+ *     SIMT path (fp32 pools, other shapes) needs no scratch.
+ * Results match pic_link_attention within the attention tolerance (the split
+ * of key ranges, and so the summation order, can differ). */
+#define PIC_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+pic_status pic_link_attention_noalloc(const void* q, const float* row_table, const int32_t* rows,
+                                      const int32_t* row_off, const void* k_pool, const void* v_pool,
+                                      int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                                      const int32_t* page_off, int32_t n_req, int64_t n_rows,
+                                      int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out,
+                                      int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Diagnostics.

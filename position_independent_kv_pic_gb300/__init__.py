@@ -22,13 +22,14 @@ __all__ = [
     "pic_count_rows", "pic_request_sizes_of", "pic_plan_offsets", "pic_strerror",
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
-    "pic_selftest_umma", "EXPORTED",
+    "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
 PIC_ERR_TIMEOUT, PIC_ERR_RANGE, PIC_ERR_WORKSPACE = 4, 5, 6
 PIC_BF16, PIC_FP32 = 0, 1
 PIC_PAGE = 16
+PIC_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # numpy views of the 16-byte structs of pic.h
 LINK_PAGE_DTYPE = np.dtype([("k_block", "<i4"), ("v_block", "<i4"), ("gpos0", "<i4"),
@@ -44,7 +45,7 @@ EXPORTED = (
     "pic_count_rows", "pic_request_sizes_of", "pic_plan_offsets", "pic_strerror",
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
-    "pic_selftest_umma",
+    "pic_selftest_umma", "pic_link_attention_noalloc",
 )
 
 
@@ -83,6 +84,8 @@ _SIGS = {
     "pic_link_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
                                           _I64, _I32, _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
     "pic_selftest_umma": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "pic_link_attention_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
+                                                  _I64, _I32, _I32, _I32, _F32, _P, _P, _P]),
 }
 
 
@@ -211,3 +214,14 @@ def pic_link_attention(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, 
 def pic_selftest_umma(a, b, d_kmajor, d_mnmajor, err_flag, stream=None):
     _check(load().pic_selftest_umma(_ptr(a), _ptr(b), _ptr(d_kmajor), _ptr(d_mnmajor), _ptr(err_flag),
                                     _stream(stream)), "pic_selftest_umma")
+
+
+def pic_link_attention_noalloc(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, pages, page_off,
+                               n_req: int, n_rows: int, Hq: int, Hkv: int, d: int, scale: float, out, err_flag,
+                               stream=None):
+    """pic_link_attention for callers that cannot allocate: the library's fixed device
+    scratch replaces the workspace (see pic.h for its size limit and sharing rules)."""
+    _check(load().pic_link_attention_noalloc(
+        _ptr(q), _ptr(row_table), _ptr(rows), _ptr(row_off), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype),
+        _ptr(pages), _ptr(page_off), int(n_req), int(n_rows), int(Hq), int(Hkv), int(d), float(scale), _ptr(out),
+        _ptr(err_flag), _stream(stream)), "pic_link_attention_noalloc")

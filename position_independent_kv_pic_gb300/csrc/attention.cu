@@ -19,6 +19,8 @@
 // (offset-causal tile skipping); rows inside the boundary tiles are masked per key.
 #include <cudaTypedefs.h>
 
+#include <mutex>
+
 #include "pic_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -998,3 +1000,126 @@ pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, floa
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------ fixed-scratch variant
+// pic_link_attention_noalloc: the tensor-core attention with its planning and
+// merge scratch in one statically sized device array instead of a caller
+// workspace.  It calls the same kernels as pic_link_attention; it gives the
+// planner a smaller split budget (4 extra units per SM for at most 32 SMs) so
+// that the scratch a call needs stays small.
+
+constexpr size_t kFixedScratchBytes = (size_t)PIC_NOALLOC_SCRATCH_BYTES;
+
+// Held by every GPU that loads this library, until the process exits.
+static __device__ __align__(256) uint8_t pic_fixed_scratch[kFixedScratchBytes];
+
+namespace pic {
+namespace {
+
+constexpr int kFixedSplitSms = 32;
+constexpr int kMaxDevices = 256;
+
+std::mutex g_fixed_mu;
+void* g_fixed_addr[kMaxDevices];  // device address of pic_fixed_scratch, per device ordinal
+
+// Device address of the scratch on the current device.  Looked up once per
+// device (cudaGetSymbolAddress with that device current); host code must never
+// hand the host-side name pic_fixed_scratch to a kernel.
+void* fixed_scratch_address() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lock(g_fixed_mu);
+  if (g_fixed_addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, pic_fixed_scratch) != cudaSuccess || p == nullptr) return nullptr;
+    g_fixed_addr[dev] = p;
+  }
+  return g_fixed_addr[dev];
+}
+
+WsLayout fixed_layout(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d) {
+  WsLayout L = ws_layout(n_rows, n_req, G, Hkv, d);
+  const int64_t units_cap = L.tiles_cap * Hkv + (int64_t)kUnitsPerSm * kFixedSplitSms;
+  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  L.units_cap = units_cap;
+  L.off_ml = al(L.off_units + units_cap * sizeof(Unit));
+  L.off_o = al(L.off_ml + (size_t)units_cap * kM * sizeof(float2));
+  L.total = al(L.off_o + (size_t)units_cap * kM * d * sizeof(float));
+  return L;
+}
+
+}  // namespace
+}  // namespace pic
+
+extern "C" pic_status pic_link_attention_noalloc(const void* q, const float* row_table, const int32_t* rows,
+                                                 const int32_t* row_off, const void* k_pool, const void* v_pool,
+                                                 int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                                                 const int32_t* page_off, int32_t n_req, int64_t n_rows,
+                                                 int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out,
+                                                 int32_t* err_flag, pic_stream_t stream) {
+  using namespace pic;
+  if (n_req < 0 || n_rows < 0 || num_blocks < 0 || Hkv < 1 || Hq < 1 || Hq % Hkv || d < 2 || d > 256 ||
+      (d & 1) || !(scale > 0.f))
+    return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (n_req == 0 || n_rows == 0) return PIC_OK;
+  const bool tc = tc_shape(dtype, Hq, Hkv, d);
+  const int G = Hq / Hkv;
+  // size check first: a call that needs more scratch than the array holds is refused before anything else
+  if (tc && fixed_layout(n_rows, n_req, G, Hkv, d).total > kFixedScratchBytes) return PIC_ERR_WORKSPACE;
+  if (!q || !row_table || !rows || !row_off || !k_pool || !v_pool || !pages || !page_off || !out || !err_flag)
+    return PIC_ERR_INVALID;
+  // the SIMT path uses no scratch at all
+  if (!tc)
+    return pic_link_attention(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
+                              n_req, n_rows, Hq, Hkv, d, scale, out, nullptr, 0, err_flag, stream);
+  const WsLayout L = fixed_layout(n_rows, n_req, G, Hkv, d);
+  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
+      (reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
+    return PIC_ERR_INVALID;
+  const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
+  if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
+  uint8_t* w = static_cast<uint8_t*>(fixed_scratch_address());
+  if (w == nullptr) return PIC_ERR_CUDA;
+  CUtensorMap kmap, vmap;
+  if (!encode_rows128(&kmap, k_pool, pool_rows) || !encode_rows128(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
+  cudaStream_t s = (cudaStream_t)stream;
+  // Nothing in the scratch has to start at zero: the planner rewrites the header,
+  // tile and unit lists on every call, and partials are written before they are read.
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  TileMeta* tiles = reinterpret_cast<TileMeta*>(w + L.off_tiles);
+  Unit* units = reinterpret_cast<Unit*>(w + L.off_units);
+  float2* part_ml = reinterpret_cast<float2*>(w + L.off_ml);
+  float* part_o = reinterpret_cast<float*>(w + L.off_o);
+  const int sms = num_sms_of_current_device();
+  const int split_sms = sms < kFixedSplitSms ? sms : kFixedSplitSms;
+  plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kM / G, Hkv, split_sms,
+                                                L.tiles_cap, L.units_cap, hdr, tiles, units, err_flag);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  if (cudaFuncSetAttribute(link_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return PIC_ERR_CUDA;
+  TcArgs a;
+  a.q = static_cast<const bf16*>(q);
+  a.row_table = reinterpret_cast<const float4*>(row_table);
+  a.rows = rows;
+  a.pages = pages;
+  a.out = static_cast<bf16*>(out);
+  a.hdr = hdr;
+  a.tiles = tiles;
+  a.units = units;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  a.err = err_flag;
+  a.num_blocks = num_blocks;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.R = kM / G;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
+  link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  merge_kernel<<<(unsigned)(L.tiles_cap * Hkv), 256, 0, s>>>(hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G, kM / G);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
