@@ -290,7 +290,7 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
  *     overlaps on the GPU (different streams, or host threads without ordering)
  *     race on the array: order them.
  *   - The tensor-core path (bf16, d = 128) splits long key ranges into at most
- *     128 extra work units; a call whose scratch would exceed the array (about
+ *     64 extra work units; a call whose scratch would exceed the array (about
  *     1,400 recomputed rows of one request at Hkv = 8, fewer with more requests)
  *     is refused with PIC_ERR_WORKSPACE before any other check or launch.  The
  *     SIMT path (fp32 pools, other shapes) needs no scratch.
@@ -312,10 +312,11 @@ pic_status pic_link_attention_noalloc(const void* q, const float* row_table, con
  * layouts, descriptors and TMEM read-back the attention kernel uses:
  *   d_kmajor[m][n] = sum_k a[m][k] * b[n][k]    (B K-major, as Q.K^T)
  *   d_mnmajor[m][n] = sum_k a[m][k] * b[k][n]   (B MN-major, as P.V)
+ *   d_tmem_a[m][n]  = sum_k a[m][k] * b[k][n]   (A read from TMEM, as P.V)
  * a, b: [128][128] bf16 row-major (device); outputs [128][128] fp32 (device).
  * One launch of one thread block.  Not part of the link step. */
 pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, float* d_mnmajor,
-                             int32_t* err_flag, pic_stream_t stream);
+                             float* d_tmem_a, int32_t* err_flag, pic_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -83,7 +83,7 @@ _SIGS = {
     "pic_link_attention_workspace": (_SZ, [_I64, _I32, _I32, _I32, _I32, ctypes.c_int]),
     "pic_link_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
                                           _I64, _I32, _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
-    "pic_selftest_umma": (ctypes.c_int, [_P, _P, _P, _P, _P, _P]),
+    "pic_selftest_umma": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "pic_link_attention_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
                                                   _I64, _I32, _I32, _I32, _F32, _P, _P, _P]),
 }
@@ -211,9 +211,9 @@ def pic_link_attention(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, 
         _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)), "pic_link_attention")
 
 
-def pic_selftest_umma(a, b, d_kmajor, d_mnmajor, err_flag, stream=None):
-    _check(load().pic_selftest_umma(_ptr(a), _ptr(b), _ptr(d_kmajor), _ptr(d_mnmajor), _ptr(err_flag),
-                                    _stream(stream)), "pic_selftest_umma")
+def pic_selftest_umma(a, b, d_kmajor, d_mnmajor, d_tmem_a, err_flag, stream=None):
+    _check(load().pic_selftest_umma(_ptr(a), _ptr(b), _ptr(d_kmajor), _ptr(d_mnmajor), _ptr(d_tmem_a),
+                                    _ptr(err_flag), _stream(stream)), "pic_selftest_umma")
 
 
 def pic_link_attention_noalloc(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, pages, page_off,

@@ -1,22 +1,28 @@
-// Recompute-row link attention (EPIC blog review, link_legolink Step 3: the
-// recomputed rows' Q, roped at their global positions, attend over the whole
-// spliced K/V under the causal mask key_pos <= query_pos of the KV-cache blog's
-// mask section; scale 1/sqrt(d); GQA group g = Hq/Hkv shares one KV head).
+// Recompute-row link attention on the tensor cores (EPIC blog review,
+// link_legolink Step 3: the recomputed rows' Q, roped at their global positions,
+// attend over the whole spliced K/V under the causal mask key_pos <= query_pos
+// of the KV-cache blog's mask section; scale 1/sqrt(d); a GQA group of
+// g = Hq/Hkv query heads shares one KV head).
 //
-// Tensor-core path (bf16, d = 128): one MMA tile is M = 128 rows = g query heads
-// x (128/g) recomputed rows that share KV head `kvh`.  Per 128-key tile (8 pages
-// of 16 keys):  S = Q K^T (tcgen05, fp32 in TMEM) -> online softmax in registers
-// (one thread per row, base-2, lazy rescale) -> P (bf16) in shared memory ->
-// O += P V (tcgen05, fp32 in TMEM).  K/V pages arrive by TMA straight from the
-// paged pool.  Warp roles: warp 0 issues TMA, warp 1 issues MMAs and owns TMEM,
-// warps 4-7 run the softmax / correction / epilogue for TMEM lanes 0-127.
+// bf16, d = 128.  One MMA tile is M = 128 rows = g query heads x (128/g)
+// recomputed rows of one KV head.  A CTA works on a pair of such Q tiles and
+// streams the key tiles (128 keys = 8 pages of 16) of one unit through a ring
+// of four 32 KB shared-memory slots (K and V tiles alternate), filled by TMA
+// straight from the paged pool.  Per key tile and Q tile i:
+//   S_i = Q_i K^T   (tcgen05, fp32 accumulators in TMEM)
+//   softmax warpgroup i: S_i -> registers (one thread per row), online softmax
+//     in base 2 with lazy rescaling, P_i (bf16) written back over S_i in TMEM
+//   O_i += P_i V    (tcgen05 with A from TMEM)
+// While warpgroup 0 turns S_0 into P_0 the tensor core computes S_1 / P_1 V,
+// and the other way round.  Warp 0 issues TMA, warp 1 issues MMAs and owns TMEM,
+// warps 4-7 and 8-11 are the two softmax warpgroups.
 //
-// Work is cut into units (tile, kvh, key-tile span).  Tiles whose key range is
-// longer than the span are split; their partial (O, m, l) are merged by the LSE
-// merge kernel.  Units are ordered longest first (the LPT greedy rule HYPIC uses
-// for balancing segment work) and dealt round-robin to a persistent grid of one
-// CTA per SM.  Key tiles beyond a tile's last row position are skipped
-// (offset-causal tile skipping); rows inside the boundary tiles are masked per key.
+// Work is cut into units (Q-tile pair, KV head, span of key tiles).  Pairs whose
+// key range is longer than the span are split; their partial (O, m, l) are merged
+// by the LSE merge kernel.  Units are ordered longest first (the LPT greedy rule
+// HYPIC uses to balance segment work) and dealt round-robin to one CTA per SM.
+// Key tiles past a pair's last row position are never visited (offset-causal
+// tile skipping); keys inside boundary tiles are masked per row.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -31,31 +37,39 @@ using bf16 = __nv_bfloat16;
 
 constexpr int kD = 128;                 // head dim of the tensor-core path
 constexpr int kM = 128;                 // rows of one MMA tile
+constexpr int kQTiles = 2;              // MMA tiles per CTA
 constexpr int kKeys = 128;              // keys per key tile
 constexpr int kPagesPerKt = kKeys / PIC_PAGE;
-constexpr int kStages = 2;
-constexpr int kThreads = 256;
+constexpr int kSlots = 4;               // K/V ring slots (32 KB each)
+constexpr int kThreads = 384;
 constexpr int kMinSpan = 8;             // key tiles per unit, lower bound
 constexpr int kUnitsPerSm = 4;          // target units per SM when splitting
-constexpr int kMaxSplitUnits = 1024;    // bound on the units splitting may add
+constexpr int kMaxSplitUnits = 640;     // bound on the units splitting may add
+constexpr int kMaxPlanReqs = 2048;      // requests one planning block handles
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow up to 2^8 before O is rescaled
 
-constexpr int kHalfBytes = kM * 128;    // one 64-column half of a 128-row operand (16 KB)
+constexpr int kHalfBytes = kM * 128;      // one 64-column half of a 128-row operand (16 KB)
 constexpr int kOpBytes = 2 * kHalfBytes;  // 128 x 128 bf16 operand (32 KB)
-constexpr int kOffQ = 0;
-constexpr int kOffP = kOffQ + kOpBytes;
-constexpr int kOffK = kOffP + kOpBytes;
-constexpr int kOffV = kOffK + kStages * kOpBytes;
-constexpr int kOffBar = kOffV + kStages * kOpBytes;
-constexpr int kSmemBytes = kOffBar + 256 + 1024;  // + barriers + alignment slack
-constexpr uint32_t kTmemCols = 512;                // S0 | S1 | O | (unused)
+constexpr int kOffQ = 0;                  // Q tiles 0 and 1
+constexpr int kOffSlot = kQTiles * kOpBytes;
+constexpr int kOffBar = kOffSlot + kSlots * kOpBytes;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
+constexpr uint32_t kTmemCols = 512;                // S0 | S1 | O0 | O1
+constexpr uint32_t kTmemO = 256;
+// Register split: the block launches with 384 x 168 registers; warpgroup 0
+// (TMA, MMA, two idle warps) gives 64 per thread back, the two softmax
+// warpgroups take 32 more each:  4*32*(168-104) == 8*32*(200-168).
+constexpr int kLaunchRegs = 168;
+constexpr uint32_t kRegsLow = 104, kRegsHigh = 200;
+static_assert(4 * 32 * (kLaunchRegs - (int)kRegsLow) == 8 * 32 * ((int)kRegsHigh - kLaunchRegs), "register split");
+static_assert(kThreads * kLaunchRegs <= 65536, "register file");
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kM, kKeys, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16_f32(kM, kD, true);
 
 struct TileMeta {
-  int32_t row0, n_rows, page_begin, n_pages;  // rows [row0, row0+n_rows); pages needed (causal)
+  int32_t row0, n_rows, page_begin, n_pages;  // rows [row0, row0+n_rows) (<= 2R); pages needed (causal)
   int32_t n_kt, n_spans, part_base, req;      // key tiles; spans per head; partial slots (-1: none)
 };
 struct Unit {
@@ -72,79 +86,101 @@ struct WsLayout {
   size_t off_tiles, off_units, off_ml, off_o, total;
 };
 
-WsLayout ws_layout(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d) {
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace for up to `extra_units` units beyond one per (Q-tile pair, KV head).
+WsLayout ws_layout_with(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d, int64_t extra_units) {
   WsLayout L;
-  const int R = kM / G;
-  L.tiles_cap = n_rows / R + n_req + 1;
-  L.units_cap = L.tiles_cap * Hkv + kMaxSplitUnits;
-  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
+  const int R2 = kQTiles * (kM / G);
+  L.tiles_cap = n_rows / R2 + n_req + 1;
+  L.units_cap = L.tiles_cap * Hkv + extra_units;
   L.off_tiles = sizeof(WsHeader);
-  L.off_units = al(L.off_tiles + L.tiles_cap * sizeof(TileMeta));
-  L.off_ml = al(L.off_units + L.units_cap * sizeof(Unit));
-  L.off_o = al(L.off_ml + (size_t)L.units_cap * kM * sizeof(float2));
-  L.total = al(L.off_o + (size_t)L.units_cap * kM * d * sizeof(float));
+  L.off_units = al256(L.off_tiles + L.tiles_cap * sizeof(TileMeta));
+  L.off_ml = al256(L.off_units + L.units_cap * sizeof(Unit));
+  L.off_o = al256(L.off_ml + (size_t)L.units_cap * kQTiles * kM * sizeof(float2));
+  L.total = al256(L.off_o + (size_t)L.units_cap * kQTiles * kM * d * sizeof(float));
   return L;
 }
 
-__device__ __forceinline__ bool page_ok(const pic_link_page& p, int64_t num_blocks) {
-  return p.k_block >= 0 && p.k_block < num_blocks && p.v_block >= 0 && p.v_block < num_blocks &&
-         p.lo >= 0 && p.hi <= PIC_PAGE && p.lo < p.hi;
+WsLayout ws_layout(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d) {
+  return ws_layout_with(n_rows, n_req, G, Hkv, d, kMaxSplitUnits);
+}
+
+__device__ __forceinline__ bool page_ok(int4 p, int64_t num_blocks) {
+  const int lo = (int16_t)(p.w & 0xffff), hi = (int16_t)(p.w >> 16);
+  return p.x >= 0 && p.x < num_blocks && p.y >= 0 && p.y < num_blocks && lo >= 0 && hi <= PIC_PAGE && lo < hi;
 }
 
 // ------------------------------------------------------------------ planning
-// One block.  Builds tile metadata (causal page count per tile), picks the span,
-// and lists the units: full-length spans first, ordered (request, kvh, span,
-// tile) so that concurrently running units read the same key range, then the
-// shorter tail spans by decreasing length.
+// One block.  (1) Q-tile pairs per request and their causal page counts (pages
+// are sorted by first valid position: binary search for the last row's
+// position).  (2) The span: enough key tiles per unit that at most
+// min(kUnitsPerSm * SMs, kMaxSplitUnits) extra units appear.  (3) Units: the
+// full-length spans first, ordered (request, KV head, span index, tile) so that
+// concurrently running units read the same key range, then the shorter tail
+// spans by decreasing length.
 constexpr int kPlanThreads = 1024;
-constexpr int kHist = 4096;
+constexpr int kHist = 2048;
 
 __global__ void __launch_bounds__(kPlanThreads)
 plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ row_off,
                   const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off,
-                  int n_req, int R, int Hkv, int num_sms, int64_t tiles_cap, int64_t units_cap,
+                  int n_req, int R2, int Hkv, int num_sms, int64_t tiles_cap, int64_t units_cap,
                   WsHeader* hdr, TileMeta* tiles, Unit* units, int32_t* err) {
-  __shared__ int s_total_kt, s_ntiles, s_part, s_hist[kHist];
-  if (threadIdx.x == 0) {
-    int acc = 0;
-    for (int r = 0; r < n_req; ++r) acc += ceil_div(row_off[r + 1] - row_off[r], R);
-    s_ntiles = acc;
+  __shared__ int s_toff[kMaxPlanReqs + 1];   // first tile of each request
+  __shared__ int s_full[kMaxPlanReqs];       // full spans of one head of each request
+  __shared__ int s_fbase[kMaxPlanReqs + 1];  // first full unit of each request
+  __shared__ int s_hist[kHist];
+  __shared__ int s_scan[kPlanThreads / 32 + 1];
+  __shared__ int s_total_kt, s_part;
+  const int tid = threadIdx.x;
+  // (1) tile offsets over requests
+  int carry = 0;
+  for (int g = 0; g < n_req; g += kPlanThreads) {
+    const int r = g + tid;
+    const int nt = (r < n_req) ? ceil_div(row_off[r + 1] - row_off[r], R2) : 0;
+    int tot;
+    const int ex = block_exclusive_scan<kPlanThreads>(nt, s_scan, &tot);
+    if (r < n_req) s_toff[r] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) {
+    s_toff[n_req] = carry;
     s_total_kt = 0;
     s_part = 0;
   }
+  for (int r = tid; r < n_req; r += kPlanThreads) s_full[r] = 0;
+  for (int i = tid; i < kHist; i += kPlanThreads) s_hist[i] = 0;
   __syncthreads();
-  const int n_tiles = s_ntiles;
+  const int n_tiles = s_toff[n_req];
   if (n_tiles > tiles_cap) {
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
       set_err(err, PIC_ERR_RANGE);
       hdr->n_units = 0;
       hdr->n_tiles = 0;
     }
     return;
   }
-  // tile metadata; request of a tile found by walking the per-request tile counts
-  for (int t = threadIdx.x; t < n_tiles; t += kPlanThreads) {
-    int r = 0, base = 0;
-    for (;; ++r) {
-      const int nt = ceil_div(row_off[r + 1] - row_off[r], R);
-      if (t < base + nt) break;
-      base += nt;
+  for (int t = tid; t < n_tiles; t += kPlanThreads) {
+    int lo = 0, hi = n_req;  // request: last r with s_toff[r] <= t
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_toff[mid] <= t) lo = mid; else hi = mid;
     }
-    const int lt = t - base;
+    const int r = lo;
     TileMeta tm;
     tm.req = r;
-    tm.row0 = row_off[r] + lt * R;
-    tm.n_rows = min(R, row_off[r + 1] - tm.row0);
+    tm.row0 = row_off[r] + (t - s_toff[r]) * R2;
+    tm.n_rows = min(R2, row_off[r + 1] - tm.row0);
     const int maxpos = rows[tm.row0 + tm.n_rows - 1];
-    // pages are sorted by first valid position: count those starting at or before maxpos
-    int lo = page_off[r], hi = page_off[r + 1];
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
+    int a = page_off[r], b = page_off[r + 1];
+    while (a < b) {
+      const int mid = (a + b) >> 1;
       const pic_link_page p = pages[mid];
-      if (p.gpos0 + p.lo <= maxpos) lo = mid + 1; else hi = mid;
+      if (p.gpos0 + p.lo <= maxpos) a = mid + 1; else b = mid;
     }
     tm.page_begin = page_off[r];
-    tm.n_pages = lo - page_off[r];
+    tm.n_pages = a - page_off[r];
     tm.n_kt = ceil_div(tm.n_pages, kPagesPerKt);
     tm.n_spans = 0;
     tm.part_base = -1;
@@ -152,77 +188,80 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     atomicAdd(&s_total_kt, tm.n_kt);
   }
   __syncthreads();
+  // (2) span
   const int64_t work = (int64_t)s_total_kt * Hkv;
   const int64_t target = min((int64_t)kUnitsPerSm * num_sms, (int64_t)kMaxSplitUnits);
   const int span = (int)max((int64_t)kMinSpan, (work + target - 1) / target);
-  for (int t = threadIdx.x; t < n_tiles; t += kPlanThreads) {
+  for (int t = tid; t < n_tiles; t += kPlanThreads) {
     TileMeta& tm = tiles[t];
     tm.n_spans = ceil_div(tm.n_kt, span);
     if (tm.n_spans > 1) tm.part_base = atomicAdd(&s_part, tm.n_spans * Hkv);
+    atomicAdd(&s_full[tm.req], tm.n_kt / span);
+    const int len = tm.n_kt % span;
+    if (len > 0) atomicAdd(&s_hist[min(len, kHist - 1)], Hkv);
   }
-  for (int i = threadIdx.x; i < kHist; i += kPlanThreads) s_hist[i] = 0;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    // full spans, (request, head, span, tile) order
-    int64_t u = 0;
-    int tile_base = 0;
-    for (int r = 0; r < n_req; ++r) {
-      const int nt = ceil_div(row_off[r + 1] - row_off[r], R);
-      for (int h = 0; h < Hkv; ++h) {
-        for (int s = 0;; ++s) {
-          bool any = false;
-          for (int lt = 0; lt < nt; ++lt) {
-            const TileMeta tm = tiles[tile_base + lt];
-            if (tm.n_kt / span > s) {
-              any = true;
-              if (u < units_cap) {
-                Unit un;
-                un.tile = tile_base + lt; un.head = h; un.kt0 = s * span; un.kt1 = (s + 1) * span;
-                un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + s : -1;
-                un.pad0 = un.pad1 = un.pad2 = 0;
-                units[u] = un;
-              }
-              ++u;
-            }
-          }
-          if (!any) break;
-        }
-      }
-      tile_base += nt;
-    }
-    // tail spans by decreasing length (counting sort on the length)
-    for (int t = 0; t < n_tiles; ++t) {
-      const int len = tiles[t].n_kt % span;
-      if (len > 0) s_hist[min(len, kHist - 1)] += Hkv;
-    }
-    int64_t pos = u;
+  // (3) first full unit of every request; tail buckets after all full units, longest first
+  carry = 0;
+  for (int g = 0; g < n_req; g += kPlanThreads) {
+    const int r = g + tid;
+    const int f = (r < n_req) ? s_full[r] * Hkv : 0;
+    int tot;
+    const int ex = block_exclusive_scan<kPlanThreads>(f, s_scan, &tot);
+    if (r < n_req) s_fbase[r] = carry + ex;
+    carry += tot;
+  }
+  const int n_full = carry;
+  if (tid == 0) {
+    int pos = n_full;
     for (int len = kHist - 1; len >= 1; --len) {
       const int c = s_hist[len];
-      s_hist[len] = (int)pos;
+      s_hist[len] = pos;
       pos += c;
     }
-    for (int t = 0; t < n_tiles; ++t) {
-      const TileMeta tm = tiles[t];
-      const int len = tm.n_kt % span;
-      if (len == 0) continue;
-      const int s = tm.n_kt / span;
-      for (int h = 0; h < Hkv; ++h) {
-        const int64_t idx = s_hist[min(len, kHist - 1)]++;
-        if (idx < units_cap) {
-          Unit un;
-          un.tile = t; un.head = h; un.kt0 = s * span; un.kt1 = tm.n_kt;
-          un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + s : -1;
-          un.pad0 = un.pad1 = un.pad2 = 0;
-          units[idx] = un;
-        }
-      }
-    }
-    if (pos > units_cap) {
+    s_fbase[n_req] = pos;  // total units
+  }
+  __syncthreads();
+  const int n_units = s_fbase[n_req];
+  if (n_units > units_cap) {
+    if (tid == 0) {
       set_err(err, PIC_ERR_RANGE);
-      pos = units_cap;
+      hdr->n_units = 0;
+      hdr->n_tiles = 0;
     }
+    return;
+  }
+  // full units: index within (request, head) ordered by (span s, tile t)
+  for (int th = tid; th < n_tiles * Hkv; th += kPlanThreads) {
+    const int t = th / Hkv, h = th % Hkv;
+    const TileMeta tm = tiles[t];
+    const int r = tm.req, t0 = s_toff[r], t1 = s_toff[r + 1];
+    const int f = tm.n_kt / span;
+    for (int s = 0; s < f; ++s) {
+      int idx = s_fbase[r] + h * s_full[r];
+      for (int t2 = t0; t2 < t1; ++t2) {
+        const int f2 = tiles[t2].n_kt / span;
+        idx += min(f2, s) + ((t2 < t && f2 > s) ? 1 : 0);
+      }
+      Unit un;
+      un.tile = t; un.head = h; un.kt0 = s * span; un.kt1 = (s + 1) * span;
+      un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + s : -1;
+      un.pad0 = un.pad1 = un.pad2 = 0;
+      units[idx] = un;
+    }
+    const int len = tm.n_kt % span;
+    if (len > 0) {
+      const int idx = atomicAdd(&s_hist[min(len, kHist - 1)], 1);
+      Unit un;
+      un.tile = t; un.head = h; un.kt0 = f * span; un.kt1 = tm.n_kt;
+      un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + f : -1;
+      un.pad0 = un.pad1 = un.pad2 = 0;
+      units[idx] = un;
+    }
+  }
+  if (tid == 0) {
     hdr->n_tiles = n_tiles;
-    hdr->n_units = (int)pos;
+    hdr->n_units = n_units;
     hdr->span = span;
     hdr->total_kt = s_total_kt;
   }
@@ -247,8 +286,8 @@ struct TcArgs {
 };
 
 struct Bars {
-  uint64_t kfull[kStages], vfull[kStages], kvempty[kStages];
-  uint64_t sfull[2], sfree[2], pfull, odone, qfull, drain;
+  uint64_t kv_full[kSlots], kv_empty[kSlots];
+  uint64_t q_full[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -269,18 +308,19 @@ __device__ __forceinline__ void fail(Bars* b, int32_t* err) {
   *reinterpret_cast<volatile int*>(&b->abort) = 1;
 }
 
+__device__ __forceinline__ bool wait_bar(Bars* b, uint64_t* bar, uint32_t parity) {
+  return tc::mbar_wait(bar, parity, &b->abort, kWaitLimitNs);
+}
+
+// ---------------------------------------------------------------- producer
 __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               uint8_t* smem, Bars* b, int n_units) {
-  const volatile int* ab = &b->abort;
-  uint32_t it = 0;
+  uint32_t ld = 0;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int page_end = tm.page_begin + tm.n_pages;
-    for (int kt = un.kt0; kt < un.kt1; ++kt, ++it) {
-      const int st = it % kStages;
-      const uint32_t ph = (it / kStages) & 1;
-      if (!tc::mbar_wait(&b->kvempty[st], ph ^ 1, ab, kWaitLimitNs)) { fail(b, a.err); return; }
+    for (int kt = un.kt0; kt < un.kt1; ++kt) {
       int kb[kPagesPerKt], vb[kPagesPerKt];
       uint32_t bytes = 0;
 #pragma unroll
@@ -289,92 +329,109 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
         vb[j] = -1;
         const int p = tm.page_begin + kt * kPagesPerKt + j;
         if (p < page_end) {
-          const pic_link_page pg = a.pages[p];
+          const int4 pg = __ldg(reinterpret_cast<const int4*>(a.pages) + p);
           if (page_ok(pg, a.num_blocks)) {
-            kb[j] = pg.k_block;
-            vb[j] = pg.v_block;
+            kb[j] = pg.x;
+            vb[j] = pg.y;
             bytes += 2 * PIC_PAGE * 64 * sizeof(bf16);  // two boxes of 16 rows x 64 columns
-          } else if (pg.lo < pg.hi) {
+          } else if ((int16_t)(pg.w & 0xffff) < (int16_t)(pg.w >> 16)) {
             set_err(a.err, PIC_ERR_RANGE);
           }
         }
       }
-      uint8_t* ks = smem + kOffK + st * kOpBytes;
-      uint8_t* vs = smem + kOffV + st * kOpBytes;
-      tc::mbar_arrive_expect_tx(&b->kfull[st], bytes);
 #pragma unroll
-      for (int j = 0; j < kPagesPerKt; ++j) {
-        if (kb[j] < 0) continue;
-        const int y = (kb[j] * a.Hkv + un.head) * PIC_PAGE;
-        tc::tma_load_2d(ks + j * 2048, kmap, 0, y, &b->kfull[st]);
-        tc::tma_load_2d(ks + kHalfBytes + j * 2048, kmap, 64, y, &b->kfull[st]);
-      }
-      tc::mbar_arrive_expect_tx(&b->vfull[st], bytes);
+      for (int kv = 0; kv < 2; ++kv, ++ld) {
+        const int slot = ld % kSlots;
+        if (!wait_bar(b, &b->kv_empty[slot], ((ld / kSlots) & 1) ^ 1)) { fail(b, a.err); return; }
+        uint8_t* dst = smem + kOffSlot + slot * kOpBytes;
+        const CUtensorMap* map = kv ? vmap : kmap;
+        tc::mbar_arrive_expect_tx(&b->kv_full[slot], bytes);
 #pragma unroll
-      for (int j = 0; j < kPagesPerKt; ++j) {
-        if (vb[j] < 0) continue;
-        const int y = (vb[j] * a.Hkv + un.head) * PIC_PAGE;
-        tc::tma_load_2d(vs + j * 2048, vmap, 0, y, &b->vfull[st]);
-        tc::tma_load_2d(vs + kHalfBytes + j * 2048, vmap, 64, y, &b->vfull[st]);
+        for (int j = 0; j < kPagesPerKt; ++j) {
+          const int blk = kv ? vb[j] : kb[j];
+          if (blk < 0) continue;
+          const int y = (blk * a.Hkv + un.head) * PIC_PAGE;
+          tc::tma_load_2d(dst + j * 2048, map, 0, y, &b->kv_full[slot]);
+          tc::tma_load_2d(dst + kHalfBytes + j * 2048, map, 64, y, &b->kv_full[slot]);
+        }
       }
     }
   }
-  // every load issued has been consumed or is awaited below: wait for the last
-  // loads of each stage so that no copy is in flight when the block exits
-  for (uint32_t k = 0; k < kStages && k < it; ++k) {
-    const uint32_t t = it - 1 - k;
-    tc::mbar_wait(&b->kfull[t % kStages], (t / kStages) & 1, ab, kWaitLimitNs);
-    tc::mbar_wait(&b->vfull[t % kStages], (t / kStages) & 1, ab, kWaitLimitNs);
+  // no copy may be in flight when the block exits
+  for (uint32_t k = 0; k < kSlots && k < ld; ++k) {
+    const uint32_t t = ld - 1 - k;
+    wait_bar(b, &b->kv_full[t % kSlots], (t / kSlots) & 1);
   }
 }
 
+// ---------------------------------------------------------------- MMA issuer
 __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units) {
-  const volatile int* ab = &b->abort;
   const uint32_t sq = tc::smem_addr(smem + kOffQ);
-  const uint32_t sp = tc::smem_addr(smem + kOffP);
-  const uint32_t sk = tc::smem_addr(smem + kOffK);
-  const uint32_t sv = tc::smem_addr(smem + kOffV);
-  const uint32_t tmem_o = tmem + 256;
-  uint32_t it = 0, uc = 0;
-  auto issue_s = [&](uint32_t t) -> bool {
-    const int st = t % kStages;
-    const int sb = t & 1;
-    if (!tc::mbar_wait(&b->kfull[st], (t / kStages) & 1, ab, kWaitLimitNs)) return false;
-    if (!tc::mbar_wait(&b->sfree[sb], ((t >> 1) & 1) ^ 1, ab, kWaitLimitNs)) return false;
-    tc::tc_fence_after();
+  const uint32_t sslot = tc::smem_addr(smem + kOffSlot);
+  uint32_t ld = 0, uq[kQTiles] = {0, 0}, c[kQTiles] = {0, 0};
+  auto issue_s = [&](int i, int slot) {
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
       const uint32_t koff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-      const uint64_t da = tc::sw128_desc(sq + koff, 16, 1024);
-      const uint64_t db = tc::sw128_desc(sk + st * kOpBytes + koff, 16, 1024);
-      tc::mma_bf16_ss(tmem + sb * 128, da, db, kIdescS, ks > 0 ? 1u : 0u);
+      const uint64_t da = tc::sw128_desc(sq + i * kOpBytes + koff, 16, 1024);
+      const uint64_t db = tc::sw128_desc(sslot + slot * kOpBytes + koff, 16, 1024);
+      tc::mma_bf16_ss(tmem + i * 128, da, db, kIdescS, ks > 0 ? 1u : 0u);
     }
-    tc::mma_commit(&b->sfull[sb]);
-    return true;
   };
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++uc) {
-    const Unit un = a.units[u];
-    const int n = un.kt1 - un.kt0;
-    if (!tc::mbar_wait(&b->qfull, uc & 1, ab, kWaitLimitNs)) { fail(b, a.err); return; }
-    tc::tc_fence_after();
-    if (!issue_s(it)) { fail(b, a.err); return; }
-    for (int j = 0; j < n; ++j, ++it) {
-      if (j + 1 < n && !issue_s(it + 1)) { fail(b, a.err); return; }
-      const int st = it % kStages;
-      if (!tc::mbar_wait(&b->pfull, it & 1, ab, kWaitLimitNs) ||
-          !tc::mbar_wait(&b->vfull[st], (it / kStages) & 1, ab, kWaitLimitNs)) {
-        fail(b, a.err);
-        return;
-      }
-      tc::tc_fence_after();
+  auto issue_pv = [&](int i, int slot, bool acc) {
 #pragma unroll
-      for (int ks = 0; ks < kKeys / 16; ++ks) {
-        const uint64_t da = tc::sw128_desc(sp + (ks >> 2) * kHalfBytes + (ks & 3) * 32, 16, 1024);
-        const uint64_t db = tc::sw128_desc(sv + st * kOpBytes + ks * 2048, kHalfBytes, 1024);
-        tc::mma_bf16_ss(tmem_o, da, db, kIdescPV, (j > 0 || ks > 0) ? 1u : 0u);
+    for (int ks = 0; ks < kKeys / 16; ++ks) {
+      const uint64_t db = tc::sw128_desc(sslot + slot * kOpBytes + ks * 2048, kHalfBytes, 1024);
+      tc::mma_bf16_ts(tmem + kTmemO + i * 128, tmem + i * 128 + ks * 8, db, kIdescPV, (acc || ks > 0) ? 1u : 0u);
+    }
+  };
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const Unit un = a.units[u];
+    const TileMeta tm = a.tiles[un.tile];
+    const int n = un.kt1 - un.kt0;
+    const bool act1 = tm.n_rows > a.R;
+    if (!wait_bar(b, &b->q_full[0], uq[0] & 1)) { fail(b, a.err); return; }
+    ++uq[0];
+    if (act1) {
+      if (!wait_bar(b, &b->q_full[1], uq[1] & 1)) { fail(b, a.err); return; }
+      ++uq[1];
+    }
+    tc::tc_fence_after();
+    {  // S for the first key tile
+      const int ks = ld % kSlots;
+      if (!wait_bar(b, &b->kv_full[ks], (ld / kSlots) & 1)) { fail(b, a.err); return; }
+      tc::tc_fence_after();
+      issue_s(0, ks);
+      tc::mma_commit(&b->s_full[0]);
+      if (act1) {
+        issue_s(1, ks);
+        tc::mma_commit(&b->s_full[1]);
       }
-      tc::mma_commit(&b->kvempty[st]);
-      tc::mma_commit(&b->odone);
+      tc::mma_commit(&b->kv_empty[ks]);
+    }
+    for (int j = 0; j < n; ++j, ld += 2) {
+      const uint32_t vld = ld + 1, nld = ld + 2;
+      const int vs = vld % kSlots, ns = nld % kSlots;
+      const bool more = j + 1 < n;
+      if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1)) { fail(b, a.err); return; }
+#pragma unroll
+      for (int i = 0; i < kQTiles; ++i) {
+        if (i == 1 && !act1) break;
+        if (!wait_bar(b, &b->p_full[i], c[i] & 1)) { fail(b, a.err); return; }
+        ++c[i];
+        tc::tc_fence_after();
+        issue_pv(i, vs, j > 0);
+        if (more) {
+          if (i == 0 && !wait_bar(b, &b->kv_full[ns], (nld / kSlots) & 1)) { fail(b, a.err); return; }
+          tc::tc_fence_after();
+          issue_s(i, ns);
+          tc::mma_commit(&b->s_full[i]);
+        } else {
+          tc::mma_commit(&b->o_done[i]);
+        }
+      }
+      tc::mma_commit(&b->kv_empty[vs]);
+      if (more) tc::mma_commit(&b->kv_empty[ns]);
     }
   }
 }
@@ -394,11 +451,11 @@ __device__ __forceinline__ void write_q_row(uint8_t* qs, int m, bool ok, const b
       uint32_t* hi_w = reinterpret_cast<uint32_t*>(&hi4);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 a = __bfloat1622float2(l2[e]);
-        const float2 bb = __bfloat1622float2(h2[e]);
+        const float2 x = __bfloat1622float2(l2[e]);
+        const float2 y = __bfloat1622float2(h2[e]);
         float y0, z0, y1, z1;
-        rope_rotate(a.x, bb.x, __ldg(tab + 8 * cc + 2 * e), y0, z0);
-        rope_rotate(a.y, bb.y, __ldg(tab + 8 * cc + 2 * e + 1), y1, z1);
+        rope_rotate(x.x, y.x, __ldg(tab + 8 * cc + 2 * e), y0, z0);
+        rope_rotate(x.y, y.y, __ldg(tab + 8 * cc + 2 * e + 1), y1, z1);
         lo_w[e] = pack_bf16x2(y0, y1);
         hi_w[e] = pack_bf16x2(z0, z1);
       }
@@ -408,72 +465,87 @@ __device__ __forceinline__ void write_q_row(uint8_t* qs, int m, bool ok, const b
   }
 }
 
-__device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units) {
-  const volatile int* ab = &b->abort;
-  const int t = threadIdx.x - 128;  // 0..127 = TMEM lane = tile row m
-  const int m = t;
+__device__ __forceinline__ int4 load_page(const pic_link_page* pages, int p, int page_end) {
+  if (p < page_end) return __ldg(reinterpret_cast<const int4*>(pages) + p);
+  return make_int4(-1, -1, 0, 0);
+}
+
+// ---------------------------------------------------------------- softmax warpgroups
+__device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units, int qt) {
+  const int t = threadIdx.x - 128 * (1 + qt);  // 0..127 = TMEM lane = row of Q tile qt
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = (uint32_t)((t & ~31) << 16);
-  const int hg = m / a.R, i = m % a.R;
-  uint8_t* qs = smem + kOffQ;
-  uint8_t* ps = smem + kOffP;
-  uint32_t it = 0;
+  const uint32_t tS = tmem + qt * 128 + lane_base;  // S_qt, then P_qt in its first 64 columns
+  const uint32_t tO = tmem + kTmemO + qt * 128 + lane_base;
+  const int hg = t / a.R, i = t % a.R;
+  uint8_t* qs = smem + kOffQ + qt * kOpBytes;
+  uint32_t c = 0, ou = 0, gt = 0;  // tiles / units this warpgroup worked on; all tiles of the CTA
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int n = un.kt1 - un.kt0;
-    const bool row_ok = i < tm.n_rows;
-    const int row = tm.row0 + (row_ok ? i : 0);
-    const int p_row = a.rows[tm.row0 + (row_ok ? i : tm.n_rows - 1)];
+    const bool active = qt == 0 || tm.n_rows > a.R;
+    const int loc = qt * a.R + i;
+    const bool row_ok = loc < tm.n_rows;
+    const int row = tm.row0 + (row_ok ? loc : 0);
+    const int p_row = a.rows[tm.row0 + (row_ok ? loc : tm.n_rows - 1)];
     const int hq = un.head * a.G + hg;
-    write_q_row(qs, m, row_ok, a.q + ((int64_t)row * a.Hq + hq) * kD, a.row_table + (int64_t)row * (kD / 2));
+    if (!active) {  // no rows for this Q tile: no Q, no barrier traffic
+      gt += n;
+      continue;
+    }
+    write_q_row(qs, t, row_ok, a.q + ((int64_t)row * a.Hq + hq) * kD, a.row_table + (int64_t)row * (kD / 2));
     tc::fence_proxy_async_smem();
     __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&b->qfull);
-
+    if (lane == 0) tc::mbar_arrive(&b->q_full[qt]);
     float m_ref = -INFINITY, l = 0.f;
     const int page_end = tm.page_begin + tm.n_pages;
-    for (int j = 0; j < n; ++j, ++it) {
-      const int sb = it & 1;
-      const int st = it % kStages;
-      if (!tc::mbar_wait(&b->sfull[sb], (it >> 1) & 1, ab, kWaitLimitNs)) { fail(b, a.err); return; }
+    const int pbase = tm.page_begin + un.kt0 * kPagesPerKt;
+    int4 pe = load_page(a.pages, lane < kPagesPerKt ? pbase + lane : page_end, page_end);
+    for (int j = 0; j < n; ++j, ++c, ++gt) {
+      const int4 cur = pe;
+      if (j + 1 < n && lane < kPagesPerKt) pe = load_page(a.pages, pbase + (j + 1) * kPagesPerKt + lane, page_end);
+      const bool pvalid = lane < kPagesPerKt && page_ok(cur, a.num_blocks);
+      const int plo = pvalid ? (int16_t)(cur.w & 0xffff) : 0;
+      const int phi = pvalid ? (int16_t)(cur.w >> 16) : 0;
+      const bool pfull = plo == 0 && phi == PIC_PAGE;
+      const bool tile_full = __all_sync(0xffffffffu, lane >= kPagesPerKt || pfull);
+      const int tile_last = __reduce_max_sync(0xffffffffu, pvalid ? cur.z + phi - 1 : INT_MIN);
+
+      if (!wait_bar(b, &b->s_full[qt], c & 1)) { fail(b, a.err); return; }
       tc::tc_fence_after();
-      uint32_t sraw[kKeys];
+      uint32_t sr[kKeys];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tc::tmem_ld32(tmem + lane_base + sb * 128 + c * 32, sraw + c * 32);
+      for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(tS + q4 * 32, sr + q4 * 32);
       tc::tmem_ld_wait();
       float s[kKeys];
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) s[c] = u2f(sraw[c]);
-      tc::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&b->sfree[sb]);
+      for (int k = 0; k < kKeys; ++k) s[k] = u2f(sr[k]);
 
-      // key-tile pages: valid slots and positions
-      int g0[kPagesPerKt], plo[kPagesPerKt], phi[kPagesPerKt];
-      bool tile_full = true;
-      const int pbase = tm.page_begin + (un.kt0 + j) * kPagesPerKt;
+      // per-page validity (also needed to zero V rows below)
+      int g0[kPagesPerKt] = {0, 0, 0, 0, 0, 0, 0, 0}, lohi[kPagesPerKt] = {0, 0, 0, 0, 0, 0, 0, 0};
+      const bool need_mask = __any_sync(0xffffffffu, !(tile_full && tile_last <= p_row));
+      if (need_mask) {
+        const int packed = plo | (phi << 16);
 #pragma unroll
-      for (int jj = 0; jj < kPagesPerKt; ++jj) {
-        g0[jj] = 0; plo[jj] = 0; phi[jj] = 0;
-        if (pbase + jj < page_end) {
-          const pic_link_page pg = a.pages[pbase + jj];
-          if (page_ok(pg, a.num_blocks)) { g0[jj] = pg.gpos0; plo[jj] = pg.lo; phi[jj] = pg.hi; }
+        for (int jj = 0; jj < kPagesPerKt; ++jj) {
+          g0[jj] = __shfl_sync(0xffffffffu, cur.z, jj);
+          lohi[jj] = __shfl_sync(0xffffffffu, packed, jj);
         }
-        tile_full = tile_full && plo[jj] == 0 && phi[jj] == PIC_PAGE;
-      }
-      const bool row_needs_mask = !(tile_full && g0[kPagesPerKt - 1] + PIC_PAGE - 1 <= p_row);
-      if (__any_sync(0xffffffffu, row_needs_mask)) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          const int jj = c >> 4, sl = c & 15;
-          const bool ok = sl >= plo[jj] && sl < phi[jj] && g0[jj] + sl <= p_row;
-          s[c] = ok ? s[c] : -INFINITY;
+        for (int k = 0; k < kKeys; ++k) {
+          const int jj = k >> 4, sl = k & 15;
+          const bool ok = sl >= (lohi[jj] & 0xffff) && sl < (lohi[jj] >> 16) && g0[jj] + sl <= p_row;
+          s[k] = ok ? s[k] : -INFINITY;
         }
       }
-      float mx = -INFINITY;
+      float mx8[8];
 #pragma unroll
-      for (int c = 0; c < kKeys; ++c) mx = fmaxf(mx, s[c]);
+      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+#pragma unroll
+      for (int k = 8; k < kKeys; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float mt = mx * a.scale_log2;
       float alpha = 1.f;
       bool resc = false;
@@ -484,90 +556,89 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
         m_ref = mt;
       }
       const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-      uint32_t pk[kKeys / 2];
-      float rs = 0.f;
+      // P in two halves of 64 keys (32 packed columns each) over the first 64 columns of S
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kKeys / 2; ++c) {
-        const float p0 = tc::ex2(fmaf(s[2 * c], a.scale_log2, -mu));
-        const float p1 = tc::ex2(fmaf(s[2 * c + 1], a.scale_log2, -mu));
-        rs += p0 + p1;
-        pk[c] = pack_bf16x2(p0, p1);
+      for (int hh = 0; hh < 2; ++hh) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float p0 = tc::ex2(fmaf(s[64 * hh + 2 * k], a.scale_log2, -mu));
+          const float p1 = tc::ex2(fmaf(s[64 * hh + 2 * k + 1], a.scale_log2, -mu));
+          rs[k & 3] += p0 + p1;
+          pk[k] = pack_bf16x2(p0, p1);
+        }
+        tc::tmem_st32(tS + 32 * hh, pk);
       }
-      l += rs;
-      // the previous P.V must be done before P is overwritten or O is rescaled
-      if (j > 0 && !tc::mbar_wait(&b->odone, (it - 1) & 1, ab, kWaitLimitNs)) { fail(b, a.err); return; }
-      tc::tc_fence_after();
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      // O_qt is stable here (the commit behind s_full covers the previous P.V) and P.V
+      // for this tile is not issued before p_full: rescale O after P is stored
       if (__any_sync(0xffffffffu, resc)) {
         const float f = resc ? alpha : 1.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int q4 = 0; q4 < 4; ++q4) {
           uint32_t r[32];
-          tc::tmem_ld32(tmem + 256 + lane_base + c * 32, r);
+          tc::tmem_ld32(tO + q4 * 32, r);
           tc::tmem_ld_wait();
 #pragma unroll
           for (int x = 0; x < 32; ++x) r[x] = f2u(u2f(r[x]) * f);
-          tc::tmem_st32(tmem + 256 + lane_base + c * 32, r);
+          tc::tmem_st32(tO + q4 * 32, r);
         }
-        tc::tmem_st_wait();
       }
-#pragma unroll
-      for (int h = 0; h < 2; ++h)
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          const uint4 v = make_uint4(pk[h * 32 + cc * 4], pk[h * 32 + cc * 4 + 1], pk[h * 32 + cc * 4 + 2],
-                                     pk[h * 32 + cc * 4 + 3]);
-          *reinterpret_cast<uint4*>(ps + h * kHalfBytes + sw128_off(m, cc)) = v;
-        }
-      // V rows of slots that hold no valid key are zeroed (masked keys get
-      // weight 0, and 0 * V must stay 0 even if the slot holds stale bits)
-      if (!tile_full) {
-        if (!tc::mbar_wait(&b->vfull[st], (it / kStages) & 1, ab, kWaitLimitNs)) { fail(b, a.err); return; }
-        uint8_t* vs = smem + kOffV + st * kOpBytes;
+      tc::tmem_st_wait();
+      // V rows of slots that hold no valid key are zeroed (masked keys get weight
+      // 0, and 0 * V must stay 0 even if the slot holds stale bits)
+      if (qt == 0 && !tile_full) {
+        const uint32_t vld = 2 * gt + 1;
+        const int vs = vld % kSlots;
+        if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1)) { fail(b, a.err); return; }
+        uint8_t* vsm = smem + kOffSlot + vs * kOpBytes;
         for (int idx = t; idx < kPagesPerKt * PIC_PAGE * 2 * 8; idx += 128) {
           const int cc = idx & 7, h = (idx >> 3) & 1, sl = (idx >> 4) & 15, jj = idx >> 8;
-          int lo_j = 0, hi_j = 0;
+          int lh = 0;
 #pragma unroll
           for (int q = 0; q < kPagesPerKt; ++q)
-            if (q == jj) { lo_j = plo[q]; hi_j = phi[q]; }
-          if (sl < lo_j || sl >= hi_j)
-            *reinterpret_cast<uint4*>(vs + h * kHalfBytes + (jj * PIC_PAGE + sl) * 128 + cc * 16) =
+            if (q == jj) lh = lohi[q];
+          if (sl < (lh & 0xffff) || sl >= (lh >> 16))
+            *reinterpret_cast<uint4*>(vsm + h * kHalfBytes + (jj * PIC_PAGE + sl) * 128 + cc * 16) =
                 make_uint4(0, 0, 0, 0);
         }
+        tc::fence_proxy_async_smem();
       }
-      tc::fence_proxy_async_smem();
       tc::tc_fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&b->pfull);
+      if (lane == 0) tc::mbar_arrive(&b->p_full[qt]);
     }
     // epilogue: O / l
-    if (!tc::mbar_wait(&b->odone, (it - 1) & 1, ab, kWaitLimitNs)) { fail(b, a.err); return; }
+    if (!wait_bar(b, &b->o_done[qt], ou & 1)) { fail(b, a.err); return; }
+    ++ou;
     tc::tc_fence_after();
-    uint32_t oraw[kD];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) tc::tmem_ld32(tmem + 256 + lane_base + c * 32, oraw + c * 32);
-    tc::tmem_ld_wait();
-    float o[kD];
-#pragma unroll
-    for (int c = 0; c < kD; ++c) o[c] = u2f(oraw[c]);
-    tc::tc_fence_before();
-    if (row_ok) {
-      const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    const int64_t slot = ((int64_t)(un.part < 0 ? 0 : un.part) * kQTiles + qt) * kM + t;
+#pragma unroll 1
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t r[32];
+      tc::tmem_ld32(tO + q4 * 32, r);
+      tc::tmem_ld_wait();
+      if (!row_ok) continue;
       if (un.part < 0) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)row * a.Hq + hq) * kD);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)row * a.Hq + hq) * kD + q4 * 32);
 #pragma unroll
-        for (int c = 0; c < kD / 8; ++c)
-          dst[c] = make_uint4(pack_bf16x2(o[8 * c] * inv, o[8 * c + 1] * inv),
-                              pack_bf16x2(o[8 * c + 2] * inv, o[8 * c + 3] * inv),
-                              pack_bf16x2(o[8 * c + 4] * inv, o[8 * c + 5] * inv),
-                              pack_bf16x2(o[8 * c + 6] * inv, o[8 * c + 7] * inv));
+        for (int k = 0; k < 4; ++k)
+          dst[k] = make_uint4(pack_bf16x2(u2f(r[8 * k]) * inv, u2f(r[8 * k + 1]) * inv),
+                              pack_bf16x2(u2f(r[8 * k + 2]) * inv, u2f(r[8 * k + 3]) * inv),
+                              pack_bf16x2(u2f(r[8 * k + 4]) * inv, u2f(r[8 * k + 5]) * inv),
+                              pack_bf16x2(u2f(r[8 * k + 6]) * inv, u2f(r[8 * k + 7]) * inv));
       } else {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + ((int64_t)un.part * kM + m) * kD);
+        float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kD + q4 * 32);
 #pragma unroll
-        for (int c = 0; c < kD / 4; ++c)
-          dst[c] = make_float4(o[4 * c] * inv, o[4 * c + 1] * inv, o[4 * c + 2] * inv, o[4 * c + 3] * inv);
-        a.part_ml[(int64_t)un.part * kM + m] = make_float2(m_ref, l);
+        for (int k = 0; k < 8; ++k)
+          dst[k] = make_float4(u2f(r[4 * k]) * inv, u2f(r[4 * k + 1]) * inv, u2f(r[4 * k + 2]) * inv,
+                               u2f(r[4 * k + 3]) * inv);
       }
     }
+    tc::tc_fence_before();
+    if (row_ok && un.part >= 0) a.part_ml[slot] = make_float2(m_ref, l);
   }
 }
 
@@ -579,18 +650,16 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   Bars* b = reinterpret_cast<Bars*>(smem + kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      tc::mbar_init(&b->kfull[s], 1);
-      tc::mbar_init(&b->vfull[s], 1);
-      tc::mbar_init(&b->kvempty[s], 1);
+    for (int s = 0; s < kSlots; ++s) {
+      tc::mbar_init(&b->kv_full[s], 1);
+      tc::mbar_init(&b->kv_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      tc::mbar_init(&b->sfull[s], 1);
-      tc::mbar_init(&b->sfree[s], 4);
+    for (int i = 0; i < kQTiles; ++i) {
+      tc::mbar_init(&b->q_full[i], 4);
+      tc::mbar_init(&b->s_full[i], 1);
+      tc::mbar_init(&b->p_full[i], 4);
+      tc::mbar_init(&b->o_done[i], 1);
     }
-    tc::mbar_init(&b->pfull, 4);
-    tc::mbar_init(&b->odone, 1);
-    tc::mbar_init(&b->qfull, 4);
     tc::mbar_init(&b->drain, 1);
     b->abort = 0;
     tc::fence_mbar_init();
@@ -608,19 +677,20 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   tc::tc_fence_after();
   const uint32_t tmem = b->tmem_base;
   const int n_units = a.hdr->n_units;
-
-  if (warp == 0) {
-    if (lane == 0) producer_loop(a, &kmap, &vmap, smem, b, n_units);
-  } else if (warp == 1) {
-    if (lane == 0) {
+  if (warp < 4) {
+    tc::regs_dec<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      producer_loop(a, &kmap, &vmap, smem, b, n_units);
+    } else if (warp == 1 && lane == 0) {
       mma_loop(a, smem, b, tmem, n_units);
       // every MMA this thread issued completes before TMEM is released (also on abort)
       tc::mma_commit(&b->drain);
       const int no_abort = 0;
       tc::mbar_wait(&b->drain, 0, &no_abort, kWaitLimitNs);
     }
-  } else if (warp >= 4) {
-    softmax_loop(a, smem, b, tmem, n_units);
+  } else {
+    tc::regs_inc<kRegsHigh>();
+    softmax_loop(a, smem, b, tmem, n_units, (warp - 4) / 4);
   }
   tc::tc_fence_before();
   __syncthreads();
@@ -631,8 +701,8 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 }
 
 // ------------------------------------------------------------------ LSE merge
-// One block per (tile, kvh); threads = rows x 16-dim chunks.  Combines the
-// per-span partials (O_s normalised by l_s, base-2 max m_s, l_s):
+// One block per (Q-tile pair, KV head) with split spans; threads = rows x 16-dim
+// chunks.  Combines the per-span partials (O_s normalised by l_s, base-2 max m_s):
 //   O = sum_s 2^(m_s - M) l_s O_s / sum_s 2^(m_s - M) l_s.
 __global__ void __launch_bounds__(256)
 merge_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tiles,
@@ -643,25 +713,28 @@ merge_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
   if (tile >= hdr->n_tiles) return;
   const TileMeta tm = tiles[tile];
   if (tm.n_spans <= 1) return;
-  for (int idx = threadIdx.x; idx < kM * (kD / 16); idx += blockDim.x) {
-    const int m = idx / (kD / 16), c = idx % (kD / 16);
-    const int hg = m / R, i = m % R;
-    if (i >= tm.n_rows) continue;
+  for (int idx = threadIdx.x; idx < kQTiles * kM * (kD / 16); idx += blockDim.x) {
+    const int m2 = idx / (kD / 16), c = idx % (kD / 16);
+    const int qt = m2 / kM, t = m2 % kM;
+    const int hg = t / R, i = t % R;
+    const int loc = qt * R + i;
+    if (loc >= tm.n_rows) continue;
     const int base = tm.part_base + head * tm.n_spans;
     float M = -INFINITY;
     for (int s = 0; s < tm.n_spans; ++s) {
-      const float2 ml = part_ml[(int64_t)(base + s) * kM + m];
+      const float2 ml = part_ml[((int64_t)(base + s) * kQTiles + qt) * kM + t];
       if (ml.y > 0.f) M = fmaxf(M, ml.x);
     }
     float acc[16], den = 0.f;
 #pragma unroll
     for (int e = 0; e < 16; ++e) acc[e] = 0.f;
     for (int s = 0; s < tm.n_spans; ++s) {
-      const float2 ml = part_ml[(int64_t)(base + s) * kM + m];
+      const int64_t slot = ((int64_t)(base + s) * kQTiles + qt) * kM + t;
+      const float2 ml = part_ml[slot];
       if (!(ml.y > 0.f)) continue;
       const float w = ml.y * exp2f(ml.x - M);
       den += w;
-      const float4* src = reinterpret_cast<const float4*>(part_o + ((int64_t)(base + s) * kM + m) * kD + c * 16);
+      const float4* src = reinterpret_cast<const float4*>(part_o + slot * kD + c * 16);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float4 v = src[e];
@@ -669,7 +742,7 @@ merge_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
       }
     }
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)(tm.row0 + i) * Hq + head * G + hg) * kD + c * 16);
+    uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)(tm.row0 + loc) * Hq + head * G + hg) * kD + c * 16);
     dst[0] = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
                         pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
     dst[1] = make_uint4(pack_bf16x2(acc[8] * inv, acc[9] * inv), pack_bf16x2(acc[10] * inv, acc[11] * inv),
@@ -677,112 +750,20 @@ merge_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
   }
 }
 
-// ------------------------------------------------------------------ SIMT kernel
-// fp32 pools and bf16 shapes outside the tensor-core path.  One warp per
-// (recomputed row, query head); lanes take 32 key slots (two pages) at a time
-// for the scores and then the head dimensions for P.V.  Online softmax in fp32.
-constexpr int kSimtMaxDimsPerLane = 8;  // d <= 256
-
-template <typename T>
-__global__ void __launch_bounds__(128)
-link_attn_simt_kernel(const T* __restrict__ q, const float4* __restrict__ row_table,
-                      const int32_t* __restrict__ rows, const int32_t* __restrict__ row_off,
-                      const T* __restrict__ kpool, const T* __restrict__ vpool, int64_t num_blocks,
-                      const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off,
-                      int n_req, int Hq, int Hkv, int d, float scale, T* __restrict__ out) {
-  extern __shared__ float qs_all[];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t i = blockIdx.x;
-  const int h = blockIdx.y * 4 + warp;
-  if (h >= Hq) return;
-  float* qs = qs_all + warp * d;
-  int lo = 0, hi = n_req;  // request of row i: last r with row_off[r] <= i
-  while (hi - lo > 1) {
-    const int mid = (lo + hi) >> 1;
-    if (row_off[mid] <= i) lo = mid; else hi = mid;
-  }
-  const int r = lo;
-  const int p = rows[i];
-  const int G = Hq / Hkv, kvh = h / G, half = d / 2;
-  const T* qrow = q + (i * Hq + h) * (int64_t)d;
-  for (int j = lane; j < half; j += 32) {
-    float ya, yb;
-    rope_rotate(to_f32(qrow[j]), to_f32(qrow[j + half]), row_table[i * half + j], ya, yb);
-    qs[j] = to_f32(from_f32<T>(ya));
-    qs[j + half] = to_f32(from_f32<T>(yb));
-  }
-  __syncwarp();
-  float acc[kSimtMaxDimsPerLane];
-#pragma unroll
-  for (int e = 0; e < kSimtMaxDimsPerLane; ++e) acc[e] = 0.f;
-  float m_run = -INFINITY, l = 0.f;
-  const int pb = page_off[r], pe = page_off[r + 1];
-  for (int pp = pb; pp < pe; pp += 2) {
-    const pic_link_page first = pages[pp];
-    if (first.gpos0 + first.lo > p) break;  // pages are sorted by first valid position
-    const int pg = pp + (lane >> 4), sl = lane & 15;
-    bool valid = false;
-    int kb = 0, vb = 0;
-    if (pg < pe) {
-      const pic_link_page e = pages[pg];
-      valid = e.k_block >= 0 && e.k_block < num_blocks && e.v_block >= 0 && e.v_block < num_blocks &&
-              sl >= e.lo && sl < e.hi && e.gpos0 + sl <= p;
-      kb = e.k_block;
-      vb = e.v_block;
-    }
-    float sc = -INFINITY;
-    if (valid) {
-      const T* krow = kpool + (((int64_t)kb * Hkv + kvh) * PIC_PAGE + sl) * d;
-      float acc_s = 0.f;
-      for (int x = 0; x < d; ++x) acc_s = fmaf(qs[x], to_f32(krow[x]), acc_s);
-      sc = acc_s * scale;
-    }
-    float mx = sc;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (mx == -INFINITY) continue;
-    const float m_new = fmaxf(m_run, mx);
-    const float alpha = (m_run == -INFINITY) ? 0.f : __expf(m_run - m_new);
-    const float pl = valid ? __expf(sc - m_new) : 0.f;
-    float ps = pl;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-    l = l * alpha + ps;
-#pragma unroll
-    for (int e = 0; e < kSimtMaxDimsPerLane; ++e) acc[e] *= alpha;
-    for (int src = 0; src < 32; ++src) {
-      const float w = __shfl_sync(0xffffffffu, pl, src);
-      const int vbs = __shfl_sync(0xffffffffu, vb, src);
-      if (w == 0.f) continue;
-      const T* vrow = vpool + (((int64_t)vbs * Hkv + kvh) * PIC_PAGE + (src & 15)) * d;
-#pragma unroll
-      for (int e = 0; e < kSimtMaxDimsPerLane; ++e) {
-        const int x = lane + 32 * e;
-        if (x < d) acc[e] = fmaf(w, to_f32(vrow[x]), acc[e]);
-      }
-    }
-    m_run = m_new;
-  }
-  const float inv = l > 0.f ? 1.f / l : 0.f;
-  T* orow = out + (i * Hq + h) * (int64_t)d;
-#pragma unroll
-  for (int e = 0; e < kSimtMaxDimsPerLane; ++e) {
-    const int x = lane + 32 * e;
-    if (x < d) orow[x] = from_f32<T>(acc[e] * inv);
-  }
-}
-
 // ------------------------------------------------------------------ self-test
+// The operand layouts of the attention kernel on one 128 x 128 x 128 product:
+// A swizzled in shared memory (as Q), B loaded by TMA with the 128-byte swizzle
+// (as a K / V tile), and A written to TMEM by tcgen05.st (as P).
 __global__ void __launch_bounds__(128, 1)
 selftest_umma_kernel(const __grid_constant__ CUtensorMap bmap, const bf16* __restrict__ a, float* dk,
-                     float* dmn, int32_t* err) {
+                     float* dmn, float* dts, int32_t* err) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   uint8_t* sa = smem;
   uint8_t* sbm = smem + kOpBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + 2 * kOpBytes);
   uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2);
-  volatile int* ab = reinterpret_cast<volatile int*>(bars + 3);
+  int* ab = reinterpret_cast<int*>(bars + 3);
   const int t = threadIdx.x, warp = t >> 5;
   if (t == 0) {
     tc::mbar_init(&bars[0], 1);
@@ -791,10 +772,9 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap bmap, const bf16* __res
     tc::fence_mbar_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(tslot, 256);
+    tc::tmem_alloc(tslot, 512);
     tc::tmem_relinquish();
   }
-  // A row t, swizzled, 128-byte rows in two 64-column halves
 #pragma unroll
   for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -806,13 +786,26 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap bmap, const bf16* __res
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = *tslot;
+  const uint32_t lb = (uint32_t)((warp * 32) << 16);
+  {  // A row t into TMEM columns 384..447 (bf16 pairs)
+    uint32_t r[64];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a + t * 128);
+#pragma unroll
+    for (int x = 0; x < 64; ++x) r[x] = src[x];
+    tc::tmem_st32(tmem + lb + 384, r);
+    tc::tmem_st32(tmem + lb + 416, r + 32);
+    tc::tmem_st_wait();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
   if (t == 0) {
     tc::mbar_arrive_expect_tx(&bars[0], kOpBytes);
     for (int j = 0; j < 8; ++j) {
       tc::tma_load_2d(sbm + j * 2048, &bmap, 0, j * 16, &bars[0]);
       tc::tma_load_2d(sbm + kHalfBytes + j * 2048, &bmap, 64, j * 16, &bars[0]);
     }
-    bool ok = tc::mbar_wait(&bars[0], 0, ab, kWaitLimitNs);
+    const bool ok = tc::mbar_wait(&bars[0], 0, ab, kWaitLimitNs);
     if (ok) {
       tc::tc_fence_after();
       const uint32_t sa_a = tc::smem_addr(sa), sb_a = tc::smem_addr(sbm);
@@ -826,25 +819,26 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap bmap, const bf16* __res
         tc::mma_bf16_ss(tmem + 128, tc::sw128_desc(sa_a + koff, 16, 1024),
                         tc::sw128_desc(sb_a + ks * 2048, kHalfBytes, 1024), kIdescPV, ks > 0);
       }
+      for (int ks = 0; ks < 8; ++ks)
+        tc::mma_bf16_ts(tmem + 256, tmem + 384 + ks * 8, tc::sw128_desc(sb_a + ks * 2048, kHalfBytes, 1024),
+                        kIdescPV, ks > 0);
       tc::mma_commit(&bars[1]);
     } else {
       set_err(err, PIC_ERR_TIMEOUT);
-      *ab = 1;
+      *reinterpret_cast<volatile int*>(ab) = 1;
     }
   }
   __syncthreads();
-  if (!*ab && tc::mbar_wait(&bars[1], 0, ab, kWaitLimitNs)) {
+  if (!*reinterpret_cast<volatile int*>(ab) && tc::mbar_wait(&bars[1], 0, ab, kWaitLimitNs)) {
     tc::tc_fence_after();
-    const uint32_t lb = (uint32_t)((warp * 32) << 16);
-    for (int c = 0; c < 4; ++c) {
-      uint32_t r[32];
-      tc::tmem_ld32(tmem + lb + c * 32, r);
-      tc::tmem_ld_wait();
-      for (int x = 0; x < 32; ++x) dk[t * 128 + c * 32 + x] = u2f(r[x]);
-      tc::tmem_ld32(tmem + 128 + lb + c * 32, r);
-      tc::tmem_ld_wait();
-      for (int x = 0; x < 32; ++x) dmn[t * 128 + c * 32 + x] = u2f(r[x]);
-    }
+    float* outs[3] = {dk, dmn, dts};
+    for (int o = 0; o < 3; ++o)
+      for (int c = 0; c < 4; ++c) {
+        uint32_t r[32];
+        tc::tmem_ld32(tmem + lb + o * 128 + c * 32, r);
+        tc::tmem_ld_wait();
+        for (int x = 0; x < 32; ++x) outs[o][t * 128 + c * 32 + x] = u2f(r[x]);
+      }
   } else if (t == 0) {
     set_err(err, PIC_ERR_TIMEOUT);
   }
@@ -852,7 +846,7 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap bmap, const bf16* __res
   __syncthreads();
   if (warp == 0) {
     tc::tc_fence_after();
-    tc::tmem_dealloc(tmem, 256);
+    tc::tmem_dealloc(tmem, 512);
   }
 }
 
@@ -889,6 +883,78 @@ bool tc_shape(pic_dtype dt, int Hq, int Hkv, int d) {
   return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
 }
 
+// Plan, attend, merge with the scratch laid out by L in `ws`.  The planner may
+// add up to 4 * split_sms units by splitting key ranges.
+pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows, const int32_t* row_off,
+                     const void* k_pool, const void* v_pool, int64_t num_blocks, const pic_link_page* pages,
+                     const int32_t* page_off, int32_t n_req, int32_t Hq, int32_t Hkv, float scale, void* out,
+                     uint8_t* w, const WsLayout& L, int split_sms, int32_t* err_flag, cudaStream_t s) {
+  const int G = Hq / Hkv;
+  if (n_req > kMaxPlanReqs) return PIC_ERR_UNSUPPORTED;
+  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
+      (reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
+      (reinterpret_cast<uintptr_t>(row_table) & 15) || (reinterpret_cast<uintptr_t>(pages) & 15))
+    return PIC_ERR_INVALID;
+  const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
+  if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
+  CUtensorMap kmap, vmap;
+  if (!encode_rows128(&kmap, k_pool, pool_rows) || !encode_rows128(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  TileMeta* tiles = reinterpret_cast<TileMeta*>(w + L.off_tiles);
+  Unit* units = reinterpret_cast<Unit*>(w + L.off_units);
+  float2* part_ml = reinterpret_cast<float2*>(w + L.off_ml);
+  float* part_o = reinterpret_cast<float*>(w + L.off_o);
+  const int sms = num_sms_of_current_device();
+  const int R = kM / G;
+  plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kQTiles * R, Hkv,
+                                                split_sms < sms ? split_sms : sms, L.tiles_cap, L.units_cap, hdr,
+                                                tiles, units, err_flag);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  if (cudaFuncSetAttribute(link_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
+      cudaSuccess)
+    return PIC_ERR_CUDA;
+  cudaFuncAttributes fa;
+  if (cudaFuncGetAttributes(&fa, link_attn_tc_kernel) != cudaSuccess) return PIC_ERR_CUDA;
+  if (fa.numRegs != kLaunchRegs) return PIC_ERR_UNSUPPORTED;  // the register split assumes this launch size
+  TcArgs a;
+  a.q = static_cast<const bf16*>(q);
+  a.row_table = reinterpret_cast<const float4*>(row_table);
+  a.rows = rows;
+  a.pages = pages;
+  a.out = static_cast<bf16*>(out);
+  a.hdr = hdr;
+  a.tiles = tiles;
+  a.units = units;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  a.err = err_flag;
+  a.num_blocks = num_blocks;
+  a.Hq = Hq;
+  a.Hkv = Hkv;
+  a.G = G;
+  a.R = R;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
+  link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  merge_kernel<<<(unsigned)(L.tiles_cap * Hkv), 256, 0, s>>>(hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G, R);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+pic_status check_attention_args(const void* q, const float* row_table, const int32_t* rows, const int32_t* row_off,
+                                const void* k_pool, const void* v_pool, int64_t num_blocks, pic_dtype dtype,
+                                const pic_link_page* pages, const int32_t* page_off, int32_t n_req, int64_t n_rows,
+                                int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out, int32_t* err_flag) {
+  if (n_req < 0 || n_rows < 0 || num_blocks < 0 || Hkv < 1 || Hq < 1 || Hq % Hkv || d < 2 || d > 256 ||
+      (d & 1) || !(scale > 0.f))
+    return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (n_req == 0 || n_rows == 0) return PIC_OK;
+  if (!q || !row_table || !rows || !row_off || !k_pool || !v_pool || !pages || !page_off || !out || !err_flag)
+    return PIC_ERR_INVALID;
+  return PIC_OK;
+}
+
 }  // namespace
 }  // namespace pic
 
@@ -909,85 +975,23 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
                               const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
                               int32_t Hkv, int32_t d, float scale, void* out, void* ws, size_t ws_bytes,
                               int32_t* err_flag, pic_stream_t stream) {
-  if (n_req < 0 || n_rows < 0 || num_blocks < 0 || Hkv < 1 || Hq < 1 || Hq % Hkv || d < 2 || d > 256 ||
-      (d & 1) || !(scale > 0.f))
-    return PIC_ERR_INVALID;
-  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
-  if (n_req == 0 || n_rows == 0) return PIC_OK;
-  if (!q || !row_table || !rows || !row_off || !k_pool || !v_pool || !pages || !page_off || !out || !err_flag)
-    return PIC_ERR_INVALID;
+  const pic_status st = check_attention_args(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages,
+                                             page_off, n_req, n_rows, Hq, Hkv, d, scale, out, err_flag);
+  if (st != PIC_OK || n_req == 0 || n_rows == 0) return st;
   cudaStream_t s = (cudaStream_t)stream;
-  const int G = Hq / Hkv;
   if (tc_shape(dtype, Hq, Hkv, d)) {
-    const WsLayout L = ws_layout(n_rows, n_req, G, Hkv, d);
+    const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
     if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
-    if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
-        (reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
-      return PIC_ERR_INVALID;
-    const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
-    if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
-    CUtensorMap kmap, vmap;
-    if (!encode_rows128(&kmap, k_pool, pool_rows) || !encode_rows128(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
-    uint8_t* w = static_cast<uint8_t*>(ws);
-    WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
-    TileMeta* tiles = reinterpret_cast<TileMeta*>(w + L.off_tiles);
-    Unit* units = reinterpret_cast<Unit*>(w + L.off_units);
-    float2* part_ml = reinterpret_cast<float2*>(w + L.off_ml);
-    float* part_o = reinterpret_cast<float*>(w + L.off_o);
-    const int sms = num_sms_of_current_device();
-    plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kM / G, Hkv, sms,
-                                                  L.tiles_cap, L.units_cap, hdr, tiles, units, err_flag);
-    if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
-    if (cudaFuncSetAttribute(link_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-        cudaSuccess)
-      return PIC_ERR_CUDA;
-    TcArgs a;
-    a.q = static_cast<const bf16*>(q);
-    a.row_table = reinterpret_cast<const float4*>(row_table);
-    a.rows = rows;
-    a.pages = pages;
-    a.out = static_cast<bf16*>(out);
-    a.hdr = hdr;
-    a.tiles = tiles;
-    a.units = units;
-    a.part_o = part_o;
-    a.part_ml = part_ml;
-    a.err = err_flag;
-    a.num_blocks = num_blocks;
-    a.Hq = Hq;
-    a.Hkv = Hkv;
-    a.G = G;
-    a.R = kM / G;
-    a.scale_log2 = scale * 1.4426950408889634f;
-    const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
-    link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
-    if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
-    merge_kernel<<<(unsigned)(L.tiles_cap * Hkv), 256, 0, s>>>(hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G,
-                                                               kM / G);
-    return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+    return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
+                     out, static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, s);
   }
-  // SIMT path
-  const size_t el = (dtype == PIC_BF16) ? 2 : 4;
-  if ((reinterpret_cast<uintptr_t>(row_table) & 15) || ((size_t)d * el) % 4) return PIC_ERR_INVALID;
-  if (n_rows > INT32_MAX) return PIC_ERR_INVALID;
-  dim3 grid((unsigned)n_rows, (unsigned)((Hq + 3) / 4));
-  const size_t smem = 4 * d * sizeof(float);
-  if (dtype == PIC_BF16)
-    link_attn_simt_kernel<bf16><<<grid, 128, smem, s>>>(
-        static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), rows, row_off,
-        static_cast<const bf16*>(k_pool), static_cast<const bf16*>(v_pool), num_blocks, pages, page_off, n_req, Hq,
-        Hkv, d, scale, static_cast<bf16*>(out));
-  else
-    link_attn_simt_kernel<float><<<grid, 128, smem, s>>>(
-        static_cast<const float*>(q), reinterpret_cast<const float4*>(row_table), rows, row_off,
-        static_cast<const float*>(k_pool), static_cast<const float*>(v_pool), num_blocks, pages, page_off, n_req,
-        Hq, Hkv, d, scale, static_cast<float*>(out));
-  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+  return launch_attention_simt(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
+                               n_req, n_rows, Hq, Hkv, d, scale, out, s);
 }
 
-pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, float* d_mnmajor, int32_t* err_flag,
-                             pic_stream_t stream) {
-  if (!a || !b || !d_kmajor || !d_mnmajor || !err_flag) return PIC_ERR_INVALID;
+pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, float* d_mnmajor, float* d_tmem_a,
+                             int32_t* err_flag, pic_stream_t stream) {
+  if (!a || !b || !d_kmajor || !d_mnmajor || !d_tmem_a || !err_flag) return PIC_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(a) & 15) || (reinterpret_cast<uintptr_t>(b) & 15)) return PIC_ERR_INVALID;
   CUtensorMap bmap;
   if (!encode_rows128(&bmap, b, 128)) return PIC_ERR_CUDA;
@@ -995,7 +999,7 @@ pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, floa
   if (cudaFuncSetAttribute(selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return PIC_ERR_CUDA;
   selftest_umma_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(bmap, static_cast<const bf16*>(a), d_kmajor,
-                                                                d_mnmajor, err_flag);
+                                                                d_mnmajor, d_tmem_a, err_flag);
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }
 
@@ -1004,8 +1008,8 @@ pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, floa
 // ------------------------------------------------------------------ fixed-scratch variant
 // pic_link_attention_noalloc: the tensor-core attention with its planning and
 // merge scratch in one statically sized device array instead of a caller
-// workspace.  It calls the same kernels as pic_link_attention; it gives the
-// planner a smaller split budget (4 extra units per SM for at most 32 SMs) so
+// workspace.  It runs the same kernels as pic_link_attention; it gives the
+// planner a smaller split budget (4 extra units per SM for at most 16 SMs) so
 // that the scratch a call needs stays small.
 
 constexpr size_t kFixedScratchBytes = (size_t)PIC_NOALLOC_SCRATCH_BYTES;
@@ -1016,7 +1020,7 @@ static __device__ __align__(256) uint8_t pic_fixed_scratch[kFixedScratchBytes];
 namespace pic {
 namespace {
 
-constexpr int kFixedSplitSms = 32;
+constexpr int kFixedSplitSms = 16;
 constexpr int kMaxDevices = 256;
 
 std::mutex g_fixed_mu;
@@ -1038,14 +1042,7 @@ void* fixed_scratch_address() {
 }
 
 WsLayout fixed_layout(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d) {
-  WsLayout L = ws_layout(n_rows, n_req, G, Hkv, d);
-  const int64_t units_cap = L.tiles_cap * Hkv + (int64_t)kUnitsPerSm * kFixedSplitSms;
-  auto al = [](size_t x) { return (x + 255) & ~(size_t)255; };
-  L.units_cap = units_cap;
-  L.off_ml = al(L.off_units + units_cap * sizeof(Unit));
-  L.off_o = al(L.off_ml + (size_t)units_cap * kM * sizeof(float2));
-  L.total = al(L.off_o + (size_t)units_cap * kM * d * sizeof(float));
-  return L;
+  return ws_layout_with(n_rows, n_req, G, Hkv, d, (int64_t)kUnitsPerSm * kFixedSplitSms);
 }
 
 }  // namespace
@@ -1064,62 +1061,20 @@ extern "C" pic_status pic_link_attention_noalloc(const void* q, const float* row
   if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
   if (n_req == 0 || n_rows == 0) return PIC_OK;
   const bool tc = tc_shape(dtype, Hq, Hkv, d);
-  const int G = Hq / Hkv;
   // size check first: a call that needs more scratch than the array holds is refused before anything else
-  if (tc && fixed_layout(n_rows, n_req, G, Hkv, d).total > kFixedScratchBytes) return PIC_ERR_WORKSPACE;
-  if (!q || !row_table || !rows || !row_off || !k_pool || !v_pool || !pages || !page_off || !out || !err_flag)
-    return PIC_ERR_INVALID;
+  if (tc && fixed_layout(n_rows, n_req, Hq / Hkv, Hkv, d).total > kFixedScratchBytes) return PIC_ERR_WORKSPACE;
+  const pic_status st = check_attention_args(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages,
+                                             page_off, n_req, n_rows, Hq, Hkv, d, scale, out, err_flag);
+  if (st != PIC_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
   // the SIMT path uses no scratch at all
   if (!tc)
-    return pic_link_attention(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
-                              n_req, n_rows, Hq, Hkv, d, scale, out, nullptr, 0, err_flag, stream);
-  const WsLayout L = fixed_layout(n_rows, n_req, G, Hkv, d);
-  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
-      (reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15))
-    return PIC_ERR_INVALID;
-  const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
-  if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
+    return launch_attention_simt(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
+                                 n_req, n_rows, Hq, Hkv, d, scale, out, s);
   uint8_t* w = static_cast<uint8_t*>(fixed_scratch_address());
   if (w == nullptr) return PIC_ERR_CUDA;
-  CUtensorMap kmap, vmap;
-  if (!encode_rows128(&kmap, k_pool, pool_rows) || !encode_rows128(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
-  cudaStream_t s = (cudaStream_t)stream;
   // Nothing in the scratch has to start at zero: the planner rewrites the header,
   // tile and unit lists on every call, and partials are written before they are read.
-  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
-  TileMeta* tiles = reinterpret_cast<TileMeta*>(w + L.off_tiles);
-  Unit* units = reinterpret_cast<Unit*>(w + L.off_units);
-  float2* part_ml = reinterpret_cast<float2*>(w + L.off_ml);
-  float* part_o = reinterpret_cast<float*>(w + L.off_o);
-  const int sms = num_sms_of_current_device();
-  const int split_sms = sms < kFixedSplitSms ? sms : kFixedSplitSms;
-  plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kM / G, Hkv, split_sms,
-                                                L.tiles_cap, L.units_cap, hdr, tiles, units, err_flag);
-  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
-  if (cudaFuncSetAttribute(link_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess)
-    return PIC_ERR_CUDA;
-  TcArgs a;
-  a.q = static_cast<const bf16*>(q);
-  a.row_table = reinterpret_cast<const float4*>(row_table);
-  a.rows = rows;
-  a.pages = pages;
-  a.out = static_cast<bf16*>(out);
-  a.hdr = hdr;
-  a.tiles = tiles;
-  a.units = units;
-  a.part_o = part_o;
-  a.part_ml = part_ml;
-  a.err = err_flag;
-  a.num_blocks = num_blocks;
-  a.Hq = Hq;
-  a.Hkv = Hkv;
-  a.G = G;
-  a.R = kM / G;
-  a.scale_log2 = scale * 1.4426950408889634f;
-  const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
-  link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
-  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
-  merge_kernel<<<(unsigned)(L.tiles_cap * Hkv), 256, 0, s>>>(hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G, kM / G);
-  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+  return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
+                   out, w, fixed_layout(n_rows, n_req, Hq / Hkv, Hkv, d), kFixedSplitSms, err_flag, s);
 }

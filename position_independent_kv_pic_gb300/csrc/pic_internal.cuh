@@ -79,4 +79,11 @@ __device__ __forceinline__ void rope_rotate(float a, float b, float4 t, float& y
 
 int num_sms_of_current_device();
 
+// SIMT attention launcher (attention_simt.cu); arguments as pic_link_attention.
+pic_status launch_attention_simt(const void* q, const float* row_table, const int32_t* rows,
+                                 const int32_t* row_off, const void* k_pool, const void* v_pool,
+                                 int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                                 const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                                 int32_t Hkv, int32_t d, float scale, void* out, cudaStream_t s);
+
 }  // namespace pic

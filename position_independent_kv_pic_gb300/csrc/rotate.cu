@@ -14,7 +14,7 @@ namespace pic {
 namespace {
 
 constexpr int kRotThreads = 256;
-constexpr int kRotUnroll = 4;  // independent items in flight per thread
+constexpr int kRotUnroll = 2;  // independent items in flight per thread
 
 template <typename T> struct Vec16;
 template <> struct Vec16<__nv_bfloat16> { static constexpr int N = 8; };
@@ -58,70 +58,98 @@ __device__ __forceinline__ void rotate(float* lo, float* hi, const float4* cs) {
   for (int i = 0; i < N; ++i) rope_rotate(lo[i], hi[i], cs[i], lo[i], hi[i]);
 }
 
+// Rotate one 16-byte vector of low-half elements against the matching vector of
+// high-half elements, word by word (keeps few values live).
+template <typename T>
+__device__ __forceinline__ void rotate_vec(const uint4& xl, const uint4& xh, const float4* cs, uint4& ol,
+                                           uint4& oh) {
+  const uint32_t* wl = reinterpret_cast<const uint32_t*>(&xl);
+  const uint32_t* wh = reinterpret_cast<const uint32_t*>(&xh);
+  uint32_t* vl = reinterpret_cast<uint32_t*>(&ol);
+  uint32_t* vh = reinterpret_cast<uint32_t*>(&oh);
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    if constexpr (sizeof(T) == 2) {
+      const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wl[w]));
+      const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh[w]));
+      float y0, z0, y1, z1;
+      rope_rotate(a.x, b.x, cs[2 * w], y0, z0);
+      rope_rotate(a.y, b.y, cs[2 * w + 1], y1, z1);
+      __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1), q = __floats2bfloat162_rn(z0, z1);
+      vl[w] = *reinterpret_cast<uint32_t*>(&p);
+      vh[w] = *reinterpret_cast<uint32_t*>(&q);
+    } else {
+      float y, z;
+      rope_rotate(__uint_as_float(wl[w]), __uint_as_float(wh[w]), cs[w], y, z);
+      vl[w] = __float_as_uint(y);
+      vh[w] = __float_as_uint(z);
+    }
+  }
+}
+
 template <int N>
 __device__ __forceinline__ void load_cs(const float4* __restrict__ p, float4* cs) {
 #pragma unroll
   for (int i = 0; i < N; ++i) cs[i] = __ldg(p + i);
 }
 
-// Item index -> (entry e, head h, slot s, vector v); G = vectors per half row.
+// One block per page entry at a time (grid-stride over entries).  Within an
+// entry, item = (head h, slot s, vector v), v fastest, so a warp covers four
+// 256-byte key rows with full sectors.  The entry record is read once per block
+// (uniform), there is no 64-bit index division, and each thread keeps the cos/sin
+// of its vector while the vector index stays the same.
 template <typename T>
-__global__ void __launch_bounds__(kRotThreads)
+__global__ void __launch_bounds__(kRotThreads, 3)
 rerotate_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d,
                 const pic_rot_page* __restrict__ rot, int64_t n_rot, const float4* __restrict__ table,
                 int64_t n_tab, int32_t* err) {
   constexpr int N = Vec16<T>::N;
   const int half = d / 2;
   const int G = half / N;
-  const int64_t per_entry = (int64_t)Hkv * PIC_PAGE * G;
-  const int64_t total = n_rot * per_entry;
-  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-  for (int64_t base = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; base < total;
-       base += stride * kRotUnroll) {
-    uint4 xl[kRotUnroll], xh[kRotUnroll];
-    T* dst[kRotUnroll];
-    const float4* cs_ptr[kRotUnroll];
-    bool act[kRotUnroll];
+  const int per_entry = Hkv * PIC_PAGE * G;
+  const int hs = d * PIC_PAGE;  // elements of one (block, head) slice
+  for (int64_t e = blockIdx.x; e < n_rot; e += gridDim.x) {
+    const pic_rot_page rp = rot[e];
+    if (rp.src_block < 0 || rp.src_block >= num_blocks || rp.dst_block < 0 || rp.dst_block >= num_blocks ||
+        rp.tab < 0 || rp.tab >= n_tab || rp.lo < 0 || rp.hi > PIC_PAGE) {
+      if (threadIdx.x == 0) set_err(err, PIC_ERR_RANGE);
+      continue;
+    }
+    const T* src_base = pool + (int64_t)rp.src_block * Hkv * hs;
+    T* dst_base = pool + (int64_t)rp.dst_block * Hkv * hs;
+    const float4* tab = table + (int64_t)rp.tab * half;
+    int v_have = -1;
+    float4 cs[N];
+    for (int base = 0; base < per_entry; base += kRotThreads * kRotUnroll) {
+      uint4 xl[kRotUnroll], xh[kRotUnroll];
+      int off[kRotUnroll], vv[kRotUnroll];
+      bool act[kRotUnroll];
 #pragma unroll
-    for (int u = 0; u < kRotUnroll; ++u) {
-      const int64_t it = base + u * stride;
-      act[u] = false;
-      if (it < total) {
-        const int64_t e = it / per_entry;
-        const int rem = (int)(it - e * per_entry);
-        const int v = rem % G;
-        const int s = (rem / G) % PIC_PAGE;
-        const int h = rem / (G * PIC_PAGE);
-        const pic_rot_page rp = rot[e];
-        if (s >= rp.lo && s < rp.hi) {
-          if (rp.src_block < 0 || rp.src_block >= num_blocks || rp.dst_block < 0 ||
-              rp.dst_block >= num_blocks || rp.tab < 0 || rp.tab >= n_tab || rp.lo < 0 ||
-              rp.hi > PIC_PAGE) {
-            set_err(err, PIC_ERR_RANGE);
-          } else {
-            const int64_t row = ((int64_t)rp.src_block * Hkv + h) * PIC_PAGE + s;
-            const int64_t drow = ((int64_t)rp.dst_block * Hkv + h) * PIC_PAGE + s;
-            const T* src = pool + row * d + v * N;
-            xl[u] = __ldcs(reinterpret_cast<const uint4*>(src));
-            xh[u] = __ldcs(reinterpret_cast<const uint4*>(src + half));
-            dst[u] = pool + drow * d + v * N;
-            cs_ptr[u] = table + (int64_t)rp.tab * half + v * N;
-            act[u] = true;
-          }
+      for (int u = 0; u < kRotUnroll; ++u) {
+        const int it = base + u * kRotThreads + threadIdx.x;
+        const int v = it % G;
+        const int sl = (it / G) % PIC_PAGE;
+        const int h = it / (G * PIC_PAGE);
+        act[u] = it < per_entry && sl >= rp.lo && sl < rp.hi;
+        off[u] = h * hs + sl * d + v * N;
+        vv[u] = v;
+        if (act[u]) {
+          xl[u] = __ldcs(reinterpret_cast<const uint4*>(src_base + off[u]));
+          xh[u] = __ldcs(reinterpret_cast<const uint4*>(src_base + off[u] + half));
         }
       }
-    }
 #pragma unroll
-    for (int u = 0; u < kRotUnroll; ++u) {
-      if (!act[u]) continue;
-      float lo[N], hi[N];
-      float4 cs[N];
-      load_cs<N>(cs_ptr[u], cs);
-      unpack<T>(xl[u], lo);
-      unpack<T>(xh[u], hi);
-      rotate<N>(lo, hi, cs);
-      __stcs(reinterpret_cast<uint4*>(dst[u]), pack<T>(lo));
-      __stcs(reinterpret_cast<uint4*>(dst[u] + half), pack<T>(hi));
+      for (int u = 0; u < kRotUnroll; ++u) {
+        if (!act[u]) continue;
+        if (vv[u] != v_have) {
+          load_cs<N>(tab + vv[u] * N, cs);
+          v_have = vv[u];
+        }
+        uint4 ol, oh;
+        rotate_vec<T>(xl[u], xh[u], cs, ol, oh);
+        __stcs(reinterpret_cast<uint4*>(dst_base + off[u]), ol);
+        __stcs(reinterpret_cast<uint4*>(dst_base + off[u] + half), oh);
+      }
     }
   }
 }
@@ -207,9 +235,9 @@ pic_status pic_rerotate_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int
   if (!k_pool || !rot || !table || !err_flag) return PIC_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(table) & 15))
     return PIC_ERR_INVALID;
-  const int n = (dtype == PIC_BF16) ? 8 : 4;
-  const int64_t items = n_rot * Hkv * PIC_PAGE * (d / 2 / n);
-  const int grid = grid_for(items);
+  const int sms = num_sms_of_current_device();
+  const int64_t cap = (int64_t)sms * 6;  // 3 resident blocks per SM, two waves of entries in flight
+  const int grid = (int)(n_rot < cap ? n_rot : cap);
   if (dtype == PIC_BF16)
     rerotate_kernel<__nv_bfloat16><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
         static_cast<__nv_bfloat16*>(k_pool), num_blocks, Hkv, d, rot, n_rot,

@@ -48,13 +48,15 @@ def test_selftest_umma():
     bm = torch.randn(128, 128, generator=g).to(torch.bfloat16)
     dk = torch.zeros(128, 128, device="cuda")
     dmn = torch.zeros(128, 128, device="cuda")
+    dts = torch.zeros(128, 128, device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
-    pic.pic_selftest_umma(a.cuda(), bm.cuda(), dk, dmn, err)
+    pic.pic_selftest_umma(a.cuda(), bm.cuda(), dk, dmn, dts, err)
     torch.cuda.synchronize()
     assert err.item() == 0
     A, B = a.double(), bm.double()
     assert (dk.double().cpu() - A @ B.T).abs().max() < 1e-3
     assert (dmn.double().cpu() - A @ B).abs().max() < 1e-3
+    assert (dts.double().cpu() - A @ B).abs().max() < 1e-3
 
 
 # ---------------------------------------------------------------- the workloads
