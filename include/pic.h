@@ -193,8 +193,9 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
  * ------------------------------------------------------------------------
  * table[i][j] = { cos_hi, sin_hi, cos_lo, sin_lo } of the angle pos[i] * theta^(-2j/d),
  * j < d/2: cos and sin are computed in fp64 on the device and stored as two fp32
- * parts each (hi = fp32(v), lo = fp32(v - hi)), so the rotation kernels can
- * apply them with ~2^-46 error and store K within one bf16 ulp of the exact
+ * parts each (hi = v rounded to 16 significant bits, lo = fp32(v - hi)).  With
+ * them the rotation kernels reach ~2^-23 relative error (bf16 inputs times a
+ * 16-bit hi are exact in fp32) and store K within one bf16 ulp of the exact
  * rotation.  Used with pos = chunk_start (offset table for the rotary correction
  * by Delta_c) and with pos = rows (per-row table for fresh K and for Q).
  *   pos [n] int32 (device); table out [n][d/2][4] fp32 (device, 16-byte aligned);
@@ -252,8 +253,9 @@ pic_status pic_write_fresh_kv(void* k_pool, void* v_pool, int64_t num_blocks, pi
  *   ws          workspace of at least pic_link_attention_workspace() bytes,
  *               256-byte aligned; contents need not be initialised.
  * bf16 pools with d = 128 and Hq/Hkv in {1, 2, 4, 8, 16} run on the tensor cores
- * (tcgen05, TMEM accumulators, TMA page loads); fp32 pools and other bf16 shapes
- * run on the SIMT kernel.  Every bounded wait that runs out sets
+ * (tcgen05, TMEM accumulators, TMA page loads; at most 1024 requests per call,
+ * else PIC_ERR_UNSUPPORTED); fp32 pools and other bf16 shapes run on the SIMT
+ * kernel.  Every bounded wait that runs out sets
  * PIC_ERR_TIMEOUT in *err_flag and the kernel returns.
  * Errors: PIC_ERR_INVALID (Hq % Hkv != 0, bad d, n_req < 0, ...),
  * PIC_ERR_WORKSPACE, PIC_ERR_UNSUPPORTED, PIC_ERR_CUDA. */

@@ -45,7 +45,8 @@ constexpr int kThreads = 384;
 constexpr int kMinSpan = 8;             // key tiles per unit, lower bound
 constexpr int kUnitsPerSm = 4;          // target units per SM when splitting
 constexpr int kMaxSplitUnits = 640;     // bound on the units splitting may add
-constexpr int kMaxPlanReqs = 2048;      // requests one planning block handles
+constexpr int kMaxPlanReqs = 1024;      // requests one planning block handles
+constexpr int kMaxPlanTiles = 1024;     // Q-tile pairs planned from shared memory (more: slower path)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow up to 2^8 before O is rescaled
 
@@ -132,6 +133,8 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
   __shared__ int s_fbase[kMaxPlanReqs + 1];  // first full unit of each request
   __shared__ int s_hist[kHist];
   __shared__ int s_scan[kPlanThreads / 32 + 1];
+  __shared__ int s_poff[kMaxPlanReqs + 1];   // page offsets of the requests
+  __shared__ int s_maxpos[kMaxPlanTiles], s_npages[kMaxPlanTiles], s_nkt[kMaxPlanTiles];
   __shared__ int s_total_kt, s_part;
   const int tid = threadIdx.x;
   // (1) tile offsets over requests
@@ -161,6 +164,8 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     }
     return;
   }
+  // tiles: rows and last row position; causal page counts from one pass over the pages
+  const bool small = n_tiles <= kMaxPlanTiles;
   for (int t = tid; t < n_tiles; t += kPlanThreads) {
     int lo = 0, hi = n_req;  // request: last r with s_toff[r] <= t
     while (hi - lo > 1) {
@@ -173,18 +178,59 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     tm.row0 = row_off[r] + (t - s_toff[r]) * R2;
     tm.n_rows = min(R2, row_off[r + 1] - tm.row0);
     const int maxpos = rows[tm.row0 + tm.n_rows - 1];
-    int a = page_off[r], b = page_off[r + 1];
-    while (a < b) {
-      const int mid = (a + b) >> 1;
-      const pic_link_page p = pages[mid];
-      if (p.gpos0 + p.lo <= maxpos) a = mid + 1; else b = mid;
-    }
     tm.page_begin = page_off[r];
-    tm.n_pages = a - page_off[r];
-    tm.n_kt = ceil_div(tm.n_pages, kPagesPerKt);
+    tm.n_pages = 0;
+    if (!small) {  // many tiles: binary search per tile
+      int a = page_off[r], b = page_off[r + 1];
+      while (a < b) {
+        const int mid = (a + b) >> 1;
+        const pic_link_page p = pages[mid];
+        if (p.gpos0 + p.lo <= maxpos) a = mid + 1; else b = mid;
+      }
+      tm.n_pages = a - page_off[r];
+    } else {
+      s_maxpos[t] = maxpos;
+      s_npages[t] = 0;
+    }
+    tm.n_kt = 0;
     tm.n_spans = 0;
     tm.part_base = -1;
     tiles[t] = tm;
+  }
+  for (int r = tid; r <= n_req; r += kPlanThreads) s_poff[r] = page_off[r];
+  __syncthreads();
+  if (small) {
+    // page p is the last page a tile needs iff first(p) <= maxpos < first(p+1)
+    // (pages of a request are sorted by first valid position, tiles by maxpos)
+    const int n_pages_all = s_poff[n_req];
+    for (int p = tid; p < n_pages_all; p += kPlanThreads) {
+      int lo = 0, hi = n_req;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_poff[mid] <= p) lo = mid; else hi = mid;
+      }
+      const int r = lo;
+      const pic_link_page pg = pages[p];
+      const int first = pg.gpos0 + pg.lo;
+      int next = INT_MAX;
+      if (p + 1 < s_poff[r + 1]) {
+        const pic_link_page pn = pages[p + 1];
+        next = pn.gpos0 + pn.lo;
+      }
+      int a = s_toff[r], b = s_toff[r + 1];  // first tile with maxpos >= first
+      while (a < b) {
+        const int mid = (a + b) >> 1;
+        if (s_maxpos[mid] < first) a = mid + 1; else b = mid;
+      }
+      for (int t = a; t < s_toff[r + 1] && s_maxpos[t] < next; ++t) s_npages[t] = p + 1 - s_poff[r];
+    }
+    __syncthreads();
+  }
+  for (int t = tid; t < n_tiles; t += kPlanThreads) {
+    TileMeta& tm = tiles[t];
+    if (small) tm.n_pages = s_npages[t];
+    tm.n_kt = ceil_div(tm.n_pages, kPagesPerKt);
+    if (small) s_nkt[t] = tm.n_kt;
     atomicAdd(&s_total_kt, tm.n_kt);
   }
   __syncthreads();
@@ -240,7 +286,7 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     for (int s = 0; s < f; ++s) {
       int idx = s_fbase[r] + h * s_full[r];
       for (int t2 = t0; t2 < t1; ++t2) {
-        const int f2 = tiles[t2].n_kt / span;
+        const int f2 = (small ? s_nkt[t2] : tiles[t2].n_kt) / span;
         idx += min(f2, s) + ((t2 < t && f2 > s) ? 1 : 0);
       }
       Unit un;
@@ -287,6 +333,7 @@ struct TcArgs {
 
 struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
+  uint64_t vz_done[kSlots];  // V slot checked, rows of invalid slots zeroed (V loads only)
   uint64_t q_full[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
   uint32_t tmem_base;
   int abort;
@@ -313,55 +360,57 @@ __device__ __forceinline__ bool wait_bar(Bars* b, uint64_t* bar, uint32_t parity
 }
 
 // ---------------------------------------------------------------- producer
+__device__ __forceinline__ int4 load_page(const pic_link_page* pages, int p, int page_end) {
+  if (p < page_end) return __ldg(reinterpret_cast<const int4*>(pages) + p);
+  return make_int4(-1, -1, 0, 0);
+}
+
+// The whole warp: lane j < 8 owns page j of the key tile (its entry is loaded a
+// tile ahead) and issues that page's boxes, so page lookups and box issue run in
+// parallel across lanes.  Lane 0 arms each slot's barrier first.
 __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               uint8_t* smem, Bars* b, int n_units) {
+  const int lane = threadIdx.x & 31;
   uint32_t ld = 0;
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int page_end = tm.page_begin + tm.n_pages;
+    const int pbase = tm.page_begin + un.kt0 * kPagesPerKt;
+    int4 nxt = load_page(a.pages, lane < kPagesPerKt ? pbase + lane : page_end, page_end);
     for (int kt = un.kt0; kt < un.kt1; ++kt) {
-      int kb[kPagesPerKt], vb[kPagesPerKt];
-      uint32_t bytes = 0;
-#pragma unroll
-      for (int j = 0; j < kPagesPerKt; ++j) {
-        kb[j] = -1;
-        vb[j] = -1;
-        const int p = tm.page_begin + kt * kPagesPerKt + j;
-        if (p < page_end) {
-          const int4 pg = __ldg(reinterpret_cast<const int4*>(a.pages) + p);
-          if (page_ok(pg, a.num_blocks)) {
-            kb[j] = pg.x;
-            vb[j] = pg.y;
-            bytes += 2 * PIC_PAGE * 64 * sizeof(bf16);  // two boxes of 16 rows x 64 columns
-          } else if ((int16_t)(pg.w & 0xffff) < (int16_t)(pg.w >> 16)) {
-            set_err(a.err, PIC_ERR_RANGE);
-          }
-        }
-      }
+      const int4 pg = nxt;
+      if (kt + 1 < un.kt1 && lane < kPagesPerKt)
+        nxt = load_page(a.pages, pbase + (kt + 1 - un.kt0) * kPagesPerKt + lane, page_end);
+      const bool ok = lane < kPagesPerKt && page_ok(pg, a.num_blocks);
+      if (lane < kPagesPerKt && !ok && (int16_t)(pg.w & 0xffff) < (int16_t)(pg.w >> 16)) set_err(a.err, PIC_ERR_RANGE);
+      const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
+      const uint32_t bytes = n_ok * (2 * PIC_PAGE * 64 * sizeof(bf16));  // two boxes of 16 rows x 64 columns
 #pragma unroll
       for (int kv = 0; kv < 2; ++kv, ++ld) {
         const int slot = ld % kSlots;
-        if (!wait_bar(b, &b->kv_empty[slot], ((ld / kSlots) & 1) ^ 1)) { fail(b, a.err); return; }
-        uint8_t* dst = smem + kOffSlot + slot * kOpBytes;
-        const CUtensorMap* map = kv ? vmap : kmap;
-        tc::mbar_arrive_expect_tx(&b->kv_full[slot], bytes);
-#pragma unroll
-        for (int j = 0; j < kPagesPerKt; ++j) {
-          const int blk = kv ? vb[j] : kb[j];
-          if (blk < 0) continue;
-          const int y = (blk * a.Hkv + un.head) * PIC_PAGE;
-          tc::tma_load_2d(dst + j * 2048, map, 0, y, &b->kv_full[slot]);
-          tc::tma_load_2d(dst + kHalfBytes + j * 2048, map, 64, y, &b->kv_full[slot]);
+        if (lane == 0) {
+          if (!wait_bar(b, &b->kv_empty[slot], ((ld / kSlots) & 1) ^ 1)) fail(b, a.err);
+          else tc::mbar_arrive_expect_tx(&b->kv_full[slot], bytes);
+        }
+        // one lane reads the abort flag so that the warp leaves together
+        if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&b->abort), 0)) return;
+        if (ok) {
+          uint8_t* dst = smem + kOffSlot + slot * kOpBytes;
+          const CUtensorMap* map = kv ? vmap : kmap;
+          const int y = ((kv ? pg.y : pg.x) * a.Hkv + un.head) * PIC_PAGE;
+          tc::tma_load_2d(dst + lane * 2048, map, 0, y, &b->kv_full[slot]);
+          tc::tma_load_2d(dst + kHalfBytes + lane * 2048, map, 64, y, &b->kv_full[slot]);
         }
       }
     }
   }
   // no copy may be in flight when the block exits
-  for (uint32_t k = 0; k < kSlots && k < ld; ++k) {
-    const uint32_t t = ld - 1 - k;
-    wait_bar(b, &b->kv_full[t % kSlots], (t / kSlots) & 1);
-  }
+  if (lane == 0)
+    for (uint32_t k = 0; k < kSlots && k < ld; ++k) {
+      const uint32_t t = ld - 1 - k;
+      wait_bar(b, &b->kv_full[t % kSlots], (t / kSlots) & 1);
+    }
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -413,7 +462,11 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       const uint32_t vld = ld + 1, nld = ld + 2;
       const int vs = vld % kSlots, ns = nld % kSlots;
       const bool more = j + 1 < n;
-      if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1)) { fail(b, a.err); return; }
+      if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1) ||
+          !wait_bar(b, &b->vz_done[vs], (vld / kSlots) & 1)) {
+        fail(b, a.err);
+        return;
+      }
 #pragma unroll
       for (int i = 0; i < kQTiles; ++i) {
         if (i == 1 && !act1) break;
@@ -454,8 +507,8 @@ __device__ __forceinline__ void write_q_row(uint8_t* qs, int m, bool ok, const b
         const float2 x = __bfloat1622float2(l2[e]);
         const float2 y = __bfloat1622float2(h2[e]);
         float y0, z0, y1, z1;
-        rope_rotate(x.x, y.x, __ldg(tab + 8 * cc + 2 * e), y0, z0);
-        rope_rotate(x.y, y.y, __ldg(tab + 8 * cc + 2 * e + 1), y1, z1);
+        rope_rotate_bf16in(x.x, y.x, __ldg(tab + 8 * cc + 2 * e), y0, z0);
+        rope_rotate_bf16in(x.y, y.y, __ldg(tab + 8 * cc + 2 * e + 1), y1, z1);
         lo_w[e] = pack_bf16x2(y0, y1);
         hi_w[e] = pack_bf16x2(z0, z1);
       }
@@ -465,9 +518,55 @@ __device__ __forceinline__ void write_q_row(uint8_t* qs, int m, bool ok, const b
   }
 }
 
-__device__ __forceinline__ int4 load_page(const pic_link_page* pages, int p, int page_end) {
-  if (p < page_end) return __ldg(reinterpret_cast<const int4*>(pages) + p);
-  return make_int4(-1, -1, 0, 0);
+
+// ---------------------------------------------------------------- V-row zeroing (warps 2, 3)
+// Masked keys get weight 0 and 0 * V must stay 0 even if a slot outside a page's
+// valid range holds stale non-finite bits: once a V tile has landed, the rows of
+// slots that hold no valid key are zeroed before the MMA issuer uses the slot.
+__device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units) {
+  const int lane = threadIdx.x & 31, wz = (threadIdx.x >> 5) - 2;  // 0, 1
+  uint32_t ld = 0;
+  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    const Unit un = a.units[u];
+    const TileMeta tm = a.tiles[un.tile];
+    const int page_end = tm.page_begin + tm.n_pages;
+    for (int kt = un.kt0; kt < un.kt1; ++kt, ld += 2) {
+      const int4 pg = load_page(a.pages, lane < kPagesPerKt ? tm.page_begin + kt * kPagesPerKt + lane : page_end,
+                                page_end);
+      const bool pvalid = lane < kPagesPerKt && page_ok(pg, a.num_blocks);
+      const int plo = pvalid ? (int16_t)(pg.w & 0xffff) : 0;
+      const int phi = pvalid ? (int16_t)(pg.w >> 16) : 0;
+      const bool full = __all_sync(0xffffffffu, lane >= kPagesPerKt || (plo == 0 && phi == PIC_PAGE));
+      const uint32_t vld = ld + 1;
+      const int vs = vld % kSlots;
+      // waiting for every V tile (not only partial ones) keeps these warps at most
+      // one phase ahead of the MMA issuer on vz_done: the slot is not refilled
+      // before its previous P.V, which waits for vz_done, has completed
+      if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1)) { fail(b, a.err); return; }
+      if (!full) {
+        const int packed = plo | (phi << 16);
+        uint8_t* vsm = smem + kOffSlot + vs * kOpBytes;
+#pragma unroll
+        for (int jj = 0; jj < kPagesPerKt; ++jj) {
+          const int lh = __shfl_sync(0xffffffffu, packed, jj);
+          if ((jj & 1) != wz) continue;
+          const int lo = lh & 0xffff, hi = lh >> 16;
+          // 16 slots x 2 halves x 8 chunks of 16 bytes: 8 stores per lane
+#pragma unroll
+          for (int r = 0; r < 8; ++r) {
+            const int idx = r * 32 + lane;
+            const int cc = idx & 7, h = (idx >> 3) & 1, sl = idx >> 4;
+            if (sl < lo || sl >= hi)
+              *reinterpret_cast<uint4*>(vsm + h * kHalfBytes + (jj * PIC_PAGE + sl) * 128 + cc * 16) =
+                  make_uint4(0, 0, 0, 0);
+          }
+        }
+        tc::fence_proxy_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) tc::mbar_arrive(&b->vz_done[vs]);
+    }
+  }
 }
 
 // ---------------------------------------------------------------- softmax warpgroups
@@ -522,22 +621,25 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
 #pragma unroll
       for (int k = 0; k < kKeys; ++k) s[k] = u2f(sr[k]);
 
-      // per-page validity (also needed to zero V rows below)
-      int g0[kPagesPerKt] = {0, 0, 0, 0, 0, 0, 0, 0}, lohi[kPagesPerKt] = {0, 0, 0, 0, 0, 0, 0, 0};
+      // masking: key slot sl of page jj is visible to this row iff
+      // lo_jj <= sl < min(hi_jj, p_row - gpos0_jj + 1); one 16-bit mask per page
       const bool need_mask = __any_sync(0xffffffffu, !(tile_full && tile_last <= p_row));
       if (need_mask) {
         const int packed = plo | (phi << 16);
+        uint32_t vis[kPagesPerKt / 2];
+#pragma unroll
+        for (int w = 0; w < kPagesPerKt / 2; ++w) vis[w] = 0;
 #pragma unroll
         for (int jj = 0; jj < kPagesPerKt; ++jj) {
-          g0[jj] = __shfl_sync(0xffffffffu, cur.z, jj);
-          lohi[jj] = __shfl_sync(0xffffffffu, packed, jj);
+          const int g0 = __shfl_sync(0xffffffffu, cur.z, jj);
+          const int lh = __shfl_sync(0xffffffffu, packed, jj);
+          const int lo = lh & 0xffff;
+          const int hi = min(lh >> 16, max(p_row - g0 + 1, 0));
+          const uint32_t m16 = hi > lo ? ((1u << hi) - 1u) & ~((1u << lo) - 1u) : 0u;
+          vis[jj >> 1] |= m16 << (16 * (jj & 1));
         }
 #pragma unroll
-        for (int k = 0; k < kKeys; ++k) {
-          const int jj = k >> 4, sl = k & 15;
-          const bool ok = sl >= (lohi[jj] & 0xffff) && sl < (lohi[jj] >> 16) && g0[jj] + sl <= p_row;
-          s[k] = ok ? s[k] : -INFINITY;
-        }
+        for (int k = 0; k < kKeys; ++k) s[k] = (vis[k >> 5] & (1u << (k & 31))) ? s[k] : -INFINITY;
       }
       float mx8[8];
 #pragma unroll
@@ -586,25 +688,6 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
         }
       }
       tc::tmem_st_wait();
-      // V rows of slots that hold no valid key are zeroed (masked keys get weight
-      // 0, and 0 * V must stay 0 even if the slot holds stale bits)
-      if (qt == 0 && !tile_full) {
-        const uint32_t vld = 2 * gt + 1;
-        const int vs = vld % kSlots;
-        if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1)) { fail(b, a.err); return; }
-        uint8_t* vsm = smem + kOffSlot + vs * kOpBytes;
-        for (int idx = t; idx < kPagesPerKt * PIC_PAGE * 2 * 8; idx += 128) {
-          const int cc = idx & 7, h = (idx >> 3) & 1, sl = (idx >> 4) & 15, jj = idx >> 8;
-          int lh = 0;
-#pragma unroll
-          for (int q = 0; q < kPagesPerKt; ++q)
-            if (q == jj) lh = lohi[q];
-          if (sl < (lh & 0xffff) || sl >= (lh >> 16))
-            *reinterpret_cast<uint4*>(vsm + h * kHalfBytes + (jj * PIC_PAGE + sl) * 128 + cc * 16) =
-                make_uint4(0, 0, 0, 0);
-        }
-        tc::fence_proxy_async_smem();
-      }
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&b->p_full[qt]);
@@ -653,6 +736,7 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     for (int s = 0; s < kSlots; ++s) {
       tc::mbar_init(&b->kv_full[s], 1);
       tc::mbar_init(&b->kv_empty[s], 1);
+      tc::mbar_init(&b->vz_done[s], 2);
     }
     for (int i = 0; i < kQTiles; ++i) {
       tc::mbar_init(&b->q_full[i], 4);
@@ -679,7 +763,7 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   const int n_units = a.hdr->n_units;
   if (warp < 4) {
     tc::regs_dec<kRegsLow>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0) {
       producer_loop(a, &kmap, &vmap, smem, b, n_units);
     } else if (warp == 1 && lane == 0) {
       mma_loop(a, smem, b, tmem, n_units);
@@ -687,6 +771,8 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mma_commit(&b->drain);
       const int no_abort = 0;
       tc::mbar_wait(&b->drain, 0, &no_abort, kWaitLimitNs);
+    } else if (warp == 2 || warp == 3) {
+      vzero_loop(a, smem, b, n_units);
     }
   } else {
     tc::regs_inc<kRegsHigh>();
@@ -713,12 +799,13 @@ merge_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
   if (tile >= hdr->n_tiles) return;
   const TileMeta tm = tiles[tile];
   if (tm.n_spans <= 1) return;
-  for (int idx = threadIdx.x; idx < kQTiles * kM * (kD / 16); idx += blockDim.x) {
+  {  // blockIdx.y: 32 rows of the 256 rows of the Q-tile pair; one thread per (row, 16 dims)
+    const int idx = blockIdx.y * 256 + threadIdx.x;
     const int m2 = idx / (kD / 16), c = idx % (kD / 16);
     const int qt = m2 / kM, t = m2 % kM;
     const int hg = t / R, i = t % R;
     const int loc = qt * R + i;
-    if (loc >= tm.n_rows) continue;
+    if (loc >= tm.n_rows) return;
     const int base = tm.part_base + head * tm.n_spans;
     float M = -INFINITY;
     for (int s = 0; s < tm.n_spans; ++s) {
@@ -937,7 +1024,8 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
   link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
-  merge_kernel<<<(unsigned)(L.tiles_cap * Hkv), 256, 0, s>>>(hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G, R);
+  merge_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), kQTiles * kM * (kD / 16) / 256), 256, 0, s>>>(
+      hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G, R);
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }
 

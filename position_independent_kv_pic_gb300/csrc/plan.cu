@@ -78,6 +78,21 @@ select_rows_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __rest
   if (threadIdx.x == 0 && row_base + q != rend - rbeg) set_err(err, PIC_ERR_RANGE);
 }
 
+// Position of `x` in a non-decreasing prefix array pre[0..n] (pre[0] = 0): the w
+// with pre[w] <= x < pre[w+1].
+__device__ __forceinline__ int find_owner(const int* pre, int n, int x) {
+  int lo = 0, hi = n;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (pre[mid] <= x) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// One block per request.  Chunks are taken kPlanThreads at a time: block scans
+// give every chunk its first link page, re-rotation entry, fresh page and
+// recomputed row; then all threads write the group's pages and row slots, one
+// item each, so long chunks do not serialise on one thread.
 __global__ void __launch_bounds__(kPlanThreads)
 splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict__ chunk_off,
               const int32_t* __restrict__ q_len, const int32_t* __restrict__ kk,
@@ -89,11 +104,14 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
               pic_link_page* __restrict__ pages, pic_rot_page* __restrict__ rot,
               int32_t* __restrict__ row_block, int32_t* __restrict__ row_slot, int32_t* err) {
   __shared__ int scratch[kPlanThreads / 32 + 1];
-  const int r = blockIdx.x;
+  __shared__ int g_link[kPlanThreads + 1], g_row[kPlanThreads + 1];
+  __shared__ int g_rot[kPlanThreads], g_fresh[kPlanThreads];
+  __shared__ int g_s[kPlanThreads], g_L[kPlanThreads], g_m[kPlanThreads], g_fp[kPlanThreads], g_j0[kPlanThreads];
+  const int r = blockIdx.x, tid = threadIdx.x;
   const int c0 = chunk_off[r], c1 = chunk_off[r + 1];
   const int q = q_len[r], k = kk[r];
   if (q < 0 || k < 0 || c1 < c0) {
-    if (threadIdx.x == 0) set_err(err, PIC_ERR_INVALID);
+    if (tid == 0) set_err(err, PIC_ERR_INVALID);
     return;
   }
   const int pbeg = page_off[r], pend = page_off[r + 1];
@@ -103,61 +121,81 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
 
   int link_base = 0, rot_base = 0, fresh_base = 0, row_base = 0, T = 0;
   for (int g = c0; g < c1; g += kPlanThreads) {
-    const int c = g + threadIdx.x;
+    const int c = g + tid;
+    const int n_in = min(kPlanThreads, c1 - g);
     ChunkInfo ci = {0, 0, 0, 0, 0};
     if (c < c1) {
       ci = chunk_info(max(chunk_lens[c], 1), c - c0, k);
       if (chunk_page_off[c + 1] - chunk_page_off[c] != ci.np) set_err(err, PIC_ERR_RANGE);
     }
     int t_link, t_rot, t_fresh, t_row, t_len;
-    const int lo_link = link_base + block_exclusive_scan<kPlanThreads>(ci.fp + ci.kept, scratch, &t_link);
-    const int lo_rot = rot_base + block_exclusive_scan<kPlanThreads>((c > c0) ? ci.kept : 0, scratch, &t_rot);
-    const int lo_fresh = fresh_base + block_exclusive_scan<kPlanThreads>(ci.fp, scratch, &t_fresh);
-    const int lo_row = row_base + block_exclusive_scan<kPlanThreads>(ci.m, scratch, &t_row);
+    const int ex_link = block_exclusive_scan<kPlanThreads>(ci.fp + ci.kept, scratch, &t_link);
+    const int ex_rot = block_exclusive_scan<kPlanThreads>((c > c0) ? ci.kept : 0, scratch, &t_rot);
+    const int ex_fresh = block_exclusive_scan<kPlanThreads>(ci.fp, scratch, &t_fresh);
+    const int ex_row = block_exclusive_scan<kPlanThreads>(ci.m, scratch, &t_row);
     block_exclusive_scan<kPlanThreads>(ci.L, scratch, &t_len);
-    if (c < c1) {
-      const int s = chunk_start[c];
-      // fresh head pages of this chunk
-      for (int f = 0; f < ci.fp; ++f) {
-        const int fi = fbeg + lo_fresh + f, pi = pbeg + lo_link + f;
-        if (fi >= fend || pi >= pend) { set_err(err, PIC_ERR_RANGE); break; }
-        const int b = fresh_blocks[fi];
-        pic_link_page pg;
-        pg.k_block = b; pg.v_block = b; pg.gpos0 = s + PIC_PAGE * f;
-        pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, ci.m - PIC_PAGE * f);
+    g_link[tid] = ex_link;
+    g_row[tid] = ex_row;
+    g_rot[tid] = ex_rot;
+    g_fresh[tid] = ex_fresh;
+    g_s[tid] = (c < c1) ? chunk_start[c] : 0;
+    g_L[tid] = ci.L;
+    g_m[tid] = ci.m;
+    g_fp[tid] = ci.fp;
+    g_j0[tid] = ci.np - ci.kept;
+    if (tid == 0) {
+      g_link[kPlanThreads] = t_link;
+      g_row[kPlanThreads] = t_row;
+    }
+    __syncthreads();
+    // the group's link pages (and re-rotation entries for chunks after the first)
+    for (int P = tid; P < t_link; P += kPlanThreads) {
+      int w = find_owner(g_link, n_in, P);
+      while (w + 1 < n_in && g_link[w + 1] <= P) ++w;  // skip chunks without pages
+      const int cw = g + w;
+      const int f = P - g_link[w];
+      const int pi = pbeg + link_base + P;
+      if (pi >= pend) { set_err(err, PIC_ERR_RANGE); continue; }
+      pic_link_page pg;
+      if (f < g_fp[w]) {  // fresh head page f of the chunk
+        const int fi = fbeg + fresh_base + g_fresh[w] + f;
+        if (fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
+        const int blk = fresh_blocks[fi];
+        pg.k_block = blk; pg.v_block = blk; pg.gpos0 = g_s[w] + PIC_PAGE * f;
+        pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, g_m[w] - PIC_PAGE * f);
         pages[pi] = pg;
-      }
-      for (int j = 0; j < ci.m; ++j) {
-        const int ri = rbeg + lo_row + j, fi = fbeg + lo_fresh + j / PIC_PAGE;
-        if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); break; }
-        row_block[ri] = fresh_blocks[fi];
-        row_slot[ri] = j % PIC_PAGE;
-      }
-      // cached pages that keep at least one slot
-      const int j0 = ci.np - ci.kept;
-      for (int j = j0; j < ci.np; ++j) {
-        const int t = j - j0;
-        const int pi = pbeg + lo_link + ci.fp + t;
-        if (pi >= pend) { set_err(err, PIC_ERR_RANGE); break; }
-        const int cp = chunk_page_off[c] + j;
+      } else {  // cached page j that keeps at least one slot
+        const int t = f - g_fp[w];
+        const int j = g_j0[w] + t;
+        const int cp = chunk_page_off[cw] + j;
         const int src = k_src[cp];
         const int dst = (k_dst != nullptr) ? k_dst[cp] : src;
-        pic_link_page pg;
-        pg.k_block = (c == c0) ? src : dst;  // chunk 0 keeps Delta = 0
+        pg.k_block = (cw == c0) ? src : dst;  // chunk 0 keeps Delta = 0
         pg.v_block = v_blk[cp];
-        pg.gpos0 = s + PIC_PAGE * j;
-        pg.lo = (int16_t)max(0, ci.m - PIC_PAGE * j);
-        pg.hi = (int16_t)min(PIC_PAGE, ci.L - PIC_PAGE * j);
+        pg.gpos0 = g_s[w] + PIC_PAGE * j;
+        pg.lo = (int16_t)max(0, g_m[w] - PIC_PAGE * j);
+        pg.hi = (int16_t)min(PIC_PAGE, g_L[w] - PIC_PAGE * j);
         pages[pi] = pg;
-        if (c > c0) {
-          const int oi = obeg + lo_rot + t;
-          if (oi >= oend) { set_err(err, PIC_ERR_RANGE); break; }
+        if (cw > c0) {
+          const int oi = obeg + rot_base + g_rot[w] + t;
+          if (oi >= oend) { set_err(err, PIC_ERR_RANGE); continue; }
           pic_rot_page rp;
-          rp.src_block = src; rp.dst_block = dst; rp.tab = c; rp.lo = pg.lo; rp.hi = pg.hi;
+          rp.src_block = src; rp.dst_block = dst; rp.tab = cw; rp.lo = pg.lo; rp.hi = pg.hi;
           rot[oi] = rp;
         }
       }
     }
+    // the group's recomputed head rows
+    for (int Rr = tid; Rr < t_row; Rr += kPlanThreads) {
+      int w = find_owner(g_row, n_in, Rr);
+      while (w + 1 < n_in && g_row[w + 1] <= Rr) ++w;
+      const int j = Rr - g_row[w];
+      const int ri = rbeg + row_base + Rr, fi = fbeg + fresh_base + g_fresh[w] + j / PIC_PAGE;
+      if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
+      row_block[ri] = fresh_blocks[fi];
+      row_slot[ri] = j % PIC_PAGE;
+    }
+    __syncthreads();
     link_base += t_link;
     rot_base += t_rot;
     fresh_base += t_fresh;
@@ -166,42 +204,53 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
   }
   // query pages and rows
   const int qp = ceil_div(q, PIC_PAGE);
-  for (int f = threadIdx.x; f < qp; f += kPlanThreads) {
+  for (int f = tid; f < qp; f += kPlanThreads) {
     const int fi = fbeg + fresh_base + f, pi = pbeg + link_base + f;
     if (fi >= fend || pi >= pend) { set_err(err, PIC_ERR_RANGE); continue; }
-    const int b = fresh_blocks[fi];
+    const int blk = fresh_blocks[fi];
     pic_link_page pg;
-    pg.k_block = b; pg.v_block = b; pg.gpos0 = T + PIC_PAGE * f;
+    pg.k_block = blk; pg.v_block = blk; pg.gpos0 = T + PIC_PAGE * f;
     pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, q - PIC_PAGE * f);
     pages[pi] = pg;
   }
-  for (int j = threadIdx.x; j < q; j += kPlanThreads) {
+  for (int j = tid; j < q; j += kPlanThreads) {
     const int ri = rbeg + row_base + j, fi = fbeg + fresh_base + j / PIC_PAGE;
     if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
     row_block[ri] = fresh_blocks[fi];
     row_slot[ri] = j % PIC_PAGE;
   }
-  if (threadIdx.x == 0) {
+  if (tid == 0) {
     if (link_base + qp != pend - pbeg || rot_base != oend - obeg ||
         fresh_base + qp != fend - fbeg || row_base + q != rend - rbeg)
       set_err(err, PIC_ERR_RANGE);
   }
 }
 
-// table[i][j] = {cos_hi, sin_hi, cos_lo, sin_lo} of pos[i] * theta^(-2j/d): fp64 math,
-// hi = fp32(v) and lo = fp32(v - hi).
-__global__ void rope_table_kernel(const int32_t* __restrict__ pos, int64_t n, int half, double theta,
-                                  float4* __restrict__ table) {
+// table[i][j] = {cos_hi, sin_hi, cos_lo, sin_lo} of pos[i] * theta^(-2j/d): fp64
+// math; hi = the value rounded to 16 significant bits (so that a bf16 times hi is
+// exact in fp32), lo = fp32(v - hi).
+__device__ __forceinline__ float round16(double v) {
+  uint32_t u = __float_as_uint((float)v);
+  u = (u + 0x7Fu + ((u >> 8) & 1u)) & ~0xFFu;  // ties to even on the 8 dropped bits
+  return __uint_as_float(u);
+}
+
+constexpr int kTabThreads = 256;
+
+__global__ void __launch_bounds__(kTabThreads)
+rope_table_kernel(const int32_t* __restrict__ pos, int64_t n, int half, double theta, float4* __restrict__ table) {
+  __shared__ double inv_freq[128];
+  for (int j = threadIdx.x; j < half; j += blockDim.x) inv_freq[j] = pow(theta, -2.0 * (double)j / (double)(2 * half));
+  __syncthreads();
   const int64_t total = n * half;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = t / half;
     const int j = (int)(t - i * half);
-    const double inv_freq = pow(theta, -2.0 * (double)j / (double)(2 * half));
-    const double ang = (double)pos[i] * inv_freq;
+    const double ang = (double)pos[i] * inv_freq[j];
     double s, c;
     sincos(ang, &s, &c);
-    const float ch = (float)c, sh = (float)s;
+    const float ch = round16(c), sh = round16(s);
     table[t] = make_float4(ch, sh, (float)(c - (double)ch), (float)(s - (double)sh));
   }
 }
@@ -250,9 +299,9 @@ pic_status pic_rope_table(const int32_t* pos, int64_t n, int32_t d, double theta
   if (n == 0) return PIC_OK;
   if (!pos || !table) return PIC_ERR_INVALID;
   const int64_t total = n * (d / 2);
-  const int threads = 256;
-  const int64_t blocks = (total + threads - 1) / threads;
-  rope_table_kernel<<<(unsigned)(blocks < 65535 ? blocks : 65535), threads, 0, (cudaStream_t)stream>>>(
+  const int64_t blocks = (total + kTabThreads - 1) / kTabThreads;
+  const int64_t cap = (int64_t)num_sms_of_current_device() * 8;
+  rope_table_kernel<<<(unsigned)(blocks < cap ? blocks : cap), kTabThreads, 0, (cudaStream_t)stream>>>(
       pos, n, d / 2, theta, reinterpret_cast<float4*>(table));
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }

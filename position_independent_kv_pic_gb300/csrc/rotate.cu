@@ -73,8 +73,8 @@ __device__ __forceinline__ void rotate_vec(const uint4& xl, const uint4& xh, con
       const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wl[w]));
       const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh[w]));
       float y0, z0, y1, z1;
-      rope_rotate(a.x, b.x, cs[2 * w], y0, z0);
-      rope_rotate(a.y, b.y, cs[2 * w + 1], y1, z1);
+      rope_rotate_bf16in(a.x, b.x, cs[2 * w], y0, z0);
+      rope_rotate_bf16in(a.y, b.y, cs[2 * w + 1], y1, z1);
       __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1), q = __floats2bfloat162_rn(z0, z1);
       vl[w] = *reinterpret_cast<uint32_t*>(&p);
       vh[w] = *reinterpret_cast<uint32_t*>(&q);
@@ -184,14 +184,12 @@ write_fresh_kernel(T* __restrict__ kpool, T* __restrict__ vpool, int64_t num_blo
     const uint4 kh = *reinterpret_cast<const uint4*>(k_raw + src + half);
     const uint4 vl = *reinterpret_cast<const uint4*>(v_raw + src);
     const uint4 vh = *reinterpret_cast<const uint4*>(v_raw + src + half);
-    float lo[N], hi[N];
     float4 cs[N];
     load_cs<N>(row_table + i * half + v * N, cs);
-    unpack<T>(kl, lo);
-    unpack<T>(kh, hi);
-    rotate<N>(lo, hi, cs);
-    *reinterpret_cast<uint4*>(kpool + dst) = pack<T>(lo);
-    *reinterpret_cast<uint4*>(kpool + dst + half) = pack<T>(hi);
+    uint4 ol, oh;
+    rotate_vec<T>(kl, kh, cs, ol, oh);
+    *reinterpret_cast<uint4*>(kpool + dst) = ol;
+    *reinterpret_cast<uint4*>(kpool + dst + half) = oh;
     *reinterpret_cast<uint4*>(vpool + dst) = vl;
     *reinterpret_cast<uint4*>(vpool + dst + half) = vh;
   }
