@@ -415,24 +415,27 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
 
 // ---------------------------------------------------------------- MMA issuer
 __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units) {
-  const uint32_t sq = tc::smem_addr(smem + kOffQ);
-  const uint32_t sslot = tc::smem_addr(smem + kOffSlot);
+  // descriptor words: hi is constant, lo = start address (>> 4) plus the LBO field
+  constexpr uint32_t kHi = tc::sw128_desc_hi(1024);
+  const uint32_t q_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffQ), 16);
+  const uint32_t k_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), 16);
+  const uint32_t v_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), kHalfBytes);
   uint32_t ld = 0, uq[kQTiles] = {0, 0}, c[kQTiles] = {0, 0};
   auto issue_s = [&](int i, int slot) {
+    const uint32_t qa = q_lo + i * (kOpBytes >> 4), kb = k_lo + slot * (kOpBytes >> 4);
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
-      const uint32_t koff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-      const uint64_t da = tc::sw128_desc(sq + i * kOpBytes + koff, 16, 1024);
-      const uint64_t db = tc::sw128_desc(sslot + slot * kOpBytes + koff, 16, 1024);
-      tc::mma_bf16_ss(tmem + i * 128, da, db, kIdescS, ks > 0 ? 1u : 0u);
+      const uint32_t koff = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+      tc::mma_bf16_ss(tmem + i * 128, tc::desc_join(qa + koff, kHi), tc::desc_join(kb + koff, kHi), kIdescS,
+                      ks > 0 ? 1u : 0u);
     }
   };
   auto issue_pv = [&](int i, int slot, bool acc) {
+    const uint32_t vb = v_lo + slot * (kOpBytes >> 4);
 #pragma unroll
-    for (int ks = 0; ks < kKeys / 16; ++ks) {
-      const uint64_t db = tc::sw128_desc(sslot + slot * kOpBytes + ks * 2048, kHalfBytes, 1024);
-      tc::mma_bf16_ts(tmem + kTmemO + i * 128, tmem + i * 128 + ks * 8, db, kIdescPV, (acc || ks > 0) ? 1u : 0u);
-    }
+    for (int ks = 0; ks < kKeys / 16; ++ks)
+      tc::mma_bf16_ts(tmem + kTmemO + i * 128, tmem + i * 128 + ks * 8, tc::desc_join(vb + ks * (2048 >> 4), kHi),
+                      kIdescPV, (acc || ks > 0) ? 1u : 0u);
   };
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit un = a.units[u];
@@ -643,11 +646,13 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       }
       float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = s[k];
+      for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = -INFINITY;
 #pragma unroll
-      for (int k = 8; k < kKeys; ++k) mx8[k & 7] = fmaxf(mx8[k & 7], s[k]);
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      for (int k = 0; k < kKeys; k += 16)
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = tc::max3(mx8[q8], s[k + 2 * q8], s[k + 2 * q8 + 1]);
+      const float mx = tc::max3(tc::max3(mx8[0], mx8[1], mx8[2]), tc::max3(mx8[3], mx8[4], mx8[5]),
+                                fmaxf(mx8[6], mx8[7]));
       const float mt = mx * a.scale_log2;
       float alpha = 1.f;
       bool resc = false;
@@ -658,19 +663,29 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
         m_ref = mt;
       }
       const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P in two halves of 64 keys (32 packed columns each) over the first 64 columns of S
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
+      // P in two halves of 64 keys (32 packed columns each) over the first 64 columns of S;
+      // x = s * scale_log2 - mu and the row sum run on packed fp32 pairs
+      const uint64_t c2 = tc::f2pack(a.scale_log2, a.scale_log2), m2 = tc::f2pack(-mu, -mu);
+      uint64_t rs2[4] = {0, 0, 0, 0};
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float p0 = tc::ex2(fmaf(s[64 * hh + 2 * k], a.scale_log2, -mu));
-          const float p1 = tc::ex2(fmaf(s[64 * hh + 2 * k + 1], a.scale_log2, -mu));
-          rs[k & 3] += p0 + p1;
+          float x0, x1;
+          tc::f2unpack(tc::fma2(tc::f2pack(s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1]), c2, m2), x0, x1);
+          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+          rs2[k & 3] = tc::add2(rs2[k & 3], tc::f2pack(p0, p1));
           pk[k] = pack_bf16x2(p0, p1);
         }
         tc::tmem_st32(tS + 32 * hh, pk);
+      }
+      float rs[4];
+      {
+        const uint64_t r01 = tc::add2(rs2[0], rs2[1]), r23 = tc::add2(rs2[2], rs2[3]);
+        tc::f2unpack(tc::add2(r01, r23), rs[0], rs[1]);
+        rs[2] = 0.f;
+        rs[3] = 0.f;
       }
       l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       // O_qt is stable here (the commit behind s_full covers the previous P.V) and P.V
