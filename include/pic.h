@@ -293,9 +293,9 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
  *     race on the array: order them.
  *   - The tensor-core path (bf16, d = 128) splits long key ranges into at most
  *     64 extra work units; a call whose scratch would exceed the array (about
- *     1,400 recomputed rows of one request at Hkv = 8, fewer with more requests)
- *     is refused with PIC_ERR_WORKSPACE before any other check or launch.  The
- *     SIMT path (fp32 pools, other shapes) needs no scratch.
+ *     900 recomputed rows of one request at Hq = 32, Hkv = 8; about 700 over 4
+ *     requests) is refused with PIC_ERR_WORKSPACE before any other check or
+ *     launch.  The SIMT path (fp32 pools, other shapes) needs no scratch.
  * Results match pic_link_attention within the attention tolerance (the split
  * of key ranges, and so the summation order, can differ). */
 #define PIC_NOALLOC_SCRATCH_BYTES (32u << 20)

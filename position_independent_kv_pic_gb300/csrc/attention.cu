@@ -40,7 +40,7 @@ constexpr int kM = 128;                 // rows of one MMA tile
 constexpr int kQTiles = 2;              // MMA tiles per CTA
 constexpr int kKeys = 128;              // keys per key tile
 constexpr int kPagesPerKt = kKeys / PIC_PAGE;
-constexpr int kSlots = 4;               // K/V ring slots (32 KB each)
+constexpr int kSlots = 5;               // K/V ring slots (32 KB each)
 constexpr int kThreads = 384;
 constexpr int kMinSpan = 8;             // key tiles per unit, lower bound
 constexpr int kUnitsPerSm = 4;          // target units per SM when splitting
@@ -84,7 +84,7 @@ static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct WsLayout {
   int64_t tiles_cap, units_cap;
-  size_t off_tiles, off_units, off_ml, off_o, total;
+  size_t off_tiles, off_units, off_ml, off_o, off_q, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -99,7 +99,9 @@ WsLayout ws_layout_with(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, i
   L.off_units = al256(L.off_tiles + L.tiles_cap * sizeof(TileMeta));
   L.off_ml = al256(L.off_units + L.units_cap * sizeof(Unit));
   L.off_o = al256(L.off_ml + (size_t)L.units_cap * kQTiles * kM * sizeof(float2));
-  L.total = al256(L.off_o + (size_t)L.units_cap * kQTiles * kM * d * sizeof(float));
+  L.off_q = al256(L.off_o + (size_t)L.units_cap * kQTiles * kM * d * sizeof(float));
+  // roped Q of every (Q-tile pair, KV head, Q tile), in the MMA's swizzled layout
+  L.total = al256(L.off_q + (size_t)L.tiles_cap * Hkv * kQTiles * kOpBytes);
   return L;
 }
 
@@ -315,6 +317,7 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
 
 // ------------------------------------------------------------------ tcgen05 kernel
 struct TcArgs {
+  const uint8_t* q_tiles;  // [tile][kvh][qt] 32 KB swizzled Q operands
   const bf16* q;
   const float4* row_table;
   const int32_t* rows;
@@ -333,8 +336,8 @@ struct TcArgs {
 
 struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
-  uint64_t vz_done[kSlots];  // V slot checked, rows of invalid slots zeroed (V loads only)
-  uint64_t q_full[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
+  uint64_t vz_done[kSlots];  // V tile t (t % kSlots) checked and its invalid rows zeroed
+  uint64_t q_full[kQTiles], q_free[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
   uint32_t tmem_base;
   int abort;
 };
@@ -371,12 +374,24 @@ __device__ __forceinline__ int4 load_page(const pic_link_page* pages, int p, int
 __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31;
-  uint32_t ld = 0;
+  uint32_t ld = 0, uq[kQTiles] = {0, 0};
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int page_end = tm.page_begin + tm.n_pages;
     const int pbase = tm.page_begin + un.kt0 * kPagesPerKt;
+    // Q operands of this unit, once the previous unit's last S products have read the buffers
+    if (lane == 0) {
+      for (int i = 0; i < kQTiles; ++i) {
+        if (i == 1 && tm.n_rows <= a.R) break;
+        if (!wait_bar(b, &b->q_free[i], (uq[i] & 1) ^ 1)) { fail(b, a.err); break; }
+        ++uq[i];
+        tc::mbar_arrive_expect_tx(&b->q_full[i], kOpBytes);
+        tc::bulk_load(smem + kOffQ + i * kOpBytes,
+                      a.q_tiles + (((int64_t)un.tile * a.Hkv + un.head) * kQTiles + i) * kOpBytes, kOpBytes,
+                      &b->q_full[i]);
+      }
+    }
     int4 nxt = load_page(a.pages, lane < kPagesPerKt ? pbase + lane : page_end, page_end);
     for (int kt = un.kt0; kt < un.kt1; ++kt) {
       const int4 pg = nxt;
@@ -455,9 +470,11 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       tc::tc_fence_after();
       issue_s(0, ks);
       tc::mma_commit(&b->s_full[0]);
+      if (n == 1) tc::mma_commit(&b->q_free[0]);
       if (act1) {
         issue_s(1, ks);
         tc::mma_commit(&b->s_full[1]);
+        if (n == 1) tc::mma_commit(&b->q_free[1]);
       }
       tc::mma_commit(&b->kv_empty[ks]);
     }
@@ -465,8 +482,9 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       const uint32_t vld = ld + 1, nld = ld + 2;
       const int vs = vld % kSlots, ns = nld % kSlots;
       const bool more = j + 1 < n;
+      const uint32_t vt = ld / 2;  // V tile number (one V load per key tile)
       if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1) ||
-          !wait_bar(b, &b->vz_done[vs], (vld / kSlots) & 1)) {
+          !wait_bar(b, &b->vz_done[vt % kSlots], (vt / kSlots) & 1)) {
         fail(b, a.err);
         return;
       }
@@ -482,6 +500,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
           tc::tc_fence_after();
           issue_s(i, ns);
           tc::mma_commit(&b->s_full[i]);
+          if (j + 2 == n) tc::mma_commit(&b->q_free[i]);  // the unit's last S product of Q tile i
         } else {
           tc::mma_commit(&b->o_done[i]);
         }
@@ -521,6 +540,26 @@ __device__ __forceinline__ void write_q_row(uint8_t* qs, int m, bool ok, const b
   }
 }
 
+
+// Q operands: RoPE at each row's position, rounded to bf16 and laid out exactly as
+// the kernel's shared-memory operand (two 64-column halves of 128 swizzled rows),
+// so one bulk copy moves a whole Q tile.  One block per (Q-tile pair, KV head).
+__global__ void __launch_bounds__(kQTiles * kM)
+qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tiles, const bf16* __restrict__ q,
+             const float4* __restrict__ row_table, uint8_t* __restrict__ q_tiles, int Hq, int Hkv, int G, int R) {
+  const int th = blockIdx.x;
+  const int tile = th / Hkv, kvh = th % Hkv;
+  if (tile >= hdr->n_tiles) return;
+  const TileMeta tm = tiles[tile];
+  const int qt = threadIdx.x / kM, m = threadIdx.x % kM;
+  if (qt == 1 && tm.n_rows <= R) return;
+  const int hg = m / R, i = m % R;
+  const int loc = qt * R + i;
+  const bool ok = loc < tm.n_rows;
+  const int row = tm.row0 + (ok ? loc : 0);
+  uint8_t* dst = q_tiles + (((int64_t)tile * Hkv + kvh) * kQTiles + qt) * kOpBytes;
+  write_q_row(dst, m, ok, q + ((int64_t)row * Hq + kvh * G + hg) * kD, row_table + (int64_t)row * (kD / 2));
+}
 
 // ---------------------------------------------------------------- V-row zeroing (warps 2, 3)
 // Masked keys get weight 0 and 0 * V must stay 0 even if a slot outside a page's
@@ -567,7 +606,7 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
         tc::fence_proxy_async_smem();
       }
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(&b->vz_done[vs]);
+      if (lane == 0) tc::mbar_arrive(&b->vz_done[(ld / 2) % kSlots]);
     }
   }
 }
@@ -580,7 +619,6 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
   const uint32_t tS = tmem + qt * 128 + lane_base;  // S_qt, then P_qt in its first 64 columns
   const uint32_t tO = tmem + kTmemO + qt * 128 + lane_base;
   const int hg = t / a.R, i = t % a.R;
-  uint8_t* qs = smem + kOffQ + qt * kOpBytes;
   uint32_t c = 0, ou = 0, gt = 0;  // tiles / units this warpgroup worked on; all tiles of the CTA
   for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
     const Unit un = a.units[u];
@@ -592,14 +630,10 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
     const int row = tm.row0 + (row_ok ? loc : 0);
     const int p_row = a.rows[tm.row0 + (row_ok ? loc : tm.n_rows - 1)];
     const int hq = un.head * a.G + hg;
-    if (!active) {  // no rows for this Q tile: no Q, no barrier traffic
+    if (!active) {  // no rows for this Q tile: no barrier traffic
       gt += n;
       continue;
     }
-    write_q_row(qs, t, row_ok, a.q + ((int64_t)row * a.Hq + hq) * kD, a.row_table + (int64_t)row * (kD / 2));
-    tc::fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) tc::mbar_arrive(&b->q_full[qt]);
     float m_ref = -INFINITY, l = 0.f;
     const int page_end = tm.page_begin + tm.n_pages;
     const int pbase = tm.page_begin + un.kt0 * kPagesPerKt;
@@ -754,7 +788,8 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mbar_init(&b->vz_done[s], 2);
     }
     for (int i = 0; i < kQTiles; ++i) {
-      tc::mbar_init(&b->q_full[i], 4);
+      tc::mbar_init(&b->q_full[i], 1);
+      tc::mbar_init(&b->q_free[i], 1);
       tc::mbar_init(&b->s_full[i], 1);
       tc::mbar_init(&b->p_full[i], 4);
       tc::mbar_init(&b->o_done[i], 1);
@@ -1012,6 +1047,10 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
                                                 split_sms < sms ? split_sms : sms, L.tiles_cap, L.units_cap, hdr,
                                                 tiles, units, err_flag);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  uint8_t* q_tiles = w + L.off_q;
+  qprep_kernel<<<(unsigned)(L.tiles_cap * Hkv), kQTiles * kM, 0, s>>>(
+      hdr, tiles, static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), q_tiles, Hq, Hkv, G, R);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   if (cudaFuncSetAttribute(link_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
       cudaSuccess)
     return PIC_ERR_CUDA;
@@ -1019,6 +1058,7 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   if (cudaFuncGetAttributes(&fa, link_attn_tc_kernel) != cudaSuccess) return PIC_ERR_CUDA;
   if (fa.numRegs != kLaunchRegs) return PIC_ERR_UNSUPPORTED;  // the register split assumes this launch size
   TcArgs a;
+  a.q_tiles = q_tiles;
   a.q = static_cast<const bf16*>(q);
   a.row_table = reinterpret_cast<const float4*>(row_table);
   a.rows = rows;

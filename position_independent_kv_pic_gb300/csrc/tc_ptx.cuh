@@ -93,6 +93,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* map, int32_t 
       : "memory");
 }
 
+// Untiled bulk copy global -> shared (addresses 16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_addr(dst)),
+               "l"(src), "r"(bytes), "r"(smem_addr(bar))
+               : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM
 // Warp-collective.  Writes the allocated TMEM base address to *dst (shared).
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
