@@ -39,7 +39,12 @@ UNIT = "tokens/s"
 # ncu DRAM bytes (read + write) per launch of the attention call and of the
 # re-rotation kernel, with the kernel source they were taken from; reported as
 # roofline traffic only while the source is unchanged.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    # link_attn_tc_kernel, long_context_100x1000: 788.38 MB read + 78.96 MB written
+    ("attention", "62ca7a61da60cbec"): 867343872,
+    # rerotate_kernel<bf16>, long_context_100x1000: 201.35 MB read + 141.29 MB written
+    ("rerotate", "dd7f35853bbc3578"): 342641920,
+}
 
 
 def _src_hash(name):
@@ -248,6 +253,7 @@ def run_gpu(args, rank, world):
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": tf_burst, "unit": "TFLOP/s",
                      "frac": att_tflops / tf_burst, "traffic": traffic,
+                     "traffic_kernel": "link_attn_tc_kernel (ncu dram__bytes_read+write, one launch)",
                      "kernel": "pic_link_attention (unit plan + tcgen05 attention + LSE merge)",
                      "algorithmic": f"4*d*Hq*sum(p_r+1) = {attn_flops:.4e} flop per launch",
                      "peak_source": f"{peak_kind} bf16 dense burst"},
