@@ -78,7 +78,8 @@ struct Unit {
 };
 struct WsHeader {
   int32_t n_tiles, n_units, span, total_kt;
-  int32_t pad[60];
+  int32_t next_unit;  // run-time unit counter of the attention kernel (zeroed by the planner)
+  int32_t pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header size");
 
@@ -163,6 +164,7 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
       set_err(err, PIC_ERR_RANGE);
       hdr->n_units = 0;
       hdr->n_tiles = 0;
+      hdr->next_unit = 0;
     }
     return;
   }
@@ -260,14 +262,15 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     carry += tot;
   }
   const int n_full = carry;
-  if (tid == 0) {
-    int pos = n_full;
-    for (int len = kHist - 1; len >= 1; --len) {
-      const int c = s_hist[len];
-      s_hist[len] = pos;
-      pos += c;
-    }
-    s_fbase[n_req] = pos;  // total units
+  {  // bucket starts by decreasing length: thread t owns lengths kHist-1-2t and kHist-2-2t
+    static_assert(kHist == 2 * kPlanThreads, "two histogram buckets per thread");
+    const int l0 = kHist - 1 - 2 * tid, l1 = l0 - 1;
+    const int c0 = s_hist[l0], c1 = (l1 >= 1) ? s_hist[l1] : 0;
+    int tot;
+    const int ex = block_exclusive_scan<kPlanThreads>(c0 + c1, s_scan, &tot);
+    s_hist[l0] = n_full + ex;
+    if (l1 >= 1) s_hist[l1] = n_full + ex + c0;
+    if (tid == 0) s_fbase[n_req] = n_full + tot;  // total units
   }
   __syncthreads();
   const int n_units = s_fbase[n_req];
@@ -276,6 +279,7 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
       set_err(err, PIC_ERR_RANGE);
       hdr->n_units = 0;
       hdr->n_tiles = 0;
+      hdr->next_unit = 0;
     }
     return;
   }
@@ -311,6 +315,7 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     hdr->n_tiles = n_tiles;
     hdr->n_units = n_units;
     hdr->span = span;
+    hdr->next_unit = 0;
     hdr->total_kt = s_total_kt;
   }
 }
@@ -324,6 +329,7 @@ struct TcArgs {
   const pic_link_page* pages;
   bf16* out;
   const WsHeader* hdr;
+  int32_t* next_unit;  // &hdr->next_unit
   const TileMeta* tiles;
   const Unit* units;
   float* part_o;
@@ -334,13 +340,19 @@ struct TcArgs {
   float scale_log2;
 };
 
+constexpr int kUnitRing = 2;                  // unit indices in flight from the producer
+constexpr int kUnitReaders = 1 + 2 + 4 * kQTiles;  // MMA thread, 2 V-zeroing warps, softmax warps
+
 struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
   uint64_t vz_done[kSlots];  // V tile t (t % kSlots) checked and its invalid rows zeroed
   uint64_t q_full[kQTiles], q_free[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
+  uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
+  int unit_idx[kUnitRing];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(Bars) <= 512, "barrier area");
 
 __device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -362,6 +374,36 @@ __device__ __forceinline__ bool wait_bar(Bars* b, uint64_t* bar, uint32_t parity
   return tc::mbar_wait(bar, parity, &b->abort, kWaitLimitNs);
 }
 
+// ---------------------------------------------------------------- unit schedule
+// Units are handed out while the kernel runs: a CTA starts with unit blockIdx.x and
+// then draws the next one from a global counter, so CTAs whose units were short take
+// more of them (the planner lists long units first).  The producer warp draws; a
+// two-entry ring in shared memory passes every index, and finally an index >=
+// n_units that ends the loops, to the other warps in the same order.
+__device__ __forceinline__ bool publish_unit(Bars* b, uint32_t k, int u) {  // producer lane 0
+  const int s = k % kUnitRing;
+  if (!wait_bar(b, &b->unit_empty[s], ((k / kUnitRing) & 1) ^ 1)) return false;
+  *reinterpret_cast<volatile int*>(&b->unit_idx[s]) = u;
+  tc::mbar_arrive(&b->unit_full[s]);
+  return true;
+}
+
+// The k-th unit of this CTA (one thread per reading warp); -1 if the wait gave up.
+__device__ __forceinline__ int read_unit(Bars* b, uint32_t k) {
+  const int s = k % kUnitRing;
+  if (!wait_bar(b, &b->unit_full[s], (k / kUnitRing) & 1)) return -1;
+  const int u = *reinterpret_cast<volatile int*>(&b->unit_idx[s]);
+  tc::mbar_arrive(&b->unit_empty[s]);
+  return u;
+}
+
+// Warp-wide read_unit: lane 0 reads, every lane gets the index.
+__device__ __forceinline__ int read_unit_warp(Bars* b, uint32_t k) {
+  int u = 0;
+  if ((threadIdx.x & 31) == 0) u = read_unit(b, k);
+  return __shfl_sync(0xffffffffu, u, 0);
+}
+
 // ---------------------------------------------------------------- producer
 __device__ __forceinline__ int4 load_page(const pic_link_page* pages, int p, int page_end) {
   if (p < page_end) return __ldg(reinterpret_cast<const int4*>(pages) + p);
@@ -375,7 +417,17 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
                               uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31;
   uint32_t ld = 0, uq[kQTiles] = {0, 0};
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  int u = blockIdx.x;
+  for (uint32_t k = 0;; ++k) {
+    int go = 1;
+    if (lane == 0) {
+      go = publish_unit(b, k, u < n_units ? u : n_units);
+      if (!go) fail(b, a.err);
+    }
+    if (!__shfl_sync(0xffffffffu, go, 0) || u >= n_units) break;
+    // the next unit is drawn now, so the atomic's latency hides behind this unit's loads
+    int u_next = 0;
+    if (lane == 0) u_next = atomicAdd(a.next_unit, 1) + (int)gridDim.x;
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int page_end = tm.page_begin + tm.n_pages;
@@ -384,7 +436,11 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
     if (lane == 0) {
       for (int i = 0; i < kQTiles; ++i) {
         if (i == 1 && tm.n_rows <= a.R) break;
-        if (!wait_bar(b, &b->q_free[i], (uq[i] & 1) ^ 1)) { fail(b, a.err); break; }
+        if (!wait_bar(b, &b->q_free[i], (uq[i] & 1) ^ 1)) {
+          fail(b, a.err);
+          go = 0;
+          break;
+        }
         ++uq[i];
         tc::mbar_arrive_expect_tx(&b->q_full[i], kOpBytes);
         tc::bulk_load(smem + kOffQ + i * kOpBytes,
@@ -392,40 +448,53 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
                       &b->q_full[i]);
       }
     }
-    int4 nxt = load_page(a.pages, lane < kPagesPerKt ? pbase + lane : page_end, page_end);
-    for (int kt = un.kt0; kt < un.kt1; ++kt) {
-      const int4 pg = nxt;
-      if (kt + 1 < un.kt1 && lane < kPagesPerKt)
-        nxt = load_page(a.pages, pbase + (kt + 1 - un.kt0) * kPagesPerKt + lane, page_end);
-      const bool ok = lane < kPagesPerKt && page_ok(pg, a.num_blocks);
-      if (lane < kPagesPerKt && !ok && (int16_t)(pg.w & 0xffff) < (int16_t)(pg.w >> 16)) set_err(a.err, PIC_ERR_RANGE);
-      const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
-      const uint32_t bytes = n_ok * (2 * PIC_PAGE * 64 * sizeof(bf16));  // two boxes of 16 rows x 64 columns
+    if (!__shfl_sync(0xffffffffu, go, 0)) goto drain;
+    {
+      int4 nxt = load_page(a.pages, lane < kPagesPerKt ? pbase + lane : page_end, page_end);
+      for (int kt = un.kt0; kt < un.kt1; ++kt) {
+        const int4 pg = nxt;
+        if (kt + 1 < un.kt1 && lane < kPagesPerKt)
+          nxt = load_page(a.pages, pbase + (kt + 1 - un.kt0) * kPagesPerKt + lane, page_end);
+        const bool ok = lane < kPagesPerKt && page_ok(pg, a.num_blocks);
+        if (lane < kPagesPerKt && !ok && (int16_t)(pg.w & 0xffff) < (int16_t)(pg.w >> 16))
+          set_err(a.err, PIC_ERR_RANGE);
+        const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
+        const uint32_t bytes = n_ok * (2 * PIC_PAGE * 64 * sizeof(bf16));  // two boxes of 16 rows x 64 columns
 #pragma unroll
-      for (int kv = 0; kv < 2; ++kv, ++ld) {
-        const int slot = ld % kSlots;
-        if (lane == 0) {
-          if (!wait_bar(b, &b->kv_empty[slot], ((ld / kSlots) & 1) ^ 1)) fail(b, a.err);
-          else tc::mbar_arrive_expect_tx(&b->kv_full[slot], bytes);
-        }
-        // one lane reads the abort flag so that the warp leaves together
-        if (__shfl_sync(0xffffffffu, *reinterpret_cast<volatile int*>(&b->abort), 0)) return;
-        if (ok) {
-          uint8_t* dst = smem + kOffSlot + slot * kOpBytes;
-          const CUtensorMap* map = kv ? vmap : kmap;
-          const int y = ((kv ? pg.y : pg.x) * a.Hkv + un.head) * PIC_PAGE;
-          tc::tma_load_2d(dst + lane * 2048, map, 0, y, &b->kv_full[slot]);
-          tc::tma_load_2d(dst + kHalfBytes + lane * 2048, map, 64, y, &b->kv_full[slot]);
+        for (int kv = 0; kv < 2; ++kv) {
+          const int slot = ld % kSlots;
+          if (lane == 0) {
+            go = wait_bar(b, &b->kv_empty[slot], ((ld / kSlots) & 1) ^ 1);
+            if (!go) fail(b, a.err);
+            else tc::mbar_arrive_expect_tx(&b->kv_full[slot], bytes);
+          }
+          // a slot is armed only when all its boxes are issued right after
+          if (!__shfl_sync(0xffffffffu, go, 0)) goto drain;
+          if (ok) {
+            uint8_t* dst = smem + kOffSlot + slot * kOpBytes;
+            const CUtensorMap* map = kv ? vmap : kmap;
+            const int y = ((kv ? pg.y : pg.x) * a.Hkv + un.head) * PIC_PAGE;
+            tc::tma_load_2d(dst + lane * 2048, map, 0, y, &b->kv_full[slot]);
+            tc::tma_load_2d(dst + kHalfBytes + lane * 2048, map, 64, y, &b->kv_full[slot]);
+          }
+          ++ld;
         }
       }
     }
+    u = __shfl_sync(0xffffffffu, u_next, 0);
   }
-  // no copy may be in flight when the block exits
-  if (lane == 0)
+drain:
+  // no copy may be in flight when the block exits, also after an abort: bounded
+  // waits that do not stop at the abort flag, on the last arming of every slot
+  if (lane == 0) {
+    const int no_abort = 0;
     for (uint32_t k = 0; k < kSlots && k < ld; ++k) {
       const uint32_t t = ld - 1 - k;
-      wait_bar(b, &b->kv_full[t % kSlots], (t / kSlots) & 1);
+      tc::mbar_wait(&b->kv_full[t % kSlots], (t / kSlots) & 1, &no_abort, kWaitLimitNs);
     }
+    for (int i = 0; i < kQTiles; ++i)
+      if (uq[i] > 0) tc::mbar_wait(&b->q_full[i], (uq[i] - 1) & 1, &no_abort, kWaitLimitNs);
+  }
 }
 
 // ---------------------------------------------------------------- MMA issuer
@@ -452,7 +521,10 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       tc::mma_bf16_ts(tmem + kTmemO + i * 128, tmem + i * 128 + ks * 8, tc::desc_join(vb + ks * (2048 >> 4), kHi),
                       kIdescPV, (acc || ks > 0) ? 1u : 0u);
   };
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    const int u = read_unit(b, k);
+    if (u < 0) { fail(b, a.err); return; }
+    if (u >= n_units) break;
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int n = un.kt1 - un.kt0;
@@ -511,11 +583,12 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
   }
 }
 
-// Q row m: RoPE at the row's position, rounded to bf16, stored swizzled.
+// Q row m, 16-byte chunks cc0 and cc0 + 1 of both 64-column halves: RoPE at the
+// row's position, rounded to bf16, stored swizzled.
 __device__ __forceinline__ void write_q_row(uint8_t* qs, int m, bool ok, const bf16* __restrict__ src,
-                                            const float4* __restrict__ tab) {
+                                            const float4* __restrict__ tab, int cc0) {
 #pragma unroll
-  for (int cc = 0; cc < 8; ++cc) {
+  for (int cc = cc0; cc < cc0 + 2; ++cc) {
     uint4 lo4 = make_uint4(0, 0, 0, 0), hi4 = make_uint4(0, 0, 0, 0);
     if (ok) {
       const uint4 xl = __ldg(reinterpret_cast<const uint4*>(src + 8 * cc));
@@ -543,7 +616,8 @@ __device__ __forceinline__ void write_q_row(uint8_t* qs, int m, bool ok, const b
 
 // Q operands: RoPE at each row's position, rounded to bf16 and laid out exactly as
 // the kernel's shared-memory operand (two 64-column halves of 128 swizzled rows),
-// so one bulk copy moves a whole Q tile.  One block per (Q-tile pair, KV head).
+// so one bulk copy moves a whole Q tile.  One block per (Q-tile pair, KV head,
+// quarter of the head dimension pairs).
 __global__ void __launch_bounds__(kQTiles * kM)
 qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tiles, const bf16* __restrict__ q,
              const float4* __restrict__ row_table, uint8_t* __restrict__ q_tiles, int Hq, int Hkv, int G, int R) {
@@ -558,7 +632,8 @@ qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
   const bool ok = loc < tm.n_rows;
   const int row = tm.row0 + (ok ? loc : 0);
   uint8_t* dst = q_tiles + (((int64_t)tile * Hkv + kvh) * kQTiles + qt) * kOpBytes;
-  write_q_row(dst, m, ok, q + ((int64_t)row * Hq + kvh * G + hg) * kD, row_table + (int64_t)row * (kD / 2));
+  write_q_row(dst, m, ok, q + ((int64_t)row * Hq + kvh * G + hg) * kD, row_table + (int64_t)row * (kD / 2),
+              2 * blockIdx.y);
 }
 
 // ---------------------------------------------------------------- V-row zeroing (warps 2, 3)
@@ -568,7 +643,10 @@ qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
 __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31, wz = (threadIdx.x >> 5) - 2;  // 0, 1
   uint32_t ld = 0;
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    const int u = read_unit_warp(b, k);
+    if (u < 0) { fail(b, a.err); return; }
+    if (u >= n_units) break;
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int page_end = tm.page_begin + tm.n_pages;
@@ -620,7 +698,10 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
   const uint32_t tO = tmem + kTmemO + qt * 128 + lane_base;
   const int hg = t / a.R, i = t % a.R;
   uint32_t c = 0, ou = 0, gt = 0;  // tiles / units this warpgroup worked on; all tiles of the CTA
-  for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+  for (uint32_t k = 0;; ++k) {
+    const int u = read_unit_warp(b, k);
+    if (u < 0) { fail(b, a.err); return; }
+    if (u >= n_units) break;
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int n = un.kt1 - un.kt0;
@@ -648,24 +729,15 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       const bool tile_full = __all_sync(0xffffffffu, lane >= kPagesPerKt || pfull);
       const int tile_last = __reduce_max_sync(0xffffffffu, pvalid ? cur.z + phi - 1 : INT_MIN);
 
-      if (!wait_bar(b, &b->s_full[qt], c & 1)) { fail(b, a.err); return; }
-      tc::tc_fence_after();
-      uint32_t sr[kKeys];
-#pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) tc::tmem_ld32(tS + q4 * 32, sr + q4 * 32);
-      tc::tmem_ld_wait();
-      float s[kKeys];
-#pragma unroll
-      for (int k = 0; k < kKeys; ++k) s[k] = u2f(sr[k]);
-
       // masking: key slot sl of page jj is visible to this row iff
-      // lo_jj <= sl < min(hi_jj, p_row - gpos0_jj + 1); one 16-bit mask per page
+      // lo_jj <= sl < min(hi_jj, p_row - gpos0_jj + 1); one 16-bit mask per page.
+      // Page entries only, so the bits are ready before S is.
       const bool need_mask = __any_sync(0xffffffffu, !(tile_full && tile_last <= p_row));
+      uint32_t vis[kPagesPerKt / 2];
+#pragma unroll
+      for (int w = 0; w < kPagesPerKt / 2; ++w) vis[w] = 0;
       if (need_mask) {
         const int packed = plo | (phi << 16);
-        uint32_t vis[kPagesPerKt / 2];
-#pragma unroll
-        for (int w = 0; w < kPagesPerKt / 2; ++w) vis[w] = 0;
 #pragma unroll
         for (int jj = 0; jj < kPagesPerKt; ++jj) {
           const int g0 = __shfl_sync(0xffffffffu, cur.z, jj);
@@ -675,53 +747,93 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
           const uint32_t m16 = hi > lo ? ((1u << hi) - 1u) & ~((1u << lo) - 1u) : 0u;
           vis[jj >> 1] |= m16 << (16 * (jj & 1));
         }
+      }
+
+      if (!wait_bar(b, &b->s_full[qt], c & 1)) { fail(b, a.err); return; }
+      tc::tc_fence_after();
+      // S in two halves of 64 keys: the second half is in flight while the first is
+      // masked, reduced and (when a reference max exists) exponentiated
+      uint32_t sr[kKeys];
+      tc::tmem_ld32(tS, sr);
+      tc::tmem_ld32(tS + 32, sr + 32);
+      tc::tmem_ld_wait();
+      tc::reg_fence<64>(sr);
+      tc::tmem_ld32(tS + 64, sr + 64);
+      tc::tmem_ld32(tS + 96, sr + 96);
+      float s[kKeys];
 #pragma unroll
-        for (int k = 0; k < kKeys; ++k) s[k] = (vis[k >> 5] & (1u << (k & 31))) ? s[k] : -INFINITY;
+      for (int k = 0; k < 64; ++k) s[k] = u2f(sr[k]);
+      if (need_mask) {
+#pragma unroll
+        for (int k = 0; k < 64; ++k) s[k] = (vis[k >> 5] & (1u << (k & 31))) ? s[k] : -INFINITY;
       }
       float mx8[8];
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < kKeys; k += 16)
+      for (int k = 0; k < 64; k += 16)
+#pragma unroll
+        for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = tc::max3(mx8[q8], s[k + 2 * q8], s[k + 2 * q8 + 1]);
+
+      // P for 64 keys (32 packed columns): x = s * scale_log2 - mu and the row sum on
+      // packed fp32 pairs
+      const uint64_t c2 = tc::f2pack(a.scale_log2, a.scale_log2);
+      auto exp_half = [&](int hh, float mu, uint32_t* pk, uint64_t* rs2) {
+        const uint64_t m2 = tc::f2pack(-mu, -mu);
+        rs2[0] = rs2[1] = 0;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          float x0, x1;
+          tc::f2unpack(tc::fma2(tc::f2pack(s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1]), c2, m2), x0, x1);
+          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+          rs2[k & 1] = tc::add2(rs2[k & 1], tc::f2pack(p0, p1));
+          pk[k] = pack_bf16x2(p0, p1);
+        }
+      };
+      // the reference max m_ref changes only when a tile's max exceeds it by more than
+      // the threshold: take the first half's exponentials against it now and redo them
+      // in that (rare) case
+      uint32_t pk0[32];
+      uint64_t rsa[2] = {0, 0};
+      const bool spec = m_ref != -INFINITY;
+      if (spec) exp_half(0, m_ref, pk0, rsa);
+
+      tc::tmem_ld_wait();
+      tc::reg_fence<64>(sr + 64);
+#pragma unroll
+      for (int k = 64; k < kKeys; ++k) s[k] = u2f(sr[k]);
+      if (need_mask) {
+#pragma unroll
+        for (int k = 64; k < kKeys; ++k) s[k] = (vis[k >> 5] & (1u << (k & 31))) ? s[k] : -INFINITY;
+      }
+#pragma unroll
+      for (int k = 64; k < kKeys; k += 16)
 #pragma unroll
         for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = tc::max3(mx8[q8], s[k + 2 * q8], s[k + 2 * q8 + 1]);
       const float mx = tc::max3(tc::max3(mx8[0], mx8[1], mx8[2]), tc::max3(mx8[3], mx8[4], mx8[5]),
                                 fmaxf(mx8[6], mx8[7]));
       const float mt = mx * a.scale_log2;
       float alpha = 1.f;
-      bool resc = false;
+      bool resc = false, redo = !spec;
       if (mt > m_ref + kRescaleThreshold) {
         alpha = tc::ex2(m_ref - mt);
-        resc = (m_ref != -INFINITY);
+        resc = spec;
+        redo = true;
         l *= alpha;
         m_ref = mt;
       }
       const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-      // P in two halves of 64 keys (32 packed columns each) over the first 64 columns of S;
-      // x = s * scale_log2 - mu and the row sum run on packed fp32 pairs
-      const uint64_t c2 = tc::f2pack(a.scale_log2, a.scale_log2), m2 = tc::f2pack(-mu, -mu);
-      uint64_t rs2[4] = {0, 0, 0, 0};
-#pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float x0, x1;
-          tc::f2unpack(tc::fma2(tc::f2pack(s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1]), c2, m2), x0, x1);
-          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-          rs2[k & 3] = tc::add2(rs2[k & 3], tc::f2pack(p0, p1));
-          pk[k] = pack_bf16x2(p0, p1);
-        }
-        tc::tmem_st32(tS + 32 * hh, pk);
-      }
-      float rs[4];
+      if (redo) exp_half(0, mu, pk0, rsa);
+      tc::tmem_st32(tS, pk0);
       {
-        const uint64_t r01 = tc::add2(rs2[0], rs2[1]), r23 = tc::add2(rs2[2], rs2[3]);
-        tc::f2unpack(tc::add2(r01, r23), rs[0], rs[1]);
-        rs[2] = 0.f;
-        rs[3] = 0.f;
+        uint32_t pk1[32];
+        uint64_t rsb[2];
+        exp_half(1, mu, pk1, rsb);
+        tc::tmem_st32(tS + 32, pk1);
+        float r0, r1;
+        tc::f2unpack(tc::add2(tc::add2(rsa[0], rsa[1]), tc::add2(rsb[0], rsb[1])), r0, r1);
+        l += r0 + r1;
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       // O_qt is stable here (the commit behind s_full covers the previous P.V) and P.V
       // for this tile is not issued before p_full: rescale O after P is stored
       if (__any_sync(0xffffffffu, resc)) {
@@ -731,6 +843,7 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
           uint32_t r[32];
           tc::tmem_ld32(tO + q4 * 32, r);
           tc::tmem_ld_wait();
+          tc::reg_fence<32>(r);
 #pragma unroll
           for (int x = 0; x < 32; ++x) r[x] = f2u(u2f(r[x]) * f);
           tc::tmem_st32(tO + q4 * 32, r);
@@ -752,6 +865,7 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       uint32_t r[32];
       tc::tmem_ld32(tO + q4 * 32, r);
       tc::tmem_ld_wait();
+      tc::reg_fence<32>(r);
       if (!row_ok) continue;
       if (un.part < 0) {
         uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)row * a.Hq + hq) * kD + q4 * 32);
@@ -795,6 +909,10 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mbar_init(&b->o_done[i], 1);
     }
     tc::mbar_init(&b->drain, 1);
+    for (int i = 0; i < kUnitRing; ++i) {
+      tc::mbar_init(&b->unit_full[i], 1);
+      tc::mbar_init(&b->unit_empty[i], kUnitReaders);
+    }
     b->abort = 0;
     tc::fence_mbar_init();
   }
@@ -837,54 +955,50 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
 }
 
 // ------------------------------------------------------------------ LSE merge
-// One block per (Q-tile pair, KV head) with split spans; threads = rows x 16-dim
-// chunks.  Combines the per-span partials (O_s normalised by l_s, base-2 max m_s):
+// Blocks of 8 rows of one (Q-tile pair, KV head) with split spans; one warp per
+// row, lane = 4-dim chunk.  Combines the per-span partials (O_s normalised by
+// l_s, base-2 max m_s):
 //   O = sum_s 2^(m_s - M) l_s O_s / sum_s 2^(m_s - M) l_s.
-__global__ void __launch_bounds__(256)
+constexpr int kMergeRows = 8;
+
+__global__ void __launch_bounds__(32 * kMergeRows)
 merge_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tiles,
              const float* __restrict__ part_o, const float2* __restrict__ part_ml, bf16* __restrict__ out,
              int Hq, int Hkv, int G, int R) {
+  static_assert(kD == 4 * 32, "one float4 per lane");
   const int th = blockIdx.x;
   const int tile = th / Hkv, head = th % Hkv;
   if (tile >= hdr->n_tiles) return;
   const TileMeta tm = tiles[tile];
   if (tm.n_spans <= 1) return;
-  {  // blockIdx.y: 32 rows of the 256 rows of the Q-tile pair; one thread per (row, 16 dims)
-    const int idx = blockIdx.y * 256 + threadIdx.x;
-    const int m2 = idx / (kD / 16), c = idx % (kD / 16);
-    const int qt = m2 / kM, t = m2 % kM;
-    const int hg = t / R, i = t % R;
-    const int loc = qt * R + i;
-    if (loc >= tm.n_rows) return;
-    const int base = tm.part_base + head * tm.n_spans;
-    float M = -INFINITY;
-    for (int s = 0; s < tm.n_spans; ++s) {
-      const float2 ml = part_ml[((int64_t)(base + s) * kQTiles + qt) * kM + t];
-      if (ml.y > 0.f) M = fmaxf(M, ml.x);
-    }
-    float acc[16], den = 0.f;
-#pragma unroll
-    for (int e = 0; e < 16; ++e) acc[e] = 0.f;
-    for (int s = 0; s < tm.n_spans; ++s) {
-      const int64_t slot = ((int64_t)(base + s) * kQTiles + qt) * kM + t;
-      const float2 ml = part_ml[slot];
-      if (!(ml.y > 0.f)) continue;
+  const int m2 = blockIdx.y * kMergeRows + (threadIdx.x >> 5), c = threadIdx.x & 31;
+  const int qt = m2 / kM, t = m2 % kM;
+  const int hg = t / R, i = t % R;
+  const int loc = qt * R + i;
+  if (loc >= tm.n_rows) return;
+  const int base = tm.part_base + head * tm.n_spans;
+  float M = -INFINITY;
+  for (int s = 0; s < tm.n_spans; ++s) {
+    const float2 ml = part_ml[((int64_t)(base + s) * kQTiles + qt) * kM + t];
+    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+  }
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float den = 0.f;
+#pragma unroll 4
+  for (int s = 0; s < tm.n_spans; ++s) {
+    const int64_t slot = ((int64_t)(base + s) * kQTiles + qt) * kM + t;
+    const float2 ml = part_ml[slot];
+    const float4 v = reinterpret_cast<const float4*>(part_o + slot * kD)[c];
+    if (ml.y > 0.f) {  // a span without visible keys contributes nothing
       const float w = ml.y * exp2f(ml.x - M);
       den += w;
-      const float4* src = reinterpret_cast<const float4*>(part_o + slot * kD + c * 16);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float4 v = src[e];
-        acc[4 * e] += w * v.x; acc[4 * e + 1] += w * v.y; acc[4 * e + 2] += w * v.z; acc[4 * e + 3] += w * v.w;
-      }
+      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
     }
-    const float inv = den > 0.f ? 1.f / den : 0.f;
-    uint4* dst = reinterpret_cast<uint4*>(out + ((int64_t)(tm.row0 + loc) * Hq + head * G + hg) * kD + c * 16);
-    dst[0] = make_uint4(pack_bf16x2(acc[0] * inv, acc[1] * inv), pack_bf16x2(acc[2] * inv, acc[3] * inv),
-                        pack_bf16x2(acc[4] * inv, acc[5] * inv), pack_bf16x2(acc[6] * inv, acc[7] * inv));
-    dst[1] = make_uint4(pack_bf16x2(acc[8] * inv, acc[9] * inv), pack_bf16x2(acc[10] * inv, acc[11] * inv),
-                        pack_bf16x2(acc[12] * inv, acc[13] * inv), pack_bf16x2(acc[14] * inv, acc[15] * inv));
   }
+  const float inv = den > 0.f ? 1.f / den : 0.f;
+  uint2* dst = reinterpret_cast<uint2*>(out + ((int64_t)(tm.row0 + loc) * Hq + head * G + hg) * kD) + c;
+  *dst = make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
 }
 
 // ------------------------------------------------------------------ self-test
@@ -1048,7 +1162,7 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
                                                 tiles, units, err_flag);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   uint8_t* q_tiles = w + L.off_q;
-  qprep_kernel<<<(unsigned)(L.tiles_cap * Hkv), kQTiles * kM, 0, s>>>(
+  qprep_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), 4), kQTiles * kM, 0, s>>>(
       hdr, tiles, static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), q_tiles, Hq, Hkv, G, R);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   if (cudaFuncSetAttribute(link_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
@@ -1065,6 +1179,7 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   a.pages = pages;
   a.out = static_cast<bf16*>(out);
   a.hdr = hdr;
+  a.next_unit = &hdr->next_unit;
   a.tiles = tiles;
   a.units = units;
   a.part_o = part_o;
@@ -1079,7 +1194,7 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
   link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
-  merge_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), kQTiles * kM * (kD / 16) / 256), 256, 0, s>>>(
+  merge_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), kQTiles * kM / kMergeRows), 32 * kMergeRows, 0, s>>>(
       hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G, R);
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }

@@ -7,6 +7,8 @@
 // land at their global positions, the recomputed rows' fresh K/V replace the
 // cached head rows (HYPIC's seam window keeps those rows out of the cache), and
 // the query's K/V are appended.
+#include <algorithm>
+
 #include "pic_internal.cuh"
 
 namespace pic {
@@ -89,10 +91,11 @@ __device__ __forceinline__ int find_owner(const int* pre, int n, int x) {
   return lo;
 }
 
-// One block per request.  Chunks are taken kPlanThreads at a time: block scans
-// give every chunk its first link page, re-rotation entry, fresh page and
-// recomputed row; then all threads write the group's pages and row slots, one
-// item each, so long chunks do not serialise on one thread.
+// gridDim.y blocks per request.  Chunks are taken kPlanThreads at a time: block
+// scans (repeated by every block of the request, they are cheap) give every
+// chunk its first link page, re-rotation entry, fresh page and recomputed row;
+// then the request's blocks share the group's pages and row slots, one item per
+// thread, so neither a long chunk nor a long request serialises.
 __global__ void __launch_bounds__(kPlanThreads)
 splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict__ chunk_off,
               const int32_t* __restrict__ q_len, const int32_t* __restrict__ kk,
@@ -111,9 +114,10 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
   const int c0 = chunk_off[r], c1 = chunk_off[r + 1];
   const int q = q_len[r], k = kk[r];
   if (q < 0 || k < 0 || c1 < c0) {
-    if (tid == 0) set_err(err, PIC_ERR_INVALID);
+    if (tid == 0 && blockIdx.y == 0) set_err(err, PIC_ERR_INVALID);
     return;
   }
+  const int item0 = blockIdx.y * kPlanThreads + tid, stride = gridDim.y * kPlanThreads;
   const int pbeg = page_off[r], pend = page_off[r + 1];
   const int obeg = rot_off[r], oend = rot_off[r + 1];
   const int fbeg = fresh_off[r], fend = fresh_off[r + 1];
@@ -126,7 +130,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
     ChunkInfo ci = {0, 0, 0, 0, 0};
     if (c < c1) {
       ci = chunk_info(max(chunk_lens[c], 1), c - c0, k);
-      if (chunk_page_off[c + 1] - chunk_page_off[c] != ci.np) set_err(err, PIC_ERR_RANGE);
+      if (chunk_page_off[c + 1] - chunk_page_off[c] != ci.np && blockIdx.y == 0) set_err(err, PIC_ERR_RANGE);
     }
     int t_link, t_rot, t_fresh, t_row, t_len;
     const int ex_link = block_exclusive_scan<kPlanThreads>(ci.fp + ci.kept, scratch, &t_link);
@@ -149,7 +153,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
     }
     __syncthreads();
     // the group's link pages (and re-rotation entries for chunks after the first)
-    for (int P = tid; P < t_link; P += kPlanThreads) {
+    for (int P = item0; P < t_link; P += stride) {
       int w = find_owner(g_link, n_in, P);
       while (w + 1 < n_in && g_link[w + 1] <= P) ++w;  // skip chunks without pages
       const int cw = g + w;
@@ -186,7 +190,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
       }
     }
     // the group's recomputed head rows
-    for (int Rr = tid; Rr < t_row; Rr += kPlanThreads) {
+    for (int Rr = item0; Rr < t_row; Rr += stride) {
       int w = find_owner(g_row, n_in, Rr);
       while (w + 1 < n_in && g_row[w + 1] <= Rr) ++w;
       const int j = Rr - g_row[w];
@@ -204,7 +208,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
   }
   // query pages and rows
   const int qp = ceil_div(q, PIC_PAGE);
-  for (int f = tid; f < qp; f += kPlanThreads) {
+  for (int f = item0; f < qp; f += stride) {
     const int fi = fbeg + fresh_base + f, pi = pbeg + link_base + f;
     if (fi >= fend || pi >= pend) { set_err(err, PIC_ERR_RANGE); continue; }
     const int blk = fresh_blocks[fi];
@@ -213,13 +217,13 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
     pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, q - PIC_PAGE * f);
     pages[pi] = pg;
   }
-  for (int j = tid; j < q; j += kPlanThreads) {
+  for (int j = item0; j < q; j += stride) {
     const int ri = rbeg + row_base + j, fi = fbeg + fresh_base + j / PIC_PAGE;
     if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
     row_block[ri] = fresh_blocks[fi];
     row_slot[ri] = j % PIC_PAGE;
   }
-  if (tid == 0) {
+  if (tid == 0 && blockIdx.y == 0) {
     if (link_base + qp != pend - pbeg || rot_base != oend - obeg ||
         fresh_base + qp != fend - fbeg || row_base + q != rend - rbeg)
       set_err(err, PIC_ERR_RANGE);
@@ -286,7 +290,10 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
   if (!chunk_off || !q_len || !k || !chunk_page_off || !fresh_off || !row_off || !page_off ||
       !rot_off || !err_flag)
     return PIC_ERR_INVALID;
-  splice_kernel<<<n_req, kPlanThreads, 0, (cudaStream_t)stream>>>(
+  // enough blocks per request that a long request's pages take about one pass
+  const int sms = num_sms_of_current_device();
+  const int per_req = std::max(1, std::min(32, (2 * sms + n_req - 1) / n_req));
+  splice_kernel<<<dim3((unsigned)n_req, (unsigned)per_req), kPlanThreads, 0, (cudaStream_t)stream>>>(
       chunk_lens, chunk_off, q_len, k, chunk_start, chunk_page_off, k_src_blocks, k_dst_blocks,
       v_blocks, fresh_off, fresh_blocks, row_off, page_off, rot_off, pages, rot, row_block, row_slot,
       err_flag);

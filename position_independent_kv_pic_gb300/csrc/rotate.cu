@@ -13,8 +13,8 @@
 namespace pic {
 namespace {
 
-constexpr int kRotThreads = 256;
-constexpr int kRotUnroll = 2;  // independent items in flight per thread
+constexpr int kRotThreads = 128;
+constexpr int kRotUnroll = 4;  // independent items in flight per thread
 
 template <typename T> struct Vec16;
 template <> struct Vec16<__nv_bfloat16> { static constexpr int N = 8; };
@@ -99,7 +99,7 @@ __device__ __forceinline__ void load_cs(const float4* __restrict__ p, float4* cs
 // (uniform), there is no 64-bit index division, and each thread keeps the cos/sin
 // of its vector while the vector index stays the same.
 template <typename T>
-__global__ void __launch_bounds__(kRotThreads, 3)
+__global__ void __launch_bounds__(kRotThreads, 4)
 rerotate_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d,
                 const pic_rot_page* __restrict__ rot, int64_t n_rot, const float4* __restrict__ table,
                 int64_t n_tab, int32_t* err) {
@@ -108,8 +108,13 @@ rerotate_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d,
   const int G = half / N;
   const int per_entry = Hkv * PIC_PAGE * G;
   const int hs = d * PIC_PAGE;  // elements of one (block, head) slice
+  // the next entry's record is loaded while this one streams, so the record's
+  // latency is not paid in front of every entry's data loads
+  pic_rot_page rp_next = {0, 0, 0, 0, 0};
+  if (blockIdx.x < n_rot) rp_next = rot[blockIdx.x];
   for (int64_t e = blockIdx.x; e < n_rot; e += gridDim.x) {
-    const pic_rot_page rp = rot[e];
+    const pic_rot_page rp = rp_next;
+    if (e + gridDim.x < n_rot) rp_next = rot[e + gridDim.x];
     if (rp.src_block < 0 || rp.src_block >= num_blocks || rp.dst_block < 0 || rp.dst_block >= num_blocks ||
         rp.tab < 0 || rp.tab >= n_tab || rp.lo < 0 || rp.hi > PIC_PAGE) {
       if (threadIdx.x == 0) set_err(err, PIC_ERR_RANGE);
@@ -234,7 +239,7 @@ pic_status pic_rerotate_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int
   if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(table) & 15))
     return PIC_ERR_INVALID;
   const int sms = num_sms_of_current_device();
-  const int64_t cap = (int64_t)sms * 6;  // 3 resident blocks per SM, two waves of entries in flight
+  const int64_t cap = (int64_t)sms * 4;  // one wave: 4 resident blocks of 128 threads per SM
   const int grid = (int)(n_rot < cap ? n_rot : cap);
   if (dtype == PIC_BF16)
     rerotate_kernel<__nv_bfloat16><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
