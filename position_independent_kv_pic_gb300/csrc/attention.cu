@@ -52,6 +52,14 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: P may grow up to 2^8 b
 
 constexpr int kHalfBytes = kM * 128;      // one 64-column half of a 128-row operand (16 KB)
 constexpr int kOpBytes = 2 * kHalfBytes;  // 128 x 128 bf16 operand (32 KB)
+// A K / V slot holds the 8 pages of a key tile, page j at j * kPageBytes, each
+// page as [row group g (2)][column half h (2)][8 rows][128 B] with the 128-byte
+// swizzle: one TMA box per page.  Rows (keys) 8g' apart then sit kGroupBytes
+// apart throughout the tile, so the tile is a K-major operand with an 8-row
+// stride of kGroupBytes and each 16-key page is one MN-major k-step.
+constexpr int kPageBytes = PIC_PAGE * kD * 2;  // 4 KB
+constexpr int kGroupBytes = kPageBytes / 2;    // 8 rows x 2 halves
+constexpr int kPageHalfBytes = 1024;           // 8 rows x 64 columns
 constexpr int kOffQ = 0;                  // Q tiles 0 and 1
 constexpr int kOffSlot = kQTiles * kOpBytes;
 constexpr int kOffBar = kOffSlot + kSlots * kOpBytes;
@@ -459,7 +467,7 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
         if (lane < kPagesPerKt && !ok && (int16_t)(pg.w & 0xffff) < (int16_t)(pg.w >> 16))
           set_err(a.err, PIC_ERR_RANGE);
         const uint32_t n_ok = __popc(__ballot_sync(0xffffffffu, ok));
-        const uint32_t bytes = n_ok * (2 * PIC_PAGE * 64 * sizeof(bf16));  // two boxes of 16 rows x 64 columns
+        const uint32_t bytes = n_ok * kPageBytes;  // one box per page
 #pragma unroll
         for (int kv = 0; kv < 2; ++kv) {
           const int slot = ld % kSlots;
@@ -473,9 +481,8 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
           if (ok) {
             uint8_t* dst = smem + kOffSlot + slot * kOpBytes;
             const CUtensorMap* map = kv ? vmap : kmap;
-            const int y = ((kv ? pg.y : pg.x) * a.Hkv + un.head) * PIC_PAGE;
-            tc::tma_load_2d(dst + lane * 2048, map, 0, y, &b->kv_full[slot]);
-            tc::tma_load_2d(dst + kHalfBytes + lane * 2048, map, 64, y, &b->kv_full[slot]);
+            const int grp = ((kv ? pg.y : pg.x) * a.Hkv + un.head) * (PIC_PAGE / 8);
+            tc::tma_load_4d(dst + lane * kPageBytes, map, 0, 0, 0, grp, &b->kv_full[slot]);
           }
           ++ld;
         }
@@ -500,17 +507,18 @@ drain:
 // ---------------------------------------------------------------- MMA issuer
 __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units) {
   // descriptor words: hi is constant, lo = start address (>> 4) plus the LBO field
-  constexpr uint32_t kHi = tc::sw128_desc_hi(1024);
+  constexpr uint32_t kHi = tc::sw128_desc_hi(1024), kHiKV = tc::sw128_desc_hi(kGroupBytes);
   const uint32_t q_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffQ), 16);
   const uint32_t k_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), 16);
-  const uint32_t v_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), kHalfBytes);
+  const uint32_t v_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), kPageHalfBytes);
   uint32_t ld = 0, uq[kQTiles] = {0, 0}, c[kQTiles] = {0, 0};
   auto issue_s = [&](int i, int slot) {
     const uint32_t qa = q_lo + i * (kOpBytes >> 4), kb = k_lo + slot * (kOpBytes >> 4);
 #pragma unroll
     for (int ks = 0; ks < kD / 16; ++ks) {
-      const uint32_t koff = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
-      tc::mma_bf16_ss(tmem + i * 128, tc::desc_join(qa + koff, kHi), tc::desc_join(kb + koff, kHi), kIdescS,
+      const uint32_t qoff = ((ks >> 2) * kHalfBytes + (ks & 3) * 32) >> 4;
+      const uint32_t koff = ((ks >> 2) * kPageHalfBytes + (ks & 3) * 32) >> 4;
+      tc::mma_bf16_ss(tmem + i * 128, tc::desc_join(qa + qoff, kHi), tc::desc_join(kb + koff, kHiKV), kIdescS,
                       ks > 0 ? 1u : 0u);
     }
   };
@@ -518,8 +526,8 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
     const uint32_t vb = v_lo + slot * (kOpBytes >> 4);
 #pragma unroll
     for (int ks = 0; ks < kKeys / 16; ++ks)
-      tc::mma_bf16_ts(tmem + kTmemO + i * 128, tmem + i * 128 + ks * 8, tc::desc_join(vb + ks * (2048 >> 4), kHi),
-                      kIdescPV, (acc || ks > 0) ? 1u : 0u);
+      tc::mma_bf16_ts(tmem + kTmemO + i * 128, tmem + i * 128 + ks * 8,
+                      tc::desc_join(vb + ks * (kPageBytes >> 4), kHiKV), kIdescPV, (acc || ks > 0) ? 1u : 0u);
   };
   for (uint32_t k = 0;; ++k) {
     const int u = read_unit(b, k);
@@ -677,8 +685,8 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
             const int idx = r * 32 + lane;
             const int cc = idx & 7, h = (idx >> 3) & 1, sl = idx >> 4;
             if (sl < lo || sl >= hi)
-              *reinterpret_cast<uint4*>(vsm + h * kHalfBytes + (jj * PIC_PAGE + sl) * 128 + cc * 16) =
-                  make_uint4(0, 0, 0, 0);
+              *reinterpret_cast<uint4*>(vsm + jj * kPageBytes + (sl >> 3) * kGroupBytes + h * kPageHalfBytes +
+                                        (sl & 7) * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
           }
         }
         tc::fence_proxy_async_smem();
@@ -1052,27 +1060,25 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap bmap, const bf16* __res
   tc::tc_fence_after();
   if (t == 0) {
     tc::mbar_arrive_expect_tx(&bars[0], kOpBytes);
-    for (int j = 0; j < 8; ++j) {
-      tc::tma_load_2d(sbm + j * 2048, &bmap, 0, j * 16, &bars[0]);
-      tc::tma_load_2d(sbm + kHalfBytes + j * 2048, &bmap, 64, j * 16, &bars[0]);
-    }
+    for (int j = 0; j < 8; ++j) tc::tma_load_4d(sbm + j * kPageBytes, &bmap, 0, 0, 0, j * (PIC_PAGE / 8), &bars[0]);
     const bool ok = tc::mbar_wait(&bars[0], 0, ab, kWaitLimitNs);
     if (ok) {
       tc::tc_fence_after();
       const uint32_t sa_a = tc::smem_addr(sa), sb_a = tc::smem_addr(sbm);
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-        tc::mma_bf16_ss(tmem, tc::sw128_desc(sa_a + koff, 16, 1024), tc::sw128_desc(sb_a + koff, 16, 1024),
+        const uint32_t qoff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+        const uint32_t koff = (ks >> 2) * kPageHalfBytes + (ks & 3) * 32;
+        tc::mma_bf16_ss(tmem, tc::sw128_desc(sa_a + qoff, 16, 1024), tc::sw128_desc(sb_a + koff, 16, kGroupBytes),
                         kIdescS, ks > 0);
       }
       for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t koff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
-        tc::mma_bf16_ss(tmem + 128, tc::sw128_desc(sa_a + koff, 16, 1024),
-                        tc::sw128_desc(sb_a + ks * 2048, kHalfBytes, 1024), kIdescPV, ks > 0);
+        const uint32_t qoff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+        tc::mma_bf16_ss(tmem + 128, tc::sw128_desc(sa_a + qoff, 16, 1024),
+                        tc::sw128_desc(sb_a + ks * kPageBytes, kPageHalfBytes, kGroupBytes), kIdescPV, ks > 0);
       }
       for (int ks = 0; ks < 8; ++ks)
-        tc::mma_bf16_ts(tmem + 256, tmem + 384 + ks * 8, tc::sw128_desc(sb_a + ks * 2048, kHalfBytes, 1024),
-                        kIdescPV, ks > 0);
+        tc::mma_bf16_ts(tmem + 256, tmem + 384 + ks * 8,
+                        tc::sw128_desc(sb_a + ks * kPageBytes, kPageHalfBytes, kGroupBytes), kIdescPV, ks > 0);
       tc::mma_commit(&bars[1]);
     } else {
       set_err(err, PIC_ERR_TIMEOUT);
@@ -1116,14 +1122,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // 2-D view [rows][128] bf16 of a buffer, boxes of 16 rows x 64 columns, 128-byte swizzle.
-bool encode_rows128(CUtensorMap* map, const void* base, uint64_t rows) {
+// Rows of 128 bf16 (one (block, head, slot) key row each) viewed as
+// [row group][half][row in group][64 columns], so that one box of 2 x 2 x 8 x 64
+// moves a whole 16-row page into the [group][half][8 rows] slot layout.
+bool encode_pages(CUtensorMap* map, const void* base, uint64_t rows) {
   auto enc = tensor_map_encoder();
-  if (enc == nullptr) return false;
-  cuuint64_t dims[2] = {128, rows};
-  cuuint64_t strides[1] = {128 * sizeof(bf16)};
-  cuuint32_t box[2] = {64, PIC_PAGE};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  if (enc == nullptr || rows % 8) return false;
+  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  cuuint64_t strides[3] = {kD * sizeof(bf16), 64 * sizeof(bf16), 8 * kD * sizeof(bf16)};
+  cuuint32_t box[4] = {64, 8, 2, PIC_PAGE / 8};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1149,7 +1158,7 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
   if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
   CUtensorMap kmap, vmap;
-  if (!encode_rows128(&kmap, k_pool, pool_rows) || !encode_rows128(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
+  if (!encode_pages(&kmap, k_pool, pool_rows) || !encode_pages(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
   WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
   TileMeta* tiles = reinterpret_cast<TileMeta*>(w + L.off_tiles);
   Unit* units = reinterpret_cast<Unit*>(w + L.off_units);
@@ -1252,7 +1261,7 @@ pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, floa
   if (!a || !b || !d_kmajor || !d_mnmajor || !d_tmem_a || !err_flag) return PIC_ERR_INVALID;
   if ((reinterpret_cast<uintptr_t>(a) & 15) || (reinterpret_cast<uintptr_t>(b) & 15)) return PIC_ERR_INVALID;
   CUtensorMap bmap;
-  if (!encode_rows128(&bmap, b, 128)) return PIC_ERR_CUDA;
+  if (!encode_pages(&bmap, b, 128)) return PIC_ERR_CUDA;
   const int smem = 2 * kOpBytes + 64 + 1024;
   if (cudaFuncSetAttribute(selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return PIC_ERR_CUDA;
