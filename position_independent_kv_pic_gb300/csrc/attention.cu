@@ -41,7 +41,8 @@ constexpr int kQTiles = 2;              // MMA tiles per CTA
 constexpr int kKeys = 128;              // keys per key tile
 constexpr int kPagesPerKt = kKeys / PIC_PAGE;
 constexpr int kSlots = 5;               // K/V ring slots (32 KB each)
-constexpr int kThreads = 384;
+constexpr int kSmWarpgroups = 2 * kQTiles;  // softmax: one warpgroup per (Q tile, half of the key columns)
+constexpr int kThreads = 128 * (1 + kSmWarpgroups);
 constexpr int kMinSpan = 8;             // key tiles per unit, lower bound
 constexpr int kUnitsPerSm = 4;          // target units per SM when splitting
 constexpr int kMaxSplitUnits = 640;     // bound on the units splitting may add
@@ -63,15 +64,17 @@ constexpr int kPageHalfBytes = 1024;           // 8 rows x 64 columns
 constexpr int kOffQ = 0;                  // Q tiles 0 and 1
 constexpr int kOffSlot = kQTiles * kOpBytes;
 constexpr int kOffBar = kOffSlot + kSlots * kOpBytes;
-constexpr int kSmemBytes = kOffBar + 512 + 1024;  // + barriers + alignment slack
+constexpr int kOffXch = kOffBar + 256;  // partial row maxima / sums of the two halves of each Q tile
+constexpr int kSmemBytes = kOffXch + kQTiles * 2 * kM * (int)sizeof(float);
+static_assert(kSmemBytes <= 232448, "shared memory per block");
 constexpr uint32_t kTmemCols = 512;                // S0 | S1 | O0 | O1
 constexpr uint32_t kTmemO = 256;
-// Register split: the block launches with 384 x 168 registers; warpgroup 0
-// (TMA, MMA, two idle warps) gives 64 per thread back, the two softmax
-// warpgroups take 32 more each:  4*32*(168-104) == 8*32*(200-168).
-constexpr int kLaunchRegs = 168;
-constexpr uint32_t kRegsLow = 104, kRegsHigh = 200;
-static_assert(4 * 32 * (kLaunchRegs - (int)kRegsLow) == 8 * 32 * ((int)kRegsHigh - kLaunchRegs), "register split");
+// Register split: the block launches with 640 x 96 registers; warpgroup 0 (TMA
+// producer, MMA issuer, V zeroing) gives 32 per thread back, the four softmax
+// warpgroups take 8 more each:  4*32*(96-64) == 16*32*(104-96).
+constexpr int kLaunchRegs = 96;
+constexpr uint32_t kRegsLow = 64, kRegsHigh = 104;
+static_assert(4 * 32 * (kLaunchRegs - (int)kRegsLow) == 16 * 32 * ((int)kRegsHigh - kLaunchRegs), "register split");
 static_assert(kThreads * kLaunchRegs <= 65536, "register file");
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kM, kKeys, false);
@@ -349,7 +352,7 @@ struct TcArgs {
 };
 
 constexpr int kUnitRing = 2;                  // unit indices in flight from the producer
-constexpr int kUnitReaders = 1 + 2 + 4 * kQTiles;  // MMA thread, 2 V-zeroing warps, softmax warps
+constexpr int kUnitReaders = 1 + 2 + 4 * kSmWarpgroups;  // MMA thread, 2 V-zeroing warps, softmax warps
 
 struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
@@ -360,7 +363,7 @@ struct Bars {
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Bars) <= 512, "barrier area");
+static_assert(sizeof(Bars) <= 256, "barrier area");
 
 __device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -698,14 +701,26 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
 }
 
 // ---------------------------------------------------------------- softmax warpgroups
-__device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units, int qt) {
-  const int t = threadIdx.x - 128 * (1 + qt);  // 0..127 = TMEM lane = row of Q tile qt
+// Named barrier (ids 1, 2) of the two warpgroups that share Q tile qt.
+__device__ __forceinline__ void pair_sync(int qt) {
+  asm volatile("bar.sync %0, 256;" ::"r"(1 + qt) : "memory");
+}
+
+// Warpgroup (qt, h) handles key columns 64h .. 64h+63 of every S tile of Q tile qt,
+// one row (TMEM lane) per thread.  The two halves of a row exchange their partial
+// maxima through shared memory once per key tile (so both take identical lazy
+// rescale decisions), write P for their keys into the S columns the MMA reads
+// (keys 64h.. -> columns 32h..), keep their own row sums, rescale and store their
+// own 64 columns of O.
+__device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units, int qt, int h) {
+  const int t = (threadIdx.x - 128) & (kM - 1);  // TMEM lane = row of Q tile qt
   const int lane = threadIdx.x & 31;
   const uint32_t lane_base = (uint32_t)((t & ~31) << 16);
-  const uint32_t tS = tmem + qt * 128 + lane_base;  // S_qt, then P_qt in its first 64 columns
-  const uint32_t tO = tmem + kTmemO + qt * 128 + lane_base;
+  const uint32_t tS = tmem + qt * 128 + lane_base;                 // S_qt; P_qt over its first 64 columns
+  const uint32_t tO = tmem + kTmemO + qt * 128 + lane_base + 64 * h;  // this half's 64 columns of O_qt
+  float* xch = reinterpret_cast<float*>(smem + kOffXch) + qt * 2 * kM;  // [half][row]
   const int hg = t / a.R, i = t % a.R;
-  uint32_t c = 0, ou = 0, gt = 0;  // tiles / units this warpgroup worked on; all tiles of the CTA
+  uint32_t c = 0, ou = 0;  // tiles / units this warpgroup worked on
   for (uint32_t k = 0;; ++k) {
     const int u = read_unit_warp(b, k);
     if (u < 0) { fail(b, a.err); return; }
@@ -713,41 +728,38 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int n = un.kt1 - un.kt0;
-    const bool active = qt == 0 || tm.n_rows > a.R;
+    if (qt == 1 && tm.n_rows <= a.R) continue;  // no rows for this Q tile: no barrier traffic
     const int loc = qt * a.R + i;
     const bool row_ok = loc < tm.n_rows;
     const int row = tm.row0 + (row_ok ? loc : 0);
     const int p_row = a.rows[tm.row0 + (row_ok ? loc : tm.n_rows - 1)];
     const int hq = un.head * a.G + hg;
-    if (!active) {  // no rows for this Q tile: no barrier traffic
-      gt += n;
-      continue;
-    }
     float m_ref = -INFINITY, l = 0.f;
     const int page_end = tm.page_begin + tm.n_pages;
     const int pbase = tm.page_begin + un.kt0 * kPagesPerKt;
-    int4 pe = load_page(a.pages, lane < kPagesPerKt ? pbase + lane : page_end, page_end);
-    for (int j = 0; j < n; ++j, ++c, ++gt) {
+    // lanes 0-3 hold the entries of this half's 4 pages of the key tile (one tile ahead)
+    const int my_page = kPagesPerKt / 2 * h + lane;
+    int4 pe = load_page(a.pages, lane < kPagesPerKt / 2 ? pbase + my_page : page_end, page_end);
+    for (int j = 0; j < n; ++j, ++c) {
       const int4 cur = pe;
-      if (j + 1 < n && lane < kPagesPerKt) pe = load_page(a.pages, pbase + (j + 1) * kPagesPerKt + lane, page_end);
-      const bool pvalid = lane < kPagesPerKt && page_ok(cur, a.num_blocks);
+      if (j + 1 < n && lane < kPagesPerKt / 2)
+        pe = load_page(a.pages, pbase + (j + 1) * kPagesPerKt + my_page, page_end);
+      const bool pvalid = lane < kPagesPerKt / 2 && page_ok(cur, a.num_blocks);
       const int plo = pvalid ? (int16_t)(cur.w & 0xffff) : 0;
       const int phi = pvalid ? (int16_t)(cur.w >> 16) : 0;
       const bool pfull = plo == 0 && phi == PIC_PAGE;
-      const bool tile_full = __all_sync(0xffffffffu, lane >= kPagesPerKt || pfull);
-      const int tile_last = __reduce_max_sync(0xffffffffu, pvalid ? cur.z + phi - 1 : INT_MIN);
+      const bool half_full = __all_sync(0xffffffffu, lane >= kPagesPerKt / 2 || pfull);
+      const int half_last = __reduce_max_sync(0xffffffffu, pvalid ? cur.z + phi - 1 : INT_MIN);
 
       // masking: key slot sl of page jj is visible to this row iff
       // lo_jj <= sl < min(hi_jj, p_row - gpos0_jj + 1); one 16-bit mask per page.
       // Page entries only, so the bits are ready before S is.
-      const bool need_mask = __any_sync(0xffffffffu, !(tile_full && tile_last <= p_row));
-      uint32_t vis[kPagesPerKt / 2];
-#pragma unroll
-      for (int w = 0; w < kPagesPerKt / 2; ++w) vis[w] = 0;
+      const bool need_mask = __any_sync(0xffffffffu, !(half_full && half_last <= p_row));
+      uint32_t vis[2] = {0, 0};
       if (need_mask) {
         const int packed = plo | (phi << 16);
 #pragma unroll
-        for (int jj = 0; jj < kPagesPerKt; ++jj) {
+        for (int jj = 0; jj < kPagesPerKt / 2; ++jj) {
           const int g0 = __shfl_sync(0xffffffffu, cur.z, jj);
           const int lh = __shfl_sync(0xffffffffu, packed, jj);
           const int lo = lh & 0xffff;
@@ -759,95 +771,71 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
 
       if (!wait_bar(b, &b->s_full[qt], c & 1)) { fail(b, a.err); return; }
       tc::tc_fence_after();
-      // S in two halves of 64 keys: the second half is in flight while the first is
-      // masked, reduced and (when a reference max exists) exponentiated
-      uint32_t sr[kKeys];
-      tc::tmem_ld32(tS, sr);
-      tc::tmem_ld32(tS + 32, sr + 32);
-      tc::tmem_ld_wait();
-      tc::reg_fence<64>(sr);
-      tc::tmem_ld32(tS + 64, sr + 64);
-      tc::tmem_ld32(tS + 96, sr + 96);
-      float s[kKeys];
+      float s[64];
+      {
+        uint32_t sr[64];
+        tc::tmem_ld32(tS + 64 * h, sr);
+        tc::tmem_ld32(tS + 64 * h + 32, sr + 32);
+        tc::tmem_ld_wait();
+        tc::reg_fence<64>(sr);
 #pragma unroll
-      for (int k = 0; k < 64; ++k) s[k] = u2f(sr[k]);
+        for (int k2 = 0; k2 < 64; ++k2) s[k2] = u2f(sr[k2]);
+      }
       if (need_mask) {
 #pragma unroll
-        for (int k = 0; k < 64; ++k) s[k] = (vis[k >> 5] & (1u << (k & 31))) ? s[k] : -INFINITY;
+        for (int k2 = 0; k2 < 64; ++k2) s[k2] = (vis[k2 >> 5] & (1u << (k2 & 31))) ? s[k2] : -INFINITY;
       }
       float mx8[8];
 #pragma unroll
       for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = -INFINITY;
 #pragma unroll
-      for (int k = 0; k < 64; k += 16)
+      for (int k2 = 0; k2 < 64; k2 += 16)
 #pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = tc::max3(mx8[q8], s[k + 2 * q8], s[k + 2 * q8 + 1]);
-
-      // P for 64 keys (32 packed columns): x = s * scale_log2 - mu and the row sum on
-      // packed fp32 pairs
-      const uint64_t c2 = tc::f2pack(a.scale_log2, a.scale_log2);
-      auto exp_half = [&](int hh, float mu, uint32_t* pk, uint64_t* rs2) {
-        const uint64_t m2 = tc::f2pack(-mu, -mu);
-        rs2[0] = rs2[1] = 0;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          float x0, x1;
-          tc::f2unpack(tc::fma2(tc::f2pack(s[64 * hh + 2 * k], s[64 * hh + 2 * k + 1]), c2, m2), x0, x1);
-          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
-          rs2[k & 1] = tc::add2(rs2[k & 1], tc::f2pack(p0, p1));
-          pk[k] = pack_bf16x2(p0, p1);
-        }
-      };
-      // the reference max m_ref changes only when a tile's max exceeds it by more than
-      // the threshold: take the first half's exponentials against it now and redo them
-      // in that (rare) case
-      uint32_t pk0[32];
-      uint64_t rsa[2] = {0, 0};
-      const bool spec = m_ref != -INFINITY;
-      if (spec) exp_half(0, m_ref, pk0, rsa);
-
-      tc::tmem_ld_wait();
-      tc::reg_fence<64>(sr + 64);
-#pragma unroll
-      for (int k = 64; k < kKeys; ++k) s[k] = u2f(sr[k]);
-      if (need_mask) {
-#pragma unroll
-        for (int k = 64; k < kKeys; ++k) s[k] = (vis[k >> 5] & (1u << (k & 31))) ? s[k] : -INFINITY;
-      }
-#pragma unroll
-      for (int k = 64; k < kKeys; k += 16)
-#pragma unroll
-        for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = tc::max3(mx8[q8], s[k + 2 * q8], s[k + 2 * q8 + 1]);
-      const float mx = tc::max3(tc::max3(mx8[0], mx8[1], mx8[2]), tc::max3(mx8[3], mx8[4], mx8[5]),
-                                fmaxf(mx8[6], mx8[7]));
-      const float mt = mx * a.scale_log2;
+        for (int q8 = 0; q8 < 8; ++q8) mx8[q8] = tc::max3(mx8[q8], s[k2 + 2 * q8], s[k2 + 2 * q8 + 1]);
+      const float pmax = tc::max3(tc::max3(mx8[0], mx8[1], mx8[2]), tc::max3(mx8[3], mx8[4], mx8[5]),
+                                  fmaxf(mx8[6], mx8[7]));
+      // both halves have read their S columns after this barrier, so P may be written;
+      // the next write of xch follows s_full of the next tile, i.e. both p_full arrivals
+      xch[h * kM + t] = pmax;
+      pair_sync(qt);
+      const float mt = fmaxf(pmax, xch[(1 - h) * kM + t]) * a.scale_log2;
       float alpha = 1.f;
-      bool resc = false, redo = !spec;
+      bool resc = false;
       if (mt > m_ref + kRescaleThreshold) {
         alpha = tc::ex2(m_ref - mt);
-        resc = spec;
-        redo = true;
+        resc = (m_ref != -INFINITY);
         l *= alpha;
         m_ref = mt;
       }
       const float mu = (m_ref == -INFINITY) ? 0.f : m_ref;
-      if (redo) exp_half(0, mu, pk0, rsa);
-      tc::tmem_st32(tS, pk0);
+      // P for this half's 64 keys in two stores of 16 packed columns; x = s * scale_log2 - mu
+      // and the row sum on packed fp32 pairs
+      const uint64_t c2 = tc::f2pack(a.scale_log2, a.scale_log2), m2 = tc::f2pack(-mu, -mu);
+      uint64_t rs2[2] = {0, 0};
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int k2 = 0; k2 < 16; ++k2) {
+          float x0, x1;
+          tc::f2unpack(tc::fma2(tc::f2pack(s[32 * cc + 2 * k2], s[32 * cc + 2 * k2 + 1]), c2, m2), x0, x1);
+          const float p0 = tc::ex2(x0), p1 = tc::ex2(x1);
+          rs2[k2 & 1] = tc::add2(rs2[k2 & 1], tc::f2pack(p0, p1));
+          pk[k2] = pack_bf16x2(p0, p1);
+        }
+        tc::tmem_st16(tS + 32 * h + 16 * cc, pk);
+      }
       {
-        uint32_t pk1[32];
-        uint64_t rsb[2];
-        exp_half(1, mu, pk1, rsb);
-        tc::tmem_st32(tS + 32, pk1);
         float r0, r1;
-        tc::f2unpack(tc::add2(tc::add2(rsa[0], rsa[1]), tc::add2(rsb[0], rsb[1])), r0, r1);
+        tc::f2unpack(tc::add2(rs2[0], rs2[1]), r0, r1);
         l += r0 + r1;
       }
       // O_qt is stable here (the commit behind s_full covers the previous P.V) and P.V
-      // for this tile is not issued before p_full: rescale O after P is stored
+      // for this tile is not issued before p_full: rescale this half of O after P is stored
       if (__any_sync(0xffffffffu, resc)) {
         const float f = resc ? alpha : 1.f;
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
+        for (int q4 = 0; q4 < 2; ++q4) {
           uint32_t r[32];
           tc::tmem_ld32(tO + q4 * 32, r);
           tc::tmem_ld_wait();
@@ -862,37 +850,42 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&b->p_full[qt]);
     }
-    // epilogue: O / l
+    // epilogue: O / l over both halves' row sums
     if (!wait_bar(b, &b->o_done[qt], ou & 1)) { fail(b, a.err); return; }
     ++ou;
     tc::tc_fence_after();
-    const float inv = (l > 0.f) ? 1.f / l : 0.f;
+    xch[h * kM + t] = l;
+    pair_sync(qt);
+    const float l_all = l + xch[(1 - h) * kM + t];
+    pair_sync(qt);  // both have read before either writes the next tile's maximum
+    const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
     const int64_t slot = ((int64_t)(un.part < 0 ? 0 : un.part) * kQTiles + qt) * kM + t;
 #pragma unroll 1
-    for (int q4 = 0; q4 < 4; ++q4) {
+    for (int q4 = 0; q4 < 2; ++q4) {
       uint32_t r[32];
       tc::tmem_ld32(tO + q4 * 32, r);
       tc::tmem_ld_wait();
       tc::reg_fence<32>(r);
       if (!row_ok) continue;
+      const int col = 64 * h + 32 * q4;
       if (un.part < 0) {
-        uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)row * a.Hq + hq) * kD + q4 * 32);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + ((int64_t)row * a.Hq + hq) * kD + col);
 #pragma unroll
-        for (int k = 0; k < 4; ++k)
-          dst[k] = make_uint4(pack_bf16x2(u2f(r[8 * k]) * inv, u2f(r[8 * k + 1]) * inv),
-                              pack_bf16x2(u2f(r[8 * k + 2]) * inv, u2f(r[8 * k + 3]) * inv),
-                              pack_bf16x2(u2f(r[8 * k + 4]) * inv, u2f(r[8 * k + 5]) * inv),
-                              pack_bf16x2(u2f(r[8 * k + 6]) * inv, u2f(r[8 * k + 7]) * inv));
+        for (int k2 = 0; k2 < 4; ++k2)
+          dst[k2] = make_uint4(pack_bf16x2(u2f(r[8 * k2]) * inv, u2f(r[8 * k2 + 1]) * inv),
+                               pack_bf16x2(u2f(r[8 * k2 + 2]) * inv, u2f(r[8 * k2 + 3]) * inv),
+                               pack_bf16x2(u2f(r[8 * k2 + 4]) * inv, u2f(r[8 * k2 + 5]) * inv),
+                               pack_bf16x2(u2f(r[8 * k2 + 6]) * inv, u2f(r[8 * k2 + 7]) * inv));
       } else {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kD + q4 * 32);
+        float4* dst = reinterpret_cast<float4*>(a.part_o + slot * kD + col);
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          dst[k] = make_float4(u2f(r[4 * k]) * inv, u2f(r[4 * k + 1]) * inv, u2f(r[4 * k + 2]) * inv,
-                               u2f(r[4 * k + 3]) * inv);
+        for (int k2 = 0; k2 < 8; ++k2)
+          dst[k2] = make_float4(u2f(r[4 * k2]) * inv, u2f(r[4 * k2 + 1]) * inv, u2f(r[4 * k2 + 2]) * inv,
+                                u2f(r[4 * k2 + 3]) * inv);
       }
     }
     tc::tc_fence_before();
-    if (row_ok && un.part >= 0) a.part_ml[slot] = make_float2(m_ref, l);
+    if (h == 0 && row_ok && un.part >= 0) a.part_ml[slot] = make_float2(m_ref, l_all);
   }
 }
 
@@ -900,7 +893,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const TcArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  // the operand layouts need 1024-byte alignment and there is no room for slack
+  if (tc::smem_addr(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_err(a.err, PIC_ERR_UNSUPPORTED);
+    return;
+  }
+  uint8_t* smem = smem_raw;
   Bars* b = reinterpret_cast<Bars*>(smem + kOffBar);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -913,7 +911,7 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mbar_init(&b->q_full[i], 1);
       tc::mbar_init(&b->q_free[i], 1);
       tc::mbar_init(&b->s_full[i], 1);
-      tc::mbar_init(&b->p_full[i], 4);
+      tc::mbar_init(&b->p_full[i], 8);  // every warp of the Q tile's two softmax warpgroups
       tc::mbar_init(&b->o_done[i], 1);
     }
     tc::mbar_init(&b->drain, 1);
@@ -952,7 +950,8 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     }
   } else {
     tc::regs_inc<kRegsHigh>();
-    softmax_loop(a, smem, b, tmem, n_units, (warp - 4) / 4);
+    const int g = (warp - 4) / 4;  // softmax warpgroup: Q tile g / 2, key columns 64 (g % 2) ..
+    softmax_loop(a, smem, b, tmem, n_units, g / 2, g % 2);
   }
   tc::tc_fence_before();
   __syncthreads();
