@@ -22,7 +22,7 @@ Sources (page title, then section):
           correctness checks" (chenhuiyu.github.io), section on the offset
           causal mask: allowed[i, j] = [j <= P + i].
 
-Readings where the pages are silent or garbled (all restated in the design doc):
+Readings where the pages are silent or garbled:
   * RoPE pairs dimension i with i + d/2 (HF Llama "rotate half", [ROPE] fn. 3);
     no frequency scaling.
   * A chunk compiled at local positions 0..L-1 and placed at start s_c is moved
