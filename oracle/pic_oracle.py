@@ -241,3 +241,30 @@ def link_request(chunks_k, chunks_v, q, k, q_raw, k_new_raw, v_new, theta, dtype
     q_rot = round_to(rope(q_raw, qpos, theta), dtype) if len(rows) else np.zeros((0,) + np.shape(q_raw)[1:])
     out = attention_rows(q_rot, qpos, K, V, scale, which)
     return dict(rows=rows, starts=starts, T=T, K_ctx=K, V_ctx=V, out=out)
+
+
+# ---------------------------------------------------------------------------
+# Decode after link  ([EPIC] the query and decode tokens gather the information;
+# [KVC] single-token cache decode: the new position is encoded, its K/V appended,
+# and its query reads every cached position)
+# ---------------------------------------------------------------------------
+
+def decode_after_link(K_ctx, V_ctx, q_raw, k_raw, v_raw, theta, dtype, scale=None):
+    """One decode row after a link step.
+
+    K_ctx / V_ctx [N][Hkv][d]: the linked context (cached chunks, recomputed rows and
+    query rows at positions 0..N-1, as ``link_request`` returns it).  The new token
+    sits at position P = N: its K is roped at P and stored (rounded to dtype), its V
+    stored, and its Q (roped at P, rounded as every tensor-core operand) attends
+    over keys 0..P.  q_raw [Hq][d], k_raw / v_raw [Hkv][d] (un-roped).
+    Returns out [Hq][d] float64.
+    """
+    N, Hkv, d = K_ctx.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    pos = np.array([N])
+    k_new = round_to(rope(np.asarray(k_raw, np.float64)[None], pos, theta), dtype)
+    K = np.concatenate([K_ctx, k_new], axis=0)
+    V = np.concatenate([V_ctx, round_to(np.asarray(v_raw, np.float64)[None], dtype)], axis=0)
+    q_rot = round_to(rope(np.asarray(q_raw, np.float64)[None], pos, theta), dtype)
+    return attention_rows(q_rot, pos, K, V, scale)[0]

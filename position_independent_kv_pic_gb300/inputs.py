@@ -30,7 +30,7 @@ import torch
 
 PAGE = 16  # tokens per KV page
 
-_STREAMS = ("lens", "order", "q", "kstore", "vstore", "knew", "vnew", "blocks", "qlen")
+_STREAMS = ("lens", "order", "q", "kstore", "vstore", "knew", "vnew", "blocks", "qlen", "decode")
 
 
 @dataclass
@@ -187,6 +187,17 @@ def row_inputs(wl: Workload, n_rows: int):
     kn = r["knew"].standard_normal((n_rows, wl.Hkv, wl.d), dtype=np.float32)
     vn = r["vnew"].standard_normal((n_rows, wl.Hkv, wl.d), dtype=np.float32)
     return _cast(q, wl.dtype), _cast(kn, wl.dtype), _cast(vn, wl.dtype)
+
+
+def decode_inputs(wl: Workload):
+    """Inputs of one decode row per request: Q_raw [n_req][Hq][d], K_raw [n_req][Hkv][d]
+    (not yet position-encoded) and V [n_req][Hkv][d]."""
+    r = _rngs(wl.seed)["decode"]
+    n = len(wl.requests)
+    q = r.standard_normal((n, wl.Hq, wl.d), dtype=np.float32)
+    k = r.standard_normal((n, wl.Hkv, wl.d), dtype=np.float32)
+    v = r.standard_normal((n, wl.Hkv, wl.d), dtype=np.float32)
+    return _cast(q, wl.dtype), _cast(k, wl.dtype), _cast(v, wl.dtype)
 
 
 def block_shuffle(wl: Workload, n_blocks: int) -> np.ndarray:

@@ -408,3 +408,73 @@ def test_mutation_local_query_positions(monkeypatch):
 
     monkeypatch.setattr(O, "query_positions", local)
     _assert_caught(good, _run())
+
+
+# ---------------------------------------------------------------------------
+# Decode after link ([EPIC] decode tokens after the query; [KVC] single-token decode)
+# ---------------------------------------------------------------------------
+
+def _decode_case(dtype, lens, q, k, Hq, Hkv, d, seed):
+    rng = np.random.default_rng(seed)
+    base = 1e4
+    chunks_k = [O.compile_chunk_k(O.round_to(rng.standard_normal((L, Hkv, d)), dtype), base, dtype) for L in lens]
+    chunks_v = [O.round_to(rng.standard_normal((L, Hkv, d)), dtype) for L in lens]
+    n = O.count_rows(np.array(lens), q, k)
+    q_raw = O.round_to(rng.standard_normal((n + 1, Hq, d)), dtype)
+    k_raw = O.round_to(rng.standard_normal((n + 1, Hkv, d)), dtype)
+    v = O.round_to(rng.standard_normal((n + 1, Hkv, d)), dtype)
+    return base, chunks_k, chunks_v, q_raw, k_raw, v, n
+
+
+@pytest.mark.parametrize("dtype", ["fp64", "bf16"])
+def test_decode_after_link_equals_longer_link(dtype):
+    """Decoding one token after a link with q query rows gives the output the same
+    token gets as the last query row of a link with q + 1 query rows."""
+    lens, q, k, Hq, Hkv, d = [6, 9, 4, 7], 3, 2, 4, 2, 16
+    base, ck, cv, q_raw, k_raw, v, n = _decode_case(dtype, lens, q, k, Hq, Hkv, d, seed=21)
+    longer = O.link_request(ck, cv, q + 1, k, q_raw, k_raw, v, base, dtype)
+    link = O.link_request(ck, cv, q, k, q_raw[:n], k_raw[:n], v[:n], base, dtype)
+    assert link["K_ctx"].shape[0] == sum(lens) + q
+    dec = O.decode_after_link(link["K_ctx"], link["V_ctx"], q_raw[n], k_raw[n], v[n], base, dtype)
+    assert np.abs(dec - longer["out"][-1]).max() < 1e-12
+
+
+def test_decode_matches_full_recompute():
+    """With k >= every chunk length the linked context is the fully recomputed one, so
+    the decode row equals the last row of full causal attention over N + 1 tokens
+    (torch SDPA, float64)."""
+    rng = np.random.default_rng(23)
+    lens, q, Hq, Hkv, d, base, dtype = [5, 4, 6], 2, 4, 2, 16, 1e4, "fp64"
+    N = sum(lens) + q
+    q_raw = rng.standard_normal((N + 1, Hq, d))
+    k_raw = rng.standard_normal((N + 1, Hkv, d))
+    v = rng.standard_normal((N + 1, Hkv, d))
+    ck, cv, s = [], [], 0
+    for L in lens:
+        ck.append(O.compile_chunk_k(k_raw[s:s + L], base, dtype))
+        cv.append(v[s:s + L])
+        s += L
+    rows = O.select_rows(lens, q, max(lens))[0]
+    link = O.link_request(ck, cv, q, max(lens), q_raw[rows], k_raw[rows], v[rows], base, dtype)
+    dec = O.decode_after_link(link["K_ctx"], link["V_ctx"], q_raw[N], k_raw[N], v[N], base, dtype)
+    fr = _full_recompute_sdpa(q_raw, k_raw, v, base, dtype, Hq, Hkv)
+    assert np.abs(dec - fr[N]).max() < 1e-12
+
+
+def test_decode_mutations_caught():
+    """A decode that forgets its own K/V, or encodes its query at the last context
+    position instead of its own, moves the output far past the GPU tolerance."""
+    lens, q, k, Hq, Hkv, d = [6, 9, 4, 7], 3, 2, 4, 2, 16
+    base, ck, cv, q_raw, k_raw, v, n = _decode_case("fp64", lens, q, k, Hq, Hkv, d, seed=22)
+    link = O.link_request(ck, cv, q, k, q_raw[:n], k_raw[:n], v[:n], base, "fp64")
+    K, V = link["K_ctx"], link["V_ctx"]
+    good = O.decode_after_link(K, V, q_raw[n], k_raw[n], v[n], base, "fp64")
+    N = K.shape[0]
+    q_rot = O.rope(q_raw[n][None], np.array([N]), base)
+    no_self = O.attention_rows(q_rot, np.array([N - 1]), K, V, 1.0 / math.sqrt(d))[0]
+    q_wrong = O.rope(q_raw[n][None], np.array([N - 1]), base)
+    k_new = O.rope(k_raw[n][None], np.array([N]), base)
+    wrong_pos = O.attention_rows(q_wrong, np.array([N]), np.concatenate([K, k_new]), np.concatenate([V, v[n][None]]),
+                                 1.0 / math.sqrt(d))[0]
+    for bad in (no_self, wrong_pos):
+        assert np.abs(bad - good).max() > 10 * 2e-2 or np.abs(bad - good).mean() > 10 * 2e-3
