@@ -233,6 +233,28 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
 
+    # decode after the link (one new row per request over the linked cache): its own
+    # timed loop after the link step's, L2 flushed before every step
+    dec = None
+    if wl.dtype == "bf16" and pic.pic_decode_workspace(batch.n_req, wl.Hq, wl.Hkv, wl.d, batch.pic_dtype) > 0:
+        batch.setup_decode()
+        for _ in range(args.warmup):
+            batch.run_decode()
+        torch.cuda.synchronize()
+        Kd = max(3, min(K, 50))
+        dstep = [(ev(), ev()) for _ in range(Kd)]
+        datt = [(ev(), ev()) for _ in range(Kd)]
+        for i in range(Kd):
+            flush.zero_()
+            dstep[i][0].record(stream)
+            batch.run_decode(marks={"decode": datt[i]})
+            dstep[i][1].record(stream)
+        torch.cuda.synchronize()
+        if batch.error() != 0:
+            raise SystemExit(f"device error: {pic.pic_strerror(batch.error())}")
+        dec = (statistics.mean(a.elapsed_time(b) for a, b in dstep),
+               statistics.mean(a.elapsed_time(b) for a, b in datt), batch.dec_bytes, Kd)
+
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
     att_avg = statistics.mean(att_ms)
     rot_avg = statistics.mean(rot_ms)
@@ -261,6 +283,11 @@ def run_gpu(args, rank, world):
             "attention": {"bound": "tensor", "achieved": att_tflops, "peak": tf_burst, "unit": "TFLOP/s",
                           "frac": att_tflops / tf_burst, "ms": att_avg, "traffic": traffic,
                           "frac_of_sustained": att_tflops / tf_sus if tf_sus else None},
+            **({"decode": {"bound": "hbm", "achieved": dec[2] / (dec[1] / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                           "frac": dec[2] / (dec[1] / 1e3) / 1e9 / hbm, "ms": dec[1], "ms_per_decode_step": dec[0],
+                           "algorithmic_bytes": dec[2], "steps": dec[3],
+                           "kernel": "pic_decode_attention (split-KV decode + merge), one new row per request; "
+                                     "the step adds its RoPE table and K/V write"}} if dec else {}),
             "rerotate": {"bound": "hbm", "achieved": rot_gbs, "peak": hbm, "unit": "GB/s", "frac": rot_gbs / hbm,
                          "ms": rot_avg, "traffic": rtraffic, "algorithmic_bytes": rot_bytes,
                          "frac_of_8tbs": rot_gbs / 8000.0},

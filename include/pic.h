@@ -308,6 +308,39 @@ pic_status pic_link_attention_noalloc(const void* q, const float* row_table, con
                                       int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Decode after link (EPIC review: the query and the tokens decoded after it
+ * gather the information of all chunks; "KV cache from scratch", single-token
+ * cache decode: a new position reads the whole cache once).
+ * ------------------------------------------------------------------------
+ * One new query row per request, at position P_r, attends over the keys listed
+ * in the request's page list (every listed key is visible: the list holds the
+ * linked context, the recomputed rows and the new row's own K/V, which the caller
+ * wrote first with pic_write_fresh_kv):
+ *   out[r][h] = softmax_j(RoPE(q[r][h], P_r) . K_j[h / g] * scale) . V_j[h / g]
+ * with RoPE(q) rounded to bf16 as on the link path.
+ *   q         [n_req][Hq][d] bf16, un-roped
+ *   q_table   [n_req][d/2][4] fp32: pic_rope_table over the positions P_r
+ *   k_pool, v_pool, num_blocks, pages, page_off: as pic_link_attention (the
+ *             lo/hi slot range of every page entry is honoured; gpos0 is unused)
+ *   out       [n_req][Hq][d] bf16
+ *   ws        at least pic_decode_workspace() bytes, 256-byte aligned, any contents
+ * bf16 pools with d = 128 and g = Hq / Hkv in {1, 2, 4, 8}; otherwise
+ * PIC_ERR_UNSUPPORTED (0 from pic_decode_workspace).  Three launches: a one-block
+ * planner gives every request splits in proportion to its pages so that all
+ * CTAs fit in one wave, the split-KV decode (pages streamed through shared
+ * memory by bulk copies), and the merge of the splits.  Bound by HBM: every
+ * listed K and V row is read once.  A bad block id or slot range sets
+ * PIC_ERR_RANGE in *err_flag and that page is skipped; a bounded wait that runs
+ * out sets PIC_ERR_TIMEOUT. */
+size_t pic_decode_workspace(int32_t n_req, int32_t Hq, int32_t Hkv, int32_t d, pic_dtype dtype);
+
+pic_status pic_decode_attention(const void* q, const float* q_table, const void* k_pool,
+                                const void* v_pool, int64_t num_blocks, pic_dtype dtype,
+                                const pic_link_page* pages, const int32_t* page_off, int32_t n_req,
+                                int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out, void* ws,
+                                size_t ws_bytes, int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------
  * One 128 x 128 x 128 bf16 tensor-core product through the same shared-memory

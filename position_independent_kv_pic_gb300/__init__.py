@@ -23,6 +23,7 @@ __all__ = [
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
+    "pic_decode_workspace", "pic_decode_attention",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -45,7 +46,7 @@ EXPORTED = (
     "pic_count_rows", "pic_request_sizes_of", "pic_plan_offsets", "pic_strerror",
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
-    "pic_selftest_umma", "pic_link_attention_noalloc",
+    "pic_selftest_umma", "pic_link_attention_noalloc", "pic_decode_workspace", "pic_decode_attention",
 )
 
 
@@ -86,6 +87,9 @@ _SIGS = {
     "pic_selftest_umma": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
     "pic_link_attention_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
                                                   _I64, _I32, _I32, _I32, _F32, _P, _P, _P]),
+    "pic_decode_workspace": (_SZ, [_I32, _I32, _I32, _I32, ctypes.c_int]),
+    "pic_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32, _I32, _I32, _I32,
+                                            _F32, _P, _P, _SZ, _P, _P]),
 }
 
 
@@ -209,6 +213,19 @@ def pic_link_attention(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, 
         _ptr(q), _ptr(row_table), _ptr(rows), _ptr(row_off), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype),
         _ptr(pages), _ptr(page_off), int(n_req), int(n_rows), int(Hq), int(Hkv), int(d), float(scale), _ptr(out),
         _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)), "pic_link_attention")
+
+
+def pic_decode_workspace(n_req: int, Hq: int, Hkv: int, d: int, dtype: int) -> int:
+    return int(load().pic_decode_workspace(int(n_req), int(Hq), int(Hkv), int(d), int(dtype)))
+
+
+def pic_decode_attention(q, q_table, k_pool, v_pool, dtype: int, pages, page_off, n_req: int, Hq: int, Hkv: int,
+                         d: int, scale: float, out, ws, err_flag, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pic_decode_attention(
+        _ptr(q), _ptr(q_table), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype), _ptr(pages), _ptr(page_off),
+        int(n_req), int(Hq), int(Hkv), int(d), float(scale), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),
+        _stream(stream)), "pic_decode_attention")
 
 
 def pic_selftest_umma(a, b, d_kmajor, d_mnmajor, d_tmem_a, err_flag, stream=None):

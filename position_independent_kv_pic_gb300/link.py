@@ -18,10 +18,10 @@ import math
 import numpy as np
 import torch
 
-from . import (PIC_BF16, PIC_FP32, PIC_PAGE, pic_link_attention, pic_link_attention_workspace,
-               pic_plan_offsets, pic_rerotate_k, pic_rope_table, pic_select_rows, pic_splice_pages,
-               pic_write_fresh_kv)
-from .inputs import Workload, block_shuffle, chunk_store, row_inputs
+from . import (PIC_BF16, PIC_FP32, PIC_PAGE, pic_decode_attention, pic_decode_workspace, pic_link_attention,
+               pic_link_attention_workspace, pic_plan_offsets, pic_rerotate_k, pic_rope_table, pic_select_rows,
+               pic_splice_pages, pic_write_fresh_kv)
+from .inputs import Workload, block_shuffle, chunk_store, decode_inputs, row_inputs
 
 
 def _cdiv(a, b):
@@ -64,8 +64,11 @@ class LinkBatch:
         n_store_pages = int(store_base[-1])
         n_chunk_pages = int(offs["chunk_page_off"][-1])
         n_dst = n_chunk_pages if wl.out_of_place else 0
-        self.num_blocks = n_store_pages + n_dst + self.n_fresh
-        perm = block_shuffle(wl, self.num_blocks).astype(np.int64)
+        n_link_blocks = n_store_pages + n_dst + self.n_fresh
+        # one more block per request takes the row a decode step appends after the link
+        self.decode_blocks = np.arange(n_link_blocks, n_link_blocks + self.n_req, dtype=np.int32)
+        self.num_blocks = n_link_blocks + self.n_req
+        perm = block_shuffle(wl, n_link_blocks).astype(np.int64)
         self.store_blocks = [perm[store_base[c]:store_base[c + 1]] for c in range(len(store_np))]
         k_src = np.concatenate([self.store_blocks[c] for c in flat_ids]) if len(flat_ids) else np.zeros(0, np.int64)
         self.k_src = k_src.astype(np.int32)
@@ -191,6 +194,58 @@ class LinkBatch:
                            wl.d, self.scale, self.out, self.ws, self.err, stream)
         if "attention" in mk:
             mk["attention"][1].record()
+
+    # ------------------------------------------------------------------ decode after the link
+    def setup_decode(self):
+        """Inputs and page lists of one decode row per request, at position T_r + q_r right
+        after the request's query rows.  Call after run() has built the link page list: a
+        request's decode page list is its link pages followed by one page holding the new
+        row (a serving engine keeps this list; building it is not part of the step)."""
+        wl, dev, i32 = self.wl, self.device, torch.int32
+        q, k, v = decode_inputs(wl)
+        self.dec_q, self.dec_k, self.dec_v = q.to(dev), k.to(dev), v.to(dev)
+        pos = np.array([int(wl.chunk_lens[r.chunk_ids].sum()) + r.q for r in wl.requests], np.int32)
+        self.dec_pos_h = pos
+        self.dec_pos = torch.from_numpy(pos).to(dev)
+        self.dec_block = torch.from_numpy(self.decode_blocks).to(dev)
+        self.dec_slot = torch.zeros(self.n_req, dtype=i32, device=dev)
+        po = self.offs["page_off"].astype(np.int64)
+        src, new_off = [], np.zeros(self.n_req + 1, np.int32)
+        for r in range(self.n_req):
+            src += list(range(po[r], po[r + 1])) + [-1]
+            new_off[r + 1] = len(src)
+        src = np.array(src, np.int64)
+        pages = self.pages[torch.from_numpy(np.maximum(src, 0)).to(dev)].clone()
+        extra = np.flatnonzero(src < 0)
+        ent = np.stack([self.decode_blocks, self.decode_blocks, pos, np.full(self.n_req, 1 << 16, np.int32)], 1)
+        pages[torch.from_numpy(extra).to(dev)] = torch.from_numpy(ent.astype(np.int32)).to(dev)
+        self.dec_pages = pages
+        self.dec_page_off = torch.from_numpy(new_off).to(dev)
+        self.dec_table = torch.empty((self.n_req, wl.d // 2, 4), dtype=torch.float32, device=dev)
+        self.dec_out = torch.empty((self.n_req, wl.Hq, wl.d), dtype=self.dtype, device=dev)
+        ws = pic_decode_workspace(self.n_req, wl.Hq, wl.Hkv, wl.d, self.pic_dtype)
+        self.dec_ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws > 0 else None
+        # HBM bytes a decode step must read: every listed valid K and V row, plus Q and out
+        lohi = self.dec_pages[:, 3].cpu().numpy()
+        slots = int(((lohi >> 16) - (lohi & 0xffff)).clip(min=0).sum())
+        elt = 2 if self.dtype == torch.bfloat16 else 4
+        self.dec_bytes = 2 * slots * wl.Hkv * wl.d * elt + 2 * self.n_req * wl.Hq * wl.d * elt
+
+    def run_decode(self, stream=None, marks=None):
+        """One decode step: the new rows' RoPE table, their K/V written into the decode
+        blocks, and the decode attention (split-KV + merge).  ``marks`` may map "decode" to
+        (start, end) events recorded around the attention call."""
+        wl, mk = self.wl, marks or {}
+        pic_rope_table(self.dec_pos, wl.d, wl.theta, self.dec_table, stream)
+        pic_write_fresh_kv(self.k_pool, self.v_pool, self.pic_dtype, wl.Hkv, wl.d, self.dec_k, self.dec_v,
+                           self.dec_table, self.dec_block, self.dec_slot, self.n_req, self.err, stream)
+        if "decode" in mk:
+            mk["decode"][0].record()
+        pic_decode_attention(self.dec_q, self.dec_table, self.k_pool, self.v_pool, self.pic_dtype, self.dec_pages,
+                             self.dec_page_off, self.n_req, wl.Hq, wl.Hkv, wl.d, self.scale, self.dec_out, self.dec_ws,
+                             self.err, stream)
+        if "decode" in mk:
+            mk["decode"][1].record()
 
     # ------------------------------------------------------------------ read-back helpers (tests)
     def error(self) -> int:

@@ -1,0 +1,77 @@
+"""Decode after link: the CUDA decode step (through the C ABI) against the float64
+oracle's decode_after_link over the oracle's own linked context."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.pic_oracle as O
+import position_independent_kv_pic_gb300 as pic
+from position_independent_kv_pic_gb300 import build as pic_build
+from position_independent_kv_pic_gb300 import inputs
+from position_independent_kv_pic_gb300.link import LinkBatch
+
+from parity_util import TOL_MAX, TOL_MEAN, oracle_request
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    pic_build.build()
+    pic.load()
+
+
+def _decode(wl):
+    b = LinkBatch(wl)
+    b.run()
+    torch.cuda.synchronize()
+    assert b.error() == 0, pic.pic_strerror(b.error())
+    b.setup_decode()
+    b.run_decode()
+    torch.cuda.synchronize()
+    assert b.error() == 0, pic.pic_strerror(b.error())
+    return b
+
+
+def _check(b, reqs):
+    wl = b.wl
+    got = b.dec_out.double().cpu().numpy()
+    dq, dk, dv = (t.double().numpy() for t in inputs.decode_inputs(wl))
+    errs = []
+    for r in reqs:
+        link = oracle_request(b, r, which=[])
+        assert link["K_ctx"].shape[0] == b.dec_pos_h[r]
+        expect = O.decode_after_link(link["K_ctx"], link["V_ctx"], dq[r], dk[r], dv[r], wl.theta, wl.dtype)
+        errs.append(np.abs(got[r] - expect))
+    e = np.concatenate([x.ravel() for x in errs])
+    return float(e.max()), float(e.mean())
+
+
+@pytest.mark.parametrize("preset", ["rag_prompt_6chunks", "many_chunk_sink_20", "long_context_100x1000"])
+def test_decode_single_request(preset):
+    b = _decode(inputs.PRESETS[preset]())
+    emax, emean = _check(b, [0])
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
+def test_decode_batched_sampled():
+    b = _decode(inputs.batched_shared())
+    emax, emean = _check(b, [0, 7, 15])
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
+@pytest.mark.parametrize("Hq", [8, 16, 32, 64])
+def test_decode_gqa_groups(Hq):
+    wl = inputs.custom([[130, 70, 45], [55, 8, 200]], [20, 1], [2, 16], Hq=Hq, Hkv=8, d=128, theta=5e5,
+                       dtype="bf16", seed=60 + Hq)
+    b = _decode(wl)
+    emax, emean = _check(b, [0, 1])
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
+def test_decode_unsupported_shape_is_refused():
+    assert pic.pic_decode_workspace(1, 4, 2, 16, pic.PIC_FP32) == 0
+    assert pic.pic_decode_workspace(1, 32, 8, 128, pic.PIC_BF16) > 0
