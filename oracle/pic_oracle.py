@@ -166,12 +166,22 @@ def query_positions(rows, starts, T):
 # Splice and attention  ([EPIC] Step 3; [HYPIC] 2.2)
 # ---------------------------------------------------------------------------
 
-def splice_context(chunks_k, chunks_v, q, k, k_new_raw, v_new, theta, dtype):
+def rope_cached_k(k_nope, start: int, theta: float, dtype: str) -> np.ndarray:
+    """Scheme B ([ROPE] 3.2): a chunk's K cached without its position encoding is
+    encoded on use at its global positions start + j, then stored (rounded once)."""
+    k_nope = np.asarray(k_nope, np.float64)
+    return round_to(rope(k_nope, start + np.arange(k_nope.shape[0]), theta), dtype)
+
+
+def splice_context(chunks_k, chunks_v, q, k, k_new_raw, v_new, theta, dtype, scheme="rotary"):
     """Build the spliced K/V of one request at global positions.
 
-    Cached chunks are concatenated in link order; chunk c's K is re-rotated by
-    Delta_c = s_c; then the recomputed rows' fresh K (roped at their global
-    position) and fresh V overwrite / append at their positions.
+    Cached chunks are concatenated in link order.  scheme "rotary" (rotary
+    correction, [ROPE] 3.3): chunk c's K was cached encoded at local positions and
+    is re-rotated by Delta_c = s_c.  scheme "nope" (scheme B, [ROPE] 3.2): chunk
+    c's K was cached without position encoding and is encoded at s_c + j.  Then
+    the recomputed rows' fresh K (roped at their global position) and fresh V
+    overwrite / append at their positions.
 
     Returns (K_ctx, V_ctx, rows, starts, T) with K_ctx, V_ctx float64 [T+q][Hkv][d].
     """
@@ -183,7 +193,12 @@ def splice_context(chunks_k, chunks_v, q, k, k_new_raw, v_new, theta, dtype):
     V = np.zeros((N, Hkv, d), np.float64)
     for c, (kc, vc) in enumerate(zip(chunks_k, chunks_v)):
         s = int(starts[c])
-        K[s:s + lens[c]] = rerotate_k(kc, s, theta, dtype)
+        if scheme == "rotary":
+            K[s:s + lens[c]] = rerotate_k(kc, s, theta, dtype)
+        elif scheme == "nope":
+            K[s:s + lens[c]] = rope_cached_k(kc, s, theta, dtype)
+        else:
+            raise ValueError(scheme)
         V[s:s + lens[c]] = np.asarray(vc, np.float64)
     if len(rows):
         K[rows] = round_to(rope(k_new_raw, rows, theta), dtype)
@@ -224,7 +239,7 @@ def attention_rows(q_rot, q_pos, K_ctx, V_ctx, scale, which=None) -> np.ndarray:
 
 
 def link_request(chunks_k, chunks_v, q, k, q_raw, k_new_raw, v_new, theta, dtype,
-                 scale=None, which=None):
+                 scale=None, which=None, scheme="rotary"):
     """The whole link step of one request.
 
     chunks_k / chunks_v: lists of stored per-chunk K / V, each [L_c][Hkv][d]
@@ -233,7 +248,7 @@ def link_request(chunks_k, chunks_v, q, k, q_raw, k_new_raw, v_new, theta, dtype
     Returns dict(rows, starts, T, K_ctx, V_ctx, out) with out float64 [n_sel][Hq][d].
     """
     K, V, rows, starts, T = splice_context(chunks_k, chunks_v, q, k, k_new_raw, v_new,
-                                           theta, dtype)
+                                           theta, dtype, scheme)
     d = K.shape[2]
     if scale is None:
         scale = 1.0 / math.sqrt(d)

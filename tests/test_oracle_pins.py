@@ -478,3 +478,83 @@ def test_decode_mutations_caught():
                                  1.0 / math.sqrt(d))[0]
     for bad in (no_self, wrong_pos):
         assert np.abs(bad - good).max() > 10 * 2e-2 or np.abs(bad - good).mean() > 10 * 2e-3
+
+
+# ---------------------------------------------------------------------------
+# Scheme B ([ROPE] 3.2): K cached without position encoding, encoded on use
+# ---------------------------------------------------------------------------
+
+def _scheme_case(dtype, lens, q, k, Hq, Hkv, d, seed):
+    rng = np.random.default_rng(seed)
+    nope = [O.round_to(rng.standard_normal((L, Hkv, d)), dtype) for L in lens]
+    cv = [O.round_to(rng.standard_normal((L, Hkv, d)), dtype) for L in lens]
+    n = O.count_rows(np.array(lens), q, k)
+    q_raw = O.round_to(rng.standard_normal((n, Hq, d)), dtype)
+    k_raw = O.round_to(rng.standard_normal((n, Hkv, d)), dtype)
+    v = O.round_to(rng.standard_normal((n, Hkv, d)), dtype)
+    return nope, cv, q_raw, k_raw, v
+
+
+def test_scheme_b_equals_rotary_correction_exactly():
+    """In exact arithmetic, caching K un-encoded and encoding it at s_c + j gives the
+    same context and outputs as caching it encoded at j and rotating by s_c."""
+    lens, q, k, Hq, Hkv, d, base = [7, 12, 5, 9], 4, 3, 4, 2, 16, 1e4
+    nope, cv, q_raw, k_raw, v = _scheme_case("fp64", lens, q, k, Hq, Hkv, d, seed=31)
+    compiled = [O.compile_chunk_k(x, base, "fp64") for x in nope]
+    a = O.link_request(nope, cv, q, k, q_raw, k_raw, v, base, "fp64", scheme="nope")
+    b = O.link_request(compiled, cv, q, k, q_raw, k_raw, v, base, "fp64", scheme="rotary")
+    assert np.abs(a["K_ctx"] - b["K_ctx"]).max() < 1e-12
+    assert np.abs(a["out"] - b["out"]).max() < 1e-12
+
+
+def test_scheme_b_full_recompute():
+    """With k >= every chunk length, scheme B's link equals full causal attention
+    over the whole sequence (torch SDPA, float64)."""
+    rng = np.random.default_rng(32)
+    lens, q, Hq, Hkv, d, base = [5, 4, 6], 3, 4, 2, 16, 1e4
+    N = sum(lens) + q
+    q_raw = rng.standard_normal((N, Hq, d))
+    k_raw = rng.standard_normal((N, Hkv, d))
+    v = rng.standard_normal((N, Hkv, d))
+    nope, cv, s = [], [], 0
+    for L in lens:
+        nope.append(k_raw[s:s + L])
+        cv.append(v[s:s + L])
+        s += L
+    rows = O.select_rows(lens, q, max(lens))[0]
+    res = O.link_request(nope, cv, q, max(lens), q_raw[rows], k_raw[rows], v[rows], base, "fp64", scheme="nope")
+    fr = _full_recompute_sdpa(q_raw, k_raw, v, base, "fp64", Hq, Hkv)
+    assert np.abs(res["out"] - fr[rows]).max() < 1e-12
+
+
+def test_scheme_b_bf16_close_to_rotary():
+    """In bf16, scheme B rounds once (RoPE at the global position) where rotary
+    correction rounds twice (at the local position, then after the rotation).  A
+    rotation keeps the norm of each dimension pair, so the two contexts differ by
+    at most a few roundings of that norm: |a - b| <= 2^-7 |pair| per element."""
+    lens, q, k, Hq, Hkv, d, base = [40, 33, 21], 2, 4, 4, 2, 32, 1e4
+    nope, cv, q_raw, k_raw, v = _scheme_case("bf16", lens, q, k, Hq, Hkv, d, seed=33)
+    compiled = [O.compile_chunk_k(x, base, "bf16") for x in nope]
+    Ka = O.splice_context(nope, cv, q, k, k_raw, v, base, "bf16", "nope")[0]
+    Kb = O.splice_context(compiled, cv, q, k, k_raw, v, base, "bf16", "rotary")[0]
+    h = d // 2
+    norm = np.sqrt(Ka[..., :h] ** 2 + Ka[..., h:] ** 2)
+    norm = np.concatenate([norm, norm], axis=-1)
+    assert (np.abs(Ka - Kb) <= 2.0 ** -7 * norm + 1e-30).all()
+    assert np.abs(Ka - Kb).max() > 0  # the roundings do differ somewhere
+
+
+def test_scheme_b_mutation_unencoded_chunk0_caught(monkeypatch):
+    """Scheme B must encode chunk 0 as well (it is cached un-encoded): leaving it as
+    cached moves the output far past the GPU tolerance."""
+    lens, q, k, Hq, Hkv, d, base = [9, 7, 8], 3, 2, 4, 2, 16, 1e4
+    nope, cv, q_raw, k_raw, v = _scheme_case("fp64", lens, q, k, Hq, Hkv, d, seed=34)
+    good = O.link_request(nope, cv, q, k, q_raw, k_raw, v, base, "fp64", scheme="nope")["out"]
+    real = O.rope_cached_k
+
+    def skip_chunk0(k_nope, start, theta, dtype):
+        return np.asarray(k_nope, np.float64) if start == 0 else real(k_nope, start, theta, dtype)
+
+    monkeypatch.setattr(O, "rope_cached_k", skip_chunk0)
+    bad = O.link_request(nope, cv, q, k, q_raw, k_raw, v, base, "fp64", scheme="nope")["out"]
+    assert np.abs(bad - good).max() > 10 * 2e-2 or np.abs(bad - good).mean() > 10 * 2e-3
