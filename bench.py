@@ -255,6 +255,33 @@ def run_gpu(args, rank, world):
         dec = (statistics.mean(a.elapsed_time(b) for a, b in dstep),
                statistics.mean(a.elapsed_time(b) for a, b in datt), batch.dec_bytes, Kd)
 
+    # scheme B (chunks cached without position encoding, encoded at the global
+    # position by the step): the same step with pic_rope_cached_k in place of the
+    # offset table and the re-rotation; in place only
+    schb = None
+    if not wl.out_of_place:
+        bb = LinkBatch(wl, scheme="nope")
+        for _ in range(args.warmup):
+            bb.run()
+        torch.cuda.synchronize()
+        Kb = max(3, min(K, 50))
+        bstep = [(ev(), ev()) for _ in range(Kb)]
+        brope = [(ev(), ev()) for _ in range(Kb)]
+        for i in range(Kb):
+            flush.zero_()
+            bstep[i][0].record(stream)
+            bb.run(marks={"rerotate": brope[i]})
+            bstep[i][1].record(stream)
+        torch.cuda.synchronize()
+        if bb.error() != 0:
+            raise SystemExit(f"device error (scheme B): {pic.pic_strerror(bb.error())}")
+        kept = int(bb.chunk_lens.sum()) - (bb.n_rows - int(bb.q_len.sum()))  # cached slots encoded
+        rope_bytes = 2 * kept * wl.Hkv * wl.d * el + kept * (wl.d // 2) * 16  # K read + write, table rows
+        schb = (statistics.mean(a.elapsed_time(b) for a, b in bstep),
+                statistics.mean(a.elapsed_time(b) for a, b in brope), rope_bytes, Kb, bb.tokens)
+        del bb
+        torch.cuda.empty_cache()
+
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
     att_avg = statistics.mean(att_ms)
     rot_avg = statistics.mean(rot_ms)
@@ -288,6 +315,13 @@ def run_gpu(args, rank, world):
                            "algorithmic_bytes": dec[2], "steps": dec[3],
                            "kernel": "pic_decode_attention (split-KV decode + merge), one new row per request; "
                                      "the step adds its RoPE table and K/V write"}} if dec else {}),
+            **({"scheme_b": {"bound": "hbm", "achieved": schb[2] / (schb[1] / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
+                             "frac": schb[2] / (schb[1] / 1e3) / 1e9 / hbm, "ms": schb[1],
+                             "algorithmic_bytes": schb[2], "ms_per_step": schb[0],
+                             "tokens_per_s": world * schb[4] / (schb[0] / 1e3), "steps": schb[3],
+                             "kernel": "pic_rope_cached_k (scheme B: cached K encoded at its global position; "
+                                       "bytes = K read + written + one table row per slot); the step runs "
+                                       "without the offset table and the re-rotation"}} if schb else {}),
             "rerotate": {"bound": "hbm", "achieved": rot_gbs, "peak": hbm, "unit": "GB/s", "frac": rot_gbs / hbm,
                          "ms": rot_avg, "traffic": rtraffic, "algorithmic_bytes": rot_bytes,
                          "frac_of_8tbs": rot_gbs / 8000.0},
@@ -295,7 +329,7 @@ def run_gpu(args, rank, world):
         "e2e": {"value": world * tokens / (e2e_ms / 1e3), "unit": UNIT, "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": batch.h2d_bytes(), "d2h_bytes_per_step": batch.d2h_bytes()},
         "clocks": clocks.summary(),
-        "gpu_launches": K * batch.LAUNCHES_PER_STEP,
+        "gpu_launches": K * batch.launches_per_step,
         "wall_s_timed_region": t_wall,
     }
     return result, batch

@@ -221,6 +221,33 @@ pic_status pic_rerotate_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int
                           int64_t n_tab, int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * a3' Scheme B (RoPE article 3.2): the cached chunks hold K WITHOUT position
+ *     encoding; on link every kept cached slot is encoded at its global
+ *     position: slot s of page j of chunk c <- RoPE(K, s_c + 16 j + s), fp32 math,
+ *     one rounding to the pool dtype.  Chunk 0 is encoded too (at 0..L_0 - 1).
+ *     Replaces the offset table and pic_rerotate_k of the rotary correction.
+ * ------------------------------------------------------------------------
+ *   k_pool            [num_blocks][Hkv][16][d] (read and written)
+ *   chunk_lens, chunk_off, k, n_req, chunk_start: as pic_select_rows (chunk_start
+ *                     is its output)
+ *   chunk_page_off    [n_chunks+1], n_chunk_pages = chunk_page_off[n_chunks] (host)
+ *   k_src_blocks      [n_chunk_pages] block of each cached page
+ *   k_dst_blocks      [n_chunk_pages] destination, or NULL for in place.  The page
+ *                     list of pic_splice_pages reads chunk 0 from k_src_blocks, so
+ *                     a link over shared chunks must run in place on private copies
+ *   pos_table         [n_pos][d/2][4]: pic_rope_table over positions 0..n_pos-1
+ *                     (a per-model table; every encoded position must be < n_pos)
+ * Slots [0, min(k, L_c)) of chunks after the first (recomputed rows) are left
+ * alone.  Device errors: PIC_ERR_RANGE (block id, or a position >= n_pos).
+ * Supported: as pic_rerotate_k. */
+pic_status pic_rope_cached_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int32_t Hkv, int32_t d,
+                             const int32_t* chunk_lens, const int32_t* chunk_off, const int32_t* k,
+                             int32_t n_req, const int32_t* chunk_start, const int32_t* chunk_page_off,
+                             int32_t n_chunks, int64_t n_chunk_pages, const int32_t* k_src_blocks,
+                             const int32_t* k_dst_blocks, const float* pos_table, int64_t n_pos,
+                             int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * a4  Fresh K/V of the recomputed rows (EPIC Step 3: the new K/V replace the
  *     cached slots / append the query): K <- RoPE(k_raw[i], p_i) rounded to the
  *     pool dtype, V <- v_raw[i], written to slot row_slot[i] of block

@@ -23,7 +23,7 @@ __all__ = [
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
-    "pic_decode_workspace", "pic_decode_attention",
+    "pic_decode_workspace", "pic_decode_attention", "pic_rope_cached_k",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -47,6 +47,7 @@ EXPORTED = (
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "pic_decode_workspace", "pic_decode_attention",
+    "pic_rope_cached_k",
 )
 
 
@@ -88,6 +89,8 @@ _SIGS = {
     "pic_link_attention_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
                                                   _I64, _I32, _I32, _I32, _F32, _P, _P, _P]),
     "pic_decode_workspace": (_SZ, [_I32, _I32, _I32, _I32, ctypes.c_int]),
+    "pic_rope_cached_k": (ctypes.c_int, [_P, _I64, ctypes.c_int, _I32, _I32, _P, _P, _P, _I32, _P, _P, _I32, _I64,
+                                         _P, _P, _P, _I64, _P, _P]),
     "pic_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32, _I32, _I32, _I32,
                                             _F32, _P, _P, _SZ, _P, _P]),
 }
@@ -213,6 +216,15 @@ def pic_link_attention(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, 
         _ptr(q), _ptr(row_table), _ptr(rows), _ptr(row_off), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype),
         _ptr(pages), _ptr(page_off), int(n_req), int(n_rows), int(Hq), int(Hkv), int(d), float(scale), _ptr(out),
         _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)), "pic_link_attention")
+
+
+def pic_rope_cached_k(k_pool, dtype: int, Hkv: int, d: int, chunk_lens, chunk_off, k, n_req: int, chunk_start,
+                      chunk_page_off, n_chunks: int, n_chunk_pages: int, k_src, k_dst, pos_table, err_flag,
+                      stream=None):
+    _check(load().pic_rope_cached_k(
+        _ptr(k_pool), k_pool.shape[0], int(dtype), int(Hkv), int(d), _ptr(chunk_lens), _ptr(chunk_off), _ptr(k),
+        int(n_req), _ptr(chunk_start), _ptr(chunk_page_off), int(n_chunks), int(n_chunk_pages), _ptr(k_src),
+        _ptr(k_dst), _ptr(pos_table), pos_table.shape[0], _ptr(err_flag), _stream(stream)), "pic_rope_cached_k")
 
 
 def pic_decode_workspace(n_req: int, Hq: int, Hkv: int, d: int, dtype: int) -> int:

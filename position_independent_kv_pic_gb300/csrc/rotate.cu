@@ -159,6 +159,95 @@ rerotate_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d,
   }
 }
 
+// Scheme B (article on RoPE and prefix caching, section 3.2): a chunk's K cached
+// without its position encoding is encoded on link at its global positions: slot
+// s of page j of chunk c gets RoPE at s_c + 16 j + s, from a table with one row
+// per position.  The work items are the rotation kernel's; the page's chunk and
+// request come from binary searches over the page and chunk offsets, and the kept
+// slots are those not recomputed (the first min(k, L_c) rows of every chunk after
+// the first are replaced by fresh rows).
+template <typename T>
+__global__ void __launch_bounds__(kRotThreads, 4)
+rope_cached_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d, const int32_t* __restrict__ chunk_lens,
+                   const int32_t* __restrict__ chunk_off, const int32_t* __restrict__ kk, int n_req,
+                   const int32_t* __restrict__ chunk_start, const int32_t* __restrict__ chunk_page_off,
+                   int n_chunks, int64_t n_cpages, const int32_t* __restrict__ k_src,
+                   const int32_t* __restrict__ k_dst, const float4* __restrict__ table, int64_t n_pos,
+                   int32_t* err) {
+  constexpr int N = Vec16<T>::N;
+  const int half = d / 2;
+  const int G = half / N;
+  const int per_entry = Hkv * PIC_PAGE * G;
+  const int hs = d * PIC_PAGE;
+  __shared__ int s_c, s_r;
+  for (int64_t cp = blockIdx.x; cp < n_cpages; cp += gridDim.x) {
+    if (threadIdx.x == 0) {
+      int lo = 0, hi = n_chunks;  // last c with chunk_page_off[c] <= cp
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (chunk_page_off[mid] <= cp) lo = mid; else hi = mid;
+      }
+      s_c = lo;
+      int a = 0, b = n_req;  // last r with chunk_off[r] <= c
+      while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (chunk_off[mid] <= lo) a = mid; else b = mid;
+      }
+      s_r = a;
+    }
+    __syncthreads();
+    const int c = s_c, r = s_r;
+    __syncthreads();  // read before the next page's search writes them
+    const int j = (int)(cp - chunk_page_off[c]);
+    const int L = chunk_lens[c];
+    const int m = (c == chunk_off[r]) ? 0 : min(kk[r], L);
+    const int slo = max(0, m - PIC_PAGE * j), shi = min(PIC_PAGE, L - PIC_PAGE * j);
+    if (slo >= shi) continue;
+    const int64_t pos0 = (int64_t)chunk_start[c] + PIC_PAGE * j;
+    const int src = k_src[cp], dst = (k_dst != nullptr) ? k_dst[cp] : src;
+    if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks || pos0 < 0 || pos0 + shi > n_pos) {
+      if (threadIdx.x == 0) set_err(err, PIC_ERR_RANGE);
+      continue;
+    }
+    const T* src_base = pool + (int64_t)src * Hkv * hs;
+    T* dst_base = pool + (int64_t)dst * Hkv * hs;
+    int key_have = -1;  // (slot, vector) whose cos/sin the thread holds
+    float4 cs[N];
+    for (int base = 0; base < per_entry; base += kRotThreads * kRotUnroll) {
+      uint4 xl[kRotUnroll], xh[kRotUnroll];
+      int off[kRotUnroll], key[kRotUnroll];
+      bool act[kRotUnroll];
+#pragma unroll
+      for (int u = 0; u < kRotUnroll; ++u) {
+        const int it = base + u * kRotThreads + threadIdx.x;
+        const int v = it % G;
+        const int sl = (it / G) % PIC_PAGE;
+        const int h = it / (G * PIC_PAGE);
+        act[u] = it < per_entry && sl >= slo && sl < shi;
+        off[u] = h * hs + sl * d + v * N;
+        key[u] = sl * G + v;
+        if (act[u]) {
+          xl[u] = __ldcs(reinterpret_cast<const uint4*>(src_base + off[u]));
+          xh[u] = __ldcs(reinterpret_cast<const uint4*>(src_base + off[u] + half));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kRotUnroll; ++u) {
+        if (!act[u]) continue;
+        if (key[u] != key_have) {
+          const int sl = key[u] / G, v = key[u] % G;
+          load_cs<N>(table + (pos0 + sl) * half + v * N, cs);
+          key_have = key[u];
+        }
+        uint4 ol, oh;
+        rotate_vec<T>(xl[u], xh[u], cs, ol, oh);
+        __stcs(reinterpret_cast<uint4*>(dst_base + off[u]), ol);
+        __stcs(reinterpret_cast<uint4*>(dst_base + off[u] + half), oh);
+      }
+    }
+  }
+}
+
 // Fresh rows: item = (row i, head h, vector v).  K is roped at the row's global
 // position (row table), V is copied.
 template <typename T>
@@ -249,6 +338,35 @@ pic_status pic_rerotate_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int
     rerotate_kernel<float><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
         static_cast<float*>(k_pool), num_blocks, Hkv, d, rot, n_rot,
         reinterpret_cast<const float4*>(table), n_tab, err_flag);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+pic_status pic_rope_cached_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int32_t Hkv, int32_t d,
+                             const int32_t* chunk_lens, const int32_t* chunk_off, const int32_t* k, int32_t n_req,
+                             const int32_t* chunk_start, const int32_t* chunk_page_off, int32_t n_chunks,
+                             int64_t n_chunk_pages, const int32_t* k_src_blocks, const int32_t* k_dst_blocks,
+                             const float* pos_table, int64_t n_pos, int32_t* err_flag, pic_stream_t stream) {
+  if (n_req < 0 || n_chunks < 0 || n_chunk_pages < 0 || num_blocks < 0 || n_pos < 0) return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (!shape_ok(dtype, Hkv, d)) return (d > 0 && !(d & 1)) ? PIC_ERR_UNSUPPORTED : PIC_ERR_INVALID;
+  if (n_req == 0 || n_chunk_pages == 0) return PIC_OK;
+  if (!k_pool || !chunk_lens || !chunk_off || !k || !chunk_start || !chunk_page_off || !k_src_blocks ||
+      !pos_table || !err_flag)
+    return PIC_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(pos_table) & 15))
+    return PIC_ERR_INVALID;
+  const int64_t cap = (int64_t)num_sms_of_current_device() * 4;
+  const int grid = (int)(n_chunk_pages < cap ? n_chunk_pages : cap);
+  if (dtype == PIC_BF16)
+    rope_cached_kernel<__nv_bfloat16><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<__nv_bfloat16*>(k_pool), num_blocks, Hkv, d, chunk_lens, chunk_off, k, n_req, chunk_start,
+        chunk_page_off, n_chunks, n_chunk_pages, k_src_blocks, k_dst_blocks,
+        reinterpret_cast<const float4*>(pos_table), n_pos, err_flag);
+  else
+    rope_cached_kernel<float><<<grid, kRotThreads, 0, (cudaStream_t)stream>>>(
+        static_cast<float*>(k_pool), num_blocks, Hkv, d, chunk_lens, chunk_off, k, n_req, chunk_start,
+        chunk_page_off, n_chunks, n_chunk_pages, k_src_blocks, k_dst_blocks,
+        reinterpret_cast<const float4*>(pos_table), n_pos, err_flag);
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }
 

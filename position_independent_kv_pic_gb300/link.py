@@ -19,8 +19,8 @@ import numpy as np
 import torch
 
 from . import (PIC_BF16, PIC_FP32, PIC_PAGE, pic_decode_attention, pic_decode_workspace, pic_link_attention,
-               pic_link_attention_workspace, pic_plan_offsets, pic_rerotate_k, pic_rope_table, pic_select_rows,
-               pic_splice_pages, pic_write_fresh_kv)
+               pic_link_attention_workspace, pic_plan_offsets, pic_rerotate_k, pic_rope_cached_k, pic_rope_table,
+               pic_select_rows, pic_splice_pages, pic_write_fresh_kv)
 from .inputs import Workload, block_shuffle, chunk_store, decode_inputs, row_inputs
 
 
@@ -31,7 +31,16 @@ def _cdiv(a, b):
 class LinkBatch:
     """Device state and inputs of one link step for the requests of a workload."""
 
-    def __init__(self, wl: Workload, device="cuda", rows_inputs=None):
+    def __init__(self, wl: Workload, device="cuda", rows_inputs=None, scheme="rotary"):
+        """scheme "rotary": the pool's cached K is encoded at local positions and the step
+        re-rotates it by the chunk offset (rotary correction).  scheme "nope": the pool's
+        cached K carries no position encoding and the step encodes every kept cached slot
+        at its global position (scheme B; in place only)."""
+        if scheme not in ("rotary", "nope"):
+            raise ValueError(scheme)
+        if scheme == "nope" and wl.out_of_place:
+            raise ValueError("scheme B runs in place: give each request private copies of its chunks")
+        self.scheme = scheme
         self.wl = wl
         self.device = torch.device(device)
         self.dtype = wl.torch_dtype
@@ -117,6 +126,12 @@ class LinkBatch:
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws > 0 else None
         self.err = torch.zeros(1, dtype=i32, device=dev)
         self.scale = 1.0 / math.sqrt(d)
+        if scheme == "nope":
+            # the model's position table (every position a cached slot can take), built once
+            self.n_pos = max([int(wl.chunk_lens[r.chunk_ids].sum()) for r in wl.requests] + [1])
+            pos_all = torch.arange(self.n_pos, dtype=i32, device=dev)
+            self.pos_table = torch.empty((self.n_pos, d // 2, 4), dtype=torch.float32, device=dev)
+            pic_rope_table(pos_all, d, wl.theta, self.pos_table)
 
     # ------------------------------------------------------------------ state
     def reset_pool(self):
@@ -162,7 +177,11 @@ class LinkBatch:
     # ------------------------------------------------------------------ step
     # kernels one run() launches: select, splice, 2 tables, re-rotate, fresh K/V, and the
     # attention call (unit planning, attention, LSE merge)
-    LAUNCHES_PER_STEP = 9
+    LAUNCHES_PER_STEP = 9  # rotary correction; scheme B has no offset table: 8
+
+    @property
+    def launches_per_step(self) -> int:
+        return self.LAUNCHES_PER_STEP - (1 if self.scheme == "nope" else 0)
 
     def run(self, stream=None, marks=None):
         """The link step: a1 select, splice, a2 tables, a3 re-rotate, a4 fresh K/V, a5+a6 attention.
@@ -177,12 +196,19 @@ class LinkBatch:
                          dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
                          dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
                          self.row_block, self.row_slot, self.err, stream)
-        pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, stream)
+        if self.scheme == "rotary":
+            pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, stream)
         pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, stream)
         if "rerotate" in mk:
             mk["rerotate"][0].record()
-        pic_rerotate_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, self.rot, self.n_rot, self.delta_table,
-                       self.n_chunks, self.err, stream)
+        if self.scheme == "rotary":
+            pic_rerotate_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, self.rot, self.n_rot, self.delta_table,
+                           self.n_chunks, self.err, stream)
+        else:
+            pic_rope_cached_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, dv["chunk_lens"], dv["chunk_off"], dv["k"],
+                              self.n_req, self.chunk_start, dv["chunk_page_off"], self.n_chunks,
+                              int(self.offs["chunk_page_off"][-1]), dv["k_src"], None, self.pos_table, self.err,
+                              stream)
         if "rerotate" in mk:
             mk["rerotate"][1].record()
         pic_write_fresh_kv(self.k_pool, self.v_pool, self.pic_dtype, wl.Hkv, wl.d, dv["k_new"], dv["v_new"],

@@ -1,0 +1,109 @@
+"""Scheme B through the C ABI: chunks cached without position encoding, encoded at
+their global positions by pic_rope_cached_k, against the float64 oracle
+(link_request with scheme "nope")."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle.pic_oracle as O
+import position_independent_kv_pic_gb300 as pic
+from position_independent_kv_pic_gb300 import build as pic_build
+from position_independent_kv_pic_gb300 import inputs
+from position_independent_kv_pic_gb300.link import LinkBatch
+
+from parity_util import TOL_MAX, TOL_MEAN, check_rows, request_inputs, sample_rows, storage_ulp
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    pic_build.build()
+    pic.load()
+
+
+def _run(wl):
+    b = LinkBatch(wl, scheme="nope")
+    b.run()
+    torch.cuda.synchronize()
+    assert b.error() == 0, pic.pic_strerror(b.error())
+    return b
+
+
+def _check_k(b, max_chunks=None):
+    """Every kept cached K slot (chunk 0 included) within one ulp of the oracle's
+    encoding at the global position."""
+    wl = b.wl
+    starts = b.chunk_start.cpu().numpy()
+    for r, req in enumerate(wl.requests):
+        c0, c1 = int(b.chunk_off[r]), int(b.chunk_off[r + 1])
+        for ci, c in enumerate(range(c0, c1)):
+            if max_chunks is not None and 1 <= ci < c1 - c0 - 1 and ci >= max_chunks:
+                continue
+            sid = int(b.flat_store_ids[c])
+            stored = b.store_k[b.store_off[sid]:b.store_off[sid + 1]].double().numpy()
+            got = b.rotated_chunk_k(c).double().numpy()
+            m = 0 if ci == 0 else min(req.k, stored.shape[0])
+            expect = O.rope_cached_k(stored, int(starts[c]), wl.theta, wl.dtype)
+            ratio = (np.abs(got[m:] - expect[m:]) / storage_ulp(expect[m:], wl.dtype)).max() if m < len(stored) else 0
+            assert ratio <= (1.0 if wl.dtype == "bf16" else 4.0), (r, ci, ratio)
+
+
+def _check_attention(b, pick=None):
+    wl = b.wl
+    out = b.out.double().cpu().numpy()
+    errs = []
+    for r in range(len(wl.requests)):
+        a, e = int(b.offs["row_off"][r]), int(b.offs["row_off"][r + 1])
+        which = list(range(e - a)) if pick is None else pick(e - a)
+        ck, cv, q, k, qr, kn, vn = request_inputs(b, r)
+        res = O.link_request(ck, cv, q, k, qr, kn, vn, wl.theta, wl.dtype, which=which, scheme="nope")
+        errs.append(np.abs(out[a:e][which] - res["out"][which]).ravel())
+    x = np.concatenate(errs)
+    return float(x.max()), float(x.mean())
+
+
+@pytest.mark.parametrize("preset", ["rag_prompt_6chunks", "many_chunk_sink_20"])
+def test_scheme_b_workloads(preset):
+    b = _run(inputs.PRESETS[preset]())
+    check_rows(b)
+    _check_k(b)
+    emax, emean = _check_attention(b)
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
+def test_scheme_b_long_context_sampled():
+    b = _run(inputs.long_context())
+    check_rows(b)
+    _check_k(b, max_chunks=10)
+    emax, emean = _check_attention(b, lambda n: sample_rows(n, 6, 6, 12))
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
+@pytest.mark.parametrize("case", [
+    ([[300, 17, 1, 64, 129]], [37], [8]),
+    ([[40, 50, 60]], [3], [40]),
+    ([[130, 70], [55, 8, 200, 31]], [20, 1], [2, 16]),
+])
+def test_scheme_b_edge_cases(case):
+    lens, qs, ks = case
+    b = _run(inputs.custom(lens, qs, ks, Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=70 + len(lens)))
+    check_rows(b)
+    _check_k(b)
+    emax, emean = _check_attention(b)
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
+def test_scheme_b_fp32_small():
+    b = _run(inputs.custom([[21, 13, 40]], [6], [5], Hq=4, Hkv=2, d=32, theta=1e4, dtype="fp32", seed=77))
+    _check_k(b)
+    emax, emean = _check_attention(b)
+    assert emax < 1e-4 and emean < 1e-5, (emax, emean)
+
+
+def test_scheme_b_refuses_shared_chunks():
+    with pytest.raises(ValueError):
+        LinkBatch(inputs.batched_shared(), scheme="nope")
