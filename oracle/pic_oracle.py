@@ -283,3 +283,43 @@ def decode_after_link(K_ctx, V_ctx, q_raw, k_raw, v_raw, theta, dtype, scale=Non
     V = np.concatenate([V_ctx, round_to(np.asarray(v_raw, np.float64)[None], dtype)], axis=0)
     q_rot = round_to(rope(np.asarray(q_raw, np.float64)[None], pos, theta), dtype)
     return attention_rows(q_rot, pos, K, V, scale)[0]
+
+
+# ---------------------------------------------------------------------------
+# Linear-attention layers  ([HYPIC] 2.1: cache each segment's transition operator)
+# ---------------------------------------------------------------------------
+# A linear-attention layer keeps a state S (d_k x d_v) per head, updated per token
+# as S_t = A_t S_{t-1} + B_t (A_t: d_k x d_k transition -- identity for plain
+# linear attention, gamma I for RetNet, alpha_t (I - beta_t k_t k_t^T) for the
+# gated delta rule; B_t: the token's rank-one write).  A segment C of tokens is
+# summarised by its cumulative transition T_C = A_L ... A_1 and its end state from
+# zero S(C|0); both depend only on the segment's own tokens.
+
+def recurrence(A, B, S0=None) -> np.ndarray:
+    """End state of S_t = A_t S_{t-1} + B_t over the tokens (A [L][dk][dk], B [L][dk][dv])."""
+    A = np.asarray(A, np.float64)
+    B = np.asarray(B, np.float64)
+    S = np.zeros(B.shape[1:]) if S0 is None else np.asarray(S0, np.float64).copy()
+    for t in range(A.shape[0]):
+        S = A[t] @ S + B[t]
+    return S
+
+
+def segment_operator(A, B):
+    """(T_C, S(C|0)) of one segment from its tokens."""
+    A = np.asarray(A, np.float64)
+    T = np.eye(A.shape[1])
+    for t in range(A.shape[0]):
+        T = A[t] @ T
+    return T, recurrence(A, B)
+
+
+def compose_states(T, S) -> np.ndarray:
+    """End state of a chain of segments from their cached (T_c, S_c), in chain order:
+    S(C1 C2) = T(C2) S(C1) + S(C2), applied left to right.  T, S [n][d][d]."""
+    T = np.asarray(T, np.float64)
+    S = np.asarray(S, np.float64)
+    acc = S[0].copy()
+    for i in range(1, S.shape[0]):
+        acc = T[i] @ acc + S[i]
+    return acc

@@ -558,3 +558,67 @@ def test_scheme_b_mutation_unencoded_chunk0_caught(monkeypatch):
     monkeypatch.setattr(O, "rope_cached_k", skip_chunk0)
     bad = O.link_request(nope, cv, q, k, q_raw, k_raw, v, base, "fp64", scheme="nope")["out"]
     assert np.abs(bad - good).max() > 10 * 2e-2 or np.abs(bad - good).mean() > 10 * 2e-3
+
+
+# ---------------------------------------------------------------------------
+# Linear-layer state composition ([HYPIC] 2.1)
+# ---------------------------------------------------------------------------
+
+def _delta_rule_tokens(rng, L, dk, dv):
+    """Gated delta rule: A_t = alpha_t (I - beta_t k_t k_t^T), B_t = beta_t k_t v_t^T."""
+    k = rng.standard_normal((L, dk))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = rng.standard_normal((L, dv))
+    alpha = rng.uniform(0.9, 1.0, L)
+    beta = rng.uniform(0.1, 0.9, L)
+    A = np.stack([alpha[t] * (np.eye(dk) - beta[t] * np.outer(k[t], k[t])) for t in range(L)])
+    B = np.stack([beta[t] * np.outer(k[t], v[t]) for t in range(L)])
+    return A, B
+
+
+@pytest.mark.parametrize("family", ["delta", "retnet"])
+def test_composition_equals_token_recurrence(family):
+    """Composing cached per-segment (T_C, S(C|0)) reproduces the state of the token
+    recurrence over the concatenated segments."""
+    rng = np.random.default_rng(41)
+    dk, dv, lens = 8, 6, [5, 9, 3, 7]
+    segs = []
+    for L in lens:
+        if family == "delta":
+            A, B = _delta_rule_tokens(rng, L, dk, dv)
+        else:
+            A = np.stack([0.97 * np.eye(dk)] * L)
+            B = np.einsum("ti,tj->tij", rng.standard_normal((L, dk)), rng.standard_normal((L, dv)))
+        segs.append((A, B))
+    T, S = zip(*[O.segment_operator(A, B) for A, B in segs])
+    direct = O.recurrence(np.concatenate([a for a, _ in segs]), np.concatenate([b for _, b in segs]))
+    assert np.abs(O.compose_states(np.array(T), np.array(S)) - direct).max() < 1e-12
+
+
+def test_composition_is_associative():
+    """Composing sub-chains first (a scan in any tree order) gives the same state."""
+    rng = np.random.default_rng(42)
+    d, n = 6, 9
+    T = 0.9 * np.eye(d) + 0.05 * rng.standard_normal((n, d, d))
+    S = rng.standard_normal((n, d, d))
+    seq = O.compose_states(T, S)
+    # (0..3) then (4..8) as sub-chains: T of a sub-chain is the product of its T
+    def sub(a, b):
+        Tp = np.eye(d)
+        for i in range(a, b):
+            Tp = T[i] @ Tp
+        return Tp, O.compose_states(T[a:b], S[a:b])
+    (T1, S1), (T2, S2) = sub(0, 4), sub(4, 9)
+    assert np.abs(T2 @ S1 + S2 - seq).max() < 1e-12
+
+
+def test_naive_sum_exact_only_without_transition():
+    """Plain linear attention (A_t = I): composition is the plain sum of the segment
+    states.  With decay the sum drops T(C2) and is structurally wrong."""
+    rng = np.random.default_rng(43)
+    d, n = 6, 5
+    S = rng.standard_normal((n, d, d))
+    assert np.abs(O.compose_states(np.stack([np.eye(d)] * n), S) - S.sum(0)).max() < 1e-12
+    T = np.stack([0.8 * np.eye(d)] * n)
+    good = O.compose_states(T, S)
+    assert np.linalg.norm(good - S.sum(0)) > 0.2 * np.linalg.norm(good)
