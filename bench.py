@@ -282,6 +282,33 @@ def run_gpu(args, rank, world):
         del bb
         torch.cuda.empty_cache()
 
+    # linear-layer state composition (a hybrid model's linear-attention layer over the
+    # same chunk chains: 32 heads of 128 x 128 states per chunk)
+    comp = None
+    if wl.d == 128:
+        from position_independent_kv_pic_gb300 import inputs
+        from position_independent_kv_pic_gb300.states import ComposeBatch
+        T, S, chains = inputs.linear_states(wl, H=32, d=128)
+        cbatch = ComposeBatch(T, S, chains)
+        del T, S
+        for _ in range(args.warmup):
+            cbatch.run()
+        torch.cuda.synchronize()
+        Kc = max(3, min(K, 50))
+        cev = [(ev(), ev()) for _ in range(Kc)]
+        for i in range(Kc):
+            flush.zero_()
+            cev[i][0].record(stream)
+            cbatch.run()
+            cev[i][1].record(stream)
+        torch.cuda.synchronize()
+        if cbatch.error() != 0:
+            raise SystemExit(f"device error (composition): {pic.pic_strerror(cbatch.error())}")
+        comp = (statistics.mean(a.elapsed_time(b) for a, b in cev), cbatch.algorithmic_bytes, Kc, cbatch.seg,
+                cbatch.n_req * cbatch.H, cbatch.n_elems, cbatch.launches)
+        del cbatch
+        torch.cuda.empty_cache()
+
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
     att_avg = statistics.mean(att_ms)
     rot_avg = statistics.mean(rot_ms)
@@ -322,6 +349,14 @@ def run_gpu(args, rank, world):
                              "kernel": "pic_rope_cached_k (scheme B: cached K encoded at its global position; "
                                        "bytes = K read + written + one table row per slot); the step runs "
                                        "without the offset table and the re-rotation"}} if schb else {}),
+            **({"compose": {"bound": "hbm", "achieved": comp[1] / (comp[0] / 1e3) / 1e9, "peak": hbm,
+                            "unit": "GB/s", "frac": comp[1] / (comp[0] / 1e3) / 1e9 / hbm, "ms": comp[0],
+                            "algorithmic_bytes": comp[1], "steps": comp[2], "seg": comp[3], "chains": comp[4],
+                            "chain_elements": comp[5], "launches": comp[6],
+                            "kernel": "pic_compose_states (linear-layer state S = T_n(..(T_2 S_1 + S_2)..) + S_n "
+                                      "per request and head, 32 heads of 128 x 128 fp32 states; bytes = S of "
+                                      "every element + T of every non-first element + the output)"}}
+               if comp else {}),
             "rerotate": {"bound": "hbm", "achieved": rot_gbs, "peak": hbm, "unit": "GB/s", "frac": rot_gbs / hbm,
                          "ms": rot_avg, "traffic": rtraffic, "algorithmic_bytes": rot_bytes,
                          "frac_of_8tbs": rot_gbs / 8000.0},

@@ -368,6 +368,44 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
                                 size_t ws_bytes, int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
+ * Linear-layer state composition (HYPIC blog, section 2.1: linear layers).
+ * ------------------------------------------------------------------------
+ * A hybrid model's linear-attention layer caches, per chunk c and head h, the pair
+ * (T_c, S_c): the chunk's cumulative transition operator T_C and its end state from
+ * a zero state S(C|0), both d x d.  Linking chunks C1 C2 .. Cn in that order gives
+ * the layer's state S = T_n (.. (T_2 S_1 + S_2) ..) + S_n, by the blog's rule
+ * S(C1 C2) = T(C2) S(C1) + S(C2); the transition of C1 is never used.
+ *
+ *   T_pool, S_pool  [n_pool][H][d][d] fp32 row-major (device): the cached pairs
+ *   ids        [n_elems] int32 (device): chain of every request, pool entries in
+ *              chain order; request r owns ids[chain_off[r] .. chain_off[r+1])
+ *   chain_off  [n_req + 1] int32 (device), chain_off[0] = 0, chain_off[n_req] = n_elems
+ *   max_chain  host: an upper bound of every chain's length (longer chains are
+ *              cut to it and flagged)
+ *   seg        0, or the level-0 segment length: chains are cut into segments of
+ *              seg elements, folded in parallel (each non-first segment also
+ *              forms its transition product), then folded per chain by a second
+ *              launch.  0 (or seg >= max_chain) folds every chain in one launch.
+ *              pic_compose_segment() gives the choice that fills one wave of `sms`
+ *              SMs.  The workspace depends on seg.
+ *   out        [n_req][H][d][d] fp32 (device); an empty chain gives zeros
+ *   ws         at least pic_compose_workspace() bytes, 256-byte aligned
+ * d = 128 only (else PIC_ERR_UNSUPPORTED; 0 from pic_compose_workspace).  Each
+ * fold step is a 128 x 128 x 128 tensor-core product of bf16 parts
+ * (hi.hi + hi.lo + lo.hi, fp32 accumulate: about 2^-16 relative error per step).
+ * Two or three launches.  A pool id outside [0, n_pool) or offsets that disagree
+ * with n_elems / max_chain set PIC_ERR_RANGE in *err_flag (pool entry 0 is read in
+ * place of a bad id); a bounded wait that runs out sets PIC_ERR_TIMEOUT. */
+int32_t pic_compose_segment(int32_t n_req, int64_t n_elems, int32_t max_chain, int32_t H, int32_t sms);
+
+size_t pic_compose_workspace(int32_t n_req, int32_t max_chain, int32_t H, int32_t d, int32_t seg);
+
+pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t n_pool, const int32_t* ids,
+                              const int32_t* chain_off, int32_t n_req, int64_t n_elems, int32_t max_chain,
+                              int32_t H, int32_t d, int32_t seg, float* out, void* ws, size_t ws_bytes,
+                              int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
  * Diagnostics.
  * ------------------------------------------------------------------------
  * One 128 x 128 x 128 bf16 tensor-core product through the same shared-memory

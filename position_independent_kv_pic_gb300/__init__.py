@@ -24,6 +24,7 @@ __all__ = [
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
     "pic_decode_workspace", "pic_decode_attention", "pic_rope_cached_k",
+    "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -47,7 +48,7 @@ EXPORTED = (
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "pic_decode_workspace", "pic_decode_attention",
-    "pic_rope_cached_k",
+    "pic_rope_cached_k", "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
 )
 
 
@@ -91,6 +92,10 @@ _SIGS = {
     "pic_decode_workspace": (_SZ, [_I32, _I32, _I32, _I32, ctypes.c_int]),
     "pic_rope_cached_k": (ctypes.c_int, [_P, _I64, ctypes.c_int, _I32, _I32, _P, _P, _P, _I32, _P, _P, _I32, _I64,
                                          _P, _P, _P, _I64, _P, _P]),
+    "pic_compose_segment": (_I32, [_I32, _I64, _I32, _I32, _I32]),
+    "pic_compose_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
+    "pic_compose_states": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _SZ,
+                                          _P, _P]),
     "pic_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32, _I32, _I32, _I32,
                                             _F32, _P, _P, _SZ, _P, _P]),
 }
@@ -238,6 +243,23 @@ def pic_decode_attention(q, q_table, k_pool, v_pool, dtype: int, pages, page_off
         _ptr(q), _ptr(q_table), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype), _ptr(pages), _ptr(page_off),
         int(n_req), int(Hq), int(Hkv), int(d), float(scale), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),
         _stream(stream)), "pic_decode_attention")
+
+
+def pic_compose_segment(n_req: int, n_elems: int, max_chain: int, H: int, sms: int) -> int:
+    return int(load().pic_compose_segment(int(n_req), int(n_elems), int(max_chain), int(H), int(sms)))
+
+
+def pic_compose_workspace(n_req: int, max_chain: int, H: int, d: int, seg: int) -> int:
+    return int(load().pic_compose_workspace(int(n_req), int(max_chain), int(H), int(d), int(seg)))
+
+
+def pic_compose_states(T_pool, S_pool, ids, chain_off, n_req: int, n_elems: int, max_chain: int, H: int, d: int,
+                       seg: int, out, ws, err_flag, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pic_compose_states(
+        _ptr(T_pool), _ptr(S_pool), T_pool.shape[0], _ptr(ids), _ptr(chain_off), int(n_req), int(n_elems),
+        int(max_chain), int(H), int(d), int(seg), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)),
+        "pic_compose_states")
 
 
 def pic_selftest_umma(a, b, d_kmajor, d_mnmajor, d_tmem_a, err_flag, stream=None):

@@ -1,0 +1,504 @@
+// Linear-attention state composition (HYPIC blog, section 2.1).  A linear layer
+// caches, per chunk and head, the pair (T_C, S(C|0)): the chunk's cumulative
+// transition operator and its end state from a zero state.  Chunks linked in any
+// order give the state of the whole chain by S(C1 C2) = T(C2) S(C1) + S(C2),
+// applied along the chain; T composes as T(C1 C2) = T(C2) T(C1).
+//
+// Parallel form: a chain of n elements is cut into segments of `seg` elements; one
+// CTA folds a segment into one element (S of the segment and, unless the segment
+// starts the chain, its transition product); a second launch folds each chain's
+// segment elements in order.  With seg >= n there is one launch and no transition
+// product is formed.
+//
+// One fold step X <- T_i X + S_i (d = 128) is one 128 x 128 x 128 product on the
+// tensor cores, taken transposed so that every operand keeps its natural place:
+//   D^T = X^T T_i^T,  A = X^T in TMEM (TMEM lane n holds column n of X),
+//                     B = T_i in shared memory (row-major T_i is the K-major B).
+// Precision: X and T_i are split into bf16 parts, x = x_hi + x_lo with
+// x_hi = bf16(x), x_lo = bf16(x - x_hi), and the product is taken as
+// hi.hi + hi.lo + lo.hi with fp32 accumulation (the dropped lo.lo term is below
+// 2^-16 of |x||y|).  The accumulator in TMEM plus S_i is the new state in fp32.
+//
+// Pipeline (320 threads).  Warp 8 lane 0 streams T_i into a shared staging buffer
+// by bulk copies; warps 0-7 convert it into one of two bf16 B buffers while the
+// tensor cores work on the other, and run the epilogue (TMEM -> + S_i -> split ->
+// TMEM), reading S_i straight from global memory one step ahead; warp 9 lane 0
+// issues the MMAs.  The critical path of a step is its MMAs plus the epilogue.
+// Every wait is bounded.
+#include <algorithm>
+
+#include "pic_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace pic {
+namespace {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kCD = 128;                              // d_k = d_v
+constexpr int kElt = kCD * kCD;                       // floats per matrix
+constexpr int kMatBytes = kElt * 4;                   // 64 KB fp32
+constexpr int kCWorkers = 256;                        // warps 0-7
+constexpr int kProdWarp = kCWorkers / 32, kMmaWarp = kProdWarp + 1;
+constexpr int kCThreads = kCWorkers + 64;
+constexpr int kBHalf = kCD * 128;                     // one 64-column half of a 128-row bf16 operand
+constexpr int kBPart = 2 * kBHalf;                    // 32 KB: one bf16 part of B
+constexpr int kBBytes = 2 * kBPart;                   // hi | lo
+constexpr int kOffB = 0;                              // two B buffers (SW128, [half][128 rows][128 B])
+constexpr int kOffTs = kOffB + 2 * kBBytes;           // T_i staging, fp32 row-major
+constexpr int kOffBar = kOffTs + kMatBytes;
+constexpr int kCSmem = kOffBar + 128;
+static_assert(kCSmem <= 232448, "shared memory per CTA");
+// TMEM columns: D_S | D_T | A_S hi | A_S lo | A_T hi | A_T lo
+constexpr uint32_t kColDS = 0, kColDT = 128, kColAS = 256, kColAT = 384;
+constexpr uint64_t kCWaitNs = 2000000000ull;
+constexpr uint32_t kCIdesc = tc::idesc_bf16_f32(128, 128, false);
+constexpr int kCopy = 16384;                          // bytes per bulk copy
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+struct CBars {
+  uint64_t t_full, t_empty, b_full[2], a_full, d_full;  // b_full per B buffer: a phase per use
+  uint32_t tmem;
+  int abort;
+};
+static_assert(sizeof(CBars) <= 128, "barrier block");
+
+struct Level {
+  const float* T_in;
+  const float* S_in;
+  const int32_t* ids;        // level 0: pool entry of every chain element; else nullptr
+  const int32_t* chain_off;  // [n_req + 1] offsets of each request's chain in ids
+  const int32_t* first;      // [n_req + 1] first CTA of each request at this level
+  int64_t n_pool;            // level 0: entries of the pool
+  int64_t in_stride;         // level 1: elements per chain in T_in / S_in
+  float* T_out;              // level 0 of two: [chain][out_stride]
+  float* S_out;              // [chain][out_stride]
+  int64_t out_stride;
+  int64_t n_elems;           // entries of ids
+  int n_req, H, seg, seg_prev;  // seg_prev: level 1 input elements per chain = ceil(n_r / seg_prev)
+  int max_chain;             // chain lengths are clamped to it (the planner flags longer ones)
+  int level;
+  bool last;
+  int32_t* err;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, CBars* cb, int32_t* err) {
+  if (tc::mbar_wait(bar, parity, &cb->abort, kCWaitNs)) return true;
+  set_err(err, PIC_ERR_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&cb->abort) = 1;
+  return false;
+}
+
+__device__ __forceinline__ void load_matrix(uint8_t* dst, const float* src, uint64_t* bar) {
+  tc::mbar_arrive_expect_tx(bar, kMatBytes);
+#pragma unroll
+  for (int c = 0; c < kMatBytes / kCopy; ++c)
+    tc::bulk_load(dst + c * kCopy, reinterpret_cast<const uint8_t*>(src) + c * kCopy, kCopy, bar);
+}
+
+// Column n, rows m0 .. m0 + 63 of a row-major d x d matrix in global memory (a
+// warp's 32 lanes read 32 consecutive columns: 128-byte rows).
+__device__ __forceinline__ void load_col64(const float* __restrict__ src, int m0, int n, float (&v)[64]) {
+  const float* p = src + m0 * kCD + n;
+#pragma unroll
+  for (int j = 0; j < 64; ++j) v[j] = __ldg(p + j * kCD);
+}
+
+// Column nc, rows m0 .. m0 + 63 of a state: sv (when USE_V) plus the accumulator
+// at TMEM column d_col (when ADD_D) -> the output (fp32, when to_out) or the A
+// operand at TMEM column a_col (bf16 hi | lo).  16 columns at a time, to keep the
+// registers for the prefetched sv.  Warp-collective.
+template <bool USE_V, bool ADD_D>
+__device__ __forceinline__ void emit(const float (&sv)[64], uint32_t tmem_row, uint32_t d_col, int m0, int nc,
+                                     bool to_out, float* out, uint32_t a_col) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    float x[16];
+    if (ADD_D) {
+      uint32_t rr[16];
+      tc::tmem_ld16(tmem_row + d_col + m0 + 16 * c, rr);
+      tc::tmem_ld_wait();
+      tc::reg_fence<16>(rr);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x[j] = USE_V ? __uint_as_float(rr[j]) + sv[16 * c + j] : __uint_as_float(rr[j]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x[j] = sv[16 * c + j];
+    }
+    if (to_out) {
+      float* o = out + (m0 + 16 * c) * kCD + nc;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j * kCD] = x[j];
+    } else {
+      uint32_t hi[8], lo[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const bf16 h0 = __float2bfloat16_rn(x[2 * j]), h1 = __float2bfloat16_rn(x[2 * j + 1]);
+        hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lo[j] = pack_bf16x2(x[2 * j] - __bfloat162float(h0), x[2 * j + 1] - __bfloat162float(h1));
+      }
+      tc::tmem_st8(tmem_row + a_col + (m0 >> 1) + 8 * c, hi);
+      tc::tmem_st8(tmem_row + a_col + 64 + (m0 >> 1) + 8 * c, lo);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* sm = smem_raw;
+  CBars* cb = reinterpret_cast<CBars*>(sm + kOffBar);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int cta = blockIdx.x;
+  if (cta >= __ldg(lv.first + lv.n_req)) return;
+  if (tc::smem_addr(smem_raw) & 1023u) {
+    if (tid == 0) set_err(lv.err, PIC_ERR_UNSUPPORTED);
+    return;
+  }
+  int r;
+  {
+    int lo = 0, hi = lv.n_req;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(lv.first + mid) <= cta) lo = mid; else hi = mid;
+    }
+    r = lo;
+  }
+  const int c0 = __ldg(lv.chain_off + r);
+  const int n_r = min(max(__ldg(lv.chain_off + r + 1) - c0, 0), lv.max_chain);
+  const int n_in = lv.level == 0 ? n_r : (n_r + lv.seg_prev - 1) / lv.seg_prev;
+  const int n_segs = max(1, (n_in + lv.seg - 1) / lv.seg);
+  const int local = cta - __ldg(lv.first + r);
+  const int h = local / n_segs, g = local % n_segs;
+  const int b = g * lv.seg, e = min(n_in, b + lv.seg), n = e - b;
+  const bool need_T = !lv.last && g > 0;
+  const int64_t chain = (int64_t)r * lv.H + h;
+  float* s_out = lv.S_out + (chain * lv.out_stride + g) * kElt;
+  float* t_out = need_T ? lv.T_out + (chain * lv.out_stride + g) * kElt : nullptr;
+
+  if (n <= 0) {  // an empty chain: its state is zero
+    for (int i = tid; i < kElt / 4; i += kCThreads)
+      reinterpret_cast<float4*>(s_out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    return;
+  }
+  auto elem = [&](const float* base, int i) -> const float* {
+    if (lv.level == 0) {
+      const int64_t at = (int64_t)c0 + i;
+      int64_t id = (at >= 0 && at < lv.n_elems) ? __ldg(lv.ids + at) : 0;
+      if (id < 0 || id >= lv.n_pool) id = 0;  // flagged by the planner
+      return base + (id * lv.H + h) * kElt;
+    }
+    return base + (chain * lv.in_stride + i) * kElt;
+  };
+
+  if (tid == 0) {
+    tc::mbar_init(&cb->t_full, 1);
+    tc::mbar_init(&cb->t_empty, kCWorkers);
+    tc::mbar_init(&cb->b_full[0], kCWorkers);
+    tc::mbar_init(&cb->b_full[1], kCWorkers);
+    tc::mbar_init(&cb->a_full, kCWorkers);
+    tc::mbar_init(&cb->d_full, 1);
+    cb->abort = 0;
+    tc::fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tc::tmem_alloc(&cb->tmem, 512);
+    tc::tmem_relinquish();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::tc_fence_after();
+  const uint32_t tmem = cb->tmem;
+  const int n_steps = n - 1;  // T loads: T_{b+1} .. T_{e-1}, one per step
+
+  if (warp == kProdWarp) {
+    // ---- producer: T_{b+1+u} into the staging buffer, one in flight
+    if (lane == 0) {
+      int issued = 0;
+      for (int u = 0; u < n_steps; ++u) {
+        if (!wait_bar(&cb->t_empty, (u & 1) ^ 1, cb, lv.err)) break;
+        load_matrix(sm + kOffTs, elem(lv.T_in, b + 1 + u), &cb->t_full);
+        issued = u + 1;
+      }
+      const int no_abort = 0;
+      if (issued > 0) tc::mbar_wait(&cb->t_full, (issued - 1) & 1, &no_abort, kCWaitNs);
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issue: D_S = A_S B_k (and D_T = A_T B_k), three bf16 part products each
+    if (lane == 0) {
+      constexpr uint32_t kHi = tc::sw128_desc_hi(1024);
+      const uint32_t b_lo0 = tc::sw128_desc_lo(tc::smem_addr(sm + kOffB), 16);
+      int issued = 0;
+      for (int k = 0; k < n_steps; ++k) {
+        if (!wait_bar(&cb->b_full[k & 1], (k >> 1) & 1, cb, lv.err)) break;
+        if (!wait_bar(&cb->a_full, k & 1, cb, lv.err)) break;
+        tc::tc_fence_after();
+        const uint32_t b_lo = b_lo0 + (uint32_t)((k & 1) * (kBBytes >> 4));
+#pragma unroll
+        for (int ks = 0; ks < kCD / 16; ++ks) {
+          const uint32_t boff = (uint32_t)(((ks >> 2) * kBHalf + (ks & 3) * 32) >> 4);
+          const uint64_t bh = tc::desc_join(b_lo + boff, kHi);
+          const uint64_t bl = tc::desc_join(b_lo + boff + (kBPart >> 4), kHi);
+          const uint32_t acc = ks > 0 ? 1u : 0u;
+          tc::mma_bf16_ts(tmem + kColDS, tmem + kColAS + ks * 8, bh, kCIdesc, acc);
+          tc::mma_bf16_ts(tmem + kColDS, tmem + kColAS + ks * 8, bl, kCIdesc, 1u);
+          tc::mma_bf16_ts(tmem + kColDS, tmem + kColAS + 64 + ks * 8, bh, kCIdesc, 1u);
+          if (need_T) {
+            tc::mma_bf16_ts(tmem + kColDT, tmem + kColAT + ks * 8, bh, kCIdesc, acc);
+            tc::mma_bf16_ts(tmem + kColDT, tmem + kColAT + ks * 8, bl, kCIdesc, 1u);
+            tc::mma_bf16_ts(tmem + kColDT, tmem + kColAT + 64 + ks * 8, bh, kCIdesc, 1u);
+          }
+        }
+        tc::mma_commit(&cb->d_full);
+        issued = k + 1;
+      }
+      const int no_abort = 0;
+      if (issued > 0) tc::mbar_wait(&cb->d_full, (issued - 1) & 1, &no_abort, kCWaitNs);
+    }
+    __syncwarp();
+  } else {
+    // ---- workers: warp w reads TMEM lanes 32 (w % 4) .. +31 (state columns
+    // n = 32 (w % 4) + lane) and accumulator columns m = 64 (w / 4) .. +63
+    const int quarter = warp & 3, hf = warp >> 2;
+    const int nc = 32 * quarter + lane, m0 = 64 * hf;
+    const uint32_t lane_base = (uint32_t)((32 * quarter) << 16);
+    const float* ts = reinterpret_cast<const float*>(sm + kOffTs);
+    bool ok = true;
+    float sv[64];
+    // staged T_i (row-major) -> B buffer `buf` (hi | lo, K-major SW128): thread t
+    // converts the 16-byte chunks (row m, k = 4 c4 .. +3), a warp one row at a time
+    auto convert_T = [&](int buf) {
+      uint8_t* bb = sm + kOffB + buf * kBBytes;
+#pragma unroll 4
+      for (int it = 0; it < kElt / 4 / kCWorkers; ++it) {
+        const int q = it * kCWorkers + tid, m = q >> 5, c4 = q & 31;
+        const float4 v = *reinterpret_cast<const float4*>(ts + m * kCD + 4 * c4);
+        const bf16 h0 = __float2bfloat16_rn(v.x), h1 = __float2bfloat16_rn(v.y);
+        const bf16 h2 = __float2bfloat16_rn(v.z), h3 = __float2bfloat16_rn(v.w);
+        const uint2 hv = make_uint2((uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16),
+                                    (uint32_t)__bfloat16_as_ushort(h2) | ((uint32_t)__bfloat16_as_ushort(h3) << 16));
+        const uint2 lv2 = make_uint2(pack_bf16x2(v.x - __bfloat162float(h0), v.y - __bfloat162float(h1)),
+                                     pack_bf16x2(v.z - __bfloat162float(h2), v.w - __bfloat162float(h3)));
+        const int ch = (c4 & 15) >> 1;
+        const uint32_t off = (uint32_t)((c4 >> 4) * kBHalf + m * 128 + ((ch ^ (m & 7)) << 4) + (c4 & 1) * 8);
+        *reinterpret_cast<uint2*>(bb + off) = hv;
+        *reinterpret_cast<uint2*>(bb + kBPart + off) = lv2;
+      }
+    };
+    int tu = 0;  // staged T_i converted
+    auto next_B = [&]() -> bool {  // the next staged T_i into B buffer tu & 1
+      if (!wait_bar(&cb->t_full, tu & 1, cb, lv.err)) return false;
+      convert_T(tu & 1);
+      tc::fence_proxy_async_smem();  // generic-proxy writes of B -> the MMA's reads
+      tc::mbar_arrive(&cb->b_full[tu & 1]);
+      tc::mbar_arrive(&cb->t_empty);
+      ++tu;
+      return true;
+    };
+    auto signal_a = [&]() {
+      tc::tmem_st_wait();
+      tc::tc_fence_before();
+      tc::mbar_arrive(&cb->a_full);
+    };
+    // first element: the accumulators (or the output, for a one-element segment)
+    load_col64(elem(lv.S_in, b), m0, nc, sv);
+    emit<true, false>(sv, tmem + lane_base, 0, m0, nc, n == 1, s_out, kColAS);
+    if (need_T) {
+      load_col64(elem(lv.T_in, b), m0, nc, sv);
+      emit<true, false>(sv, tmem + lane_base, 0, m0, nc, n == 1, t_out, kColAT);
+    }
+    if (n_steps > 0) {
+      signal_a();
+      load_col64(elem(lv.S_in, b + 1), m0, nc, sv);
+      ok = next_B();
+    }
+    // steps 0 .. n_steps - 2 feed the next step; the last writes the output (kept
+    // out of the loop so that the output addresses are not held across it)
+    for (int k = 0; ok && k + 1 < n_steps; ++k) {
+      // B buffer (k + 1) & 1 was read by MMA k - 1, complete: convert T_{b+k+2}
+      // while MMA k runs
+      if (!(ok = next_B())) break;
+      if (!(ok = wait_bar(&cb->d_full, k & 1, cb, lv.err))) break;
+      tc::tc_fence_after();
+      emit<true, true>(sv, tmem + lane_base, kColDS, m0, nc, false, nullptr, kColAS);
+      if (need_T) emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, false, nullptr, kColAT);
+      signal_a();
+      load_col64(elem(lv.S_in, b + k + 2), m0, nc, sv);
+    }
+    if (ok && n_steps > 0 && wait_bar(&cb->d_full, (n_steps - 1) & 1, cb, lv.err)) {
+      tc::tc_fence_after();
+      emit<true, true>(sv, tmem + lane_base, kColDS, m0, nc, true, s_out, kColAS);
+      if (need_T) emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, true, t_out, kColAT);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc(tmem, 512);
+  }
+}
+
+// One block: the first CTA of every request at both levels, and a check of the
+// chain offsets and of every chain element id.  Level 0 gives request r
+// H * ceil(n_r / seg0) CTAs (H at least, for an empty chain's zero state, when
+// level 0 is the last); level 1 gives H.
+__global__ void __launch_bounds__(1024)
+compose_plan_kernel(const int32_t* __restrict__ ids, const int32_t* __restrict__ chain_off, int n_req, int H,
+                    int64_t n_pool, int64_t n_elems, int max_chain, int seg0, bool one_level,
+                    int32_t* __restrict__ first0, int32_t* __restrict__ first1, int32_t* err) {
+  __shared__ int scratch[1024 / 32 + 1];
+  int carry0 = 0, carry1 = 0;
+  for (int base = 0; base < n_req; base += 1024) {
+    const int r = base + threadIdx.x;
+    int w0 = 0, w1 = 0;
+    if (r < n_req) {
+      int n_r = chain_off[r + 1] - chain_off[r];
+      if (n_r < 0 || n_r > max_chain || chain_off[r] < 0 || chain_off[r + 1] > n_elems) set_err(err, PIC_ERR_RANGE);
+      n_r = min(max(n_r, 0), max_chain);
+      const int segs = n_r > 0 ? (n_r + seg0 - 1) / seg0 : 0;
+      w0 = H * (one_level ? max(segs, 1) : segs);
+      w1 = H;
+    }
+    int tot;
+    const int ex0 = block_exclusive_scan<1024>(w0, scratch, &tot);
+    if (r < n_req) first0[r] = carry0 + ex0;
+    carry0 += tot;
+    const int ex1 = block_exclusive_scan<1024>(w1, scratch, &tot);
+    if (r < n_req) first1[r] = carry1 + ex1;
+    carry1 += tot;
+  }
+  if (threadIdx.x == 0) {
+    first0[n_req] = carry0;
+    first1[n_req] = carry1;
+  }
+  if (threadIdx.x == 0 && (chain_off[0] != 0 || chain_off[n_req] != n_elems)) set_err(err, PIC_ERR_RANGE);
+  for (int64_t i = threadIdx.x; i < n_elems; i += blockDim.x)
+    if (ids[i] < 0 || (int64_t)ids[i] >= n_pool) set_err(err, PIC_ERR_RANGE);
+}
+
+struct CLayout {
+  bool one_level;
+  int seg0;
+  int64_t n_out0;  // level-0 outputs per chain when there are two levels
+  size_t off_first0, off_first1, off_T, off_S, total;
+};
+
+CLayout c_layout(int n_req, int max_chain, int H, int seg) {
+  CLayout L;
+  L.one_level = seg <= 1 || seg >= max_chain;
+  L.seg0 = L.one_level ? std::max(max_chain, 1) : seg;
+  L.n_out0 = L.one_level ? 0 : (max_chain + seg - 1) / seg;
+  const size_t inter = (size_t)n_req * H * L.n_out0 * (size_t)kMatBytes;
+  L.off_first0 = 0;
+  L.off_first1 = al256((size_t)(n_req + 1) * 4);
+  L.off_T = L.off_first1 + al256((size_t)(n_req + 1) * 4);
+  L.off_S = L.off_T + al256(inter);
+  L.total = L.off_S + al256(inter);
+  return L;
+}
+
+}  // namespace
+}  // namespace pic
+
+using namespace pic;
+
+extern "C" {
+
+int32_t pic_compose_segment(int32_t n_req, int64_t n_elems, int32_t max_chain, int32_t H, int32_t sms) {
+  if (n_req < 1 || H < 1 || max_chain < 1 || sms < 1 || n_elems < max_chain) return 0;
+  // one level when the chains alone fill the SMs; else the shortest segment whose
+  // level-0 CTAs (at most H * (ceil(n_elems / seg) + n_req - 1)) fit in one wave
+  if ((int64_t)n_req * H >= sms) return 0;
+  for (int seg = 2; seg < max_chain; ++seg)
+    if ((int64_t)H * ((n_elems + seg - 1) / seg + n_req - 1) <= sms) return seg;
+  return 0;
+}
+
+size_t pic_compose_workspace(int32_t n_req, int32_t max_chain, int32_t H, int32_t d, int32_t seg) {
+  if (n_req < 0 || max_chain < 0 || H < 1 || d != kCD || seg < 0) return 0;
+  return c_layout(n_req, max_chain, H, seg).total;
+}
+
+pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t n_pool, const int32_t* ids,
+                              const int32_t* chain_off, int32_t n_req, int64_t n_elems, int32_t max_chain,
+                              int32_t H, int32_t d, int32_t seg, float* out, void* ws, size_t ws_bytes,
+                              int32_t* err_flag, pic_stream_t stream) {
+  if (n_req < 0 || n_elems < 0 || H < 1 || max_chain < 0 || max_chain > n_elems || n_pool < 0 || seg < 0)
+    return PIC_ERR_INVALID;
+  if (d != kCD) return PIC_ERR_UNSUPPORTED;
+  if (n_req == 0) return PIC_OK;
+  if (n_elems > 0 && n_pool < 1) return PIC_ERR_INVALID;
+  if (!T_pool || !S_pool || !ids || !chain_off || !out || !err_flag) return PIC_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(T_pool) | reinterpret_cast<uintptr_t>(S_pool) |
+       reinterpret_cast<uintptr_t>(out)) & 15)
+    return PIC_ERR_INVALID;
+  const CLayout L = c_layout(n_req, max_chain, H, seg);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
+  const int64_t grid0 = (int64_t)H * ((n_elems + L.seg0 - 1) / L.seg0 + n_req);
+  if (grid0 > 0x7fffffff || (int64_t)n_req * H > 0x7fffffff) return PIC_ERR_UNSUPPORTED;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (cudaFuncSetAttribute(compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kCSmem) != cudaSuccess)
+    return PIC_ERR_CUDA;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  int32_t* first0 = reinterpret_cast<int32_t*>(w + L.off_first0);
+  int32_t* first1 = reinterpret_cast<int32_t*>(w + L.off_first1);
+  compose_plan_kernel<<<1, 1024, 0, s>>>(ids, chain_off, n_req, H, n_pool, n_elems, max_chain, L.seg0,
+                                         L.one_level, first0, first1, err_flag);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+
+  Level l0{};
+  l0.T_in = T_pool;
+  l0.S_in = S_pool;
+  l0.ids = ids;
+  l0.chain_off = chain_off;
+  l0.first = first0;
+  l0.n_pool = n_pool;
+  l0.n_elems = n_elems;
+  l0.n_req = n_req;
+  l0.H = H;
+  l0.max_chain = max_chain;
+  l0.seg = L.seg0;
+  l0.seg_prev = 1;
+  l0.level = 0;
+  l0.last = L.one_level;
+  l0.err = err_flag;
+  if (L.one_level) {
+    l0.S_out = out;
+    l0.out_stride = 1;
+  } else {
+    l0.T_out = reinterpret_cast<float*>(w + L.off_T);
+    l0.S_out = reinterpret_cast<float*>(w + L.off_S);
+    l0.out_stride = L.n_out0;
+  }
+  // level-0 CTAs: at most H * (ceil(n_elems / seg0) + n_req) (one more per chain
+  // for rounding, and one for an empty chain's zero state); the rest exit at once
+  compose_kernel<<<(unsigned)std::max<int64_t>(grid0, 1), kCThreads, kCSmem, s>>>(l0);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  if (L.one_level) return PIC_OK;
+
+  Level l1 = l0;
+  l1.T_in = l0.T_out;
+  l1.S_in = l0.S_out;
+  l1.ids = nullptr;
+  l1.first = first1;
+  l1.in_stride = L.n_out0;
+  l1.T_out = nullptr;
+  l1.S_out = out;
+  l1.out_stride = 1;
+  l1.seg = (int)std::max<int64_t>(L.n_out0, 1);
+  l1.seg_prev = L.seg0;
+  l1.level = 1;
+  l1.last = true;
+  compose_kernel<<<(unsigned)((int64_t)n_req * H), kCThreads, kCSmem, s>>>(l1);
+  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  return PIC_OK;
+}
+
+}  // extern "C"

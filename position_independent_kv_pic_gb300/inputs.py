@@ -30,7 +30,7 @@ import torch
 
 PAGE = 16  # tokens per KV page
 
-_STREAMS = ("lens", "order", "q", "kstore", "vstore", "knew", "vnew", "blocks", "qlen", "decode")
+_STREAMS = ("lens", "order", "q", "kstore", "vstore", "knew", "vnew", "blocks", "qlen", "decode", "states")
 
 
 @dataclass
@@ -198,6 +198,25 @@ def decode_inputs(wl: Workload):
     k = r.standard_normal((n, wl.Hkv, wl.d), dtype=np.float32)
     v = r.standard_normal((n, wl.Hkv, wl.d), dtype=np.float32)
     return _cast(q, wl.dtype), _cast(k, wl.dtype), _cast(v, wl.dtype)
+
+
+def linear_states(wl: Workload, H: int = 32, d: int = 128):
+    """Cached per-chunk pairs (T_c, S_c) of a linear-attention layer with H heads and
+    d x d states (HYPIC blog, section 2.1), for every distinct chunk of the workload,
+    and each request's chain of chunk ids in link order.
+
+    Recipe: T_c = g I + E with g ~ U[0.5, 0.75] per (chunk, head) and E i.i.d.
+    N(0, 0.01 / d) (so the spectral norm of T_c stays below about 0.95, like a
+    decayed delta-rule transition), S_c i.i.d. N(0, 1).  Returns (T, S, chains):
+    T, S float32 CPU tensors [n_store][H][d][d], chains a list of int32 arrays."""
+    r = _rngs(wl.seed)["states"]
+    n = len(wl.chunk_lens)
+    g = r.uniform(0.5, 0.75, size=(n, H, 1, 1)).astype(np.float32)
+    T = r.standard_normal((n, H, d, d), dtype=np.float32)
+    T *= np.float32(0.1 / np.sqrt(d))
+    T += g * np.eye(d, dtype=np.float32)
+    S = r.standard_normal((n, H, d, d), dtype=np.float32)
+    return torch.from_numpy(T), torch.from_numpy(S), [np.asarray(q.chunk_ids, np.int32) for q in wl.requests]
 
 
 def block_shuffle(wl: Workload, n_blocks: int) -> np.ndarray:

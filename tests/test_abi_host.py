@@ -151,3 +151,25 @@ def test_device_entry_points_reject_bad_arguments_without_launch():
     assert bad == pic.PIC_ERR_INVALID                                               # Hq % Hkv != 0
     assert lib.pic_link_attention(None, None, None, None, None, None, 10, 0, None, None, 0, 0, 32, 8, 128,
                                   0.1, None, None, 0, None, None) == pic.PIC_OK
+
+
+def test_compose_segment_and_workspace():
+    """Host sizing of the state composition: one level when the chains fill the SMs,
+    else the shortest segment whose level-0 CTAs fit one wave; the workspace holds
+    two levels' (T, S) intermediates only when there are two levels."""
+    assert pic.pic_compose_segment(16, 264, 30, 32, 152) == 0          # 512 chains: one level
+    seg = pic.pic_compose_segment(1, 100, 100, 32, 152)
+    assert seg == 25 and 32 * -(-100 // seg) <= 152 and 32 * -(-100 // (seg - 1)) > 152
+    assert pic.pic_compose_segment(1, 3, 3, 1, 152) == 2
+    assert pic.pic_compose_segment(0, 0, 0, 32, 152) == 0
+    one = pic.pic_compose_workspace(1, 100, 32, 128, 0)
+    two = pic.pic_compose_workspace(1, 100, 32, 128, 25)
+    assert 0 < one < 4096 and two >= one + 2 * 32 * 4 * 128 * 128 * 4
+    assert pic.pic_compose_workspace(1, 100, 32, 64, 25) == 0          # d = 128 only
+    lib = pic.load()
+    assert lib.pic_compose_states(None, None, 0, None, None, 0, 0, 0, 32, 128, 0, None, None, 0, None,
+                                  None) == pic.PIC_OK                  # no requests: a no-op
+    assert lib.pic_compose_states(None, None, 4, None, None, 1, 5, 6, 32, 128, 0, None, None, 0, None,
+                                  None) == pic.PIC_ERR_INVALID         # max_chain > n_elems
+    assert lib.pic_compose_states(None, None, 4, None, None, 1, 5, 5, 32, 64, 0, None, None, 0, None,
+                                  None) == pic.PIC_ERR_UNSUPPORTED
