@@ -23,7 +23,8 @@
 // by bulk copies; warps 0-7 convert it into one of two bf16 B buffers while the
 // tensor cores work on the other, and run the epilogue (TMEM -> + S_i -> split ->
 // TMEM), reading S_i straight from global memory one step ahead; warp 9 lane 0
-// issues the MMAs.  The critical path of a step is its MMAs plus the epilogue.
+// issues the MMAs.  The S products and the T products are committed apart, so that
+// each epilogue overlaps the other's MMAs.
 // Every wait is bounded.
 #include <algorithm>
 
@@ -58,7 +59,10 @@ constexpr int kCopy = 16384;                          // bytes per bulk copy
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct CBars {
-  uint64_t t_full, t_empty, b_full[2], a_full, d_full;  // b_full per B buffer: a phase per use
+  uint64_t t_full, t_empty;
+  uint64_t b_full[2];    // per B buffer: one phase per use
+  uint64_t a_s, a_t;     // A_S / A_T written for the next step
+  uint64_t d_s, d_t;     // the step's S / T products complete
   uint32_t tmem;
   int abort;
 };
@@ -91,6 +95,18 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity, CBars* cb, int32_t* err) {
   if (tc::mbar_wait(bar, parity, &cb->abort, kCWaitNs)) return true;
   set_err(err, PIC_ERR_TIMEOUT);
+  *reinterpret_cast<volatile int*>(&cb->abort) = 1;
+  return false;
+}
+
+// The same for a whole warp that goes on to warp-collective work (TMEM accesses):
+// every lane waits, and the outcome is the same in all lanes (a lane that saw the
+// phase complete gives up with the others when one of them ran out), so that the
+// warp never reaches a .sync.aligned instruction diverged.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, CBars* cb, int32_t* err) {
+  const bool ok = tc::mbar_wait(bar, parity, &cb->abort, kCWaitNs);
+  if (__all_sync(0xffffffffu, ok)) return true;
+  if (!ok) set_err(err, PIC_ERR_TIMEOUT);
   *reinterpret_cast<volatile int*>(&cb->abort) = 1;
   return false;
 }
@@ -201,8 +217,10 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
     tc::mbar_init(&cb->t_empty, kCWorkers);
     tc::mbar_init(&cb->b_full[0], kCWorkers);
     tc::mbar_init(&cb->b_full[1], kCWorkers);
-    tc::mbar_init(&cb->a_full, kCWorkers);
-    tc::mbar_init(&cb->d_full, 1);
+    tc::mbar_init(&cb->a_s, kCWorkers);
+    tc::mbar_init(&cb->a_t, kCWorkers);
+    tc::mbar_init(&cb->d_s, 1);
+    tc::mbar_init(&cb->d_t, 1);
     cb->abort = 0;
     tc::fence_mbar_init();
   }
@@ -230,36 +248,45 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---- MMA issue: D_S = A_S B_k (and D_T = A_T B_k), three bf16 part products each
+    // ---- MMA issue: D_S = A_S B_k, then D_T = A_T B_k, three bf16 part products
+    // each, committed apart so that the S epilogue overlaps the T products and the
+    // T epilogue the next S products
     if (lane == 0) {
       constexpr uint32_t kHi = tc::sw128_desc_hi(1024);
       const uint32_t b_lo0 = tc::sw128_desc_lo(tc::smem_addr(sm + kOffB), 16);
-      int issued = 0;
-      for (int k = 0; k < n_steps; ++k) {
-        if (!wait_bar(&cb->b_full[k & 1], (k >> 1) & 1, cb, lv.err)) break;
-        if (!wait_bar(&cb->a_full, k & 1, cb, lv.err)) break;
-        tc::tc_fence_after();
-        const uint32_t b_lo = b_lo0 + (uint32_t)((k & 1) * (kBBytes >> 4));
+      auto products = [&](uint32_t d_col, uint32_t a_col, uint32_t b_lo) {
 #pragma unroll
         for (int ks = 0; ks < kCD / 16; ++ks) {
           const uint32_t boff = (uint32_t)(((ks >> 2) * kBHalf + (ks & 3) * 32) >> 4);
           const uint64_t bh = tc::desc_join(b_lo + boff, kHi);
           const uint64_t bl = tc::desc_join(b_lo + boff + (kBPart >> 4), kHi);
-          const uint32_t acc = ks > 0 ? 1u : 0u;
-          tc::mma_bf16_ts(tmem + kColDS, tmem + kColAS + ks * 8, bh, kCIdesc, acc);
-          tc::mma_bf16_ts(tmem + kColDS, tmem + kColAS + ks * 8, bl, kCIdesc, 1u);
-          tc::mma_bf16_ts(tmem + kColDS, tmem + kColAS + 64 + ks * 8, bh, kCIdesc, 1u);
-          if (need_T) {
-            tc::mma_bf16_ts(tmem + kColDT, tmem + kColAT + ks * 8, bh, kCIdesc, acc);
-            tc::mma_bf16_ts(tmem + kColDT, tmem + kColAT + ks * 8, bl, kCIdesc, 1u);
-            tc::mma_bf16_ts(tmem + kColDT, tmem + kColAT + 64 + ks * 8, bh, kCIdesc, 1u);
-          }
+          tc::mma_bf16_ts(tmem + d_col, tmem + a_col + ks * 8, bh, kCIdesc, ks > 0 ? 1u : 0u);
+          tc::mma_bf16_ts(tmem + d_col, tmem + a_col + ks * 8, bl, kCIdesc, 1u);
+          tc::mma_bf16_ts(tmem + d_col, tmem + a_col + 64 + ks * 8, bh, kCIdesc, 1u);
         }
-        tc::mma_commit(&cb->d_full);
+      };
+      // every commit's arrival lands before the CTA exits: the thread waits for the
+      // last phase of each barrier it committed to
+      int issued = 0, issued_t = 0;
+      for (int k = 0; k < n_steps; ++k) {
+        if (!wait_bar(&cb->b_full[k & 1], (k >> 1) & 1, cb, lv.err)) break;
+        if (!wait_bar(&cb->a_s, k & 1, cb, lv.err)) break;
+        tc::tc_fence_after();
+        const uint32_t b_lo = b_lo0 + (uint32_t)((k & 1) * (kBBytes >> 4));
+        products(kColDS, kColAS, b_lo);
+        tc::mma_commit(&cb->d_s);
         issued = k + 1;
+        if (need_T) {
+          if (!wait_bar(&cb->a_t, k & 1, cb, lv.err)) break;
+          tc::tc_fence_after();
+          products(kColDT, kColAT, b_lo);
+          tc::mma_commit(&cb->d_t);
+          issued_t = k + 1;
+        }
       }
       const int no_abort = 0;
-      if (issued > 0) tc::mbar_wait(&cb->d_full, (issued - 1) & 1, &no_abort, kCWaitNs);
+      if (issued > 0) tc::mbar_wait(&cb->d_s, (issued - 1) & 1, &no_abort, kCWaitNs);
+      if (issued_t > 0) tc::mbar_wait(&cb->d_t, (issued_t - 1) & 1, &no_abort, kCWaitNs);
     }
     __syncwarp();
   } else {
@@ -293,7 +320,7 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
     };
     int tu = 0;  // staged T_i converted
     auto next_B = [&]() -> bool {  // the next staged T_i into B buffer tu & 1
-      if (!wait_bar(&cb->t_full, tu & 1, cb, lv.err)) return false;
+      if (!wait_bar_warp(&cb->t_full, tu & 1, cb, lv.err)) return false;
       convert_T(tu & 1);
       tc::fence_proxy_async_smem();  // generic-proxy writes of B -> the MMA's reads
       tc::mbar_arrive(&cb->b_full[tu & 1]);
@@ -301,40 +328,49 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
       ++tu;
       return true;
     };
-    auto signal_a = [&]() {
+    auto signal = [&](uint64_t* bar) {
       tc::tmem_st_wait();
       tc::tc_fence_before();
-      tc::mbar_arrive(&cb->a_full);
+      tc::mbar_arrive(bar);
     };
     // first element: the accumulators (or the output, for a one-element segment)
     load_col64(elem(lv.S_in, b), m0, nc, sv);
     emit<true, false>(sv, tmem + lane_base, 0, m0, nc, n == 1, s_out, kColAS);
+    if (n_steps > 0) signal(&cb->a_s);
     if (need_T) {
       load_col64(elem(lv.T_in, b), m0, nc, sv);
       emit<true, false>(sv, tmem + lane_base, 0, m0, nc, n == 1, t_out, kColAT);
+      if (n_steps > 0) signal(&cb->a_t);
     }
     if (n_steps > 0) {
-      signal_a();
       load_col64(elem(lv.S_in, b + 1), m0, nc, sv);
       ok = next_B();
     }
     // steps 0 .. n_steps - 2 feed the next step; the last writes the output (kept
     // out of the loop so that the output addresses are not held across it)
     for (int k = 0; ok && k + 1 < n_steps; ++k) {
-      // B buffer (k + 1) & 1 was read by MMA k - 1, complete: convert T_{b+k+2}
-      // while MMA k runs
+      // B buffer (k + 1) & 1 was read by step k - 1's products, complete: convert
+      // T_{b+k+2} while step k's run
       if (!(ok = next_B())) break;
-      if (!(ok = wait_bar(&cb->d_full, k & 1, cb, lv.err))) break;
+      if (!(ok = wait_bar_warp(&cb->d_s, k & 1, cb, lv.err))) break;
       tc::tc_fence_after();
       emit<true, true>(sv, tmem + lane_base, kColDS, m0, nc, false, nullptr, kColAS);
-      if (need_T) emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, false, nullptr, kColAT);
-      signal_a();
+      signal(&cb->a_s);
       load_col64(elem(lv.S_in, b + k + 2), m0, nc, sv);
+      if (need_T) {
+        if (!(ok = wait_bar_warp(&cb->d_t, k & 1, cb, lv.err))) break;
+        tc::tc_fence_after();
+        emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, false, nullptr, kColAT);
+        signal(&cb->a_t);
+      }
     }
-    if (ok && n_steps > 0 && wait_bar(&cb->d_full, (n_steps - 1) & 1, cb, lv.err)) {
+    if (ok && n_steps > 0 && wait_bar_warp(&cb->d_s, (n_steps - 1) & 1, cb, lv.err)) {
       tc::tc_fence_after();
       emit<true, true>(sv, tmem + lane_base, kColDS, m0, nc, true, s_out, kColAS);
-      if (need_T) emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, true, t_out, kColAT);
+      if (need_T && wait_bar_warp(&cb->d_t, (n_steps - 1) & 1, cb, lv.err)) {
+        tc::tc_fence_after();
+        emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, true, t_out, kColAT);
+      }
     }
   }
   tc::tc_fence_before();

@@ -51,18 +51,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait for the phase with the given parity.  Polls, then checks the
-// global timer every 256 polls; gives up after `limit_ns` or when *abort is set
-// by another role, returning false.  Never traps.
+// Bounded wait for the phase with the given parity.  Polls, then every 256 polls
+// checks *abort (set by another role) and the SM cycle counter, giving up (false)
+// after about `limit_ns` at up to 2 GHz (longer at lower clocks).  The SM's own
+// cycle counter is monotonic, unlike a timer that the driver may step; a signed
+// difference keeps a counter step from ending the wait early.  Never traps.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort,
                                           uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  const long long c0 = clock64();
+  const long long limit = (long long)(2 * limit_ns);
   for (uint32_t n = 1;; ++n) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((n & 255u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) return false;
+      if (clock64() - c0 > limit) return false;
     }
   }
 }
