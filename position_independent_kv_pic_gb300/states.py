@@ -65,3 +65,41 @@ class ComposeBatch:
         mat = self.d * self.d * 4
         nonempty = sum(1 for c in self.chains if len(c))
         return (2 * self.n_elems - nonempty + self.n_req) * self.H * mat
+
+
+def _main():
+    """Run the composition on a seeded preset's chunk chains and print one JSON line
+    (mean time of the timed runs, algorithmic bytes, GB/s)."""
+    import argparse
+    import json
+
+    from . import build, inputs
+
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--workload", default="long_context_100x1000", choices=sorted(inputs.PRESETS))
+    ap.add_argument("--heads", type=int, default=32)
+    ap.add_argument("--seg", type=int, default=None, help="level-0 segment (default: one wave of SMs)")
+    ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--runs", type=int, default=2)
+    a = ap.parse_args()
+    build.build()
+    wl = inputs.PRESETS[a.workload]()
+    T, S, chains = inputs.linear_states(wl, H=a.heads, d=128)
+    b = ComposeBatch(T, S, chains, seg=a.seg)
+    for _ in range(a.warmup):
+        b.run()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.runs)]
+    for e0, e1 in ev:
+        e0.record()
+        b.run()
+        e1.record()
+    torch.cuda.synchronize()
+    if b.error():
+        raise SystemExit(f"device error {b.error()}")
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / max(len(ev), 1)
+    print(json.dumps({"workload": a.workload, "heads": a.heads, "seg": b.seg, "launches": b.launches,
+                      "ms": ms, "bytes": b.algorithmic_bytes, "GB/s": b.algorithmic_bytes / (ms / 1e3) / 1e9}))
+
+
+if __name__ == "__main__":
+    _main()
