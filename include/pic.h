@@ -176,7 +176,15 @@ pic_status pic_select_rows(const int32_t* chunk_lens, const int32_t* chunk_off,
  *   rot     out [rot_off[n_req]]    re-rotation work (tab = flat chunk index)
  *   row_block, row_slot out [n_rows]: pool block and slot of each recomputed row
  *                 (row order as written by pic_select_rows; row_off gives n_rows)
+ *   page_tab out [page_off[n_req]] or NULL: per link page, the offset-table row
+ *                 that rotates its K to the global position (the flat chunk index
+ *                 for cached pages of chunks after the first), -1 for pages that
+ *                 need none (chunk 0, fresh and query pages); the input of
+ *                 pic_link_attention_ror
  *   row_off [n_req+1]
+ * With k_dst_blocks NULL the cached pages of the list are the cached blocks
+ * themselves: rotated in place by pic_rerotate_k, or left as cached for
+ * rotate-on-read.
  * Device errors: PIC_ERR_RANGE when a count disagrees with the offsets. */
 pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
                             const int32_t* q_len, const int32_t* k, int32_t n_req,
@@ -186,7 +194,7 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
                             const int32_t* fresh_blocks, const int32_t* row_off,
                             const int32_t* page_off, const int32_t* rot_off,
                             pic_link_page* pages, pic_rot_page* rot, int32_t* row_block,
-                            int32_t* row_slot, int32_t* err_flag, pic_stream_t stream);
+                            int32_t* row_slot, int32_t* page_tab, int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * a2  RoPE tables (RoPE article 2.2 and footnote 3).
@@ -333,6 +341,32 @@ pic_status pic_link_attention_noalloc(const void* q, const float* row_table, con
                                       const int32_t* page_off, int32_t n_req, int64_t n_rows,
                                       int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out,
                                       int32_t* err_flag, pic_stream_t stream);
+
+/* ------------------------------------------------------------------------
+ * a3+a5  Rotate-on-read link attention (RoPE article 3.3: the rotary correction
+ *     applied where the kernel reads the cache, a mixed reuse + correction
+ *     path).  The cached K pages stay as cached (local positions); the attention
+ *     kernel rotates each K page by its table row in shared memory before the
+ *     S product, with the arithmetic of pic_rerotate_k (same table, same
+ *     rounding), so its K — and with the same unit plan its output — is bit for
+ *     bit that of pic_rerotate_k followed by pic_link_attention.  No re-rotation
+ *     pass and no per-request copies of shared chunks.
+ * ------------------------------------------------------------------------
+ *   arguments as pic_link_attention, plus
+ *   page_tab   [page_off[n_req]] int32: table row of each link page, < 0 = none
+ *              (pic_splice_pages' page_tab output, with k_dst_blocks NULL so that
+ *              the list points at the cached blocks)
+ *   rot_table  [n_tab][d/2][4] fp32 offset table (pic_rope_table over chunk_start)
+ * Tensor-core shapes only (bf16 pools, d = 128, Hq / Hkv in {1, 2, 4, 8, 16});
+ * otherwise PIC_ERR_UNSUPPORTED.  A table row >= n_tab sets PIC_ERR_RANGE in
+ * *err_flag and that page is read unrotated. */
+pic_status pic_link_attention_ror(const void* q, const float* row_table, const int32_t* rows,
+                                  const int32_t* row_off, const void* k_pool, const void* v_pool,
+                                  int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                                  const int32_t* page_tab, const float* rot_table, int64_t n_tab,
+                                  const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                                  int32_t Hkv, int32_t d, float scale, void* out, void* ws, size_t ws_bytes,
+                                  int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Decode after link (EPIC review: the query and the tokens decoded after it

@@ -24,7 +24,7 @@ __all__ = [
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
     "pic_decode_workspace", "pic_decode_attention", "pic_rope_cached_k",
-    "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
+    "pic_compose_segment", "pic_compose_workspace", "pic_compose_states", "pic_link_attention_ror",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -49,6 +49,7 @@ EXPORTED = (
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "pic_decode_workspace", "pic_decode_attention",
     "pic_rope_cached_k", "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
+    "pic_link_attention_ror",
 )
 
 
@@ -78,7 +79,7 @@ _SIGS = {
     "pic_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pic_select_rows": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P]),
     "pic_splice_pages": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                        _P, _P, _P, _P, _P, _P]),
+                                        _P, _P, _P, _P, _P, _P, _P]),
     "pic_rope_table": (ctypes.c_int, [_P, _I64, _I32, _F64, _P, _P]),
     "pic_rerotate_k": (ctypes.c_int, [_P, _I64, ctypes.c_int, _I32, _I32, _P, _I64, _P, _I64, _P, _P]),
     "pic_write_fresh_kv": (ctypes.c_int, [_P, _P, _I64, ctypes.c_int, _I32, _I32, _P, _P, _P, _P, _P,
@@ -92,6 +93,8 @@ _SIGS = {
     "pic_decode_workspace": (_SZ, [_I32, _I32, _I32, _I32, ctypes.c_int]),
     "pic_rope_cached_k": (ctypes.c_int, [_P, _I64, ctypes.c_int, _I32, _I32, _P, _P, _P, _I32, _P, _P, _I32, _I64,
                                          _P, _P, _P, _I64, _P, _P]),
+    "pic_link_attention_ror": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _P, _I64, _P,
+                                              _I32, _I64, _I32, _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
     "pic_compose_segment": (_I32, [_I32, _I64, _I32, _I32, _I32]),
     "pic_compose_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "pic_compose_states": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _SZ,
@@ -187,13 +190,13 @@ def pic_select_rows(chunk_lens, chunk_off, q_len, k, row_off, rows, chunk_start,
 
 def pic_splice_pages(chunk_lens, chunk_off, q_len, k, chunk_start, chunk_page_off, k_src_blocks, k_dst_blocks,
                      v_blocks, fresh_off, fresh_blocks, row_off, page_off, rot_off, pages, rot, row_block,
-                     row_slot, err_flag, stream=None):
+                     row_slot, err_flag, stream=None, page_tab=None):
     n_req = q_len.numel()
     _check(load().pic_splice_pages(
         _ptr(chunk_lens), _ptr(chunk_off), _ptr(q_len), _ptr(k), n_req, _ptr(chunk_start), _ptr(chunk_page_off),
         _ptr(k_src_blocks), _ptr(k_dst_blocks), _ptr(v_blocks), _ptr(fresh_off), _ptr(fresh_blocks), _ptr(row_off),
-        _ptr(page_off), _ptr(rot_off), _ptr(pages), _ptr(rot), _ptr(row_block), _ptr(row_slot), _ptr(err_flag),
-        _stream(stream)), "pic_splice_pages")
+        _ptr(page_off), _ptr(rot_off), _ptr(pages), _ptr(rot), _ptr(row_block), _ptr(row_slot), _ptr(page_tab),
+        _ptr(err_flag), _stream(stream)), "pic_splice_pages")
 
 
 def pic_rope_table(pos, d: int, theta: float, table, stream=None):
@@ -243,6 +246,17 @@ def pic_decode_attention(q, q_table, k_pool, v_pool, dtype: int, pages, page_off
         _ptr(q), _ptr(q_table), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype), _ptr(pages), _ptr(page_off),
         int(n_req), int(Hq), int(Hkv), int(d), float(scale), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),
         _stream(stream)), "pic_decode_attention")
+
+
+def pic_link_attention_ror(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, pages, page_tab, rot_table,
+                           page_off, n_req: int, n_rows: int, Hq: int, Hkv: int, d: int, scale: float, out, ws,
+                           err_flag, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pic_link_attention_ror(
+        _ptr(q), _ptr(row_table), _ptr(rows), _ptr(row_off), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype),
+        _ptr(pages), _ptr(page_tab), _ptr(rot_table), rot_table.shape[0], _ptr(page_off), int(n_req), int(n_rows),
+        int(Hq), int(Hkv), int(d), float(scale), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)),
+        "pic_link_attention_ror")
 
 
 def pic_compose_segment(n_req: int, n_elems: int, max_chain: int, H: int, sms: int) -> int:

@@ -64,7 +64,7 @@ constexpr int kPageHalfBytes = 1024;           // 8 rows x 64 columns
 constexpr int kOffQ = 0;                  // Q tiles 0 and 1
 constexpr int kOffSlot = kQTiles * kOpBytes;
 constexpr int kOffBar = kOffSlot + kSlots * kOpBytes;
-constexpr int kOffXch = kOffBar + 256;  // partial row maxima / sums of the two halves of each Q tile
+constexpr int kOffXch = kOffBar + 512;  // partial row maxima / sums of the two halves of each Q tile
 constexpr int kSmemBytes = kOffXch + kQTiles * 2 * kM * (int)sizeof(float);
 static_assert(kSmemBytes <= 232448, "shared memory per block");
 constexpr uint32_t kTmemCols = 512;                // S0 | S1 | O0 | O1
@@ -349,6 +349,11 @@ struct TcArgs {
   int64_t num_blocks;
   int Hq, Hkv, G, R;
   float scale_log2;
+  // rotate-on-read (page_tab != nullptr): K of page p is rotated by table row
+  // page_tab[p] (none when negative) in shared memory before the S product
+  const int32_t* page_tab;
+  const float4* rot_tab;  // [n_tab][kD / 2] {cos_hi, sin_hi, cos_lo, sin_lo}
+  int64_t n_tab;
 };
 
 constexpr int kUnitRing = 2;                  // unit indices in flight from the producer
@@ -357,13 +362,14 @@ constexpr int kUnitReaders = 1 + 2 + 4 * kSmWarpgroups;  // MMA thread, 2 V-zero
 struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
   uint64_t vz_done[kSlots];  // V tile t (t % kSlots) checked and its invalid rows zeroed
+  uint64_t kr_done[kSlots];  // rotate-on-read: K tile t (t % kSlots) rotated to its global positions
   uint64_t q_full[kQTiles], q_free[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
   int unit_idx[kUnitRing];
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier area");
+static_assert(sizeof(Bars) <= 512, "barrier area");
 
 __device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
   return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
@@ -515,6 +521,11 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
   const uint32_t k_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), 16);
   const uint32_t v_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), kPageHalfBytes);
   uint32_t ld = 0, uq[kQTiles] = {0, 0}, c[kQTiles] = {0, 0};
+  // K load l (even): landed, and rotated when rotating on read
+  auto wait_k = [&](uint32_t l) -> bool {
+    if (!wait_bar(b, &b->kv_full[l % kSlots], (l / kSlots) & 1)) return false;
+    return a.page_tab == nullptr || wait_bar(b, &b->kr_done[(l / 2) % kSlots], ((l / 2) / kSlots) & 1);
+  };
   auto issue_s = [&](int i, int slot) {
     const uint32_t qa = q_lo + i * (kOpBytes >> 4), kb = k_lo + slot * (kOpBytes >> 4);
 #pragma unroll
@@ -549,7 +560,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
     tc::tc_fence_after();
     {  // S for the first key tile
       const int ks = ld % kSlots;
-      if (!wait_bar(b, &b->kv_full[ks], (ld / kSlots) & 1)) { fail(b, a.err); return; }
+      if (!wait_k(ld)) { fail(b, a.err); return; }
       tc::tc_fence_after();
       issue_s(0, ks);
       tc::mma_commit(&b->s_full[0]);
@@ -579,7 +590,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
         tc::tc_fence_after();
         issue_pv(i, vs, j > 0);
         if (more) {
-          if (i == 0 && !wait_bar(b, &b->kv_full[ns], (nld / kSlots) & 1)) { fail(b, a.err); return; }
+          if (i == 0 && !wait_k(nld)) { fail(b, a.err); return; }
           tc::tc_fence_after();
           issue_s(i, ns);
           tc::mma_commit(&b->s_full[i]);
@@ -651,6 +662,55 @@ qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
 // Masked keys get weight 0 and 0 * V must stay 0 even if a slot outside a page's
 // valid range holds stale non-finite bits: once a V tile has landed, the rows of
 // slots that hold no valid key are zeroed before the MMA issuer uses the slot.
+// One 32-bit word (two bf16 dimensions i, i + 1) of a K row's low half against the
+// matching word of its high half (dimensions i + 64, i + 65), rotated in place
+// exactly as the re-rotation pass does it (rope_rotate_bf16in, one bf16 rounding).
+__device__ __forceinline__ void rotate_word(uint32_t& wl, uint32_t& wh, const float4& t0, const float4& t1) {
+  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wl));
+  const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh));
+  float a0, b0, a1, b1;
+  rope_rotate_bf16in(x.x, y.x, t0, a0, b0);
+  rope_rotate_bf16in(x.y, y.y, t1, a1, b1);
+  __nv_bfloat162 p = __floats2bfloat162_rn(a0, a1), q = __floats2bfloat162_rn(b0, b1);
+  wl = *reinterpret_cast<uint32_t*>(&p);
+  wh = *reinterpret_cast<uint32_t*>(&q);
+}
+
+// Rotate-on-read: rotate in place the pages of the key tile at `ksm` whose table
+// row (lane j holds page j's) is not negative, by R(theta * Delta) of that row —
+// the same table and arithmetic as pic_rerotate_k, so the K the MMA reads is bit
+// for bit the one the re-rotation pass would have written.  Warps 2-3 (t64 =
+// 0..63): position pos of rows r0 = t64 / 8 and r0 + 8 of every page, i.e. the
+// 16-byte chunk c = pos ^ r0 (the 128-byte swizzle) of both column halves.
+__device__ __forceinline__ void rotate_k_tile(uint8_t* ksm, int tab_lane, const float4* __restrict__ rot_tab,
+                                              int t64) {
+  const int pos = t64 & 7, r0 = t64 >> 3, c = pos ^ r0;
+#pragma unroll 1
+  for (int jj = 0; jj < kPagesPerKt; ++jj) {
+    const int tab = __shfl_sync(0xffffffffu, tab_lane, jj);
+    if (tab < 0) continue;
+    const float4* cs = rot_tab + (int64_t)tab * (kD / 2) + 8 * c;
+    uint8_t* p0 = ksm + jj * kPageBytes + r0 * 128 + pos * 16;  // row r0: group 0, low half
+    uint8_t* p1 = p0 + kGroupBytes;                              // row r0 + 8: group 1
+    uint4 l0 = *reinterpret_cast<const uint4*>(p0), h0 = *reinterpret_cast<const uint4*>(p0 + kPageHalfBytes);
+    uint4 l1 = *reinterpret_cast<const uint4*>(p1), h1 = *reinterpret_cast<const uint4*>(p1 + kPageHalfBytes);
+    uint32_t* wl0 = reinterpret_cast<uint32_t*>(&l0);
+    uint32_t* wh0 = reinterpret_cast<uint32_t*>(&h0);
+    uint32_t* wl1 = reinterpret_cast<uint32_t*>(&l1);
+    uint32_t* wh1 = reinterpret_cast<uint32_t*>(&h1);
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 t0 = __ldg(cs + 2 * w), t1 = __ldg(cs + 2 * w + 1);
+      rotate_word(wl0[w], wh0[w], t0, t1);
+      rotate_word(wl1[w], wh1[w], t0, t1);
+    }
+    *reinterpret_cast<uint4*>(p0) = l0;
+    *reinterpret_cast<uint4*>(p0 + kPageHalfBytes) = h0;
+    *reinterpret_cast<uint4*>(p1) = l1;
+    *reinterpret_cast<uint4*>(p1 + kPageHalfBytes) = h1;
+  }
+}
+
 __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31, wz = (threadIdx.x >> 5) - 2;  // 0, 1
   uint32_t ld = 0;
@@ -668,6 +728,23 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
       const int plo = pvalid ? (int16_t)(pg.w & 0xffff) : 0;
       const int phi = pvalid ? (int16_t)(pg.w >> 16) : 0;
       const bool full = __all_sync(0xffffffffu, lane >= kPagesPerKt || (plo == 0 && phi == PIC_PAGE));
+      if (a.page_tab != nullptr) {  // rotate-on-read: K of this tile before its S product
+        int tab = -1;
+        if (pvalid) {
+          tab = __ldg(a.page_tab + tm.page_begin + kt * kPagesPerKt + lane);
+          if (tab >= a.n_tab) {
+            set_err(a.err, PIC_ERR_RANGE);
+            tab = -1;
+          }
+        }
+        const int ks = ld % kSlots;
+        const bool got = wait_bar(b, &b->kv_full[ks], (ld / kSlots) & 1);
+        if (!__all_sync(0xffffffffu, got)) { fail(b, a.err); return; }
+        rotate_k_tile(smem + kOffSlot + ks * kOpBytes, tab, a.rot_tab, 32 * wz + lane);
+        tc::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) tc::mbar_arrive(&b->kr_done[(ld / 2) % kSlots]);
+      }
       const uint32_t vld = ld + 1;
       const int vs = vld % kSlots;
       // waiting for every V tile (not only partial ones) keeps these warps at most
@@ -906,6 +983,7 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mbar_init(&b->kv_full[s], 1);
       tc::mbar_init(&b->kv_empty[s], 1);
       tc::mbar_init(&b->vz_done[s], 2);
+      tc::mbar_init(&b->kr_done[s], 2);
     }
     for (int i = 0; i < kQTiles; ++i) {
       tc::mbar_init(&b->q_full[i], 1);
@@ -1147,7 +1225,8 @@ bool tc_shape(pic_dtype dt, int Hq, int Hkv, int d) {
 pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows, const int32_t* row_off,
                      const void* k_pool, const void* v_pool, int64_t num_blocks, const pic_link_page* pages,
                      const int32_t* page_off, int32_t n_req, int32_t Hq, int32_t Hkv, float scale, void* out,
-                     uint8_t* w, const WsLayout& L, int split_sms, int32_t* err_flag, cudaStream_t s) {
+                     uint8_t* w, const WsLayout& L, int split_sms, int32_t* err_flag, cudaStream_t s,
+                     const int32_t* page_tab = nullptr, const float* rot_table = nullptr, int64_t n_tab = 0) {
   const int G = Hq / Hkv;
   if (n_req > kMaxPlanReqs) return PIC_ERR_UNSUPPORTED;
   if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
@@ -1199,6 +1278,9 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   a.G = G;
   a.R = R;
   a.scale_log2 = scale * 1.4426950408889634f;
+  a.page_tab = page_tab;
+  a.rot_tab = reinterpret_cast<const float4*>(rot_table);
+  a.n_tab = n_tab;
   const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
   link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
@@ -1253,6 +1335,27 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
   }
   return launch_attention_simt(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
                                n_req, n_rows, Hq, Hkv, d, scale, out, s);
+}
+
+pic_status pic_link_attention_ror(const void* q, const float* row_table, const int32_t* rows,
+                                  const int32_t* row_off, const void* k_pool, const void* v_pool,
+                                  int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                                  const int32_t* page_tab, const float* rot_table, int64_t n_tab,
+                                  const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                                  int32_t Hkv, int32_t d, float scale, void* out, void* ws, size_t ws_bytes,
+                                  int32_t* err_flag, pic_stream_t stream) {
+  const pic_status st = check_attention_args(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages,
+                                             page_off, n_req, n_rows, Hq, Hkv, d, scale, out, err_flag);
+  if (st != PIC_OK) return st;
+  if (n_tab < 0) return PIC_ERR_INVALID;
+  if (!tc_shape(dtype, Hq, Hkv, d)) return PIC_ERR_UNSUPPORTED;
+  if (n_req == 0 || n_rows == 0) return PIC_OK;
+  if (!page_tab || (n_tab > 0 && !rot_table) || (reinterpret_cast<uintptr_t>(rot_table) & 15)) return PIC_ERR_INVALID;
+  const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
+  return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
+                   out, static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, (cudaStream_t)stream,
+                   page_tab, rot_table, n_tab);
 }
 
 pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, float* d_mnmajor, float* d_tmem_a,

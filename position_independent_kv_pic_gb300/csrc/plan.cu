@@ -105,7 +105,8 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
               const int32_t* __restrict__ fresh_blocks, const int32_t* __restrict__ row_off,
               const int32_t* __restrict__ page_off, const int32_t* __restrict__ rot_off,
               pic_link_page* __restrict__ pages, pic_rot_page* __restrict__ rot,
-              int32_t* __restrict__ row_block, int32_t* __restrict__ row_slot, int32_t* err) {
+              int32_t* __restrict__ row_block, int32_t* __restrict__ row_slot, int32_t* __restrict__ page_tab,
+              int32_t* err) {
   __shared__ int scratch[kPlanThreads / 32 + 1];
   __shared__ int g_link[kPlanThreads + 1], g_row[kPlanThreads + 1];
   __shared__ int g_rot[kPlanThreads], g_fresh[kPlanThreads];
@@ -168,6 +169,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
         pg.k_block = blk; pg.v_block = blk; pg.gpos0 = g_s[w] + PIC_PAGE * f;
         pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, g_m[w] - PIC_PAGE * f);
         pages[pi] = pg;
+        if (page_tab != nullptr) page_tab[pi] = -1;
       } else {  // cached page j that keeps at least one slot
         const int t = f - g_fp[w];
         const int j = g_j0[w] + t;
@@ -180,6 +182,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
         pg.lo = (int16_t)max(0, g_m[w] - PIC_PAGE * j);
         pg.hi = (int16_t)min(PIC_PAGE, g_L[w] - PIC_PAGE * j);
         pages[pi] = pg;
+        if (page_tab != nullptr) page_tab[pi] = (cw > c0) ? cw : -1;
         if (cw > c0) {
           const int oi = obeg + rot_base + g_rot[w] + t;
           if (oi >= oend) { set_err(err, PIC_ERR_RANGE); continue; }
@@ -216,6 +219,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
     pg.k_block = blk; pg.v_block = blk; pg.gpos0 = T + PIC_PAGE * f;
     pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, q - PIC_PAGE * f);
     pages[pi] = pg;
+    if (page_tab != nullptr) page_tab[pi] = -1;
   }
   for (int j = item0; j < q; j += stride) {
     const int ri = rbeg + row_base + j, fi = fbeg + fresh_base + j / PIC_PAGE;
@@ -284,7 +288,7 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
                             const int32_t* fresh_off, const int32_t* fresh_blocks,
                             const int32_t* row_off, const int32_t* page_off, const int32_t* rot_off,
                             pic_link_page* pages, pic_rot_page* rot, int32_t* row_block,
-                            int32_t* row_slot, int32_t* err_flag, pic_stream_t stream) {
+                            int32_t* row_slot, int32_t* page_tab, int32_t* err_flag, pic_stream_t stream) {
   if (n_req < 0) return PIC_ERR_INVALID;
   if (n_req == 0) return PIC_OK;
   if (!chunk_off || !q_len || !k || !chunk_page_off || !fresh_off || !row_off || !page_off ||
@@ -296,7 +300,7 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
   splice_kernel<<<dim3((unsigned)n_req, (unsigned)per_req), kPlanThreads, 0, (cudaStream_t)stream>>>(
       chunk_lens, chunk_off, q_len, k, chunk_start, chunk_page_off, k_src_blocks, k_dst_blocks,
       v_blocks, fresh_off, fresh_blocks, row_off, page_off, rot_off, pages, rot, row_block, row_slot,
-      err_flag);
+      page_tab, err_flag);
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }
 

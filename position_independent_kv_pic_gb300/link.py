@@ -19,8 +19,8 @@ import numpy as np
 import torch
 
 from . import (PIC_BF16, PIC_FP32, PIC_PAGE, pic_decode_attention, pic_decode_workspace, pic_link_attention,
-               pic_link_attention_workspace, pic_plan_offsets, pic_rerotate_k, pic_rope_cached_k, pic_rope_table,
-               pic_select_rows, pic_splice_pages, pic_write_fresh_kv)
+               pic_link_attention_ror, pic_link_attention_workspace, pic_plan_offsets, pic_rerotate_k,
+               pic_rope_cached_k, pic_rope_table, pic_select_rows, pic_splice_pages, pic_write_fresh_kv)
 from .inputs import Workload, block_shuffle, chunk_store, decode_inputs, row_inputs
 
 
@@ -33,10 +33,12 @@ class LinkBatch:
 
     def __init__(self, wl: Workload, device="cuda", rows_inputs=None, scheme="rotary"):
         """scheme "rotary": the pool's cached K is encoded at local positions and the step
-        re-rotates it by the chunk offset (rotary correction).  scheme "nope": the pool's
-        cached K carries no position encoding and the step encodes every kept cached slot
-        at its global position (scheme B; in place only)."""
-        if scheme not in ("rotary", "nope"):
+        re-rotates it by the chunk offset (rotary correction).  scheme "ror": the same
+        correction applied on read inside link attention (rotate-on-read): the cached
+        pages are never written, so shared chunks need no per-request copies.  scheme
+        "nope": the pool's cached K carries no position encoding and the step encodes
+        every kept cached slot at its global position (scheme B; in place only)."""
+        if scheme not in ("rotary", "ror", "nope"):
             raise ValueError(scheme)
         if scheme == "nope" and wl.out_of_place:
             raise ValueError("scheme B runs in place: give each request private copies of its chunks")
@@ -72,7 +74,8 @@ class LinkBatch:
         store_base[1:] = np.cumsum(store_np)
         n_store_pages = int(store_base[-1])
         n_chunk_pages = int(offs["chunk_page_off"][-1])
-        n_dst = n_chunk_pages if wl.out_of_place else 0
+        copies = wl.out_of_place and scheme == "rotary"  # rotate-on-read reads the shared chunks in place
+        n_dst = n_chunk_pages if copies else 0
         n_link_blocks = n_store_pages + n_dst + self.n_fresh
         # one more block per request takes the row a decode step appends after the link
         self.decode_blocks = np.arange(n_link_blocks, n_link_blocks + self.n_req, dtype=np.int32)
@@ -82,7 +85,7 @@ class LinkBatch:
         k_src = np.concatenate([self.store_blocks[c] for c in flat_ids]) if len(flat_ids) else np.zeros(0, np.int64)
         self.k_src = k_src.astype(np.int32)
         self.v_blocks = self.k_src.copy()
-        self.k_dst = perm[n_store_pages:n_store_pages + n_dst].astype(np.int32) if wl.out_of_place else None
+        self.k_dst = perm[n_store_pages:n_store_pages + n_dst].astype(np.int32) if copies else None
         self.fresh_blocks = perm[n_store_pages + n_dst:].astype(np.int32)
 
         # ---- pool: the cached chunks as compiled
@@ -117,6 +120,7 @@ class LinkBatch:
         self.chunk_start = torch.empty(self.n_chunks, dtype=i32, device=dev)
         self.pages = torch.empty((self.n_pages, 4), dtype=i32, device=dev)   # pic_link_page, 16 B
         self.rot = torch.empty((self.n_rot, 4), dtype=i32, device=dev)       # pic_rot_page, 16 B
+        self.page_tab = torch.empty(self.n_pages, dtype=i32, device=dev) if scheme == "ror" else None
         self.row_block = torch.empty(self.n_rows, dtype=i32, device=dev)
         self.row_slot = torch.empty(self.n_rows, dtype=i32, device=dev)
         self.delta_table = torch.empty((self.n_chunks, d // 2, 4), dtype=torch.float32, device=dev)
@@ -177,11 +181,11 @@ class LinkBatch:
     # ------------------------------------------------------------------ step
     # kernels one run() launches: select, splice, 2 tables, re-rotate, fresh K/V, and the
     # attention call (unit planning, attention, LSE merge)
-    LAUNCHES_PER_STEP = 9  # rotary correction; scheme B has no offset table: 8
+    LAUNCHES_PER_STEP = 9  # rotary correction; scheme B (no offset table) and rotate-on-read (no re-rotation): 8
 
     @property
     def launches_per_step(self) -> int:
-        return self.LAUNCHES_PER_STEP - (1 if self.scheme == "nope" else 0)
+        return self.LAUNCHES_PER_STEP - (1 if self.scheme in ("nope", "ror") else 0)
 
     def run(self, stream=None, marks=None):
         """The link step: a1 select, splice, a2 tables, a3 re-rotate, a4 fresh K/V, a5+a6 attention.
@@ -195,13 +199,15 @@ class LinkBatch:
         pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
                          dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
                          dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
-                         self.row_block, self.row_slot, self.err, stream)
-        if self.scheme == "rotary":
+                         self.row_block, self.row_slot, self.err, stream, page_tab=self.page_tab)
+        if self.scheme in ("rotary", "ror"):
             pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, stream)
         pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, stream)
         if "rerotate" in mk:
             mk["rerotate"][0].record()
-        if self.scheme == "rotary":
+        if self.scheme == "ror":
+            pass  # the correction runs inside the attention kernel
+        elif self.scheme == "rotary":
             pic_rerotate_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, self.rot, self.n_rot, self.delta_table,
                            self.n_chunks, self.err, stream)
         else:
@@ -215,9 +221,15 @@ class LinkBatch:
                            self.row_table, self.row_block, self.row_slot, self.n_rows, self.err, stream)
         if "attention" in mk:
             mk["attention"][0].record()
-        pic_link_attention(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
-                           self.pic_dtype, self.pages, dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv,
-                           wl.d, self.scale, self.out, self.ws, self.err, stream)
+        if self.scheme == "ror":
+            pic_link_attention_ror(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
+                                   self.pic_dtype, self.pages, self.page_tab, self.delta_table, dv["page_off"],
+                                   self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.scale, self.out, self.ws,
+                                   self.err, stream)
+        else:
+            pic_link_attention(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
+                               self.pic_dtype, self.pages, dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv,
+                               wl.d, self.scale, self.out, self.ws, self.err, stream)
         if "attention" in mk:
             mk["attention"][1].record()
 
@@ -227,6 +239,9 @@ class LinkBatch:
         after the request's query rows.  Call after run() has built the link page list: a
         request's decode page list is its link pages followed by one page holding the new
         row (a serving engine keeps this list; building it is not part of the step)."""
+        if self.scheme == "ror":
+            raise NotImplementedError("decode reads the linked pages as stored: rotate-on-read links keep them "
+                                      "at local positions")
         wl, dev, i32 = self.wl, self.device, torch.int32
         q, k, v = decode_inputs(wl)
         self.dec_q, self.dec_k, self.dec_v = q.to(dev), k.to(dev), v.to(dev)

@@ -173,3 +173,14 @@ def test_compose_segment_and_workspace():
                                   None) == pic.PIC_ERR_INVALID         # max_chain > n_elems
     assert lib.pic_compose_states(None, None, 4, None, None, 1, 5, 5, 32, 64, 0, None, None, 0, None,
                                   None) == pic.PIC_ERR_UNSUPPORTED
+
+
+def test_rotate_on_read_entry_checks_without_launch():
+    lib = pic.load()
+    args = lambda n_tab, dtype, Hq, Hkv, d, n_req, n_rows: (None, None, None, None, None, None, 10, dtype, None,
+                                                             None, None, n_tab, None, n_req, n_rows, Hq, Hkv, d,
+                                                             0.1, None, None, 0, None, None)
+    assert lib.pic_link_attention_ror(*args(0, pic.PIC_BF16, 32, 8, 128, 0, 0)) == pic.PIC_OK
+    assert lib.pic_link_attention_ror(*args(-1, pic.PIC_BF16, 32, 8, 128, 0, 0)) == pic.PIC_ERR_INVALID
+    assert lib.pic_link_attention_ror(*args(0, pic.PIC_FP32, 4, 2, 16, 0, 0)) == pic.PIC_ERR_UNSUPPORTED
+    assert lib.pic_link_attention_ror(*args(0, pic.PIC_BF16, 30, 8, 128, 1, 5)) == pic.PIC_ERR_INVALID
