@@ -282,6 +282,30 @@ def run_gpu(args, rank, world):
         del bb
         torch.cuda.empty_cache()
 
+    # rotate-on-read: the same step with the correction applied inside link attention
+    # (no re-rotation pass; the cached pages are read as cached)
+    ror = None
+    if pic.pic_link_attention_workspace(batch.n_rows, batch.n_req, wl.Hq, wl.Hkv, wl.d, batch.pic_dtype) > 0:
+        rb = LinkBatch(wl, scheme="ror")
+        for _ in range(args.warmup):
+            rb.run()
+        torch.cuda.synchronize()
+        Kr = max(3, min(K, 50))
+        rstep = [(ev(), ev()) for _ in range(Kr)]
+        ratt = [(ev(), ev()) for _ in range(Kr)]
+        for i in range(Kr):
+            flush.zero_()
+            rstep[i][0].record(stream)
+            rb.run(marks={"attention": ratt[i]})
+            rstep[i][1].record(stream)
+        torch.cuda.synchronize()
+        if rb.error() != 0:
+            raise SystemExit(f"device error (rotate-on-read): {pic.pic_strerror(rb.error())}")
+        ror = (statistics.mean(a.elapsed_time(b) for a, b in rstep),
+               statistics.mean(a.elapsed_time(b) for a, b in ratt), Kr, rb.tokens, rb.launches_per_step)
+        del rb
+        torch.cuda.empty_cache()
+
     # linear-layer state composition (a hybrid model's linear-attention layer over the
     # same chunk chains: 32 heads of 128 x 128 states per chunk)
     comp = None
@@ -349,6 +373,14 @@ def run_gpu(args, rank, world):
                              "kernel": "pic_rope_cached_k (scheme B: cached K encoded at its global position; "
                                        "bytes = K read + written + one table row per slot); the step runs "
                                        "without the offset table and the re-rotation"}} if schb else {}),
+            **({"rotate_on_read": {"bound": "tensor", "achieved": attn_flops / (ror[1] / 1e3) / 1e12,
+                                   "peak": tf_burst, "unit": "TFLOP/s",
+                                   "frac": attn_flops / (ror[1] / 1e3) / 1e12 / tf_burst, "ms": ror[1],
+                                   "ms_per_step": ror[0], "tokens_per_s": world * ror[3] / (ror[0] / 1e3),
+                                   "steps": ror[2], "launches_per_step": ror[4],
+                                   "kernel": "pic_link_attention_ror (link attention rotating each cached K page "
+                                             "in shared memory before its S product); the step has no "
+                                             "re-rotation pass"}} if ror else {}),
             **({"compose": {"bound": "hbm", "achieved": comp[1] / (comp[0] / 1e3) / 1e9, "peak": hbm,
                             "unit": "GB/s", "frac": comp[1] / (comp[0] / 1e3) / 1e9 / hbm, "ms": comp[0],
                             "algorithmic_bytes": comp[1], "steps": comp[2], "seg": comp[3], "chains": comp[4],

@@ -514,6 +514,7 @@ drain:
 }
 
 // ---------------------------------------------------------------- MMA issuer
+template <bool kRor>
 __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units) {
   // descriptor words: hi is constant, lo = start address (>> 4) plus the LBO field
   constexpr uint32_t kHi = tc::sw128_desc_hi(1024), kHiKV = tc::sw128_desc_hi(kGroupBytes);
@@ -524,7 +525,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
   // K load l (even): landed, and rotated when rotating on read
   auto wait_k = [&](uint32_t l) -> bool {
     if (!wait_bar(b, &b->kv_full[l % kSlots], (l / kSlots) & 1)) return false;
-    return a.page_tab == nullptr || wait_bar(b, &b->kr_done[(l / 2) % kSlots], ((l / 2) / kSlots) & 1);
+    return !kRor || wait_bar(b, &b->kr_done[(l / 2) % kSlots], ((l / 2) / kSlots) & 1);
   };
   auto issue_s = [&](int i, int slot) {
     const uint32_t qa = q_lo + i * (kOpBytes >> 4), kb = k_lo + slot * (kOpBytes >> 4);
@@ -662,16 +663,57 @@ qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
 // Masked keys get weight 0 and 0 * V must stay 0 even if a slot outside a page's
 // valid range holds stale non-finite bits: once a V tile has landed, the rows of
 // slots that hold no valid key are zeroed before the MMA issuer uses the slot.
-// One 32-bit word (two bf16 dimensions i, i + 1) of a K row's low half against the
-// matching word of its high half (dimensions i + 64, i + 65), rotated in place
-// exactly as the re-rotation pass does it (rope_rotate_bf16in, one bf16 rounding).
-__device__ __forceinline__ void rotate_word(uint32_t& wl, uint32_t& wh, const float4& t0, const float4& t1) {
-  const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wl));
-  const float2 y = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&wh));
-  float a0, b0, a1, b1;
-  rope_rotate_bf16in(x.x, y.x, t0, a0, b0);
-  rope_rotate_bf16in(x.y, y.y, t1, a1, b1);
-  __nv_bfloat162 p = __floats2bfloat162_rn(a0, a1), q = __floats2bfloat162_rn(b0, b1);
+// Packed fp32 pairs without flush-to-zero: each lane is the IEEE operation the
+// scalar __fmaf_rn / __fmul_rn / __fadd_rn performs.
+__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ uint64_t mul2_rn(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// bf16 pair (low half: element 0) -> packed fp32 pair, exactly
+__device__ __forceinline__ uint64_t bf16x2_unpack(uint32_t w) { return tc::f2pack(__uint_as_float(w << 16),
+                                                                                  __uint_as_float(w & 0xffff0000u)); }
+
+// cos / sin of two consecutive frequencies as packed pairs: hi, lo parts and the
+// negated sines
+struct RotPair {
+  uint64_t c_hi, s_hi, ns_hi, c_lo, s_lo, ns_lo;
+};
+__device__ __forceinline__ RotPair rot_pair(const float4& t0, const float4& t1) {
+  RotPair r;
+  r.c_hi = tc::f2pack(t0.x, t1.x);
+  r.s_hi = tc::f2pack(t0.y, t1.y);
+  r.ns_hi = tc::f2pack(-t0.y, -t1.y);
+  r.c_lo = tc::f2pack(t0.z, t1.z);
+  r.s_lo = tc::f2pack(t0.w, t1.w);
+  r.ns_lo = tc::f2pack(-t0.w, -t1.w);
+  return r;
+}
+
+// One 32-bit word of a K row's low half (dimensions i, i + 1) against the word of
+// its high half (i + 64, i + 65), rotated in place with the operations of
+// rope_rotate_bf16in (the re-rotation pass), two lanes at a time, one bf16
+// rounding: bit for bit the pass's result.
+__device__ __forceinline__ void rotate_word2(uint32_t& wl, uint32_t& wh, const RotPair& t) {
+  const uint64_t a = bf16x2_unpack(wl), b = bf16x2_unpack(wh);
+  const uint64_t u = fma2_rn(a, t.c_hi, mul2_rn(b, t.ns_hi));
+  const uint64_t v = fma2_rn(b, t.c_hi, mul2_rn(a, t.s_hi));
+  const uint64_t ya = add2_rn(u, fma2_rn(a, t.c_lo, mul2_rn(b, t.ns_lo)));
+  const uint64_t yb = add2_rn(v, fma2_rn(b, t.c_lo, mul2_rn(a, t.s_lo)));
+  float y0, y1, z0, z1;
+  tc::f2unpack(ya, y0, y1);
+  tc::f2unpack(yb, z0, z1);
+  __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1), q = __floats2bfloat162_rn(z0, z1);
   wl = *reinterpret_cast<uint32_t*>(&p);
   wh = *reinterpret_cast<uint32_t*>(&q);
 }
@@ -680,40 +722,47 @@ __device__ __forceinline__ void rotate_word(uint32_t& wl, uint32_t& wh, const fl
 // row (lane j holds page j's) is not negative, by R(theta * Delta) of that row —
 // the same table and arithmetic as pic_rerotate_k, so the K the MMA reads is bit
 // for bit the one the re-rotation pass would have written.  Warps 2-3 (t64 =
-// 0..63): position pos of rows r0 = t64 / 8 and r0 + 8 of every page, i.e. the
-// 16-byte chunk c = pos ^ r0 (the 128-byte swizzle) of both column halves.
+// 0..63): thread (c, hh, rq) takes dimensions 8c + 4hh .. +3 of both column halves
+// in rows rq, rq + 4, rq + 8, rq + 12 of every page (physical 16-byte position
+// c ^ (row % 8), the 128-byte swizzle); its four frequencies' cos / sin stay in
+// registers while consecutive pages share a table row.
+struct RotCache {
+  int tab;
+  RotPair p0, p1;
+};
 __device__ __forceinline__ void rotate_k_tile(uint8_t* ksm, int tab_lane, const float4* __restrict__ rot_tab,
-                                              int t64) {
-  const int pos = t64 & 7, r0 = t64 >> 3, c = pos ^ r0;
+                                              int t64, RotCache& rc) {
+  const int c = t64 & 7, hh = (t64 >> 3) & 1, rq = t64 >> 4;
 #pragma unroll 1
   for (int jj = 0; jj < kPagesPerKt; ++jj) {
     const int tab = __shfl_sync(0xffffffffu, tab_lane, jj);
     if (tab < 0) continue;
-    const float4* cs = rot_tab + (int64_t)tab * (kD / 2) + 8 * c;
-    uint8_t* p0 = ksm + jj * kPageBytes + r0 * 128 + pos * 16;  // row r0: group 0, low half
-    uint8_t* p1 = p0 + kGroupBytes;                              // row r0 + 8: group 1
-    uint4 l0 = *reinterpret_cast<const uint4*>(p0), h0 = *reinterpret_cast<const uint4*>(p0 + kPageHalfBytes);
-    uint4 l1 = *reinterpret_cast<const uint4*>(p1), h1 = *reinterpret_cast<const uint4*>(p1 + kPageHalfBytes);
-    uint32_t* wl0 = reinterpret_cast<uint32_t*>(&l0);
-    uint32_t* wh0 = reinterpret_cast<uint32_t*>(&h0);
-    uint32_t* wl1 = reinterpret_cast<uint32_t*>(&l1);
-    uint32_t* wh1 = reinterpret_cast<uint32_t*>(&h1);
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float4 t0 = __ldg(cs + 2 * w), t1 = __ldg(cs + 2 * w + 1);
-      rotate_word(wl0[w], wh0[w], t0, t1);
-      rotate_word(wl1[w], wh1[w], t0, t1);
+    if (tab != rc.tab) {
+      const float4* cs = rot_tab + (int64_t)tab * (kD / 2) + 8 * c + 4 * hh;
+      rc.p0 = rot_pair(__ldg(cs), __ldg(cs + 1));
+      rc.p1 = rot_pair(__ldg(cs + 2), __ldg(cs + 3));
+      rc.tab = tab;
     }
-    *reinterpret_cast<uint4*>(p0) = l0;
-    *reinterpret_cast<uint4*>(p0 + kPageHalfBytes) = h0;
-    *reinterpret_cast<uint4*>(p1) = l1;
-    *reinterpret_cast<uint4*>(p1 + kPageHalfBytes) = h1;
+    uint8_t* pg = ksm + jj * kPageBytes + hh * 8;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = rq + 4 * i;
+      uint8_t* p = pg + (r >> 3) * kGroupBytes + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
+      uint2 l = *reinterpret_cast<const uint2*>(p), h = *reinterpret_cast<const uint2*>(p + kPageHalfBytes);
+      rotate_word2(l.x, h.x, rc.p0);
+      rotate_word2(l.y, h.y, rc.p1);
+      *reinterpret_cast<uint2*>(p) = l;
+      *reinterpret_cast<uint2*>(p + kPageHalfBytes) = h;
+    }
   }
 }
 
+template <bool kRor>
 __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31, wz = (threadIdx.x >> 5) - 2;  // 0, 1
   uint32_t ld = 0;
+  RotCache rc;
+  rc.tab = -1;
   for (uint32_t k = 0;; ++k) {
     const int u = read_unit_warp(b, k);
     if (u < 0) { fail(b, a.err); return; }
@@ -728,7 +777,7 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
       const int plo = pvalid ? (int16_t)(pg.w & 0xffff) : 0;
       const int phi = pvalid ? (int16_t)(pg.w >> 16) : 0;
       const bool full = __all_sync(0xffffffffu, lane >= kPagesPerKt || (plo == 0 && phi == PIC_PAGE));
-      if (a.page_tab != nullptr) {  // rotate-on-read: K of this tile before its S product
+      if (kRor) {  // rotate-on-read: K of this tile before its S product
         int tab = -1;
         if (pvalid) {
           tab = __ldg(a.page_tab + tm.page_begin + kt * kPagesPerKt + lane);
@@ -740,7 +789,7 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
         const int ks = ld % kSlots;
         const bool got = wait_bar(b, &b->kv_full[ks], (ld / kSlots) & 1);
         if (!__all_sync(0xffffffffu, got)) { fail(b, a.err); return; }
-        rotate_k_tile(smem + kOffSlot + ks * kOpBytes, tab, a.rot_tab, 32 * wz + lane);
+        rotate_k_tile(smem + kOffSlot + ks * kOpBytes, tab, a.rot_tab, 32 * wz + lane, rc);
         tc::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) tc::mbar_arrive(&b->kr_done[(ld / 2) % kSlots]);
@@ -966,6 +1015,7 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
   }
 }
 
+template <bool kRor>
 __global__ void __launch_bounds__(kThreads, 1)
 link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                     const TcArgs a) {
@@ -1018,13 +1068,13 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
     if (warp == 0) {
       producer_loop(a, &kmap, &vmap, smem, b, n_units);
     } else if (warp == 1 && lane == 0) {
-      mma_loop(a, smem, b, tmem, n_units);
+      mma_loop<kRor>(a, smem, b, tmem, n_units);
       // every MMA this thread issued completes before TMEM is released (also on abort)
       tc::mma_commit(&b->drain);
       const int no_abort = 0;
       tc::mbar_wait(&b->drain, 0, &no_abort, kWaitLimitNs);
     } else if (warp == 2 || warp == 3) {
-      vzero_loop(a, smem, b, n_units);
+      vzero_loop<kRor>(a, smem, b, n_units);
     }
   } else {
     tc::regs_inc<kRegsHigh>();
@@ -1252,11 +1302,12 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   qprep_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), 4), kQTiles * kM, 0, s>>>(
       hdr, tiles, static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), q_tiles, Hq, Hkv, G, R);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
-  if (cudaFuncSetAttribute(link_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) !=
-      cudaSuccess)
+  // rotate-on-read is its own instantiation, so the plain kernel carries none of it
+  const auto kern = page_tab != nullptr ? link_attn_tc_kernel<true> : link_attn_tc_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
     return PIC_ERR_CUDA;
   cudaFuncAttributes fa;
-  if (cudaFuncGetAttributes(&fa, link_attn_tc_kernel) != cudaSuccess) return PIC_ERR_CUDA;
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return PIC_ERR_CUDA;
   if (fa.numRegs != kLaunchRegs) return PIC_ERR_UNSUPPORTED;  // the register split assumes this launch size
   TcArgs a;
   a.q_tiles = q_tiles;
@@ -1282,7 +1333,7 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   a.rot_tab = reinterpret_cast<const float4*>(rot_table);
   a.n_tab = n_tab;
   const int64_t grid = L.units_cap < sms ? L.units_cap : sms;
-  link_attn_tc_kernel<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
+  kern<<<(unsigned)grid, kThreads, kSmemBytes, s>>>(kmap, vmap, a);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   merge_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), kQTiles * kM / kMergeRows), 32 * kMergeRows, 0, s>>>(
       hdr, tiles, part_o, part_ml, a.out, Hq, Hkv, G, R);

@@ -307,3 +307,39 @@ class LinkBatch:
         b = torch.from_numpy(table[cp0 + j // PIC_PAGE].astype(np.int64)).to(self.device)
         s = torch.from_numpy(j % PIC_PAGE).to(self.device)
         return self.k_pool[b, :, s, :].cpu()
+
+
+def _main():
+    """Run the link step of a seeded preset workload a few times and print one JSON
+    line (mean time of the timed steps, context tokens/s)."""
+    import argparse
+    import json
+
+    from . import build
+    from .inputs import PRESETS
+
+    ap = argparse.ArgumentParser(description=_main.__doc__.splitlines()[0])
+    ap.add_argument("--workload", default="long_context_100x1000", choices=sorted(PRESETS))
+    ap.add_argument("--scheme", default="rotary", choices=["rotary", "ror", "nope"])
+    ap.add_argument("--warmup", type=int, default=1)
+    ap.add_argument("--runs", type=int, default=2)
+    a = ap.parse_args()
+    build.build()
+    b = LinkBatch(PRESETS[a.workload](), scheme=a.scheme)
+    for _ in range(a.warmup):
+        b.run()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.runs)]
+    for e0, e1 in ev:
+        e0.record()
+        b.run()
+        e1.record()
+    torch.cuda.synchronize()
+    if b.error():
+        raise SystemExit(f"device error {b.error()}")
+    ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / max(len(ev), 1)
+    print(json.dumps({"workload": a.workload, "scheme": a.scheme, "ms_per_step": ms,
+                      "tokens_per_s": b.tokens / (ms / 1e3), "launches_per_step": b.launches_per_step}))
+
+
+if __name__ == "__main__":
+    _main()
