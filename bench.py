@@ -354,7 +354,8 @@ def run_gpu(args, rank, world):
         "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": tf_burst, "unit": "TFLOP/s",
                      "frac": att_tflops / tf_burst, "traffic": traffic,
                      "traffic_kernel": "link_attn_tc_kernel (ncu dram__bytes_read+write, one launch)",
-                     "kernel": "pic_link_attention (unit plan + tcgen05 attention + LSE merge)",
+                     "kernel": "pic_link_attention_run (tcgen05 attention + LSE merge; the unit plan and the Q "
+                               "pre-pass run beside the re-rotation pass on another stream)",
                      "algorithmic": f"4*d*Hq*sum(p_r+1) = {attn_flops:.4e} flop per launch",
                      "peak_source": f"{peak_kind} bf16 dense burst"},
         "rooflines": {

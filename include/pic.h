@@ -342,6 +342,27 @@ pic_status pic_link_attention_noalloc(const void* q, const float* row_table, con
                                       int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out,
                                       int32_t* err_flag, pic_stream_t stream);
 
+/* The same call in two halves, so that the part that reads no K or V can overlap
+ * the re-rotation pass on another stream:
+ *   pic_link_attention_plan  plans the work units and writes the roped Q operands
+ *       into ws (reads q, row_table, rows, row_off, pages, page_off only; a no-op
+ *       for shapes off the tensor cores);
+ *   pic_link_attention_run   the attention and the merge, from that plan.
+ * run must follow plan (stream order or an event) with the same arguments and the
+ * same ws, untouched in between; plan + run = pic_link_attention, bit for bit. */
+pic_status pic_link_attention_plan(const void* q, const float* row_table, const int32_t* rows,
+                                   const int32_t* row_off, const pic_link_page* pages, const int32_t* page_off,
+                                   int32_t n_req, int64_t n_rows, int32_t Hq, int32_t Hkv, int32_t d,
+                                   pic_dtype dtype, void* ws, size_t ws_bytes, int32_t* err_flag,
+                                   pic_stream_t stream);
+
+pic_status pic_link_attention_run(const void* q, const float* row_table, const int32_t* rows,
+                                  const int32_t* row_off, const void* k_pool, const void* v_pool,
+                                  int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                                  const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                                  int32_t Hkv, int32_t d, float scale, void* out, void* ws, size_t ws_bytes,
+                                  int32_t* err_flag, pic_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * a3+a5  Rotate-on-read link attention (RoPE article 3.3: the rotary correction
  *     applied where the kernel reads the cache, a mixed reuse + correction

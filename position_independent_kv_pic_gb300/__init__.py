@@ -25,6 +25,7 @@ __all__ = [
     "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
     "pic_decode_workspace", "pic_decode_attention", "pic_rope_cached_k",
     "pic_compose_segment", "pic_compose_workspace", "pic_compose_states", "pic_link_attention_ror",
+    "pic_link_attention_plan", "pic_link_attention_run",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -49,7 +50,7 @@ EXPORTED = (
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "pic_decode_workspace", "pic_decode_attention",
     "pic_rope_cached_k", "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
-    "pic_link_attention_ror",
+    "pic_link_attention_ror", "pic_link_attention_plan", "pic_link_attention_run",
 )
 
 
@@ -95,6 +96,10 @@ _SIGS = {
                                          _P, _P, _P, _I64, _P, _P]),
     "pic_link_attention_ror": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _P, _I64, _P,
                                               _I32, _I64, _I32, _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
+    "pic_link_attention_plan": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, ctypes.c_int,
+                                               _P, _SZ, _P, _P]),
+    "pic_link_attention_run": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32, _I64, _I32,
+                                              _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
     "pic_compose_segment": (_I32, [_I32, _I64, _I32, _I32, _I32]),
     "pic_compose_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "pic_compose_states": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _SZ,
@@ -246,6 +251,24 @@ def pic_decode_attention(q, q_table, k_pool, v_pool, dtype: int, pages, page_off
         _ptr(q), _ptr(q_table), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype), _ptr(pages), _ptr(page_off),
         int(n_req), int(Hq), int(Hkv), int(d), float(scale), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),
         _stream(stream)), "pic_decode_attention")
+
+
+def pic_link_attention_plan(q, row_table, rows, row_off, pages, page_off, n_req: int, n_rows: int, Hq: int,
+                            Hkv: int, d: int, dtype: int, ws, err_flag, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pic_link_attention_plan(
+        _ptr(q), _ptr(row_table), _ptr(rows), _ptr(row_off), _ptr(pages), _ptr(page_off), int(n_req), int(n_rows),
+        int(Hq), int(Hkv), int(d), int(dtype), _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)),
+        "pic_link_attention_plan")
+
+
+def pic_link_attention_run(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, pages, page_off, n_req: int,
+                           n_rows: int, Hq: int, Hkv: int, d: int, scale: float, out, ws, err_flag, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pic_link_attention_run(
+        _ptr(q), _ptr(row_table), _ptr(rows), _ptr(row_off), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype),
+        _ptr(pages), _ptr(page_off), int(n_req), int(n_rows), int(Hq), int(Hkv), int(d), float(scale), _ptr(out),
+        _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)), "pic_link_attention_run")
 
 
 def pic_link_attention_ror(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, pages, page_tab, rot_table,

@@ -684,37 +684,37 @@ __device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
 __device__ __forceinline__ uint64_t bf16x2_unpack(uint32_t w) { return tc::f2pack(__uint_as_float(w << 16),
                                                                                   __uint_as_float(w & 0xffff0000u)); }
 
-// cos / sin of two consecutive frequencies as packed pairs: hi, lo parts and the
-// negated sines
+// cos / sin of two consecutive frequencies as packed pairs: hi and lo parts
 struct RotPair {
-  uint64_t c_hi, s_hi, ns_hi, c_lo, s_lo, ns_lo;
+  uint64_t c_hi, s_hi, c_lo, s_lo;
 };
 __device__ __forceinline__ RotPair rot_pair(const float4& t0, const float4& t1) {
   RotPair r;
   r.c_hi = tc::f2pack(t0.x, t1.x);
   r.s_hi = tc::f2pack(t0.y, t1.y);
-  r.ns_hi = tc::f2pack(-t0.y, -t1.y);
   r.c_lo = tc::f2pack(t0.z, t1.z);
   r.s_lo = tc::f2pack(t0.w, t1.w);
-  r.ns_lo = tc::f2pack(-t0.w, -t1.w);
   return r;
 }
 
 // One 32-bit word of a K row's low half (dimensions i, i + 1) against the word of
 // its high half (i + 64, i + 65), rotated in place with the operations of
 // rope_rotate_bf16in (the re-rotation pass), two lanes at a time, one bf16
-// rounding: bit for bit the pass's result.
+// rounding: bit for bit the pass's result.  The low output is formed negated —
+// with -a in place of a, fma(a, c, -p) = -fma(-a, c, p) and the sum and the bf16
+// rounding are odd functions, all exact under round-to-nearest — and its sign is
+// flipped back on the bf16 bits, so no negated sines need to be held.
 __device__ __forceinline__ void rotate_word2(uint32_t& wl, uint32_t& wh, const RotPair& t) {
-  const uint64_t a = bf16x2_unpack(wl), b = bf16x2_unpack(wh);
-  const uint64_t u = fma2_rn(a, t.c_hi, mul2_rn(b, t.ns_hi));
+  const uint64_t a = bf16x2_unpack(wl), na = bf16x2_unpack(wl ^ 0x80008000u), b = bf16x2_unpack(wh);
+  const uint64_t nu = fma2_rn(na, t.c_hi, mul2_rn(b, t.s_hi));  // -(a c_hi - b s_hi)
   const uint64_t v = fma2_rn(b, t.c_hi, mul2_rn(a, t.s_hi));
-  const uint64_t ya = add2_rn(u, fma2_rn(a, t.c_lo, mul2_rn(b, t.ns_lo)));
+  const uint64_t nya = add2_rn(nu, fma2_rn(na, t.c_lo, mul2_rn(b, t.s_lo)));
   const uint64_t yb = add2_rn(v, fma2_rn(b, t.c_lo, mul2_rn(a, t.s_lo)));
   float y0, y1, z0, z1;
-  tc::f2unpack(ya, y0, y1);
+  tc::f2unpack(nya, y0, y1);
   tc::f2unpack(yb, z0, z1);
   __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1), q = __floats2bfloat162_rn(z0, z1);
-  wl = *reinterpret_cast<uint32_t*>(&p);
+  wl = *reinterpret_cast<uint32_t*>(&p) ^ 0x80008000u;
   wh = *reinterpret_cast<uint32_t*>(&q);
 }
 
@@ -1270,23 +1270,32 @@ bool tc_shape(pic_dtype dt, int Hq, int Hkv, int d) {
   return G == 1 || G == 2 || G == 4 || G == 8 || G == 16;
 }
 
-// Plan, attend, merge with the scratch laid out by L in `ws`.  The planner may
-// add up to 4 * split_sms units by splitting key ranges.
+// The two phases of a tensor-core attention call, with the scratch laid out by L
+// in `ws`: the plan (unit list, Q operands — reads no K or V) and the run
+// (attention, merge).  The planner may add up to 4 * split_sms units by splitting
+// key ranges.
+enum { kPhasePlan = 1, kPhaseRun = 2, kPhaseAll = 3 };
+
 pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows, const int32_t* row_off,
                      const void* k_pool, const void* v_pool, int64_t num_blocks, const pic_link_page* pages,
                      const int32_t* page_off, int32_t n_req, int32_t Hq, int32_t Hkv, float scale, void* out,
                      uint8_t* w, const WsLayout& L, int split_sms, int32_t* err_flag, cudaStream_t s,
-                     const int32_t* page_tab = nullptr, const float* rot_table = nullptr, int64_t n_tab = 0) {
+                     const int32_t* page_tab = nullptr, const float* rot_table = nullptr, int64_t n_tab = 0,
+                     int phases = kPhaseAll) {
   const int G = Hq / Hkv;
   if (n_req > kMaxPlanReqs) return PIC_ERR_UNSUPPORTED;
-  if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
-      (reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(out) & 15) ||
-      (reinterpret_cast<uintptr_t>(row_table) & 15) || (reinterpret_cast<uintptr_t>(pages) & 15))
+  if ((reinterpret_cast<uintptr_t>(q) & 15) || (reinterpret_cast<uintptr_t>(row_table) & 15) ||
+      (reinterpret_cast<uintptr_t>(pages) & 15))
     return PIC_ERR_INVALID;
-  const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
-  if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
   CUtensorMap kmap, vmap;
-  if (!encode_pages(&kmap, k_pool, pool_rows) || !encode_pages(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
+  if (phases & kPhaseRun) {
+    if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
+        (reinterpret_cast<uintptr_t>(out) & 15))
+      return PIC_ERR_INVALID;
+    const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
+    if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
+    if (!encode_pages(&kmap, k_pool, pool_rows) || !encode_pages(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
+  }
   WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
   TileMeta* tiles = reinterpret_cast<TileMeta*>(w + L.off_tiles);
   Unit* units = reinterpret_cast<Unit*>(w + L.off_units);
@@ -1294,14 +1303,18 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   float* part_o = reinterpret_cast<float*>(w + L.off_o);
   const int sms = num_sms_of_current_device();
   const int R = kM / G;
-  plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kQTiles * R, Hkv,
-                                                split_sms < sms ? split_sms : sms, L.tiles_cap, L.units_cap, hdr,
-                                                tiles, units, err_flag);
-  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   uint8_t* q_tiles = w + L.off_q;
-  qprep_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), 4), kQTiles * kM, 0, s>>>(
-      hdr, tiles, static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), q_tiles, Hq, Hkv, G, R);
-  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  if (phases & kPhasePlan) {
+    plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kQTiles * R, Hkv,
+                                                  split_sms < sms ? split_sms : sms, L.tiles_cap, L.units_cap, hdr,
+                                                  tiles, units, err_flag);
+    if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+    qprep_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), 4), kQTiles * kM, 0, s>>>(
+        hdr, tiles, static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), q_tiles, Hq, Hkv, G,
+        R);
+    if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  }
+  if (!(phases & kPhaseRun)) return PIC_OK;
   // rotate-on-read is its own instantiation, so the plain kernel carries none of it
   const auto kern = page_tab != nullptr ? link_attn_tc_kernel<true> : link_attn_tc_kernel<false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
@@ -1383,6 +1396,44 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
     if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
     return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
                      out, static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, s);
+  }
+  return launch_attention_simt(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
+                               n_req, n_rows, Hq, Hkv, d, scale, out, s);
+}
+
+pic_status pic_link_attention_plan(const void* q, const float* row_table, const int32_t* rows,
+                                   const int32_t* row_off, const pic_link_page* pages, const int32_t* page_off,
+                                   int32_t n_req, int64_t n_rows, int32_t Hq, int32_t Hkv, int32_t d,
+                                   pic_dtype dtype, void* ws, size_t ws_bytes, int32_t* err_flag,
+                                   pic_stream_t stream) {
+  if (n_req < 0 || n_rows < 0 || Hkv < 1 || Hq < 1 || Hq % Hkv || d < 2 || d > 256 || (d & 1))
+    return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (n_req == 0 || n_rows == 0 || !tc_shape(dtype, Hq, Hkv, d)) return PIC_OK;  // nothing to plan
+  if (!q || !row_table || !rows || !row_off || !pages || !page_off || !err_flag) return PIC_ERR_INVALID;
+  const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
+  return launch_tc(q, row_table, rows, row_off, nullptr, nullptr, 0, pages, page_off, n_req, Hq, Hkv, 1.f, nullptr,
+                   static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, (cudaStream_t)stream,
+                   nullptr, nullptr, 0, kPhasePlan);
+}
+
+pic_status pic_link_attention_run(const void* q, const float* row_table, const int32_t* rows,
+                                  const int32_t* row_off, const void* k_pool, const void* v_pool,
+                                  int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
+                                  const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                                  int32_t Hkv, int32_t d, float scale, void* out, void* ws, size_t ws_bytes,
+                                  int32_t* err_flag, pic_stream_t stream) {
+  const pic_status st = check_attention_args(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages,
+                                             page_off, n_req, n_rows, Hq, Hkv, d, scale, out, err_flag);
+  if (st != PIC_OK || n_req == 0 || n_rows == 0) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  if (tc_shape(dtype, Hq, Hkv, d)) {
+    const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
+    if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
+    return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
+                     out, static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, s, nullptr, nullptr,
+                     0, kPhaseRun);
   }
   return launch_attention_simt(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
                                n_req, n_rows, Hq, Hkv, d, scale, out, s);

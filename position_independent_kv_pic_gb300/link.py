@@ -19,8 +19,9 @@ import numpy as np
 import torch
 
 from . import (PIC_BF16, PIC_FP32, PIC_PAGE, pic_decode_attention, pic_decode_workspace, pic_link_attention,
-               pic_link_attention_ror, pic_link_attention_workspace, pic_plan_offsets, pic_rerotate_k,
-               pic_rope_cached_k, pic_rope_table, pic_select_rows, pic_splice_pages, pic_write_fresh_kv)
+               pic_link_attention_plan, pic_link_attention_ror, pic_link_attention_run, pic_link_attention_workspace,
+               pic_plan_offsets, pic_rerotate_k, pic_rope_cached_k, pic_rope_table, pic_select_rows,
+               pic_splice_pages, pic_write_fresh_kv)
 from .inputs import Workload, block_shuffle, chunk_store, decode_inputs, row_inputs
 
 
@@ -130,6 +131,7 @@ class LinkBatch:
         self.ws = torch.empty(max(ws, 256), dtype=torch.uint8, device=dev) if ws > 0 else None
         self.err = torch.zeros(1, dtype=i32, device=dev)
         self.scale = 1.0 / math.sqrt(d)
+        self._side = None  # stream of the cached-K pass (created on first use)
         if scheme == "nope":
             # the model's position table (every position a cached slot can take), built once
             self.n_pos = max([int(wl.chunk_lens[r.chunk_ids].sum()) for r in wl.requests] + [1])
@@ -190,48 +192,71 @@ class LinkBatch:
     def run(self, stream=None, marks=None):
         """The link step: a1 select, splice, a2 tables, a3 re-rotate, a4 fresh K/V, a5+a6 attention.
 
-        ``marks`` (optional) maps "rerotate" / "attention" to (start, end) CUDA events that
-        are recorded around those calls on the current stream."""
+        The cached-K pass (re-rotation, or scheme B's encoding) runs on a side stream
+        beside the work that reads no cached K — the row table, the fresh K/V, the
+        attention plan — and the attention run waits for both.  ``marks`` (optional)
+        maps "rerotate" / "attention" to (start, end) CUDA events recorded around the
+        cached-K pass (on the side stream) and the attention run."""
         wl, dv = self.wl, self.dev
         mk = marks or {}
+        if stream is None:
+            main = torch.cuda.current_stream(self.device)
+        elif isinstance(stream, int):
+            main = torch.cuda.ExternalStream(stream)
+        else:
+            main = stream
         pic_select_rows(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], dv["row_off"], self.rows,
-                        self.chunk_start, self.err, stream)
+                        self.chunk_start, self.err, main)
         pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
                          dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
                          dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
-                         self.row_block, self.row_slot, self.err, stream, page_tab=self.page_tab)
+                         self.row_block, self.row_slot, self.err, main, page_tab=self.page_tab)
+        pass_stream = main
+        if self.scheme in ("rotary", "nope"):
+            if self._side is None:
+                self._side = torch.cuda.Stream(self.device)
+                self._ev_fork, self._ev_join = torch.cuda.Event(), torch.cuda.Event()
+            pass_stream = self._side
+            self._ev_fork.record(main)
+            pass_stream.wait_event(self._ev_fork)
         if self.scheme in ("rotary", "ror"):
-            pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, stream)
-        pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, stream)
+            pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, pass_stream)
         if "rerotate" in mk:
-            mk["rerotate"][0].record()
-        if self.scheme == "ror":
-            pass  # the correction runs inside the attention kernel
-        elif self.scheme == "rotary":
+            mk["rerotate"][0].record(pass_stream)
+        if self.scheme == "rotary":
             pic_rerotate_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, self.rot, self.n_rot, self.delta_table,
-                           self.n_chunks, self.err, stream)
-        else:
+                           self.n_chunks, self.err, pass_stream)
+        elif self.scheme == "nope":
             pic_rope_cached_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, dv["chunk_lens"], dv["chunk_off"], dv["k"],
                               self.n_req, self.chunk_start, dv["chunk_page_off"], self.n_chunks,
                               int(self.offs["chunk_page_off"][-1]), dv["k_src"], None, self.pos_table, self.err,
-                              stream)
+                              pass_stream)
         if "rerotate" in mk:
-            mk["rerotate"][1].record()
+            mk["rerotate"][1].record(pass_stream)
+        if pass_stream is not main:
+            self._ev_join.record(pass_stream)
+        pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, main)
         pic_write_fresh_kv(self.k_pool, self.v_pool, self.pic_dtype, wl.Hkv, wl.d, dv["k_new"], dv["v_new"],
-                           self.row_table, self.row_block, self.row_slot, self.n_rows, self.err, stream)
-        if "attention" in mk:
-            mk["attention"][0].record()
+                           self.row_table, self.row_block, self.row_slot, self.n_rows, self.err, main)
         if self.scheme == "ror":
+            if "attention" in mk:
+                mk["attention"][0].record(main)
             pic_link_attention_ror(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
                                    self.pic_dtype, self.pages, self.page_tab, self.delta_table, dv["page_off"],
                                    self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.scale, self.out, self.ws,
-                                   self.err, stream)
+                                   self.err, main)
         else:
-            pic_link_attention(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
-                               self.pic_dtype, self.pages, dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv,
-                               wl.d, self.scale, self.out, self.ws, self.err, stream)
+            pic_link_attention_plan(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.pages,
+                                    dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.pic_dtype,
+                                    self.ws, self.err, main)
+            main.wait_event(self._ev_join)
+            if "attention" in mk:
+                mk["attention"][0].record(main)
+            pic_link_attention_run(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
+                                   self.pic_dtype, self.pages, dv["page_off"], self.n_req, self.n_rows, wl.Hq,
+                                   wl.Hkv, wl.d, self.scale, self.out, self.ws, self.err, main)
         if "attention" in mk:
-            mk["attention"][1].record()
+            mk["attention"][1].record(main)
 
     # ------------------------------------------------------------------ decode after the link
     def setup_decode(self):

@@ -137,3 +137,20 @@ def test_unsupported_shapes():
         b.run()
     with pytest.raises(NotImplementedError):
         LinkBatch(inputs.rag_prompt(), scheme="ror").setup_decode()
+
+
+def test_plan_and_run_equal_the_single_call():
+    """The step plans the attention beside the re-rotation pass (side stream) and runs
+    it after both: the same bits as one pic_link_attention call."""
+    wl = inputs.rag_prompt()
+    b = LinkBatch(wl)
+    b.run()
+    torch.cuda.synchronize()
+    assert b.error() == 0
+    out = torch.empty_like(b.out)
+    pic.pic_link_attention(b.dev["q_raw"], b.row_table, b.rows, b.dev["row_off"], b.k_pool, b.v_pool, b.pic_dtype,
+                           b.pages, b.dev["page_off"], b.n_req, b.n_rows, wl.Hq, wl.Hkv, wl.d, b.scale, out, b.ws,
+                           b.err)
+    torch.cuda.synchronize()
+    assert b.error() == 0
+    assert torch.equal(out, b.out)
