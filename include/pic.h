@@ -431,7 +431,16 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
  * the layer's state S = T_n (.. (T_2 S_1 + S_2) ..) + S_n, by the blog's rule
  * S(C1 C2) = T(C2) S(C1) + S(C2); the transition of C1 is never used.
  *
- *   T_pool, S_pool  [n_pool][H][d][d] fp32 row-major (device): the cached pairs
+ * The cache keeps T in the form the tensor cores take: two bf16 planes per
+ * matrix, hi = bf16(T) and lo = bf16(T - hi) (T = hi + lo to about 2^-16 of |T|,
+ * which is all the split product below uses of it).  pic_compose_split_t writes
+ * that form from fp32 T once, when a chunk's pair is cached:
+ *   T        [n_mats][d][d] fp32 (device)
+ *   T_split  [n_mats][2][d][d] bf16 out (device): plane 0 hi, plane 1 lo
+ *
+ * pic_compose_states:
+ *   T_split  [n_pool][H][2][d][d] bf16 (device): the cached transitions
+ *   S_pool   [n_pool][H][d][d] fp32 row-major (device): the cached end states
  *   ids        [n_elems] int32 (device): chain of every request, pool entries in
  *              chain order; request r owns ids[chain_off[r] .. chain_off[r+1])
  *   chain_off  [n_req + 1] int32 (device), chain_off[0] = 0, chain_off[n_req] = n_elems
@@ -447,15 +456,18 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
  *   ws         at least pic_compose_workspace() bytes, 256-byte aligned
  * d = 128 only (else PIC_ERR_UNSUPPORTED; 0 from pic_compose_workspace).  Each
  * fold step is a 128 x 128 x 128 tensor-core product of bf16 parts
- * (hi.hi + hi.lo + lo.hi, fp32 accumulate: about 2^-16 relative error per step).
- * Two or three launches.  A pool id outside [0, n_pool) or offsets that disagree
- * with n_elems / max_chain set PIC_ERR_RANGE in *err_flag (pool entry 0 is read in
- * place of a bad id); a bounded wait that runs out sets PIC_ERR_TIMEOUT. */
+ * (hi.hi + hi.lo + lo.hi, fp32 accumulate: about 2^-16 relative error per step);
+ * S is added in fp32.  Two or three launches.  A pool id outside [0, n_pool) or
+ * offsets that disagree with n_elems / max_chain set PIC_ERR_RANGE in *err_flag
+ * (pool entry 0 is read in place of a bad id); a bounded wait that runs out sets
+ * PIC_ERR_TIMEOUT. */
+pic_status pic_compose_split_t(const float* T, int64_t n_mats, int32_t d, void* T_split, pic_stream_t stream);
+
 int32_t pic_compose_segment(int32_t n_req, int64_t n_elems, int32_t max_chain, int32_t H, int32_t sms);
 
 size_t pic_compose_workspace(int32_t n_req, int32_t max_chain, int32_t H, int32_t d, int32_t seg);
 
-pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t n_pool, const int32_t* ids,
+pic_status pic_compose_states(const void* T_split, const float* S_pool, int64_t n_pool, const int32_t* ids,
                               const int32_t* chain_off, int32_t n_req, int64_t n_elems, int32_t max_chain,
                               int32_t H, int32_t d, int32_t seg, float* out, void* ws, size_t ws_bytes,
                               int32_t* err_flag, pic_stream_t stream);

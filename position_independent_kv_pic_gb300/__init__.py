@@ -25,7 +25,7 @@ __all__ = [
     "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
     "pic_decode_workspace", "pic_decode_attention", "pic_rope_cached_k",
     "pic_compose_segment", "pic_compose_workspace", "pic_compose_states", "pic_link_attention_ror",
-    "pic_link_attention_plan", "pic_link_attention_run",
+    "pic_link_attention_plan", "pic_link_attention_run", "pic_compose_split_t",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -50,7 +50,7 @@ EXPORTED = (
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
     "pic_selftest_umma", "pic_link_attention_noalloc", "pic_decode_workspace", "pic_decode_attention",
     "pic_rope_cached_k", "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
-    "pic_link_attention_ror", "pic_link_attention_plan", "pic_link_attention_run",
+    "pic_link_attention_ror", "pic_link_attention_plan", "pic_link_attention_run", "pic_compose_split_t",
 )
 
 
@@ -100,6 +100,7 @@ _SIGS = {
                                                _P, _SZ, _P, _P]),
     "pic_link_attention_run": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32, _I64, _I32,
                                               _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
+    "pic_compose_split_t": (ctypes.c_int, [_P, _I64, _I32, _P, _P]),
     "pic_compose_segment": (_I32, [_I32, _I64, _I32, _I32, _I32]),
     "pic_compose_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "pic_compose_states": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _SZ,
@@ -290,11 +291,18 @@ def pic_compose_workspace(n_req: int, max_chain: int, H: int, d: int, seg: int) 
     return int(load().pic_compose_workspace(int(n_req), int(max_chain), int(H), int(d), int(seg)))
 
 
-def pic_compose_states(T_pool, S_pool, ids, chain_off, n_req: int, n_elems: int, max_chain: int, H: int, d: int,
+def pic_compose_split_t(T, T_split, stream=None):
+    """T [..][d][d] fp32 -> T_split [..][2][d][d] bf16 (hi, lo planes)."""
+    n = T.numel() // (T.shape[-1] * T.shape[-2])
+    _check(load().pic_compose_split_t(_ptr(T), n, int(T.shape[-1]), _ptr(T_split), _stream(stream)),
+           "pic_compose_split_t")
+
+
+def pic_compose_states(T_split, S_pool, ids, chain_off, n_req: int, n_elems: int, max_chain: int, H: int, d: int,
                        seg: int, out, ws, err_flag, stream=None):
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(load().pic_compose_states(
-        _ptr(T_pool), _ptr(S_pool), T_pool.shape[0], _ptr(ids), _ptr(chain_off), int(n_req), int(n_elems),
+        _ptr(T_split), _ptr(S_pool), S_pool.shape[0], _ptr(ids), _ptr(chain_off), int(n_req), int(n_elems),
         int(max_chain), int(H), int(d), int(seg), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)),
         "pic_compose_states")
 

@@ -14,18 +14,18 @@
 // tensor cores, taken transposed so that every operand keeps its natural place:
 //   D^T = X^T T_i^T,  A = X^T in TMEM (TMEM lane n holds column n of X),
 //                     B = T_i in shared memory (row-major T_i is the K-major B).
-// Precision: X and T_i are split into bf16 parts, x = x_hi + x_lo with
-// x_hi = bf16(x), x_lo = bf16(x - x_hi), and the product is taken as
-// hi.hi + hi.lo + lo.hi with fp32 accumulation (the dropped lo.lo term is below
-// 2^-16 of |x||y|).  The accumulator in TMEM plus S_i is the new state in fp32.
+// Precision: both factors as two bf16 parts, x = x_hi + x_lo with x_hi = bf16(x),
+// x_lo = bf16(x - x_hi); the product is hi.hi + hi.lo + lo.hi with fp32
+// accumulation (the dropped lo.lo term is below 2^-16 of |x||y|).  The cache keeps
+// T in exactly that form (pic_compose_split_t), two bf16 planes, so T_i goes from
+// global memory into the B operand by TMA without any conversion; the state is
+// split by the epilogue each step.  S_i stays fp32 and is added exactly.
 //
-// Pipeline (320 threads).  Warp 8 lane 0 streams T_i into a shared staging buffer
-// by bulk copies; warps 0-7 convert it into one of two bf16 B buffers while the
-// tensor cores work on the other, and run the epilogue (TMEM -> + S_i -> split ->
-// TMEM), reading S_i straight from global memory one step ahead; warp 9 lane 0
-// issues the MMAs.  The S products and the T products are committed apart, so that
-// each epilogue overlaps the other's MMAs.
-// Every wait is bounded.
+// Pipeline (320 threads, one CTA per SM).  Warp 8 lane 0 loads T_i by four 16 KB
+// TMA boxes into one of two B buffers and S_i by bulk copies into a staging
+// buffer; warp 9 lane 0 issues the MMAs; warps 0-7 run the epilogue (TMEM + S_i ->
+// split -> TMEM).  The S products and the T products are committed apart, so that
+// each epilogue overlaps the other's MMAs.  Every wait is bounded.
 #include <algorithm>
 
 #include "pic_internal.cuh"
@@ -37,46 +37,46 @@ namespace {
 using bf16 = __nv_bfloat16;
 
 constexpr int kCD = 128;                              // d_k = d_v
-constexpr int kElt = kCD * kCD;                       // floats per matrix
-constexpr int kMatBytes = kElt * 4;                   // 64 KB fp32
+constexpr int kElt = kCD * kCD;                       // elements per matrix
+constexpr int kMatBytes = kElt * 4;                   // 64 KB: one fp32 matrix, or its two bf16 planes
 constexpr int kCWorkers = 256;                        // warps 0-7
 constexpr int kProdWarp = kCWorkers / 32, kMmaWarp = kProdWarp + 1;
 constexpr int kCThreads = kCWorkers + 64;
 constexpr int kBHalf = kCD * 128;                     // one 64-column half of a 128-row bf16 operand
 constexpr int kBPart = 2 * kBHalf;                    // 32 KB: one bf16 part of B
 constexpr int kBBytes = 2 * kBPart;                   // hi | lo
-constexpr int kOffB = 0;                              // two B buffers (SW128, [half][128 rows][128 B])
-constexpr int kOffTs = kOffB + 2 * kBBytes;           // T_i staging, fp32 row-major
-constexpr int kOffBar = kOffTs + kMatBytes;
+constexpr int kOffB = 0;                              // two B buffers ([part][k half][128 rows][128 B], SW128)
+constexpr int kOffSs = kOffB + 2 * kBBytes;           // S_i staging, fp32 row-major
+constexpr int kOffBar = kOffSs + kMatBytes;
 constexpr int kCSmem = kOffBar + 128;
 static_assert(kCSmem <= 232448, "shared memory per CTA");
 // TMEM columns: D_S | D_T | A_S hi | A_S lo | A_T hi | A_T lo
 constexpr uint32_t kColDS = 0, kColDT = 128, kColAS = 256, kColAT = 384;
 constexpr uint64_t kCWaitNs = 2000000000ull;
 constexpr uint32_t kCIdesc = tc::idesc_bf16_f32(128, 128, false);
-constexpr int kCopy = 16384;                          // bytes per bulk copy
+constexpr int kCopy = 16384;                          // bytes per bulk copy of S
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct CBars {
-  uint64_t t_full, t_empty;
-  uint64_t b_full[2];    // per B buffer: one phase per use
-  uint64_t a_s, a_t;     // A_S / A_T written for the next step
-  uint64_t d_s, d_t;     // the step's S / T products complete
+  uint64_t b_full[2], b_empty[2];  // per B buffer: T_i landed / released by the step that read it
+  uint64_t s_full, s_empty;        // the S staging buffer
+  uint64_t a_s, a_t;               // A_S / A_T written for the next step
+  uint64_t d_s, d_t;               // the step's S / T products complete
   uint32_t tmem;
   int abort;
 };
 static_assert(sizeof(CBars) <= 128, "barrier block");
 
 struct Level {
-  const float* T_in;
+  const bf16* T_in;          // two bf16 planes per matrix: [matrix][part][128][128]
   const float* S_in;
   const int32_t* ids;        // level 0: pool entry of every chain element; else nullptr
   const int32_t* chain_off;  // [n_req + 1] offsets of each request's chain in ids
   const int32_t* first;      // [n_req + 1] first CTA of each request at this level
   int64_t n_pool;            // level 0: entries of the pool
   int64_t in_stride;         // level 1: elements per chain in T_in / S_in
-  float* T_out;              // level 0 of two: [chain][out_stride]
+  bf16* T_out;               // level 0 of two: [chain][out_stride][part][128][128]
   float* S_out;              // [chain][out_stride]
   int64_t out_stride;
   int64_t n_elems;           // entries of ids
@@ -111,61 +111,49 @@ __device__ __forceinline__ bool wait_bar_warp(uint64_t* bar, uint32_t parity, CB
   return false;
 }
 
-__device__ __forceinline__ void load_matrix(uint8_t* dst, const float* src, uint64_t* bar) {
-  tc::mbar_arrive_expect_tx(bar, kMatBytes);
+// 16 rows m_first .. +15 of state column nc: the staged S rows (srow[j * kCD], when
+// USE_S) plus the accumulator at TMEM column d_col + m_first -> the fp32 output
+// (when OUT == 1), the two bf16 planes of a split output (OUT == 2), or the A
+// operand (bf16 hi at a_col + m_first / 2, lo 64 columns further).  Warp-collective.
+template <bool USE_S, int OUT>
+__device__ __forceinline__ void piece16(const float* srow, uint32_t tmem_row, uint32_t d_col, int m_first, int nc,
+                                        void* out, uint32_t a_col) {
+  float x[16];
+  {
+    uint32_t rr[16];
+    tc::tmem_ld16(tmem_row + d_col + m_first, rr);
+    tc::tmem_ld_wait();
+    tc::reg_fence<16>(rr);
 #pragma unroll
-  for (int c = 0; c < kMatBytes / kCopy; ++c)
-    tc::bulk_load(dst + c * kCopy, reinterpret_cast<const uint8_t*>(src) + c * kCopy, kCopy, bar);
-}
-
-// Column n, rows m0 .. m0 + 63 of a row-major d x d matrix in global memory (a
-// warp's 32 lanes read 32 consecutive columns: 128-byte rows).
-__device__ __forceinline__ void load_col64(const float* __restrict__ src, int m0, int n, float (&v)[64]) {
-  const float* p = src + m0 * kCD + n;
+    for (int j = 0; j < 16; ++j) x[j] = USE_S ? __uint_as_float(rr[j]) + srow[j * kCD] : __uint_as_float(rr[j]);
+  }
+  if (OUT == 1) {
+    float* o = static_cast<float*>(out) + m_first * kCD + nc;
 #pragma unroll
-  for (int j = 0; j < 64; ++j) v[j] = __ldg(p + j * kCD);
-}
-
-// Column nc, rows m0 .. m0 + 63 of a state: sv (when USE_V) plus the accumulator
-// at TMEM column d_col (when ADD_D) -> the output (fp32, when to_out) or the A
-// operand at TMEM column a_col (bf16 hi | lo).  16 columns at a time, to keep the
-// registers for the prefetched sv.  Warp-collective.
-template <bool USE_V, bool ADD_D>
-__device__ __forceinline__ void emit(const float (&sv)[64], uint32_t tmem_row, uint32_t d_col, int m0, int nc,
-                                     bool to_out, float* out, uint32_t a_col) {
+    for (int j = 0; j < 16; ++j) o[j * kCD] = x[j];
+  } else if (OUT == 2) {
+    bf16* o = static_cast<bf16*>(out) + m_first * kCD + nc;
 #pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    float x[16];
-    if (ADD_D) {
-      uint32_t rr[16];
-      tc::tmem_ld16(tmem_row + d_col + m0 + 16 * c, rr);
-      tc::tmem_ld_wait();
-      tc::reg_fence<16>(rr);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) x[j] = USE_V ? __uint_as_float(rr[j]) + sv[16 * c + j] : __uint_as_float(rr[j]);
-    } else {
-#pragma unroll
-      for (int j = 0; j < 16; ++j) x[j] = sv[16 * c + j];
+    for (int j = 0; j < 16; ++j) {
+      const bf16 h = __float2bfloat16_rn(x[j]);
+      o[j * kCD] = h;
+      o[kElt + j * kCD] = __float2bfloat16_rn(x[j] - __bfloat162float(h));
     }
-    if (to_out) {
-      float* o = out + (m0 + 16 * c) * kCD + nc;
+  } else {
+    uint32_t hi[8], lo[8];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) o[j * kCD] = x[j];
-    } else {
-      uint32_t hi[8], lo[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const bf16 h0 = __float2bfloat16_rn(x[2 * j]), h1 = __float2bfloat16_rn(x[2 * j + 1]);
-        hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lo[j] = pack_bf16x2(x[2 * j] - __bfloat162float(h0), x[2 * j + 1] - __bfloat162float(h1));
-      }
-      tc::tmem_st8(tmem_row + a_col + (m0 >> 1) + 8 * c, hi);
-      tc::tmem_st8(tmem_row + a_col + 64 + (m0 >> 1) + 8 * c, lo);
+    for (int j = 0; j < 8; ++j) {
+      const bf16 h0 = __float2bfloat16_rn(x[2 * j]), h1 = __float2bfloat16_rn(x[2 * j + 1]);
+      hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      lo[j] = pack_bf16x2(x[2 * j] - __bfloat162float(h0), x[2 * j + 1] - __bfloat162float(h1));
     }
+    tc::tmem_st8(tmem_row + a_col + (m_first >> 1), hi);
+    tc::tmem_st8(tmem_row + a_col + 64 + (m_first >> 1), lo);
   }
 }
 
-__global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
+__global__ void __launch_bounds__(kCThreads, 1)
+compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* sm = smem_raw;
   CBars* cb = reinterpret_cast<CBars*>(sm + kOffBar);
@@ -195,28 +183,32 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
   const bool need_T = !lv.last && g > 0;
   const int64_t chain = (int64_t)r * lv.H + h;
   float* s_out = lv.S_out + (chain * lv.out_stride + g) * kElt;
-  float* t_out = need_T ? lv.T_out + (chain * lv.out_stride + g) * kElt : nullptr;
+  bf16* t_out = need_T ? lv.T_out + (chain * lv.out_stride + g) * 2 * kElt : nullptr;
 
   if (n <= 0) {  // an empty chain: its state is zero
     for (int i = tid; i < kElt / 4; i += kCThreads)
       reinterpret_cast<float4*>(s_out)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
     return;
   }
-  auto elem = [&](const float* base, int i) -> const float* {
+  // matrix index of chain element i: its S at S_in + index * kElt, its T planes at
+  // T_in + index * 2 kElt (rows 256 index .. of the T tensor map)
+  auto mat = [&](int i) -> int64_t {
     if (lv.level == 0) {
       const int64_t at = (int64_t)c0 + i;
       int64_t id = (at >= 0 && at < lv.n_elems) ? __ldg(lv.ids + at) : 0;
       if (id < 0 || id >= lv.n_pool) id = 0;  // flagged by the planner
-      return base + (id * lv.H + h) * kElt;
+      return id * lv.H + h;
     }
-    return base + (chain * lv.in_stride + i) * kElt;
+    return chain * lv.in_stride + i;
   };
 
   if (tid == 0) {
-    tc::mbar_init(&cb->t_full, 1);
-    tc::mbar_init(&cb->t_empty, kCWorkers);
-    tc::mbar_init(&cb->b_full[0], kCWorkers);
-    tc::mbar_init(&cb->b_full[1], kCWorkers);
+    for (int i = 0; i < 2; ++i) {
+      tc::mbar_init(&cb->b_full[i], 1);
+      tc::mbar_init(&cb->b_empty[i], kCWorkers);
+    }
+    tc::mbar_init(&cb->s_full, 1);
+    tc::mbar_init(&cb->s_empty, kCWorkers);
     tc::mbar_init(&cb->a_s, kCWorkers);
     tc::mbar_init(&cb->a_t, kCWorkers);
     tc::mbar_init(&cb->d_s, 1);
@@ -228,23 +220,58 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
     tc::tmem_alloc(&cb->tmem, 512);
     tc::tmem_relinquish();
   }
+  if (warp == kProdWarp && lane == 0) tc::tma_prefetch_desc(&tmap);
   tc::tc_fence_before();
   __syncthreads();
   tc::tc_fence_after();
   const uint32_t tmem = cb->tmem;
-  const int n_steps = n - 1;  // T loads: T_{b+1} .. T_{e-1}, one per step
+  const int n_steps = n - 1;
 
   if (warp == kProdWarp) {
-    // ---- producer: T_{b+1+u} into the staging buffer, one in flight
+    // ---- producer: S_b, T(0), T(1), then S(u) and T(u + 1) in step order.  T(j) =
+    // T_{b+1+j} goes to B buffer j & 1 once the step two before released it; S(u) =
+    // S_{b+u} to the staging buffer once S(u - 1) was read.
     if (lane == 0) {
-      int issued = 0;
-      for (int u = 0; u < n_steps; ++u) {
-        if (!wait_bar(&cb->t_empty, (u & 1) ^ 1, cb, lv.err)) break;
-        load_matrix(sm + kOffTs, elem(lv.T_in, b + 1 + u), &cb->t_full);
-        issued = u + 1;
+      int s_issued = 0, t_issued = 0;
+      bool ok = true;
+      auto load_s = [&](int u) -> bool {
+        if (!wait_bar(&cb->s_empty, (u & 1) ^ 1, cb, lv.err)) return false;
+        const float* src = lv.S_in + mat(b + u) * kElt;
+        tc::mbar_arrive_expect_tx(&cb->s_full, kMatBytes);
+#pragma unroll
+        for (int c = 0; c < kMatBytes / kCopy; ++c)
+          tc::bulk_load(sm + kOffSs + c * kCopy, reinterpret_cast<const uint8_t*>(src) + c * kCopy, kCopy,
+                        &cb->s_full);
+        s_issued = u + 1;
+        return true;
+      };
+      auto load_t = [&](int j) -> bool {
+        const int buf = j & 1;
+        if (j >= 2 && !wait_bar(&cb->b_empty[buf], ((j >> 1) & 1) ^ 1, cb, lv.err)) return false;
+        const int32_t y0 = (int32_t)(mat(b + 1 + j) * 2 * kCD);
+        uint8_t* dst = sm + kOffB + buf * kBBytes;
+        tc::mbar_arrive_expect_tx(&cb->b_full[buf], kBBytes);
+#pragma unroll
+        for (int p = 0; p < 2; ++p)
+#pragma unroll
+          for (int kh = 0; kh < 2; ++kh)
+            tc::tma_load_2d(dst + p * kBPart + kh * kBHalf, &tmap, 64 * kh, y0 + p * kCD, &cb->b_full[buf]);
+        t_issued = j + 1;
+        return true;
+      };
+      ok = load_s(0);
+      for (int j = 0; ok && j < 2 && j < n_steps; ++j) ok = load_t(j);
+      for (int u = 1; ok && u < n; ++u) {
+        ok = load_s(u);
+        if (ok && u + 1 < n_steps) ok = load_t(u + 1);
       }
+      // no copy may be in flight when the block exits
       const int no_abort = 0;
-      if (issued > 0) tc::mbar_wait(&cb->t_full, (issued - 1) & 1, &no_abort, kCWaitNs);
+      if (s_issued > 0) tc::mbar_wait(&cb->s_full, (s_issued - 1) & 1, &no_abort, kCWaitNs);
+      for (int k = 0; k < 2 && k < t_issued; ++k) {
+        const int j = t_issued - 1 - k;
+        tc::mbar_wait(&cb->b_full[j & 1], (j >> 1) & 1, &no_abort, kCWaitNs);
+      }
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -290,86 +317,108 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
     }
     __syncwarp();
   } else {
-    // ---- workers: warp w reads TMEM lanes 32 (w % 4) .. +31 (state columns
-    // n = 32 (w % 4) + lane) and accumulator columns m = 64 (w / 4) .. +63
+    // ---- epilogue warps: warp w reads TMEM lanes 32 (w % 4) .. +31 (state columns
+    // nc = 32 (w % 4) + lane) and accumulator columns m = 64 (w / 4) .. +63
     const int quarter = warp & 3, hf = warp >> 2;
     const int nc = 32 * quarter + lane, m0 = 64 * hf;
-    const uint32_t lane_base = (uint32_t)((32 * quarter) << 16);
-    const float* ts = reinterpret_cast<const float*>(sm + kOffTs);
+    const uint32_t trow = tmem + (uint32_t)((32 * quarter) << 16);
+    const float* ss = reinterpret_cast<const float*>(sm + kOffSs) + nc;
+    int su = 0;  // S fills consumed
     bool ok = true;
-    float sv[64];
-    // staged T_i (row-major) -> B buffer `buf` (hi | lo, K-major SW128): thread t
-    // converts the 16-byte chunks (row m, k = 4 c4 .. +3), a warp one row at a time
-    auto convert_T = [&](int buf) {
-      uint8_t* bb = sm + kOffB + buf * kBBytes;
-#pragma unroll 4
-      for (int it = 0; it < kElt / 4 / kCWorkers; ++it) {
-        const int q = it * kCWorkers + tid, m = q >> 5, c4 = q & 31;
-        const float4 v = *reinterpret_cast<const float4*>(ts + m * kCD + 4 * c4);
-        const bf16 h0 = __float2bfloat16_rn(v.x), h1 = __float2bfloat16_rn(v.y);
-        const bf16 h2 = __float2bfloat16_rn(v.z), h3 = __float2bfloat16_rn(v.w);
-        const uint2 hv = make_uint2((uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16),
-                                    (uint32_t)__bfloat16_as_ushort(h2) | ((uint32_t)__bfloat16_as_ushort(h3) << 16));
-        const uint2 lv2 = make_uint2(pack_bf16x2(v.x - __bfloat162float(h0), v.y - __bfloat162float(h1)),
-                                     pack_bf16x2(v.z - __bfloat162float(h2), v.w - __bfloat162float(h3)));
-        const int ch = (c4 & 15) >> 1;
-        const uint32_t off = (uint32_t)((c4 >> 4) * kBHalf + m * 128 + ((ch ^ (m & 7)) << 4) + (c4 & 1) * 8);
-        *reinterpret_cast<uint2*>(bb + off) = hv;
-        *reinterpret_cast<uint2*>(bb + kBPart + off) = lv2;
-      }
-    };
-    int tu = 0;  // staged T_i converted
-    auto next_B = [&]() -> bool {  // the next staged T_i into B buffer tu & 1
-      if (!wait_bar_warp(&cb->t_full, tu & 1, cb, lv.err)) return false;
-      convert_T(tu & 1);
-      tc::fence_proxy_async_smem();  // generic-proxy writes of B -> the MMA's reads
-      tc::mbar_arrive(&cb->b_full[tu & 1]);
-      tc::mbar_arrive(&cb->t_empty);
-      ++tu;
-      return true;
-    };
     auto signal = [&](uint64_t* bar) {
       tc::tmem_st_wait();
       tc::tc_fence_before();
       tc::mbar_arrive(bar);
     };
-    // first element: the accumulators (or the output, for a one-element segment)
-    load_col64(elem(lv.S_in, b), m0, nc, sv);
-    emit<true, false>(sv, tmem + lane_base, 0, m0, nc, n == 1, s_out, kColAS);
-    if (n_steps > 0) signal(&cb->a_s);
+    // the staged S (+ the accumulator at d_col, when add_d) -> A at a_col, or the output
+    auto s_emit = [&](bool add_d, bool to_out) -> bool {
+      if (!wait_bar_warp(&cb->s_full, su & 1, cb, lv.err)) return false;
+      if (!add_d && !to_out) {  // the first element: S_b -> A_S
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int mf = m0 + 16 * c;
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float x0 = ss[(mf + 2 * j) * kCD], x1 = ss[(mf + 2 * j + 1) * kCD];
+            const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+            hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+            lo[j] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+          }
+          tc::tmem_st8(trow + kColAS + (mf >> 1), hi);
+          tc::tmem_st8(trow + kColAS + 64 + (mf >> 1), lo);
+        }
+      } else if (!add_d) {  // a one-element segment: S_b is the output
+#pragma unroll
+        for (int c = 0; c < 64; ++c) s_out[(m0 + c) * kCD + nc] = ss[(m0 + c) * kCD];
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int mf = m0 + 16 * c;
+          if (to_out) piece16<true, 1>(ss + mf * kCD, trow, kColDS, mf, nc, s_out, kColAS);
+          else piece16<true, 0>(ss + mf * kCD, trow, kColDS, mf, nc, nullptr, kColAS);
+        }
+      }
+      tc::mbar_arrive(&cb->s_empty);
+      ++su;
+      return true;
+    };
+    auto t_emit = [&](bool to_out) {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (to_out) piece16<false, 2>(nullptr, trow, kColDT, m0 + 16 * c, nc, t_out, kColAT);
+        else piece16<false, 0>(nullptr, trow, kColDT, m0 + 16 * c, nc, nullptr, kColAT);
+      }
+    };
+    // first element: T_b (its two planes, column nc) -> A_T (or the output)
     if (need_T) {
-      load_col64(elem(lv.T_in, b), m0, nc, sv);
-      emit<true, false>(sv, tmem + lane_base, 0, m0, nc, n == 1, t_out, kColAT);
-      if (n_steps > 0) signal(&cb->a_t);
+      const bf16* tb = lv.T_in + mat(b) * 2 * kElt + nc;
+      if (n == 1) {
+        for (int c = 0; c < 64; ++c) {
+          t_out[(m0 + c) * kCD + nc] = tb[(m0 + c) * kCD];
+          t_out[kElt + (m0 + c) * kCD + nc] = tb[kElt + (m0 + c) * kCD];
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const int mf = m0 + 16 * c;
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            hi[j] = (uint32_t)__bfloat16_as_ushort(tb[(mf + 2 * j) * kCD]) |
+                    ((uint32_t)__bfloat16_as_ushort(tb[(mf + 2 * j + 1) * kCD]) << 16);
+            lo[j] = (uint32_t)__bfloat16_as_ushort(tb[kElt + (mf + 2 * j) * kCD]) |
+                    ((uint32_t)__bfloat16_as_ushort(tb[kElt + (mf + 2 * j + 1) * kCD]) << 16);
+          }
+          tc::tmem_st8(trow + kColAT + (mf >> 1), hi);
+          tc::tmem_st8(trow + kColAT + 64 + (mf >> 1), lo);
+        }
+      }
     }
-    if (n_steps > 0) {
-      load_col64(elem(lv.S_in, b + 1), m0, nc, sv);
-      ok = next_B();
+    ok = s_emit(false, n == 1);
+    if (ok && n_steps > 0) {
+      signal(&cb->a_s);
+      if (need_T) signal(&cb->a_t);
     }
-    // steps 0 .. n_steps - 2 feed the next step; the last writes the output (kept
-    // out of the loop so that the output addresses are not held across it)
+    // steps 0 .. n_steps - 2 feed the next step; the last writes the output
     for (int k = 0; ok && k + 1 < n_steps; ++k) {
-      // B buffer (k + 1) & 1 was read by step k - 1's products, complete: convert
-      // T_{b+k+2} while step k's run
-      if (!(ok = next_B())) break;
       if (!(ok = wait_bar_warp(&cb->d_s, k & 1, cb, lv.err))) break;
       tc::tc_fence_after();
-      emit<true, true>(sv, tmem + lane_base, kColDS, m0, nc, false, nullptr, kColAS);
+      if (!(ok = s_emit(true, false))) break;
       signal(&cb->a_s);
-      load_col64(elem(lv.S_in, b + k + 2), m0, nc, sv);
       if (need_T) {
         if (!(ok = wait_bar_warp(&cb->d_t, k & 1, cb, lv.err))) break;
         tc::tc_fence_after();
-        emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, false, nullptr, kColAT);
+        t_emit(false);
         signal(&cb->a_t);
       }
+      tc::mbar_arrive(&cb->b_empty[k & 1]);  // step k's products are complete: its B buffer is free
     }
     if (ok && n_steps > 0 && wait_bar_warp(&cb->d_s, (n_steps - 1) & 1, cb, lv.err)) {
       tc::tc_fence_after();
-      emit<true, true>(sv, tmem + lane_base, kColDS, m0, nc, true, s_out, kColAS);
-      if (need_T && wait_bar_warp(&cb->d_t, (n_steps - 1) & 1, cb, lv.err)) {
+      if (s_emit(true, true) && need_T && wait_bar_warp(&cb->d_t, (n_steps - 1) & 1, cb, lv.err)) {
         tc::tc_fence_after();
-        emit<false, true>(sv, tmem + lane_base, kColDT, m0, nc, true, t_out, kColAT);
+        t_emit(true);
       }
     }
   }
@@ -379,6 +428,39 @@ __global__ void __launch_bounds__(kCThreads, 1) compose_kernel(const Level lv) {
     tc::tc_fence_after();
     tc::tmem_dealloc(tmem, 512);
   }
+}
+
+// T in the cached form: hi = bf16(T), lo = bf16(T - hi), two planes per matrix.
+__global__ void __launch_bounds__(256) split_t_kernel(const float* __restrict__ T, int64_t n, bf16* __restrict__ out) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const float4 v = __ldg(reinterpret_cast<const float4*>(T) + i);
+    const int64_t m = i / (kElt / 4), w = i % (kElt / 4);
+    const bf16 h0 = __float2bfloat16_rn(v.x), h1 = __float2bfloat16_rn(v.y);
+    const bf16 h2 = __float2bfloat16_rn(v.z), h3 = __float2bfloat16_rn(v.w);
+    uint2 hv, lv;
+    hv.x = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+    hv.y = (uint32_t)__bfloat16_as_ushort(h2) | ((uint32_t)__bfloat16_as_ushort(h3) << 16);
+    lv.x = pack_bf16x2(v.x - __bfloat162float(h0), v.y - __bfloat162float(h1));
+    lv.y = pack_bf16x2(v.z - __bfloat162float(h2), v.w - __bfloat162float(h3));
+    reinterpret_cast<uint2*>(out + m * 2 * kElt)[w] = hv;
+    reinterpret_cast<uint2*>(out + m * 2 * kElt + kElt)[w] = lv;
+  }
+}
+
+// 2-D view [rows][128] bf16 of a split-T array (rows = 256 per matrix), boxes of
+// 128 rows x 64 columns with the 128-byte swizzle: one box is one k half of one
+// plane of a B operand.
+bool encode_t(CUtensorMap* map, const void* base, uint64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || rows == 0 || rows > (uint64_t)INT32_MAX) return false;
+  cuuint64_t dims[2] = {kCD, rows};
+  cuuint64_t strides[1] = {kCD * sizeof(bf16)};
+  cuuint32_t box[2] = {64, 128};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // One block: the first CTA of every request at both levels, and a check of the
@@ -462,7 +544,19 @@ size_t pic_compose_workspace(int32_t n_req, int32_t max_chain, int32_t H, int32_
   return c_layout(n_req, max_chain, H, seg).total;
 }
 
-pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t n_pool, const int32_t* ids,
+pic_status pic_compose_split_t(const float* T, int64_t n_mats, int32_t d, void* T_split, pic_stream_t stream) {
+  if (n_mats < 0) return PIC_ERR_INVALID;
+  if (d != kCD) return PIC_ERR_UNSUPPORTED;
+  if (n_mats == 0) return PIC_OK;
+  if (!T || !T_split || (reinterpret_cast<uintptr_t>(T) & 15) || (reinterpret_cast<uintptr_t>(T_split) & 15))
+    return PIC_ERR_INVALID;
+  const int64_t n = n_mats * (kElt / 4);
+  const int64_t blocks = std::min<int64_t>((n + 255) / 256, (int64_t)num_sms_of_current_device() * 16);
+  split_t_kernel<<<(unsigned)blocks, 256, 0, (cudaStream_t)stream>>>(T, n, static_cast<bf16*>(T_split));
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+pic_status pic_compose_states(const void* T_split, const float* S_pool, int64_t n_pool, const int32_t* ids,
                               const int32_t* chain_off, int32_t n_req, int64_t n_elems, int32_t max_chain,
                               int32_t H, int32_t d, int32_t seg, float* out, void* ws, size_t ws_bytes,
                               int32_t* err_flag, pic_stream_t stream) {
@@ -471,8 +565,8 @@ pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t 
   if (d != kCD) return PIC_ERR_UNSUPPORTED;
   if (n_req == 0) return PIC_OK;
   if (n_elems > 0 && n_pool < 1) return PIC_ERR_INVALID;
-  if (!T_pool || !S_pool || !ids || !chain_off || !out || !err_flag) return PIC_ERR_INVALID;
-  if ((reinterpret_cast<uintptr_t>(T_pool) | reinterpret_cast<uintptr_t>(S_pool) |
+  if (!T_split || !S_pool || !ids || !chain_off || !out || !err_flag) return PIC_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(T_split) | reinterpret_cast<uintptr_t>(S_pool) |
        reinterpret_cast<uintptr_t>(out)) & 15)
     return PIC_ERR_INVALID;
   const CLayout L = c_layout(n_req, max_chain, H, seg);
@@ -485,12 +579,14 @@ pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t 
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* first0 = reinterpret_cast<int32_t*>(w + L.off_first0);
   int32_t* first1 = reinterpret_cast<int32_t*>(w + L.off_first1);
+  CUtensorMap t0map;
+  if (!encode_t(&t0map, T_split, (uint64_t)n_pool * H * 2 * kCD)) return PIC_ERR_CUDA;
   compose_plan_kernel<<<1, 1024, 0, s>>>(ids, chain_off, n_req, H, n_pool, n_elems, max_chain, L.seg0,
                                          L.one_level, first0, first1, err_flag);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
 
   Level l0{};
-  l0.T_in = T_pool;
+  l0.T_in = static_cast<const bf16*>(T_split);
   l0.S_in = S_pool;
   l0.ids = ids;
   l0.chain_off = chain_off;
@@ -509,16 +605,18 @@ pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t 
     l0.S_out = out;
     l0.out_stride = 1;
   } else {
-    l0.T_out = reinterpret_cast<float*>(w + L.off_T);
+    l0.T_out = reinterpret_cast<bf16*>(w + L.off_T);
     l0.S_out = reinterpret_cast<float*>(w + L.off_S);
     l0.out_stride = L.n_out0;
   }
   // level-0 CTAs: at most H * (ceil(n_elems / seg0) + n_req) (one more per chain
   // for rounding, and one for an empty chain's zero state); the rest exit at once
-  compose_kernel<<<(unsigned)std::max<int64_t>(grid0, 1), kCThreads, kCSmem, s>>>(l0);
+  compose_kernel<<<(unsigned)std::max<int64_t>(grid0, 1), kCThreads, kCSmem, s>>>(t0map, l0);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   if (L.one_level) return PIC_OK;
 
+  CUtensorMap t1map;
+  if (!encode_t(&t1map, w + L.off_T, (uint64_t)n_req * H * L.n_out0 * 2 * kCD)) return PIC_ERR_CUDA;
   Level l1 = l0;
   l1.T_in = l0.T_out;
   l1.S_in = l0.S_out;
@@ -532,7 +630,7 @@ pic_status pic_compose_states(const float* T_pool, const float* S_pool, int64_t 
   l1.seg_prev = L.seg0;
   l1.level = 1;
   l1.last = true;
-  compose_kernel<<<(unsigned)((int64_t)n_req * H), kCThreads, kCSmem, s>>>(l1);
+  compose_kernel<<<(unsigned)((int64_t)n_req * H), kCThreads, kCSmem, s>>>(t1map, l1);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   return PIC_OK;
 }

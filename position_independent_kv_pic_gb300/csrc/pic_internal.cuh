@@ -1,6 +1,8 @@
 // Internal helpers shared by the CUDA translation units of the PIC library.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -90,6 +92,10 @@ __device__ __forceinline__ void rope_rotate_bf16in(float a, float b, float4 t, f
 }
 
 int num_sms_of_current_device();
+
+// The driver's cuTensorMapEncodeTiled, looked up once through the runtime (null if
+// the driver lacks it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // SIMT attention launcher (attention_simt.cu); arguments as pic_link_attention.
 pic_status launch_attention_simt(const void* q, const float* row_table, const int32_t* rows,

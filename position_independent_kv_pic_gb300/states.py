@@ -11,19 +11,23 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from . import pic_compose_segment, pic_compose_states, pic_compose_workspace
+from . import pic_compose_segment, pic_compose_split_t, pic_compose_states, pic_compose_workspace
 
 
 class ComposeBatch:
     """``T``, ``S``: [n_pool][H][d][d] float32 tensors; ``chains``: per request, the
     pool entries of its linked chunks in link order.  ``seg`` None picks the
-    level-0 segment that fills one wave of the device's SMs."""
+    level-0 segment that fills one wave of the device's SMs.  T is cached in the
+    split form the kernel reads (two bf16 planes), written once here."""
 
     def __init__(self, T, S, chains, device="cuda", seg=None):
         assert T.shape == S.shape and T.dim() == 4 and T.shape[2] == T.shape[3]
         self.device = torch.device(device)
         self.n_pool, self.H, self.d = int(T.shape[0]), int(T.shape[1]), int(T.shape[2])
-        self.T = T.to(self.device, torch.float32).contiguous()
+        t32 = T.to(self.device, torch.float32).contiguous()
+        self.T = torch.empty((self.n_pool, self.H, 2, self.d, self.d), dtype=torch.bfloat16, device=self.device)
+        pic_compose_split_t(t32, self.T)
+        del t32
         self.S = S.to(self.device, torch.float32).contiguous()
         lens = np.array([len(c) for c in chains], np.int64)
         off = np.zeros(len(chains) + 1, np.int32)

@@ -184,3 +184,10 @@ def test_rotate_on_read_entry_checks_without_launch():
     assert lib.pic_link_attention_ror(*args(-1, pic.PIC_BF16, 32, 8, 128, 0, 0)) == pic.PIC_ERR_INVALID
     assert lib.pic_link_attention_ror(*args(0, pic.PIC_FP32, 4, 2, 16, 0, 0)) == pic.PIC_ERR_UNSUPPORTED
     assert lib.pic_link_attention_ror(*args(0, pic.PIC_BF16, 30, 8, 128, 1, 5)) == pic.PIC_ERR_INVALID
+
+
+def test_compose_split_checks_without_launch():
+    lib = pic.load()
+    assert lib.pic_compose_split_t(None, -1, 128, None, None) == pic.PIC_ERR_INVALID
+    assert lib.pic_compose_split_t(None, 4, 64, None, None) == pic.PIC_ERR_UNSUPPORTED
+    assert lib.pic_compose_split_t(None, 0, 128, None, None) == pic.PIC_OK

@@ -129,3 +129,16 @@ def test_unsupported_head_dim():
                                torch.empty(1, 1, 64, 64, device="cuda"), torch.empty(256, dtype=torch.uint8,
                                                                                      device="cuda"),
                                torch.zeros(1, dtype=torch.int32, device="cuda"))
+
+
+def test_split_t_is_the_bf16_hi_lo_pair():
+    T, _ = _pool(3, 2, seed=15)
+    Td = T.cuda()
+    out = torch.empty((3, 2, 2, D, D), dtype=torch.bfloat16, device="cuda")
+    pic.pic_compose_split_t(Td, out)
+    torch.cuda.synchronize()
+    hi = Td.to(torch.bfloat16)
+    lo = (Td - hi.float()).to(torch.bfloat16)
+    assert torch.equal(out[:, :, 0], hi) and torch.equal(out[:, :, 1], lo)
+    rel = ((out[:, :, 0].double() + out[:, :, 1].double()) - Td.double()).abs() / Td.double().abs().clamp_min(1e-30)
+    assert rel.max().item() <= 2.0 ** -16
