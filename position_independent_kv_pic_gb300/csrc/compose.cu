@@ -404,15 +404,16 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
     for (int k = 0; ok && k + 1 < n_steps; ++k) {
       if (!(ok = wait_bar_warp(&cb->d_s, k & 1, cb, lv.err))) break;
       tc::tc_fence_after();
+      if (!need_T) tc::mbar_arrive(&cb->b_empty[k & 1]);  // step k's products are complete: B is free
       if (!(ok = s_emit(true, false))) break;
       signal(&cb->a_s);
       if (need_T) {
         if (!(ok = wait_bar_warp(&cb->d_t, k & 1, cb, lv.err))) break;
         tc::tc_fence_after();
+        tc::mbar_arrive(&cb->b_empty[k & 1]);
         t_emit(false);
         signal(&cb->a_t);
       }
-      tc::mbar_arrive(&cb->b_empty[k & 1]);  // step k's products are complete: its B buffer is free
     }
     if (ok && n_steps > 0 && wait_bar_warp(&cb->d_s, (n_steps - 1) & 1, cb, lv.err)) {
       tc::tc_fence_after();
