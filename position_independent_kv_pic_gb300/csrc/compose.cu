@@ -21,11 +21,15 @@
 // global memory into the B operand by TMA without any conversion; the state is
 // split by the epilogue each step.  S_i stays fp32 and is added exactly.
 //
-// Pipeline (320 threads, one CTA per SM).  Warp 8 lane 0 loads T_i by four 16 KB
-// TMA boxes into one of two B buffers and S_i by bulk copies into a staging
-// buffer; warp 9 lane 0 issues the MMAs; warps 0-7 run the epilogue (TMEM + S_i ->
-// split -> TMEM).  The S products and the T products are committed apart, so that
-// each epilogue overlaps the other's MMAs.  Every wait is bounded.
+// Pipeline (352 threads, one CTA per SM).  Warp 8 lane 0 loads T_i by four 16 KB
+// TMA boxes into one of two B buffers; warp 10 lane 0 loads S_i by bulk copies,
+// 32 rows at a time, into two rings of three 16 KB slots — ring h holds the rows that epilogue half h
+// reads, and only that half consumes it, in order (a slot shared by two consumer
+// groups that take turns could be waited on while the other group's earlier fill
+// of it is still in flight, and its parity would then report that fill's previous
+// phase as complete); warp 9 lane 0 issues the MMAs; warps 0-7 run the epilogue
+// (TMEM + S_i -> split -> TMEM).  The S products and the T products are committed
+// apart, so that each epilogue overlaps the other's MMAs.  Every wait is bounded.
 #include <algorithm>
 
 #include "pic_internal.cuh"
@@ -40,33 +44,35 @@ constexpr int kCD = 128;                              // d_k = d_v
 constexpr int kElt = kCD * kCD;                       // elements per matrix
 constexpr int kMatBytes = kElt * 4;                   // 64 KB: one fp32 matrix, or its two bf16 planes
 constexpr int kCWorkers = 256;                        // warps 0-7
-constexpr int kProdWarp = kCWorkers / 32, kMmaWarp = kProdWarp + 1;
-constexpr int kCThreads = kCWorkers + 64;
+constexpr int kProdWarp = kCWorkers / 32, kMmaWarp = kProdWarp + 1, kSProdWarp = kMmaWarp + 1;
+constexpr int kCThreads = kCWorkers + 96;
 constexpr int kBHalf = kCD * 128;                     // one 64-column half of a 128-row bf16 operand
 constexpr int kBPart = 2 * kBHalf;                    // 32 KB: one bf16 part of B
 constexpr int kBBytes = 2 * kBPart;                   // hi | lo
 constexpr int kOffB = 0;                              // two B buffers ([part][k half][128 rows][128 B], SW128)
-constexpr int kOffSs = kOffB + 2 * kBBytes;           // S_i staging, fp32 row-major
-constexpr int kOffBar = kOffSs + kMatBytes;
-constexpr int kCSmem = kOffBar + 128;
+constexpr int kSRows = 32;                            // rows of S per ring block
+constexpr int kSBlk = kSRows * kCD * 4;               // 16 KB
+constexpr int kSRing = 3;                             // slots per ring
+constexpr int kOffSr = kOffB + 2 * kBBytes;           // ring h at kOffSr + h * kSRing * kSBlk
+constexpr int kOffBar = kOffSr + 2 * kSRing * kSBlk;
+constexpr int kCSmem = kOffBar + 256;
 static_assert(kCSmem <= 232448, "shared memory per CTA");
 // TMEM columns: D_S | D_T | A_S hi | A_S lo | A_T hi | A_T lo
 constexpr uint32_t kColDS = 0, kColDT = 128, kColAS = 256, kColAT = 384;
 constexpr uint64_t kCWaitNs = 2000000000ull;
 constexpr uint32_t kCIdesc = tc::idesc_bf16_f32(128, 128, false);
-constexpr int kCopy = 16384;                          // bytes per bulk copy of S
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct CBars {
-  uint64_t b_full[2], b_empty[2];  // per B buffer: T_i landed / released by the step that read it
-  uint64_t s_full, s_empty;        // the S staging buffer
-  uint64_t a_s, a_t;               // A_S / A_T written for the next step
-  uint64_t d_s, d_t;               // the step's S / T products complete
+  uint64_t b_full[2], b_empty[2];            // per B buffer: T_i landed / released by the step that read it
+  uint64_t s_full[2][kSRing], s_empty[2][kSRing];  // per S ring slot
+  uint64_t a_s, a_t;                         // A_S / A_T written for the next step
+  uint64_t d_s, d_t;                         // the step's S / T products complete
   uint32_t tmem;
   int abort;
 };
-static_assert(sizeof(CBars) <= 128, "barrier block");
+static_assert(sizeof(CBars) <= 256, "barrier block");
 
 struct Level {
   const bf16* T_in;          // two bf16 planes per matrix: [matrix][part][128][128]
@@ -207,8 +213,11 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
       tc::mbar_init(&cb->b_full[i], 1);
       tc::mbar_init(&cb->b_empty[i], kCWorkers);
     }
-    tc::mbar_init(&cb->s_full, 1);
-    tc::mbar_init(&cb->s_empty, kCWorkers);
+    for (int hh = 0; hh < 2; ++hh)
+      for (int sl = 0; sl < kSRing; ++sl) {
+        tc::mbar_init(&cb->s_full[hh][sl], 1);
+        tc::mbar_init(&cb->s_empty[hh][sl], kCWorkers / 2);
+      }
     tc::mbar_init(&cb->a_s, kCWorkers);
     tc::mbar_init(&cb->a_t, kCWorkers);
     tc::mbar_init(&cb->d_s, 1);
@@ -227,27 +236,16 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
   const uint32_t tmem = cb->tmem;
   const int n_steps = n - 1;
 
-  if (warp == kProdWarp) {
-    // ---- producer: S_b, T(0), T(1), then S(u) and T(u + 1) in step order.  T(j) =
-    // T_{b+1+j} goes to B buffer j & 1 once the step two before released it; S(u) =
-    // S_{b+u} to the staging buffer once S(u - 1) was read.
-    if (lane == 0) {
-      int s_issued = 0, t_issued = 0;
-      bool ok = true;
-      auto load_s = [&](int u) -> bool {
-        if (!wait_bar(&cb->s_empty, (u & 1) ^ 1, cb, lv.err)) return false;
-        const float* src = lv.S_in + mat(b + u) * kElt;
-        tc::mbar_arrive_expect_tx(&cb->s_full, kMatBytes);
-#pragma unroll
-        for (int c = 0; c < kMatBytes / kCopy; ++c)
-          tc::bulk_load(sm + kOffSs + c * kCopy, reinterpret_cast<const uint8_t*>(src) + c * kCopy, kCopy,
-                        &cb->s_full);
-        s_issued = u + 1;
-        return true;
-      };
-      auto load_t = [&](int j) -> bool {
+  if (warp == kProdWarp || warp == kSProdWarp) {
+    // ---- producers, each its own stream so that neither waits behind the other.
+    // T: T(j) = T_{b+1+j} to B buffer j & 1 once the step two before released it.
+    // S: S(u) = S_{b+u} as block w = 2u + q (rows 64 h + 32 q ..) to slot w % 3 of
+    // ring h once that slot's block w - 3 was read.
+    if (lane == 0 && warp == kProdWarp) {
+      int t_issued = 0;
+      for (int j = 0; j < n_steps; ++j) {
         const int buf = j & 1;
-        if (j >= 2 && !wait_bar(&cb->b_empty[buf], ((j >> 1) & 1) ^ 1, cb, lv.err)) return false;
+        if (j >= 2 && !wait_bar(&cb->b_empty[buf], ((j >> 1) & 1) ^ 1, cb, lv.err)) break;
         const int32_t y0 = (int32_t)(mat(b + 1 + j) * 2 * kCD);
         uint8_t* dst = sm + kOffB + buf * kBBytes;
         tc::mbar_arrive_expect_tx(&cb->b_full[buf], kBBytes);
@@ -257,20 +255,40 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
           for (int kh = 0; kh < 2; ++kh)
             tc::tma_load_2d(dst + p * kBPart + kh * kBHalf, &tmap, 64 * kh, y0 + p * kCD, &cb->b_full[buf]);
         t_issued = j + 1;
-        return true;
-      };
-      ok = load_s(0);
-      for (int j = 0; ok && j < 2 && j < n_steps; ++j) ok = load_t(j);
-      for (int u = 1; ok && u < n; ++u) {
-        ok = load_s(u);
-        if (ok && u + 1 < n_steps) ok = load_t(u + 1);
       }
       // no copy may be in flight when the block exits
       const int no_abort = 0;
-      if (s_issued > 0) tc::mbar_wait(&cb->s_full, (s_issued - 1) & 1, &no_abort, kCWaitNs);
       for (int k = 0; k < 2 && k < t_issued; ++k) {
         const int j = t_issued - 1 - k;
         tc::mbar_wait(&cb->b_full[j & 1], (j >> 1) & 1, &no_abort, kCWaitNs);
+      }
+    } else if (lane == 0) {
+      int w_issued[2] = {0, 0};  // blocks issued per ring
+      bool ok = true;
+      for (int u = 0; ok && u < n; ++u) {
+        const float* src = lv.S_in + mat(b + u) * kElt;
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int w = 2 * u + q, sl = w % kSRing;
+            if (ok && !(ok = wait_bar(&cb->s_empty[hh][sl], ((w / kSRing) & 1) ^ 1, cb, lv.err))) break;
+            if (!ok) break;
+            tc::mbar_arrive_expect_tx(&cb->s_full[hh][sl], kSBlk);
+            tc::bulk_load(sm + kOffSr + (hh * kSRing + sl) * kSBlk,
+                          reinterpret_cast<const uint8_t*>(src + (64 * hh + kSRows * q) * kCD), kSBlk,
+                          &cb->s_full[hh][sl]);
+            if (hh == 0) w_issued[0] = w + 1; else w_issued[1] = w + 1;
+          }
+      }
+      // the last fill of every slot (each earlier fill of a slot was read before
+      // the slot was filled again)
+      const int no_abort = 0;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int wn = hh == 0 ? w_issued[0] : w_issued[1];
+        for (int w = wn - 1; w >= 0 && w >= wn - kSRing; --w)
+          tc::mbar_wait(&cb->s_full[hh][w % kSRing], (w / kSRing) & 1, &no_abort, kCWaitNs);
       }
     }
     __syncwarp();
@@ -322,44 +340,50 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
     const int quarter = warp & 3, hf = warp >> 2;
     const int nc = 32 * quarter + lane, m0 = 64 * hf;
     const uint32_t trow = tmem + (uint32_t)((32 * quarter) << 16);
-    const float* ss = reinterpret_cast<const float*>(sm + kOffSs) + nc;
-    int su = 0;  // S fills consumed
+    const float* ring = reinterpret_cast<const float*>(sm + kOffSr) + hf * kSRing * (kSBlk / 4) + nc;
+    int su = 0;  // S matrices consumed
     bool ok = true;
     auto signal = [&](uint64_t* bar) {
       tc::tmem_st_wait();
       tc::tc_fence_before();
       tc::mbar_arrive(bar);
     };
-    // the staged S (+ the accumulator at d_col, when add_d) -> A at a_col, or the output
+    // the next S (this half's two ring blocks) plus the accumulator at D_S (when
+    // add_d) -> A_S, or the output
     auto s_emit = [&](bool add_d, bool to_out) -> bool {
-      if (!wait_bar_warp(&cb->s_full, su & 1, cb, lv.err)) return false;
-      if (!add_d && !to_out) {  // the first element: S_b -> A_S
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int mf = m0 + 16 * c;
-          uint32_t hi[8], lo[8];
+      for (int q = 0; q < 2; ++q) {
+        const int w = 2 * su + q, sl = w % kSRing;
+        if (!wait_bar_warp(&cb->s_full[hf][sl], (w / kSRing) & 1, cb, lv.err)) return false;
+        const float* blk = ring + sl * (kSBlk / 4);  // rows m0 + 32 q .. of S, column nc
+        if (!add_d && !to_out) {  // the first element: S_b -> A_S
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float x0 = ss[(mf + 2 * j) * kCD], x1 = ss[(mf + 2 * j + 1) * kCD];
-            const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-            hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-            lo[j] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+          for (int c = 0; c < 2; ++c) {
+            const int mf = m0 + kSRows * q + 16 * c;
+            uint32_t hi[8], lo[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float x0 = blk[(16 * c + 2 * j) * kCD], x1 = blk[(16 * c + 2 * j + 1) * kCD];
+              const bf16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+              hi[j] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+              lo[j] = pack_bf16x2(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
+            }
+            tc::tmem_st8(trow + kColAS + (mf >> 1), hi);
+            tc::tmem_st8(trow + kColAS + 64 + (mf >> 1), lo);
           }
-          tc::tmem_st8(trow + kColAS + (mf >> 1), hi);
-          tc::tmem_st8(trow + kColAS + 64 + (mf >> 1), lo);
-        }
-      } else if (!add_d) {  // a one-element segment: S_b is the output
+        } else if (!add_d) {  // a one-element segment: S_b is the output
 #pragma unroll
-        for (int c = 0; c < 64; ++c) s_out[(m0 + c) * kCD + nc] = ss[(m0 + c) * kCD];
-      } else {
+          for (int c = 0; c < kSRows; ++c) s_out[(m0 + kSRows * q + c) * kCD + nc] = blk[c * kCD];
+        } else {
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const int mf = m0 + 16 * c;
-          if (to_out) piece16<true, 1>(ss + mf * kCD, trow, kColDS, mf, nc, s_out, kColAS);
-          else piece16<true, 0>(ss + mf * kCD, trow, kColDS, mf, nc, nullptr, kColAS);
+          for (int c = 0; c < 2; ++c) {
+            const int mf = m0 + kSRows * q + 16 * c;
+            if (to_out) piece16<true, 1>(blk + 16 * c * kCD, trow, kColDS, mf, nc, s_out, kColAS);
+            else piece16<true, 0>(blk + 16 * c * kCD, trow, kColDS, mf, nc, nullptr, kColAS);
+          }
         }
+        tc::mbar_arrive(&cb->s_empty[hf][sl]);
       }
-      tc::mbar_arrive(&cb->s_empty);
       ++su;
       return true;
     };
