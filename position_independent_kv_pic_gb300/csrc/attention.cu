@@ -796,10 +796,19 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
       }
       const uint32_t vld = ld + 1;
       const int vs = vld % kSlots;
-      // waiting for every V tile (not only partial ones) keeps these warps at most
-      // one phase ahead of the MMA issuer on vz_done: the slot is not refilled
-      // before its previous P.V, which waits for vz_done, has completed
-      if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1)) { fail(b, a.err); return; }
+      // A slot takes K and V loads in turn, and these warps must see every phase of
+      // it in order: a parity wait on the V load's phase while the slot's previous
+      // fill (a K load) is still in flight would find that fill's previous phase
+      // complete and pass at once.  So the K load is waited for first (rotate-on-read
+      // did so above).  Waiting for every V tile (not only partial ones) keeps these
+      // warps at most one phase ahead of the MMA issuer on vz_done: the slot is not
+      // refilled before its previous P.V, which waits for vz_done, has completed.
+      if (!kRor) {
+        const bool got = wait_bar(b, &b->kv_full[ld % kSlots], (ld / kSlots) & 1);
+        if (!__all_sync(0xffffffffu, got)) { fail(b, a.err); return; }
+      }
+      const bool vgot = wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1);
+      if (!__all_sync(0xffffffffu, vgot)) { fail(b, a.err); return; }
       if (!full) {
         const int packed = plo | (phi << 16);
         uint8_t* vsm = smem + kOffSlot + vs * kOpBytes;

@@ -75,3 +75,30 @@ def test_decode_gqa_groups(Hq):
 def test_decode_unsupported_shape_is_refused():
     assert pic.pic_decode_workspace(1, 4, 2, 16, pic.PIC_FP32) == 0
     assert pic.pic_decode_workspace(1, 32, 8, 128, pic.PIC_BF16) > 0
+
+
+def test_link_attention_on_decode_rows_repeated():
+    """One row per request through the link attention kernel, many calls back to
+    back (the shape that exposed the V-zeroing warps' parity wait on a slot's K
+    phase): no error, the decode kernel's result, the same bits every call."""
+    wl = inputs.batched_shared()
+    b = LinkBatch(wl)
+    b.run()
+    b.setup_decode()
+    b.run_decode()
+    torch.cuda.synchronize()
+    assert b.error() == 0
+    row_off = torch.arange(b.n_req + 1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(max(pic.pic_link_attention_workspace(b.n_req, b.n_req, wl.Hq, wl.Hkv, wl.d, b.pic_dtype), 256),
+                     dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(12):
+        out = torch.empty_like(b.dec_out)
+        pic.pic_link_attention(b.dec_q, b.dec_table, b.dec_pos, row_off, b.k_pool, b.v_pool, b.pic_dtype,
+                               b.dec_pages, b.dec_page_off, b.n_req, b.n_req, wl.Hq, wl.Hkv, wl.d, b.scale, out, ws,
+                               b.err)
+        outs.append(out)
+    torch.cuda.synchronize()
+    assert b.error() == 0, pic.pic_strerror(b.error())
+    assert all(torch.equal(o, outs[0]) for o in outs)
+    assert (outs[0].float() - b.dec_out.float()).abs().max().item() <= 2e-3
