@@ -36,14 +36,20 @@ sys.path.insert(0, ROOT)
 METRIC = "PIC link: context tokens/s per layer; % of HBM / bf16 tensor-core roofline"
 UNIT = "tokens/s"
 
-# ncu DRAM bytes (read + write) per launch of the attention call and of the
-# re-rotation kernel, with the kernel source they were taken from; reported as
-# roofline traffic only while the source is unchanged.
+# ncu DRAM bytes (read + write) per launch of each timed kernel (per call for the
+# two-launch composition), with the kernel source they were taken from; reported
+# as roofline traffic only while the source is unchanged.
 NCU_TRAFFIC = {
-    # link_attn_tc_kernel, long_context_100x1000: 826.76 MB read + 79.89 MB written
-    ("attention", "4ef262dc2ec56e0f"): 906654464,
-    # rerotate_kernel<bf16>, long_context_100x1000: 201.39 MB read + 140.65 MB written
-    ("rerotate", "4674536b57c630e1"): 342040576,
+    # link_attn_tc_kernel<0>, long_context_100x1000: 833.74 MB read + 80.06 MB written
+    ("attention", "6ee31b9e33ca4f89"): 913804288,
+    # rerotate_kernel<bf16>, long_context_100x1000: 201.35 MB read + 140.40 MB written
+    ("rerotate", "94fbac229e1fc877"): 341751552,
+    # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.40 MB written
+    ("scheme_b", "94fbac229e1fc877"): 449222144,
+    # decode_kernel<4>, one row per request over the long-context link: 420.66 MB read + 3.59 MB written
+    ("decode", "5beb31d91b1b73b1"): 424247296,
+    # compose_kernel, 32 heads x 100-chunk chain, both levels: 417.43 + 14.75 MB read + 3.52 MB written
+    ("compose", "e43e88d53b50babb"): 435703296,
 }
 
 
@@ -340,6 +346,9 @@ def run_gpu(args, rank, world):
     rot_gbs = rot_bytes / (rot_avg / 1e3) / 1e9
     traffic = NCU_TRAFFIC.get(("attention", _src_hash("attention.cu")))
     rtraffic = NCU_TRAFFIC.get(("rerotate", _src_hash("rotate.cu")))
+    btraffic = NCU_TRAFFIC.get(("scheme_b", _src_hash("rotate.cu")))
+    dtraffic = NCU_TRAFFIC.get(("decode", _src_hash("decode.cu")))
+    ctraffic = NCU_TRAFFIC.get(("compose", _src_hash("compose.cu")))
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -364,12 +373,12 @@ def run_gpu(args, rank, world):
                           "frac_of_sustained": att_tflops / tf_sus if tf_sus else None},
             **({"decode": {"bound": "hbm", "achieved": dec[2] / (dec[1] / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                            "frac": dec[2] / (dec[1] / 1e3) / 1e9 / hbm, "ms": dec[1], "ms_per_decode_step": dec[0],
-                           "algorithmic_bytes": dec[2], "steps": dec[3],
+                           "algorithmic_bytes": dec[2], "steps": dec[3], "traffic": dtraffic,
                            "kernel": "pic_decode_attention (split-KV decode + merge), one new row per request; "
                                      "the step adds its RoPE table and K/V write"}} if dec else {}),
             **({"scheme_b": {"bound": "hbm", "achieved": schb[2] / (schb[1] / 1e3) / 1e9, "peak": hbm, "unit": "GB/s",
                              "frac": schb[2] / (schb[1] / 1e3) / 1e9 / hbm, "ms": schb[1],
-                             "algorithmic_bytes": schb[2], "ms_per_step": schb[0],
+                             "algorithmic_bytes": schb[2], "ms_per_step": schb[0], "traffic": btraffic,
                              "tokens_per_s": world * schb[4] / (schb[0] / 1e3), "steps": schb[3],
                              "kernel": "pic_rope_cached_k (scheme B: cached K encoded at its global position; "
                                        "bytes = K read + written + one table row per slot); the step runs "
@@ -384,7 +393,7 @@ def run_gpu(args, rank, world):
                                              "re-rotation pass"}} if ror else {}),
             **({"compose": {"bound": "hbm", "achieved": comp[1] / (comp[0] / 1e3) / 1e9, "peak": hbm,
                             "unit": "GB/s", "frac": comp[1] / (comp[0] / 1e3) / 1e9 / hbm, "ms": comp[0],
-                            "algorithmic_bytes": comp[1], "steps": comp[2], "seg": comp[3], "chains": comp[4],
+                            "algorithmic_bytes": comp[1], "steps": comp[2], "seg": comp[3], "chains": comp[4], "traffic": ctraffic,
                             "chain_elements": comp[5], "launches": comp[6],
                             "kernel": "pic_compose_states (linear-layer state S = T_n(..(T_2 S_1 + S_2)..) + S_n "
                                       "per request and head, 32 heads of 128 x 128 fp32 states; bytes = S of "

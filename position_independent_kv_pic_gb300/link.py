@@ -182,8 +182,8 @@ class LinkBatch:
 
     # ------------------------------------------------------------------ step
     # kernels one run() launches: select, splice, 2 tables, re-rotate, fresh K/V, and the
-    # attention call (unit planning, attention, LSE merge)
-    LAUNCHES_PER_STEP = 9  # rotary correction; scheme B (no offset table) and rotate-on-read (no re-rotation): 8
+    # attention (unit planning, Q pre-pass, attention, LSE merge)
+    LAUNCHES_PER_STEP = 10  # rotary correction; scheme B (no offset table) and rotate-on-read (no re-rotation): 9
 
     @property
     def launches_per_step(self) -> int:
