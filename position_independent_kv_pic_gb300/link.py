@@ -189,15 +189,19 @@ class LinkBatch:
     def launches_per_step(self) -> int:
         return self.LAUNCHES_PER_STEP - (1 if self.scheme in ("nope", "ror") else 0)
 
-    def run(self, stream=None, marks=None):
+    def run(self, stream=None, marks=None, inputs=None, out=None):
         """The link step: a1 select, splice, a2 tables, a3 re-rotate, a4 fresh K/V, a5+a6 attention.
 
         The cached-K pass (re-rotation, or scheme B's encoding) runs on a side stream
         beside the work that reads no cached K — the row table, the fresh K/V, the
         attention plan — and the attention run waits for both.  ``marks`` (optional)
         maps "rerotate" / "attention" to (start, end) CUDA events recorded around the
-        cached-K pass (on the side stream) and the attention run."""
-        wl, dv = self.wl, self.dev
+        cached-K pass (on the side stream) and the attention run.  ``inputs`` / ``out``
+        (optional) replace the step's device inputs (a dict like ``self.dev``) and its
+        output tensor, for a caller that double-buffers them (LinkPipeline)."""
+        wl = self.wl
+        dv = self.dev if inputs is None else inputs
+        out_t = self.out if out is None else out
         mk = marks or {}
         if stream is None:
             main = torch.cuda.current_stream(self.device)
@@ -243,7 +247,7 @@ class LinkBatch:
                 mk["attention"][0].record(main)
             pic_link_attention_ror(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
                                    self.pic_dtype, self.pages, self.page_tab, self.delta_table, dv["page_off"],
-                                   self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.scale, self.out, self.ws,
+                                   self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.scale, out_t, self.ws,
                                    self.err, main)
         else:
             pic_link_attention_plan(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.pages,
@@ -254,7 +258,7 @@ class LinkBatch:
                 mk["attention"][0].record(main)
             pic_link_attention_run(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.k_pool, self.v_pool,
                                    self.pic_dtype, self.pages, dv["page_off"], self.n_req, self.n_rows, wl.Hq,
-                                   wl.Hkv, wl.d, self.scale, self.out, self.ws, self.err, main)
+                                   wl.Hkv, wl.d, self.scale, out_t, self.ws, self.err, main)
         if "attention" in mk:
             mk["attention"][1].record(main)
 
@@ -368,3 +372,55 @@ def _main():
 
 if __name__ == "__main__":
     _main()
+
+
+class LinkPipeline:
+    """Link steps back to back with every step's input upload (host -> device, from
+    pinned memory) and output read-back (device -> host) on their own copy streams,
+    overlapped with the neighbouring steps' kernels: the device inputs and outputs
+    are double-buffered, so step i + 1's upload and step i - 1's read-back run while
+    step i computes.  The step itself is LinkBatch.run on the current stream."""
+
+    def __init__(self, batch: LinkBatch):
+        self.b = batch
+        dev = batch.device
+        self.sets = [batch.dev, {n: torch.empty_like(t) for n, t in batch.dev.items()}]
+        self.outs = [batch.out, torch.empty_like(batch.out)]
+        self.host_out = [torch.empty(batch.out.shape, dtype=batch.out.dtype).pin_memory() for _ in range(2)]
+        self.h2d = torch.cuda.Stream(dev)
+        self.d2h = torch.cuda.Stream(dev)
+        self.uploaded = [torch.cuda.Event() for _ in range(2)]
+        self.computed = [torch.cuda.Event() for _ in range(2)]
+        self.read = [torch.cuda.Event() for _ in range(2)]
+        self.i = 0
+
+    def begin(self, stream=None):
+        """Order the copy streams after everything issued so far on ``stream``."""
+        main = torch.cuda.current_stream(self.b.device) if stream is None else stream
+        ev = torch.cuda.Event()
+        ev.record(main)
+        self.h2d.wait_event(ev)
+        self.d2h.wait_event(ev)
+
+    def submit(self, host_inputs, stream=None):
+        """Queue one step on ``host_inputs`` (pinned tensors named as LinkBatch.host).
+        Returns (pinned host output, event recorded once it has arrived)."""
+        main = torch.cuda.current_stream(self.b.device) if stream is None else stream
+        k = self.i % 2
+        if self.i >= 2:
+            self.h2d.wait_event(self.computed[k])  # the step two back has finished reading set k
+        for n, t in host_inputs.items():
+            with torch.cuda.stream(self.h2d):
+                self.sets[k][n].copy_(t, non_blocking=True)
+        self.uploaded[k].record(self.h2d)
+        main.wait_event(self.uploaded[k])
+        if self.i >= 2:
+            main.wait_event(self.read[k])  # out k's previous result has been read back
+        self.b.run(stream=main, inputs=self.sets[k], out=self.outs[k])
+        self.computed[k].record(main)
+        self.d2h.wait_event(self.computed[k])
+        with torch.cuda.stream(self.d2h):
+            self.host_out[k].copy_(self.outs[k], non_blocking=True)
+        self.read[k].record(self.d2h)
+        self.i += 1
+        return self.host_out[k], self.read[k]
