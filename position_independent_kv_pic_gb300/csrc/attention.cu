@@ -361,8 +361,9 @@ constexpr int kUnitReaders = 1 + 2 + 4 * kSmWarpgroups;  // MMA thread, 2 V-zero
 
 struct Bars {
   uint64_t kv_full[kSlots], kv_empty[kSlots];
-  uint64_t vz_done[kSlots];  // V tile t (t % kSlots) checked and its invalid rows zeroed
-  uint64_t kr_done[kSlots];  // rotate-on-read: K tile t (t % kSlots) rotated to its global positions
+  // key tile t (t % kSlots) ready for the MMAs: its K and V landed, K rotated to its
+  // global positions when rotating on read, V's invalid rows zeroed
+  uint64_t vz_done[kSlots];
   uint64_t q_full[kQTiles], q_free[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
   int unit_idx[kUnitRing];
@@ -522,10 +523,13 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
   const uint32_t k_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), 16);
   const uint32_t v_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), kPageHalfBytes);
   uint32_t ld = 0, uq[kQTiles] = {0, 0}, c[kQTiles] = {0, 0};
-  // K load l (even): landed, and rotated when rotating on read
-  auto wait_k = [&](uint32_t l) -> bool {
-    if (!wait_bar(b, &b->kv_full[l % kSlots], (l / kSlots) & 1)) return false;
-    return !kRor || wait_bar(b, &b->kr_done[(l / 2) % kSlots], ((l / 2) / kSlots) & 1);
+  // Key tile t: its K and V landed (the V-zeroing warps waited for both loads),
+  // K rotated when rotating on read, V's invalid rows zeroed.  The issuer waits for
+  // this one barrier per tile, before the tile's first S product, and never for the
+  // loads themselves: every wait costs issue time between MMA groups, when the
+  // tensor pipe runs dry.
+  auto wait_tile = [&](uint32_t t) -> bool {
+    return wait_bar(b, &b->vz_done[t % kSlots], (t / kSlots) & 1);
   };
   auto issue_s = [&](int i, int slot) {
     const uint32_t qa = q_lo + i * (kOpBytes >> 4), kb = k_lo + slot * (kOpBytes >> 4);
@@ -561,7 +565,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
     tc::tc_fence_after();
     {  // S for the first key tile
       const int ks = ld % kSlots;
-      if (!wait_k(ld)) { fail(b, a.err); return; }
+      if (!wait_tile(ld / 2)) { fail(b, a.err); return; }
       tc::tc_fence_after();
       issue_s(0, ks);
       tc::mma_commit(&b->s_full[0]);
@@ -577,12 +581,6 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       const uint32_t vld = ld + 1, nld = ld + 2;
       const int vs = vld % kSlots, ns = nld % kSlots;
       const bool more = j + 1 < n;
-      const uint32_t vt = ld / 2;  // V tile number (one V load per key tile)
-      if (!wait_bar(b, &b->kv_full[vs], (vld / kSlots) & 1) ||
-          !wait_bar(b, &b->vz_done[vt % kSlots], (vt / kSlots) & 1)) {
-        fail(b, a.err);
-        return;
-      }
 #pragma unroll
       for (int i = 0; i < kQTiles; ++i) {
         if (i == 1 && !act1) break;
@@ -591,7 +589,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
         tc::tc_fence_after();
         issue_pv(i, vs, j > 0);
         if (more) {
-          if (i == 0 && !wait_k(nld)) { fail(b, a.err); return; }
+          if (i == 0 && !wait_tile(nld / 2)) { fail(b, a.err); return; }
           tc::tc_fence_after();
           issue_s(i, ns);
           tc::mma_commit(&b->s_full[i]);
@@ -792,7 +790,6 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
         rotate_k_tile(smem + kOffSlot + ks * kOpBytes, tab, a.rot_tab, 32 * wz + lane, rc);
         tc::fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(&b->kr_done[(ld / 2) % kSlots]);
       }
       const uint32_t vld = ld + 1;
       const int vs = vld % kSlots;
@@ -800,9 +797,11 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
       // it in order: a parity wait on the V load's phase while the slot's previous
       // fill (a K load) is still in flight would find that fill's previous phase
       // complete and pass at once.  So the K load is waited for first (rotate-on-read
-      // did so above).  Waiting for every V tile (not only partial ones) keeps these
-      // warps at most one phase ahead of the MMA issuer on vz_done: the slot is not
-      // refilled before its previous P.V, which waits for vz_done, has completed.
+      // did so above).  vz_done is the MMA issuer's only sign that the tile's K and V
+      // have landed, so it is arrived for every tile (not only partial ones), after
+      // both loads were seen; this also keeps these warps at most one phase ahead of
+      // the issuer on it: a slot is not refilled before the MMAs that read it, which
+      // follow the issuer's wait for vz_done, have completed.
       if (!kRor) {
         const bool got = wait_bar(b, &b->kv_full[ld % kSlots], (ld / kSlots) & 1);
         if (!__all_sync(0xffffffffu, got)) { fail(b, a.err); return; }
@@ -1042,7 +1041,6 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mbar_init(&b->kv_full[s], 1);
       tc::mbar_init(&b->kv_empty[s], 1);
       tc::mbar_init(&b->vz_done[s], 2);
-      tc::mbar_init(&b->kr_done[s], 2);
     }
     for (int i = 0; i < kQTiles; ++i) {
       tc::mbar_init(&b->q_full[i], 1);
