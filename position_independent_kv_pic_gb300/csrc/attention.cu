@@ -1242,22 +1242,6 @@ selftest_umma_kernel(const __grid_constant__ CUtensorMap bmap, const bf16* __res
 }
 
 // ------------------------------------------------------------------ host side
-// 2-D view [rows][128] bf16 of a buffer, boxes of 16 rows x 64 columns, 128-byte swizzle.
-// Rows of 128 bf16 (one (block, head, slot) key row each) viewed as
-// [row group][half][row in group][64 columns], so that one box of 2 x 2 x 8 x 64
-// moves a whole 16-row page into the [group][half][8 rows] slot layout.
-bool encode_pages(CUtensorMap* map, const void* base, uint64_t rows) {
-  auto enc = tensor_map_encoder();
-  if (enc == nullptr || rows % 8) return false;
-  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
-  cuuint64_t strides[3] = {kD * sizeof(bf16), 64 * sizeof(bf16), 8 * kD * sizeof(bf16)};
-  cuuint32_t box[4] = {64, 8, 2, PIC_PAGE / 8};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 bool tc_shape(pic_dtype dt, int Hq, int Hkv, int d) {
   if (dt != PIC_BF16 || d != kD || Hkv < 1 || Hq % Hkv) return false;
   const int G = Hq / Hkv;
@@ -1374,6 +1358,20 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }();
   return fn;
+}
+
+// Rows of 128 bf16 viewed as [row group][half][row in group][64 columns]: one box of
+// 2 x 2 x 8 x 64 moves a whole 16-row page into the [group][half][8 rows] layout.
+bool encode_pages(CUtensorMap* map, const void* base, uint64_t rows) {
+  auto enc = tensor_map_encoder();
+  if (enc == nullptr || rows % 8) return false;
+  cuuint64_t dims[4] = {64, 8, 2, rows / 8};
+  cuuint64_t strides[3] = {128 * sizeof(__nv_bfloat16), 64 * sizeof(__nv_bfloat16), 8 * 128 * sizeof(__nv_bfloat16)};
+  cuuint32_t box[4] = {64, 8, 2, PIC_PAGE / 8};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace pic

@@ -5,14 +5,17 @@
 // cached K and V row is read once, and g query heads share each row.
 //
 // Split-KV: CTA (split, KV head, request) walks one span of the request's pages.
-// A producer thread streams each page's K and V (4 KB each, one bulk copy apiece)
-// into a ring of shared-memory stages; four consumer warps take the stages in
-// turn, each keeping an online softmax for the g query heads of the KV head.  In a
-// page, lane l scores key l % 16 over half l / 16 of the head dimension for all g
-// heads (reading its 16-byte chunks in an order rotated by the key, so a warp's
-// reads hit distinct banks), the two halves add up, and P.V runs with lane l
-// owning columns 4l..4l+3.  The CTA combines its warps and writes one partial
-// (m, l, unnormalised o); a merge kernel combines the splits.
+// A producer thread moves each page's K and V (4 KB each, one swizzled TMA box
+// apiece, the link attention's page layout) into a ring of shared-memory stages;
+// four consumer warps take the stages in turn, each keeping an online softmax for
+// the g query heads of the KV head.  A page is two small contractions per warp —
+// S = Q K^T (g heads x 16 keys x 128) and O += P V (g heads x 16 keys x 128) —
+// done with the warp-level bf16 tensor-core MMA (m16n8k16, fp32 accumulate; the g
+// heads are rows 0..g-1 of the 16-row operand), operands read with ldmatrix from
+// the swizzled page (conflict-free), P kept in registers between the two.  That
+// is ~100 instructions per page and warp instead of ~700 on the FMA pipe, so the
+// CTA streams pages at the HBM rate.  The CTA combines its warps and writes one
+// partial (m, l, unnormalised o); a merge kernel combines the splits.
 #include <algorithm>
 
 #include "pic_internal.cuh"
@@ -26,9 +29,12 @@ using bf16 = __nv_bfloat16;
 constexpr int kDecD = 128;
 constexpr int kDecWarps = 4;                     // consumer warps
 constexpr int kDecThreads = 32 * (kDecWarps + 1);  // + the producer warp
-constexpr int kDecStages = 4;                    // ring stages of one page (K and V): one per consumer warp
+constexpr int kDecStages = 8;                    // ring stages of one page (K and V), two per consumer warp
+// A consumer warp must see every phase of its stages' barriers in order (a parity
+// wait two phases ahead would pass on the older phase): warp w takes pages
+// w, w + 4, .., so stage i % kDecStages must always belong to warp i % kDecWarps.
+static_assert(kDecStages % kDecWarps == 0, "each stage belongs to one consumer warp");
 constexpr int kPageHead = PIC_PAGE * kDecD * 2;  // bytes of one page of one KV head
-constexpr int kQPad = 12;                        // floats per 8-column chunk of Q in shared memory
 constexpr int kMergeGroups = 8;   // thread groups of the merge, each over every 8th split
 constexpr uint64_t kDecWaitNs = 2000000000ull;
 
@@ -86,10 +92,43 @@ decode_plan_kernel(const int32_t* __restrict__ page_off, int n_req, int Hkv, int
   if (tid == 0) first[n_req] = carry;
 }
 
-// Two bf16 (low, high half of w) as a packed fp32 pair: a bf16 is the top half of
-// the fp32 with the same value.
-__device__ __forceinline__ uint64_t bf16x2_to_f32x2(uint32_t w) {
-  return (uint64_t)(w << 16) | ((uint64_t)(w & 0xffff0000u) << 32);
+// Warp-level bf16 MMA m16n8k16 with fp32 accumulate, rows 8..15 of A zero: d0, d1
+// (row g = lane / 4, columns 2 (lane % 4), +1) accumulate in place; the outputs of
+// the zero rows are discarded.
+__device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  float z0, z1;
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%10,%11,%12,%13};"
+      : "=f"(d0), "=f"(d1), "=f"(z0), "=f"(z1)
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(0.f), "f"(0.f));
+}
+
+// Four 8x8 bf16 matrices from shared memory; lane l gives the address of row l % 8
+// of matrix l / 8.  trans: each matrix transposed on the way.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Byte offset in a swizzled page (see encode_pages) of key row `key`, 16-byte
+// chunk `chunk` (0..15 over the 128 columns).
+__device__ __forceinline__ uint32_t swz_off(int key, int chunk) {
+  const int r = key & 7;
+  return (uint32_t)((key >> 3) * 2048 + (chunk >> 3) * 1024 + r * 128 + (((chunk & 7) ^ r) << 4));
 }
 
 // Named barrier (id 1) of all the block's warps, met by the producer after its last
@@ -100,27 +139,36 @@ __device__ __forceinline__ void ring_drained_sync() {
 
 template <int G>
 struct DecSmem {
-  // K page, V page per stage; once every copy has landed and been read, the ring
-  // takes the warps' partial outputs
+  // K page, V page per stage (1 KB-aligned swizzle atoms); once every copy has
+  // landed and been read, the ring takes the warps' partial outputs
   union {
     uint8_t ring[kDecStages][2][kPageHead];
     float w_o[kDecWarps][G][kDecD];
   };
   uint64_t full[kDecStages], empty[kDecStages];
-  float q[G][2][8][kQPad];                 // [head][half][chunk][8 + pad]
-  float p[kDecWarps][G][PIC_PAGE];         // a page's weights, per consumer warp
+  int meta[kDecStages];          // the stage's page: valid slots lo | hi << 8, or -1 when skipped
+  __nv_bfloat16 qb[G][kDecD];    // Q of the g heads, roped and rounded to bf16
   float w_m[kDecWarps][G], w_l[kDecWarps][G];
   int abort;
 };
 
+// Three CTAs per SM (registers capped at 136): the bytes in flight per SM and the
+// number of consumer warps both bound the streaming rate (two CTAs were 1.7x slower
+// on a 16-request batch).
 template <int G>
-__global__ void __launch_bounds__(kDecThreads)
-decode_kernel(const bf16* __restrict__ q, const float4* __restrict__ q_table, const bf16* __restrict__ kp,
-              const bf16* __restrict__ vp, int64_t num_blocks, const pic_link_page* __restrict__ pages,
-              const int32_t* __restrict__ page_off, int n_req, int Hq, int Hkv, float scale_log2,
-              const int32_t* __restrict__ first, const int32_t* __restrict__ nsplit, float2* __restrict__ part_ml,
-              float* __restrict__ part_o, int32_t* err) {
-  extern __shared__ __align__(128) uint8_t dec_smem_raw[];
+__global__ void __launch_bounds__(kDecThreads, 3)
+decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+              const bf16* __restrict__ q, const float4* __restrict__ q_table, int64_t num_blocks,
+              const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off, int n_req, int Hq,
+              int Hkv, float scale_log2, const int32_t* __restrict__ first, const int32_t* __restrict__ nsplit,
+              float2* __restrict__ part_ml, float* __restrict__ part_o, int32_t* err) {
+  static_assert(G <= 8, "heads of a KV head: rows 0..7 of the MMA operand");
+  extern __shared__ __align__(1024) uint8_t dec_smem_raw[];
+  // the swizzled stages need 1024-byte alignment
+  if (tc::smem_addr(dec_smem_raw) & 1023u) {
+    if (threadIdx.x == 0) set_err(err, PIC_ERR_UNSUPPORTED);
+    return;
+  }
   DecSmem<G>& sm = *reinterpret_cast<DecSmem<G>*>(dec_smem_raw);
   const int cta = blockIdx.x;
   if (cta >= first[n_req]) return;  // the grid is an upper bound
@@ -151,8 +199,8 @@ decode_kernel(const bf16* __restrict__ q, const float4* __restrict__ q_table, co
     const bf16* src = q + ((int64_t)r * Hq + kvh * G + hh) * kDecD;
     float ya, yb;
     rope_rotate_bf16in(to_f32(src[i]), to_f32(src[i + kDecD / 2]), q_table[(int64_t)r * (kDecD / 2) + i], ya, yb);
-    sm.q[hh][0][i >> 3][i & 7] = to_f32(from_f32<bf16>(ya));
-    sm.q[hh][1][i >> 3][i & 7] = to_f32(from_f32<bf16>(yb));
+    sm.qb[hh][i] = from_f32<bf16>(ya);
+    sm.qb[hh][i + kDecD / 2] = from_f32<bf16>(yb);
   }
   __syncthreads();
 
@@ -162,24 +210,30 @@ decode_kernel(const bf16* __restrict__ q, const float4* __restrict__ q_table, co
   const int n = max(pe - pb, 0);
 
   if (warp == kDecWarps) {
-    // ---- producer: lane 0 streams the span's pages through the ring
+    // ---- producer: lane 0 streams the span's pages through the ring, reading each
+    // page entry one page ahead
     if (lane == 0) {
       int issued = 0;
+      int4 nxt = n > 0 ? __ldg(reinterpret_cast<const int4*>(pages) + pb) : make_int4(-1, -1, 0, 0);
       for (int i = 0; i < n; ++i) {
         const int st = i % kDecStages;
+        const int4 pg = nxt;
+        if (i + 1 < n) nxt = __ldg(reinterpret_cast<const int4*>(pages) + pb + i + 1);
         if (!tc::mbar_wait(&sm.empty[st], ((i / kDecStages) & 1) ^ 1, &sm.abort, kDecWaitNs)) {
           set_err(err, PIC_ERR_TIMEOUT);
           *reinterpret_cast<volatile int*>(&sm.abort) = 1;
           break;
         }
-        const int4 pg = __ldg(reinterpret_cast<const int4*>(pages) + pb + i);
         const int lo = (int16_t)(pg.w & 0xffff), hi = (int16_t)(pg.w >> 16);
         const bool ok = pg.x >= 0 && pg.x < num_blocks && pg.y >= 0 && pg.y < num_blocks && lo >= 0 &&
                         hi <= PIC_PAGE && lo < hi;
+        if (!ok && !(lo >= hi && lo >= 0 && hi <= PIC_PAGE)) set_err(err, PIC_ERR_RANGE);
+        // the consumers read the page's slots from here (published by the arrival below)
+        sm.meta[st] = ok ? (lo | (hi << 8)) : -1;
         if (ok) {
           tc::mbar_arrive_expect_tx(&sm.full[st], 2 * kPageHead);
-          tc::bulk_load(sm.ring[st][0], kp + ((int64_t)pg.x * Hkv + kvh) * PIC_PAGE * kDecD, kPageHead, &sm.full[st]);
-          tc::bulk_load(sm.ring[st][1], vp + ((int64_t)pg.y * Hkv + kvh) * PIC_PAGE * kDecD, kPageHead, &sm.full[st]);
+          tc::tma_load_4d(sm.ring[st][0], &kmap, 0, 0, 0, (pg.x * Hkv + kvh) * (PIC_PAGE / 8), &sm.full[st]);
+          tc::tma_load_4d(sm.ring[st][1], &vmap, 0, 0, 0, (pg.y * Hkv + kvh) * (PIC_PAGE / 8), &sm.full[st]);
         } else {
           tc::mbar_arrive(&sm.full[st]);  // nothing to load: the consumer skips the page
         }
@@ -195,18 +249,24 @@ decode_kernel(const bf16* __restrict__ q, const float4* __restrict__ q_table, co
     __syncwarp();
     ring_drained_sync();
   } else {
-    // ---- consumers: warp w takes pages w, w + 4, ..
-    const int key = lane & 15, half = lane >> 4;
-    // o: columns 4 lane .. +3 of every head as two packed pairs; lsum: this lane's
-    // share of the row sums (its key, counted in the half-0 lane only)
-    float m[G], lsum[G];
-    uint64_t o01[G], o23[G];
+    // ---- consumers: warp w takes pages w, w + 4, ..  Lane (g, t) = (lane / 4,
+    // lane % 4) holds row g (head g of the KV head; rows >= G are padding) of the
+    // MMA fragments: Q at columns 16 ks + 2t, +1 and +8, +9; S at keys 2t, 2t+1 and
+    // 8 + 2t, 9 + 2t; O at columns 8 nt + 2t, +1.
+    const int g = lane >> 2, t = lane & 3;
+    const bool row = g < G;
+    uint32_t qa[kDecD / 16], qc[kDecD / 16];
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      m[hh] = -INFINITY;
-      lsum[hh] = 0.f;
-      o01[hh] = o23[hh] = 0;
+    for (int ks = 0; ks < kDecD / 16; ++ks) {
+      qa[ks] = row ? *reinterpret_cast<const uint32_t*>(&sm.qb[row ? g : 0][16 * ks + 2 * t]) : 0u;
+      qc[ks] = row ? *reinterpret_cast<const uint32_t*>(&sm.qb[row ? g : 0][16 * ks + 2 * t + 8]) : 0u;
     }
+    float o[kDecD / 8][2];
+#pragma unroll
+    for (int nt = 0; nt < kDecD / 8; ++nt) o[nt][0] = o[nt][1] = 0.f;
+    float m_ref = -INFINITY, lsum = 0.f;  // lazy running max (log2 units) and this lane's row-sum share
+    // ldmatrix row addresses: lane l gives row l % 8 of matrix l / 8
+    const int mr = lane & 7, mi = lane >> 3;
     for (int i = warp; i < n; i += kDecWarps) {
       const int st = i % kDecStages;
       if (!tc::mbar_wait(&sm.full[st], (i / kDecStages) & 1, &sm.abort, kDecWaitNs)) {
@@ -216,98 +276,82 @@ decode_kernel(const bf16* __restrict__ q, const float4* __restrict__ q_table, co
         }
         break;
       }
-      const int4 pg = __ldg(reinterpret_cast<const int4*>(pages) + pb + i);
-      const int lo = (int16_t)(pg.w & 0xffff), hi = (int16_t)(pg.w >> 16);
-      const bool ok = pg.x >= 0 && pg.x < num_blocks && pg.y >= 0 && pg.y < num_blocks && lo >= 0 &&
-                      hi <= PIC_PAGE && lo < hi;
-      if (!ok) {
-        if (lane == 0 && !(lo >= hi && lo >= 0 && hi <= PIC_PAGE)) set_err(err, PIC_ERR_RANGE);
-      } else {
-        const uint8_t* kpage = sm.ring[st][0];
-        const uint8_t* vpage = sm.ring[st][1];
-        // scores on packed pairs (even, odd columns)
-        uint64_t s2[G];
+      const int mt = sm.meta[st];
+      if (mt >= 0) {
+        const int lo = mt & 0xff, hi = (mt >> 8) & 0xff;
+        const uint32_t kbase = tc::smem_addr(sm.ring[st][0]), vbase = tc::smem_addr(sm.ring[st][1]);
+        // S = Q K^T over the 16 keys: matrices (keys 0-7 | 8-15) x (columns 16ks.. | 16ks+8..)
+        float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) s2[hh] = 0;
+        for (int ks = 0; ks < kDecD / 16; ++ks) {
+          uint32_t b[4];
+          ldsm_x4(b, kbase + swz_off(8 * (mi >> 1) + mr, 2 * ks + (mi & 1)));
+          mma_rows8(s0[0], s0[1], qa[ks], qc[ks], b[0], b[1]);
+          mma_rows8(s1[0], s1[1], qa[ks], qc[ks], b[2], b[3]);
+        }
+        // online softmax of row g over the page's valid keys [lo, hi)
+        const int k0 = 2 * t;
+        float sc[4] = {s0[0], s0[1], s1[0], s1[1]};
+        const int kk[4] = {k0, k0 + 1, k0 + 8, k0 + 9};
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const int cc = (c8 + key) & 7;
-          const uint4 kr = *reinterpret_cast<const uint4*>(kpage + key * (2 * kDecD) + half * kDecD + cc * 16);
-          const uint64_t k2[4] = {bf16x2_to_f32x2(kr.x), bf16x2_to_f32x2(kr.y), bf16x2_to_f32x2(kr.z),
-                                  bf16x2_to_f32x2(kr.w)};
+        for (int x = 0; x < 4; ++x) sc[x] = (kk[x] >= lo && kk[x] < hi) ? sc[x] * scale_log2 : -INFINITY;
+        float mx = fmaxf(fmaxf(sc[0], sc[1]), fmaxf(sc[2], sc[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        // lazy rescale: P may grow up to 2^8 before O and the sums are rescaled
+        const bool up = mx > m_ref + 8.f;
+        if (__any_sync(0xffffffffu, up)) {
+          const float alpha = up ? tc::ex2(m_ref - mx) : 1.f;  // 0 on the first page (m_ref = -inf)
+          lsum *= alpha;
 #pragma unroll
-          for (int hh = 0; hh < G; ++hh) {
-            const ulonglong2 qa = *reinterpret_cast<const ulonglong2*>(&sm.q[hh][half][cc][0]);
-            const ulonglong2 qb = *reinterpret_cast<const ulonglong2*>(&sm.q[hh][half][cc][4]);
-            s2[hh] = tc::fma2(k2[0], qa.x, s2[hh]);
-            s2[hh] = tc::fma2(k2[1], qa.y, s2[hh]);
-            s2[hh] = tc::fma2(k2[2], qb.x, s2[hh]);
-            s2[hh] = tc::fma2(k2[3], qb.y, s2[hh]);
+          for (int nt = 0; nt < kDecD / 8; ++nt) {
+            o[nt][0] *= alpha;
+            o[nt][1] *= alpha;
           }
+          if (up) m_ref = mx;
         }
-        const bool valid = key >= lo && key < hi;
+        float pv[4];
 #pragma unroll
-        for (int hh = 0; hh < G; ++hh) {
-          float se, so;
-          tc::f2unpack(s2[hh], se, so);
-          float sv = se + so;
-          sv += __shfl_xor_sync(0xffffffffu, sv, 16);
-          sv = valid ? sv * scale_log2 : -INFINITY;
-          float mx = sv;
+        for (int x = 0; x < 4; ++x) pv[x] = row ? tc::ex2(sc[x] - m_ref) : 0.f;
+        lsum += (pv[0] + pv[1]) + (pv[2] + pv[3]);
+        const uint32_t pa = pack_bf16x2(pv[0], pv[1]), pc = pack_bf16x2(pv[2], pv[3]);
+        // slots outside [lo, hi) may hold anything (NaN): zero them in V so that
+        // 0 * V stays 0 (rare: seam pages only)
+        if (lo > 0 || hi < PIC_PAGE) {
+          uint4* vz = reinterpret_cast<uint4*>(sm.ring[st][1]);
 #pragma unroll
-          for (int x = 1; x < 16; x <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
-          const float mn = fmaxf(m[hh], mx);  // finite: the page has a valid key
-          const float alpha = tc::ex2(m[hh] - mn);
-          const float pv = valid ? tc::ex2(sv - mn) : 0.f;
-          lsum[hh] = lsum[hh] * alpha + (half ? 0.f : pv);
-          m[hh] = mn;
-          const uint64_t a2 = tc::f2pack(alpha, alpha), z2 = 0;
-          o01[hh] = tc::fma2(o01[hh], a2, z2);
-          o23[hh] = tc::fma2(o23[hh], a2, z2);
-          if (half == 0) sm.p[warp][hh][key] = pv;
-        }
-        __syncwarp();
-#pragma unroll
-        for (int k4 = 0; k4 < PIC_PAGE / 4; ++k4) {
-          float4 w4[G];
-#pragma unroll
-          for (int hh = 0; hh < G; ++hh) w4[hh] = *reinterpret_cast<const float4*>(&sm.p[warp][hh][4 * k4]);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const int k2 = 4 * k4 + j;
-            if (k2 < lo || k2 >= hi) continue;  // masked slots may hold anything
-            const uint2 vv = *reinterpret_cast<const uint2*>(vpage + k2 * (2 * kDecD) + 8 * lane);
-            const uint64_t v01 = bf16x2_to_f32x2(vv.x), v23 = bf16x2_to_f32x2(vv.y);
-#pragma unroll
-            for (int hh = 0; hh < G; ++hh) {
-              const float w = j == 0 ? w4[hh].x : j == 1 ? w4[hh].y : j == 2 ? w4[hh].z : w4[hh].w;
-              const uint64_t w2 = tc::f2pack(w, w);
-              o01[hh] = tc::fma2(w2, v01, o01[hh]);
-              o23[hh] = tc::fma2(w2, v23, o23[hh]);
-            }
+          for (int x = 0; x < PIC_PAGE * 2 * 8 / 32; ++x) {  // 16 rows x 2 halves x 8 chunks
+            const int c = x * 32 + lane, key = c >> 4;
+            if (key < lo || key >= hi) vz[((key >> 3) * 2048 + ((c >> 3) & 1) * 1024 + (key & 7) * 128) / 16 + (c & 7)] =
+                make_uint4(0, 0, 0, 0);
           }
+          __syncwarp();
         }
+        // O += P V: matrices (keys 0-7 | 8-15) x columns 8nt.. for nt = 2np, 2np + 1, transposed
+#pragma unroll
+        for (int np = 0; np < kDecD / 16; ++np) {
+          uint32_t b[4];
+          ldsm_x4_trans(b, vbase + swz_off(8 * (mi & 1) + mr, 2 * np + (mi >> 1)));
+          mma_rows8(o[2 * np][0], o[2 * np][1], pa, pc, b[0], b[1]);
+          mma_rows8(o[2 * np + 1][0], o[2 * np + 1][1], pa, pc, b[2], b[3]);
+        }
+        if (lo > 0 || hi < PIC_PAGE) tc::fence_proxy_async_smem();  // generic writes before the next TMA fill
       }
-      __syncwarp();  // the weights are read before the next page writes them
+      __syncwarp();  // the stage is read before it is released
       if (lane == 0) tc::mbar_arrive(&sm.empty[st]);  // the stage may be refilled
     }
-    // row sums over the lanes; partials kept until the ring is free
-#pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-#pragma unroll
-      for (int x = 1; x < 32; x <<= 1) lsum[hh] += __shfl_xor_sync(0xffffffffu, lsum[hh], x);
-      if (lane == 0) {
-        sm.w_m[warp][hh] = m[hh];
-        sm.w_l[warp][hh] = lsum[hh];
-      }
+    // row sums over the quad; partials kept until the ring is free
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 1);
+    lsum += __shfl_xor_sync(0xffffffffu, lsum, 2);
+    if (row && t == 0) {
+      sm.w_m[warp][g] = m_ref;
+      sm.w_l[warp][g] = lsum;
     }
     ring_drained_sync();  // no copy in flight and no consumer reading: the ring takes the partials
+    if (row) {
 #pragma unroll
-    for (int hh = 0; hh < G; ++hh) {
-      float a0, a1, a2v, a3;
-      tc::f2unpack(o01[hh], a0, a1);
-      tc::f2unpack(o23[hh], a2v, a3);
-      *reinterpret_cast<float4*>(&sm.w_o[warp][hh][4 * lane]) = make_float4(a0, a1, a2v, a3);
+      for (int nt = 0; nt < kDecD / 8; ++nt)
+        *reinterpret_cast<float2*>(&sm.w_o[warp][row ? g : 0][8 * nt + 2 * t]) = make_float2(o[nt][0], o[nt][1]);
     }
   }
   __syncthreads();
@@ -448,20 +492,22 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
   const int slots = (int)(L.ctas - (int64_t)n_req * Hkv);
   decode_plan_kernel<<<1, 1024, 0, s>>>(page_off, n_req, Hkv, slots, first, nsplit);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
+  if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
+  CUtensorMap kmap, vmap;
+  if (!encode_pages(&kmap, k_pool, pool_rows) || !encode_pages(&vmap, v_pool, pool_rows)) return PIC_ERR_CUDA;
   const unsigned grid = (unsigned)L.ctas;
   const float sl2 = scale * 1.4426950408889634f;
   const bf16* qb = static_cast<const bf16*>(q);
   const float4* qt = reinterpret_cast<const float4*>(q_table);
-  const bf16* kb = static_cast<const bf16*>(k_pool);
-  const bf16* vb = static_cast<const bf16*>(v_pool);
   switch (Hq / Hkv) {
-    case 1: decode_kernel<1><<<grid, kDecThreads, sizeof(DecSmem<1>), s>>>(qb, qt, kb, vb, num_blocks, pages, page_off,
-        n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
-    case 2: decode_kernel<2><<<grid, kDecThreads, sizeof(DecSmem<2>), s>>>(qb, qt, kb, vb, num_blocks, pages, page_off,
-        n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
-    case 4: decode_kernel<4><<<grid, kDecThreads, sizeof(DecSmem<4>), s>>>(qb, qt, kb, vb, num_blocks, pages, page_off,
-        n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
-    default: decode_kernel<8><<<grid, kDecThreads, sizeof(DecSmem<8>), s>>>(qb, qt, kb, vb, num_blocks, pages,
+    case 1: decode_kernel<1><<<grid, kDecThreads, sizeof(DecSmem<1>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
+        page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
+    case 2: decode_kernel<2><<<grid, kDecThreads, sizeof(DecSmem<2>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
+        page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
+    case 4: decode_kernel<4><<<grid, kDecThreads, sizeof(DecSmem<4>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
+        page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
+    default: decode_kernel<8><<<grid, kDecThreads, sizeof(DecSmem<8>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
         page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
   }
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;

@@ -97,6 +97,13 @@ int num_sms_of_current_device();
 // the driver lacks it).
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
+// Tensor map of a K or V pool viewed as rows of 128 bf16 (one (block, head, slot) key
+// row each): one 4-D box [2 row groups][2 column halves][8 rows][64 columns], 128-byte
+// swizzle, moves a whole 16-row page into shared memory as 4 swizzle atoms of 1 KB
+// (group g, half h at byte g * 2048 + h * 1024; row r's 16-byte chunk c at
+// r * 128 + (c ^ r) * 16).  rows must be a multiple of 8.
+bool encode_pages(CUtensorMap* map, const void* base, uint64_t rows);
+
 // SIMT attention launcher (attention_simt.cu); arguments as pic_link_attention.
 pic_status launch_attention_simt(const void* q, const float* row_table, const int32_t* rows,
                                  const int32_t* row_off, const void* k_pool, const void* v_pool,
