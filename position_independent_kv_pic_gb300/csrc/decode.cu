@@ -35,6 +35,7 @@ constexpr int kDecStages = 8;                    // ring stages of one page (K a
 // w, w + 4, .., so stage i % kDecStages must always belong to warp i % kDecWarps.
 static_assert(kDecStages % kDecWarps == 0, "each stage belongs to one consumer warp");
 constexpr int kPageHead = PIC_PAGE * kDecD * 2;  // bytes of one page of one KV head
+constexpr int kPlanThreads = 1024;  // the planner's one block
 constexpr int kMergeGroups = 8;   // thread groups of the merge, each over every 8th split
 constexpr uint64_t kDecWaitNs = 2000000000ull;
 
@@ -42,7 +43,7 @@ size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 struct DecLayout {
   int64_t ctas;  // upper bound of the decode grid
-  size_t off_plan, off_ml, off_o, total;
+  size_t off_plan, off_desc, off_ml, off_o, total;
 };
 
 // ctas_per_sm: decode CTAs one SM holds at once.  The planner gives request r
@@ -54,16 +55,17 @@ DecLayout dec_layout(int n_req, int Hq, int Hkv, int sms, int ctas_per_sm) {
   L.ctas = (int64_t)ctas_per_sm * sms + (int64_t)n_req * Hkv;
   const int G = Hq / Hkv;
   L.off_plan = 0;  // int32 [n_req + 1] first CTA of each request, int32 [n_req] splits, int32 span
-  L.off_ml = al256((size_t)(2 * n_req + 2) * sizeof(int32_t));
+  L.off_desc = al256((size_t)(2 * n_req + 2) * sizeof(int32_t));  // int4 [ctas] (request, KV head, pages)
+  L.off_ml = al256(L.off_desc + (size_t)L.ctas * sizeof(int4));
   L.off_o = al256(L.off_ml + (size_t)L.ctas * G * sizeof(float2));
   L.total = al256(L.off_o + (size_t)L.ctas * G * kDecD * sizeof(float));
   return L;
 }
 
 // One block: splits per request and the first CTA of each request.
-__global__ void __launch_bounds__(1024)
-decode_plan_kernel(const int32_t* __restrict__ page_off, int n_req, int Hkv, int slots, int32_t* __restrict__ first,
-                   int32_t* __restrict__ nsplit) {
+__global__ void __launch_bounds__(kPlanThreads)
+decode_plan_kernel(const int32_t* __restrict__ page_off, int n_req, int Hkv, int slots, int ctas,
+                   int32_t* __restrict__ first, int32_t* __restrict__ nsplit, int4* __restrict__ desc) {
   __shared__ int scratch[1024 / 32 + 1];
   __shared__ int s_span;
   const int tid = threadIdx.x;
@@ -90,6 +92,25 @@ decode_plan_kernel(const int32_t* __restrict__ page_off, int n_req, int Hkv, int
     carry += tot;
   }
   if (tid == 0) first[n_req] = carry;
+  __syncthreads();
+  // one descriptor per CTA of the grid, so that a CTA starts from a single load:
+  // (request, KV head, first page, end page), request -1 past the last CTA
+  for (int c = tid; c < ctas; c += kPlanThreads) {
+    int4 d = make_int4(-1, 0, 0, 0);
+    if (c < carry) {
+      int lo = 0, hi = n_req;  // the last r with first[r] <= c
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (first[mid] <= c) lo = mid; else hi = mid;
+      }
+      const int splits = nsplit[lo], kvh = (c - first[lo]) / splits, split = (c - first[lo]) % splits;
+      const int p0 = page_off[lo], p1 = page_off[lo + 1];
+      const int per = (p1 - p0 + splits - 1) / splits;
+      const int pb = min(p1, p0 + split * per);
+      d = make_int4(lo, kvh, pb, min(p1, pb + per));
+    }
+    desc[c] = d;
+  }
 }
 
 // Warp-level bf16 MMA m16n8k16 with fp32 accumulate, rows 8..15 of A zero: d0, d1
@@ -160,8 +181,8 @@ __global__ void __launch_bounds__(kDecThreads, 3)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const bf16* __restrict__ q, const float4* __restrict__ q_table, int64_t num_blocks,
               const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off, int n_req, int Hq,
-              int Hkv, float scale_log2, const int32_t* __restrict__ first, const int32_t* __restrict__ nsplit,
-              float2* __restrict__ part_ml, float* __restrict__ part_o, int32_t* err) {
+              int Hkv, float scale_log2, const int4* __restrict__ desc, float2* __restrict__ part_ml,
+              float* __restrict__ part_o, int32_t* err) {
   static_assert(G <= 8, "heads of a KV head: rows 0..7 of the MMA operand");
   extern __shared__ __align__(1024) uint8_t dec_smem_raw[];
   // the swizzled stages need 1024-byte alignment
@@ -171,18 +192,9 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   }
   DecSmem<G>& sm = *reinterpret_cast<DecSmem<G>*>(dec_smem_raw);
   const int cta = blockIdx.x;
-  if (cta >= first[n_req]) return;  // the grid is an upper bound
-  int r;
-  {  // request of this CTA: the last r with first[r] <= cta
-    int lo = 0, hi = n_req;
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (first[mid] <= cta) lo = mid; else hi = mid;
-    }
-    r = lo;
-  }
-  const int splits = nsplit[r];
-  const int kvh = (cta - first[r]) / splits, split = (cta - first[r]) % splits;
+  const int4 dsc = desc[cta];  // (request, KV head, first page, end page)
+  if (dsc.x < 0) return;       // the grid is an upper bound
+  const int r = dsc.x, kvh = dsc.y, pb = dsc.z, n = max(dsc.w - dsc.z, 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int st = 0; st < kDecStages; ++st) {
@@ -192,22 +204,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     sm.abort = 0;
     tc::fence_mbar_init();
   }
-  // Q of the g heads roped at the row's position and rounded to bf16, as on the
-  // link path's tensor-core operand
-  for (int it = tid; it < G * kDecD / 2; it += kDecThreads) {
-    const int hh = it / (kDecD / 2), i = it % (kDecD / 2);
-    const bf16* src = q + ((int64_t)r * Hq + kvh * G + hh) * kDecD;
-    float ya, yb;
-    rope_rotate_bf16in(to_f32(src[i]), to_f32(src[i + kDecD / 2]), q_table[(int64_t)r * (kDecD / 2) + i], ya, yb);
-    sm.qb[hh][i] = from_f32<bf16>(ya);
-    sm.qb[hh][i + kDecD / 2] = from_f32<bf16>(yb);
-  }
   __syncthreads();
-
-  const int p0 = page_off[r], p1 = page_off[r + 1];
-  const int per = (p1 - p0 + splits - 1) / splits;
-  const int pb = p0 + split * per, pe = min(p1, pb + per);
-  const int n = max(pe - pb, 0);
 
   if (warp == kDecWarps) {
     // ---- producer: lane 0 streams the span's pages through the ring, reading each
@@ -249,6 +246,17 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     __syncwarp();
     ring_drained_sync();
   } else {
+    // Q of the g heads roped at the row's position and rounded to bf16, as on the
+    // link path's tensor-core operand; meanwhile the producer has started the copies
+    for (int it = tid; it < G * kDecD / 2; it += 32 * kDecWarps) {
+      const int hh = it / (kDecD / 2), i = it % (kDecD / 2);
+      const bf16* src = q + ((int64_t)r * Hq + kvh * G + hh) * kDecD;
+      float ya, yb;
+      rope_rotate_bf16in(to_f32(src[i]), to_f32(src[i + kDecD / 2]), q_table[(int64_t)r * (kDecD / 2) + i], ya, yb);
+      sm.qb[hh][i] = from_f32<bf16>(ya);
+      sm.qb[hh][i + kDecD / 2] = from_f32<bf16>(yb);
+    }
+    asm volatile("bar.sync 2, %0;" ::"n"(32 * kDecWarps) : "memory");  // the consumer warps only
     // ---- consumers: warp w takes pages w, w + 4, ..  Lane (g, t) = (lane / 4,
     // lane % 4) holds row g (head g of the KV head; rows >= G are padding) of the
     // MMA fragments: Q at columns 16 ks + 2t, +1 and +8, +9; S at keys 2t, 2t+1 and
@@ -486,11 +494,12 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
   uint8_t* w = static_cast<uint8_t*>(ws);
   int32_t* first = reinterpret_cast<int32_t*>(w + L.off_plan);
   int32_t* nsplit = first + (n_req + 1);
+  int4* desc = reinterpret_cast<int4*>(w + L.off_desc);
   float2* part_ml = reinterpret_cast<float2*>(w + L.off_ml);
   float* part_o = reinterpret_cast<float*>(w + L.off_o);
   cudaStream_t s = (cudaStream_t)stream;
   const int slots = (int)(L.ctas - (int64_t)n_req * Hkv);
-  decode_plan_kernel<<<1, 1024, 0, s>>>(page_off, n_req, Hkv, slots, first, nsplit);
+  decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(page_off, n_req, Hkv, slots, (int)L.ctas, first, nsplit, desc);
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
   if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
@@ -502,13 +511,13 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
   const float4* qt = reinterpret_cast<const float4*>(q_table);
   switch (Hq / Hkv) {
     case 1: decode_kernel<1><<<grid, kDecThreads, sizeof(DecSmem<1>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
     case 2: decode_kernel<2><<<grid, kDecThreads, sizeof(DecSmem<2>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
     case 4: decode_kernel<4><<<grid, kDecThreads, sizeof(DecSmem<4>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
     default: decode_kernel<8><<<grid, kDecThreads, sizeof(DecSmem<8>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
   }
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   decode_merge_kernel<<<dim3((unsigned)Hq, (unsigned)n_req), 32 * kMergeGroups, 0, s>>>(
