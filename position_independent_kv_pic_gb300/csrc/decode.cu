@@ -395,18 +395,32 @@ decode_merge_kernel(const float2* __restrict__ part_ml, const float* __restrict_
   const int G = Hq / Hkv, kvh = h / G, hh = h % G;
   const int splits = nsplit[r];
   const int64_t base = first[r] + (int64_t)kvh * splits;  // partials are indexed by CTA
-  float M = -INFINITY;
-  for (int s = g; s < splits; s += kMergeGroups) M = fmaxf(M, part_ml[(base + s) * G + hh].x);
-  float Lsum = 0.f;
+  // one pass with a running maximum, four splits' loads in flight at a time
+  float M = -INFINITY, Lsum = 0.f;
   float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int s = g; s < splits; s += kMergeGroups) {
-    const float2 ml = part_ml[(base + s) * G + hh];
-    const float4 v = reinterpret_cast<const float4*>(part_o + ((base + s) * G + hh) * kDecD)[c];
-    if (ml.x == -INFINITY) continue;  // a split without keys
-    const float f = tc::ex2(ml.x - M);
-    Lsum += f * ml.y;
-    O.x = fmaf(f, v.x, O.x); O.y = fmaf(f, v.y, O.y); O.z = fmaf(f, v.z, O.z); O.w = fmaf(f, v.w, O.w);
+  for (int s0 = g; s0 < splits; s0 += 4 * kMergeGroups) {
+    float2 ml[4];
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int sp = s0 + k * kMergeGroups;
+      ml[k] = make_float2(-INFINITY, 0.f);
+      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (sp < splits) {
+        ml[k] = part_ml[(base + sp) * G + hh];
+        v[k] = reinterpret_cast<const float4*>(part_o + ((base + sp) * G + hh) * kDecD)[c];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (ml[k].x == -INFINITY) continue;  // a split without keys
+      const float Mn = fmaxf(M, ml[k].x);
+      const float a = tc::ex2(M - Mn), f = tc::ex2(ml[k].x - Mn);  // a = 0 while M = -inf
+      Lsum = fmaf(Lsum, a, f * ml[k].y);
+      O.x = fmaf(O.x, a, f * v[k].x); O.y = fmaf(O.y, a, f * v[k].y);
+      O.z = fmaf(O.z, a, f * v[k].z); O.w = fmaf(O.w, a, f * v[k].w);
+      M = Mn;
+    }
   }
   if (c == 0) {
     g_m[g] = M;
