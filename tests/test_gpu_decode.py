@@ -102,3 +102,24 @@ def test_link_attention_on_decode_rows_repeated():
     assert b.error() == 0, pic.pic_strerror(b.error())
     assert all(torch.equal(o, outs[0]) for o in outs)
     assert (outs[0].float() - b.dec_out.float()).abs().max().item() <= 2e-3
+
+
+def test_decode_bad_block_is_flagged_and_skipped():
+    """A page whose V block id is past the pool is reported (PIC_ERR_RANGE) and not
+    read; the call still ends (no wait runs out) and the other heads' pages are
+    untouched by it."""
+    wl = inputs.custom([[40, 50, 60]], [3], [4], Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=97)
+    b = _decode(wl)
+    bad = b.dec_pages.clone()
+    bad[1, 1] = b.num_blocks + 7
+    good = b.dec_pages
+    b.dec_pages = bad
+    b.run_decode()
+    torch.cuda.synchronize()
+    assert b.error() == pic.PIC_ERR_RANGE
+    assert torch.isfinite(b.dec_out.float()).all()
+    b.dec_pages = good
+    b.err.zero_()
+    b.run_decode()
+    torch.cuda.synchronize()
+    assert b.error() == 0
