@@ -742,15 +742,26 @@ __device__ __forceinline__ void rotate_k_tile(uint8_t* ksm, int tab_lane, const 
       rc.tab = tab;
     }
     uint8_t* pg = ksm + jj * kPageBytes + hh * 8;
+    // all four rows loaded before any is stored: the stores could alias later loads
+    // as far as the compiler knows, which would otherwise serialise the rows
+    uint8_t* pr[4];
+    uint2 l[4], h[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = rq + 4 * i;
-      uint8_t* p = pg + (r >> 3) * kGroupBytes + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-      uint2 l = *reinterpret_cast<const uint2*>(p), h = *reinterpret_cast<const uint2*>(p + kPageHalfBytes);
-      rotate_word2(l.x, h.x, rc.p0);
-      rotate_word2(l.y, h.y, rc.p1);
-      *reinterpret_cast<uint2*>(p) = l;
-      *reinterpret_cast<uint2*>(p + kPageHalfBytes) = h;
+      pr[i] = pg + (r >> 3) * kGroupBytes + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
+      l[i] = *reinterpret_cast<const uint2*>(pr[i]);
+      h[i] = *reinterpret_cast<const uint2*>(pr[i] + kPageHalfBytes);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      rotate_word2(l[i].x, h[i].x, rc.p0);
+      rotate_word2(l[i].y, h[i].y, rc.p1);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      *reinterpret_cast<uint2*>(pr[i]) = l[i];
+      *reinterpret_cast<uint2*>(pr[i] + kPageHalfBytes) = h[i];
     }
   }
 }
