@@ -728,7 +728,7 @@ struct RotCache {
   int tab;
   RotPair p0, p1;
 };
-__device__ __forceinline__ void rotate_k_tile(uint8_t* ksm, int tab_lane, const float4* __restrict__ rot_tab,
+__device__ __forceinline__ void rotate_k_tile(uint32_t ksm, int tab_lane, const float4* __restrict__ rot_tab,
                                               int t64, RotCache& rc) {
   const int c = t64 & 7, hh = (t64 >> 3) & 1, rq = t64 >> 4;
 #pragma unroll 1
@@ -741,27 +741,20 @@ __device__ __forceinline__ void rotate_k_tile(uint8_t* ksm, int tab_lane, const 
       rc.p1 = rot_pair(__ldg(cs + 2), __ldg(cs + 3));
       rc.tab = tab;
     }
-    uint8_t* pg = ksm + jj * kPageBytes + hh * 8;
-    // all four rows loaded before any is stored: the stores could alias later loads
-    // as far as the compiler knows, which would otherwise serialise the rows
-    uint8_t* pr[4];
-    uint2 l[4], h[4];
+    // one row at a time, 32-bit shared-memory addresses: the V-zeroing warps run
+    // with 64 registers, and holding more rows in flight spilled to local memory
+    const uint32_t pg = ksm + jj * kPageBytes + hh * 8;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int r = rq + 4 * i;
-      pr[i] = pg + (r >> 3) * kGroupBytes + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-      l[i] = *reinterpret_cast<const uint2*>(pr[i]);
-      h[i] = *reinterpret_cast<const uint2*>(pr[i] + kPageHalfBytes);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      rotate_word2(l[i].x, h[i].x, rc.p0);
-      rotate_word2(l[i].y, h[i].y, rc.p1);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      *reinterpret_cast<uint2*>(pr[i]) = l[i];
-      *reinterpret_cast<uint2*>(pr[i] + kPageHalfBytes) = h[i];
+      const uint32_t pa = pg + (r >> 3) * kGroupBytes + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
+      uint32_t l0, l1, h0, h1;
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(l0), "=r"(l1) : "r"(pa));
+      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(h0), "=r"(h1) : "r"(pa + kPageHalfBytes));
+      rotate_word2(l0, h0, rc.p0);
+      rotate_word2(l1, h1, rc.p1);
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(pa), "r"(l0), "r"(l1) : "memory");
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(pa + kPageHalfBytes), "r"(h0), "r"(h1) : "memory");
     }
   }
 }
@@ -798,7 +791,7 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
         const int ks = ld % kSlots;
         const bool got = wait_bar(b, &b->kv_full[ks], (ld / kSlots) & 1);
         if (!__all_sync(0xffffffffu, got)) { fail(b, a.err); return; }
-        rotate_k_tile(smem + kOffSlot + ks * kOpBytes, tab, a.rot_tab, 32 * wz + lane, rc);
+        rotate_k_tile(tc::smem_addr(smem + kOffSlot + ks * kOpBytes), tab, a.rot_tab, 32 * wz + lane, rc);
         tc::fence_proxy_async_smem();
         __syncwarp();
       }
