@@ -1123,23 +1123,31 @@ merge_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
   const int loc = qt * R + i;
   if (loc >= tm.n_rows) return;
   const int base = tm.part_base + head * tm.n_spans;
-  float M = -INFINITY;
-  for (int s = 0; s < tm.n_spans; ++s) {
-    const float2 ml = part_ml[((int64_t)(base + s) * kQTiles + qt) * kM + t];
-    if (ml.y > 0.f) M = fmaxf(M, ml.x);
-  }
+  // one pass with a running maximum, four spans' loads in flight at a time
+  float M = -INFINITY, den = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float den = 0.f;
-#pragma unroll 4
-  for (int s = 0; s < tm.n_spans; ++s) {
-    const int64_t slot = ((int64_t)(base + s) * kQTiles + qt) * kM + t;
-    const float2 ml = part_ml[slot];
-    const float4 v = reinterpret_cast<const float4*>(part_o + slot * kD)[c];
-    if (ml.y > 0.f) {  // a span without visible keys contributes nothing
-      const float w = ml.y * exp2f(ml.x - M);
-      den += w;
-      acc.x = fmaf(w, v.x, acc.x); acc.y = fmaf(w, v.y, acc.y);
-      acc.z = fmaf(w, v.z, acc.z); acc.w = fmaf(w, v.w, acc.w);
+  for (int s0 = 0; s0 < tm.n_spans; s0 += 4) {
+    float2 ml[4];
+    float4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      ml[k] = make_float2(-INFINITY, 0.f);
+      v[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (s0 + k < tm.n_spans) {
+        const int64_t slot = ((int64_t)(base + s0 + k) * kQTiles + qt) * kM + t;
+        ml[k] = part_ml[slot];
+        v[k] = reinterpret_cast<const float4*>(part_o + slot * kD)[c];
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      if (!(ml[k].y > 0.f)) continue;  // a span without visible keys contributes nothing
+      const float Mn = fmaxf(M, ml[k].x);
+      const float a = exp2f(M - Mn), w = ml[k].y * exp2f(ml[k].x - Mn);  // a = 0 while M = -inf
+      den = fmaf(den, a, w);
+      acc.x = fmaf(acc.x, a, w * v[k].x); acc.y = fmaf(acc.y, a, w * v[k].y);
+      acc.z = fmaf(acc.z, a, w * v[k].z); acc.w = fmaf(acc.w, a, w * v[k].w);
+      M = Mn;
     }
   }
   const float inv = den > 0.f ? 1.f / den : 0.f;
