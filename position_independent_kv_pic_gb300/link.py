@@ -211,19 +211,27 @@ class LinkBatch:
             main = stream
         pic_select_rows(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], dv["row_off"], self.rows,
                         self.chunk_start, self.err, main)
-        pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
-                         dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
-                         dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
-                         self.row_block, self.row_slot, self.err, main, page_tab=self.page_tab)
+        # the side stream forks once the chunk starts exist: the offset table (which
+        # needs only them) runs beside the splice, the pass itself waits for the splice
         pass_stream = main
         if self.scheme in ("rotary", "nope"):
             if self._side is None:
                 self._side = torch.cuda.Stream(self.device)
                 self._ev_fork, self._ev_join = torch.cuda.Event(), torch.cuda.Event()
+                self._ev_spliced = torch.cuda.Event()
             pass_stream = self._side
             self._ev_fork.record(main)
             pass_stream.wait_event(self._ev_fork)
-        if self.scheme in ("rotary", "ror"):
+        if self.scheme == "rotary":
+            pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, pass_stream)
+        pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
+                         dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
+                         dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
+                         self.row_block, self.row_slot, self.err, main, page_tab=self.page_tab)
+        if pass_stream is not main:
+            self._ev_spliced.record(main)
+            pass_stream.wait_event(self._ev_spliced)
+        if self.scheme == "ror":
             pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, pass_stream)
         if "rerotate" in mk:
             mk["rerotate"][0].record(pass_stream)
