@@ -327,7 +327,7 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
  *     overlaps on the GPU (different streams, or host threads without ordering)
  *     race on the array: order them.
  *   - The tensor-core path (bf16, d = 128) splits long key ranges into at most
- *     64 extra work units; a call whose scratch would exceed the array (about
+ *     60 extra work units; a call whose scratch would exceed the array (about
  *     900 recomputed rows of one request at Hq = 32, Hkv = 8; about 700 over 4
  *     requests) is refused with PIC_ERR_WORKSPACE before any other check or
  *     launch.  The SIMT path (fp32 pools, other shapes) needs no scratch.

@@ -44,8 +44,9 @@ constexpr int kSlots = 5;               // K/V ring slots (32 KB each)
 constexpr int kSmWarpgroups = 2 * kQTiles;  // softmax: one warpgroup per (Q tile, half of the key columns)
 constexpr int kThreads = 128 * (1 + kSmWarpgroups);
 constexpr int kMinSpan = 8;             // key tiles per unit, lower bound
-constexpr int kUnitsPerSm = 4;          // target units per SM when splitting
-constexpr int kMaxSplitUnits = 640;     // bound on the units splitting may add
+constexpr int kSpanPref = 16;           // ... and while every SM still gets a unit
+constexpr int kUnitsPerSm = 6;          // target units per SM when splitting
+constexpr int kMaxSplitUnits = 960;     // bound on the units splitting may add
 constexpr int kMaxPlanReqs = 1024;      // requests one planning block handles
 constexpr int kMaxPlanTiles = 1024;     // Q-tile pairs planned from shared memory (more: slower path)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -251,8 +252,13 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
   __syncthreads();
   // (2) span
   const int64_t work = (int64_t)s_total_kt * Hkv;
+  // about six units per SM balance the long calls (measured: 4 or 5 left SMs idle
+  // at the end of the long-context call, 7 or 8 paid more unit overhead); a short
+  // call keeps spans of at least 16 tiles as long as every SM still gets a unit,
+  // since each unit pays a Q load and a pipeline fill
   const int64_t target = min((int64_t)kUnitsPerSm * num_sms, (int64_t)kMaxSplitUnits);
-  const int span = (int)max((int64_t)kMinSpan, (work + target - 1) / target);
+  const int64_t span_fill = min((int64_t)kSpanPref, (work + num_sms - 1) / num_sms);
+  const int span = (int)max((int64_t)kMinSpan, max((work + target - 1) / target, span_fill));
   for (int t = tid; t < n_tiles; t += kPlanThreads) {
     TileMeta& tm = tiles[t];
     tm.n_spans = ceil_div(tm.n_kt, span);
@@ -1262,7 +1268,7 @@ bool tc_shape(pic_dtype dt, int Hq, int Hkv, int d) {
 
 // The two phases of a tensor-core attention call, with the scratch laid out by L
 // in `ws`: the plan (unit list, Q operands — reads no K or V) and the run
-// (attention, merge).  The planner may add up to 4 * split_sms units by splitting
+// (attention, merge).  The planner may add up to 6 * split_sms units by splitting
 // key ranges.
 enum { kPhasePlan = 1, kPhaseRun = 2, kPhaseAll = 3 };
 
@@ -1509,7 +1515,7 @@ static __device__ __align__(256) uint8_t pic_fixed_scratch[kFixedScratchBytes];
 namespace pic {
 namespace {
 
-constexpr int kFixedSplitSms = 16;
+constexpr int kFixedSplitSms = 10;  // at most kUnitsPerSm * 10 = 60 split units in the fixed scratch
 constexpr int kMaxDevices = 256;
 
 std::mutex g_fixed_mu;
