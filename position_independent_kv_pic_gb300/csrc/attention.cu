@@ -47,6 +47,8 @@ constexpr int kMinSpan = 8;             // key tiles per unit, lower bound
 constexpr int kSpanPref = 16;           // ... and while every SM still gets a unit
 constexpr int kUnitsPerSm = 6;          // target units per SM when splitting
 constexpr int kMaxSplitUnits = 960;     // bound on the units splitting may add
+constexpr int kTailDiv = 3;             // a call with few (tile pair, head) items cuts its tails in 3
+constexpr int kTailExtra = 640;         // room for those extra tail pieces (2 per item, < 2 * 160 items)
 constexpr int kMaxPlanReqs = 1024;      // requests one planning block handles
 constexpr int kMaxPlanTiles = 1024;     // Q-tile pairs planned from shared memory (more: slower path)
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -96,18 +98,21 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header size");
 
 struct WsLayout {
-  int64_t tiles_cap, units_cap;
+  int64_t tiles_cap, units_cap, tail_extra;
   size_t off_tiles, off_units, off_ml, off_o, off_q, total;
 };
 
 size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace for up to `extra_units` units beyond one per (Q-tile pair, KV head).
-WsLayout ws_layout_with(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d, int64_t extra_units) {
+// Workspace for up to `extra_units` units beyond one per (Q-tile pair, KV head), and
+// `tail_extra` more for tails cut into pieces.
+WsLayout ws_layout_with(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d, int64_t extra_units,
+                        int64_t tail_extra) {
   WsLayout L;
   const int R2 = kQTiles * (kM / G);
   L.tiles_cap = n_rows / R2 + n_req + 1;
-  L.units_cap = L.tiles_cap * Hkv + extra_units;
+  L.units_cap = L.tiles_cap * Hkv + extra_units + tail_extra;
+  L.tail_extra = tail_extra;
   L.off_tiles = sizeof(WsHeader);
   L.off_units = al256(L.off_tiles + L.tiles_cap * sizeof(TileMeta));
   L.off_ml = al256(L.off_units + L.units_cap * sizeof(Unit));
@@ -119,7 +124,7 @@ WsLayout ws_layout_with(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, i
 }
 
 WsLayout ws_layout(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d) {
-  return ws_layout_with(n_rows, n_req, G, Hkv, d, kMaxSplitUnits);
+  return ws_layout_with(n_rows, n_req, G, Hkv, d, kMaxSplitUnits, kTailExtra);
 }
 
 __device__ __forceinline__ bool page_ok(int4 p, int64_t num_blocks) {
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ row_off,
                   const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off,
                   int n_req, int R2, int Hkv, int num_sms, int64_t tiles_cap, int64_t units_cap,
-                  WsHeader* hdr, TileMeta* tiles, Unit* units, int32_t* err) {
+                  int64_t tail_extra, WsHeader* hdr, TileMeta* tiles, Unit* units, int32_t* err) {
   __shared__ int s_toff[kMaxPlanReqs + 1];   // first tile of each request
   __shared__ int s_full[kMaxPlanReqs];       // full spans of one head of each request
   __shared__ int s_fbase[kMaxPlanReqs + 1];  // first full unit of each request
@@ -191,8 +196,12 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     const int r = lo;
     TileMeta tm;
     tm.req = r;
-    tm.row0 = row_off[r] + (t - s_toff[r]) * R2;
-    tm.n_rows = min(R2, row_off[r + 1] - tm.row0);
+    // the request's rows in tiles of R2, the partial tile (if any) first: its rows
+    // have the smallest positions, so a half-empty tile pair (one Q tile, the MMA
+    // ping-pong idle) spans the fewest key tiles
+    const int nr = row_off[r + 1] - row_off[r], rem = nr % R2, k = t - s_toff[r];
+    tm.row0 = row_off[r] + (rem > 0 ? (k == 0 ? 0 : rem + (k - 1) * R2) : k * R2);
+    tm.n_rows = (rem > 0 && k == 0) ? rem : R2;
     const int maxpos = rows[tm.row0 + tm.n_rows - 1];
     tm.page_begin = page_off[r];
     tm.n_pages = 0;
@@ -259,13 +268,20 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
   const int64_t target = min((int64_t)kUnitsPerSm * num_sms, (int64_t)kMaxSplitUnits);
   const int64_t span_fill = min((int64_t)kSpanPref, (work + num_sms - 1) / num_sms);
   const int span = (int)max((int64_t)kMinSpan, max((work + target - 1) / target, span_fill));
+  // With few (tile pair, head) items the tails are few and long, and the SMs that
+  // draw the last of them finish late: cut each tail into pieces of about a third
+  // of a span (long-context call 914 -> 891 us).  Many items already end on many
+  // short tails, and more units only add overhead there (16-request batch: slower).
+  const int items = n_tiles * Hkv;
+  const bool cut = items < 2 * num_sms && (int64_t)(kTailDiv - 1) * items <= tail_extra;
+  const int ts = cut ? max(kMinSpan, ceil_div(span, kTailDiv)) : span;  // tail pieces
   for (int t = tid; t < n_tiles; t += kPlanThreads) {
     TileMeta& tm = tiles[t];
-    tm.n_spans = ceil_div(tm.n_kt, span);
+    const int len = tm.n_kt % span;
+    tm.n_spans = tm.n_kt / span + ceil_div(len, ts);
     if (tm.n_spans > 1) tm.part_base = atomicAdd(&s_part, tm.n_spans * Hkv);
     atomicAdd(&s_full[tm.req], tm.n_kt / span);
-    const int len = tm.n_kt % span;
-    if (len > 0) atomicAdd(&s_hist[min(len, kHist - 1)], Hkv);
+    for (int o = 0; o < len; o += ts) atomicAdd(&s_hist[min(min(ts, len - o), kHist - 1)], Hkv);
   }
   __syncthreads();
   // (3) first full unit of every request; tail buckets after all full units, longest first
@@ -319,11 +335,12 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
       units[idx] = un;
     }
     const int len = tm.n_kt % span;
-    if (len > 0) {
-      const int idx = atomicAdd(&s_hist[min(len, kHist - 1)], 1);
+    for (int o = 0, j = 0; o < len; o += ts, ++j) {  // the tail, in pieces of at most ts tiles
+      const int pl = min(ts, len - o);
+      const int idx = atomicAdd(&s_hist[min(pl, kHist - 1)], 1);
       Unit un;
-      un.tile = t; un.head = h; un.kt0 = f * span; un.kt1 = tm.n_kt;
-      un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + f : -1;
+      un.tile = t; un.head = h; un.kt0 = f * span + o; un.kt1 = f * span + o + pl;
+      un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + f + j : -1;
       un.pad0 = un.pad1 = un.pad2 = 0;
       units[idx] = un;
     }
@@ -1302,8 +1319,8 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   uint8_t* q_tiles = w + L.off_q;
   if (phases & kPhasePlan) {
     plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kQTiles * R, Hkv,
-                                                  split_sms < sms ? split_sms : sms, L.tiles_cap, L.units_cap, hdr,
-                                                  tiles, units, err_flag);
+                                                  split_sms < sms ? split_sms : sms, L.tiles_cap, L.units_cap,
+                                                  L.tail_extra, hdr, tiles, units, err_flag);
     if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
     qprep_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), 4), kQTiles * kM, 0, s>>>(
         hdr, tiles, static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), q_tiles, Hq, Hkv, G,
@@ -1537,7 +1554,7 @@ void* fixed_scratch_address() {
 }
 
 WsLayout fixed_layout(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d) {
-  return ws_layout_with(n_rows, n_req, G, Hkv, d, (int64_t)kUnitsPerSm * kFixedSplitSms);
+  return ws_layout_with(n_rows, n_req, G, Hkv, d, (int64_t)kUnitsPerSm * kFixedSplitSms, 0);
 }
 
 }  // namespace
