@@ -40,8 +40,8 @@ UNIT = "tokens/s"
 # two-launch composition), with the kernel source they were taken from; reported
 # as roofline traffic only while the source is unchanged.
 NCU_TRAFFIC = {
-    # link_attn_tc_kernel<0>, long_context_100x1000: 690.84 MB read + 108.44 MB written
-    ("attention", "3b3bf6dff2f38f24"): 799277056,
+    # link_attn_tc_kernel<0>, long_context_100x1000: 662.60 MB read + 130.66 MB written
+    ("attention", "25ad24902e9e1252"): 793256192,
     # rerotate_kernel<bf16>, long_context_100x1000: 201.35 MB read + 140.40 MB written
     ("rerotate", "94fbac229e1fc877"): 341751552,
     # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.40 MB written
