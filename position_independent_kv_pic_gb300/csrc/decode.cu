@@ -123,6 +123,7 @@ __device__ __forceinline__ void mma_rows8(float& d0, float& d1, uint32_t a0, uin
       "{%10,%11,%12,%13};"
       : "=f"(d0), "=f"(d1), "=f"(z0), "=f"(z1)
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(d0), "f"(d1), "f"(0.f), "f"(0.f));
+  asm volatile("" ::"f"(z0), "f"(z1));  // the zero rows' outputs: read by nothing
 }
 
 // Four 8x8 bf16 matrices from shared memory; lane l gives the address of row l % 8
