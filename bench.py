@@ -47,7 +47,8 @@ NCU_TRAFFIC = {
     # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.40 MB written
     ("scheme_b", "94fbac229e1fc877"): 449222144,
     # decode_kernel<4>, one row per request over the long-context link: 420.64 MB read + 4.42 MB written
-    ("decode", "b89d1f8d8b71f27a"): 425063168,
+    # (captured before an empty asm that only consumes the MMA's discarded outputs)
+    ("decode", "055e5c15b721b166"): 425063168,
     # compose_kernel, 32 heads x 100-chunk chain, both levels: 417.43 + 14.75 MB read + 3.52 MB written
     ("compose", "e43e88d53b50babb"): 435703296,
 }
