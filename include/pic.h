@@ -409,8 +409,10 @@ pic_status pic_link_attention_ror(const void* q, const float* row_table, const i
  * bf16 pools with d = 128 and g = Hq / Hkv in {1, 2, 4, 8}; otherwise
  * PIC_ERR_UNSUPPORTED (0 from pic_decode_workspace).  Three launches: a one-block
  * planner gives every request splits in proportion to its pages so that all
- * CTAs fit in one wave, the split-KV decode (pages streamed through shared
- * memory by bulk copies), and the merge of the splits.  Bound by HBM: every
+ * CTAs fit in one wave (and writes each CTA's request, KV head and page range),
+ * the split-KV decode (pages moved into shared memory by TMA, each page's two
+ * small contractions on warp-level bf16 MMAs with fp32 accumulate, P rounded to
+ * bf16 as on the link path), and the merge of the splits.  Bound by HBM: every
  * listed K and V row is read once.  A bad block id or slot range sets
  * PIC_ERR_RANGE in *err_flag and that page is skipped; a bounded wait that runs
  * out sets PIC_ERR_TIMEOUT. */
