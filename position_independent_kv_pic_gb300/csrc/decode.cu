@@ -182,8 +182,9 @@ __global__ void __launch_bounds__(kDecThreads, 3)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const bf16* __restrict__ q, const float4* __restrict__ q_table, int64_t num_blocks,
               const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off, int n_req, int Hq,
-              int Hkv, float scale_log2, const int4* __restrict__ desc, float2* __restrict__ part_ml,
-              float* __restrict__ part_o, int32_t* err) {
+              int Hkv, float scale_log2, const int4* __restrict__ desc, int slots, int32_t* __restrict__ first,
+              int32_t* __restrict__ nsplit, float2* __restrict__ part_ml, float* __restrict__ part_o,
+              int32_t* err) {
   static_assert(G <= 8, "heads of a KV head: rows 0..7 of the MMA operand");
   extern __shared__ __align__(1024) uint8_t dec_smem_raw[];
   // the swizzled stages need 1024-byte alignment
@@ -193,10 +194,40 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
   }
   DecSmem<G>& sm = *reinterpret_cast<DecSmem<G>*>(dec_smem_raw);
   const int cta = blockIdx.x;
-  const int4 dsc = desc[cta];  // (request, KV head, first page, end page)
-  if (dsc.x < 0) return;       // the grid is an upper bound
-  const int r = dsc.x, kvh = dsc.y, pb = dsc.z, n = max(dsc.w - dsc.z, 0);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // (request, KV head, first page, end page) of this CTA: with few requests every
+  // CTA takes the planner's split itself (one launch less; CTA 0 writes the split
+  // counts the merge reads), else it reads the planner's descriptor
+  int4 dsc;
+  if (n_req <= kDecThreads) {
+    __shared__ int s_scan[kDecThreads / 32 + 1];
+    __shared__ int4 s_desc;
+    const int64_t W = (int64_t)Hkv * __ldg(page_off + n_req);
+    const int64_t room = (int64_t)slots - (int64_t)n_req * Hkv;
+    const int span = (int)max((int64_t)1, room > 0 ? (W + room - 1) / room : W);
+    const int p0r = tid < n_req ? __ldg(page_off + tid) : 0;
+    const int np = tid < n_req ? __ldg(page_off + tid + 1) - p0r : 0;
+    const int sr = tid < n_req ? max(1, (np + span - 1) / span) : 0;
+    int total;
+    const int ex = block_exclusive_scan<kDecThreads>(sr * Hkv, s_scan, &total);
+    if (cta == 0 && tid < n_req) {
+      first[tid] = ex;
+      nsplit[tid] = sr;
+    }
+    if (cta == 0 && tid == 0) first[n_req] = total;
+    if (tid == 0 && cta >= total) s_desc = make_int4(-1, 0, 0, 0);
+    if (tid < n_req && cta >= ex && cta < ex + sr * Hkv) {
+      const int split = (cta - ex) % sr, per = (np + sr - 1) / sr;
+      const int pb0 = min(p0r + np, p0r + split * per);
+      s_desc = make_int4(tid, (cta - ex) / sr, pb0, min(p0r + np, pb0 + per));
+    }
+    __syncthreads();
+    dsc = s_desc;
+  } else {
+    dsc = desc[cta];
+  }
+  if (dsc.x < 0) return;  // the grid is an upper bound
+  const int r = dsc.x, kvh = dsc.y, pb = dsc.z, n = max(dsc.w - dsc.z, 0);
   if (tid == 0) {
     for (int st = 0; st < kDecStages; ++st) {
       tc::mbar_init(&sm.full[st], 1);
@@ -514,8 +545,10 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
   float* part_o = reinterpret_cast<float*>(w + L.off_o);
   cudaStream_t s = (cudaStream_t)stream;
   const int slots = (int)(L.ctas - (int64_t)n_req * Hkv);
-  decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(page_off, n_req, Hkv, slots, (int)L.ctas, first, nsplit, desc);
-  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  if (n_req > kDecThreads) {  // else the decode CTAs split the work themselves
+    decode_plan_kernel<<<1, kPlanThreads, 0, s>>>(page_off, n_req, Hkv, slots, (int)L.ctas, first, nsplit, desc);
+    if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  }
   const uint64_t pool_rows = (uint64_t)num_blocks * Hkv * PIC_PAGE;
   if (pool_rows == 0 || pool_rows > (uint64_t)INT32_MAX) return PIC_ERR_INVALID;
   CUtensorMap kmap, vmap;
@@ -526,13 +559,13 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
   const float4* qt = reinterpret_cast<const float4*>(q_table);
   switch (Hq / Hkv) {
     case 1: decode_kernel<1><<<grid, kDecThreads, sizeof(DecSmem<1>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
     case 2: decode_kernel<2><<<grid, kDecThreads, sizeof(DecSmem<2>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
     case 4: decode_kernel<4><<<grid, kDecThreads, sizeof(DecSmem<4>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
     default: decode_kernel<8><<<grid, kDecThreads, sizeof(DecSmem<8>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, part_ml, part_o, err_flag); break;
+        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
   }
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   decode_merge_kernel<<<dim3((unsigned)Hq, (unsigned)n_req), 32 * kMergeGroups, 0, s>>>(

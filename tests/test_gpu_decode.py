@@ -63,6 +63,18 @@ def test_decode_batched_sampled():
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 
 
+@pytest.mark.parametrize("n_req", [160, 170])
+def test_decode_many_requests(n_req):
+    """Up to 160 requests the decode CTAs split the work themselves; above, a planner
+    launch writes their descriptors: both give every request its own decode."""
+    rng = np.random.default_rng(n_req)
+    lens = [[int(x) for x in rng.integers(1, 60, size=int(rng.integers(1, 4)))] for _ in range(n_req)]
+    wl = inputs.custom(lens, [1] * n_req, [2] * n_req, Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=n_req)
+    b = _decode(wl)
+    emax, emean = _check(b, [0, n_req // 2, n_req - 1])
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
 @pytest.mark.parametrize("Hq", [8, 16, 32, 64])
 def test_decode_gqa_groups(Hq):
     wl = inputs.custom([[130, 70, 45], [55, 8, 200]], [20, 1], [2, 16], Hq=Hq, Hkv=8, d=128, theta=5e5,
