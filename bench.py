@@ -46,9 +46,8 @@ NCU_TRAFFIC = {
     ("rerotate", "94fbac229e1fc877"): 341751552,
     # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.40 MB written
     ("scheme_b", "94fbac229e1fc877"): 449222144,
-    # decode_kernel<4>, one row per request over the long-context link: 420.64 MB read + 4.42 MB written
-    # (captured before an empty asm that only consumes the MMA's discarded outputs)
-    ("decode", "055e5c15b721b166"): 425063168,
+    # decode_kernel<4>, one row per request over the long-context link: 420.65 MB read + 4.73 MB written
+    ("decode", "e8e2ed89ce131e93"): 425376000,
     # compose_kernel, 32 heads x 100-chunk chain, both levels: 417.43 + 14.75 MB read + 3.52 MB written
     ("compose", "e43e88d53b50babb"): 435703296,
 }
