@@ -48,8 +48,8 @@ NCU_TRAFFIC = {
     ("scheme_b", "94fbac229e1fc877"): 449222144,
     # decode_kernel<4>, one row per request over the long-context link: 420.65 MB read + 4.73 MB written
     ("decode", "e8e2ed89ce131e93"): 425376000,
-    # compose_kernel, 32 heads x 100-chunk chain, both levels: 417.43 + 14.75 MB read + 3.52 MB written
-    ("compose", "e43e88d53b50babb"): 435703296,
+    # compose_kernel, 32 heads x 100-chunk chain, both levels: 417.43 + 14.76 MB read + 3.54 MB written
+    ("compose", "1f16bf2f2eb3b24d"): 435723520,
 }
 
 

@@ -407,9 +407,9 @@ pic_status pic_link_attention_ror(const void* q, const float* row_table, const i
  *   out       [n_req][Hq][d] bf16
  *   ws        at least pic_decode_workspace() bytes, 256-byte aligned, any contents
  * bf16 pools with d = 128 and g = Hq / Hkv in {1, 2, 4, 8}; otherwise
- * PIC_ERR_UNSUPPORTED (0 from pic_decode_workspace).  Three launches: a one-block
- * planner gives every request splits in proportion to its pages so that all
- * CTAs fit in one wave (and writes each CTA's request, KV head and page range),
+ * PIC_ERR_UNSUPPORTED (0 from pic_decode_workspace).  Every request gets splits in
+ * proportion to its pages so that all CTAs fit in one wave — found by the decode
+ * CTAs themselves up to 160 requests, by a one-block planner launch above —,
  * the split-KV decode (pages moved into shared memory by TMA, each page's two
  * small contractions on warp-level bf16 MMAs with fp32 accumulate, P rounded to
  * bf16 as on the link path), and the merge of the splits.  Bound by HBM: every
@@ -459,7 +459,8 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
  * d = 128 only (else PIC_ERR_UNSUPPORTED; 0 from pic_compose_workspace).  Each
  * fold step is a 128 x 128 x 128 tensor-core product of bf16 parts
  * (hi.hi + hi.lo + lo.hi, fp32 accumulate: about 2^-16 relative error per step);
- * S is added in fp32.  Two or three launches.  A pool id outside [0, n_pool) or
+ * S is added in fp32.  One or two launches (one more, a planner, above 352
+ * requests).  A pool id outside [0, n_pool) or
  * offsets that disagree with n_elems / max_chain set PIC_ERR_RANGE in *err_flag
  * (pool entry 0 is read in place of a bad id); a bounded wait that runs out sets
  * PIC_ERR_TIMEOUT. */

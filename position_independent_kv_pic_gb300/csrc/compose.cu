@@ -90,6 +90,8 @@ struct Level {
   int max_chain;             // chain lengths are clamped to it (the planner flags longer ones)
   int level;
   bool last;
+  bool self_plan;            // few requests: every CTA finds its own (request, head, segment)
+  bool one_level;            // the call folds in one level (an empty chain still gets its CTAs)
   int32_t* err;
 };
 
@@ -165,25 +167,55 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
   CBars* cb = reinterpret_cast<CBars*>(sm + kOffBar);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int cta = blockIdx.x;
-  if (cta >= __ldg(lv.first + lv.n_req)) return;
   if (tc::smem_addr(smem_raw) & 1023u) {
     if (tid == 0) set_err(lv.err, PIC_ERR_UNSUPPORTED);
     return;
   }
-  int r;
-  {
+  int r, first_r;
+  if (lv.self_plan) {
+    // the planner's CTA counts, found by every CTA itself (one launch less): a scan
+    // over the requests; level 0's CTA 0 also checks the chain offsets
+    __shared__ int s_scan[kCThreads / 32 + 1];
+    __shared__ int s_req[2];
+    int w = 0;
+    if (tid < lv.n_req) {
+      int nr = __ldg(lv.chain_off + tid + 1) - __ldg(lv.chain_off + tid);
+      if (lv.level == 0 && cta == 0 &&
+          (nr < 0 || nr > lv.max_chain || __ldg(lv.chain_off + tid) < 0 || __ldg(lv.chain_off + tid + 1) > lv.n_elems))
+        set_err(lv.err, PIC_ERR_RANGE);
+      nr = min(max(nr, 0), lv.max_chain);
+      const int segs = nr > 0 ? (nr + lv.seg - 1) / lv.seg : 0;
+      w = lv.level == 0 ? lv.H * (lv.one_level ? max(segs, 1) : segs) : lv.H;
+    }
+    if (lv.level == 0 && cta == 0 && tid == 0 &&
+        (__ldg(lv.chain_off) != 0 || __ldg(lv.chain_off + lv.n_req) != lv.n_elems))
+      set_err(lv.err, PIC_ERR_RANGE);
+    int total;
+    const int ex = block_exclusive_scan<kCThreads>(w, s_scan, &total);
+    if (tid == 0 && cta >= total) s_req[0] = -1;
+    if (tid < lv.n_req && cta >= ex && cta < ex + w) {
+      s_req[0] = tid;
+      s_req[1] = ex;
+    }
+    __syncthreads();
+    if (s_req[0] < 0) return;  // the grid is an upper bound
+    r = s_req[0];
+    first_r = s_req[1];
+  } else {
+    if (cta >= __ldg(lv.first + lv.n_req)) return;
     int lo = 0, hi = lv.n_req;
     while (hi - lo > 1) {
       const int mid = (lo + hi) >> 1;
       if (__ldg(lv.first + mid) <= cta) lo = mid; else hi = mid;
     }
     r = lo;
+    first_r = __ldg(lv.first + r);
   }
   const int c0 = __ldg(lv.chain_off + r);
   const int n_r = min(max(__ldg(lv.chain_off + r + 1) - c0, 0), lv.max_chain);
   const int n_in = lv.level == 0 ? n_r : (n_r + lv.seg_prev - 1) / lv.seg_prev;
   const int n_segs = max(1, (n_in + lv.seg - 1) / lv.seg);
-  const int local = cta - __ldg(lv.first + r);
+  const int local = cta - first_r;
   const int h = local / n_segs, g = local % n_segs;
   const int b = g * lv.seg, e = min(n_in, b + lv.seg), n = e - b;
   const bool need_T = !lv.last && g > 0;
@@ -202,7 +234,10 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
     if (lv.level == 0) {
       const int64_t at = (int64_t)c0 + i;
       int64_t id = (at >= 0 && at < lv.n_elems) ? __ldg(lv.ids + at) : 0;
-      if (id < 0 || id >= lv.n_pool) id = 0;  // flagged by the planner
+      if (id < 0 || id >= lv.n_pool) {  // flagged by the planner, or here when there is none
+        if (lv.self_plan) set_err(lv.err, PIC_ERR_RANGE);
+        id = 0;
+      }
       return id * lv.H + h;
     }
     return chain * lv.in_stride + i;
@@ -606,9 +641,12 @@ pic_status pic_compose_states(const void* T_split, const float* S_pool, int64_t 
   int32_t* first1 = reinterpret_cast<int32_t*>(w + L.off_first1);
   CUtensorMap t0map;
   if (!encode_t(&t0map, T_split, (uint64_t)n_pool * H * 2 * kCD)) return PIC_ERR_CUDA;
-  compose_plan_kernel<<<1, 1024, 0, s>>>(ids, chain_off, n_req, H, n_pool, n_elems, max_chain, L.seg0,
-                                         L.one_level, first0, first1, err_flag);
-  if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  const bool self_plan = n_req <= kCThreads;  // else a one-block planner writes the CTA counts
+  if (!self_plan) {
+    compose_plan_kernel<<<1, 1024, 0, s>>>(ids, chain_off, n_req, H, n_pool, n_elems, max_chain, L.seg0,
+                                           L.one_level, first0, first1, err_flag);
+    if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  }
 
   Level l0{};
   l0.T_in = static_cast<const bf16*>(T_split);
@@ -626,6 +664,8 @@ pic_status pic_compose_states(const void* T_split, const float* S_pool, int64_t 
   l0.level = 0;
   l0.last = L.one_level;
   l0.err = err_flag;
+  l0.self_plan = self_plan;
+  l0.one_level = L.one_level;
   if (L.one_level) {
     l0.S_out = out;
     l0.out_stride = 1;

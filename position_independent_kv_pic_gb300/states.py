@@ -57,10 +57,12 @@ class ComposeBatch:
 
     @property
     def launches(self) -> int:
-        """Kernel launches of one call: the planner, level 0 and (two levels) level 1."""
+        """Kernel launches of one call: level 0, level 1 (two levels) and, above 352
+        requests, the planner (with fewer the CTAs find their work themselves)."""
         if self.n_req == 0:
             return 0
-        return 2 if (self.seg <= 1 or self.seg >= self.max_chain) else 3
+        levels = 1 if (self.seg <= 1 or self.seg >= self.max_chain) else 2
+        return levels + (1 if self.n_req > 352 else 0)
 
     @property
     def algorithmic_bytes(self) -> int:

@@ -89,10 +89,25 @@ def test_segment_choice_and_two_levels():
     T, S = _pool(8, 4, seed=13)
     chains = [list(np.random.default_rng(3).integers(0, 8, 100))]
     b = ComposeBatch(T, S, chains)
-    assert 1 < b.seg < 100 and b.launches == 3
+    assert 1 < b.seg < 100 and b.launches == 2  # level 0 and level 1; the CTAs plan themselves
     b.run()
     torch.cuda.synchronize()
     assert b.error() == 0
+    check(b, T, S, chains)
+
+
+@pytest.mark.parametrize("n_req", [352, 360])
+def test_many_requests(n_req):
+    """Up to 352 requests the CTAs find their (request, head, segment) themselves;
+    above, a planner launch writes the counts: both compose every chain."""
+    T, S = _pool(6, 1, seed=16)
+    rng = np.random.default_rng(n_req)
+    chains = [list(rng.integers(0, 6, int(rng.integers(0, 5)))) for _ in range(n_req)]
+    b = ComposeBatch(T, S, chains, seg=2)
+    assert b.launches == (2 if n_req <= 352 else 3)
+    b.run()
+    torch.cuda.synchronize()
+    assert b.error() == 0, pic.pic_strerror(b.error())
     check(b, T, S, chains)
 
 
