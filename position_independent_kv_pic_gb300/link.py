@@ -132,6 +132,7 @@ class LinkBatch:
         self.err = torch.zeros(1, dtype=i32, device=dev)
         self.scale = 1.0 / math.sqrt(d)
         self._side = None  # stream of the cached-K pass (created on first use)
+        self._plan_s = None  # stream of the row table and the attention plan (created on first use)
         if scheme == "nope":
             # the model's position table (every position a cached slot can take), built once
             self.n_pos = max([int(wl.chunk_lens[r.chunk_ids].sum()) for r in wl.requests] + [1])
@@ -224,6 +225,18 @@ class LinkBatch:
             pass_stream.wait_event(self._ev_fork)
         if self.scheme == "rotary":
             pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, pass_stream)
+        # a third stream, also forked after row selection, takes the row table and then
+        # (after the splice) the attention plan, beside the splice and the fresh K/V: the
+        # plan was the longest path to the attention run
+        plan_stream = main
+        if self.scheme in ("rotary", "nope"):
+            if self._plan_s is None:
+                self._plan_s = torch.cuda.Stream(self.device)
+                self._ev_rowtab, self._ev_planned = torch.cuda.Event(), torch.cuda.Event()
+            plan_stream = self._plan_s
+            plan_stream.wait_event(self._ev_fork)
+            pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, plan_stream)
+            self._ev_rowtab.record(plan_stream)
         pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
                          dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
                          dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
@@ -231,6 +244,12 @@ class LinkBatch:
         if pass_stream is not main:
             self._ev_spliced.record(main)
             pass_stream.wait_event(self._ev_spliced)
+        if plan_stream is not main:
+            plan_stream.wait_event(self._ev_spliced)
+            pic_link_attention_plan(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.pages,
+                                    dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.pic_dtype,
+                                    self.ws, self.err, plan_stream)
+            self._ev_planned.record(plan_stream)
         if self.scheme == "ror":
             pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, pass_stream)
         if "rerotate" in mk:
@@ -247,7 +266,10 @@ class LinkBatch:
             mk["rerotate"][1].record(pass_stream)
         if pass_stream is not main:
             self._ev_join.record(pass_stream)
-        pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, main)
+        if plan_stream is main:
+            pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, main)
+        else:
+            main.wait_event(self._ev_rowtab)
         pic_write_fresh_kv(self.k_pool, self.v_pool, self.pic_dtype, wl.Hkv, wl.d, dv["k_new"], dv["v_new"],
                            self.row_table, self.row_block, self.row_slot, self.n_rows, self.err, main)
         if self.scheme == "ror":
@@ -258,9 +280,7 @@ class LinkBatch:
                                    self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.scale, out_t, self.ws,
                                    self.err, main)
         else:
-            pic_link_attention_plan(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.pages,
-                                    dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.pic_dtype,
-                                    self.ws, self.err, main)
+            main.wait_event(self._ev_planned)
             main.wait_event(self._ev_join)
             if "attention" in mk:
                 mk["attention"][0].record(main)
