@@ -200,7 +200,8 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
  * a2  RoPE tables (RoPE article 2.2 and footnote 3).
  * ------------------------------------------------------------------------
  * table[i][j] = { cos_hi, sin_hi, cos_lo, sin_lo } of the angle pos[i] * theta^(-2j/d),
- * j < d/2: cos and sin are computed in fp64 on the device and stored as two fp32
+ * j < d/2: theta^(-2j/d) by the host's fp64 pow (once per call, passed to the
+ * kernel), cos and sin computed in fp64 on the device and stored as two fp32
  * parts each (hi = v rounded to 16 significant bits, lo = fp32(v - hi)).  With
  * them the rotation kernels reach ~2^-23 relative error (bf16 inputs times a
  * 16-bit hi are exact in fp32) and store K within one bf16 ulp of the exact

@@ -9,6 +9,8 @@
 // the query's K/V are appended.
 #include <algorithm>
 
+#include <cmath>
+
 #include "pic_internal.cuh"
 
 namespace pic {
@@ -243,19 +245,27 @@ __device__ __forceinline__ float round16(double v) {
   return __uint_as_float(u);
 }
 
-constexpr int kTabThreads = 256;
+// Small blocks: a table of a few thousand entries (the per-chunk offset table, one
+// decode row) still spreads over many SMs, whose fp64 units are few.
+constexpr int kTabThreads = 64;
+
+// theta^(-2j/d), j < d/2, in fp64 (the host's pow, once per call).
+struct InvFreq {
+  double w[128];
+};
 
 __global__ void __launch_bounds__(kTabThreads)
-rope_table_kernel(const int32_t* __restrict__ pos, int64_t n, int half, double theta, float4* __restrict__ table) {
+rope_table_kernel(const int32_t* __restrict__ pos, int64_t n, int half, const __grid_constant__ InvFreq f,
+                  float4* __restrict__ table) {
   __shared__ double inv_freq[128];
-  for (int j = threadIdx.x; j < half; j += blockDim.x) inv_freq[j] = pow(theta, -2.0 * (double)j / (double)(2 * half));
+  for (int j = threadIdx.x; j < half; j += blockDim.x) inv_freq[j] = f.w[j];
   __syncthreads();
   const int64_t total = n * half;
   for (int64_t t = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; t < total;
        t += (int64_t)gridDim.x * blockDim.x) {
     const int64_t i = t / half;
     const int j = (int)(t - i * half);
-    const double ang = (double)pos[i] * inv_freq[j];
+    const double ang = (double)__ldg(pos + i) * inv_freq[j];
     double s, c;
     sincos(ang, &s, &c);
     const float ch = round16(c), sh = round16(s);
@@ -309,11 +319,13 @@ pic_status pic_rope_table(const int32_t* pos, int64_t n, int32_t d, double theta
   if (n < 0 || d < 2 || d > 256 || (d & 1) || !(theta > 0.0)) return PIC_ERR_INVALID;
   if (n == 0) return PIC_OK;
   if (!pos || !table) return PIC_ERR_INVALID;
+  InvFreq f;
+  for (int j = 0; j < d / 2; ++j) f.w[j] = std::pow(theta, -2.0 * (double)j / (double)d);
   const int64_t total = n * (d / 2);
   const int64_t blocks = (total + kTabThreads - 1) / kTabThreads;
-  const int64_t cap = (int64_t)num_sms_of_current_device() * 8;
+  const int64_t cap = (int64_t)num_sms_of_current_device() * 32;
   rope_table_kernel<<<(unsigned)(blocks < cap ? blocks : cap), kTabThreads, 0, (cudaStream_t)stream>>>(
-      pos, n, d / 2, theta, reinterpret_cast<float4*>(table));
+      pos, n, d / 2, f, reinterpret_cast<float4*>(table));
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }
 
