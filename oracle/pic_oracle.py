@@ -1,6 +1,7 @@
 """Oracle for the PIC link step.  TEST INFRASTRUCTURE ONLY.
 
-A plain, slow, float64 CPU restatement of what the link step computes.  Only the
+A plain, slow, float64 CPU restatement of what the link step computes (NumPy,
+and PyTorch CPU operations for the attention's products).  Only the
 tests, ``__graft_entry__.smoke()`` and the CPU-baseline / reference leg of
 ``bench.py`` may import it; the product path (the CUDA library and its binding)
 never does.  It shares no code, tables or constants with the CUDA path and works
@@ -45,6 +46,7 @@ from __future__ import annotations
 import math
 
 import numpy as np
+import torch
 
 __all__ = [
     "select_rows", "count_rows", "inv_freq", "rope", "round_to", "compile_chunk_k",
@@ -206,36 +208,48 @@ def splice_context(chunks_k, chunks_v, q, k, k_new_raw, v_new, theta, dtype, sch
     return K, V, rows, starts, T
 
 
-def attention_rows(q_rot, q_pos, K_ctx, V_ctx, scale, which=None) -> np.ndarray:
+def attention_rows(q_rot, q_pos, K_ctx, V_ctx, scale, which=None, group=16) -> np.ndarray:
     """Masked softmax attention of position-encoded queries over the spliced context.
 
     q_rot [n][Hq][d], q_pos [n]; key j sits at global position j.  For every
     selected row and head: O = sum_j softmax_j(q.K_j * scale) V_j over visible j,
     KV head floor(h/g).  ``which`` restricts the rows computed (others are NaN).
+
+    Rows are independent.  They are taken ``group`` at a time so that one matrix
+    product per KV head serves the group's g * group query vectors; each row keeps
+    its own visibility mask (built by ``visible`` for that row alone), masked
+    scores are -inf and so get weight exactly 0.  Everything is float64; the
+    products and elementwise passes are PyTorch CPU operations, which use every
+    host core.
     """
     n, Hq, d = q_rot.shape
     N, Hkv, _ = K_ctx.shape
     g = Hq // Hkv
-    Kt = np.ascontiguousarray(K_ctx.transpose(1, 0, 2))  # [Hkv][N][d]
-    Vt = np.ascontiguousarray(V_ctx.transpose(1, 0, 2))
+    Q = torch.from_numpy(np.ascontiguousarray(q_rot, np.float64))
+    Kt = torch.from_numpy(np.ascontiguousarray(np.asarray(K_ctx, np.float64).transpose(1, 0, 2)))  # [Hkv][N][d]
+    Vt = torch.from_numpy(np.ascontiguousarray(np.asarray(V_ctx, np.float64).transpose(1, 0, 2)))
     key_pos = np.arange(N)
-    out = np.full((n, Hq, d), np.nan)
-    for i in (range(n) if which is None else which):
-        vis = visible(key_pos, int(q_pos[i]))
-        idx = np.flatnonzero(vis)
-        if idx.size == 0:
+    out = torch.full((n, Hq, d), float("nan"), dtype=torch.float64)
+    todo = list(range(n)) if which is None else [int(i) for i in which]
+    for b0 in range(0, len(todo), group):
+        sel = todo[b0:b0 + group]
+        vis = np.stack([visible(key_pos, int(q_pos[i])) for i in sel])   # [nb][N]
+        if not vis.any(axis=1).all():
             raise ValueError("a query row sees no key")
-        last = int(idx[-1]) + 1
-        m = vis[:last]
-        qh = q_rot[i].reshape(Hkv, g, d).transpose(0, 2, 1)   # [Hkv][d][g]
-        s = (Kt[:, :last, :] @ qh) * scale                    # [Hkv][last][g]
-        s = np.where(m[None, :, None], s, -np.inf)
-        s = s - s.max(axis=1, keepdims=True)
-        w = np.where(m[None, :, None], np.exp(s), 0.0)
-        w = w / w.sum(axis=1, keepdims=True)
-        o = w.transpose(0, 2, 1) @ Vt[:, :last, :]          # [Hkv][g][d]
-        out[i] = o.reshape(Hq, d)
-    return out
+        last = int(np.flatnonzero(vis.any(axis=0))[-1]) + 1
+        mask = torch.from_numpy(vis[:, None, :last])                        # [nb][1][last]
+        nb = len(sel)
+        idx = torch.tensor(sel, dtype=torch.int64)
+        for h in range(Hkv):
+            qh = Q[idx, h * g:(h + 1) * g, :].reshape(nb * g, d)
+            s = (qh @ Kt[h, :last].T).reshape(nb, g, last)
+            s.mul_(scale)
+            s.masked_fill_(~mask, float("-inf"))
+            s.sub_(s.amax(dim=2, keepdim=True))
+            s.exp_()
+            s.div_(s.sum(dim=2, keepdim=True))
+            out[idx, h * g:(h + 1) * g, :] = (s.reshape(nb * g, last) @ Vt[h, :last]).reshape(nb, g, d)
+    return out.numpy()
 
 
 def link_request(chunks_k, chunks_v, q, k, q_raw, k_new_raw, v_new, theta, dtype,
