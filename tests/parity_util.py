@@ -4,6 +4,7 @@ import numpy as np
 import torch
 
 import oracle.pic_oracle as O
+from position_independent_kv_pic_gb300 import inputs
 
 TOL_MAX, TOL_MEAN = 2e-2, 2e-3   # attention: fp32 accumulate, bf16 out
 
@@ -19,10 +20,28 @@ def request_inputs(batch, r):
             batch.k_new_h[a:b].double().numpy(), batch.v_new_h[a:b].double().numpy())
 
 
-def oracle_request(batch, r, which=None):
+def oracle_request(batch, r, which=None, scheme="rotary"):
     wl = batch.wl
     ck, cv, q, k, qr, kn, vn = request_inputs(batch, r)
-    return O.link_request(ck, cv, q, k, qr, kn, vn, wl.theta, wl.dtype, which=which)
+    return O.link_request(ck, cv, q, k, qr, kn, vn, wl.theta, wl.dtype, which=which, scheme=scheme)
+
+
+# Oracle outputs of whole requests of the preset workloads, kept for the session:
+# the rotary-correction and rotate-on-read steps of one preset share their inputs,
+# so they share the oracle's answer (the oracle's cost dominates these tests).
+_ORACLE_CACHE = {}
+
+
+def oracle_out(batch, r, scheme="rotary"):
+    """float64 oracle output [n_rows(r)][Hq][d] of request r (every row)."""
+    wl = batch.wl
+    key = (wl.name, wl.seed, r, scheme) if wl.name in inputs.PRESETS else None
+    if key is not None and key in _ORACLE_CACHE:
+        return _ORACLE_CACHE[key]
+    out = oracle_request(batch, r, scheme=scheme)["out"]
+    if key is not None:
+        _ORACLE_CACHE[key] = out
+    return out
 
 
 def bf16_ulp(x):
@@ -90,20 +109,50 @@ def sample_rows(n, k_first=8, k_last=8, k_rand=16, seed=0):
     return sorted(idx)
 
 
-def check_attention(batch, which_per_request=None):
-    """Max-abs and mean-abs error of the attention output against the oracle."""
+def check_attention(batch, which_per_request=None, scheme="rotary"):
+    """Max-abs and mean-abs error of the attention output against the oracle
+    (every row of every request unless ``which_per_request`` picks rows)."""
     out = batch.out.double().cpu().numpy()
     errs = []
     for r in range(batch.n_req):
         a, b = int(batch.offs["row_off"][r]), int(batch.offs["row_off"][r + 1])
         if b == a:
             continue
-        which = None if which_per_request is None else which_per_request(b - a)
-        res = oracle_request(batch, r, which)
-        sel = list(range(b - a)) if which is None else which
-        errs.append(np.abs(out[a:b][sel] - res["out"][sel]).reshape(-1))
+        if which_per_request is None:
+            errs.append(np.abs(out[a:b] - oracle_out(batch, r, scheme)).reshape(-1))
+        else:
+            which = which_per_request(b - a)
+            res = oracle_request(batch, r, which, scheme)
+            errs.append(np.abs(out[a:b][which] - res["out"][which]).reshape(-1))
     if not errs:
         return 0.0, 0.0
     e = np.concatenate(errs)
     assert np.isfinite(e).all()
     return float(e.max()), float(e.mean())
+
+
+def check_fresh_kv(batch):
+    """a4, read back from the pools: the slot of every recomputed row (row_block,
+    row_slot from the splice) holds K = RoPE(K_new, p_r) rounded to the pool dtype,
+    within one ulp of the oracle's rounding of the float64 rotation, and V = V_new
+    bit for bit.  p_r comes from the oracle's row selection.  Returns the worst K
+    error in ulps."""
+    wl = batch.wl
+    if batch.n_rows == 0:
+        return 0.0
+    blk, slot = batch.row_block.long(), batch.row_slot.long()
+    k_got = batch.k_pool[blk, :, slot, :].double().cpu().numpy()
+    v_got = batch.v_pool[blk, :, slot, :].cpu()
+    assert torch.equal(v_got, batch.v_new_h), "fresh V differs from V_new"
+    worst = 0.0
+    bound = 1.0 if wl.dtype == "bf16" else 4.0
+    for r, req in enumerate(wl.requests):
+        a, b = int(batch.offs["row_off"][r]), int(batch.offs["row_off"][r + 1])
+        if b == a:
+            continue
+        rows, _, _ = O.select_rows(wl.chunk_lens[req.chunk_ids], req.q, req.k)
+        expect = O.round_to(O.rope(batch.k_new_h[a:b].double().numpy(), rows, wl.theta), wl.dtype)
+        ratio = float((np.abs(k_got[a:b] - expect) / storage_ulp(expect, wl.dtype)).max())
+        worst = max(worst, ratio)
+        assert ratio <= bound, f"fresh K of request {r}: {ratio} ulp"
+    return worst

@@ -1,12 +1,13 @@
 """Parity of the CUDA path (through the C ABI) against the float64 oracle.
 
-Rows and chunk starts: bit-exact.  Re-rotated K: within 1 ulp of the storage
-dtype.  Attention: max-abs <= 2e-2 and mean-abs <= 2e-3 (fp32 accumulate, bf16
-out).  Small workloads are compared on every output; the ~100k-token and batched
-workloads (the sizes and launch configuration the benchmark times) on sampled rows.
+Rows and chunk starts: bit-exact.  Re-rotated K and the recomputed rows' fresh K:
+within 1 ulp of the storage dtype; fresh V bit-identical.  Attention: max-abs <=
+2e-2 and mean-abs <= 2e-3 (fp32 accumulate, bf16 out).  Every workload, the
+~100k-token and batched ones included (the sizes and launch configuration the
+benchmark times), is compared on every row and every re-rotated chunk.  Two
+mistakes planted in the step's host sequence (no re-rotation; a row table on
+local positions) must each miss the attention tolerance by more than 10x.
 """
-
-import math
 
 import numpy as np
 import pytest
@@ -18,8 +19,7 @@ from position_independent_kv_pic_gb300 import build as pic_build
 from position_independent_kv_pic_gb300 import inputs
 from position_independent_kv_pic_gb300.link import LinkBatch
 
-from parity_util import (TOL_MAX, TOL_MEAN, check_attention, check_rerotated_k, check_rows, oracle_request,
-                         sample_rows)
+from parity_util import TOL_MAX, TOL_MEAN, check_attention, check_fresh_kv, check_rerotated_k, check_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -66,46 +66,65 @@ def test_worked_example_fp32():
     check_rows(b)
     assert b.rows.cpu().tolist() == [4, 5, 9, 10, 14, 15, 16]
     check_rerotated_k(b)
+    check_fresh_kv(b)
     emax, emean = check_attention(b)
     assert emax < 1e-5 and emean < 1e-6, (emax, emean)
 
 
-def test_rag_prompt():
-    b = _run(inputs.rag_prompt())
+@pytest.mark.parametrize("preset", ["rag_prompt_6chunks", "many_chunk_sink_20", "long_context_100x1000",
+                                    "batched_shared_16req"])
+def test_bf16_workload(preset):
+    """Every row, every re-rotated chunk and every fresh slot of the workload."""
+    b = _run(inputs.PRESETS[preset]())
     check_rows(b)
     check_rerotated_k(b)
+    check_fresh_kv(b)
     emax, emean = check_attention(b)
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+    if b.wl.out_of_place:  # the shared sources are untouched
+        for c, blocks in enumerate(b.store_blocks):
+            L = int(b.wl.chunk_lens[c])
+            j = np.arange(L)
+            got = b.k_pool[torch.from_numpy(blocks[j // 16]).cuda(), :, torch.from_numpy(j % 16).cuda(), :].cpu()
+            assert torch.equal(got, b.store_k[b.store_off[c]:b.store_off[c + 1]])
 
 
-def test_many_chunk_sink():
-    b = _run(inputs.many_chunk())
-    check_rows(b)
-    check_rerotated_k(b)
+# ---------------------------------------------------------------- planted mistakes (host sequence)
+
+def _assert_caught(b):
     emax, emean = check_attention(b)
-    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+    assert emax > 10 * TOL_MAX or emean > 10 * TOL_MEAN, (emax, emean)
 
 
-def test_long_context_sampled():
-    b = _run(inputs.long_context())
-    check_rows(b)
-    check_rerotated_k(b, max_chunks=12)
-    emax, emean = check_attention(b, lambda n: sample_rows(n, 6, 6, 12))
-    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+def test_mutation_skipped_rerotation_is_caught(monkeypatch):
+    """The step without pic_rerotate_k (cached K left at local positions) fails parity."""
+    import position_independent_kv_pic_gb300.link as link
+    monkeypatch.setattr(link, "pic_rerotate_k", lambda *a, **kw: None)
+    _assert_caught(_run(inputs.rag_prompt()))
 
 
-def test_batched_shared_sampled():
-    b = _run(inputs.batched_shared())
-    check_rows(b)
-    check_rerotated_k(b, max_chunks=3)
-    emax, emean = check_attention(b, lambda n: sample_rows(n, 2, 2, 3))
-    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
-    # out-of-place: the shared sources are untouched
-    for c, blocks in enumerate(b.store_blocks[:8]):
-        L = int(b.wl.chunk_lens[c])
-        j = np.arange(L)
-        got = b.k_pool[torch.from_numpy(blocks[j // 16]).cuda(), :, torch.from_numpy(j % 16).cuda(), :].cpu()
-        assert torch.equal(got, b.store_k[b.store_off[c]:b.store_off[c + 1]])
+def test_mutation_local_position_row_table_is_caught(monkeypatch):
+    """The step with the per-row RoPE table built on chunk-local positions (the row's
+    offset in its chunk, or in the query) fails parity."""
+    import position_independent_kv_pic_gb300.link as link
+    wl = inputs.rag_prompt()
+    b = LinkBatch(wl)
+    local = []
+    for req in wl.requests:
+        rows, starts, T = O.select_rows(wl.chunk_lens[req.chunk_ids], req.q, req.k)
+        c = np.searchsorted(starts, rows, side="right") - 1
+        local.append(np.where(rows >= T, rows - T, rows - starts[c]))
+    local_dev = torch.from_numpy(np.concatenate(local).astype(np.int32)).cuda()
+    real = link.pic_rope_table
+
+    def table_on_local_rows(pos, d, theta, table, stream=None):
+        return real(local_dev if pos.data_ptr() == b.rows.data_ptr() else pos, d, theta, table, stream)
+
+    monkeypatch.setattr(link, "pic_rope_table", table_on_local_rows)
+    b.run()
+    torch.cuda.synchronize()
+    assert b.error() == 0
+    _assert_caught(b)
 
 
 # ---------------------------------------------------------------- edge cases
@@ -134,6 +153,7 @@ def test_edge_cases(case):
     b = _run(wl)
     check_rows(b)
     check_rerotated_k(b)
+    check_fresh_kv(b)
     emax, emean = check_attention(b)
     tol = (1e-4, 1e-5) if dtype == "fp32" else (TOL_MAX, TOL_MEAN)
     assert emax <= tol[0] and emean <= tol[1], (emax, emean)
@@ -151,6 +171,7 @@ def test_fp32_small_head_dims():
         b = _run(wl)
         check_rows(b)
         check_rerotated_k(b)
+        check_fresh_kv(b)
         emax, emean = check_attention(b)
         assert emax < 1e-4 and emean < 1e-5, (d, emax, emean)
 

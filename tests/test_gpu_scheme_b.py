@@ -12,7 +12,7 @@ from position_independent_kv_pic_gb300 import build as pic_build
 from position_independent_kv_pic_gb300 import inputs
 from position_independent_kv_pic_gb300.link import LinkBatch
 
-from parity_util import TOL_MAX, TOL_MEAN, check_rows, request_inputs, sample_rows, storage_ulp
+from parity_util import TOL_MAX, TOL_MEAN, check_attention, check_fresh_kv, check_rows, storage_ulp
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +33,7 @@ def _run(wl):
     return b
 
 
-def _check_k(b, max_chunks=None):
+def _check_k(b):
     """Every kept cached K slot (chunk 0 included) within one ulp of the oracle's
     encoding at the global position."""
     wl = b.wl
@@ -41,8 +41,6 @@ def _check_k(b, max_chunks=None):
     for r, req in enumerate(wl.requests):
         c0, c1 = int(b.chunk_off[r]), int(b.chunk_off[r + 1])
         for ci, c in enumerate(range(c0, c1)):
-            if max_chunks is not None and 1 <= ci < c1 - c0 - 1 and ci >= max_chunks:
-                continue
             sid = int(b.flat_store_ids[c])
             stored = b.store_k[b.store_off[sid]:b.store_off[sid + 1]].double().numpy()
             got = b.rotated_chunk_k(c).double().numpy()
@@ -52,34 +50,18 @@ def _check_k(b, max_chunks=None):
             assert ratio <= (1.0 if wl.dtype == "bf16" else 4.0), (r, ci, ratio)
 
 
-def _check_attention(b, pick=None):
-    wl = b.wl
-    out = b.out.double().cpu().numpy()
-    errs = []
-    for r in range(len(wl.requests)):
-        a, e = int(b.offs["row_off"][r]), int(b.offs["row_off"][r + 1])
-        which = list(range(e - a)) if pick is None else pick(e - a)
-        ck, cv, q, k, qr, kn, vn = request_inputs(b, r)
-        res = O.link_request(ck, cv, q, k, qr, kn, vn, wl.theta, wl.dtype, which=which, scheme="nope")
-        errs.append(np.abs(out[a:e][which] - res["out"][which]).ravel())
-    x = np.concatenate(errs)
-    return float(x.max()), float(x.mean())
+def _check_attention(b):
+    return check_attention(b, scheme="nope")
 
 
-@pytest.mark.parametrize("preset", ["rag_prompt_6chunks", "many_chunk_sink_20"])
+@pytest.mark.parametrize("preset", ["rag_prompt_6chunks", "many_chunk_sink_20", "long_context_100x1000"])
 def test_scheme_b_workloads(preset):
+    """Every kept cached slot, every fresh slot and every row of the workload."""
     b = _run(inputs.PRESETS[preset]())
     check_rows(b)
     _check_k(b)
+    check_fresh_kv(b)
     emax, emean = _check_attention(b)
-    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
-
-
-def test_scheme_b_long_context_sampled():
-    b = _run(inputs.long_context())
-    check_rows(b)
-    _check_k(b, max_chunks=10)
-    emax, emean = _check_attention(b, lambda n: sample_rows(n, 6, 6, 12))
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 
 
@@ -93,6 +75,7 @@ def test_scheme_b_edge_cases(case):
     b = _run(inputs.custom(lens, qs, ks, Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=70 + len(lens)))
     check_rows(b)
     _check_k(b)
+    check_fresh_kv(b)
     emax, emean = _check_attention(b)
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 
