@@ -318,19 +318,27 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
  * with its planning and split-KV scratch in one fixed device array of
  * PIC_NOALLOC_SCRATCH_BYTES inside the library.  It calls no cudaMalloc,
  * cudaFree or allocating routine.
- *   - The array exists on every GPU that loads the library and stays allocated
- *     until the process exits.
- *   - The first call on a device looks up the array's device address (with that
- *     device current) and keeps it; make that first call before any stream
- *     capture.
+ *   - The array is reserved on a GPU when the library's device code is loaded
+ *     there.  CUDA loads device code lazily by default: at the first launch of
+ *     one of this library's attention kernels on that GPU, or at this entry
+ *     point's first call, whichever comes first; it then stays reserved until
+ *     the process exits.  Loading may also synchronise the device.
+ *   - Warm-up: call this entry point once on each device, with that device
+ *     current, BEFORE reserving most of HBM and before any stream capture.  A
+ *     call with n_req = 0 or n_rows = 0 does exactly this (it launches nothing,
+ *     loads the device code, looks up and keeps the array's device address) and
+ *     returns PIC_OK, or PIC_ERR_CUDA if the device code cannot be loaded (for
+ *     example when HBM is already full).
+ *   - The looked-up address is kept for the life of the process: do not use
+ *     the library across a cudaDeviceReset.
  *   - Every call on a device uses the same array, which keeps the previous
  *     call's contents (nothing in it needs to start at zero).  Calls whose work
  *     overlaps on the GPU (different streams, or host threads without ordering)
  *     race on the array: order them.
  *   - The tensor-core path (bf16, d = 128) splits long key ranges into at most
- *     60 extra work units; a call whose scratch would exceed the array (about
- *     900 recomputed rows of one request at Hq = 32, Hkv = 8; about 700 over 4
- *     requests) is refused with PIC_ERR_WORKSPACE before any other check or
+ *     60 extra work units; a call whose scratch would exceed the array (more
+ *     than 959 recomputed rows of one request at Hq = 32, Hkv = 8, more than
+ *     767 over 4 requests) is refused with PIC_ERR_WORKSPACE before any other check or
  *     launch.  The SIMT path (fp32 pools, other shapes) needs no scratch.
  * Results match pic_link_attention within the attention tolerance (the split
  * of key ranges, and so the summation order, can differ). */

@@ -67,7 +67,10 @@ class _Sizes(ctypes.Structure):
 
 
 def library_path() -> str:
-    return os.path.join(_HERE, "libpic.so")
+    """The in-tree libpic.so, or the build of the library that the environment
+    variable PIC_LIBRARY names (a file name in this package's directory, e.g. the
+    failure-injection test build)."""
+    return os.path.join(_HERE, os.environ.get("PIC_LIBRARY", "libpic.so"))
 
 
 _P = ctypes.c_void_p
@@ -116,7 +119,7 @@ def load():
     if _LIB is None:
         path = library_path()
         if not os.path.exists(path):
-            raise ImportError(f"libpic.so not built ({path}); run position_independent_kv_pic_gb300.build")
+            raise ImportError(f"{os.path.basename(path)} not built ({path}); run position_independent_kv_pic_gb300.build")
         lib = ctypes.CDLL(path)
         for name, (res, args) in _SIGS.items():
             fn = getattr(lib, name)

@@ -23,7 +23,6 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
-LIB = os.path.join(PKG, "libpic.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE,
@@ -50,10 +49,10 @@ def _deps():
     return glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def _up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def _up_to_date(lib: str) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
@@ -64,19 +63,26 @@ def _run(cmd):
     return r.stdout
 
 
-def build(force: bool = False, verbose: bool = False, extra_nvcc=()) -> str:
-    """Compile and link libpic.so; returns its path.  Skips work when up to date."""
-    if not force and not extra_nvcc and _up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_nvcc=(), name: str = "libpic.so") -> str:
+    """Compile and link the library; returns its path.  Skips work when up to date.
+
+    ``name`` other than libpic.so builds a variant of the library (its own objects
+    and file, next to libpic.so) with ``extra_nvcc`` added, e.g. the failure-injection
+    test build; a variant is rebuilt only when it is missing or older than a source."""
+    lib = os.path.join(PKG, name)
+    variant = name != "libpic.so"
+    if not force and (variant or not extra_nvcc) and _up_to_date(lib):
+        return lib
+    bdir = os.path.join(BUILD, os.path.splitext(name)[0]) if variant else BUILD
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
     cus, cpps = _sources()
     jobs = []
     for src in cus:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         jobs.append(([nvcc, *ARCH, *NVCC_FLAGS, *extra_nvcc, "-c", src, "-o", obj], obj))
     for src in cpps:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         jobs.append((["g++", *CXX_FLAGS, "-c", src, "-o", obj], obj))
     with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 1))) as ex:
         outs = list(ex.map(lambda j: _run(j[0]), jobs))
@@ -84,10 +90,10 @@ def build(force: bool = False, verbose: bool = False, extra_nvcc=()) -> str:
         for o in outs:
             if o.strip():
                 print(o)
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp] + [o for _, o in jobs])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -5,24 +5,33 @@
 // g = Hq/Hkv query heads shares one KV head).
 //
 // bf16, d = 128.  One MMA tile is M = 128 rows = g query heads x (128/g)
-// recomputed rows of one KV head.  A CTA works on a pair of such Q tiles and
-// streams the key tiles (128 keys = 8 pages of 16) of one unit through a ring
-// of four 32 KB shared-memory slots (K and V tiles alternate), filled by TMA
-// straight from the paged pool.  Per key tile and Q tile i:
+// recomputed rows of one KV head.  A persistent CTA (one per SM, 640 threads)
+// works on a pair of such Q tiles and streams the key tiles (128 keys = 8 pages
+// of 16) of one unit through a ring of five 32 KB shared-memory slots (K and V
+// tiles alternate), filled by TMA straight from the paged pool, one 4 KB box per
+// page.  Per key tile and Q tile i:
 //   S_i = Q_i K^T   (tcgen05, fp32 accumulators in TMEM)
-//   softmax warpgroup i: S_i -> registers (one thread per row), online softmax
-//     in base 2 with lazy rescaling, P_i (bf16) written back over S_i in TMEM
+//   softmax: S_i -> registers, online softmax in base 2 with lazy rescaling,
+//     P_i (bf16) written back over S_i in TMEM
 //   O_i += P_i V    (tcgen05 with A from TMEM)
-// While warpgroup 0 turns S_0 into P_0 the tensor core computes S_1 / P_1 V,
-// and the other way round.  Warp 0 issues TMA, warp 1 issues MMAs and owns TMEM,
-// warps 4-7 and 8-11 are the two softmax warpgroups.
+// While Q tile 0's softmax runs the tensor core computes S_1 / P_1 V, and the
+// other way round.  Roles: warp 0 issues TMA (K/V pages, Q operands); warp 1
+// lane 0 issues the MMAs and warp 1 owns TMEM (S0 | S1 | O0 | O1, 512 columns);
+// warps 2-3 wait for each key tile's loads, zero V rows outside a page's valid
+// slots (and rotate K in the rotate-on-read instantiation), and release the tile
+// to the issuer; warps 4-19 are four softmax warpgroups, one per (Q tile, half of
+// the 128 key columns), the two halves of a row exchanging their partial maxima
+// through shared memory at a named barrier once per key tile.
 //
 // Work is cut into units (Q-tile pair, KV head, span of key tiles).  Pairs whose
 // key range is longer than the span are split; their partial (O, m, l) are merged
-// by the LSE merge kernel.  Units are ordered longest first (the LPT greedy rule
-// HYPIC uses to balance segment work) and dealt round-robin to one CTA per SM.
-// Key tiles past a pair's last row position are never visited (offset-causal
-// tile skipping); keys inside boundary tiles are masked per row.
+// by the LSE merge kernel.  The planner lists full spans first and tails by
+// decreasing length (the LPT greedy rule HYPIC uses to balance segment work);
+// CTAs draw units from a global counter while they run.  Key tiles past a pair's
+// last row position are never visited (offset-causal tile skipping); keys inside
+// boundary tiles are masked per row.  Every mbarrier wait is bounded; a wait that
+// runs out sets PIC_ERR_TIMEOUT and the CTA's roles leave together (copies in
+// flight drained, TMEM freed).
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -389,6 +398,7 @@ struct Bars {
   uint64_t vz_done[kSlots];
   uint64_t q_full[kQTiles], q_free[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
+  uint64_t never;  // no thread ever arrives on it (the failure-injection test build waits on it)
   int unit_idx[kUnitRing];
   uint32_t tmem_base;
   int abort;
@@ -571,6 +581,12 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       tc::mma_bf16_ts(tmem + kTmemO + i * 128, tmem + i * 128 + ks * 8,
                       tc::desc_join(vb + ks * (kPageBytes >> 4), kHiKV), kIdescPV, (acc || ks > 0) ? 1u : 0u);
   };
+#ifdef PIC_INJECT_WAIT_TIMEOUT
+  // Failure-injection test build only: a bounded wait on a barrier that nothing
+  // arrives on runs out, reports PIC_ERR_TIMEOUT and must bring every role of the
+  // CTA to a clean exit (copies drained, TMEM freed).
+  if (!tc::mbar_wait(&b->never, 0, &b->abort, PIC_INJECT_WAIT_TIMEOUT)) { fail(b, a.err); return; }
+#endif
   for (uint32_t k = 0;; ++k) {
     const int u = read_unit(b, k);
     if (u < 0) { fail(b, a.err); return; }
@@ -867,6 +883,22 @@ __device__ __forceinline__ void pair_sync(int qt) {
   asm volatile("bar.sync %0, 256;" ::"r"(1 + qt) : "memory");
 }
 
+// The same barrier, also returning whether any of its 256 threads passed `failed`.
+// A warpgroup whose wait gave up still meets its partner here, and both leave
+// together: returning alone would leave the partner at its next barrier forever.
+__device__ __forceinline__ bool pair_sync_any(int qt, bool failed) {
+  uint32_t any;
+  asm volatile(
+      "{\n\t.reg .pred f, a;\n\t"
+      "setp.ne.u32 f, %1, 0;\n\t"
+      "bar.red.or.pred a, %2, 256, f;\n\t"
+      "selp.u32 %0, 1, 0, a;\n\t}"
+      : "=r"(any)
+      : "r"((uint32_t)failed), "r"(1 + qt)
+      : "memory");
+  return any != 0;
+}
+
 // Warpgroup (qt, h) handles key columns 64h .. 64h+63 of every S tile of Q tile qt,
 // one row (TMEM lane) per thread.  The two halves of a row exchange their partial
 // maxima through shared memory once per key tile (so both take identical lazy
@@ -884,7 +916,8 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
   uint32_t c = 0, ou = 0;  // tiles / units this warpgroup worked on
   for (uint32_t k = 0;; ++k) {
     const int u = read_unit_warp(b, k);
-    if (u < 0) { fail(b, a.err); return; }
+    // both warpgroups of the Q tile read the same unit sequence; they give up together
+    if (pair_sync_any(qt, u < 0)) { fail(b, a.err); return; }
     if (u >= n_units) break;
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
@@ -930,14 +963,20 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
         }
       }
 
-      if (!wait_bar(b, &b->s_full[qt], c & 1)) { fail(b, a.err); return; }
+      // a warp that gave up skips its TMEM read and meets its partner at the pair barrier below
+      const bool s_ok = __all_sync(0xffffffffu, wait_bar(b, &b->s_full[qt], c & 1));
       tc::tc_fence_after();
       float s[64];
       {
         uint32_t sr[64];
-        tc::tmem_ld32(tS + 64 * h, sr);
-        tc::tmem_ld32(tS + 64 * h + 32, sr + 32);
-        tc::tmem_ld_wait();
+        if (s_ok) {
+          tc::tmem_ld32(tS + 64 * h, sr);
+          tc::tmem_ld32(tS + 64 * h + 32, sr + 32);
+          tc::tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int k2 = 0; k2 < 64; ++k2) sr[k2] = 0u;
+        }
         tc::reg_fence<64>(sr);
 #pragma unroll
         for (int k2 = 0; k2 < 64; ++k2) s[k2] = u2f(sr[k2]);
@@ -958,7 +997,7 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       // both halves have read their S columns after this barrier, so P may be written;
       // the next write of xch follows s_full of the next tile, i.e. both p_full arrivals
       xch[h * kM + t] = pmax;
-      pair_sync(qt);
+      if (pair_sync_any(qt, !s_ok)) { fail(b, a.err); return; }
       const float mt = fmaxf(pmax, xch[(1 - h) * kM + t]) * a.scale_log2;
       float alpha = 1.f;
       bool resc = false;
@@ -1012,11 +1051,11 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       if (lane == 0) tc::mbar_arrive(&b->p_full[qt]);
     }
     // epilogue: O / l over both halves' row sums
-    if (!wait_bar(b, &b->o_done[qt], ou & 1)) { fail(b, a.err); return; }
+    const bool o_ok = __all_sync(0xffffffffu, wait_bar(b, &b->o_done[qt], ou & 1));
     ++ou;
     tc::tc_fence_after();
     xch[h * kM + t] = l;
-    pair_sync(qt);
+    if (pair_sync_any(qt, !o_ok)) { fail(b, a.err); return; }
     const float l_all = l + xch[(1 - h) * kM + t];
     pair_sync(qt);  // both have read before either writes the next tile's maximum
     const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
@@ -1077,6 +1116,7 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mbar_init(&b->o_done[i], 1);
     }
     tc::mbar_init(&b->drain, 1);
+    tc::mbar_init(&b->never, 1);
     for (int i = 0; i < kUnitRing; ++i) {
       tc::mbar_init(&b->unit_full[i], 1);
       tc::mbar_init(&b->unit_empty[i], kUnitReaders);
@@ -1521,8 +1561,9 @@ pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, floa
 // pic_link_attention_noalloc: the tensor-core attention with its planning and
 // merge scratch in one statically sized device array instead of a caller
 // workspace.  It runs the same kernels as pic_link_attention; it gives the
-// planner a smaller split budget (4 extra units per SM for at most 16 SMs) so
-// that the scratch a call needs stays small.
+// planner a smaller split budget (kUnitsPerSm extra units for each of at most
+// kFixedSplitSms SMs: 6 * 10 = 60 extra units) so that the scratch a call needs
+// stays small.
 
 constexpr size_t kFixedScratchBytes = (size_t)PIC_NOALLOC_SCRATCH_BYTES;
 
@@ -1532,15 +1573,20 @@ static __device__ __align__(256) uint8_t pic_fixed_scratch[kFixedScratchBytes];
 namespace pic {
 namespace {
 
-constexpr int kFixedSplitSms = 10;  // at most kUnitsPerSm * 10 = 60 split units in the fixed scratch
+constexpr int kFixedSplitSms = 10;  // at most kUnitsPerSm * kFixedSplitSms = 60 extra units in the fixed scratch
+static_assert(kUnitsPerSm * kFixedSplitSms == 60, "the split cap pic.h states");
 constexpr int kMaxDevices = 256;
 
 std::mutex g_fixed_mu;
 void* g_fixed_addr[kMaxDevices];  // device address of pic_fixed_scratch, per device ordinal
 
 // Device address of the scratch on the current device.  Looked up once per
-// device (cudaGetSymbolAddress with that device current); host code must never
-// hand the host-side name pic_fixed_scratch to a kernel.
+// device (cudaGetSymbolAddress with that device current) and kept for the life of
+// the process, so the library must not be used across a cudaDeviceReset (the
+// array may move when the device code is loaded again).  The lookup also loads
+// this file's device code on the device if that has not happened yet, which is
+// when the array is reserved.  Host code must never hand the host-side name
+// pic_fixed_scratch to a kernel.
 void* fixed_scratch_address() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
@@ -1571,7 +1617,10 @@ extern "C" pic_status pic_link_attention_noalloc(const void* q, const float* row
       (d & 1) || !(scale > 0.f))
     return PIC_ERR_INVALID;
   if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
-  if (n_req == 0 || n_rows == 0) return PIC_OK;
+  // A call without rows is the warm-up: it makes the current device load the
+  // library's device code (reserving the array) and looks up the array's address,
+  // so that neither happens later, after the caller has reserved HBM.
+  if (n_req == 0 || n_rows == 0) return fixed_scratch_address() != nullptr ? PIC_OK : PIC_ERR_CUDA;
   const bool tc = tc_shape(dtype, Hq, Hkv, d);
   // size check first: a call that needs more scratch than the array holds is refused before anything else
   if (tc && fixed_layout(n_rows, n_req, Hq / Hkv, Hkv, d).total > kFixedScratchBytes) return PIC_ERR_WORKSPACE;

@@ -69,6 +69,7 @@ struct CBars {
   uint64_t s_full[2][kSRing], s_empty[2][kSRing];  // per S ring slot
   uint64_t a_s, a_t;                         // A_S / A_T written for the next step
   uint64_t d_s, d_t;                         // the step's S / T products complete
+  uint64_t never;                            // no thread arrives on it (failure-injection test build)
   uint32_t tmem;
   int abort;
 };
@@ -257,6 +258,7 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
     tc::mbar_init(&cb->a_t, kCWorkers);
     tc::mbar_init(&cb->d_s, 1);
     tc::mbar_init(&cb->d_t, 1);
+    tc::mbar_init(&cb->never, 1);
     cb->abort = 0;
     tc::fence_mbar_init();
   }
@@ -348,7 +350,17 @@ compose_kernel(const __grid_constant__ CUtensorMap tmap, const Level lv) {
       // every commit's arrival lands before the CTA exits: the thread waits for the
       // last phase of each barrier it committed to
       int issued = 0, issued_t = 0;
-      for (int k = 0; k < n_steps; ++k) {
+      int steps = n_steps;
+#ifdef PIC_INJECT_WAIT_TIMEOUT
+      // Failure-injection test build only: a bounded wait on a barrier that nothing
+      // arrives on runs out, reports PIC_ERR_TIMEOUT and stops the CTA cleanly.
+      if (!tc::mbar_wait(&cb->never, 0, &cb->abort, PIC_INJECT_WAIT_TIMEOUT)) {
+        set_err(lv.err, PIC_ERR_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&cb->abort) = 1;
+        steps = 0;
+      }
+#endif
+      for (int k = 0; k < steps; ++k) {
         if (!wait_bar(&cb->b_full[k & 1], (k >> 1) & 1, cb, lv.err)) break;
         if (!wait_bar(&cb->a_s, k & 1, cb, lv.err)) break;
         tc::tc_fence_after();

@@ -168,6 +168,7 @@ struct DecSmem {
     float w_o[kDecWarps][G][kDecD];
   };
   uint64_t full[kDecStages], empty[kDecStages];
+  uint64_t never;                // no thread ever arrives on it (failure-injection test build)
   int meta[kDecStages];          // the stage's page: valid slots lo | hi << 8, or -1 when skipped
   __nv_bfloat16 qb[G][kDecD];    // Q of the g heads, roped and rounded to bf16
   float w_m[kDecWarps][G], w_l[kDecWarps][G];
@@ -233,6 +234,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       tc::mbar_init(&sm.full[st], 1);
       tc::mbar_init(&sm.empty[st], 1);
     }
+    tc::mbar_init(&sm.never, 1);
     sm.abort = 0;
     tc::fence_mbar_init();
   }
@@ -243,8 +245,19 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     // page entry one page ahead
     if (lane == 0) {
       int issued = 0;
+      int n_go = n;
+#ifdef PIC_INJECT_WAIT_TIMEOUT
+      // Failure-injection test build only: a bounded wait on a barrier that nothing
+      // arrives on runs out and reports PIC_ERR_TIMEOUT; the consumers then give up
+      // on their first page and every warp reaches the drained-ring barrier.
+      if (!tc::mbar_wait(&sm.never, 0, &sm.abort, PIC_INJECT_WAIT_TIMEOUT)) {
+        set_err(err, PIC_ERR_TIMEOUT);
+        *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+        n_go = 0;
+      }
+#endif
       int4 nxt = n > 0 ? __ldg(reinterpret_cast<const int4*>(pages) + pb) : make_int4(-1, -1, 0, 0);
-      for (int i = 0; i < n; ++i) {
+      for (int i = 0; i < n_go; ++i) {
         const int st = i % kDecStages;
         const int4 pg = nxt;
         if (i + 1 < n) nxt = __ldg(reinterpret_cast<const int4*>(pages) + pb + i + 1);
@@ -309,7 +322,10 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const int mr = lane & 7, mi = lane >> 3;
     for (int i = warp; i < n; i += kDecWarps) {
       const int st = i % kDecStages;
-      if (!tc::mbar_wait(&sm.full[st], (i / kDecStages) & 1, &sm.abort, kDecWaitNs)) {
+      // the outcome is made the same in every lane: the page's work is warp-wide
+      // (ldmatrix, mma.sync), so a warp must not go on with some lanes missing
+      const bool got = tc::mbar_wait(&sm.full[st], (i / kDecStages) & 1, &sm.abort, kDecWaitNs);
+      if (!__all_sync(0xffffffffu, got)) {
         if (lane == 0) {
           set_err(err, PIC_ERR_TIMEOUT);
           *reinterpret_cast<volatile int*>(&sm.abort) = 1;
