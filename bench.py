@@ -12,8 +12,13 @@ and ranks) per second of device time, the pool and inputs resident in HBM; L2 is
 flushed (512 MB read, untimed) before every timed step.  e2e = the same metric
 through the Python binding with per-step host->device copies of the step's inputs
 from pinned memory and a device->host copy of the attention output.
-`--impl reference` times the float64 CPU oracle on a bounded sample of the same
-workload on the host cores.
+`per_config` times the other workloads (the RAG prompt, the 20-chunk sink prompt,
+the 16-request batch) with the same step.  On rank 0 at N = 1 the float64 oracle
+then runs on the host cores, in full, on every workload: its time is
+`cpu_baseline` (headline) and `per_config[].oracle`, and its output gives the GPU
+outputs' parity errors (`parity`, `per_config[].parity`).
+`--impl reference` times the oracle on slices of the headline workload (see
+OracleSlices).
 """
 
 from __future__ import annotations
@@ -155,6 +160,82 @@ def whole_job_throughput(world: int, steps: int, tokens_per_rank_step: int, max_
 
 # ----------------------------------------------------------------------------- GPU arm
 
+# the pages' other prompt shapes, timed after the headline workload with the same step
+PER_CONFIG = ("rag_prompt_6chunks", "many_chunk_sink_20", "batched_shared_16req")
+
+
+def step_work(batch):
+    """Algorithmic work of one link step, from the step's own outputs: re-rotated
+    bytes (K read + written) and attention flops 4 d Hq sum(p_r + 1)."""
+    wl = batch.wl
+    rows = batch.rows.cpu().numpy().astype(np.int64)
+    rot = batch.rot.cpu().numpy()
+    lohi = np.ascontiguousarray(rot[:, 3]).view(np.int16).reshape(-1, 2) if len(rot) else np.zeros((0, 2), np.int16)
+    rot_tokens = int((lohi[:, 1].astype(np.int64) - lohi[:, 0]).sum())
+    el = 2 if wl.dtype == "bf16" else 4
+    return 2 * rot_tokens * wl.Hkv * wl.d * el, 4.0 * wl.d * wl.Hq * float((rows + 1).sum())
+
+
+def time_link(batch, steps, l2_flush, stream):
+    """Per-step CUDA-event times (ms) of `steps` link steps, L2 flushed before each:
+    (whole step, re-rotation pass, attention run)."""
+    import torch
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    step_ev = [(ev(), ev()) for _ in range(steps)]
+    rot_ev = [(ev(), ev()) for _ in range(steps)]
+    att_ev = [(ev(), ev()) for _ in range(steps)]
+    for i in range(steps):
+        l2_flush()
+        step_ev[i][0].record(stream)
+        batch.run(marks={"rerotate": rot_ev[i], "attention": att_ev[i]})
+        step_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return ([a.elapsed_time(b) for a, b in step_ev], [a.elapsed_time(b) for a, b in rot_ev],
+            [a.elapsed_time(b) for a, b in att_ev])
+
+
+def link_output(batch):
+    """The step's attention output from the pool as cached (the in-place re-rotation
+    of a repeated step would rotate K again), copied to the host."""
+    import torch
+    batch.reset_pool()
+    batch.err.zero_()
+    batch.run()
+    torch.cuda.synchronize()
+    if batch.error() != 0:
+        raise SystemExit(f"device error ({batch.wl.name}): {batch.error()}")
+    return batch.out.double().cpu().numpy()
+
+
+def per_config_gpu(name, steps, warmup, l2_flush, stream, hbm, tf_burst):
+    """One of the other workloads: mean step time, tokens/s, attention and
+    re-rotation roofline fractions, and the step's output (for the parity check)."""
+    import torch
+    from position_independent_kv_pic_gb300.link import LinkBatch
+    wl = _workload(name)
+    b = LinkBatch(wl)
+    for _ in range(warmup):
+        b.run()
+    torch.cuda.synchronize()
+    if b.error() != 0:
+        raise SystemExit(f"device error ({name}): {b.error()}")
+    rot_bytes, flops = step_work(b)
+    st, ro, at = time_link(b, steps, l2_flush, stream)
+    if b.error() != 0:
+        raise SystemExit(f"device error ({name}): {b.error()}")
+    ms, rms, ams = statistics.mean(st), statistics.mean(ro), statistics.mean(at)
+    entry = {"workload": name, "requests": b.n_req, "chunks": b.n_chunks, "tokens": b.tokens, "rows": b.n_rows,
+             "steps": steps, "ms_per_step": ms, "tokens_per_s": b.tokens / (ms / 1e3),
+             "attention": {"ms": ams, "tflops": flops / (ams / 1e3) / 1e12,
+                           "frac": flops / (ams / 1e3) / 1e12 / tf_burst, "flop": flops},
+             "rerotate": {"ms": rms, "gbs": rot_bytes / (rms / 1e3) / 1e9,
+                          "frac": rot_bytes / (rms / 1e3) / 1e9 / hbm, "bytes": rot_bytes}}
+    out = link_output(b)
+    del b
+    torch.cuda.empty_cache()
+    return entry, out
+
+
 def run_gpu(args, rank, world):
     import torch
     import torch.distributed as dist
@@ -188,38 +269,20 @@ def run_gpu(args, rank, world):
     if batch.error() != 0:
         raise SystemExit(f"device error: {pic.pic_strerror(batch.error())}")
 
-    # algorithmic work, from the step's own outputs
-    rows = batch.rows.cpu().numpy().astype(np.int64)
-    rot = batch.rot.cpu().numpy()
-    lohi = np.ascontiguousarray(rot[:, 3]).view(np.int16).reshape(-1, 2) if len(rot) else np.zeros((0, 2), np.int16)
-    rot_tokens = int((lohi[:, 1].astype(np.int64) - lohi[:, 0]).sum())
+    rot_bytes, attn_flops = step_work(batch)
     el = 2 if wl.dtype == "bf16" else 4
-    rot_bytes = 2 * rot_tokens * wl.Hkv * wl.d * el
-    attn_flops = 4.0 * wl.d * wl.Hq * float((rows + 1).sum())
-
     K = args.steps
     ev = lambda: torch.cuda.Event(enable_timing=True)
-    step_ev = [(ev(), ev()) for _ in range(K)]
-    rot_ev = [(ev(), ev()) for _ in range(K)]
-    att_ev = [(ev(), ev()) for _ in range(K)]
 
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_wall0 = time.perf_counter()
-        for i in range(K):
-            l2_flush()
-            step_ev[i][0].record(stream)
-            batch.run(marks={"rerotate": rot_ev[i], "attention": att_ev[i]})
-            step_ev[i][1].record(stream)
-        torch.cuda.synchronize()
+        step_ms, rot_ms, att_ms = time_link(batch, K, l2_flush, stream)
         t_wall = time.perf_counter() - t_wall0
     if world > 1:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in step_ev]
-    rot_ms = [a.elapsed_time(b) for a, b in rot_ev]
-    att_ms = [a.elapsed_time(b) for a, b in att_ev]
     if batch.error() != 0:
         raise SystemExit(f"device error: {pic.pic_strerror(batch.error())}")
 
@@ -348,6 +411,14 @@ def run_gpu(args, rank, world):
         torch.cuda.empty_cache()
 
     hbm, tf_burst, tf_sus, peak_kind = _peaks()
+    # the other workloads (rank 0 reports them; every rank runs the same work)
+    per_config, outputs = [], {}
+    if not args.no_per_config:
+        for name in PER_CONFIG:
+            entry, out = per_config_gpu(name, max(3, min(K, 20)), args.warmup, l2_flush, stream, hbm, tf_burst)
+            per_config.append(entry)
+            outputs[name] = out
+    outputs[wl.name] = link_output(batch)
     att_avg = statistics.mean(att_ms)
     rot_avg = statistics.mean(rot_ms)
     att_tflops = attn_flops / (att_avg / 1e3) / 1e12
@@ -417,93 +488,153 @@ def run_gpu(args, rank, world):
         "gpu_launches": K * batch.launches_per_step,
         "wall_s_timed_region": t_wall,
     }
-    return result, batch
+    if per_config:
+        result["per_config"] = per_config
+    return result, batch, outputs
 
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-class OracleSampler:
-    """The float64 oracle, as it stands, timed on a bounded sample of one step.
+def _oracle_inputs(wl):
+    """The workload's inputs as the oracle takes them, float64, one tuple per request
+    (chunks' stored K and V in link order, q, k, un-roped Q / K_new and V_new of the
+    request's recomputed rows).  Drawn from the same seeded generators as the GPU arm."""
+    import oracle.pic_oracle as O
+    from position_independent_kv_pic_gb300 import inputs
+    kst, vst, off = inputs.chunk_store(wl)
+    counts = [O.count_rows(wl.chunk_lens[r.chunk_ids], r.q, r.k) for r in wl.requests]
+    qr, kn, vn = (t.double().numpy() for t in inputs.row_inputs(wl, int(sum(counts))))
+    reqs, a = [], 0
+    for req, n in zip(wl.requests, counts):
+        ck = [kst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
+        cv = [vst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
+        reqs.append((ck, cv, req.q, req.k, qr[a:a + n], kn[a:a + n], vn[a:a + n]))
+        a += n
+    return reqs
 
-    Set-up (untimed): draw the workload's inputs and build the spliced context of
-    up to two requests with the oracle.  A sample re-runs the oracle's re-rotation
-    on a few chunks and its attention on a few recomputed rows, and extrapolates to
-    the whole step by re-rotated tokens and by sum(p + 1) over rows."""
 
-    def __init__(self, wl):
+def oracle_step(wl, reqs, threads=None):
+    """The float64 oracle, as it stands, on the whole link step of every request (row
+    selection, splice with the re-rotation of every chunk, fresh K/V, attention of
+    every recomputed row).  Returns (seconds, output rows [n_rows][Hq][d])."""
+    import torch
+
+    import oracle.pic_oracle as O
+    prev = torch.get_num_threads()
+    if threads:
+        torch.set_num_threads(threads)
+    try:
+        t0 = time.perf_counter()
+        outs = [O.link_request(*r, wl.theta, wl.dtype)["out"] for r in reqs]
+        dt = time.perf_counter() - t0
+    finally:
+        torch.set_num_threads(prev)
+    return dt, np.concatenate(outs) if outs else np.zeros((0, wl.Hq, wl.d))
+
+
+def timed_oracle(wl, reqs, threads=None, reps=3):
+    """One untimed warm-up, then the median of `reps` whole-step runs (the KV-cache
+    blog's timing method: warm-ups, then the median).  Returns (seconds, output)."""
+    _, out = oracle_step(wl, reqs, threads)
+    ts = [oracle_step(wl, reqs, threads)[0] for _ in range(reps)]
+    return statistics.median(ts), out
+
+
+def parity_errors(gpu_out, ref):
+    e = np.abs(gpu_out - ref)
+    return {"max_abs": float(e.max()) if e.size else 0.0, "mean_abs": float(e.mean()) if e.size else 0.0,
+            "tol_max_abs": 2e-2, "tol_mean_abs": 2e-3, "rows": int(ref.shape[0])}
+
+
+def cpu_legs(result, wl, outputs):
+    """rank 0, N = 1: the oracle timed on the host cores, in full (no sampling), and
+    the GPU outputs' errors against it.  Headline workload: one whole-step run on
+    all cores.  Other workloads: all cores and one core, 1 warm-up + median of 3
+    (the 16-request batch, about 2e12 float64 flop: one all-core run)."""
+    import torch
+    threads = torch.get_num_threads()
+    host = {"threads": threads, "cpu_count": os.cpu_count()}
+    t, ref = oracle_step(wl, _oracle_inputs(wl))
+    result["cpu_baseline"] = {
+        "value": wl.total_tokens() / t, "unit": UNIT, "cores": threads, "kind": "oracle", "seconds": t,
+        "sample": f"the whole step of {wl.name} (all {ref.shape[0]} recomputed rows, every chunk re-rotated; no "
+                  f"sampling, no extrapolation), one run on {threads} threads"}
+    result["parity"] = {wl.name: parity_errors(outputs[wl.name], ref)}
+    for entry in result.get("per_config", []):
+        name = entry["workload"]
+        cwl = _workload(name)
+        reqs = _oracle_inputs(cwl)
+        if name == "batched_shared_16req":
+            t_all, ref = oracle_step(cwl, reqs)
+            orc = {"all_cores_s": t_all, "runs": "one", **host}
+        else:
+            t_all, ref = timed_oracle(cwl, reqs)
+            t_one, _ = timed_oracle(cwl, reqs, threads=1)
+            orc = {"all_cores_s": t_all, "one_core_s": t_one, "runs": "1 warm-up + median of 3", **host,
+                   "one_core_tokens_per_s": entry["tokens"] / t_one}
+        orc["all_cores_tokens_per_s"] = entry["tokens"] / t_all
+        orc["gpu_speedup_all_cores"] = t_all / (entry["ms_per_step"] / 1e3)
+        entry["oracle"] = orc
+        entry["parity"] = parity_errors(outputs[name], ref)
+        del reqs, ref
+
+
+class OracleSlices:
+    """`--impl reference`: the float64 oracle, as it stands, on slices of the link step.
+
+    Set-up (untimed): the workload's inputs and the oracle's spliced context of every
+    request.  Slice i of m: the oracle's re-rotation of the chunks c >= 1 with
+    c = i (mod m) and its attention on the recomputed rows j = i (mod m) of every
+    request.  A slice is timed whole and credited with 1/m of the step's context
+    tokens, so ms_per_step is the time the slice really took."""
+
+    def __init__(self, wl, m=8):
+        import torch
+
         import oracle.pic_oracle as O
-        from position_independent_kv_pic_gb300 import inputs
-        self.O, self.wl = O, wl
-        kst, vst, off = inputs.chunk_store(wl)
+        self.O, self.wl, self.m = O, wl, m
+        self.threads = torch.get_num_threads()
         self.reqs = []
-        self.n_used = min(len(wl.requests), 2)
-        for req in wl.requests[:self.n_used]:
-            ck = [kst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
-            cv = [vst[off[c]:off[c + 1]].double().numpy() for c in req.chunk_ids]
-            n = O.count_rows(wl.chunk_lens[req.chunk_ids], req.q, req.k)
-            qr, kn, vn = (t.double().numpy() for t in inputs.row_inputs(wl, n))
-            K, V, rows, starts, T = O.splice_context(ck, cv, req.q, req.k, kn, vn, wl.theta, wl.dtype)
-            q_rot = O.round_to(O.rope(qr, rows, wl.theta), wl.dtype)
-            fixed = []
-            for _ in range(3):
-                t0 = time.perf_counter()
-                O.attention_rows(q_rot, rows, K, V, 1.0 / np.sqrt(wl.d), which=[])
-                fixed.append(time.perf_counter() - t0)
-            self.reqs.append(dict(ck=ck, K=K, V=V, rows=rows, starts=starts, q_rot=q_rot,
-                                  rot_tokens=sum(len(c) for c in ck[1:]), t_fixed=statistics.median(fixed)))
-        self.threads = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+        for ck, cv, q, k, qr, kn, vn in _oracle_inputs(wl):
+            K, V, rows, starts, _ = O.splice_context(ck, cv, q, k, kn, vn, wl.theta, wl.dtype)
+            q_rot = O.round_to(O.rope(qr, rows, wl.theta), wl.dtype) if len(rows) else None
+            self.reqs.append((ck, starts, rows, q_rot, K, V))
 
-    def sample(self, n_chunks, n_rows, seed=0):
-        """Seconds the oracle would need for the whole step, from one bounded sample."""
-        O, wl = self.O, self.wl
-        rng = np.random.default_rng(seed)
-        full = 0.0
-        for r in self.reqs:
-            ck, rows = r["ck"], r["rows"]
-            cs = rng.choice(np.arange(1, len(ck)), size=min(n_chunks, len(ck) - 1), replace=False) \
-                if len(ck) > 1 else []
-            t0 = time.perf_counter()
-            for c in cs:
-                O.rerotate_k(ck[c], int(r["starts"][c]), wl.theta, wl.dtype)
-            t_rot = time.perf_counter() - t0
-            s_tok = sum(len(ck[c]) for c in cs)
-            n = len(rows)
-            which = sorted(rng.choice(n, size=min(n_rows, n), replace=False).tolist()) if n else []
-            # the oracle's attention pays a fixed cost per call (it lays out the whole
-            # context per KV head, timed at set-up) and then a cost per row: only the
-            # per-row part is scaled from the sampled rows to all rows
-            t_fixed = r["t_fixed"]
-            t0 = time.perf_counter()
-            O.attention_rows(r["q_rot"], rows, r["K"], r["V"], 1.0 / np.sqrt(wl.d), which=which)
-            t_att = time.perf_counter() - t0
-            per_rows = max(t_att - t_fixed, 0.0) * n / max(len(which), 1)
-            full += t_rot * r["rot_tokens"] / max(s_tok, 1) + t_fixed + per_rows
-        return full * len(wl.requests) / self.n_used
+    def run(self, i):
+        O, wl, m = self.O, self.wl, self.m
+        t0 = time.perf_counter()
+        for ck, starts, rows, q_rot, K, V in self.reqs:
+            for c in range(1, len(ck)):
+                if c % m == i % m:
+                    O.rerotate_k(ck[c], int(starts[c]), wl.theta, wl.dtype)
+            which = list(range(i % m, len(rows), m))
+            if which:
+                O.attention_rows(q_rot, rows, K, V, 1.0 / np.sqrt(wl.d), which=which)
+        return time.perf_counter() - t0
 
-    def describe(self, n_chunks, n_rows):
-        return (f"float64 oracle as it stands: re-rotation of {n_chunks} random chunks and attention of {n_rows} "
-                f"uniformly drawn recomputed rows per request (first {self.n_used} request(s)); re-rotation "
-                f"extrapolated by re-rotated tokens, attention as its fixed per-call cost (median of 3 calls without rows, "
-                f"at set-up) plus the "
-                f"per-row cost scaled by row count; spliced context built once, untimed")
+    def describe(self):
+        return (f"float64 oracle as it stands on 1/{self.m} slices of the step: re-rotation of every "
+                f"{self.m}-th chunk and attention of every {self.m}-th recomputed row of each request (offset "
+                f"cycling over steps); each slice timed whole and credited with 1/{self.m} of the context "
+                f"tokens; spliced context built once, untimed; {self.threads} threads")
 
 
 def run_reference(args):
     wl = _workload(args.workload)
     tokens = wl.total_tokens()
-    sampler = OracleSampler(wl)
+    sl = OracleSlices(wl)
     for i in range(args.warmup):
-        sampler.sample(1, 1, seed=1000 + i)
-    times = [sampler.sample(1, 1, seed=i) for i in range(args.steps)]
+        sl.run(i)
+    times = [sl.run(args.warmup + i) for i in range(args.steps)]
     step_s = statistics.mean(times)
-    value = tokens / step_s
+    value = tokens / sl.m / step_s
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded inputs as the GPU arm)",
-        "config": {"workload": wl.name, "tokens": tokens},
-        "cpu_baseline": {"value": value, "unit": UNIT, "cores": sampler.threads, "kind": "oracle",
-                         "sample": sampler.describe(1, 1) + f"; mean over {args.steps} samples"},
+        "config": {"workload": wl.name, "tokens": tokens, "tokens_per_step": tokens / sl.m},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": sl.threads, "kind": "oracle",
+                         "sample": sl.describe() + f"; mean over {args.steps} slices"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -516,6 +647,7 @@ def main():
     ap.add_argument("--workload", default="long_context_100x1000")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true", help="time the headline workload only")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -531,13 +663,10 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    result, batch = run_gpu(args, rank, world)
+    result, batch, outputs = run_gpu(args, rank, world)
     if rank == 0:
-        if not args.no_cpu_baseline:
-            sampler = OracleSampler(batch.wl)
-            full = statistics.mean(sampler.sample(8, 8, seed=i) for i in range(3))
-            result["cpu_baseline"] = {"value": batch.tokens / full, "unit": UNIT, "cores": sampler.threads,
-                                      "kind": "oracle", "sample": sampler.describe(8, 8) + "; mean of 3 samples"}
+        if not args.no_cpu_baseline and world == 1:
+            cpu_legs(result, batch.wl, outputs)
         print(json.dumps(result), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -914,15 +914,20 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
   float* xch = reinterpret_cast<float*>(smem + kOffXch) + qt * 2 * kM;  // [half][row]
   const int hg = t / a.R, i = t % a.R;
   uint32_t c = 0, ou = 0;  // tiles / units this warpgroup worked on
-  for (uint32_t k = 0;; ++k) {
-    const int u = read_unit_warp(b, k);
-    // both warpgroups of the Q tile read the same unit sequence; they give up together
-    if (pair_sync_any(qt, u < 0)) { fail(b, a.err); return; }
-    if (u >= n_units) break;
+  // Both warpgroups of the Q tile read the same unit sequence and give up together:
+  // whether every one of them got unit k + 1 is agreed at the last pair barrier of
+  // unit k (the first unit: at a barrier of its own).
+  int u = read_unit_warp(b, 0);
+  if (pair_sync_any(qt, u < 0)) { fail(b, a.err); return; }
+  for (uint32_t k = 0; u < n_units; ++k) {
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
     const int n = un.kt1 - un.kt0;
-    if (qt == 1 && tm.n_rows <= a.R) continue;  // no rows for this Q tile: no barrier traffic
+    if (qt == 1 && tm.n_rows <= a.R) {  // no rows for this Q tile: only the next unit
+      u = read_unit_warp(b, k + 1);
+      if (pair_sync_any(qt, u < 0)) { fail(b, a.err); return; }
+      continue;
+    }
     const int loc = qt * a.R + i;
     const bool row_ok = loc < tm.n_rows;
     const int row = tm.row0 + (row_ok ? loc : 0);
@@ -963,20 +968,17 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
         }
       }
 
-      // a warp that gave up skips its TMEM read and meets its partner at the pair barrier below
-      const bool s_ok = __all_sync(0xffffffffu, wait_bar(b, &b->s_full[qt], c & 1));
+      // A thread whose wait gave up goes on to the pair barrier below (reading S
+      // regardless: a stale TMEM read is harmless, and the warp stays converged for
+      // the warp-wide load), where both warpgroups of the Q tile learn of it and leave.
+      const bool s_ok = wait_bar(b, &b->s_full[qt], c & 1);
       tc::tc_fence_after();
       float s[64];
       {
         uint32_t sr[64];
-        if (s_ok) {
-          tc::tmem_ld32(tS + 64 * h, sr);
-          tc::tmem_ld32(tS + 64 * h + 32, sr + 32);
-          tc::tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int k2 = 0; k2 < 64; ++k2) sr[k2] = 0u;
-        }
+        tc::tmem_ld32(tS + 64 * h, sr);
+        tc::tmem_ld32(tS + 64 * h + 32, sr + 32);
+        tc::tmem_ld_wait();
         tc::reg_fence<64>(sr);
 #pragma unroll
         for (int k2 = 0; k2 < 64; ++k2) s[k2] = u2f(sr[k2]);
@@ -1051,13 +1053,15 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       if (lane == 0) tc::mbar_arrive(&b->p_full[qt]);
     }
     // epilogue: O / l over both halves' row sums
-    const bool o_ok = __all_sync(0xffffffffu, wait_bar(b, &b->o_done[qt], ou & 1));
+    const bool o_ok = wait_bar(b, &b->o_done[qt], ou & 1);
     ++ou;
     tc::tc_fence_after();
     xch[h * kM + t] = l;
     if (pair_sync_any(qt, !o_ok)) { fail(b, a.err); return; }
     const float l_all = l + xch[(1 - h) * kM + t];
-    pair_sync(qt);  // both have read before either writes the next tile's maximum
+    // both have read before either writes the next tile's maximum; the next unit agreed
+    const int u_next = read_unit_warp(b, k + 1);
+    if (pair_sync_any(qt, u_next < 0)) { fail(b, a.err); return; }
     const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
     const int64_t slot = ((int64_t)(un.part < 0 ? 0 : un.part) * kQTiles + qt) * kM + t;
 #pragma unroll 1
@@ -1086,6 +1090,7 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
     }
     tc::tc_fence_before();
     if (h == 0 && row_ok && un.part >= 0) a.part_ml[slot] = make_float2(m_ref, l_all);
+    u = u_next;
   }
 }
 
