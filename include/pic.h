@@ -68,12 +68,32 @@ typedef enum {
 typedef enum { PIC_BF16 = 0, PIC_FP32 = 1 } pic_dtype;
 
 #define PIC_PAGE 16 /* tokens per KV page (block) */
+#define PIC_TILE_PAGES 8 /* pages per key tile of the tensor-core attention (128 keys) */
+
+/* How a request's link page list is laid out (pic_request_sizes_of,
+ * pic_plan_offsets, pic_splice_pages):
+ *   PIC_LAYOUT_SPLICED  the chunks' pages back to back at their global positions;
+ *                       every key the attention reads is encoded at its global
+ *                       position (rotary correction by pic_rerotate_k, or scheme B
+ *                       by pic_rope_cached_k).
+ *   PIC_LAYOUT_FRAMED   for rotate-on-read: every chunk's run of pages (its fresh
+ *                       head pages, then its cached pages) is padded with empty
+ *                       entries to a whole number of key tiles (PIC_TILE_PAGES), so
+ *                       that every key tile lies in one chunk; each chunk's keys stay
+ *                       in the chunk's own frame (encoded at positions local to the
+ *                       chunk: the cached pages as cached, the recomputed head rows
+ *                       at their position within the chunk); chunk 0 and the query
+ *                       are in the global frame (their local and global positions
+ *                       coincide, or the query's fresh K is at its global position). */
+typedef enum { PIC_LAYOUT_SPLICED = 0, PIC_LAYOUT_FRAMED = 1 } pic_layout;
 
 /* One entry of a request's spliced context: 16 key slots at global positions
  * gpos0 .. gpos0+15, of which slots [lo, hi) are valid.  K comes from block
  * k_block of the K pool and V from block v_block of the V pool (they differ
  * when K was rotated out of place while V stays shared).  A request's entries
- * are sorted by gpos0 + lo (strictly increasing).  16 bytes. */
+ * are sorted by gpos0 + lo: strictly increasing over entries with valid slots;
+ * an empty entry (lo == hi, blocks -1: the padding of the framed layout) carries
+ * the gpos0 of the next chunk's start.  16 bytes. */
 typedef struct {
   int32_t k_block;
   int32_t v_block;
@@ -117,20 +137,24 @@ int64_t pic_count_rows(const int32_t* chunk_lens_host, int32_t n_chunks, int32_t
  *   recomputed head rows (m_c = min(k, L_c) for c >= 1, 0 for c = 0), then the
  *   chunk's cached pages j that keep at least one slot (valid slots
  *   [max(0, m_c - 16j), min(16, L_c - 16j))); finally ceil(q/16) fresh query pages.
+ *   In PIC_LAYOUT_FRAMED every chunk's fresh + cached pages are followed by empty
+ *   entries up to a multiple of PIC_TILE_PAGES (link_pages counts them).
  *   rot pages: the kept cached pages of chunks c >= 1 (chunk 0 has Delta = 0).
  *   fresh pages: the fresh link pages above, in the same order.
- * Returns PIC_ERR_INVALID on the same conditions as pic_count_rows. */
+ * Returns PIC_ERR_INVALID on the same conditions as pic_count_rows, or for an
+ * unknown layout. */
 pic_status pic_request_sizes_of(const int32_t* chunk_lens_host, int32_t n_chunks, int32_t q,
-                                int32_t k, pic_request_sizes* out);
+                                int32_t k, pic_layout layout, pic_request_sizes* out);
 
 /* Exclusive prefix offsets over n_req requests, from host copies of the
  * metadata: row_off, page_off, rot_off, fresh_off and chunk_page_off receive
  * n_req+1 (chunk_page_off: n_chunks_total+1) entries; any output may be NULL.
  * chunk_page_off[c] is the first page of chunk c in a per-chunk page table that
- * gives every chunk ceil(L_c/16) pages.  Returns PIC_ERR_INVALID on bad input. */
+ * gives every chunk ceil(L_c/16) pages.  page_off follows `layout` (the framed
+ * layout's padding included).  Returns PIC_ERR_INVALID on bad input. */
 pic_status pic_plan_offsets(const int32_t* chunk_lens_host, const int32_t* chunk_off_host,
                             const int32_t* q_len_host, const int32_t* k_host, int32_t n_req,
-                            int32_t* row_off_host, int32_t* page_off_host,
+                            pic_layout layout, int32_t* row_off_host, int32_t* page_off_host,
                             int32_t* rot_off_host, int32_t* fresh_off_host,
                             int32_t* chunk_page_off_host);
 
@@ -171,15 +195,25 @@ pic_status pic_select_rows(const int32_t* chunk_lens, const int32_t* chunk_off,
  *   v_blocks        same shape: V-pool block of each chunk page (never written)
  *   fresh_off       [n_req+1] CSR into fresh_blocks
  *   fresh_blocks    block ids (same id in the K and V pools) for recomputed rows
- *   page_off, rot_off [n_req+1] from pic_plan_offsets
+ *   page_off, rot_off [n_req+1] from pic_plan_offsets (with the same layout)
+ *   layout  PIC_LAYOUT_SPLICED, or PIC_LAYOUT_FRAMED for rotate-on-read (each
+ *                 chunk's run padded to whole key tiles with entries {-1, -1,
+ *                 next chunk's start, 0, 0}; k_dst_blocks must be NULL)
  *   pages   out [page_off[n_req]]   link page lists (gpos0 global)
  *   rot     out [rot_off[n_req]]    re-rotation work (tab = flat chunk index)
  *   row_block, row_slot out [n_rows]: pool block and slot of each recomputed row
  *                 (row order as written by pic_select_rows; row_off gives n_rows)
+ *   row_frame_pos out [n_rows] or NULL: the position at which each recomputed
+ *                 row's fresh K is to be encoded: its global position in the
+ *                 spliced layout; in the framed layout its position within its
+ *                 chunk (seam rows of chunks c >= 1) or its global position
+ *                 (query rows).  pic_rope_table over it gives the table for
+ *                 pic_write_fresh_kv.
  *   page_tab out [page_off[n_req]] or NULL: per link page, the offset-table row
- *                 that rotates its K to the global position (the flat chunk index
- *                 for cached pages of chunks after the first), -1 for pages that
- *                 need none (chunk 0, fresh and query pages); the input of
+ *                 of the page's frame: the flat chunk index for the pages of a
+ *                 chunk after the first (in the framed layout its fresh pages and
+ *                 padding too), -1 for pages in the global frame (chunk 0, query
+ *                 pages; fresh pages in the spliced layout); the input of
  *                 pic_link_attention_ror
  *   row_off [n_req+1]
  * With k_dst_blocks NULL the cached pages of the list are the cached blocks
@@ -192,9 +226,10 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
                             const int32_t* k_src_blocks, const int32_t* k_dst_blocks,
                             const int32_t* v_blocks, const int32_t* fresh_off,
                             const int32_t* fresh_blocks, const int32_t* row_off,
-                            const int32_t* page_off, const int32_t* rot_off,
+                            const int32_t* page_off, const int32_t* rot_off, pic_layout layout,
                             pic_link_page* pages, pic_rot_page* rot, int32_t* row_block,
-                            int32_t* row_slot, int32_t* page_tab, int32_t* err_flag, pic_stream_t stream);
+                            int32_t* row_slot, int32_t* row_frame_pos, int32_t* page_tab,
+                            int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * a2  RoPE tables (RoPE article 2.2 and footnote 3).
@@ -413,6 +448,14 @@ pic_status pic_link_attention_ror(const void* q, const float* row_table, const i
  *   q_table   [n_req][d/2][4] fp32: pic_rope_table over the positions P_r
  *   k_pool, v_pool, num_blocks, pages, page_off: as pic_link_attention (the
  *             lo/hi slot range of every page entry is honoured; gpos0 is unused)
+ *   page_tab, rot_table, n_tab: NULL / NULL / 0 when every listed key is encoded
+ *             at its global position (the spliced layout).  After a rotate-on-read
+ *             link (the framed layout) the page list's page_tab from
+ *             pic_splice_pages (-1 for the new row's own page) and the offset table
+ *             of pic_link_attention_ror: the keys of a page with row f >= 0 are in
+ *             that chunk's frame, and the consumer rotates Q back by its offset,
+ *             R(-theta * Delta_f) RoPE(q, P), rounded to bf16, for them.  A row
+ *             >= n_tab sets PIC_ERR_RANGE and the page is read in the global frame
  *   out       [n_req][Hq][d] bf16
  *   ws        at least pic_decode_workspace() bytes, 256-byte aligned, any contents
  * bf16 pools with d = 128 and g = Hq / Hkv in {1, 2, 4, 8}; otherwise
@@ -429,9 +472,10 @@ size_t pic_decode_workspace(int32_t n_req, int32_t Hq, int32_t Hkv, int32_t d, p
 
 pic_status pic_decode_attention(const void* q, const float* q_table, const void* k_pool,
                                 const void* v_pool, int64_t num_blocks, pic_dtype dtype,
-                                const pic_link_page* pages, const int32_t* page_off, int32_t n_req,
-                                int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out, void* ws,
-                                size_t ws_bytes, int32_t* err_flag, pic_stream_t stream);
+                                const pic_link_page* pages, const int32_t* page_off,
+                                const int32_t* page_tab, const float* rot_table, int64_t n_tab,
+                                int32_t n_req, int32_t Hq, int32_t Hkv, int32_t d, float scale, void* out,
+                                void* ws, size_t ws_bytes, int32_t* err_flag, pic_stream_t stream);
 
 /* ------------------------------------------------------------------------
  * Linear-layer state composition (HYPIC blog, section 2.1: linear layers).

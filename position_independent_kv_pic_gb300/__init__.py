@@ -18,7 +18,8 @@ import numpy as np
 __all__ = [
     "load", "library_path", "PicError", "PIC_OK", "PIC_ERR_INVALID", "PIC_ERR_CUDA",
     "PIC_ERR_UNSUPPORTED", "PIC_ERR_TIMEOUT", "PIC_ERR_RANGE", "PIC_ERR_WORKSPACE",
-    "PIC_BF16", "PIC_FP32", "PIC_PAGE", "LINK_PAGE_DTYPE", "ROT_PAGE_DTYPE",
+    "PIC_BF16", "PIC_FP32", "PIC_PAGE", "PIC_TILE_PAGES", "PIC_LAYOUT_SPLICED", "PIC_LAYOUT_FRAMED",
+    "LINK_PAGE_DTYPE", "ROT_PAGE_DTYPE",
     "pic_count_rows", "pic_request_sizes_of", "pic_plan_offsets", "pic_strerror",
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
@@ -32,6 +33,8 @@ PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
 PIC_ERR_TIMEOUT, PIC_ERR_RANGE, PIC_ERR_WORKSPACE = 4, 5, 6
 PIC_BF16, PIC_FP32 = 0, 1
 PIC_PAGE = 16
+PIC_TILE_PAGES = 8
+PIC_LAYOUT_SPLICED, PIC_LAYOUT_FRAMED = 0, 1
 PIC_NOALLOC_SCRATCH_BYTES = 32 << 20
 
 # numpy views of the 16-byte structs of pic.h
@@ -78,12 +81,12 @@ _I32, _I64, _F32, _F64, _SZ = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ct
 
 _SIGS = {
     "pic_count_rows": (_I64, [_P, _I32, _I32, _I32]),
-    "pic_request_sizes_of": (ctypes.c_int, [_P, _I32, _I32, _I32, ctypes.POINTER(_Sizes)]),
-    "pic_plan_offsets": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P]),
+    "pic_request_sizes_of": (ctypes.c_int, [_P, _I32, _I32, _I32, ctypes.c_int, ctypes.POINTER(_Sizes)]),
+    "pic_plan_offsets": (ctypes.c_int, [_P, _P, _P, _P, _I32, ctypes.c_int, _P, _P, _P, _P, _P]),
     "pic_strerror": (ctypes.c_char_p, [ctypes.c_int]),
     "pic_select_rows": (ctypes.c_int, [_P, _P, _P, _P, _P, _I32, _P, _P, _P, _P]),
     "pic_splice_pages": (ctypes.c_int, [_P, _P, _P, _P, _I32, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
-                                        _P, _P, _P, _P, _P, _P, _P]),
+                                        ctypes.c_int, _P, _P, _P, _P, _P, _P, _P, _P]),
     "pic_rope_table": (ctypes.c_int, [_P, _I64, _I32, _F64, _P, _P]),
     "pic_rerotate_k": (ctypes.c_int, [_P, _I64, ctypes.c_int, _I32, _I32, _P, _I64, _P, _I64, _P, _P]),
     "pic_write_fresh_kv": (ctypes.c_int, [_P, _P, _I64, ctypes.c_int, _I32, _I32, _P, _P, _P, _P, _P,
@@ -108,8 +111,8 @@ _SIGS = {
     "pic_compose_workspace": (_SZ, [_I32, _I32, _I32, _I32, _I32]),
     "pic_compose_states": (ctypes.c_int, [_P, _P, _I64, _P, _P, _I32, _I64, _I32, _I32, _I32, _I32, _P, _P, _SZ,
                                           _P, _P]),
-    "pic_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32, _I32, _I32, _I32,
-                                            _F32, _P, _P, _SZ, _P, _P]),
+    "pic_decode_attention": (ctypes.c_int, [_P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _P, _P, _I64, _I32, _I32,
+                                            _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
 }
 
 
@@ -165,21 +168,23 @@ def pic_count_rows(chunk_lens_host, q: int, k: int) -> int:
     return int(load().pic_count_rows(_ptr(a), len(a), int(q), int(k)))
 
 
-def pic_request_sizes_of(chunk_lens_host, q: int, k: int) -> dict:
+def pic_request_sizes_of(chunk_lens_host, q: int, k: int, layout: int = 0) -> dict:
     a = _host_i32(chunk_lens_host)
     s = _Sizes()
-    _check(load().pic_request_sizes_of(_ptr(a), len(a), int(q), int(k), ctypes.byref(s)), "pic_request_sizes_of")
+    _check(load().pic_request_sizes_of(_ptr(a), len(a), int(q), int(k), int(layout), ctypes.byref(s)),
+           "pic_request_sizes_of")
     return {f: int(getattr(s, f)) for f, _ in _Sizes._fields_}
 
 
-def pic_plan_offsets(chunk_lens_host, chunk_off_host, q_len_host, k_host) -> dict:
+def pic_plan_offsets(chunk_lens_host, chunk_off_host, q_len_host, k_host, layout: int = 0) -> dict:
     """Host offsets (row_off, page_off, rot_off, fresh_off, chunk_page_off) as int32 arrays."""
     lens, coff = _host_i32(chunk_lens_host), _host_i32(chunk_off_host)
     ql, kk = _host_i32(q_len_host), _host_i32(k_host)
     n_req = len(ql)
     outs = {n: np.zeros(n_req + 1, np.int32) for n in ("row_off", "page_off", "rot_off", "fresh_off")}
     outs["chunk_page_off"] = np.zeros(len(lens) + 1, np.int32)
-    _check(load().pic_plan_offsets(_ptr(lens), _ptr(coff), _ptr(ql), _ptr(kk), n_req, _ptr(outs["row_off"]),
+    _check(load().pic_plan_offsets(_ptr(lens), _ptr(coff), _ptr(ql), _ptr(kk), n_req, int(layout),
+                                   _ptr(outs["row_off"]),
                                    _ptr(outs["page_off"]), _ptr(outs["rot_off"]), _ptr(outs["fresh_off"]),
                                    _ptr(outs["chunk_page_off"])), "pic_plan_offsets")
     return outs
@@ -199,13 +204,13 @@ def pic_select_rows(chunk_lens, chunk_off, q_len, k, row_off, rows, chunk_start,
 
 def pic_splice_pages(chunk_lens, chunk_off, q_len, k, chunk_start, chunk_page_off, k_src_blocks, k_dst_blocks,
                      v_blocks, fresh_off, fresh_blocks, row_off, page_off, rot_off, pages, rot, row_block,
-                     row_slot, err_flag, stream=None, page_tab=None):
+                     row_slot, err_flag, stream=None, page_tab=None, layout: int = 0, row_frame_pos=None):
     n_req = q_len.numel()
     _check(load().pic_splice_pages(
         _ptr(chunk_lens), _ptr(chunk_off), _ptr(q_len), _ptr(k), n_req, _ptr(chunk_start), _ptr(chunk_page_off),
         _ptr(k_src_blocks), _ptr(k_dst_blocks), _ptr(v_blocks), _ptr(fresh_off), _ptr(fresh_blocks), _ptr(row_off),
-        _ptr(page_off), _ptr(rot_off), _ptr(pages), _ptr(rot), _ptr(row_block), _ptr(row_slot), _ptr(page_tab),
-        _ptr(err_flag), _stream(stream)), "pic_splice_pages")
+        _ptr(page_off), _ptr(rot_off), int(layout), _ptr(pages), _ptr(rot), _ptr(row_block), _ptr(row_slot),
+        _ptr(row_frame_pos), _ptr(page_tab), _ptr(err_flag), _stream(stream)), "pic_splice_pages")
 
 
 def pic_rope_table(pos, d: int, theta: float, table, stream=None):
@@ -249,12 +254,15 @@ def pic_decode_workspace(n_req: int, Hq: int, Hkv: int, d: int, dtype: int) -> i
 
 
 def pic_decode_attention(q, q_table, k_pool, v_pool, dtype: int, pages, page_off, n_req: int, Hq: int, Hkv: int,
-                         d: int, scale: float, out, ws, err_flag, stream=None):
+                         d: int, scale: float, out, ws, err_flag, stream=None, page_tab=None, rot_table=None):
+    """page_tab / rot_table: the page frames and offset table of a rotate-on-read link (None: every key is
+    at its global position)."""
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    n_tab = 0 if rot_table is None else rot_table.shape[0]
     _check(load().pic_decode_attention(
         _ptr(q), _ptr(q_table), _ptr(k_pool), _ptr(v_pool), k_pool.shape[0], int(dtype), _ptr(pages), _ptr(page_off),
-        int(n_req), int(Hq), int(Hkv), int(d), float(scale), _ptr(out), _ptr(ws), ws_bytes, _ptr(err_flag),
-        _stream(stream)), "pic_decode_attention")
+        _ptr(page_tab), _ptr(rot_table), int(n_tab), int(n_req), int(Hq), int(Hkv), int(d), float(scale), _ptr(out),
+        _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)), "pic_decode_attention")
 
 
 def pic_link_attention_plan(q, row_table, rows, row_off, pages, page_off, n_req: int, n_rows: int, Hq: int,

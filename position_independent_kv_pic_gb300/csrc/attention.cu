@@ -381,8 +381,9 @@ struct TcArgs {
   int64_t num_blocks;
   int Hq, Hkv, G, R;
   float scale_log2;
-  // rotate-on-read (page_tab != nullptr): K of page p is rotated by table row
-  // page_tab[p] (none when negative) in shared memory before the S product
+  // rotate-on-read (page_tab != nullptr): the keys of page p sit in the frame of
+  // offset-table row page_tab[p] (the global frame when negative); all pages of a
+  // key tile share one frame (the framed layout), and Q is rotated into it
   const int32_t* page_tab;
   const float4* rot_tab;  // [n_tab][kD / 2] {cos_hi, sin_hi, cos_lo, sin_lo}
   int64_t n_tab;
@@ -397,6 +398,9 @@ struct Bars {
   // global positions when rotating on read, V's invalid rows zeroed
   uint64_t vz_done[kSlots];
   uint64_t q_full[kQTiles], q_free[kQTiles], s_full[kQTiles], p_full[kQTiles], o_done[kQTiles], drain;
+  // rotate-on-read: Q tile i written in shared memory for the frame of its next key
+  // tiles by its two softmax warpgroups (the MMA issuer waits for it at frame changes)
+  uint64_t q_ready[kQTiles];
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
   uint64_t never;  // no thread ever arrives on it (the failure-injection test build waits on it)
   int unit_idx[kUnitRing];
@@ -461,9 +465,22 @@ __device__ __forceinline__ int4 load_page(const pic_link_page* pages, int p, int
   return make_int4(-1, -1, 0, 0);
 }
 
+// Rotate-on-read: the frame (offset-table row, -1 = global) of key tile kt of the
+// tile pair, read from the tile's first page.  The MMA issuer and the softmax warps
+// both derive the frame changes from it, so they agree on them.
+__device__ __forceinline__ int tile_frame(const TcArgs& a, const TileMeta& tm, int kt) {
+  const int f = __ldg(a.page_tab + tm.page_begin + kt * kPagesPerKt);
+  if (f >= a.n_tab) {  // a row past the offset table: flagged, read in the global frame
+    set_err(a.err, PIC_ERR_RANGE);
+    return -1;
+  }
+  return f < 0 ? -1 : f;
+}
+
 // The whole warp: lane j < 8 owns page j of the key tile (its entry is loaded a
 // tile ahead) and issues that page's boxes, so page lookups and box issue run in
 // parallel across lanes.  Lane 0 arms each slot's barrier first.
+template <bool kRor>
 __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CUtensorMap* vmap,
                               uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31;
@@ -484,7 +501,8 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
     const int page_end = tm.page_begin + tm.n_pages;
     const int pbase = tm.page_begin + un.kt0 * kPagesPerKt;
     // Q operands of this unit, once the previous unit's last S products have read the buffers
-    if (lane == 0) {
+    // (rotating on read, the softmax warps write Q into the buffers themselves)
+    if (!kRor && lane == 0) {
       for (int i = 0; i < kQTiles; ++i) {
         if (i == 1 && tm.n_rows <= a.R) break;
         if (!wait_bar(b, &b->q_free[i], (uq[i] & 1) ^ 1)) {
@@ -595,10 +613,19 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
     const TileMeta tm = a.tiles[un.tile];
     const int n = un.kt1 - un.kt0;
     const bool act1 = tm.n_rows > a.R;
-    if (!wait_bar(b, &b->q_full[0], uq[0] & 1)) { fail(b, a.err); return; }
+    // Q tile i in shared memory: loaded by the producer, or (rotating on read) written
+    // for the frame of the unit's first key tile by its softmax warps
+    // frames of key tiles j and j + 1, read a tile ahead
+    int f_cur = 0, f_nxt = 0;
+    if (kRor) {
+      f_cur = tile_frame(a, tm, un.kt0);
+      f_nxt = n > 1 ? tile_frame(a, tm, un.kt0 + 1) : f_cur;
+    }
+    uint64_t* const q_in = kRor ? b->q_ready : b->q_full;
+    if (!wait_bar(b, &q_in[0], uq[0] & 1)) { fail(b, a.err); return; }
     ++uq[0];
     if (act1) {
-      if (!wait_bar(b, &b->q_full[1], uq[1] & 1)) { fail(b, a.err); return; }
+      if (!wait_bar(b, &q_in[1], uq[1] & 1)) { fail(b, a.err); return; }
       ++uq[1];
     }
     tc::tc_fence_after();
@@ -608,11 +635,11 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       tc::tc_fence_after();
       issue_s(0, ks);
       tc::mma_commit(&b->s_full[0]);
-      if (n == 1) tc::mma_commit(&b->q_free[0]);
+      if (!kRor && n == 1) tc::mma_commit(&b->q_free[0]);
       if (act1) {
         issue_s(1, ks);
         tc::mma_commit(&b->s_full[1]);
-        if (n == 1) tc::mma_commit(&b->q_free[1]);
+        if (!kRor && n == 1) tc::mma_commit(&b->q_free[1]);
       }
       tc::mma_commit(&b->kv_empty[ks]);
     }
@@ -620,6 +647,9 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       const uint32_t vld = ld + 1, nld = ld + 2;
       const int vs = vld % kSlots, ns = nld % kSlots;
       const bool more = j + 1 < n;
+      // rotating on read, key tile j + 1 in another frame than tile j needs Q rotated
+      // into it: its softmax warps do that once they have written P of tile j
+      const bool new_frame = kRor && more && f_nxt != f_cur;
 #pragma unroll
       for (int i = 0; i < kQTiles; ++i) {
         if (i == 1 && !act1) break;
@@ -629,16 +659,24 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
         issue_pv(i, vs, j > 0);
         if (more) {
           if (i == 0 && !wait_tile(nld / 2)) { fail(b, a.err); return; }
+          if (new_frame) {
+            if (!wait_bar(b, &b->q_ready[i], uq[i] & 1)) { fail(b, a.err); return; }
+            ++uq[i];
+          }
           tc::tc_fence_after();
           issue_s(i, ns);
           tc::mma_commit(&b->s_full[i]);
-          if (j + 2 == n) tc::mma_commit(&b->q_free[i]);  // the unit's last S product of Q tile i
+          if (!kRor && j + 2 == n) tc::mma_commit(&b->q_free[i]);  // the unit's last S product of Q tile i
         } else {
           tc::mma_commit(&b->o_done[i]);
         }
       }
       tc::mma_commit(&b->kv_empty[vs]);
       if (more) tc::mma_commit(&b->kv_empty[ns]);
+      if (kRor) {
+        f_cur = f_nxt;
+        if (j + 2 < n) f_nxt = tile_frame(a, tm, un.kt0 + j + 2);
+      }
     }
   }
 }
@@ -700,110 +738,9 @@ qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
 // Masked keys get weight 0 and 0 * V must stay 0 even if a slot outside a page's
 // valid range holds stale non-finite bits: once a V tile has landed, the rows of
 // slots that hold no valid key are zeroed before the MMA issuer uses the slot.
-// Packed fp32 pairs without flush-to-zero: each lane is the IEEE operation the
-// scalar __fmaf_rn / __fmul_rn / __fadd_rn performs.
-__device__ __forceinline__ uint64_t fma2_rn(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-__device__ __forceinline__ uint64_t mul2_rn(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t add2_rn(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-// bf16 pair (low half: element 0) -> packed fp32 pair, exactly
-__device__ __forceinline__ uint64_t bf16x2_unpack(uint32_t w) { return tc::f2pack(__uint_as_float(w << 16),
-                                                                                  __uint_as_float(w & 0xffff0000u)); }
-
-// cos / sin of two consecutive frequencies as packed pairs: hi and lo parts
-struct RotPair {
-  uint64_t c_hi, s_hi, c_lo, s_lo;
-};
-__device__ __forceinline__ RotPair rot_pair(const float4& t0, const float4& t1) {
-  RotPair r;
-  r.c_hi = tc::f2pack(t0.x, t1.x);
-  r.s_hi = tc::f2pack(t0.y, t1.y);
-  r.c_lo = tc::f2pack(t0.z, t1.z);
-  r.s_lo = tc::f2pack(t0.w, t1.w);
-  return r;
-}
-
-// One 32-bit word of a K row's low half (dimensions i, i + 1) against the word of
-// its high half (i + 64, i + 65), rotated in place with the operations of
-// rope_rotate_bf16in (the re-rotation pass), two lanes at a time, one bf16
-// rounding: bit for bit the pass's result.  The low output is formed negated —
-// with -a in place of a, fma(a, c, -p) = -fma(-a, c, p) and the sum and the bf16
-// rounding are odd functions, all exact under round-to-nearest — and its sign is
-// flipped back on the bf16 bits, so no negated sines need to be held.
-__device__ __forceinline__ void rotate_word2(uint32_t& wl, uint32_t& wh, const RotPair& t) {
-  const uint64_t a = bf16x2_unpack(wl), na = bf16x2_unpack(wl ^ 0x80008000u), b = bf16x2_unpack(wh);
-  const uint64_t nu = fma2_rn(na, t.c_hi, mul2_rn(b, t.s_hi));  // -(a c_hi - b s_hi)
-  const uint64_t v = fma2_rn(b, t.c_hi, mul2_rn(a, t.s_hi));
-  const uint64_t nya = add2_rn(nu, fma2_rn(na, t.c_lo, mul2_rn(b, t.s_lo)));
-  const uint64_t yb = add2_rn(v, fma2_rn(b, t.c_lo, mul2_rn(a, t.s_lo)));
-  float y0, y1, z0, z1;
-  tc::f2unpack(nya, y0, y1);
-  tc::f2unpack(yb, z0, z1);
-  __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1), q = __floats2bfloat162_rn(z0, z1);
-  wl = *reinterpret_cast<uint32_t*>(&p) ^ 0x80008000u;
-  wh = *reinterpret_cast<uint32_t*>(&q);
-}
-
-// Rotate-on-read: rotate in place the pages of the key tile at `ksm` whose table
-// row (lane j holds page j's) is not negative, by R(theta * Delta) of that row —
-// the same table and arithmetic as pic_rerotate_k, so the K the MMA reads is bit
-// for bit the one the re-rotation pass would have written.  Warps 2-3 (t64 =
-// 0..63): thread (c, hh, rq) takes dimensions 8c + 4hh .. +3 of both column halves
-// in rows rq, rq + 4, rq + 8, rq + 12 of every page (physical 16-byte position
-// c ^ (row % 8), the 128-byte swizzle); its four frequencies' cos / sin stay in
-// registers while consecutive pages share a table row.
-struct RotCache {
-  int tab;
-  RotPair p0, p1;
-};
-__device__ __forceinline__ void rotate_k_tile(uint32_t ksm, int tab_lane, const float4* __restrict__ rot_tab,
-                                              int t64, RotCache& rc) {
-  const int c = t64 & 7, hh = (t64 >> 3) & 1, rq = t64 >> 4;
-#pragma unroll 1
-  for (int jj = 0; jj < kPagesPerKt; ++jj) {
-    const int tab = __shfl_sync(0xffffffffu, tab_lane, jj);
-    if (tab < 0) continue;
-    if (tab != rc.tab) {
-      const float4* cs = rot_tab + (int64_t)tab * (kD / 2) + 8 * c + 4 * hh;
-      rc.p0 = rot_pair(__ldg(cs), __ldg(cs + 1));
-      rc.p1 = rot_pair(__ldg(cs + 2), __ldg(cs + 3));
-      rc.tab = tab;
-    }
-    // one row at a time, 32-bit shared-memory addresses: the V-zeroing warps run
-    // with 64 registers, and holding more rows in flight spilled to local memory
-    const uint32_t pg = ksm + jj * kPageBytes + hh * 8;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int r = rq + 4 * i;
-      const uint32_t pa = pg + (r >> 3) * kGroupBytes + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
-      uint32_t l0, l1, h0, h1;
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(l0), "=r"(l1) : "r"(pa));
-      asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(h0), "=r"(h1) : "r"(pa + kPageHalfBytes));
-      rotate_word2(l0, h0, rc.p0);
-      rotate_word2(l1, h1, rc.p1);
-      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(pa), "r"(l0), "r"(l1) : "memory");
-      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(pa + kPageHalfBytes), "r"(h0), "r"(h1) : "memory");
-    }
-  }
-}
-
-template <bool kRor>
 __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31, wz = (threadIdx.x >> 5) - 2;  // 0, 1
   uint32_t ld = 0;
-  RotCache rc;
-  rc.tab = -1;
   for (uint32_t k = 0;; ++k) {
     const int u = read_unit_warp(b, k);
     if (u < 0) { fail(b, a.err); return; }
@@ -818,34 +755,17 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
       const int plo = pvalid ? (int16_t)(pg.w & 0xffff) : 0;
       const int phi = pvalid ? (int16_t)(pg.w >> 16) : 0;
       const bool full = __all_sync(0xffffffffu, lane >= kPagesPerKt || (plo == 0 && phi == PIC_PAGE));
-      if (kRor) {  // rotate-on-read: K of this tile before its S product
-        int tab = -1;
-        if (pvalid) {
-          tab = __ldg(a.page_tab + tm.page_begin + kt * kPagesPerKt + lane);
-          if (tab >= a.n_tab) {
-            set_err(a.err, PIC_ERR_RANGE);
-            tab = -1;
-          }
-        }
-        const int ks = ld % kSlots;
-        const bool got = wait_bar(b, &b->kv_full[ks], (ld / kSlots) & 1);
-        if (!__all_sync(0xffffffffu, got)) { fail(b, a.err); return; }
-        rotate_k_tile(tc::smem_addr(smem + kOffSlot + ks * kOpBytes), tab, a.rot_tab, 32 * wz + lane, rc);
-        tc::fence_proxy_async_smem();
-        __syncwarp();
-      }
       const uint32_t vld = ld + 1;
       const int vs = vld % kSlots;
       // A slot takes K and V loads in turn, and these warps must see every phase of
       // it in order: a parity wait on the V load's phase while the slot's previous
       // fill (a K load) is still in flight would find that fill's previous phase
-      // complete and pass at once.  So the K load is waited for first (rotate-on-read
-      // did so above).  vz_done is the MMA issuer's only sign that the tile's K and V
+      // complete and pass at once.  So the K load is waited for first.  vz_done is the MMA issuer's only sign that the tile's K and V
       // have landed, so it is arrived for every tile (not only partial ones), after
       // both loads were seen; this also keeps these warps at most one phase ahead of
       // the issuer on it: a slot is not refilled before the MMAs that read it, which
       // follow the issuer's wait for vz_done, have completed.
-      if (!kRor) {
+      {
         const bool got = wait_bar(b, &b->kv_full[ld % kSlots], (ld / kSlots) & 1);
         if (!__all_sync(0xffffffffu, got)) { fail(b, a.err); return; }
       }
@@ -878,12 +798,8 @@ __device__ void vzero_loop(const TcArgs& a, uint8_t* smem, Bars* b, int n_units)
 }
 
 // ---------------------------------------------------------------- softmax warpgroups
-// Named barrier (ids 1, 2) of the two warpgroups that share Q tile qt.
-__device__ __forceinline__ void pair_sync(int qt) {
-  asm volatile("bar.sync %0, 256;" ::"r"(1 + qt) : "memory");
-}
-
-// The same barrier, also returning whether any of its 256 threads passed `failed`.
+// Named barrier (ids 1, 2) of the two warpgroups that share Q tile qt, returning
+// whether any of its 256 threads passed `failed`.
 // A warpgroup whose wait gave up still meets its partner here, and both leave
 // together: returning alone would leave the partner at its next barrier forever.
 __device__ __forceinline__ bool pair_sync_any(int qt, bool failed) {
@@ -899,12 +815,78 @@ __device__ __forceinline__ bool pair_sync_any(int qt, bool failed) {
   return any != 0;
 }
 
+// Rotate-on-read: Q tile qt of unit `un` written into shared memory for the key
+// frame `frame` (offset-table row, -1 = global).  Since RoPE(q, p) . R(Delta) k =
+// R(-Delta) RoPE(q, p) . k, the keys of a chunk can stay at their local positions
+// when Q is rotated back by the chunk's offset instead (one Q tile per frame
+// instead of one rotation per key tile read).  Thread (t, h) of the Q tile's two
+// warpgroups takes row t, columns 32h .. 32h + 31 of both 64-column halves (the
+// dimension pairs (i, i + 64) for those i) of the roped operand the Q pre-pass
+// wrote (global memory, already in the swizzled shared-memory layout), rotates
+// each pair by -theta_i * Delta in fp32 (cos / sin = hi + lo parts of the offset
+// table), rounds to bf16 and stores it at the same place in shared memory; for the
+// global frame it copies.  Then each warp arrives on q_ready[qt].  The caller
+// guarantees that no S product still reads the buffer.
+__device__ __forceinline__ uint32_t rot_pair_bf16(uint32_t& whi, uint32_t wlo, const float4& t0, const float4& t1) {
+  const float c0 = t0.x + t0.z, s0 = t0.y + t0.w, c1 = t1.x + t1.z, s1 = t1.y + t1.w;
+  const float a0 = __uint_as_float(wlo << 16), a1 = __uint_as_float(wlo & 0xffff0000u);
+  const float b0 = __uint_as_float(whi << 16), b1 = __uint_as_float(whi & 0xffff0000u);
+  // R(-phi): (a, b) -> (a cos phi + b sin phi, b cos phi - a sin phi)
+  whi = pack_bf16x2(fmaf(b0, c0, -a0 * s0), fmaf(b1, c1, -a1 * s1));
+  return pack_bf16x2(fmaf(a0, c0, b0 * s0), fmaf(a1, c1, b1 * s1));
+}
+
+__device__ __forceinline__ void prep_q_frame(const TcArgs& a, uint8_t* smem, Bars* b, const Unit& un, int qt, int h,
+                                             int t, int frame) {
+  const uint8_t* src = a.q_tiles + (((int64_t)un.tile * a.Hkv + un.head) * kQTiles + qt) * kOpBytes;
+  uint8_t* dst = smem + kOffQ + qt * kOpBytes;
+  uint4 lo[4], hi[4];
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const uint32_t off = sw128_off(t, 4 * h + cc);
+    lo[cc] = *reinterpret_cast<const uint4*>(src + off);
+    hi[cc] = *reinterpret_cast<const uint4*>(src + kHalfBytes + off);
+  }
+  if (frame >= 0) {
+    const float4* cs = a.rot_tab + (int64_t)frame * (kD / 2) + 32 * h;
+#pragma unroll
+    for (int cc = 0; cc < 4; ++cc) {
+      uint32_t* lw = reinterpret_cast<uint32_t*>(&lo[cc]);
+      uint32_t* hw = reinterpret_cast<uint32_t*>(&hi[cc]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e)  // dimensions 32h + 8cc + 2e, + 1 and their partners + 64
+        lw[e] = rot_pair_bf16(hw[e], lw[e], __ldg(cs + 8 * cc + 2 * e), __ldg(cs + 8 * cc + 2 * e + 1));
+    }
+  }
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const uint32_t off = sw128_off(t, 4 * h + cc);
+    *reinterpret_cast<uint4*>(dst + off) = lo[cc];
+    *reinterpret_cast<uint4*>(dst + kHalfBytes + off) = hi[cc];
+  }
+  tc::fence_proxy_async_smem();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) tc::mbar_arrive(&b->q_ready[qt]);
+}
+
+// Rotate-on-read: Q tile qt of unit u for the frame of the unit's first key tile,
+// if the unit has rows for the Q tile (the MMA issuer waits for it exactly then).
+__device__ __forceinline__ void prep_unit_q(const TcArgs& a, uint8_t* smem, Bars* b, int u, int n_units, int qt,
+                                            int h, int t) {
+  if (u < 0 || u >= n_units) return;
+  const Unit un = a.units[u];
+  const TileMeta tm = a.tiles[un.tile];
+  if (qt == 1 && tm.n_rows <= a.R) return;
+  prep_q_frame(a, smem, b, un, qt, h, t, tile_frame(a, tm, un.kt0));
+}
+
 // Warpgroup (qt, h) handles key columns 64h .. 64h+63 of every S tile of Q tile qt,
 // one row (TMEM lane) per thread.  The two halves of a row exchange their partial
 // maxima through shared memory once per key tile (so both take identical lazy
 // rescale decisions), write P for their keys into the S columns the MMA reads
 // (keys 64h.. -> columns 32h..), keep their own row sums, rescale and store their
 // own 64 columns of O.
+template <bool kRor>
 __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem, int n_units, int qt, int h) {
   const int t = (threadIdx.x - 128) & (kM - 1);  // TMEM lane = row of Q tile qt
   const int lane = threadIdx.x & 31;
@@ -919,6 +901,7 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
   // unit k (the first unit: at a barrier of its own).
   int u = read_unit_warp(b, 0);
   if (pair_sync_any(qt, u < 0)) { fail(b, a.err); return; }
+  if (kRor) prep_unit_q(a, smem, b, u, n_units, qt, h, t);
   for (uint32_t k = 0; u < n_units; ++k) {
     const Unit un = a.units[u];
     const TileMeta tm = a.tiles[un.tile];
@@ -926,6 +909,7 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
     if (qt == 1 && tm.n_rows <= a.R) {  // no rows for this Q tile: only the next unit
       u = read_unit_warp(b, k + 1);
       if (pair_sync_any(qt, u < 0)) { fail(b, a.err); return; }
+      if (kRor) prep_unit_q(a, smem, b, u, n_units, qt, h, t);
       continue;
     }
     const int loc = qt * a.R + i;
@@ -939,6 +923,12 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
     // lanes 0-3 hold the entries of this half's 4 pages of the key tile (one tile ahead)
     const int my_page = kPagesPerKt / 2 * h + lane;
     int4 pe = load_page(a.pages, lane < kPagesPerKt / 2 ? pbase + my_page : page_end, page_end);
+    // rotating on read: frames of key tiles j and j + 1, read a tile ahead
+    int f_cur = 0, f_nxt = 0;
+    if (kRor) {
+      f_cur = tile_frame(a, tm, un.kt0);
+      f_nxt = n > 1 ? tile_frame(a, tm, un.kt0 + 1) : f_cur;
+    }
     for (int j = 0; j < n; ++j, ++c) {
       const int4 cur = pe;
       if (j + 1 < n && lane < kPagesPerKt / 2)
@@ -1051,7 +1041,19 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
       tc::tc_fence_before();
       __syncwarp();
       if (lane == 0) tc::mbar_arrive(&b->p_full[qt]);
+      // the next key tile in another frame: S of this tile has read Q, and the next S
+      // product waits for q_ready, so Q is rotated into the new frame now, beside P.V
+      if (kRor && j + 1 < n) {
+        if (f_nxt != f_cur) prep_q_frame(a, smem, b, un, qt, h, t, f_nxt);
+        f_cur = f_nxt;
+        if (j + 2 < n) f_nxt = tile_frame(a, tm, un.kt0 + j + 2);
+      }
     }
+    // The next unit, read now; rotating on read, its first Q tile is written at once
+    // (this unit's last S product has completed, so the buffer is free), beside the
+    // last P.V, before the epilogue.
+    const int u_next = read_unit_warp(b, k + 1);
+    if (kRor) prep_unit_q(a, smem, b, u_next, n_units, qt, h, t);
     // epilogue: O / l over both halves' row sums
     const bool o_ok = wait_bar(b, &b->o_done[qt], ou & 1);
     ++ou;
@@ -1060,7 +1062,6 @@ __device__ void softmax_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t t
     if (pair_sync_any(qt, !o_ok)) { fail(b, a.err); return; }
     const float l_all = l + xch[(1 - h) * kM + t];
     // both have read before either writes the next tile's maximum; the next unit agreed
-    const int u_next = read_unit_warp(b, k + 1);
     if (pair_sync_any(qt, u_next < 0)) { fail(b, a.err); return; }
     const float inv = (l_all > 0.f) ? 1.f / l_all : 0.f;
     const int64_t slot = ((int64_t)(un.part < 0 ? 0 : un.part) * kQTiles + qt) * kM + t;
@@ -1119,6 +1120,7 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       tc::mbar_init(&b->s_full[i], 1);
       tc::mbar_init(&b->p_full[i], 8);  // every warp of the Q tile's two softmax warpgroups
       tc::mbar_init(&b->o_done[i], 1);
+      tc::mbar_init(&b->q_ready[i], 8);  // every warp of the Q tile's two softmax warpgroups
     }
     tc::mbar_init(&b->drain, 1);
     tc::mbar_init(&b->never, 1);
@@ -1145,7 +1147,7 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   if (warp < 4) {
     tc::regs_dec<kRegsLow>();
     if (warp == 0) {
-      producer_loop(a, &kmap, &vmap, smem, b, n_units);
+      producer_loop<kRor>(a, &kmap, &vmap, smem, b, n_units);
     } else if (warp == 1 && lane == 0) {
       mma_loop<kRor>(a, smem, b, tmem, n_units);
       // every MMA this thread issued completes before TMEM is released (also on abort)
@@ -1153,12 +1155,12 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
       const int no_abort = 0;
       tc::mbar_wait(&b->drain, 0, &no_abort, kWaitLimitNs);
     } else if (warp == 2 || warp == 3) {
-      vzero_loop<kRor>(a, smem, b, n_units);
+      vzero_loop(a, smem, b, n_units);
     }
   } else {
     tc::regs_inc<kRegsHigh>();
     const int g = (warp - 4) / 4;  // softmax warpgroup: Q tile g / 2, key columns 64 (g % 2) ..
-    softmax_loop(a, smem, b, tmem, n_units, g / 2, g % 2);
+    softmax_loop<kRor>(a, smem, b, tmem, n_units, g / 2, g % 2);
   }
   tc::tc_fence_before();
   __syncthreads();

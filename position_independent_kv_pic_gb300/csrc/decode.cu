@@ -16,6 +16,12 @@
 // is ~100 instructions per page and warp instead of ~700 on the FMA pipe, so the
 // CTA streams pages at the HBM rate.  The CTA combines its warps and writes one
 // partial (m, l, unnormalised o); a merge kernel combines the splits.
+//
+// After a rotate-on-read link (the framed page layout) the keys of a chunk stay in
+// the chunk's own frame: the page's frame (its offset-table row) travels with the
+// page to the consumer, and a consumer warp whose page is in another frame than the
+// last one rebuilds its Q fragments rotated back by that frame's offset (RoPE(q, P)
+// . R(Delta) k = R(-Delta) RoPE(q, P) . k).
 #include <algorithm>
 
 #include "pic_internal.cuh"
@@ -178,11 +184,55 @@ struct DecSmem {
 // Three CTAs per SM (registers capped at 136): the bytes in flight per SM and the
 // number of consumer warps both bound the streaming rate (two CTAs were 1.7x slower
 // on a 16-request batch).
+// Q fragments of row g (head g of the KV head; rows >= G are padding) for the keys of
+// frame `frame` (offset-table row; -1: the global frame, Q as roped): lane (g, t)
+// holds columns 16 ks + 2t, +1 (qa) and 16 ks + 2t + 8, +9 (qc); column c < 64 and
+// c + 64 are a RoPE pair, held by the same lane in fragments ks and ks + 4, so a
+// lane rotates its own pairs: (x, y) -> (x cos + y sin, y cos - x sin) for the
+// frame's angle, in fp32 (cos / sin = hi + lo parts of the table), rounded to bf16.
+template <int G>
+__device__ __forceinline__ void q_fragments(const __nv_bfloat16 (*qb)[kDecD], int g, int t, int frame,
+                                            const float4* __restrict__ rot_tab, uint32_t* qa, uint32_t* qc) {
+  const bool row = g < G;
+  const int gg = row ? g : 0;
+#pragma unroll
+  for (int ks = 0; ks < kDecD / 32; ++ks) {
+#pragma unroll
+    for (int part = 0; part < 2; ++part) {  // part 0: columns 16 ks + 2t, +1; part 1: + 8
+      const int c = 16 * ks + 2 * t + 8 * part;
+      float x[2], y[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        x[e] = __bfloat162float(qb[gg][c + e]);
+        y[e] = __bfloat162float(qb[gg][c + e + kDecD / 2]);
+        if (frame >= 0) {
+          const float4 cs = __ldg(rot_tab + (int64_t)frame * (kDecD / 2) + c + e);
+          const float co = cs.x + cs.z, si = cs.y + cs.w;
+          const float xr = fmaf(x[e], co, y[e] * si);
+          y[e] = fmaf(y[e], co, -x[e] * si);
+          x[e] = xr;
+        }
+      }
+      __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]), hi = __floats2bfloat162_rn(y[0], y[1]);
+      const uint32_t wl = row ? *reinterpret_cast<uint32_t*>(&lo) : 0u;
+      const uint32_t wh = row ? *reinterpret_cast<uint32_t*>(&hi) : 0u;
+      if (part == 0) {
+        qa[ks] = wl;
+        qa[ks + kDecD / 32] = wh;
+      } else {
+        qc[ks] = wl;
+        qc[ks + kDecD / 32] = wh;
+      }
+    }
+  }
+}
+
 template <int G>
 __global__ void __launch_bounds__(kDecThreads, 3)
 decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
               const bf16* __restrict__ q, const float4* __restrict__ q_table, int64_t num_blocks,
-              const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off, int n_req, int Hq,
+              const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off,
+              const int32_t* __restrict__ page_tab, const float4* __restrict__ rot_tab, int64_t n_tab, int n_req, int Hq,
               int Hkv, float scale_log2, const int4* __restrict__ desc, int slots, int32_t* __restrict__ first,
               int32_t* __restrict__ nsplit, float2* __restrict__ part_ml, float* __restrict__ part_o,
               int32_t* err) {
@@ -270,8 +320,18 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
         const bool ok = pg.x >= 0 && pg.x < num_blocks && pg.y >= 0 && pg.y < num_blocks && lo >= 0 &&
                         hi <= PIC_PAGE && lo < hi;
         if (!ok && !(lo >= hi && lo >= 0 && hi <= PIC_PAGE)) set_err(err, PIC_ERR_RANGE);
-        // the consumers read the page's slots from here (published by the arrival below)
-        sm.meta[st] = ok ? (lo | (hi << 8)) : -1;
+        // the consumers read the page's slots and frame from here (published by the
+        // arrival below): lo | hi << 5 | (frame + 1) << 10
+        int frame = -1;
+        if (ok && page_tab != nullptr) {
+          frame = __ldg(page_tab + pb + i);
+          if (frame >= n_tab) {
+            set_err(err, PIC_ERR_RANGE);
+            frame = -1;
+          }
+          frame = frame < 0 ? -1 : frame;
+        }
+        sm.meta[st] = ok ? (lo | (hi << 5) | ((frame + 1) << 10)) : -1;
         if (ok) {
           tc::mbar_arrive_expect_tx(&sm.full[st], 2 * kPageHead);
           tc::tma_load_4d(sm.ring[st][0], &kmap, 0, 0, 0, (pg.x * Hkv + kvh) * (PIC_PAGE / 8), &sm.full[st]);
@@ -309,6 +369,7 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
     const int g = lane >> 2, t = lane & 3;
     const bool row = g < G;
     uint32_t qa[kDecD / 16], qc[kDecD / 16];
+    int q_frame = -1;  // the frame the fragments are in
 #pragma unroll
     for (int ks = 0; ks < kDecD / 16; ++ks) {
       qa[ks] = row ? *reinterpret_cast<const uint32_t*>(&sm.qb[row ? g : 0][16 * ks + 2 * t]) : 0u;
@@ -334,7 +395,11 @@ decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ 
       }
       const int mt = sm.meta[st];
       if (mt >= 0) {
-        const int lo = mt & 0xff, hi = (mt >> 8) & 0xff;
+        const int lo = mt & 31, hi = (mt >> 5) & 31, frame = (mt >> 10) - 1;
+        if (frame != q_frame) {  // keys in another frame: Q rotated back by its offset
+          q_fragments<G>(sm.qb, g, t, frame, rot_tab, qa, qc);
+          q_frame = frame;
+        }
         const uint32_t kbase = tc::smem_addr(sm.ring[st][0]), vbase = tc::smem_addr(sm.ring[st][1]);
         // S = Q K^T over the 16 keys: matrices (keys 0-7 | 8-15) x (columns 16ks.. | 16ks+8..)
         float s0[2] = {0.f, 0.f}, s1[2] = {0.f, 0.f};
@@ -539,10 +604,14 @@ size_t pic_decode_workspace(int32_t n_req, int32_t Hq, int32_t Hkv, int32_t d, p
 
 pic_status pic_decode_attention(const void* q, const float* q_table, const void* k_pool, const void* v_pool,
                                 int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
-                                const int32_t* page_off, int32_t n_req, int32_t Hq, int32_t Hkv, int32_t d,
-                                float scale, void* out, void* ws, size_t ws_bytes, int32_t* err_flag,
-                                pic_stream_t stream) {
+                                const int32_t* page_off, const int32_t* page_tab, const float* rot_table,
+                                int64_t n_tab, int32_t n_req, int32_t Hq, int32_t Hkv, int32_t d, float scale,
+                                void* out, void* ws, size_t ws_bytes, int32_t* err_flag, pic_stream_t stream) {
   if (n_req < 0 || num_blocks < 0 || !(scale > 0.f)) return PIC_ERR_INVALID;
+  // frames travel with a page in 21 bits
+  if (n_tab < 0 || n_tab >= (1 << 21) - 1 || (page_tab != nullptr && n_tab > 0 && rot_table == nullptr) ||
+      (reinterpret_cast<uintptr_t>(rot_table) & 15))
+    return PIC_ERR_INVALID;
   if (Hkv < 1 || Hq < Hkv || Hq % Hkv || d < 2 || (d & 1)) return PIC_ERR_INVALID;
   if (!dec_shape(dtype, Hq, Hkv, d)) return PIC_ERR_UNSUPPORTED;
   if (n_req == 0) return PIC_OK;
@@ -573,15 +642,16 @@ pic_status pic_decode_attention(const void* q, const float* q_table, const void*
   const float sl2 = scale * 1.4426950408889634f;
   const bf16* qb = static_cast<const bf16*>(q);
   const float4* qt = reinterpret_cast<const float4*>(q_table);
+  const float4* rt = reinterpret_cast<const float4*>(rot_table);
   switch (Hq / Hkv) {
     case 1: decode_kernel<1><<<grid, kDecThreads, sizeof(DecSmem<1>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, page_tab, rt, n_tab, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
     case 2: decode_kernel<2><<<grid, kDecThreads, sizeof(DecSmem<2>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, page_tab, rt, n_tab, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
     case 4: decode_kernel<4><<<grid, kDecThreads, sizeof(DecSmem<4>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, page_tab, rt, n_tab, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
     default: decode_kernel<8><<<grid, kDecThreads, sizeof(DecSmem<8>), s>>>(kmap, vmap, qb, qt, num_blocks, pages,
-        page_off, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
+        page_off, page_tab, rt, n_tab, n_req, Hq, Hkv, sl2, desc, slots, first, nsplit, part_ml, part_o, err_flag); break;
   }
   if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   decode_merge_kernel<<<dim3((unsigned)Hq, (unsigned)n_req), 32 * kMergeGroups, 0, s>>>(

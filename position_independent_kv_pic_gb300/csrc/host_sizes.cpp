@@ -15,9 +15,10 @@ inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 extern "C" {
 
 pic_status pic_request_sizes_of(const int32_t* lens, int32_t n_chunks, int32_t q, int32_t k,
-                                pic_request_sizes* out) {
+                                pic_layout layout, pic_request_sizes* out) {
   if (out == nullptr || n_chunks < 0 || q < 0 || k < 0 || (n_chunks > 0 && lens == nullptr))
     return PIC_ERR_INVALID;
+  if (layout != PIC_LAYOUT_SPLICED && layout != PIC_LAYOUT_FRAMED) return PIC_ERR_INVALID;
   int64_t T = 0, rows = 0, link = 0, rot = 0, fresh = 0, cpages = 0;
   for (int32_t c = 0; c < n_chunks; ++c) {
     const int64_t L = lens[c];
@@ -28,7 +29,8 @@ pic_status pic_request_sizes_of(const int32_t* lens, int32_t n_chunks, int32_t q
     cpages += np;
     rows += m;
     fresh += cdiv(m, PIC_PAGE);
-    link += cdiv(m, PIC_PAGE) + kept;
+    const int64_t run = cdiv(m, PIC_PAGE) + kept;  // the chunk's link pages
+    link += (layout == PIC_LAYOUT_FRAMED) ? cdiv(run, PIC_TILE_PAGES) * PIC_TILE_PAGES : run;
     if (c > 0) rot += kept;
     T += L;
   }
@@ -45,12 +47,12 @@ pic_status pic_request_sizes_of(const int32_t* lens, int32_t n_chunks, int32_t q
 
 int64_t pic_count_rows(const int32_t* lens, int32_t n_chunks, int32_t q, int32_t k) {
   pic_request_sizes s;
-  if (pic_request_sizes_of(lens, n_chunks, q, k, &s) != PIC_OK) return -1;
+  if (pic_request_sizes_of(lens, n_chunks, q, k, PIC_LAYOUT_SPLICED, &s) != PIC_OK) return -1;
   return s.rows;
 }
 
 pic_status pic_plan_offsets(const int32_t* lens, const int32_t* chunk_off, const int32_t* q_len,
-                            const int32_t* k, int32_t n_req, int32_t* row_off, int32_t* page_off,
+                            const int32_t* k, int32_t n_req, pic_layout layout, int32_t* row_off, int32_t* page_off,
                             int32_t* rot_off, int32_t* fresh_off, int32_t* chunk_page_off) {
   if (n_req < 0 || (n_req > 0 && (chunk_off == nullptr || q_len == nullptr || k == nullptr)))
     return PIC_ERR_INVALID;
@@ -66,7 +68,7 @@ pic_status pic_plan_offsets(const int32_t* lens, const int32_t* chunk_off, const
     const int32_t c0 = chunk_off[r], c1 = chunk_off[r + 1];
     if (c1 < c0 || (c1 > c0 && lens == nullptr)) return PIC_ERR_INVALID;
     pic_request_sizes s;
-    if (pic_request_sizes_of(lens + c0, c1 - c0, q_len[r], k[r], &s) != PIC_OK) return PIC_ERR_INVALID;
+    if (pic_request_sizes_of(lens + c0, c1 - c0, q_len[r], k[r], layout, &s) != PIC_OK) return PIC_ERR_INVALID;
     acc[0] += s.rows;
     acc[1] += s.link_pages;
     acc[2] += s.rot_pages;

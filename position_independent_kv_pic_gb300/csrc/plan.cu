@@ -105,14 +105,15 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
               const int32_t* __restrict__ k_src, const int32_t* __restrict__ k_dst,
               const int32_t* __restrict__ v_blk, const int32_t* __restrict__ fresh_off,
               const int32_t* __restrict__ fresh_blocks, const int32_t* __restrict__ row_off,
-              const int32_t* __restrict__ page_off, const int32_t* __restrict__ rot_off,
+              const int32_t* __restrict__ page_off, const int32_t* __restrict__ rot_off, int framed,
               pic_link_page* __restrict__ pages, pic_rot_page* __restrict__ rot,
-              int32_t* __restrict__ row_block, int32_t* __restrict__ row_slot, int32_t* __restrict__ page_tab,
-              int32_t* err) {
+              int32_t* __restrict__ row_block, int32_t* __restrict__ row_slot, int32_t* __restrict__ row_frame_pos,
+              int32_t* __restrict__ page_tab, int32_t* err) {
   __shared__ int scratch[kPlanThreads / 32 + 1];
   __shared__ int g_link[kPlanThreads + 1], g_row[kPlanThreads + 1];
   __shared__ int g_rot[kPlanThreads], g_fresh[kPlanThreads];
   __shared__ int g_s[kPlanThreads], g_L[kPlanThreads], g_m[kPlanThreads], g_fp[kPlanThreads], g_j0[kPlanThreads];
+  __shared__ int g_run[kPlanThreads];
   const int r = blockIdx.x, tid = threadIdx.x;
   const int c0 = chunk_off[r], c1 = chunk_off[r + 1];
   const int q = q_len[r], k = kk[r];
@@ -136,7 +137,11 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
       if (chunk_page_off[c + 1] - chunk_page_off[c] != ci.np && blockIdx.y == 0) set_err(err, PIC_ERR_RANGE);
     }
     int t_link, t_rot, t_fresh, t_row, t_len;
-    const int ex_link = block_exclusive_scan<kPlanThreads>(ci.fp + ci.kept, scratch, &t_link);
+    // a chunk's link pages: fresh head pages, kept cached pages, and in the framed
+    // layout empty entries up to a whole number of key tiles
+    const int run = ci.fp + ci.kept;
+    const int n_link = (framed && c < c1) ? ceil_div(run, PIC_TILE_PAGES) * PIC_TILE_PAGES : run;
+    const int ex_link = block_exclusive_scan<kPlanThreads>(n_link, scratch, &t_link);
     const int ex_rot = block_exclusive_scan<kPlanThreads>((c > c0) ? ci.kept : 0, scratch, &t_rot);
     const int ex_fresh = block_exclusive_scan<kPlanThreads>(ci.fp, scratch, &t_fresh);
     const int ex_row = block_exclusive_scan<kPlanThreads>(ci.m, scratch, &t_row);
@@ -150,6 +155,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
     g_m[tid] = ci.m;
     g_fp[tid] = ci.fp;
     g_j0[tid] = ci.np - ci.kept;
+    g_run[tid] = run;
     if (tid == 0) {
       g_link[kPlanThreads] = t_link;
       g_row[kPlanThreads] = t_row;
@@ -164,6 +170,9 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
       const int pi = pbeg + link_base + P;
       if (pi >= pend) { set_err(err, PIC_ERR_RANGE); continue; }
       pic_link_page pg;
+      // the frame of the chunk's keys: its offset-table row in the framed layout
+      // (chunks after the first), else the global frame
+      const int frame = (cw > c0) ? cw : -1;
       if (f < g_fp[w]) {  // fresh head page f of the chunk
         const int fi = fbeg + fresh_base + g_fresh[w] + f;
         if (fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
@@ -171,7 +180,12 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
         pg.k_block = blk; pg.v_block = blk; pg.gpos0 = g_s[w] + PIC_PAGE * f;
         pg.lo = 0; pg.hi = (int16_t)min(PIC_PAGE, g_m[w] - PIC_PAGE * f);
         pages[pi] = pg;
-        if (page_tab != nullptr) page_tab[pi] = -1;
+        if (page_tab != nullptr) page_tab[pi] = framed ? frame : -1;
+      } else if (f >= g_run[w]) {  // framed layout: padding up to the key-tile boundary
+        pg.k_block = -1; pg.v_block = -1; pg.gpos0 = g_s[w] + g_L[w];
+        pg.lo = 0; pg.hi = 0;
+        pages[pi] = pg;
+        if (page_tab != nullptr) page_tab[pi] = frame;
       } else {  // cached page j that keeps at least one slot
         const int t = f - g_fp[w];
         const int j = g_j0[w] + t;
@@ -184,7 +198,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
         pg.lo = (int16_t)max(0, g_m[w] - PIC_PAGE * j);
         pg.hi = (int16_t)min(PIC_PAGE, g_L[w] - PIC_PAGE * j);
         pages[pi] = pg;
-        if (page_tab != nullptr) page_tab[pi] = (cw > c0) ? cw : -1;
+        if (page_tab != nullptr) page_tab[pi] = frame;
         if (cw > c0) {
           const int oi = obeg + rot_base + g_rot[w] + t;
           if (oi >= oend) { set_err(err, PIC_ERR_RANGE); continue; }
@@ -203,6 +217,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
       if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
       row_block[ri] = fresh_blocks[fi];
       row_slot[ri] = j % PIC_PAGE;
+      if (row_frame_pos != nullptr) row_frame_pos[ri] = framed ? j : g_s[w] + j;
     }
     __syncthreads();
     link_base += t_link;
@@ -228,6 +243,7 @@ splice_kernel(const int32_t* __restrict__ chunk_lens, const int32_t* __restrict_
     if (ri >= rend || fi >= fend) { set_err(err, PIC_ERR_RANGE); continue; }
     row_block[ri] = fresh_blocks[fi];
     row_slot[ri] = j % PIC_PAGE;
+    if (row_frame_pos != nullptr) row_frame_pos[ri] = T + j;  // the query is in the global frame
   }
   if (tid == 0 && blockIdx.y == 0) {
     if (link_base + qp != pend - pbeg || rot_base != oend - obeg ||
@@ -297,9 +313,12 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
                             const int32_t* k_dst_blocks, const int32_t* v_blocks,
                             const int32_t* fresh_off, const int32_t* fresh_blocks,
                             const int32_t* row_off, const int32_t* page_off, const int32_t* rot_off,
-                            pic_link_page* pages, pic_rot_page* rot, int32_t* row_block,
-                            int32_t* row_slot, int32_t* page_tab, int32_t* err_flag, pic_stream_t stream) {
-  if (n_req < 0) return PIC_ERR_INVALID;
+                            pic_layout layout, pic_link_page* pages, pic_rot_page* rot, int32_t* row_block,
+                            int32_t* row_slot, int32_t* row_frame_pos, int32_t* page_tab, int32_t* err_flag,
+                            pic_stream_t stream) {
+  if (n_req < 0 || (layout != PIC_LAYOUT_SPLICED && layout != PIC_LAYOUT_FRAMED)) return PIC_ERR_INVALID;
+  // the framed layout keeps every chunk's K where it is cached
+  if (layout == PIC_LAYOUT_FRAMED && k_dst_blocks != nullptr) return PIC_ERR_INVALID;
   if (n_req == 0) return PIC_OK;
   if (!chunk_off || !q_len || !k || !chunk_page_off || !fresh_off || !row_off || !page_off ||
       !rot_off || !err_flag)
@@ -309,8 +328,8 @@ pic_status pic_splice_pages(const int32_t* chunk_lens, const int32_t* chunk_off,
   const int per_req = std::max(1, std::min(32, (2 * sms + n_req - 1) / n_req));
   splice_kernel<<<dim3((unsigned)n_req, (unsigned)per_req), kPlanThreads, 0, (cudaStream_t)stream>>>(
       chunk_lens, chunk_off, q_len, k, chunk_start, chunk_page_off, k_src_blocks, k_dst_blocks,
-      v_blocks, fresh_off, fresh_blocks, row_off, page_off, rot_off, pages, rot, row_block, row_slot,
-      page_tab, err_flag);
+      v_blocks, fresh_off, fresh_blocks, row_off, page_off, rot_off, layout == PIC_LAYOUT_FRAMED ? 1 : 0, pages,
+      rot, row_block, row_slot, row_frame_pos, page_tab, err_flag);
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }
 

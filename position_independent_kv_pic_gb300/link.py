@@ -18,8 +18,8 @@ import math
 import numpy as np
 import torch
 
-from . import (PIC_BF16, PIC_FP32, PIC_PAGE, pic_decode_attention, pic_decode_workspace, pic_link_attention,
-               pic_link_attention_plan, pic_link_attention_ror, pic_link_attention_run, pic_link_attention_workspace,
+from . import (PIC_BF16, PIC_FP32, PIC_LAYOUT_FRAMED, PIC_LAYOUT_SPLICED, PIC_PAGE, pic_decode_attention,
+               pic_decode_workspace, pic_link_attention, pic_link_attention_plan, pic_link_attention_ror, pic_link_attention_run, pic_link_attention_workspace,
                pic_plan_offsets, pic_rerotate_k, pic_rope_cached_k, pic_rope_table, pic_select_rows,
                pic_splice_pages, pic_write_fresh_kv)
 from .inputs import Workload, block_shuffle, chunk_store, decode_inputs, row_inputs
@@ -35,8 +35,11 @@ class LinkBatch:
     def __init__(self, wl: Workload, device="cuda", rows_inputs=None, scheme="rotary"):
         """scheme "rotary": the pool's cached K is encoded at local positions and the step
         re-rotates it by the chunk offset (rotary correction).  scheme "ror": the same
-        correction applied on read inside link attention (rotate-on-read): the cached
-        pages are never written, so shared chunks need no per-request copies.  scheme
+        correction applied on read inside link attention (rotate-on-read, on the framed
+        page layout): every chunk's keys stay in the chunk's frame (the cached pages are
+        never written, the recomputed head rows' fresh K is encoded at its position in
+        the chunk) and Q is rotated back by the chunk's offset instead, so shared chunks
+        need no per-request copies.  scheme
         "nope": the pool's cached K carries no position encoding and the step encodes
         every kept cached slot at its global position (scheme B; in place only)."""
         if scheme not in ("rotary", "ror", "nope"):
@@ -59,7 +62,8 @@ class LinkBatch:
         self.chunk_off[1:] = np.cumsum([len(r.chunk_ids) for r in wl.requests])
         self.q_len = np.array([r.q for r in wl.requests], np.int32)
         self.k = np.array([r.k for r in wl.requests], np.int32)
-        offs = pic_plan_offsets(self.chunk_lens, self.chunk_off, self.q_len, self.k)
+        self.layout = PIC_LAYOUT_FRAMED if scheme == "ror" else PIC_LAYOUT_SPLICED
+        offs = pic_plan_offsets(self.chunk_lens, self.chunk_off, self.q_len, self.k, self.layout)
         self.offs = offs
         self.n_req = len(wl.requests)
         self.n_rows = int(offs["row_off"][-1])
@@ -122,6 +126,11 @@ class LinkBatch:
         self.pages = torch.empty((self.n_pages, 4), dtype=i32, device=dev)   # pic_link_page, 16 B
         self.rot = torch.empty((self.n_rot, 4), dtype=i32, device=dev)       # pic_rot_page, 16 B
         self.page_tab = torch.empty(self.n_pages, dtype=i32, device=dev) if scheme == "ror" else None
+        # rotate-on-read: each recomputed row's position in its frame, and the table the
+        # fresh K is encoded with
+        self.row_frame_pos = torch.empty(self.n_rows, dtype=i32, device=dev) if scheme == "ror" else None
+        self.fresh_table = torch.empty((self.n_rows, d // 2, 4), dtype=torch.float32, device=dev) \
+            if scheme == "ror" else None
         self.row_block = torch.empty(self.n_rows, dtype=i32, device=dev)
         self.row_slot = torch.empty(self.n_rows, dtype=i32, device=dev)
         self.delta_table = torch.empty((self.n_chunks, d // 2, 4), dtype=torch.float32, device=dev)
@@ -184,11 +193,11 @@ class LinkBatch:
     # ------------------------------------------------------------------ step
     # kernels one run() launches: select, splice, 2 tables, re-rotate, fresh K/V, and the
     # attention (unit planning, Q pre-pass, attention, LSE merge)
-    LAUNCHES_PER_STEP = 10  # rotary correction; scheme B (no offset table) and rotate-on-read (no re-rotation): 9
+    LAUNCHES_PER_STEP = 10  # rotary correction and rotate-on-read (a third table, no re-rotation); scheme B: 9
 
     @property
     def launches_per_step(self) -> int:
-        return self.LAUNCHES_PER_STEP - (1 if self.scheme in ("nope", "ror") else 0)
+        return self.LAUNCHES_PER_STEP - (1 if self.scheme == "nope" else 0)
 
     def run(self, stream=None, marks=None, inputs=None, out=None):
         """The link step: a1 select, splice, a2 tables, a3 re-rotate, a4 fresh K/V, a5+a6 attention.
@@ -240,7 +249,8 @@ class LinkBatch:
         pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
                          dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
                          dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
-                         self.row_block, self.row_slot, self.err, main, page_tab=self.page_tab)
+                         self.row_block, self.row_slot, self.err, main, page_tab=self.page_tab, layout=self.layout,
+                         row_frame_pos=self.row_frame_pos)
         if pass_stream is not main:
             self._ev_spliced.record(main)
             pass_stream.wait_event(self._ev_spliced)
@@ -270,8 +280,12 @@ class LinkBatch:
             pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, main)
         else:
             main.wait_event(self._ev_rowtab)
+        fresh_table = self.row_table
+        if self.scheme == "ror":  # fresh K in its chunk's frame
+            pic_rope_table(self.row_frame_pos, wl.d, wl.theta, self.fresh_table, main)
+            fresh_table = self.fresh_table
         pic_write_fresh_kv(self.k_pool, self.v_pool, self.pic_dtype, wl.Hkv, wl.d, dv["k_new"], dv["v_new"],
-                           self.row_table, self.row_block, self.row_slot, self.n_rows, self.err, main)
+                           fresh_table, self.row_block, self.row_slot, self.n_rows, self.err, main)
         if self.scheme == "ror":
             if "attention" in mk:
                 mk["attention"][0].record(main)
@@ -296,9 +310,6 @@ class LinkBatch:
         after the request's query rows.  Call after run() has built the link page list: a
         request's decode page list is its link pages followed by one page holding the new
         row (a serving engine keeps this list; building it is not part of the step)."""
-        if self.scheme == "ror":
-            raise NotImplementedError("decode reads the linked pages as stored: rotate-on-read links keep them "
-                                      "at local positions")
         wl, dev, i32 = self.wl, self.device, torch.int32
         q, k, v = decode_inputs(wl)
         self.dec_q, self.dec_k, self.dec_v = q.to(dev), k.to(dev), v.to(dev)
@@ -319,6 +330,13 @@ class LinkBatch:
         pages[torch.from_numpy(extra).to(dev)] = torch.from_numpy(ent.astype(np.int32)).to(dev)
         self.dec_pages = pages
         self.dec_page_off = torch.from_numpy(new_off).to(dev)
+        # after a rotate-on-read link the linked pages keep their frames; the new row's
+        # page is in the global frame
+        self.dec_page_tab = None
+        if self.scheme == "ror":
+            tab = self.page_tab[torch.from_numpy(np.maximum(src, 0)).to(dev)].clone()
+            tab[torch.from_numpy(extra).to(dev)] = -1
+            self.dec_page_tab = tab
         self.dec_table = torch.empty((self.n_req, wl.d // 2, 4), dtype=torch.float32, device=dev)
         self.dec_out = torch.empty((self.n_req, wl.Hq, wl.d), dtype=self.dtype, device=dev)
         ws = pic_decode_workspace(self.n_req, wl.Hq, wl.Hkv, wl.d, self.pic_dtype)
@@ -341,7 +359,8 @@ class LinkBatch:
             mk["decode"][0].record()
         pic_decode_attention(self.dec_q, self.dec_table, self.k_pool, self.v_pool, self.pic_dtype, self.dec_pages,
                              self.dec_page_off, self.n_req, wl.Hq, wl.Hkv, wl.d, self.scale, self.dec_out, self.dec_ws,
-                             self.err, stream)
+                             self.err, stream, page_tab=self.dec_page_tab,
+                             rot_table=self.delta_table if self.dec_page_tab is not None else None)
         if "decode" in mk:
             mk["decode"][1].record()
 

@@ -131,12 +131,20 @@ def check_attention(batch, which_per_request=None, scheme="rotary"):
     return float(e.max()), float(e.mean())
 
 
+def frame_positions(rows, starts, T):
+    """Positions at which the framed layout encodes recomputed rows' fresh K: a seam
+    row's position within its chunk, a query row's global position."""
+    c = np.searchsorted(starts, rows, side="right") - 1
+    return np.where(rows >= T, rows, rows - starts[c])
+
+
 def check_fresh_kv(batch):
     """a4, read back from the pools: the slot of every recomputed row (row_block,
     row_slot from the splice) holds K = RoPE(K_new, p_r) rounded to the pool dtype,
     within one ulp of the oracle's rounding of the float64 rotation, and V = V_new
-    bit for bit.  p_r comes from the oracle's row selection.  Returns the worst K
-    error in ulps."""
+    bit for bit.  p_r comes from the oracle's row selection: the global position, or
+    in the framed layout (rotate-on-read) the position in the row's frame.  Returns
+    the worst K error in ulps."""
     wl = batch.wl
     if batch.n_rows == 0:
         return 0.0
@@ -150,8 +158,9 @@ def check_fresh_kv(batch):
         a, b = int(batch.offs["row_off"][r]), int(batch.offs["row_off"][r + 1])
         if b == a:
             continue
-        rows, _, _ = O.select_rows(wl.chunk_lens[req.chunk_ids], req.q, req.k)
-        expect = O.round_to(O.rope(batch.k_new_h[a:b].double().numpy(), rows, wl.theta), wl.dtype)
+        rows, starts, T = O.select_rows(wl.chunk_lens[req.chunk_ids], req.q, req.k)
+        pos = frame_positions(rows, starts, T) if batch.scheme == "ror" else rows
+        expect = O.round_to(O.rope(batch.k_new_h[a:b].double().numpy(), pos, wl.theta), wl.dtype)
         ratio = float((np.abs(k_got[a:b] - expect) / storage_ulp(expect, wl.dtype)).max())
         worst = max(worst, ratio)
         assert ratio <= bound, f"fresh K of request {r}: {ratio} ulp"

@@ -110,6 +110,29 @@ def test_request_sizes_match_layout(seed):
     assert fresh_slots == rows
 
 
+@pytest.mark.parametrize("seed", range(20))
+def test_framed_layout_sizes(seed):
+    """The framed layout (rotate-on-read) pads every chunk's run of link pages to whole
+    key tiles: the count follows from the spliced layout's pages grouped by chunk."""
+    rng = np.random.default_rng(300 + seed)
+    lens = rng.integers(1, 200, size=rng.integers(1, 12)).tolist()
+    q, k = int(rng.integers(0, 70)), int(rng.integers(0, 40))
+    link, rot, fresh, cpages, T = _enumerate_layout(lens, q, k)
+    starts = np.concatenate([[0], np.cumsum(lens)])
+    per_chunk = [sum(1 for g0, lo, hi in link if starts[c] <= g0 + lo < starts[c + 1]) for c in range(len(lens))]
+    assert sum(per_chunk) + -(-q // 16) == len(link)
+    tile = pic.PIC_TILE_PAGES
+    framed = pic.pic_request_sizes_of(lens, q, k, pic.PIC_LAYOUT_FRAMED)
+    spliced = pic.pic_request_sizes_of(lens, q, k, pic.PIC_LAYOUT_SPLICED)
+    assert framed["link_pages"] == sum(-(-n // tile) * tile for n in per_chunk) + -(-q // 16)
+    assert {f: v for f, v in framed.items() if f != "link_pages"} == \
+        {f: v for f, v in spliced.items() if f != "link_pages"}
+    offs = pic.pic_plan_offsets(lens, [0, len(lens)], [q], [k], pic.PIC_LAYOUT_FRAMED)
+    assert offs["page_off"].tolist() == [0, framed["link_pages"]]
+    with pytest.raises(pic.PicError):
+        pic.pic_request_sizes_of(lens, q, k, 7)
+
+
 def test_plan_offsets():
     lens = [4, 5, 5, 7, 33, 1]
     chunk_off = [0, 3, 3, 6]

@@ -1,5 +1,7 @@
 """Decode after link: the CUDA decode step (through the C ABI) against the float64
-oracle's decode_after_link over the oracle's own linked context."""
+oracle's decode_after_link over the oracle's own linked context, after a link by
+the rotary correction and after a rotate-on-read link (whose pages keep every
+chunk's keys in the chunk's frame)."""
 
 import numpy as np
 import pytest
@@ -24,8 +26,8 @@ def built():
     pic.load()
 
 
-def _decode(wl):
-    b = LinkBatch(wl)
+def _decode(wl, scheme="rotary"):
+    b = LinkBatch(wl, scheme=scheme)
     b.run()
     torch.cuda.synchronize()
     assert b.error() == 0, pic.pic_strerror(b.error())
@@ -50,16 +52,20 @@ def _check(b, reqs):
     return float(e.max()), float(e.mean())
 
 
+@pytest.mark.parametrize("scheme", ["rotary", "ror"])
 @pytest.mark.parametrize("preset", ["rag_prompt_6chunks", "many_chunk_sink_20", "long_context_100x1000"])
-def test_decode_single_request(preset):
-    b = _decode(inputs.PRESETS[preset]())
+def test_decode_single_request(preset, scheme):
+    b = _decode(inputs.PRESETS[preset](), scheme)
     emax, emean = _check(b, [0])
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 
 
-def test_decode_batched_sampled():
-    b = _decode(inputs.batched_shared())
-    emax, emean = _check(b, [0, 7, 15])
+@pytest.mark.parametrize("scheme", ["rotary", "ror"])
+def test_decode_batched(scheme):
+    """Every request of the 16-request batch (shared chunks: rotated into private
+    pages by the rotary correction, read in place by rotate-on-read)."""
+    b = _decode(inputs.batched_shared(), scheme)
+    emax, emean = _check(b, range(b.n_req))
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 
 
@@ -75,11 +81,12 @@ def test_decode_many_requests(n_req):
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 
 
+@pytest.mark.parametrize("scheme", ["rotary", "ror"])
 @pytest.mark.parametrize("Hq", [8, 16, 32, 64])
-def test_decode_gqa_groups(Hq):
+def test_decode_gqa_groups(Hq, scheme):
     wl = inputs.custom([[130, 70, 45], [55, 8, 200]], [20, 1], [2, 16], Hq=Hq, Hkv=8, d=128, theta=5e5,
                        dtype="bf16", seed=60 + Hq)
-    b = _decode(wl)
+    b = _decode(wl, scheme)
     emax, emean = _check(b, [0, 1])
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 

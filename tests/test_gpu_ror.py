@@ -1,19 +1,23 @@
-"""Rotate-on-read through the C ABI: the cached K pages stay at local positions and
-pic_link_attention_ror rotates them inside the attention kernel.  Its K is, by
-construction, the re-rotation pass's K, so its output must equal the rotary
-correction path's output bit for bit; it is also checked against the float64
-oracle directly, and the cached pages must come out of the step untouched."""
+"""Rotate-on-read through the C ABI (RoPE article 3.3: the correction applied where
+the kernel reads the cache).  The step splices the framed layout: every chunk's
+keys stay in the chunk's own frame (cached pages never written, the recomputed
+head rows' fresh K encoded at their position in the chunk) and every key tile
+lies in one chunk; pic_link_attention_ror rotates Q back by the chunk's offset
+for the key tiles of that chunk instead of rotating K.  Checked against the float64
+oracle on every row of every workload, with the pool read back: cached pages
+untouched, fresh K in its frame."""
 
 import numpy as np
 import pytest
 import torch
 
+import oracle.pic_oracle as O
 import position_independent_kv_pic_gb300 as pic
 from position_independent_kv_pic_gb300 import build as pic_build
 from position_independent_kv_pic_gb300 import inputs
 from position_independent_kv_pic_gb300.link import LinkBatch
 
-from parity_util import TOL_MAX, TOL_MEAN, check_attention, oracle_request
+from parity_util import TOL_MAX, TOL_MEAN, check_attention, check_fresh_kv, check_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -26,16 +30,12 @@ def built():
     pic.load()
 
 
-def _pair(wl):
-    """The same link step by the rotary correction and by rotate-on-read."""
-    rot = LinkBatch(wl, scheme="rotary")
-    ror = LinkBatch(wl, scheme="ror", rows_inputs=(rot.q_raw_h, rot.k_new_h, rot.v_new_h))
-    rot.run()
-    ror.run()
+def _run(wl):
+    b = LinkBatch(wl, scheme="ror")
+    b.run()
     torch.cuda.synchronize()
-    assert rot.error() == 0, pic.pic_strerror(rot.error())
-    assert ror.error() == 0, pic.pic_strerror(ror.error())
-    return rot, ror
+    assert b.error() == 0, pic.pic_strerror(b.error())
+    return b
 
 
 def _cached_pages_untouched(b):
@@ -50,76 +50,87 @@ def _cached_pages_untouched(b):
 
 @pytest.mark.parametrize("preset", ["rag_prompt_6chunks", "many_chunk_sink_20", "long_context_100x1000",
                                     "batched_shared_16req"])
-def test_bit_identical_to_rerotation(preset):
-    rot, ror = _pair(inputs.PRESETS[preset]())
-    assert torch.equal(ror.out, rot.out)
-    _cached_pages_untouched(ror)
+def test_against_oracle(preset):
+    b = _run(inputs.PRESETS[preset]())
+    check_rows(b)
+    check_fresh_kv(b)
+    emax, emean = check_attention(b)
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+    _cached_pages_untouched(b)
 
 
-def test_page_tab_marks_cached_pages_after_the_first_chunk():
-    b = LinkBatch(inputs.batched_shared(), scheme="ror")
-    b.run()
-    torch.cuda.synchronize()
+def test_framed_layout():
+    """Every chunk's run of pages starts on a key-tile boundary of its request's list
+    and is padded with empty entries; page_tab names the chunk for every page of a
+    chunk after the first (fresh, cached and padding) and -1 for chunk 0 and the
+    query; the fresh rows' frame positions are their positions in the chunk."""
+    b = _run(inputs.batched_shared())
+    pages = b.pages_host()
     tab = b.page_tab.cpu().numpy()
-    pages = b.pages.cpu().numpy()
     starts = b.chunk_start.cpu().numpy()
-    src = set(b.k_src.tolist())
-    po = b.offs["page_off"]
-    for r in range(b.n_req):
-        c0 = int(b.chunk_off[r])
-        for p in range(int(po[r]), int(po[r + 1])):
-            t = int(tab[p])
-            if t < 0:
-                continue
-            # a cached page of a later chunk of this request, at that chunk's offset
-            assert c0 < t < int(b.chunk_off[r + 1])
-            assert int(pages[p, 0]) in src
-            assert (int(pages[p, 2]) - int(starts[t])) % 16 == 0
-    n_rotating = int((tab >= 0).sum())
-    assert n_rotating == b.n_rot  # one page per entry the re-rotation pass would have run
+    frame_pos = b.row_frame_pos.cpu().numpy()
+    rows = b.rows.cpu().numpy()
+    po, ro = b.offs["page_off"], b.offs["row_off"]
+    for r, req in enumerate(b.wl.requests):
+        c0, c1 = int(b.chunk_off[r]), int(b.chunk_off[r + 1])
+        p = int(po[r])
+        for c in range(c0, c1):
+            L = int(b.chunk_lens[c])
+            end = int(starts[c]) + L
+            run = [p]
+            while p < int(po[r + 1]) and pages["lo"][p] < pages["hi"][p] and pages["gpos0"][p] < end:
+                p += 1
+            n_real = p - run[0]
+            while p < int(po[r + 1]) and pages["lo"][p] == pages["hi"][p] and pages["gpos0"][p] == end:
+                assert pages["k_block"][p] == -1 and pages["v_block"][p] == -1
+                p += 1
+            assert (run[0] - int(po[r])) % pic.PIC_TILE_PAGES == 0 and (p - run[0]) % pic.PIC_TILE_PAGES == 0
+            assert p - run[0] - n_real < pic.PIC_TILE_PAGES
+            want = c if c > c0 else -1
+            assert np.all(tab[run[0]:p] == want), (r, c)
+        assert np.all(tab[p:int(po[r + 1])] == -1)  # the query pages
+        lens = b.wl.chunk_lens[req.chunk_ids]
+        o_rows, o_starts, T = O.select_rows(lens, req.q, req.k)
+        a, e = int(ro[r]), int(ro[r + 1])
+        assert np.array_equal(rows[a:e], o_rows)
+        c = np.searchsorted(o_starts, o_rows, side="right") - 1
+        assert np.array_equal(frame_pos[a:e], np.where(o_rows >= T, o_rows, o_rows - o_starts[c]))
 
 
 @pytest.mark.parametrize("case", [
     ([[300, 17, 1, 64, 129]], [37], [8]),
     ([[40, 50, 60]], [3], [40]),
     ([[130, 70], [55, 8, 200, 31]], [20, 1], [2, 16]),
+    ([[1, 1, 1, 1, 1, 1]], [1], [1]),
+    ([[77, 91, 33]], [5], [0]),
+    ([[100, 250]], [0], [16]),
 ])
 def test_edge_cases_against_oracle(case):
     lens, qs, ks = case
     wl = inputs.custom(lens, qs, ks, Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=90 + len(lens))
-    rot, ror = _pair(wl)
-    assert torch.equal(ror.out, rot.out)
-    out = ror.out.double().cpu().numpy()
-    errs = []
-    for r in range(ror.n_req):
-        a, e = int(ror.offs["row_off"][r]), int(ror.offs["row_off"][r + 1])
-        res = oracle_request(ror, r)
-        errs.append(np.abs(out[a:e] - res["out"]).ravel())
-    x = np.concatenate(errs)
-    assert x.max() <= TOL_MAX and x.mean() <= TOL_MEAN, (x.max(), x.mean())
+    b = _run(wl)
+    check_rows(b)
+    check_fresh_kv(b)
+    emax, emean = check_attention(b)
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+    _cached_pages_untouched(b)
 
 
-def test_rag_prompt_against_oracle():
-    wl = inputs.rag_prompt()
-    b = LinkBatch(wl, scheme="ror")
-    b.run()
-    torch.cuda.synchronize()
-    assert b.error() == 0
+@pytest.mark.parametrize("Hq", [8, 16, 64])
+def test_gqa_groups_against_oracle(Hq):
+    wl = inputs.custom([[90, 140, 20]], [29], [8], Hq=Hq, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=97)
+    b = _run(wl)
     emax, emean = check_attention(b)
     assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
 
 
 def test_bad_table_row_is_flagged():
     wl = inputs.custom([[40, 50, 60]], [3], [4], Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=95)
-    b = LinkBatch(wl, scheme="ror")
-    b.run()
-    torch.cuda.synchronize()
-    assert b.error() == 0
-    t = b.page_tab.clone()
-    rotating = torch.nonzero(t >= 0).flatten()
-    assert len(rotating) > 0
-    # run the attention alone with one page pointing past the table
-    b.page_tab[rotating[0]] = b.n_chunks + 3
+    b = _run(wl)
+    framed = torch.nonzero(b.page_tab >= 0).flatten()
+    assert len(framed) > 0
+    # run the attention alone with the frames of one chunk pointing past the table
+    b.page_tab[framed] = b.n_chunks + 3
     pic.pic_link_attention_ror(b.dev["q_raw"], b.row_table, b.rows, b.dev["row_off"], b.k_pool, b.v_pool,
                                b.pic_dtype, b.pages, b.page_tab, b.delta_table, b.dev["page_off"], b.n_req,
                                b.n_rows, wl.Hq, wl.Hkv, wl.d, b.scale, b.out, b.ws, b.err)
@@ -132,8 +143,6 @@ def test_unsupported_shapes():
     b = LinkBatch(wl, scheme="ror")
     with pytest.raises(pic.PicError):
         b.run()
-    with pytest.raises(NotImplementedError):
-        LinkBatch(inputs.rag_prompt(), scheme="ror").setup_decode()
 
 
 def test_plan_and_run_equal_the_single_call():
