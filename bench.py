@@ -380,6 +380,20 @@ def run_gpu(args, rank, world):
             raise SystemExit(f"device error (rotate-on-read): {pic.pic_strerror(rb.error())}")
         ror = (statistics.mean(a.elapsed_time(b) for a, b in rstep),
                statistics.mean(a.elapsed_time(b) for a, b in ratt), Kr, rb.tokens, rb.launches_per_step)
+        # decode after the rotate-on-read link: the pages keep each chunk's frame
+        if wl.dtype == "bf16" and pic.pic_decode_workspace(rb.n_req, wl.Hq, wl.Hkv, wl.d, rb.pic_dtype) > 0:
+            rb.setup_decode()
+            for _ in range(args.warmup):
+                rb.run_decode()
+            torch.cuda.synchronize()
+            rdec = [(ev(), ev()) for _ in range(Kr)]
+            for i in range(Kr):
+                l2_flush()
+                rb.run_decode(marks={"decode": rdec[i]})
+            torch.cuda.synchronize()
+            if rb.error() != 0:
+                raise SystemExit(f"device error (decode after rotate-on-read): {pic.pic_strerror(rb.error())}")
+            ror = ror + (statistics.mean(a.elapsed_time(b) for a, b in rdec), rb.dec_bytes)
         del rb
         torch.cuda.empty_cache()
 
@@ -467,9 +481,14 @@ def run_gpu(args, rank, world):
                                    "frac": attn_flops / (ror[1] / 1e3) / 1e12 / tf_burst, "ms": ror[1],
                                    "ms_per_step": ror[0], "tokens_per_s": world * ror[3] / (ror[0] / 1e3),
                                    "steps": ror[2], "launches_per_step": ror[4],
-                                   "kernel": "pic_link_attention_ror (link attention rotating each cached K page "
-                                             "in shared memory before its S product); the step has no "
-                                             "re-rotation pass"}} if ror else {}),
+                                   "kernel": "pic_link_attention_ror (framed page layout: each chunk's keys stay "
+                                             "in its frame, Q is rotated back by the chunk's offset at frame "
+                                             "changes); the step has no re-rotation pass"}} if ror else {}),
+            **({"decode_after_ror": {"bound": "hbm", "achieved": ror[6] / (ror[5] / 1e3) / 1e9, "peak": hbm,
+                                     "unit": "GB/s", "frac": ror[6] / (ror[5] / 1e3) / 1e9 / hbm, "ms": ror[5],
+                                     "algorithmic_bytes": ror[6],
+                                     "kernel": "pic_decode_attention over the rotate-on-read link's framed pages "
+                                               "(Q fragments rotated per frame)"}} if ror and len(ror) > 5 else {}),
             **({"compose": {"bound": "hbm", "achieved": comp[1] / (comp[0] / 1e3) / 1e9, "peak": hbm,
                             "unit": "GB/s", "frac": comp[1] / (comp[0] / 1e3) / 1e9 / hbm, "ms": comp[0],
                             "algorithmic_bytes": comp[1], "steps": comp[2], "seg": comp[3], "chains": comp[4], "traffic": ctraffic,
