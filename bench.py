@@ -334,30 +334,29 @@ def run_gpu(args, rank, world):
 
     # scheme B (chunks cached without position encoding, encoded at the global
     # position by the step): the same step with pic_rope_cached_k in place of the
-    # offset table and the re-rotation; in place only
+    # re-rotation (out of place into private pages when chunks are shared)
     schb = None
-    if not wl.out_of_place:
-        bb = LinkBatch(wl, scheme="nope")
-        for _ in range(args.warmup):
-            bb.run()
-        torch.cuda.synchronize()
-        Kb = max(3, min(K, 50))
-        bstep = [(ev(), ev()) for _ in range(Kb)]
-        brope = [(ev(), ev()) for _ in range(Kb)]
-        for i in range(Kb):
-            l2_flush()
-            bstep[i][0].record(stream)
-            bb.run(marks={"rerotate": brope[i]})
-            bstep[i][1].record(stream)
-        torch.cuda.synchronize()
-        if bb.error() != 0:
-            raise SystemExit(f"device error (scheme B): {pic.pic_strerror(bb.error())}")
-        kept = int(bb.chunk_lens.sum()) - (bb.n_rows - int(bb.q_len.sum()))  # cached slots encoded
-        rope_bytes = 2 * kept * wl.Hkv * wl.d * el + kept * (wl.d // 2) * 16  # K read + write, table rows
-        schb = (statistics.mean(a.elapsed_time(b) for a, b in bstep),
-                statistics.mean(a.elapsed_time(b) for a, b in brope), rope_bytes, Kb, bb.tokens)
-        del bb
-        torch.cuda.empty_cache()
+    bb = LinkBatch(wl, scheme="nope")
+    for _ in range(args.warmup):
+        bb.run()
+    torch.cuda.synchronize()
+    Kb = max(3, min(K, 50))
+    bstep = [(ev(), ev()) for _ in range(Kb)]
+    brope = [(ev(), ev()) for _ in range(Kb)]
+    for i in range(Kb):
+        l2_flush()
+        bstep[i][0].record(stream)
+        bb.run(marks={"rerotate": brope[i]})
+        bstep[i][1].record(stream)
+    torch.cuda.synchronize()
+    if bb.error() != 0:
+        raise SystemExit(f"device error (scheme B): {pic.pic_strerror(bb.error())}")
+    kept = int(bb.chunk_lens.sum()) - (bb.n_rows - int(bb.q_len.sum()))  # cached slots encoded
+    rope_bytes = 2 * kept * wl.Hkv * wl.d * el  # K read + written; the position table's rows are not counted
+    schb = (statistics.mean(a.elapsed_time(b) for a, b in bstep),
+            statistics.mean(a.elapsed_time(b) for a, b in brope), rope_bytes, Kb, bb.tokens)
+    del bb
+    torch.cuda.empty_cache()
 
     # rotate-on-read: the same step with the correction applied inside link attention
     # (no re-rotation pass; the cached pages are read as cached)
@@ -473,9 +472,11 @@ def run_gpu(args, rank, world):
                              "frac": schb[2] / (schb[1] / 1e3) / 1e9 / hbm, "ms": schb[1],
                              "algorithmic_bytes": schb[2], "ms_per_step": schb[0], "traffic": btraffic,
                              "tokens_per_s": world * schb[4] / (schb[0] / 1e3), "steps": schb[3],
-                             "kernel": "pic_rope_cached_k (scheme B: cached K encoded at its global position; "
-                                       "bytes = K read + written + one table row per slot); the step runs "
-                                       "without the offset table and the re-rotation"}} if schb else {}),
+                             "kernel": "pic_rope_cached_k (scheme B: cached K encoded at its global position "
+                                       "from a per-position table; bytes = K read + written only, the table "
+                                       "rows it also reads are not counted); the step runs it in place of "
+                                       "the offset table and the re-rotation"}}
+               if schb else {}),
             **({"rotate_on_read": {"bound": "tensor", "achieved": attn_flops / (ror[1] / 1e3) / 1e12,
                                    "peak": tf_burst, "unit": "TFLOP/s",
                                    "frac": attn_flops / (ror[1] / 1e3) / 1e12 / tf_burst, "ms": ror[1],

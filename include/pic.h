@@ -276,9 +276,11 @@ pic_status pic_rerotate_k(void* k_pool, int64_t num_blocks, pic_dtype dtype, int
  *                     is its output)
  *   chunk_page_off    [n_chunks+1], n_chunk_pages = chunk_page_off[n_chunks] (host)
  *   k_src_blocks      [n_chunk_pages] block of each cached page
- *   k_dst_blocks      [n_chunk_pages] destination, or NULL for in place.  The page
- *                     list of pic_splice_pages reads chunk 0 from k_src_blocks, so
- *                     a link over shared chunks must run in place on private copies
+ *   k_dst_blocks      [n_chunk_pages] destination, or NULL for in place.  With
+ *                     chunks shared by requests every chunk (the first too) is
+ *                     encoded out of place into the request's private pages, and
+ *                     pic_splice_pages is given those pages as its k_src_blocks
+ *                     so that the page list reads them
  *   pos_table         [n_pos][d/2][4]: pic_rope_table over positions 0..n_pos-1
  *                     (a per-model table; every encoded position must be < n_pos)
  * Slots [0, min(k, L_c)) of chunks after the first (recomputed rows) are left

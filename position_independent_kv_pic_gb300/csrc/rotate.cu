@@ -162,10 +162,14 @@ rerotate_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d,
 // Scheme B (article on RoPE and prefix caching, section 3.2): a chunk's K cached
 // without its position encoding is encoded on link at its global positions: slot
 // s of page j of chunk c gets RoPE at s_c + 16 j + s, from a table with one row
-// per position.  The work items are the rotation kernel's; the page's chunk and
-// request come from binary searches over the page and chunk offsets, and the kept
-// slots are those not recomputed (the first min(k, L_c) rows of every chunk after
-// the first are replaced by fresh rows).
+// per position (a per-model table; composing each angle from a chunk-offset row
+// and a chunk-local row instead, by compensated angle addition, kept HBM to K
+// alone but made the pass slower: 105 vs 89 us on the long-context link).  The
+// work items are the rotation kernel's; the page's chunk and request come from
+// binary searches over the page and chunk offsets, and the kept slots are those
+// not recomputed (the first min(k, L_c) rows of every chunk after the first are
+// replaced by fresh rows).  Out of place (every chunk, the first too, encoded into
+// private pages) when chunks are shared by requests.
 template <typename T>
 __global__ void __launch_bounds__(kRotThreads, 4)
 rope_cached_kernel(T* __restrict__ pool, int64_t num_blocks, int Hkv, int d, const int32_t* __restrict__ chunk_lens,

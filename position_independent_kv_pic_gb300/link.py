@@ -41,11 +41,10 @@ class LinkBatch:
         the chunk) and Q is rotated back by the chunk's offset instead, so shared chunks
         need no per-request copies.  scheme
         "nope": the pool's cached K carries no position encoding and the step encodes
-        every kept cached slot at its global position (scheme B; in place only)."""
+        every kept cached slot at its global position (scheme B; with shared chunks into
+        per-request pages, the first chunk's too)."""
         if scheme not in ("rotary", "ror", "nope"):
             raise ValueError(scheme)
-        if scheme == "nope" and wl.out_of_place:
-            raise ValueError("scheme B runs in place: give each request private copies of its chunks")
         self.scheme = scheme
         self.wl = wl
         self.device = torch.device(device)
@@ -79,7 +78,9 @@ class LinkBatch:
         store_base[1:] = np.cumsum(store_np)
         n_store_pages = int(store_base[-1])
         n_chunk_pages = int(offs["chunk_page_off"][-1])
-        copies = wl.out_of_place and scheme == "rotary"  # rotate-on-read reads the shared chunks in place
+        # shared chunks: rotated (or, scheme B, encoded) into per-request pages; rotate-on-read
+        # reads them in place
+        copies = wl.out_of_place and scheme in ("rotary", "nope")
         n_dst = n_chunk_pages if copies else 0
         n_link_blocks = n_store_pages + n_dst + self.n_fresh
         # one more block per request takes the row a decode step appends after the link
@@ -246,8 +247,10 @@ class LinkBatch:
             plan_stream.wait_event(self._ev_fork)
             pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, plan_stream)
             self._ev_rowtab.record(plan_stream)
+        # scheme B with shared chunks: the page list reads every chunk from its private pages
+        list_src = dv["k_dst"] if (self.scheme == "nope" and "k_dst" in dv) else dv["k_src"]
         pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
-                         dv["chunk_page_off"], dv["k_src"], dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
+                         dv["chunk_page_off"], list_src, dv.get("k_dst"), dv["v_blocks"], dv["fresh_off"],
                          dv["fresh_blocks"], dv["row_off"], dv["page_off"], dv["rot_off"], self.pages, self.rot,
                          self.row_block, self.row_slot, self.err, main, page_tab=self.page_tab, layout=self.layout,
                          row_frame_pos=self.row_frame_pos)
@@ -270,8 +273,8 @@ class LinkBatch:
         elif self.scheme == "nope":
             pic_rope_cached_k(self.k_pool, self.pic_dtype, wl.Hkv, wl.d, dv["chunk_lens"], dv["chunk_off"], dv["k"],
                               self.n_req, self.chunk_start, dv["chunk_page_off"], self.n_chunks,
-                              int(self.offs["chunk_page_off"][-1]), dv["k_src"], None, self.pos_table, self.err,
-                              pass_stream)
+                              int(self.offs["chunk_page_off"][-1]), dv["k_src"], dv.get("k_dst"), self.pos_table,
+                              self.err, pass_stream)
         if "rerotate" in mk:
             mk["rerotate"][1].record(pass_stream)
         if pass_stream is not main:
@@ -378,7 +381,8 @@ class LinkBatch:
         cp0 = int(self.offs["chunk_page_off"][flat_chunk])
         r = int(np.searchsorted(self.chunk_off, flat_chunk, side="right") - 1)
         first = flat_chunk == int(self.chunk_off[r])
-        table = self.k_src if (self.k_dst is None or first) else self.k_dst
+        # private pages when chunks were copied; the first chunk is copied only by scheme B
+        table = self.k_src if (self.k_dst is None or (first and self.scheme != "nope")) else self.k_dst
         j = np.arange(L)
         b = torch.from_numpy(table[cp0 + j // PIC_PAGE].astype(np.int64)).to(self.device)
         s = torch.from_numpy(j % PIC_PAGE).to(self.device)

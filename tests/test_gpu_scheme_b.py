@@ -1,6 +1,6 @@
 """Scheme B through the C ABI: chunks cached without position encoding, encoded at
-their global positions by pic_rope_cached_k, against the float64 oracle
-(link_request with scheme "nope")."""
+their global positions by pic_rope_cached_k, against the float64 oracle (link_request with scheme "nope"):
+in place, and out of place into private pages when chunks are shared."""
 
 import numpy as np
 import pytest
@@ -87,6 +87,18 @@ def test_scheme_b_fp32_small():
     assert emax < 1e-4 and emean < 1e-5, (emax, emean)
 
 
-def test_scheme_b_refuses_shared_chunks():
-    with pytest.raises(ValueError):
-        LinkBatch(inputs.batched_shared(), scheme="nope")
+def test_scheme_b_shared_chunks():
+    """16 requests over a shared store: every chunk (the first too) is encoded at its
+    global position into the request's private pages, against the oracle on every
+    kept slot and every row; the shared sources stay as cached (un-encoded)."""
+    b = _run(inputs.batched_shared())
+    check_rows(b)
+    _check_k(b)
+    check_fresh_kv(b)
+    emax, emean = _check_attention(b)
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+    for c, blocks in enumerate(b.store_blocks):
+        L = int(b.wl.chunk_lens[c])
+        j = np.arange(L)
+        got = b.k_pool[torch.from_numpy(blocks[j // 16]).cuda(), :, torch.from_numpy(j % 16).cuda(), :].cpu()
+        assert torch.equal(got, b.store_k[b.store_off[c]:b.store_off[c + 1]])
