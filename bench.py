@@ -45,16 +45,18 @@ UNIT = "tokens/s"
 # two-launch composition), with the kernel source they were taken from; reported
 # as roofline traffic only while the source is unchanged.
 NCU_TRAFFIC = {
-    # link_attn_tc_kernel<0>, long_context_100x1000: 662.60 MB read + 130.66 MB written
-    ("attention", "25ad24902e9e1252"): 793256192,
-    # rerotate_kernel<bf16>, long_context_100x1000: 201.35 MB read + 140.40 MB written
-    ("rerotate", "94fbac229e1fc877"): 341751552,
-    # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.40 MB written
-    ("scheme_b", "94fbac229e1fc877"): 449222144,
-    # decode_kernel<4>, one row per request over the long-context link: 420.65 MB read + 4.73 MB written
-    ("decode", "e8e2ed89ce131e93"): 425376000,
-    # compose_kernel, 32 heads x 100-chunk chain, both levels: 417.43 + 14.76 MB read + 3.54 MB written
-    ("compose", "1f16bf2f2eb3b24d"): 435723520,
+    # link_attn_tc_kernel<0>, long_context_100x1000: 668.73 MB read + 137.82 MB written
+    ("attention", "26b6e89685293154"): 806551040,
+    # link_attn_tc_kernel<1> (rotate-on-read), long_context_100x1000: 673.29 MB read + 150.55 MB written
+    ("rotate_on_read", "26b6e89685293154"): 823843328,
+    # rerotate_kernel<bf16>, long_context_100x1000: 201.36 MB read + 140.36 MB written
+    ("rerotate", "f862c45770d2a0fa"): 341722880,
+    # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.01 MB written
+    ("scheme_b", "f862c45770d2a0fa"): 448839168,
+    # decode_kernel<4>, one row per request over the long-context link: 420.65 MB read + 4.84 MB written
+    ("decode", "3e15b5e3dc89f7e3"): 425493760,
+    # compose_kernel, 32 heads x 100-chunk chain, both levels: 417.43 + 14.76 MB read + 3.60 MB written
+    ("compose", "51b0a7600676d22a"): 435783936,
 }
 
 
@@ -437,6 +439,7 @@ def run_gpu(args, rank, world):
     att_tflops = attn_flops / (att_avg / 1e3) / 1e12
     rot_gbs = rot_bytes / (rot_avg / 1e3) / 1e9
     traffic = NCU_TRAFFIC.get(("attention", _src_hash("attention.cu")))
+    ortraffic = NCU_TRAFFIC.get(("rotate_on_read", _src_hash("attention.cu")))
     rtraffic = NCU_TRAFFIC.get(("rerotate", _src_hash("rotate.cu")))
     btraffic = NCU_TRAFFIC.get(("scheme_b", _src_hash("rotate.cu")))
     dtraffic = NCU_TRAFFIC.get(("decode", _src_hash("decode.cu")))
@@ -481,6 +484,7 @@ def run_gpu(args, rank, world):
                                    "peak": tf_burst, "unit": "TFLOP/s",
                                    "frac": attn_flops / (ror[1] / 1e3) / 1e12 / tf_burst, "ms": ror[1],
                                    "ms_per_step": ror[0], "tokens_per_s": world * ror[3] / (ror[0] / 1e3),
+                                   "traffic": ortraffic,
                                    "steps": ror[2], "launches_per_step": ror[4],
                                    "kernel": "pic_link_attention_ror (framed page layout: each chunk's keys stay "
                                              "in its frame, Q is rotated back by the chunk's offset at frame "

@@ -403,21 +403,28 @@ def _main():
     ap.add_argument("--scheme", default="rotary", choices=["rotary", "ror", "nope"])
     ap.add_argument("--warmup", type=int, default=1)
     ap.add_argument("--runs", type=int, default=2)
+    ap.add_argument("--decode", action="store_true", help="time one decode step after the link instead")
     a = ap.parse_args()
     build.build()
     b = LinkBatch(PRESETS[a.workload](), scheme=a.scheme)
-    for _ in range(a.warmup):
+    if a.decode:
         b.run()
+        b.setup_decode()
+        step = b.run_decode
+    else:
+        step = b.run
+    for _ in range(a.warmup):
+        step()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.runs)]
     for e0, e1 in ev:
         e0.record()
-        b.run()
+        step()
         e1.record()
     torch.cuda.synchronize()
     if b.error():
         raise SystemExit(f"device error {b.error()}")
     ms = sum(e0.elapsed_time(e1) for e0, e1 in ev) / max(len(ev), 1)
-    print(json.dumps({"workload": a.workload, "scheme": a.scheme, "ms_per_step": ms,
+    print(json.dumps({"workload": a.workload, "scheme": a.scheme, "decode": a.decode, "ms_per_step": ms,
                       "tokens_per_s": b.tokens / (ms / 1e3), "launches_per_step": b.launches_per_step}))
 
 
