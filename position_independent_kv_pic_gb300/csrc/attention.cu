@@ -622,21 +622,19 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       f_nxt = n > 1 ? tile_frame(a, tm, un.kt0 + 1) : f_cur;
     }
     uint64_t* const q_in = kRor ? b->q_ready : b->q_full;
-    if (!wait_bar(b, &q_in[0], uq[0] & 1)) { fail(b, a.err); return; }
-    ++uq[0];
-    if (act1) {
-      if (!wait_bar(b, &q_in[1], uq[1] & 1)) { fail(b, a.err); return; }
-      ++uq[1];
-    }
-    tc::tc_fence_after();
-    {  // S for the first key tile
+    {  // S for the first key tile, each Q tile's as soon as its Q is in shared memory
       const int ks = ld % kSlots;
+      if (!wait_bar(b, &q_in[0], uq[0] & 1)) { fail(b, a.err); return; }
+      ++uq[0];
       if (!wait_tile(ld / 2)) { fail(b, a.err); return; }
       tc::tc_fence_after();
       issue_s(0, ks);
       tc::mma_commit(&b->s_full[0]);
       if (!kRor && n == 1) tc::mma_commit(&b->q_free[0]);
       if (act1) {
+        if (!wait_bar(b, &q_in[1], uq[1] & 1)) { fail(b, a.err); return; }
+        ++uq[1];
+        tc::tc_fence_after();
         issue_s(1, ks);
         tc::mma_commit(&b->s_full[1]);
         if (!kRor && n == 1) tc::mma_commit(&b->q_free[1]);
@@ -650,25 +648,46 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
       // rotating on read, key tile j + 1 in another frame than tile j needs Q rotated
       // into it: its softmax warps do that once they have written P of tile j
       const bool new_frame = kRor && more && f_nxt != f_cur;
+      if (!new_frame) {
 #pragma unroll
-      for (int i = 0; i < kQTiles; ++i) {
-        if (i == 1 && !act1) break;
-        if (!wait_bar(b, &b->p_full[i], c[i] & 1)) { fail(b, a.err); return; }
-        ++c[i];
-        tc::tc_fence_after();
-        issue_pv(i, vs, j > 0);
-        if (more) {
-          if (i == 0 && !wait_tile(nld / 2)) { fail(b, a.err); return; }
-          if (new_frame) {
-            if (!wait_bar(b, &b->q_ready[i], uq[i] & 1)) { fail(b, a.err); return; }
-            ++uq[i];
+        for (int i = 0; i < kQTiles; ++i) {
+          if (i == 1 && !act1) break;
+          if (!wait_bar(b, &b->p_full[i], c[i] & 1)) { fail(b, a.err); return; }
+          ++c[i];
+          tc::tc_fence_after();
+          issue_pv(i, vs, j > 0);
+          if (more) {
+            if (i == 0 && !wait_tile(nld / 2)) { fail(b, a.err); return; }
+            tc::tc_fence_after();
+            issue_s(i, ns);
+            tc::mma_commit(&b->s_full[i]);
+            if (!kRor && j + 2 == n) tc::mma_commit(&b->q_free[i]);  // the unit's last S product of Q tile i
+          } else {
+            tc::mma_commit(&b->o_done[i]);
           }
+        }
+      } else {
+        // a frame change: both P.V products first, so that the pipe has work while the
+        // softmax warps rotate Q into the new frame, then each Q tile's next S product
+        // once its Q is written (waiting for Q tile 0's before issuing Q tile 1's P.V
+        // left the pipe idle: rotate-on-read call 1.358 -> 1.244 ms)
+#pragma unroll
+        for (int i = 0; i < kQTiles; ++i) {
+          if (i == 1 && !act1) break;
+          if (!wait_bar(b, &b->p_full[i], c[i] & 1)) { fail(b, a.err); return; }
+          ++c[i];
+          tc::tc_fence_after();
+          issue_pv(i, vs, j > 0);
+        }
+        if (!wait_tile(nld / 2)) { fail(b, a.err); return; }
+#pragma unroll
+        for (int i = 0; i < kQTiles; ++i) {
+          if (i == 1 && !act1) break;
+          if (!wait_bar(b, &b->q_ready[i], uq[i] & 1)) { fail(b, a.err); return; }
+          ++uq[i];
           tc::tc_fence_after();
           issue_s(i, ns);
           tc::mma_commit(&b->s_full[i]);
-          if (!kRor && j + 2 == n) tc::mma_commit(&b->q_free[i]);  // the unit's last S product of Q tile i
-        } else {
-          tc::mma_commit(&b->o_done[i]);
         }
       }
       tc::mma_commit(&b->kv_empty[vs]);
@@ -819,14 +838,13 @@ __device__ __forceinline__ bool pair_sync_any(int qt, bool failed) {
 // frame `frame` (offset-table row, -1 = global).  Since RoPE(q, p) . R(Delta) k =
 // R(-Delta) RoPE(q, p) . k, the keys of a chunk can stay at their local positions
 // when Q is rotated back by the chunk's offset instead (one Q tile per frame
-// instead of one rotation per key tile read).  Thread (t, h) of the Q tile's two
-// warpgroups takes row t, columns 32h .. 32h + 31 of both 64-column halves (the
-// dimension pairs (i, i + 64) for those i) of the roped operand the Q pre-pass
-// wrote (global memory, already in the swizzled shared-memory layout), rotates
-// each pair by -theta_i * Delta in fp32 (cos / sin = hi + lo parts of the offset
-// table), rounds to bf16 and stores it at the same place in shared memory; for the
-// global frame it copies.  Then each warp arrives on q_ready[qt].  The caller
-// guarantees that no S product still reads the buffer.
+// instead of one rotation per key tile read).  The 256 threads of the Q tile's two
+// warpgroups take the roped operand the Q pre-pass wrote (global memory, already
+// in the swizzled shared-memory layout), rotate each dimension pair (i, i + 64) by
+// -theta_i * Delta in fp32 (cos / sin = hi + lo parts of the offset table), round
+// to bf16 and store it at the same place in shared memory; for the global frame
+// they copy.  Then each warp arrives on q_ready[qt].  The caller guarantees that no
+// S product still reads the buffer.
 __device__ __forceinline__ uint32_t rot_pair_bf16(uint32_t& whi, uint32_t wlo, const float4& t0, const float4& t1) {
   const float c0 = t0.x + t0.z, s0 = t0.y + t0.w, c1 = t1.x + t1.z, s1 = t1.y + t1.w;
   const float a0 = __uint_as_float(wlo << 16), a1 = __uint_as_float(wlo & 0xffff0000u);
@@ -840,29 +858,35 @@ __device__ __forceinline__ void prep_q_frame(const TcArgs& a, uint8_t* smem, Bar
                                              int t, int frame) {
   const uint8_t* src = a.q_tiles + (((int64_t)un.tile * a.Hkv + un.head) * kQTiles + qt) * kOpBytes;
   uint8_t* dst = smem + kOffQ + qt * kOpBytes;
+  // thread (h, t) of the Q tile's 256: column chunk c (dimensions 8c .. 8c + 7 and
+  // their partners + 64) of rows r0, r0 + 32, r0 + 64, r0 + 96, so that it needs the
+  // cos / sin of only 8 frequencies
+  const int tid = h * kM + t, c = tid & 7, r0 = tid >> 3;
   uint4 lo[4], hi[4];
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    const uint32_t off = sw128_off(t, 4 * h + cc);
-    lo[cc] = *reinterpret_cast<const uint4*>(src + off);
-    hi[cc] = *reinterpret_cast<const uint4*>(src + kHalfBytes + off);
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t off = sw128_off(r0 + 32 * k, c);
+    lo[k] = *reinterpret_cast<const uint4*>(src + off);
+    hi[k] = *reinterpret_cast<const uint4*>(src + kHalfBytes + off);
   }
   if (frame >= 0) {
-    const float4* cs = a.rot_tab + (int64_t)frame * (kD / 2) + 32 * h;
+    const float4* cs = a.rot_tab + (int64_t)frame * (kD / 2) + 8 * c;
+    float4 tb[8];
 #pragma unroll
-    for (int cc = 0; cc < 4; ++cc) {
-      uint32_t* lw = reinterpret_cast<uint32_t*>(&lo[cc]);
-      uint32_t* hw = reinterpret_cast<uint32_t*>(&hi[cc]);
+    for (int e = 0; e < 8; ++e) tb[e] = __ldg(cs + e);
 #pragma unroll
-      for (int e = 0; e < 4; ++e)  // dimensions 32h + 8cc + 2e, + 1 and their partners + 64
-        lw[e] = rot_pair_bf16(hw[e], lw[e], __ldg(cs + 8 * cc + 2 * e), __ldg(cs + 8 * cc + 2 * e + 1));
+    for (int k = 0; k < 4; ++k) {
+      uint32_t* lw = reinterpret_cast<uint32_t*>(&lo[k]);
+      uint32_t* hw = reinterpret_cast<uint32_t*>(&hi[k]);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) lw[e] = rot_pair_bf16(hw[e], lw[e], tb[2 * e], tb[2 * e + 1]);
     }
   }
 #pragma unroll
-  for (int cc = 0; cc < 4; ++cc) {
-    const uint32_t off = sw128_off(t, 4 * h + cc);
-    *reinterpret_cast<uint4*>(dst + off) = lo[cc];
-    *reinterpret_cast<uint4*>(dst + kHalfBytes + off) = hi[cc];
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t off = sw128_off(r0 + 32 * k, c);
+    *reinterpret_cast<uint4*>(dst + off) = lo[k];
+    *reinterpret_cast<uint4*>(dst + kHalfBytes + off) = hi[k];
   }
   tc::fence_proxy_async_smem();
   __syncwarp();
