@@ -196,6 +196,32 @@ def time_link(batch, steps, l2_flush, stream):
             [a.elapsed_time(b) for a, b in att_ev])
 
 
+def time_graph(batch, steps, warmup, l2_flush, stream):
+    """The same step captured as one CUDA graph (LinkGraph), `steps` replays timed with
+    CUDA events, L2 flushed before each.  Returns (per-replay ms, None) or (None, the
+    reason the capture failed)."""
+    import torch
+    from position_independent_kv_pic_gb300.link import LinkGraph
+    try:
+        g = LinkGraph(batch)
+    except RuntimeError as e:  # reported in the result line; the eager step stands
+        torch.cuda.synchronize()
+        return None, str(e).splitlines()[0][:200]
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    evs = [(ev(), ev()) for _ in range(steps)]
+    for i in range(steps):
+        l2_flush()
+        evs[i][0].record(stream)
+        g.replay()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    del g
+    return [a.elapsed_time(b) for a, b in evs], None
+
+
 def link_output(batch):
     """The step's attention output from the pool as cached (the in-place re-rotation
     of a repeated step would rotate K again), copied to the host."""
@@ -226,8 +252,13 @@ def per_config_gpu(name, steps, warmup, l2_flush, stream, hbm, tf_burst):
     if b.error() != 0:
         raise SystemExit(f"device error ({name}): {b.error()}")
     ms, rms, ams = statistics.mean(st), statistics.mean(ro), statistics.mean(at)
+    gms, gerr = time_graph(b, steps, warmup, l2_flush, stream)
+    if b.error() != 0:
+        raise SystemExit(f"device error ({name}, graph): {b.error()}")
     entry = {"workload": name, "requests": b.n_req, "chunks": b.n_chunks, "tokens": b.tokens, "rows": b.n_rows,
              "steps": steps, "ms_per_step": ms, "tokens_per_s": b.tokens / (ms / 1e3),
+             "graph": ({"ms_per_step": statistics.mean(gms), "tokens_per_s": b.tokens / (statistics.mean(gms) / 1e3)}
+                       if gms else {"error": gerr}),
              "attention": {"ms": ams, "tflops": flops / (ams / 1e3) / 1e12,
                            "frac": flops / (ams / 1e3) / 1e12 / tf_burst, "flop": flops},
              "rerotate": {"ms": rms, "gbs": rot_bytes / (rms / 1e3) / 1e9,
@@ -281,14 +312,18 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_wall0 = time.perf_counter()
+        # eager steps (ten launches from the host on three streams), with the re-rotation
+        # and attention runs timed inside, then the same step as one CUDA graph launch
         step_ms, rot_ms, att_ms = time_link(batch, K, l2_flush, stream)
+        graph_ms, graph_err = time_graph(batch, K, args.warmup, l2_flush, stream)
         t_wall = time.perf_counter() - t_wall0
     if world > 1:
         dist.barrier()
     if batch.error() != 0:
         raise SystemExit(f"device error: {pic.pic_strerror(batch.error())}")
 
-    total_ms = reduce_max(sum(step_ms), "cuda")
+    eager_total_ms = reduce_max(sum(step_ms), "cuda")
+    total_ms = reduce_max(sum(graph_ms), "cuda") if graph_ms else eager_total_ms
     tokens = batch.tokens
     value = whole_job_throughput(world, K, tokens, total_ms)
 
@@ -447,13 +482,16 @@ def run_gpu(args, rank, world):
 
     result = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
-        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "ms_per_step": total_ms / K, "ms_per_step_eager": eager_total_ms / K,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.dtype,
         "data": "synthetic: seeded N(0,1) K/V/Q, cached K drawn as stored (position-encoded) keys",
         "config": {"workload": wl.name, "requests": batch.n_req, "chunks": batch.n_chunks,
                    "tokens": tokens, "rows": batch.n_rows, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
                    "page": 16, "pages": batch.n_pages, "rot_pages": batch.n_rot,
                    "l2": "flushed (512 MB read, untimed) before every timed step",
+                   "launch": ("one CUDA graph per step (the step's ten kernels on three streams)" if graph_ms
+                              else f"eager (graph capture failed: {graph_err})"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": tf_burst, "unit": "TFLOP/s",
                      "frac": att_tflops / tf_burst, "traffic": traffic,

@@ -432,6 +432,26 @@ if __name__ == "__main__":
     _main()
 
 
+class LinkGraph:
+    """One link step (every kernel of LinkBatch.run on its three streams) captured as a
+    CUDA graph, so that a step costs one graph launch instead of ten kernel launches
+    from the host.  The graph reads and writes the batch's own device buffers: update
+    their contents (same shapes) between replays, not the tensors."""
+
+    def __init__(self, batch: LinkBatch):
+        self.b = batch
+        batch.run()  # loads the device code and sets kernel attributes outside the capture
+        torch.cuda.synchronize(batch.device)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            batch.run()
+        torch.cuda.synchronize(batch.device)
+
+    def replay(self):
+        """Launch the captured step on the current stream."""
+        self.graph.replay()
+
+
 class LinkPipeline:
     """Link steps back to back with every step's input upload (host -> device, from
     pinned memory) and output read-back (device -> host) on their own copy streams,

@@ -190,3 +190,24 @@ def test_pipelined_steps_match_single_steps():
     torch.cuda.synchronize()
     assert b.error() == 0
     assert torch.equal(results[-1][0], ref) and torch.equal(results[-2][0], ref)
+
+
+@pytest.mark.parametrize("scheme", ["rotary", "ror", "nope"])
+def test_graph_replay_equals_the_eager_step(scheme):
+    """The step captured as a CUDA graph (LinkGraph) gives the eager step's output bit
+    for bit, replay after replay (the pool reset to the cached chunks each time)."""
+    from position_independent_kv_pic_gb300.link import LinkGraph
+
+    b = LinkBatch(inputs.rag_prompt(), scheme=scheme)
+    b.run()
+    torch.cuda.synchronize()
+    assert b.error() == 0
+    ref = b.out.clone()
+    g = LinkGraph(b)
+    for _ in range(3):
+        b.reset_pool()
+        b.out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert b.error() == 0
+        assert torch.equal(b.out, ref)
