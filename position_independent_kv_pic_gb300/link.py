@@ -457,13 +457,25 @@ class LinkPipeline:
     pinned memory) and output read-back (device -> host) on their own copy streams,
     overlapped with the neighbouring steps' kernels: the device inputs and outputs
     are double-buffered, so step i + 1's upload and step i - 1's read-back run while
-    step i computes.  The step itself is LinkBatch.run on the current stream."""
+    step i computes.  The step itself is LinkBatch.run on the current stream, or with
+    ``graphs`` one CUDA graph per buffer set (captured once, replayed per step)."""
 
-    def __init__(self, batch: LinkBatch):
+    def __init__(self, batch: LinkBatch, graphs: bool = False):
         self.b = batch
         dev = batch.device
-        self.sets = [batch.dev, {n: torch.empty_like(t) for n, t in batch.dev.items()}]
+        self.sets = [batch.dev, {n: t.clone() for n, t in batch.dev.items()}]
         self.outs = [batch.out, torch.empty_like(batch.out)]
+        self.graphs = None
+        if graphs:
+            self.graphs = []
+            for k in range(2):
+                batch.run(inputs=self.sets[k], out=self.outs[k])  # outside the capture first
+                torch.cuda.synchronize(dev)
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g):
+                    batch.run(inputs=self.sets[k], out=self.outs[k])
+                self.graphs.append(g)
+            torch.cuda.synchronize(dev)
         self.host_out = [torch.empty(batch.out.shape, dtype=batch.out.dtype).pin_memory() for _ in range(2)]
         self.h2d = torch.cuda.Stream(dev)
         self.d2h = torch.cuda.Stream(dev)
@@ -494,7 +506,11 @@ class LinkPipeline:
         main.wait_event(self.uploaded[k])
         if self.i >= 2:
             main.wait_event(self.read[k])  # out k's previous result has been read back
-        self.b.run(stream=main, inputs=self.sets[k], out=self.outs[k])
+        if self.graphs is not None:
+            with torch.cuda.stream(main):
+                self.graphs[k].replay()
+        else:
+            self.b.run(stream=main, inputs=self.sets[k], out=self.outs[k])
         self.computed[k].record(main)
         self.d2h.wait_event(self.computed[k])
         with torch.cuda.stream(self.d2h):

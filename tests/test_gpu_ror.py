@@ -162,10 +162,11 @@ def test_plan_and_run_equal_the_single_call():
     assert torch.equal(out, b.out)
 
 
-def test_pipelined_steps_match_single_steps():
+@pytest.mark.parametrize("graphs", [False, True])
+def test_pipelined_steps_match_single_steps(graphs):
     """LinkPipeline (uploads and read-backs on copy streams, double-buffered inputs and
-    outputs) gives every step the single step's result: shared chunks rotated out of
-    place, so repeated steps are identical."""
+    outputs; eagerly or as one CUDA graph per buffer set) gives every step the single
+    step's result: shared chunks rotated out of place, so repeated steps are identical."""
     from position_independent_kv_pic_gb300.link import LinkPipeline
 
     b = LinkBatch(inputs.batched_shared())
@@ -174,7 +175,7 @@ def test_pipelined_steps_match_single_steps():
     assert b.error() == 0
     ref = b.out.cpu()
     b.pin_host_inputs()
-    pipe = LinkPipeline(b)
+    pipe = LinkPipeline(b, graphs=graphs)
     pipe.begin()
     outs = []
     for _ in range(5):
