@@ -45,8 +45,8 @@ UNIT = "tokens/s"
 # two-launch composition), with the kernel source they were taken from; reported
 # as roofline traffic only while the source is unchanged.
 NCU_TRAFFIC = {
-    # link_attn_tc_kernel<0>, long_context_100x1000: 668.73 MB read + 137.82 MB written
-    ("attention", "26b6e89685293154"): 806551040,
+    # link_attn_tc_kernel<0>, long_context_100x1000: 664.08 MB read + 137.69 MB written
+    ("attention", "7f2ed6ae9aec8cb2"): 801773312,
     # link_attn_tc_kernel<1> (rotate-on-read), long_context_100x1000: 676.23 MB read + 148.15 MB written
     ("rotate_on_read", "7f2ed6ae9aec8cb2"): 824385024,
     # rerotate_kernel<bf16>, long_context_100x1000: 201.36 MB read + 140.36 MB written
