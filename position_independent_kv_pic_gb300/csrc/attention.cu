@@ -390,10 +390,19 @@ struct TcArgs {
 };
 
 constexpr int kUnitRing = 2;                  // unit indices in flight from the producer
+// Slot frees: the MMA issuer commits once per step (a unit's start, then each key
+// tile) to kv_step[step % kStepRing]; a step frees the slots its products last read
+// (the start the unit's first K, step j V_j and K_(j+1)).  Before load L the producer
+// waits for the step that freed load L - kSlots; a later step can complete first only
+// if all the loads it reads precede L, i.e. lie among the kSlots loads before it:
+// at most three key tiles' worth, each read by at most two steps (a unit's start and
+// its first step), so at most five steps run ahead and eight barriers keep every
+// awaited phase's parity unambiguous.
+constexpr int kStepRing = 8;
 constexpr int kUnitReaders = 1 + 2 + 4 * kSmWarpgroups;  // MMA thread, 2 V-zeroing warps, softmax warps
 
 struct Bars {
-  uint64_t kv_full[kSlots], kv_empty[kSlots];
+  uint64_t kv_full[kSlots], kv_step[kStepRing];
   // key tile t (t % kSlots) ready for the MMAs: its K and V landed, K rotated to its
   // global positions when rotating on read, V's invalid rows zeroed
   uint64_t vz_done[kSlots];
@@ -404,6 +413,7 @@ struct Bars {
   uint64_t unit_full[kUnitRing], unit_empty[kUnitRing];
   uint64_t never;  // no thread ever arrives on it (the failure-injection test build waits on it)
   int unit_idx[kUnitRing];
+  uint32_t free_step[kSlots];  // producer lane 0 only: the step that frees each slot's load
   uint32_t tmem_base;
   int abort;
 };
@@ -485,6 +495,9 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
                               uint8_t* smem, Bars* b, int n_units) {
   const int lane = threadIdx.x & 31;
   uint32_t ld = 0, uq[kQTiles] = {0, 0};
+  // the issuer's step numbering: a unit's start, then one step per key tile; the
+  // start frees the unit's first K, step j frees V_j and K_(j+1)
+  uint32_t s0 = 0;
   int u = blockIdx.x;
   for (uint32_t k = 0;; ++k) {
     int go = 1;
@@ -533,9 +546,16 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
         for (int kv = 0; kv < 2; ++kv) {
           const int slot = ld % kSlots;
           if (lane == 0) {
-            go = wait_bar(b, &b->kv_empty[slot], ((ld / kSlots) & 1) ^ 1);
-            if (!go) fail(b, a.err);
-            else tc::mbar_arrive_expect_tx(&b->kv_full[slot], bytes);
+            if (ld >= (uint32_t)kSlots) {
+              const uint32_t fs = b->free_step[slot];
+              go = wait_bar(b, &b->kv_step[fs % kStepRing], (fs / kStepRing) & 1);
+            }
+            if (!go) {
+              fail(b, a.err);
+            } else {
+              b->free_step[slot] = s0 + (uint32_t)(kt - un.kt0) + (uint32_t)kv;
+              tc::mbar_arrive_expect_tx(&b->kv_full[slot], bytes);
+            }
           }
           // a slot is armed only when all its boxes are issued right after
           if (!__shfl_sync(0xffffffffu, go, 0)) goto drain;
@@ -549,6 +569,7 @@ __device__ void producer_loop(const TcArgs& a, const CUtensorMap* kmap, const CU
         }
       }
     }
+    s0 += (uint32_t)(un.kt1 - un.kt0) + 1u;
     u = __shfl_sync(0xffffffffu, u_next, 0);
   }
 drain:
@@ -573,7 +594,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
   const uint32_t q_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffQ), 16);
   const uint32_t k_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), 16);
   const uint32_t v_lo = tc::sw128_desc_lo(tc::smem_addr(smem + kOffSlot), kPageHalfBytes);
-  uint32_t ld = 0, uq[kQTiles] = {0, 0}, c[kQTiles] = {0, 0};
+  uint32_t ld = 0, uq[kQTiles] = {0, 0}, c[kQTiles] = {0, 0}, st = 0;
   // Key tile t: its K and V landed (the V-zeroing warps waited for both loads),
   // K rotated when rotating on read, V's invalid rows zeroed.  The issuer waits for
   // this one barrier per tile, before the tile's first S product, and never for the
@@ -639,7 +660,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
         tc::mma_commit(&b->s_full[1]);
         if (!kRor && n == 1) tc::mma_commit(&b->q_free[1]);
       }
-      tc::mma_commit(&b->kv_empty[ks]);
+      tc::mma_commit(&b->kv_step[st++ % kStepRing]);  // frees the first K
     }
     for (int j = 0; j < n; ++j, ld += 2) {
       const uint32_t vld = ld + 1, nld = ld + 2;
@@ -690,8 +711,7 @@ __device__ void mma_loop(const TcArgs& a, uint8_t* smem, Bars* b, uint32_t tmem,
           tc::mma_commit(&b->s_full[i]);
         }
       }
-      tc::mma_commit(&b->kv_empty[vs]);
-      if (more) tc::mma_commit(&b->kv_empty[ns]);
+      tc::mma_commit(&b->kv_step[st++ % kStepRing]);  // frees V_j and K_(j+1)
       if (kRor) {
         f_cur = f_nxt;
         if (j + 2 < n) f_nxt = tile_frame(a, tm, un.kt0 + j + 2);
@@ -1135,9 +1155,9 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSlots; ++s) {
       tc::mbar_init(&b->kv_full[s], 1);
-      tc::mbar_init(&b->kv_empty[s], 1);
       tc::mbar_init(&b->vz_done[s], 2);
     }
+    for (int s = 0; s < kStepRing; ++s) tc::mbar_init(&b->kv_step[s], 1);
     for (int i = 0; i < kQTiles; ++i) {
       tc::mbar_init(&b->q_full[i], 1);
       tc::mbar_init(&b->q_free[i], 1);

@@ -4,7 +4,8 @@ The roles that share the five K/V slots — the TMA producer (K and V of every k
 tile, in turn), the V-zeroing warps (wait for the tile's K load, then its V
 load, zero V's invalid rows, arrive vz_done),
 the MMA issuer (waits only for vz_done of a tile before its first S product and
-for the softmax's P; commits each slot free when its products complete) and the
+for the softmax's P; commits once per step to a ring of step barriers: a unit's
+start frees its first K, key tile j's step frees V_j and K_(j+1)) and the
 softmax (P from S) — are coroutines over the kernel's mbarriers, run in random
 interleavings with the hardware's wait semantics (a wait for phase k passes
 whenever the current phase's parity differs from k's) and copies that complete
@@ -13,7 +14,8 @@ reaches it through vz_done, which the model checks by recording, at every MMA,
 whether the slot it reads holds the load it means.  The shipped protocol must
 never deadlock, let a wait pass on a wrong phase or read a slot too early; the
 variant whose V-zeroing warps waited only for the V loads of a slot (skipping
-its K phases) is caught.  A second model covers rotate-on-read's handshake on the
+its K phases) is caught, and so is a step ring of four barriers, which runs of
+one-tile units let the issuer lap.  A second model covers rotate-on-read's handshake on the
 Q tile (written per key frame by the softmax warps, waited for by the issuer)."""
 
 import random
@@ -23,9 +25,14 @@ import pytest
 from test_compose_protocol import Agent, Aliased, Bar
 
 SLOTS = 5
+STEP_RING = 8
 
 
-def run(n_tiles, n_units, seed, vzero_waits_k=True, mma_waits_tile=True):
+def run(tiles, seed, vzero_waits_k=True, mma_waits_tile=True, ring=STEP_RING, lagging_producer=False):
+    """tiles[u]: key tiles of the CTA's unit u.  lagging_producer: the producer moves
+    only once every other role is blocked and no copy or commit is in flight (a
+    producer as slow as the protocol allows: the issuer runs as far ahead on the step
+    barriers as the loads let it)."""
     rng = random.Random(seed)
     bars = {}
 
@@ -34,13 +41,14 @@ def run(n_tiles, n_units, seed, vzero_waits_k=True, mma_waits_tile=True):
 
     for s in range(SLOTS):
         mk(f"kv_full{s}", 1)
-        mk(f"kv_empty{s}", 1)
         mk(f"vz_done{s}", 1)
+    for r in range(ring):
+        mk(f"kv_step{r}", 1)
     mk("s_full", 1)
     mk("p_full", 1)
     inflight, pipe = [], []
     landed = {}  # slot -> load number whose data the slot holds
-    total = n_tiles * n_units  # key tiles over the CTA's units, loads ld = 0 .. 2 total - 1
+    total = sum(tiles)  # key tiles over the CTA's units, loads ld = 0 .. 2 total - 1
 
     def land(s, ld):
         def f():
@@ -49,11 +57,18 @@ def run(n_tiles, n_units, seed, vzero_waits_k=True, mma_waits_tile=True):
         return f
 
     def producer():
-        for ld in range(2 * total):
-            s = ld % SLOTS
-            if ld >= SLOTS:
-                yield ("wait", f"kv_empty{s}", ld // SLOTS - 1)
-            yield ("act", lambda s=s, ld=ld: inflight.append(land(s, ld)))
+        ld, s0, free_step = 0, 0, [0] * SLOTS
+        for n in tiles:
+            for t in range(n):
+                for kv in range(2):
+                    s = ld % SLOTS
+                    if ld >= SLOTS:
+                        fs = free_step[s]
+                        yield ("wait", f"kv_step{fs % ring}", fs // ring)
+                    free_step[s] = s0 + t + kv
+                    yield ("act", lambda s=s, ld=ld: inflight.append(land(s, ld)))
+                    ld += 1
+            s0 += n + 1
 
     def reads(ld):  # an MMA that reads load ld's slot: the data must be there
         def f():
@@ -62,12 +77,13 @@ def run(n_tiles, n_units, seed, vzero_waits_k=True, mma_waits_tile=True):
         return f
 
     def mma():
-        ld, c = 0, 0
-        for _ in range(n_units):
+        ld, c, st = 0, 0, 0
+        for n_tiles in tiles:
             yield ("wait", f"vz_done{(ld // 2) % SLOTS}", (ld // 2) // SLOTS)  # S of the unit's first tile
             yield ("act", reads(ld))
             pipe.append("s_full")
-            pipe.append(f"kv_empty{ld % SLOTS}")
+            pipe.append(f"kv_step{st % ring}")  # frees the unit's first K
+            st += 1
             for j in range(n_tiles):
                 vld, nld = ld + 1, ld + 2
                 yield ("wait", "p_full", c)
@@ -79,9 +95,8 @@ def run(n_tiles, n_units, seed, vzero_waits_k=True, mma_waits_tile=True):
                         yield ("wait", f"vz_done{(nld // 2) % SLOTS}", (nld // 2) // SLOTS)
                     yield ("act", reads(nld))
                     pipe.append("s_full")
-                yield ("act", lambda vs=vld % SLOTS: pipe.append(f"kv_empty{vs}"))
-                if more:
-                    yield ("act", lambda ns=nld % SLOTS: pipe.append(f"kv_empty{ns}"))
+                yield ("act", lambda r=st % ring: pipe.append(f"kv_step{r}"))  # frees V_j and K_(j+1)
+                st += 1
                 ld += 2
 
     def softmax():
@@ -104,6 +119,20 @@ def run(n_tiles, n_units, seed, vzero_waits_k=True, mma_waits_tile=True):
         if not live and not inflight and not pipe:
             return "ok"
         moved = False
+        if lagging_producer:
+            others = [a for a in live if a.name != "producer"]
+            rng.shuffle(others)
+            if any(a.step(bars) for a in others):
+                continue
+            if inflight:
+                inflight.pop(rng.randrange(len(inflight)))()
+                continue
+            if pipe:
+                bars[pipe.pop(0)].arrive()
+                continue
+            if any(a.step(bars) for a in live if a.name == "producer"):
+                continue
+            return "deadlock: " + str([(a.name, a.cur[:3] if a.cur else None) for a in agents if not a.done])
         if inflight and rng.random() < 0.3:
             inflight.pop(rng.randrange(len(inflight)))()
             moved = True
@@ -125,17 +154,33 @@ def run(n_tiles, n_units, seed, vzero_waits_k=True, mma_waits_tile=True):
                 return "deadlock: " + str([(a.name, a.cur[:3] if a.cur else None) for a in agents if not a.done])
 
 
-@pytest.mark.parametrize("n_tiles,n_units", [(1, 6), (2, 4), (3, 3), (8, 2), (13, 1)])
-def test_shipped_slot_protocol_is_safe(n_tiles, n_units):
+@pytest.mark.parametrize("tiles", [[1] * 6, [2] * 4, [3] * 3, [8] * 2, [13], [1] * 12,
+                                   [1, 3, 1, 1, 2, 1, 1, 5], [4, 1, 1, 1, 1, 6]])
+@pytest.mark.parametrize("lagging_producer", [False, True])
+def test_shipped_slot_protocol_is_safe(tiles, lagging_producer):
     for seed in range(160):
-        assert run(n_tiles, n_units, seed) == "ok", (n_tiles, n_units, seed)
+        assert run(tiles, seed, lagging_producer=lagging_producer) == "ok", (tiles, seed)
+
+
+def test_step_ring_of_four_is_caught():
+    """Runs of one-tile units let the issuer complete five steps past the one the
+    producer waits for: four barriers alias a phase."""
+    caught = 0
+    for seed in range(20):
+        try:
+            r = run([1] * 12, seed, ring=4, lagging_producer=True)
+        except Aliased:
+            caught += 1
+            continue
+        caught += r != "ok"
+    assert caught > 0
 
 
 def test_v_zeroing_that_skips_k_phases_is_caught():
     caught = 0
     for seed in range(300):
         try:
-            run(1, 8, seed, vzero_waits_k=False)
+            run([1] * 8, seed, vzero_waits_k=False)
         except Aliased:
             caught += 1
     assert caught > 0
@@ -146,7 +191,7 @@ def test_issuer_that_skips_the_tile_wait_is_caught():
     caught = 0
     for seed in range(300):
         try:
-            r = run(4, 2, seed, mma_waits_tile=False)
+            r = run([4, 4], seed, mma_waits_tile=False)
         except Aliased:
             caught += 1
             continue
