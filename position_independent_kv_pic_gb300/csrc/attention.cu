@@ -52,7 +52,7 @@ constexpr int kPagesPerKt = kKeys / PIC_PAGE;
 constexpr int kSlots = 5;               // K/V ring slots (32 KB each)
 constexpr int kSmWarpgroups = 2 * kQTiles;  // softmax: one warpgroup per (Q tile, half of the key columns)
 constexpr int kThreads = 128 * (1 + kSmWarpgroups);
-constexpr int kMinSpan = 8;             // key tiles per unit, lower bound
+constexpr int kMinSpan = 4;             // key tiles per unit, lower bound
 constexpr int kSpanPref = 16;           // ... and while every SM still gets a unit
 constexpr int kUnitsPerSm = 6;          // target units per SM when splitting
 constexpr int kMaxSplitUnits = 960;     // bound on the units splitting may add
@@ -273,7 +273,9 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
   // about six units per SM balance the long calls (measured: 4 or 5 left SMs idle
   // at the end of the long-context call, 7 or 8 paid more unit overhead); a short
   // call keeps spans of at least 16 tiles as long as every SM still gets a unit,
-  // since each unit pays a Q load and a pipeline fill
+  // since each unit pays a Q load and a pipeline fill, and a call too short for that
+  // spreads over more SMs in spans down to 4 tiles (6-chunk prompt: 46 -> 41 us; 2
+  // tiles slowed the 20-chunk call by a tenth)
   const int64_t target = min((int64_t)kUnitsPerSm * num_sms, (int64_t)kMaxSplitUnits);
   const int64_t span_fill = min((int64_t)kSpanPref, (work + num_sms - 1) / num_sms);
   const int span = (int)max((int64_t)kMinSpan, max((work + target - 1) / target, span_fill));
