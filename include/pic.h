@@ -543,6 +543,18 @@ pic_status pic_compose_states(const void* T_split, const float* S_pool, int64_t 
 pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, float* d_mnmajor,
                              float* d_tmem_a, int32_t* err_flag, pic_stream_t stream);
 
+/* The CTA-pair products (tcgen05 cta_group::2: two SMs on one M = 256 product, B
+ * split along N between them) with the operand layouts of the two-SM attention:
+ *   d_s[m][n]  = sum_k a[m][k] * b[n][k]     m < 256, n < 256 (S = Q.K^T: CTA r
+ *                holds rows 128r.. of a and keys 128r.. of b)
+ *   d_pv[m][n] = sum_j a[m][j] * v[j][n]     m < 256, j, n < 128 (P.V: P from
+ *                TMEM, CTA r holds columns 64r.. of v)
+ * a, b: [256][128] bf16; v: [128][128] bf16 (device, row-major); d_s [256][256],
+ * d_pv [256][128] fp32 (device); info [2] int32: the TMEM base address each CTA
+ * was given.  One launch of one cluster of two CTAs.  Not part of the link step. */
+pic_status pic_selftest_umma_pair(const void* a, const void* b, const void* v, float* d_s, float* d_pv,
+                                  int32_t* info, int32_t* err_flag, pic_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -23,7 +23,8 @@ __all__ = [
     "pic_count_rows", "pic_request_sizes_of", "pic_plan_offsets", "pic_strerror",
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
-    "pic_selftest_umma", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES", "EXPORTED",
+    "pic_selftest_umma", "pic_selftest_umma_pair", "pic_link_attention_noalloc", "PIC_NOALLOC_SCRATCH_BYTES",
+    "EXPORTED",
     "pic_decode_workspace", "pic_decode_attention", "pic_rope_cached_k",
     "pic_compose_segment", "pic_compose_workspace", "pic_compose_states", "pic_link_attention_ror",
     "pic_link_attention_plan", "pic_link_attention_run", "pic_compose_split_t",
@@ -51,7 +52,8 @@ EXPORTED = (
     "pic_count_rows", "pic_request_sizes_of", "pic_plan_offsets", "pic_strerror",
     "pic_select_rows", "pic_splice_pages", "pic_rope_table", "pic_rerotate_k",
     "pic_write_fresh_kv", "pic_link_attention_workspace", "pic_link_attention",
-    "pic_selftest_umma", "pic_link_attention_noalloc", "pic_decode_workspace", "pic_decode_attention",
+    "pic_selftest_umma", "pic_selftest_umma_pair", "pic_link_attention_noalloc", "pic_decode_workspace",
+    "pic_decode_attention",
     "pic_rope_cached_k", "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
     "pic_link_attention_ror", "pic_link_attention_plan", "pic_link_attention_run", "pic_compose_split_t",
 )
@@ -95,6 +97,7 @@ _SIGS = {
     "pic_link_attention": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
                                           _I64, _I32, _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
     "pic_selftest_umma": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P]),
+    "pic_selftest_umma_pair": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _P, _P]),
     "pic_link_attention_noalloc": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32,
                                                   _I64, _I32, _I32, _I32, _F32, _P, _P, _P]),
     "pic_decode_workspace": (_SZ, [_I32, _I32, _I32, _I32, ctypes.c_int]),
@@ -321,6 +324,11 @@ def pic_compose_states(T_split, S_pool, ids, chain_off, n_req: int, n_elems: int
 def pic_selftest_umma(a, b, d_kmajor, d_mnmajor, d_tmem_a, err_flag, stream=None):
     _check(load().pic_selftest_umma(_ptr(a), _ptr(b), _ptr(d_kmajor), _ptr(d_mnmajor), _ptr(d_tmem_a),
                                     _ptr(err_flag), _stream(stream)), "pic_selftest_umma")
+
+
+def pic_selftest_umma_pair(a, b, v, d_s, d_pv, info, err_flag, stream=None):
+    _check(load().pic_selftest_umma_pair(_ptr(a), _ptr(b), _ptr(v), _ptr(d_s), _ptr(d_pv), _ptr(info),
+                                         _ptr(err_flag), _stream(stream)), "pic_selftest_umma_pair")
 
 
 def pic_link_attention_noalloc(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, pages, page_off,

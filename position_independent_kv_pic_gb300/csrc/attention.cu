@@ -1216,6 +1216,134 @@ link_attn_tc_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_const
   }
 }
 
+// ------------------------------------------------------------------ CTA-pair self-test
+// One pair of CTAs (a cluster of two): the pair products the two-SM attention
+// issues, on operands laid out as that kernel lays them out, read back from both
+// CTAs' TMEM.  CTA r holds rows 128r.. of A, keys 128r.. of B (K-major pages) and
+// columns 64r.. of V (one half page per 16 keys).  Each CTA allocates 256 TMEM
+// columns; info[r] receives the base address CTA r was given.
+constexpr int kPairTestSmem = 2 * kOpBytes + kOpBytes / 2 + 64;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(128, 1)
+selftest_umma_pair_kernel(const bf16* __restrict__ a, const bf16* __restrict__ b, const bf16* __restrict__ v,
+                          float* ds, float* dpv, int32_t* info, int32_t* err) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint8_t* sa = smem;                 // A: own 128 rows, two 64-column halves
+  uint8_t* sb = smem + kOpBytes;      // B: own 128 keys as 8 pages
+  uint8_t* sv = smem + 2 * kOpBytes;  // V: own 64 columns of 128 keys, 8 half pages
+  uint64_t* done = reinterpret_cast<uint64_t*>(sv + kOpBytes / 2);
+  uint32_t* tslot = reinterpret_cast<uint32_t*>(done + 1);
+  int* ab = reinterpret_cast<int*>(done + 2);
+  const int t = threadIdx.x, warp = t >> 5;
+  const uint32_t r = tc::cluster_rank();
+  if (t == 0) {
+    tc::mbar_init(done, 1);
+    *ab = 0;
+    tc::fence_mbar_init_cluster();
+  }
+  if (warp == 0) {
+    tc::tmem_alloc2(tslot, 256);
+    tc::tmem_relinquish2();
+  }
+  // operands: thread t fills row / key t
+  {
+    const int row = 128 * r + t;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(sa + h * kHalfBytes + sw128_off(t, cc)) =
+            *reinterpret_cast<const uint4*>(a + row * 128 + h * 64 + cc * 8);
+    const int pg = t / PIC_PAGE, sl = t % PIC_PAGE, grp = sl / 8, rr = sl % 8;
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+      for (int cc = 0; cc < 8; ++cc)
+        *reinterpret_cast<uint4*>(sb + pg * kPageBytes + grp * kGroupBytes + h * kPageHalfBytes + rr * 128 +
+                                  ((cc ^ rr) << 4)) = *reinterpret_cast<const uint4*>(b + row * 128 + h * 64 + cc * 8);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc)
+      *reinterpret_cast<uint4*>(sv + pg * (kPageBytes / 2) + grp * kPageHalfBytes + rr * 128 + ((cc ^ rr) << 4)) =
+          *reinterpret_cast<const uint4*>(v + t * 128 + 64 * r + cc * 8);
+  }
+  tc::fence_proxy_async_smem();
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();  // both CTAs' operands and barrier in place
+  tc::tc_fence_after();
+  const uint32_t tmem = *tslot;
+  if (t == 0) info[r] = (int32_t)tmem;
+  const uint32_t lb = (uint32_t)((warp * 32) << 16);
+  constexpr uint32_t kIdS2 = tc::idesc_bf16_f32(256, 256, false);
+  constexpr uint32_t kIdPV2 = tc::idesc_bf16_f32(256, 128, true);
+  // S = A B^T (256 x 256)
+  if (r == 0 && t == 0) {
+    const uint32_t sa_a = tc::smem_addr(sa), sb_a = tc::smem_addr(sb);
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t aoff = (ks >> 2) * kHalfBytes + (ks & 3) * 32;
+      const uint32_t boff = (ks >> 2) * kPageHalfBytes + (ks & 3) * 32;
+      tc::mma2_bf16_ss(tmem, tc::sw128_desc(sa_a + aoff, 16, 1024), tc::sw128_desc(sb_a + boff, 16, kGroupBytes),
+                       kIdS2, ks > 0);
+    }
+    tc::mma2_commit(done, 3);
+  }
+  bool ok = tc::mbar_wait(done, 0, ab, kWaitLimitNs);
+  if (!__all_sync(0xffffffffu, ok)) {
+    if ((t & 31) == 0) set_err(err, PIC_ERR_TIMEOUT);
+  } else {
+    tc::tc_fence_after();
+    for (int c0 = 0; c0 < 256; c0 += 32) {
+      uint32_t x[32];
+      tc::tmem_ld32(tmem + lb + c0, x);
+      tc::tmem_ld_wait();
+      tc::reg_fence<32>(x);
+      for (int k = 0; k < 32; ++k) ds[(int64_t)(128 * r + t) * 256 + c0 + k] = u2f(x[k]);
+    }
+  }
+  // P = A's first 128 columns into TMEM columns 128..191 (bf16 pairs), then P V
+  {
+    uint32_t x[64];
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(a + (128 * r + t) * 128);
+#pragma unroll
+    for (int k = 0; k < 64; ++k) x[k] = src[k];
+    tc::tmem_st32(tmem + lb + 128, x);
+    tc::tmem_st32(tmem + lb + 160, x + 32);
+    tc::tmem_st_wait();
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();  // both CTAs read S and wrote P
+  tc::tc_fence_after();
+  if (r == 0 && t == 0) {
+    const uint32_t sv_a = tc::smem_addr(sv);
+    for (int ks = 0; ks < 8; ++ks)
+      tc::mma2_bf16_ts(tmem, tmem + 128 + ks * 8, tc::sw128_desc(sv_a + ks * (kPageBytes / 2), 16, kPageHalfBytes),
+                       kIdPV2, ks > 0);
+    tc::mma2_commit(done, 3);
+  }
+  ok = tc::mbar_wait(done, 1, ab, kWaitLimitNs);
+  if (!__all_sync(0xffffffffu, ok)) {
+    if ((t & 31) == 0) set_err(err, PIC_ERR_TIMEOUT);
+  } else {
+    tc::tc_fence_after();
+    for (int c0 = 0; c0 < 128; c0 += 32) {
+      uint32_t x[32];
+      tc::tmem_ld32(tmem + lb + c0, x);
+      tc::tmem_ld_wait();
+      tc::reg_fence<32>(x);
+      for (int k = 0; k < 32; ++k) dpv[(int64_t)(128 * r + t) * 128 + c0 + k] = u2f(x[k]);
+    }
+  }
+  tc::tc_fence_before();
+  __syncthreads();
+  tc::cluster_sync();  // no pair product or peer access outstanding
+  if (warp == 0) {
+    tc::tc_fence_after();
+    tc::tmem_dealloc2(tmem, 256);
+  }
+}
+
 // ------------------------------------------------------------------ LSE merge
 // Blocks of 8 rows of one (Q-tile pair, KV head) with split spans; one warp per
 // row, lane = 4-dim chunk.  Combines the per-span partials (O_s normalised by
@@ -1605,6 +1733,21 @@ pic_status pic_selftest_umma(const void* a, const void* b, float* d_kmajor, floa
     return PIC_ERR_CUDA;
   selftest_umma_kernel<<<1, 128, smem, (cudaStream_t)stream>>>(bmap, static_cast<const bf16*>(a), d_kmajor,
                                                                 d_mnmajor, d_tmem_a, err_flag);
+  return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
+}
+
+pic_status pic_selftest_umma_pair(const void* a, const void* b, const void* v, float* d_s, float* d_pv,
+                                  int32_t* info, int32_t* err_flag, pic_stream_t stream) {
+  if (!a || !b || !v || !d_s || !d_pv || !info || !err_flag) return PIC_ERR_INVALID;
+  if ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(v)) & 15)
+    return PIC_ERR_INVALID;
+  const int smem = kPairTestSmem + 1024;
+  if (cudaFuncSetAttribute(selftest_umma_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+      cudaSuccess)
+    return PIC_ERR_CUDA;
+  selftest_umma_pair_kernel<<<2, 128, smem, (cudaStream_t)stream>>>(
+      static_cast<const bf16*>(a), static_cast<const bf16*>(b), static_cast<const bf16*>(v), d_s, d_pv, info,
+      err_flag);
   return cudaGetLastError() == cudaSuccess ? PIC_OK : PIC_ERR_CUDA;
 }
 

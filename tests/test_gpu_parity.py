@@ -59,6 +59,30 @@ def test_selftest_umma():
     assert (dts.double().cpu() - A @ B).abs().max() < 1e-3
 
 
+def test_selftest_umma_pair():
+    """The CTA-pair products: S = A.B^T with M = N = 256 (each CTA 128 rows of A and
+    128 keys of B), P.V with P from TMEM and V split by columns between the CTAs."""
+    g = torch.Generator().manual_seed(1)
+    a = torch.randn(256, 128, generator=g).to(torch.bfloat16)
+    b = torch.randn(256, 128, generator=g).to(torch.bfloat16)
+    v = torch.randn(128, 128, generator=g).to(torch.bfloat16)
+    ds = torch.full((256, 256), float("nan"), device="cuda")
+    dpv = torch.full((256, 128), float("nan"), device="cuda")
+    info = torch.full((2,), -1, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pic.pic_selftest_umma_pair(a.cuda(), b.cuda(), v.cuda(), ds, dpv, info, err)
+    torch.cuda.synchronize()
+    A, B, V = a.double(), b.double(), v.double()
+    es = (ds.double().cpu() - A @ B.T).abs().nan_to_num(1e9)
+    epv = (dpv.double().cpu() - A @ V).abs().nan_to_num(1e9)
+    print("tmem bases", info.tolist(), "err", err.item(), "S err by quadrant",
+          [[float(es[128 * i:128 * i + 128, 128 * j:128 * j + 128].max()) for j in range(2)] for i in range(2)],
+          "PV err by quadrant",
+          [[float(epv[128 * i:128 * i + 128, 64 * j:64 * j + 64].max()) for j in range(2)] for i in range(2)])
+    assert err.item() == 0
+    assert es.max() < 1e-3 and epv.max() < 1e-3
+
+
 # ---------------------------------------------------------------- the workloads
 
 def test_worked_example_fp32():
