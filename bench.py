@@ -45,10 +45,10 @@ UNIT = "tokens/s"
 # two-launch composition), with the kernel source they were taken from; reported
 # as roofline traffic only while the source is unchanged.
 NCU_TRAFFIC = {
-    # link_attn_tc_kernel<0>, long_context_100x1000: 664.08 MB read + 137.69 MB written
-    ("attention", "7f2ed6ae9aec8cb2"): 801773312,
-    # link_attn_tc_kernel<1> (rotate-on-read), long_context_100x1000: 676.23 MB read + 148.15 MB written
-    ("rotate_on_read", "7f2ed6ae9aec8cb2"): 824385024,
+    # link_attn_tc_kernel<0>, long_context_100x1000: 668.39 MB read + 138.73 MB written
+    ("attention", "776d5b9c86ccc04d"): 807120128,
+    # link_attn_tc_kernel<1> (rotate-on-read), long_context_100x1000: 674.80 MB read + 148.21 MB written
+    ("rotate_on_read", "776d5b9c86ccc04d"): 823006976,
     # rerotate_kernel<bf16>, long_context_100x1000: 201.36 MB read + 140.36 MB written
     ("rerotate", "f862c45770d2a0fa"): 341722880,
     # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.01 MB written
