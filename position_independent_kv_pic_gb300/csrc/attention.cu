@@ -54,8 +54,9 @@ constexpr int kSmWarpgroups = 2 * kQTiles;  // softmax: one warpgroup per (Q til
 constexpr int kThreads = 128 * (1 + kSmWarpgroups);
 constexpr int kMinSpan = 4;             // key tiles per unit, lower bound
 constexpr int kSpanPref = 16;           // ... and while every SM still gets a unit
-constexpr int kUnitsPerSm = 6;          // target units per SM when splitting
+constexpr int kUnitsPerSm = 7;          // target units per SM when splitting (the cap below binds at 152 SMs)
 constexpr int kMaxSplitUnits = 960;     // bound on the units splitting may add
+constexpr int kAllSms = 1 << 20;         // split budget: every SM of the device
 constexpr int kTailDiv = 3;             // a call with few (tile pair, head) items cuts its tails in 3
 constexpr int kTailExtra = 640;         // room for those extra tail pieces (2 per item, < 2 * 160 items)
 constexpr int kMaxPlanReqs = 1024;      // requests one planning block handles
@@ -145,7 +146,7 @@ __device__ __forceinline__ bool page_ok(int4 p, int64_t num_blocks) {
 // One block.  (1) Q-tile pairs per request and their causal page counts (pages
 // are sorted by first valid position: binary search for the last row's
 // position).  (2) The span: enough key tiles per unit that at most
-// min(kUnitsPerSm * SMs, kMaxSplitUnits) extra units appear.  (3) Units: the
+// min(kUnitsPerSm * SMs, max_split) extra units appear.  (3) Units: the
 // full-length spans first, ordered (request, KV head, span index, tile) so that
 // concurrently running units read the same key range, then the shorter tail
 // spans by decreasing length.
@@ -155,7 +156,7 @@ constexpr int kHist = 2048;
 __global__ void __launch_bounds__(kPlanThreads)
 plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ row_off,
                   const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off,
-                  int n_req, int R2, int Hkv, int num_sms, int64_t tiles_cap, int64_t units_cap,
+                  int n_req, int R2, int Hkv, int num_sms, int max_split, int64_t tiles_cap, int64_t units_cap,
                   int64_t tail_extra, WsHeader* hdr, TileMeta* tiles, Unit* units, int32_t* err) {
   __shared__ int s_toff[kMaxPlanReqs + 1];   // first tile of each request
   __shared__ int s_full[kMaxPlanReqs];       // full spans of one head of each request
@@ -270,13 +271,14 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
   __syncthreads();
   // (2) span
   const int64_t work = (int64_t)s_total_kt * Hkv;
-  // about six units per SM balance the long calls (measured: 4 or 5 left SMs idle
-  // at the end of the long-context call, 7 or 8 paid more unit overhead); a short
+  // six to seven units per SM balance the long calls (long-context call, units in
+  // all: 912 -> 897 us, 960 -> 872, 1,000 -> 874, 1,064 -> 900, 1,216 -> 906; fewer
+  // left SMs idle at the end, more paid unit overhead and partials); a short
   // call keeps spans of at least 16 tiles as long as every SM still gets a unit,
   // since each unit pays a Q load and a pipeline fill, and a call too short for that
   // spreads over more SMs in spans down to 4 tiles (6-chunk prompt: 46 -> 41 us; 2
   // tiles slowed the 20-chunk call by a tenth)
-  const int64_t target = min((int64_t)kUnitsPerSm * num_sms, (int64_t)kMaxSplitUnits);
+  const int64_t target = min((int64_t)kUnitsPerSm * num_sms, (int64_t)max_split);
   const int64_t span_fill = min((int64_t)kSpanPref, (work + num_sms - 1) / num_sms);
   const int span = (int)max((int64_t)kMinSpan, max((work + target - 1) / target, span_fill));
   // With few (tile pair, head) items the tails are few and long, and the SMs that
@@ -1506,14 +1508,14 @@ bool tc_shape(pic_dtype dt, int Hq, int Hkv, int d) {
 
 // The two phases of a tensor-core attention call, with the scratch laid out by L
 // in `ws`: the plan (unit list, Q operands — reads no K or V) and the run
-// (attention, merge).  The planner may add up to 6 * split_sms units by splitting
-// key ranges.
+// (attention, merge).  The planner may add up to min(kUnitsPerSm * split_sms,
+// split_cap) units by splitting key ranges.
 enum { kPhasePlan = 1, kPhaseRun = 2, kPhaseAll = 3 };
 
 pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows, const int32_t* row_off,
                      const void* k_pool, const void* v_pool, int64_t num_blocks, const pic_link_page* pages,
                      const int32_t* page_off, int32_t n_req, int32_t Hq, int32_t Hkv, float scale, void* out,
-                     uint8_t* w, const WsLayout& L, int split_sms, int32_t* err_flag, cudaStream_t s,
+                     uint8_t* w, const WsLayout& L, int split_sms, int split_cap, int32_t* err_flag, cudaStream_t s,
                      const int32_t* page_tab = nullptr, const float* rot_table = nullptr, int64_t n_tab = 0,
                      int phases = kPhaseAll) {
   const int G = Hq / Hkv;
@@ -1540,7 +1542,7 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   uint8_t* q_tiles = w + L.off_q;
   if (phases & kPhasePlan) {
     plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kQTiles * R, Hkv,
-                                                  split_sms < sms ? split_sms : sms, L.tiles_cap, L.units_cap,
+                                                  split_sms < sms ? split_sms : sms, split_cap, L.tiles_cap, L.units_cap,
                                                   L.tail_extra, hdr, tiles, units, err_flag);
     if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
     qprep_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), 4), kQTiles * kM, 0, s>>>(
@@ -1657,7 +1659,7 @@ pic_status pic_link_attention(const void* q, const float* row_table, const int32
     const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
     if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
     return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
-                     out, static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, s);
+                     out, static_cast<uint8_t*>(ws), L, kAllSms, kMaxSplitUnits, err_flag, s);
   }
   return launch_attention_simt(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
                                n_req, n_rows, Hq, Hkv, d, scale, out, s);
@@ -1676,7 +1678,7 @@ pic_status pic_link_attention_plan(const void* q, const float* row_table, const 
   const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
   if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
   return launch_tc(q, row_table, rows, row_off, nullptr, nullptr, 0, pages, page_off, n_req, Hq, Hkv, 1.f, nullptr,
-                   static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, (cudaStream_t)stream,
+                   static_cast<uint8_t*>(ws), L, kAllSms, kMaxSplitUnits, err_flag, (cudaStream_t)stream,
                    nullptr, nullptr, 0, kPhasePlan);
 }
 
@@ -1694,7 +1696,7 @@ pic_status pic_link_attention_run(const void* q, const float* row_table, const i
     const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
     if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
     return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
-                     out, static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, s, nullptr, nullptr,
+                     out, static_cast<uint8_t*>(ws), L, kAllSms, kMaxSplitUnits, err_flag, s, nullptr, nullptr,
                      0, kPhaseRun);
   }
   return launch_attention_simt(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, dtype, pages, page_off,
@@ -1718,7 +1720,7 @@ pic_status pic_link_attention_ror(const void* q, const float* row_table, const i
   const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
   if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
   return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
-                   out, static_cast<uint8_t*>(ws), L, kMaxSplitUnits / kUnitsPerSm, err_flag, (cudaStream_t)stream,
+                   out, static_cast<uint8_t*>(ws), L, kAllSms, kMaxSplitUnits, err_flag, (cudaStream_t)stream,
                    page_tab, rot_table, n_tab);
 }
 
@@ -1757,9 +1759,8 @@ pic_status pic_selftest_umma_pair(const void* a, const void* b, const void* v, f
 // pic_link_attention_noalloc: the tensor-core attention with its planning and
 // merge scratch in one statically sized device array instead of a caller
 // workspace.  It runs the same kernels as pic_link_attention; it gives the
-// planner a smaller split budget (kUnitsPerSm extra units for each of at most
-// kFixedSplitSms SMs: 6 * 10 = 60 extra units) so that the scratch a call needs
-// stays small.
+// planner a smaller split budget (units balanced for kFixedSplitSms SMs, at most
+// kFixedSplitUnits = 60 extra units) so that the scratch a call needs stays small.
 
 constexpr size_t kFixedScratchBytes = (size_t)PIC_NOALLOC_SCRATCH_BYTES;
 
@@ -1769,8 +1770,9 @@ static __device__ __align__(256) uint8_t pic_fixed_scratch[kFixedScratchBytes];
 namespace pic {
 namespace {
 
-constexpr int kFixedSplitSms = 10;  // at most kUnitsPerSm * kFixedSplitSms = 60 extra units in the fixed scratch
-static_assert(kUnitsPerSm * kFixedSplitSms == 60, "the split cap pic.h states");
+constexpr int kFixedSplitSms = 10;    // the planner balances for 10 SMs' worth of units ...
+constexpr int kFixedSplitUnits = 60;  // ... and adds at most 60 to the fixed scratch
+static_assert(kFixedSplitUnits == 60 && kFixedSplitUnits <= kUnitsPerSm * kFixedSplitSms, "the split cap pic.h states");
 constexpr int kMaxDevices = 256;
 
 std::mutex g_fixed_mu;
@@ -1796,7 +1798,7 @@ void* fixed_scratch_address() {
 }
 
 WsLayout fixed_layout(int64_t n_rows, int32_t n_req, int32_t G, int32_t Hkv, int32_t d) {
-  return ws_layout_with(n_rows, n_req, G, Hkv, d, (int64_t)kUnitsPerSm * kFixedSplitSms, 0);
+  return ws_layout_with(n_rows, n_req, G, Hkv, d, kFixedSplitUnits, 0);
 }
 
 }  // namespace
@@ -1833,5 +1835,5 @@ extern "C" pic_status pic_link_attention_noalloc(const void* q, const float* row
   // Nothing in the scratch has to start at zero: the planner rewrites the header,
   // tile and unit lists on every call, and partials are written before they are read.
   return launch_tc(q, row_table, rows, row_off, k_pool, v_pool, num_blocks, pages, page_off, n_req, Hq, Hkv, scale,
-                   out, w, fixed_layout(n_rows, n_req, Hq / Hkv, Hkv, d), kFixedSplitSms, err_flag, s);
+                   out, w, fixed_layout(n_rows, n_req, Hq / Hkv, Hkv, d), kFixedSplitSms, kFixedSplitUnits, err_flag, s);
 }
