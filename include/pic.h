@@ -409,6 +409,25 @@ pic_status pic_link_attention_run(const void* q, const float* row_table, const i
                                   int32_t Hkv, int32_t d, float scale, void* out, void* ws, size_t ws_bytes,
                                   int32_t* err_flag, pic_stream_t stream);
 
+/* pic_link_attention_plan in two parts, so that the part that needs no page list
+ * can run before the splice has written it:
+ *   pic_link_attention_plan_q      the tile pairs' rows and the roped Q operands
+ *                                  (reads q, row_table, row_off);
+ *   pic_link_attention_plan_units  the work units (reads rows, row_off, pages,
+ *                                  page_off).
+ * Arguments as pic_link_attention_plan.  They write different fields of the
+ * plan in ws (the tiles' rows and the Q operands; the units and the tiles' key
+ * ranges), so they run in either order or at the same time on two streams; both
+ * together are pic_link_attention_plan, bit for bit, and both precede the run. */
+pic_status pic_link_attention_plan_q(const void* q, const float* row_table, const int32_t* row_off,
+                                     int32_t n_req, int64_t n_rows, int32_t Hq, int32_t Hkv, int32_t d,
+                                     pic_dtype dtype, void* ws, size_t ws_bytes, int32_t* err_flag,
+                                     pic_stream_t stream);
+pic_status pic_link_attention_plan_units(const int32_t* rows, const int32_t* row_off, const pic_link_page* pages,
+                                         const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                                         int32_t Hkv, int32_t d, pic_dtype dtype, void* ws, size_t ws_bytes,
+                                         int32_t* err_flag, pic_stream_t stream);
+
 /* ------------------------------------------------------------------------
  * a3+a5  Rotate-on-read link attention (RoPE article 3.3: the rotary correction
  *     applied where the kernel reads the cache, a mixed reuse + correction

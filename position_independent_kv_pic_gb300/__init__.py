@@ -27,7 +27,8 @@ __all__ = [
     "EXPORTED",
     "pic_decode_workspace", "pic_decode_attention", "pic_rope_cached_k",
     "pic_compose_segment", "pic_compose_workspace", "pic_compose_states", "pic_link_attention_ror",
-    "pic_link_attention_plan", "pic_link_attention_run", "pic_compose_split_t",
+    "pic_link_attention_plan", "pic_link_attention_plan_q", "pic_link_attention_plan_units",
+    "pic_link_attention_run", "pic_compose_split_t",
 ]
 
 PIC_OK, PIC_ERR_INVALID, PIC_ERR_CUDA, PIC_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -55,7 +56,8 @@ EXPORTED = (
     "pic_selftest_umma", "pic_selftest_umma_pair", "pic_link_attention_noalloc", "pic_decode_workspace",
     "pic_decode_attention",
     "pic_rope_cached_k", "pic_compose_segment", "pic_compose_workspace", "pic_compose_states",
-    "pic_link_attention_ror", "pic_link_attention_plan", "pic_link_attention_run", "pic_compose_split_t",
+    "pic_link_attention_ror", "pic_link_attention_plan", "pic_link_attention_plan_q",
+    "pic_link_attention_plan_units", "pic_link_attention_run", "pic_compose_split_t",
 )
 
 
@@ -107,6 +109,10 @@ _SIGS = {
                                               _I32, _I64, _I32, _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
     "pic_link_attention_plan": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, ctypes.c_int,
                                                _P, _SZ, _P, _P]),
+    "pic_link_attention_plan_q": (ctypes.c_int, [_P, _P, _P, _I32, _I64, _I32, _I32, _I32, ctypes.c_int, _P, _SZ,
+                                                 _P, _P]),
+    "pic_link_attention_plan_units": (ctypes.c_int, [_P, _P, _P, _P, _I32, _I64, _I32, _I32, _I32, ctypes.c_int, _P,
+                                                     _SZ, _P, _P]),
     "pic_link_attention_run": (ctypes.c_int, [_P, _P, _P, _P, _P, _P, _I64, ctypes.c_int, _P, _P, _I32, _I64, _I32,
                                               _I32, _I32, _F32, _P, _P, _SZ, _P, _P]),
     "pic_compose_split_t": (ctypes.c_int, [_P, _I64, _I32, _P, _P]),
@@ -275,6 +281,22 @@ def pic_link_attention_plan(q, row_table, rows, row_off, pages, page_off, n_req:
         _ptr(q), _ptr(row_table), _ptr(rows), _ptr(row_off), _ptr(pages), _ptr(page_off), int(n_req), int(n_rows),
         int(Hq), int(Hkv), int(d), int(dtype), _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)),
         "pic_link_attention_plan")
+
+
+def pic_link_attention_plan_q(q, row_table, row_off, n_req: int, n_rows: int, Hq: int, Hkv: int, d: int, dtype: int,
+                              ws, err_flag, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pic_link_attention_plan_q(
+        _ptr(q), _ptr(row_table), _ptr(row_off), int(n_req), int(n_rows), int(Hq), int(Hkv), int(d), int(dtype),
+        _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)), "pic_link_attention_plan_q")
+
+
+def pic_link_attention_plan_units(rows, row_off, pages, page_off, n_req: int, n_rows: int, Hq: int, Hkv: int, d: int,
+                                  dtype: int, ws, err_flag, stream=None):
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(load().pic_link_attention_plan_units(
+        _ptr(rows), _ptr(row_off), _ptr(pages), _ptr(page_off), int(n_req), int(n_rows), int(Hq), int(Hkv), int(d),
+        int(dtype), _ptr(ws), ws_bytes, _ptr(err_flag), _stream(stream)), "pic_link_attention_plan_units")
 
 
 def pic_link_attention_run(q, row_table, rows, row_off, k_pool, v_pool, dtype: int, pages, page_off, n_req: int,

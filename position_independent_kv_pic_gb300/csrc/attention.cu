@@ -153,6 +153,76 @@ __device__ __forceinline__ bool page_ok(int4 p, int64_t num_blocks) {
 constexpr int kPlanThreads = 1024;
 constexpr int kHist = 2048;
 
+// The tile pairs: each request's rows in pairs of R2 rows, the partial pair (if
+// any) first.  s_toff[r] = first tile of request r; returns the number of tiles.
+// Block-wide (kPlanThreads threads).
+__device__ int plan_tile_offsets(const int32_t* __restrict__ row_off, int n_req, int R2, int* s_toff, int* s_scan) {
+  const int tid = threadIdx.x;
+  int carry = 0;
+  for (int g = 0; g < n_req; g += kPlanThreads) {
+    const int r = g + tid;
+    const int nt = (r < n_req) ? ceil_div(row_off[r + 1] - row_off[r], R2) : 0;
+    int tot;
+    const int ex = block_exclusive_scan<kPlanThreads>(nt, s_scan, &tot);
+    if (r < n_req) s_toff[r] = carry + ex;
+    carry += tot;
+  }
+  if (tid == 0) s_toff[n_req] = carry;
+  __syncthreads();
+  return s_toff[n_req];
+}
+// Request, first row and rows of tile t: the partial pair first, since its rows
+// have the smallest positions, so a half-empty tile pair (one Q tile, the MMA
+// ping-pong idle) spans the fewest key tiles.
+__device__ __forceinline__ void plan_tile_rows(const int32_t* __restrict__ row_off, const int* s_toff, int n_req,
+                                               int R2, int t, TileMeta& tm) {
+  int lo = 0, hi = n_req;  // request: last r with s_toff[r] <= t
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_toff[mid] <= t) lo = mid; else hi = mid;
+  }
+  const int r = lo;
+  tm.req = r;
+  const int nr = row_off[r + 1] - row_off[r], rem = nr % R2, k = t - s_toff[r];
+  tm.row0 = row_off[r] + (rem > 0 ? (k == 0 ? 0 : rem + (k - 1) * R2) : k * R2);
+  tm.n_rows = (rem > 0 && k == 0) ? rem : R2;
+}
+
+__device__ __forceinline__ int plan_tile_req(const int* s_toff, int n_req, int t) {
+  int lo = 0, hi = n_req;  // last r with s_toff[r] <= t
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_toff[mid] <= t) lo = mid; else hi = mid;
+  }
+  return lo;
+}
+
+// One block: the tile pairs' rows alone (the first part of the unit plan), so that
+// the Q operands can be written before the page list exists.  Writes only the row
+// fields of each tile; the unit plan writes the same values and the rest.
+__global__ void __launch_bounds__(kPlanThreads)
+tile_rows_kernel(const int32_t* __restrict__ row_off, int n_req, int R2, int64_t tiles_cap, WsHeader* hdr,
+                 TileMeta* tiles, int32_t* err) {
+  __shared__ int s_toff[kMaxPlanReqs + 1];
+  __shared__ int s_scan[kPlanThreads / 32 + 1];
+  const int n_tiles = plan_tile_offsets(row_off, n_req, R2, s_toff, s_scan);
+  if (n_tiles > tiles_cap) {
+    if (threadIdx.x == 0) {
+      set_err(err, PIC_ERR_RANGE);
+      hdr->n_tiles = 0;
+    }
+    return;
+  }
+  for (int t = threadIdx.x; t < n_tiles; t += kPlanThreads) {
+    TileMeta tm;
+    plan_tile_rows(row_off, s_toff, n_req, R2, t, tm);
+    tiles[t].req = tm.req;
+    tiles[t].row0 = tm.row0;
+    tiles[t].n_rows = tm.n_rows;
+  }
+  if (threadIdx.x == 0) hdr->n_tiles = n_tiles;
+}
+
 __global__ void __launch_bounds__(kPlanThreads)
 plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ row_off,
                   const pic_link_page* __restrict__ pages, const int32_t* __restrict__ page_off,
@@ -168,24 +238,14 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
   __shared__ int s_total_kt, s_part;
   const int tid = threadIdx.x;
   // (1) tile offsets over requests
-  int carry = 0;
-  for (int g = 0; g < n_req; g += kPlanThreads) {
-    const int r = g + tid;
-    const int nt = (r < n_req) ? ceil_div(row_off[r + 1] - row_off[r], R2) : 0;
-    int tot;
-    const int ex = block_exclusive_scan<kPlanThreads>(nt, s_scan, &tot);
-    if (r < n_req) s_toff[r] = carry + ex;
-    carry += tot;
-  }
+  const int n_tiles = plan_tile_offsets(row_off, n_req, R2, s_toff, s_scan);
   if (tid == 0) {
-    s_toff[n_req] = carry;
     s_total_kt = 0;
     s_part = 0;
   }
   for (int r = tid; r < n_req; r += kPlanThreads) s_full[r] = 0;
   for (int i = tid; i < kHist; i += kPlanThreads) s_hist[i] = 0;
   __syncthreads();
-  const int n_tiles = s_toff[n_req];
   if (n_tiles > tiles_cap) {
     if (tid == 0) {
       set_err(err, PIC_ERR_RANGE);
@@ -198,20 +258,9 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
   // tiles: rows and last row position; causal page counts from one pass over the pages
   const bool small = n_tiles <= kMaxPlanTiles;
   for (int t = tid; t < n_tiles; t += kPlanThreads) {
-    int lo = 0, hi = n_req;  // request: last r with s_toff[r] <= t
-    while (hi - lo > 1) {
-      const int mid = (lo + hi) >> 1;
-      if (s_toff[mid] <= t) lo = mid; else hi = mid;
-    }
-    const int r = lo;
     TileMeta tm;
-    tm.req = r;
-    // the request's rows in tiles of R2, the partial tile (if any) first: its rows
-    // have the smallest positions, so a half-empty tile pair (one Q tile, the MMA
-    // ping-pong idle) spans the fewest key tiles
-    const int nr = row_off[r + 1] - row_off[r], rem = nr % R2, k = t - s_toff[r];
-    tm.row0 = row_off[r] + (rem > 0 ? (k == 0 ? 0 : rem + (k - 1) * R2) : k * R2);
-    tm.n_rows = (rem > 0 && k == 0) ? rem : R2;
+    plan_tile_rows(row_off, s_toff, n_req, R2, t, tm);
+    const int r = tm.req;
     const int maxpos = rows[tm.row0 + tm.n_rows - 1];
     tm.page_begin = page_off[r];
     tm.n_pages = 0;
@@ -227,37 +276,58 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
       s_maxpos[t] = maxpos;
       s_npages[t] = 0;
     }
-    tm.n_kt = 0;
-    tm.n_spans = 0;
-    tm.part_base = -1;
-    tiles[t] = tm;
+    // the row fields (req, row0, n_rows) and the tile count are tile_rows_kernel's:
+    // the Q operands are read against them, also while this kernel runs
+    TileMeta& out = tiles[t];
+    out.page_begin = tm.page_begin;
+    out.n_pages = tm.n_pages;
+    out.n_kt = 0;
+    out.n_spans = 0;
+    out.part_base = -1;
   }
   for (int r = tid; r <= n_req; r += kPlanThreads) s_poff[r] = page_off[r];
   __syncthreads();
   if (small) {
     // page p is the last page a tile needs iff first(p) <= maxpos < first(p+1)
     // (pages of a request are sorted by first valid position, tiles by maxpos)
+    // four pages per thread and round, their loads issued together, and only the
+    // 8 bytes (gpos0, lo | hi) each page's first position needs; the next page's
+    // comes from the neighbouring lane (one block reads the whole list, so the bytes
+    // it moves set this pass's length on a long list)
+    constexpr int kPagesAtOnce = 4;
     const int n_pages_all = s_poff[n_req];
-    for (int p = tid; p < n_pages_all; p += kPlanThreads) {
-      int lo = 0, hi = n_req;
-      while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (s_poff[mid] <= p) lo = mid; else hi = mid;
+    const int2* pg2 = reinterpret_cast<const int2*>(pages);  // {gpos0, lo | hi << 16} at int2 index 2p + 1
+    const int lane = tid & 31;
+    for (int p0 = tid; p0 - lane < n_pages_all; p0 += kPagesAtOnce * kPlanThreads) {
+      int first[kPagesAtOnce], nextf[kPagesAtOnce];
+#pragma unroll
+      for (int u = 0; u < kPagesAtOnce; ++u) {
+        const int p = p0 + u * kPlanThreads;
+        int2 e = make_int2(INT_MAX, 0), en = make_int2(INT_MAX, 0);
+        if (p < n_pages_all) e = __ldg(pg2 + 2 * p + 1);
+        if (lane == 31 && p + 1 < n_pages_all) en = __ldg(pg2 + 2 * (p + 1) + 1);
+        first[u] = e.x == INT_MAX ? INT_MAX : e.x + (int16_t)(e.y & 0xffff);
+        const int nb = __shfl_down_sync(0xffffffffu, first[u], 1);
+        nextf[u] = lane == 31 ? (en.x == INT_MAX ? INT_MAX : en.x + (int16_t)(en.y & 0xffff)) : nb;
       }
-      const int r = lo;
-      const pic_link_page pg = pages[p];
-      const int first = pg.gpos0 + pg.lo;
-      int next = INT_MAX;
-      if (p + 1 < s_poff[r + 1]) {
-        const pic_link_page pn = pages[p + 1];
-        next = pn.gpos0 + pn.lo;
+#pragma unroll
+      for (int u = 0; u < kPagesAtOnce; ++u) {
+        const int p = p0 + u * kPlanThreads;
+        if (p >= n_pages_all) break;
+        int lo = 0, hi = n_req;
+        while (hi - lo > 1) {
+          const int mid = (lo + hi) >> 1;
+          if (s_poff[mid] <= p) lo = mid; else hi = mid;
+        }
+        const int r = lo;
+        const int next = (p + 1 < s_poff[r + 1]) ? nextf[u] : INT_MAX;
+        int a = s_toff[r], b = s_toff[r + 1];  // first tile with maxpos >= first
+        while (a < b) {
+          const int mid = (a + b) >> 1;
+          if (s_maxpos[mid] < first[u]) a = mid + 1; else b = mid;
+        }
+        for (int t = a; t < s_toff[r + 1] && s_maxpos[t] < next; ++t) s_npages[t] = p + 1 - s_poff[r];
       }
-      int a = s_toff[r], b = s_toff[r + 1];  // first tile with maxpos >= first
-      while (a < b) {
-        const int mid = (a + b) >> 1;
-        if (s_maxpos[mid] < first) a = mid + 1; else b = mid;
-      }
-      for (int t = a; t < s_toff[r + 1] && s_maxpos[t] < next; ++t) s_npages[t] = p + 1 - s_poff[r];
     }
     __syncthreads();
   }
@@ -293,12 +363,12 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     const int len = tm.n_kt % span;
     tm.n_spans = tm.n_kt / span + ceil_div(len, ts);
     if (tm.n_spans > 1) tm.part_base = atomicAdd(&s_part, tm.n_spans * Hkv);
-    atomicAdd(&s_full[tm.req], tm.n_kt / span);
+    atomicAdd(&s_full[plan_tile_req(s_toff, n_req, t)], tm.n_kt / span);
     for (int o = 0; o < len; o += ts) atomicAdd(&s_hist[min(min(ts, len - o), kHist - 1)], Hkv);
   }
   __syncthreads();
   // (3) first full unit of every request; tail buckets after all full units, longest first
-  carry = 0;
+  int carry = 0;
   for (int g = 0; g < n_req; g += kPlanThreads) {
     const int r = g + tid;
     const int f = (r < n_req) ? s_full[r] * Hkv : 0;
@@ -329,13 +399,45 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
     }
     return;
   }
-  // full units: index within (request, head) ordered by (span s, tile t)
+  // full units: index within (request, head) ordered by (span s, tile t).  With the
+  // tiles' key-tile counts in shared memory, one thread per (tile, head, span): a
+  // thread per (tile, head) writing its spans in turn was the plan's longest chain
+  static_assert(kMaxPlanTiles <= kPlanThreads, "one tile per thread in the scan below");
+  if (small) {
+    int* s_fpre = s_maxpos;  // free again: full units before each tile, over all heads
+    int n_full_items;
+    const int ex = block_exclusive_scan<kPlanThreads>(tid < n_tiles ? (s_nkt[tid] / span) * Hkv : 0, s_scan,
+                                                      &n_full_items);
+    if (tid < n_tiles) s_fpre[tid] = ex;
+    __syncthreads();
+    for (int i = tid; i < n_full_items; i += kPlanThreads) {
+      int a = 0, b = n_tiles;  // the last tile with s_fpre[t] <= i (it has units)
+      while (b - a > 1) {
+        const int mid = (a + b) >> 1;
+        if (s_fpre[mid] <= i) a = mid; else b = mid;
+      }
+      const int t = a, f = s_nkt[t] / span, loc = i - s_fpre[t], h = loc / f, sp = loc % f;
+      const int r = plan_tile_req(s_toff, n_req, t), t0 = s_toff[r], t1 = s_toff[r + 1];
+      int idx = s_fbase[r] + h * s_full[r];
+      for (int t2 = t0; t2 < t1; ++t2) {
+        const int f2 = s_nkt[t2] / span;
+        idx += min(f2, sp) + ((t2 < t && f2 > sp) ? 1 : 0);
+      }
+      const int n_spans = tiles[t].n_spans, part_base = tiles[t].part_base;
+      Unit un;
+      un.tile = t; un.head = h; un.kt0 = sp * span; un.kt1 = (sp + 1) * span;
+      un.part = (n_spans > 1) ? part_base + h * n_spans + sp : -1;
+      un.pad0 = un.pad1 = un.pad2 = 0;
+      units[idx] = un;
+    }
+  }
   for (int th = tid; th < n_tiles * Hkv; th += kPlanThreads) {
     const int t = th / Hkv, h = th % Hkv;
-    const TileMeta tm = tiles[t];
-    const int r = tm.req, t0 = s_toff[r], t1 = s_toff[r + 1];
-    const int f = tm.n_kt / span;
-    for (int s = 0; s < f; ++s) {
+    // this kernel's fields only (tile_rows_kernel may be writing the others)
+    const int n_kt = tiles[t].n_kt, n_spans = tiles[t].n_spans, part_base = tiles[t].part_base;
+    const int r = plan_tile_req(s_toff, n_req, t), t0 = s_toff[r], t1 = s_toff[r + 1];
+    const int f = n_kt / span;
+    for (int s = 0; !small && s < f; ++s) {
       int idx = s_fbase[r] + h * s_full[r];
       for (int t2 = t0; t2 < t1; ++t2) {
         const int f2 = (small ? s_nkt[t2] : tiles[t2].n_kt) / span;
@@ -343,23 +445,22 @@ plan_units_kernel(const int32_t* __restrict__ rows, const int32_t* __restrict__ 
       }
       Unit un;
       un.tile = t; un.head = h; un.kt0 = s * span; un.kt1 = (s + 1) * span;
-      un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + s : -1;
+      un.part = (n_spans > 1) ? part_base + h * n_spans + s : -1;
       un.pad0 = un.pad1 = un.pad2 = 0;
       units[idx] = un;
     }
-    const int len = tm.n_kt % span;
+    const int len = n_kt % span;
     for (int o = 0, j = 0; o < len; o += ts, ++j) {  // the tail, in pieces of at most ts tiles
       const int pl = min(ts, len - o);
       const int idx = atomicAdd(&s_hist[min(pl, kHist - 1)], 1);
       Unit un;
       un.tile = t; un.head = h; un.kt0 = f * span + o; un.kt1 = f * span + o + pl;
-      un.part = (tm.n_spans > 1) ? tm.part_base + h * tm.n_spans + f + j : -1;
+      un.part = (n_spans > 1) ? part_base + h * n_spans + f + j : -1;
       un.pad0 = un.pad1 = un.pad2 = 0;
       units[idx] = un;
     }
   }
   if (tid == 0) {
-    hdr->n_tiles = n_tiles;
     hdr->n_units = n_units;
     hdr->span = span;
     hdr->next_unit = 0;
@@ -765,13 +866,13 @@ qprep_kernel(const WsHeader* __restrict__ hdr, const TileMeta* __restrict__ tile
   const int th = blockIdx.x;
   const int tile = th / Hkv, kvh = th % Hkv;
   if (tile >= hdr->n_tiles) return;
-  const TileMeta tm = tiles[tile];
+  const int t_row0 = tiles[tile].row0, t_n_rows = tiles[tile].n_rows;  // tile_rows_kernel's fields
   const int qt = threadIdx.x / kM, m = threadIdx.x % kM;
-  if (qt == 1 && tm.n_rows <= R) return;
+  if (qt == 1 && t_n_rows <= R) return;
   const int hg = m / R, i = m % R;
   const int loc = qt * R + i;
-  const bool ok = loc < tm.n_rows;
-  const int row = tm.row0 + (ok ? loc : 0);
+  const bool ok = loc < t_n_rows;
+  const int row = t_row0 + (ok ? loc : 0);
   uint8_t* dst = q_tiles + (((int64_t)tile * Hkv + kvh) * kQTiles + qt) * kOpBytes;
   write_q_row(dst, m, ok, q + ((int64_t)row * Hq + kvh * G + hg) * kD, row_table + (int64_t)row * (kD / 2),
               2 * blockIdx.y);
@@ -1510,7 +1611,9 @@ bool tc_shape(pic_dtype dt, int Hq, int Hkv, int d) {
 // in `ws`: the plan (unit list, Q operands — reads no K or V) and the run
 // (attention, merge).  The planner may add up to min(kUnitsPerSm * split_sms,
 // split_cap) units by splitting key ranges.
-enum { kPhasePlan = 1, kPhaseRun = 2, kPhaseAll = 3 };
+// kPhaseQ: the tiles' rows and Q operands (no page list needed); kPhaseUnits: the
+// unit plan (reads the page list); kPhaseRun: attention and merge.
+enum { kPhaseQ = 1, kPhaseRun = 2, kPhaseUnits = 4, kPhasePlan = kPhaseQ | kPhaseUnits, kPhaseAll = 7 };
 
 pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows, const int32_t* row_off,
                      const void* k_pool, const void* v_pool, int64_t num_blocks, const pic_link_page* pages,
@@ -1540,14 +1643,18 @@ pic_status launch_tc(const void* q, const float* row_table, const int32_t* rows,
   const int sms = num_sms_of_current_device();
   const int R = kM / G;
   uint8_t* q_tiles = w + L.off_q;
-  if (phases & kPhasePlan) {
-    plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kQTiles * R, Hkv,
-                                                  split_sms < sms ? split_sms : sms, split_cap, L.tiles_cap, L.units_cap,
-                                                  L.tail_extra, hdr, tiles, units, err_flag);
+  if (phases & kPhaseQ) {
+    tile_rows_kernel<<<1, kPlanThreads, 0, s>>>(row_off, n_req, kQTiles * R, L.tiles_cap, hdr, tiles, err_flag);
     if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
     qprep_kernel<<<dim3((unsigned)(L.tiles_cap * Hkv), 4), kQTiles * kM, 0, s>>>(
         hdr, tiles, static_cast<const bf16*>(q), reinterpret_cast<const float4*>(row_table), q_tiles, Hq, Hkv, G,
         R);
+    if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
+  }
+  if (phases & kPhaseUnits) {
+    plan_units_kernel<<<1, kPlanThreads, 0, s>>>(rows, row_off, pages, page_off, n_req, kQTiles * R, Hkv,
+                                                  split_sms < sms ? split_sms : sms, split_cap, L.tiles_cap, L.units_cap,
+                                                  L.tail_extra, hdr, tiles, units, err_flag);
     if (cudaGetLastError() != cudaSuccess) return PIC_ERR_CUDA;
   }
   if (!(phases & kPhaseRun)) return PIC_OK;
@@ -1680,6 +1787,38 @@ pic_status pic_link_attention_plan(const void* q, const float* row_table, const 
   return launch_tc(q, row_table, rows, row_off, nullptr, nullptr, 0, pages, page_off, n_req, Hq, Hkv, 1.f, nullptr,
                    static_cast<uint8_t*>(ws), L, kAllSms, kMaxSplitUnits, err_flag, (cudaStream_t)stream,
                    nullptr, nullptr, 0, kPhasePlan);
+}
+
+pic_status pic_link_attention_plan_q(const void* q, const float* row_table, const int32_t* row_off,
+                                     int32_t n_req, int64_t n_rows, int32_t Hq, int32_t Hkv, int32_t d,
+                                     pic_dtype dtype, void* ws, size_t ws_bytes, int32_t* err_flag,
+                                     pic_stream_t stream) {
+  if (n_req < 0 || n_rows < 0 || Hkv < 1 || Hq < 1 || Hq % Hkv || d < 2 || d > 256 || (d & 1))
+    return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (n_req == 0 || n_rows == 0 || !tc_shape(dtype, Hq, Hkv, d)) return PIC_OK;  // nothing to plan
+  if (!q || !row_table || !row_off || !err_flag) return PIC_ERR_INVALID;
+  const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
+  return launch_tc(q, row_table, nullptr, row_off, nullptr, nullptr, 0, nullptr, nullptr, n_req, Hq, Hkv, 1.f,
+                   nullptr, static_cast<uint8_t*>(ws), L, kAllSms, kMaxSplitUnits, err_flag, (cudaStream_t)stream,
+                   nullptr, nullptr, 0, kPhaseQ);
+}
+
+pic_status pic_link_attention_plan_units(const int32_t* rows, const int32_t* row_off, const pic_link_page* pages,
+                                         const int32_t* page_off, int32_t n_req, int64_t n_rows, int32_t Hq,
+                                         int32_t Hkv, int32_t d, pic_dtype dtype, void* ws, size_t ws_bytes,
+                                         int32_t* err_flag, pic_stream_t stream) {
+  if (n_req < 0 || n_rows < 0 || Hkv < 1 || Hq < 1 || Hq % Hkv || d < 2 || d > 256 || (d & 1))
+    return PIC_ERR_INVALID;
+  if (dtype != PIC_BF16 && dtype != PIC_FP32) return PIC_ERR_INVALID;
+  if (n_req == 0 || n_rows == 0 || !tc_shape(dtype, Hq, Hkv, d)) return PIC_OK;  // nothing to plan
+  if (!rows || !row_off || !pages || !page_off || !err_flag) return PIC_ERR_INVALID;
+  const WsLayout L = ws_layout(n_rows, n_req, Hq / Hkv, Hkv, d);
+  if (ws == nullptr || ws_bytes < L.total || (reinterpret_cast<uintptr_t>(ws) & 255)) return PIC_ERR_WORKSPACE;
+  return launch_tc(nullptr, nullptr, rows, row_off, nullptr, nullptr, 0, pages, page_off, n_req, Hq, Hkv, 1.f,
+                   nullptr, static_cast<uint8_t*>(ws), L, kAllSms, kMaxSplitUnits, err_flag, (cudaStream_t)stream,
+                   nullptr, nullptr, 0, kPhaseUnits);
 }
 
 pic_status pic_link_attention_run(const void* q, const float* row_table, const int32_t* rows,

@@ -19,7 +19,8 @@ import numpy as np
 import torch
 
 from . import (PIC_BF16, PIC_FP32, PIC_LAYOUT_FRAMED, PIC_LAYOUT_SPLICED, PIC_PAGE, pic_decode_attention,
-               pic_decode_workspace, pic_link_attention, pic_link_attention_plan, pic_link_attention_ror, pic_link_attention_run, pic_link_attention_workspace,
+               pic_decode_workspace, pic_link_attention, pic_link_attention_plan_q, pic_link_attention_plan_units,
+               pic_link_attention_ror, pic_link_attention_run, pic_link_attention_workspace,
                pic_plan_offsets, pic_rerotate_k, pic_rope_cached_k, pic_rope_table, pic_select_rows,
                pic_splice_pages, pic_write_fresh_kv)
 from .inputs import Workload, block_shuffle, chunk_store, decode_inputs, row_inputs
@@ -235,9 +236,8 @@ class LinkBatch:
             pass_stream.wait_event(self._ev_fork)
         if self.scheme == "rotary":
             pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, pass_stream)
-        # a third stream, also forked after row selection, takes the row table and then
-        # (after the splice) the attention plan, beside the splice and the fresh K/V: the
-        # plan was the longest path to the attention run
+        # a third stream, also forked after row selection, takes the row table and the
+        # attention plan's Q operands (which need no page list), beside the splice
         plan_stream = main
         if self.scheme in ("rotary", "nope"):
             if self._plan_s is None:
@@ -247,6 +247,9 @@ class LinkBatch:
             plan_stream.wait_event(self._ev_fork)
             pic_rope_table(self.rows, wl.d, wl.theta, self.row_table, plan_stream)
             self._ev_rowtab.record(plan_stream)
+            # the Q operands need only the rows: written beside the splice
+            pic_link_attention_plan_q(dv["q_raw"], self.row_table, dv["row_off"], self.n_req, self.n_rows, wl.Hq,
+                                      wl.Hkv, wl.d, self.pic_dtype, self.ws, self.err, plan_stream)
         # scheme B with shared chunks: the page list reads every chunk from its private pages
         list_src = dv["k_dst"] if (self.scheme == "nope" and "k_dst" in dv) else dv["k_src"]
         pic_splice_pages(dv["chunk_lens"], dv["chunk_off"], dv["q_len"], dv["k"], self.chunk_start,
@@ -258,10 +261,11 @@ class LinkBatch:
             self._ev_spliced.record(main)
             pass_stream.wait_event(self._ev_spliced)
         if plan_stream is not main:
-            plan_stream.wait_event(self._ev_spliced)
-            pic_link_attention_plan(dv["q_raw"], self.row_table, self.rows, dv["row_off"], self.pages,
-                                    dv["page_off"], self.n_req, self.n_rows, wl.Hq, wl.Hkv, wl.d, self.pic_dtype,
-                                    self.ws, self.err, plan_stream)
+            # the unit plan (one block) runs on the pass stream just before the pass: beside
+            # the pass it would find no SM with room until the pass ended
+            pic_link_attention_plan_units(self.rows, dv["row_off"], self.pages, dv["page_off"], self.n_req,
+                                          self.n_rows, wl.Hq, wl.Hkv, wl.d, self.pic_dtype, self.ws, self.err,
+                                          pass_stream)
             self._ev_planned.record(plan_stream)
         if self.scheme == "ror":
             pic_rope_table(self.chunk_start, wl.d, wl.theta, self.delta_table, pass_stream)

@@ -162,6 +162,33 @@ def test_plan_and_run_equal_the_single_call():
     assert torch.equal(out, b.out)
 
 
+def test_plan_parts_in_either_order_equal_the_single_call():
+    """The plan in its two parts (the Q operands, which need no page list, and the
+    unit plan), the units first here, then the run: the same bits as one
+    pic_link_attention call."""
+    wl = inputs.many_chunk()
+    b = LinkBatch(wl)
+    b.run()
+    torch.cuda.synchronize()
+    assert b.error() == 0
+    ref = torch.empty_like(b.out)
+    pic.pic_link_attention(b.dev["q_raw"], b.row_table, b.rows, b.dev["row_off"], b.k_pool, b.v_pool, b.pic_dtype,
+                           b.pages, b.dev["page_off"], b.n_req, b.n_rows, wl.Hq, wl.Hkv, wl.d, b.scale, ref, b.ws,
+                           b.err)
+    b.ws.fill_(0xFF)  # nothing may survive from the previous plan
+    pic.pic_link_attention_plan_units(b.rows, b.dev["row_off"], b.pages, b.dev["page_off"], b.n_req, b.n_rows,
+                                      wl.Hq, wl.Hkv, wl.d, b.pic_dtype, b.ws, b.err)
+    pic.pic_link_attention_plan_q(b.dev["q_raw"], b.row_table, b.dev["row_off"], b.n_req, b.n_rows, wl.Hq, wl.Hkv,
+                                  wl.d, b.pic_dtype, b.ws, b.err)
+    out = torch.empty_like(b.out)
+    pic.pic_link_attention_run(b.dev["q_raw"], b.row_table, b.rows, b.dev["row_off"], b.k_pool, b.v_pool,
+                               b.pic_dtype, b.pages, b.dev["page_off"], b.n_req, b.n_rows, wl.Hq, wl.Hkv, wl.d,
+                               b.scale, out, b.ws, b.err)
+    torch.cuda.synchronize()
+    assert b.error() == 0
+    assert torch.equal(out, ref)
+
+
 @pytest.mark.parametrize("graphs", [False, True])
 def test_pipelined_steps_match_single_steps(graphs):
     """LinkPipeline (uploads and read-backs on copy streams, double-buffered inputs and
