@@ -431,21 +431,28 @@ pic_status pic_link_attention_plan_units(const int32_t* rows, const int32_t* row
 /* ------------------------------------------------------------------------
  * a3+a5  Rotate-on-read link attention (RoPE article 3.3: the rotary correction
  *     applied where the kernel reads the cache, a mixed reuse + correction
- *     path).  The cached K pages stay as cached (local positions); the attention
- *     kernel rotates each K page by its table row in shared memory before the
- *     S product, with the arithmetic of pic_rerotate_k (same table, same
- *     rounding), so its K — and with the same unit plan its output — is bit for
- *     bit that of pic_rerotate_k followed by pic_link_attention.  No re-rotation
- *     pass and no per-request copies of shared chunks.
+ *     path).  Over a page list of the framed layout (PIC_LAYOUT_FRAMED): every
+ *     chunk's keys stay in the chunk's own frame — the cached pages as cached,
+ *     the recomputed head rows encoded at their position in the chunk — and
+ *     every key tile (PIC_TILE_PAGES pages) lies in one chunk.  Since
+ *     RoPE(q, p) . R(Delta) k = R(-Delta) RoPE(q, p) . k, the kernel rotates Q
+ *     back by the chunk's offset (fp32, cos / sin = hi + lo of the table row, one
+ *     more bf16 rounding) for the key tiles of that chunk instead of rotating K:
+ *     no re-rotation pass, cached pages never written, no per-request copies of
+ *     shared chunks.  Not bit-identical to pic_rerotate_k + pic_link_attention
+ *     (Q is rounded in another frame); checked against the same float64
+ *     reference at the same tolerance.
  * ------------------------------------------------------------------------
  *   arguments as pic_link_attention, plus
- *   page_tab   [page_off[n_req]] int32: table row of each link page, < 0 = none
- *              (pic_splice_pages' page_tab output, with k_dst_blocks NULL so that
- *              the list points at the cached blocks)
+ *   page_tab   [page_off[n_req]] int32: each link page's frame — the row of its
+ *              chunk's offset in rot_table, < 0 for the global frame (chunk 0,
+ *              the query) — pic_splice_pages' page_tab output for the framed
+ *              layout, with k_dst_blocks NULL so that the list points at the
+ *              cached blocks
  *   rot_table  [n_tab][d/2][4] fp32 offset table (pic_rope_table over chunk_start)
  * Tensor-core shapes only (bf16 pools, d = 128, Hq / Hkv in {1, 2, 4, 8, 16});
- * otherwise PIC_ERR_UNSUPPORTED.  A table row >= n_tab sets PIC_ERR_RANGE in
- * *err_flag and that page is read unrotated. */
+ * otherwise PIC_ERR_UNSUPPORTED.  A frame >= n_tab sets PIC_ERR_RANGE in
+ * *err_flag and that key tile is read in the global frame. */
 pic_status pic_link_attention_ror(const void* q, const float* row_table, const int32_t* rows,
                                   const int32_t* row_off, const void* k_pool, const void* v_pool,
                                   int64_t num_blocks, pic_dtype dtype, const pic_link_page* pages,
