@@ -45,10 +45,10 @@ UNIT = "tokens/s"
 # two-launch composition), with the kernel source they were taken from; reported
 # as roofline traffic only while the source is unchanged.
 NCU_TRAFFIC = {
-    # link_attn_tc_kernel<0>, long_context_100x1000: 668.39 MB read + 138.73 MB written
-    ("attention", "776d5b9c86ccc04d"): 807120128,
-    # link_attn_tc_kernel<1> (rotate-on-read), long_context_100x1000: 674.80 MB read + 148.21 MB written
-    ("rotate_on_read", "776d5b9c86ccc04d"): 823006976,
+    # link_attn_tc_kernel<0>, long_context_100x1000: 665.66 MB read + 138.84 MB written
+    ("attention", "1941c91a9f32e19f"): 804495360,
+    # link_attn_tc_kernel<1> (rotate-on-read), long_context_100x1000: 643.53 MB read + 145.00 MB written
+    ("rotate_on_read", "1941c91a9f32e19f"): 788534784,
     # rerotate_kernel<bf16>, long_context_100x1000: 201.36 MB read + 140.36 MB written
     ("rerotate", "f862c45770d2a0fa"): 341722880,
     # rope_cached_kernel<bf16> (scheme B), long_context_100x1000: 304.83 MB read + 144.01 MB written
