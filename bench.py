@@ -312,7 +312,7 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t_wall0 = time.perf_counter()
-        # eager steps (ten launches from the host on three streams), with the re-rotation
+        # eager steps (eleven launches from the host on three streams), with the re-rotation
         # and attention runs timed inside, then the same step as one CUDA graph launch
         step_ms, rot_ms, att_ms = time_link(batch, K, l2_flush, stream)
         graph_ms, graph_err = time_graph(batch, K, args.warmup, l2_flush, stream)
@@ -491,7 +491,7 @@ def run_gpu(args, rank, world):
                    "tokens": tokens, "rows": batch.n_rows, "Hq": wl.Hq, "Hkv": wl.Hkv, "d": wl.d,
                    "page": 16, "pages": batch.n_pages, "rot_pages": batch.n_rot,
                    "l2": "flushed (512 MB read, untimed) before every timed step",
-                   "launch": ("one CUDA graph per step (the step's ten kernels on three streams)" if graph_ms
+                   "launch": ("one CUDA graph per step (the step's eleven kernels on three streams)" if graph_ms
                               else f"eager (graph capture failed: {graph_err})"),
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "tensor", "achieved": att_tflops, "peak": tf_burst, "unit": "TFLOP/s",

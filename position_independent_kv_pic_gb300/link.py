@@ -194,8 +194,8 @@ class LinkBatch:
 
     # ------------------------------------------------------------------ step
     # kernels one run() launches: select, splice, 2 tables, re-rotate, fresh K/V, and the
-    # attention (unit planning, Q pre-pass, attention, LSE merge)
-    LAUNCHES_PER_STEP = 10  # rotary correction and rotate-on-read (a third table, no re-rotation); scheme B: 9
+    # attention (its tile rows, Q operands and unit plan, the attention, the LSE merge)
+    LAUNCHES_PER_STEP = 11  # rotary correction and rotate-on-read (a third table, no re-rotation); scheme B: 10
 
     @property
     def launches_per_step(self) -> int:
