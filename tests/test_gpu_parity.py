@@ -183,6 +183,44 @@ def test_edge_cases(case):
     assert emax <= tol[0] and emean <= tol[1], (emax, emean)
 
 
+def test_more_q_tile_pairs_than_the_planner_holds_in_shared_memory():
+    """Over 1,024 Q-tile pairs in one call (520 requests of 66-79 recomputed rows, two
+    pairs of 64 rows each at Hq = 32, Hkv = 8): the unit planner takes its path for
+    tile tables larger than its shared-memory arrays (a search per tile instead of
+    the staged counts).  Every row against the oracle."""
+    rng = np.random.default_rng(123)
+    n = 520
+    lens = [[int(rng.integers(20, 60)), int(rng.integers(10, 40))] for _ in range(n)]
+    qs = [int(rng.integers(58, 72)) for _ in range(n)]
+    wl = inputs.custom(lens, qs, [8] * n, Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=123)
+    b = _run(wl)
+    ro = b.offs["row_off"]
+    pairs = sum(-(-int(ro[r + 1] - ro[r]) // 64) for r in range(b.n_req))
+    assert pairs > 1024, pairs
+    check_rows(b)
+    emax, emean = check_attention(b)
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+
+
+def test_request_limit_of_one_call():
+    """The tensor-core path plans at most 1,024 requests per call: 1,024 requests link
+    and match the oracle on every row, 1,025 are refused with PIC_ERR_UNSUPPORTED."""
+    def wl_of(n):
+        return inputs.custom([[6, 5]] * n, [2] * n, [2] * n, Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16",
+                             seed=7)
+
+    b = _run(wl_of(1024))
+    assert b.n_req == 1024
+    check_rows(b)
+    emax, emean = check_attention(b)
+    assert emax <= TOL_MAX and emean <= TOL_MEAN, (emax, emean)
+    over = LinkBatch(wl_of(1025))
+    with pytest.raises(pic.PicError) as e:
+        over.run()
+    torch.cuda.synchronize()
+    assert e.value.status == pic.PIC_ERR_UNSUPPORTED
+
+
 def test_no_rows_is_a_no_op():
     wl = inputs.custom([[50]], [0], [4], Hq=32, Hkv=8, d=128, theta=5e5, dtype="bf16", seed=3)
     b = _run(wl)
